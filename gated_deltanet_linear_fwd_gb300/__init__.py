@@ -1,0 +1,8 @@
+"""GB300 (sm_103a) Gated Delta Network chunked-prefill forward.
+
+The compute lives in libgdn.so (C ABI in include/gdn.h); this package is its
+thin Python binding plus the seeded input generators.
+"""
+from .api import Plan, gdn_chunk_fwd, gdn_cp_head_modes, gdn_cp_plan, gdn_get_device_status
+
+__all__ = ["Plan", "gdn_chunk_fwd", "gdn_cp_head_modes", "gdn_cp_plan", "gdn_get_device_status"]

@@ -1,0 +1,132 @@
+"""Python binding of the C ABI (include/gdn.h): argument marshalling only.
+
+Every step of the forward runs in libgdn.so's CUDA kernels; PyTorch only
+provides device memory and the stream.  The names mirror the C entry points.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib as L
+
+_MODES = {"off": L.GDN_CP_OFF, "exact": L.GDN_CP_EXACT, "warmup": L.GDN_CP_WARMUP, "auto": L.GDN_CP_AUTO}
+_DT = {torch.bfloat16: L.GDN_BF16, torch.float32: L.GDN_F32}
+
+
+@dataclasses.dataclass
+class Plan:
+    """A filled gdn_cp_plan_t together with the dims it was made for."""
+    raw: L.gdn_cp_plan_t
+    dims: L.gdn_dims
+    cu_seqlens_host: Optional[list]
+
+    @property
+    def mode(self) -> str:
+        return {v: k for k, v in _MODES.items()}[self.raw.mode]
+
+    @property
+    def workspace_bytes(self) -> int:
+        return int(self.raw.workspace_bytes)
+
+    @property
+    def n_seg_total(self) -> int:
+        return int(self.raw.n_seg_total)
+
+
+def _cu_list(cu_seqlens) -> Optional[list]:
+    if cu_seqlens is None:
+        return None
+    if isinstance(cu_seqlens, torch.Tensor):
+        return [int(x) for x in cu_seqlens.tolist()]
+    return [int(x) for x in cu_seqlens]
+
+
+def gdn_cp_plan(*, T: int, h_qk: int, h_v: int, B: int = 1, cu_seqlens=None,
+                dtype: torch.dtype = torch.bfloat16, mode: str = "auto", lambda_: float = 1.0,
+                warmup_chunks: int = 8, warmup_tol: float = 1e-4, sm_count: int = 0,
+                scale: float = 0.0, d_k: int = 128, d_v: int = 128) -> Plan:
+    """Host-only planning (gdn_cp_plan).  T = tokens per row (varlen: total)."""
+    cu = _cu_list(cu_seqlens)
+    n_seqs = B if cu is None else len(cu) - 1
+    dims = L.gdn_dims(B, T, h_qk, h_v, d_k, d_v, n_seqs, scale, _DT.get(dtype, -1))
+    opts = L.gdn_cp_opts(_MODES[mode], lambda_, warmup_chunks, warmup_tol, sm_count)
+    raw = L.gdn_cp_plan_t()
+    cu_arr = None if cu is None else (ctypes.c_int32 * len(cu))(*cu)
+    L.check(L.load().gdn_cp_plan(ctypes.byref(dims), cu_arr, ctypes.byref(opts), ctypes.byref(raw)),
+            "gdn_cp_plan")
+    return Plan(raw, dims, cu)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+                  initial_state: Optional[torch.Tensor] = None, cu_seqlens: Optional[torch.Tensor] = None,
+                  *, plan: Optional[Plan] = None, out: Optional[torch.Tensor] = None,
+                  final_state: Optional[torch.Tensor] = None, output_final_state: bool = True,
+                  workspace: Optional[torch.Tensor] = None, stream=None, scale: float = 0.0,
+                  mode: str = "auto", lambda_: float = 1.0, warmup_chunks: int = 8,
+                  warmup_tol: float = 1e-4):
+    """The chunked-prefill forward (gdn_chunk_fwd).
+
+    q,k [B,T,h_qk,128] or [T,h_qk,128]; v [.., h_v, 128]; g,beta [.., h_v] fp32;
+    initial_state [N,h_v,128,128] fp32 or None; cu_seqlens int32 [N+1] on the
+    device (varlen, B = 1) or None.  Returns (o, final_state or None).
+    """
+    batched = q.dim() == 4
+    B = q.shape[0] if batched else 1
+    T = q.shape[-3]
+    h_qk, h_v = q.shape[-2], v.shape[-2]
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise ValueError("g and beta must be float32")
+    if plan is None:
+        plan = gdn_cp_plan(T=T, h_qk=h_qk, h_v=h_v, B=B, cu_seqlens=cu_seqlens, dtype=q.dtype, mode=mode,
+                           lambda_=lambda_, warmup_chunks=warmup_chunks, warmup_tol=warmup_tol, scale=scale)
+    dims = L.gdn_dims(B, T, h_qk, h_v, q.shape[-1], v.shape[-1], plan.raw.n_seqs, scale, _DT.get(q.dtype, -1))
+    if out is None:
+        out = torch.empty_like(v)
+    if final_state is None and output_final_state:
+        final_state = torch.empty(plan.raw.n_seqs, h_v, 128, 128, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=q.device)
+    if initial_state is not None and (initial_state.dtype != torch.float32 or not initial_state.is_contiguous()):
+        raise ValueError("initial_state must be contiguous float32")
+    st = L.load().gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                                _ptr(cu_seqlens), _ptr(out), _ptr(final_state), ctypes.byref(dims),
+                                ctypes.byref(plan.raw), _ptr(workspace), workspace.numel(),
+                                _stream_handle(stream))
+    L.check(st, "gdn_chunk_fwd")
+    return out, final_state
+
+
+def gdn_get_device_status(workspace: torch.Tensor, stream=None):
+    """(code, detail) of the status word of the last call on this workspace (synchronises)."""
+    code, detail = ctypes.c_int(), ctypes.c_int()
+    L.check(L.load().gdn_get_device_status(_ptr(workspace), _stream_handle(stream), ctypes.byref(code),
+                                           ctypes.byref(detail)), "gdn_get_device_status")
+    return code.value, detail.value
+
+
+def gdn_cp_head_modes(workspace: torch.Tensor, plan: Plan, stream=None):
+    """Per (sequence, head): the mode taken (1 exact, 2 warmup, 0 off) and log warmup bound."""
+    n = plan.raw.n_seqs * plan.raw.h_v
+    modes = (ctypes.c_int32 * n)()
+    bounds = (ctypes.c_float * n)()
+    L.check(L.load().gdn_cp_head_modes(_ptr(workspace), ctypes.byref(plan.raw), modes, bounds,
+                                       _stream_handle(stream)), "gdn_cp_head_modes")
+    shape = (plan.raw.n_seqs, plan.raw.h_v)
+    return (torch.tensor(list(modes), dtype=torch.int32).reshape(shape),
+            torch.tensor(list(bounds), dtype=torch.float32).reshape(shape))

@@ -1,0 +1,314 @@
+// Host side of the C ABI declared in include/gdn.h: planning, argument
+// checks, TMA tensor maps, and the launch sequence of the forward.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "gdn.h"
+#include "gdn_internal.cuh"
+
+using namespace gdn;
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+gdn_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = (int)e;
+  return GDN_ERR_CUDA;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---- one-time, per-device set-up ----
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mu;
+bool g_setup_done[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+gdn_status device_setup(int* dev_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_UNSUPPORTED;
+  *dev_out = dev;
+  std::lock_guard<std::mutex> lk(g_setup_mu);
+  if (g_setup_done[dev]) return GDN_OK;
+  if (!g_encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cuda_fail(e == cudaSuccess ? cudaErrorUnknown : e);
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  if ((e = scan_kernel_setup()) != cudaSuccess) return cuda_fail(e);
+  if ((e = combine_kernel_setup()) != cudaSuccess) return cuda_fail(e);
+  int sms = 0;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return cuda_fail(e);
+  g_sm_count[dev] = sms;
+  g_setup_done[dev] = true;
+  return GDN_OK;
+}
+
+gdn_status check_dims(const gdn_dims* d) {
+  if (!d) return GDN_ERR_INVALID_ARG;
+  if (d->d_k != kDim || d->d_v != kDim) return GDN_ERR_UNSUPPORTED;
+  if (d->dtype != GDN_BF16 && d->dtype != GDN_F32) return GDN_ERR_UNSUPPORTED;
+  if (d->B < 1 || d->T < 0 || d->h_qk < 1 || d->h_v < 1 || d->n_seqs < 1) return GDN_ERR_INVALID_ARG;
+  if ((int64_t)d->B * d->T > (int64_t)0x7fffffff - kChunk) return GDN_ERR_INVALID_ARG;
+  if (d->h_qk > 65535 || d->h_v > 65535) return GDN_ERR_INVALID_ARG;
+  return GDN_OK;
+}
+
+// ---- tensor maps: [tokens, heads, 128] -> 3-D (d, head, token), 64x1x64 boxes, 128B swizzle ----
+gdn_status encode_map(CUtensorMap* m, const void* base, int heads, int64_t tokens, bool f32) {
+  const cuuint64_t esz = f32 ? 4 : 2;
+  cuuint64_t dims[3] = {(cuuint64_t)kDim, (cuuint64_t)heads, (cuuint64_t)(tokens > 0 ? tokens : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)kDim * esz, (cuuint64_t)heads * kDim * esz};
+  cuuint32_t box[3] = {(cuuint32_t)(f32 ? 32 : 64), 1, (cuuint32_t)kChunk};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    g_last_cuda_error = (int)r;
+    return GDN_ERR_CUDA;
+  }
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gdn_status_string(gdn_status s) {
+  switch (s) {
+    case GDN_OK: return "ok";
+    case GDN_ERR_INVALID_ARG: return "invalid argument";
+    case GDN_ERR_UNSUPPORTED: return "unsupported (d_k/d_v must be 128; dtype bf16 or f32)";
+    case GDN_ERR_MISALIGNED: return "misaligned pointer (16 bytes; workspace 256 bytes)";
+    case GDN_ERR_CUDA: return "CUDA call failed";
+    case GDN_ERR_DEVICE_TIMEOUT: return "a bounded on-device wait timed out";
+    case GDN_ERR_WORKSPACE: return "workspace missing or too small";
+    case GDN_ERR_DEVICE_CHECK: return "a kernel's consistency check failed";
+  }
+  return "unknown status";
+}
+
+int gdn_last_cuda_error(void) { return g_last_cuda_error; }
+
+gdn_status gdn_cp_plan(const gdn_dims* dims, const int32_t* cu, const gdn_cp_opts* opts, gdn_cp_plan_t* out) {
+  if (!out) return GDN_ERR_INVALID_ARG;
+  gdn_status st = check_dims(dims);
+  if (st != GDN_OK) return st;
+  const int64_t T_total = (int64_t)dims->B * dims->T;
+  if (cu) {
+    if (dims->B != 1) return GDN_ERR_INVALID_ARG;
+    if (cu[0] != 0 || cu[dims->n_seqs] != dims->T) return GDN_ERR_INVALID_ARG;
+    for (int n = 0; n < dims->n_seqs; ++n)
+      if (cu[n + 1] < cu[n]) return GDN_ERR_INVALID_ARG;
+  } else if (dims->n_seqs != dims->B) {
+    return GDN_ERR_INVALID_ARG;
+  }
+  gdn_cp_opts o = {GDN_CP_AUTO, 1.0f, 8, 1e-4f, 0};
+  if (opts) o = *opts;
+  if (o.mode < GDN_CP_OFF || o.mode > GDN_CP_AUTO) return GDN_ERR_UNSUPPORTED;
+  if (!(o.lambda > 0.f)) o.lambda = 1.0f;
+  if (o.lambda > 1000.f) return GDN_ERR_INVALID_ARG;
+  if (o.warmup_chunks <= 0) o.warmup_chunks = 8;
+  if (!(o.warmup_tol > 0.f)) o.warmup_tol = 1e-4f;
+  if (o.sm_count <= 0) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    o.sm_count = sms;
+  }
+  int mode = o.mode;
+  if (mode == GDN_CP_AUTO) mode = ((int64_t)dims->n_seqs * dims->h_v < o.sm_count) ? GDN_CP_WARMUP : GDN_CP_OFF;
+
+  gdn_cp_plan_t p;
+  std::memset(&p, 0, sizeof(p));
+  p.mode = mode;
+  p.n_seqs = dims->n_seqs;
+  p.T_total = (int)T_total;
+  p.h_v = dims->h_v;
+  p.h_qk = dims->h_qk;
+  p.dtype = dims->dtype;
+  p.lambda_q8 = (int)std::lround(o.lambda * 256.0);
+  if (p.lambda_q8 < 1) p.lambda_q8 = 1;
+  p.warmup_chunks = o.warmup_chunks;
+  p.warmup_tol = o.warmup_tol;
+  p.sm_count = o.sm_count;
+  int64_t n_seg_total = 0;
+  for (int n = 0; n < dims->n_seqs; ++n) {
+    const int64_t len = cu ? (int64_t)cu[n + 1] - cu[n] : dims->T;
+    const int N = chunks_of(len);
+    const int ns = seg_count(N, p.lambda_q8, mode == GDN_CP_OFF);
+    n_seg_total += ns;
+    if (N > p.max_chunks) p.max_chunks = N;
+    for (int s = 0; s < ns; ++s) {
+      const int w = seg_first(s + 1, N, ns) - seg_first(s, N, ns);
+      if (w > p.max_seg_chunks) p.max_seg_chunks = w;
+    }
+  }
+  if (n_seg_total > 0x7fffffff) return GDN_ERR_INVALID_ARG;
+  p.n_seg_total = (int)n_seg_total;
+  // workspace: status | head modes + bounds | segment bounds | R | S_loc | S_start
+  const size_t heads = (size_t)dims->n_seqs * dims->h_v;
+  const size_t segheads = (size_t)n_seg_total * dims->h_v;
+  size_t off = 256;
+  p.off_head = off;
+  off = align_up(off + heads * 8, 256);
+  p.off_seg_bound = off;
+  off = align_up(off + segheads * 4, 256);
+  if (mode != GDN_CP_OFF) {
+    const size_t mat = (size_t)kDim * kDim * 4;
+    p.off_R = off;
+    off += segheads * mat;
+    p.off_Sloc = off;
+    off += segheads * mat;
+    p.off_Sstart = off;
+    off += segheads * mat;
+  }
+  p.workspace_bytes = off;
+  *out = p;
+  return GDN_OK;
+}
+
+gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                         const float* initial_state, const int32_t* cu_dev, void* out, float* final_state,
+                         const gdn_dims* dims, const gdn_cp_plan_t* plan, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  gdn_status st = check_dims(dims);
+  if (st != GDN_OK) return st;
+  if (!plan) return GDN_ERR_INVALID_ARG;
+  const int64_t T_total = (int64_t)dims->B * dims->T;
+  if (plan->n_seqs != dims->n_seqs || plan->T_total != T_total || plan->h_v != dims->h_v ||
+      plan->h_qk != dims->h_qk || plan->dtype != dims->dtype)
+    return GDN_ERR_INVALID_ARG;
+  if (cu_dev && dims->B != 1) return GDN_ERR_INVALID_ARG;
+  if (!cu_dev && dims->n_seqs != dims->B) return GDN_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < plan->workspace_bytes) return GDN_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_MISALIGNED;
+  if (T_total > 0) {
+    if (!q || !k || !v || !g || !beta || !out) return GDN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(g) || !aligned16(beta))
+      return GDN_ERR_MISALIGNED;
+  }
+  if ((initial_state && !aligned16(initial_state)) || (final_state && !aligned16(final_state)) ||
+      (cu_dev && (reinterpret_cast<uintptr_t>(cu_dev) & 3u)))
+    return GDN_ERR_MISALIGNED;
+  if (dims->dtype == GDN_F32) return GDN_ERR_UNSUPPORTED;  // fp32 path: see the fp32 kernels
+
+  int dev = 0;
+  st = device_setup(&dev);
+  if (st != GDN_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+
+  Problem p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.g = g;
+  p.beta = beta;
+  p.h0 = initial_state;
+  p.cu = cu_dev;
+  p.out = out;
+  p.hT = final_state;
+  p.T_row = dims->T;
+  p.n_seqs = dims->n_seqs;
+  p.h_qk = dims->h_qk;
+  p.h_v = dims->h_v;
+  p.scale = dims->scale != 0.f ? dims->scale : 1.0f / std::sqrt((float)dims->d_k);
+  p.elem_f32 = dims->dtype == GDN_F32;
+  p.plan_mode = plan->mode == GDN_CP_OFF ? kModeOff : (plan->mode == GDN_CP_EXACT ? kModeExact : kModeWarmup);
+  p.lambda_q8 = plan->lambda_q8;
+  p.warmup_chunks = plan->warmup_chunks;
+  p.log_tol = std::log(plan->warmup_tol);
+  p.n_seg_total = plan->n_seg_total;
+  p.status = reinterpret_cast<int*>(ws);
+  p.head_mode = reinterpret_cast<int*>(ws + plan->off_head);
+  p.head_bound = reinterpret_cast<float*>(ws + plan->off_head + (size_t)dims->n_seqs * dims->h_v * 4);
+  p.seg_bound = reinterpret_cast<float*>(ws + plan->off_seg_bound);
+  if (plan->mode != GDN_CP_OFF) {
+    p.R = reinterpret_cast<float*>(ws + plan->off_R);
+    p.Sloc = reinterpret_cast<float*>(ws + plan->off_Sloc);
+    p.Sstart = reinterpret_cast<float*>(ws + plan->off_Sstart);
+  }
+
+  cudaError_t e = cudaMemsetAsync(ws, 0, 256, cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (T_total == 0) {
+    // No tokens: the final state is the initial state.
+    if (final_state) {
+      const size_t bytes = (size_t)dims->n_seqs * dims->h_v * kDim * kDim * 4;
+      e = initial_state ? cudaMemcpyAsync(final_state, initial_state, bytes, cudaMemcpyDeviceToDevice, cs)
+                        : cudaMemsetAsync(final_state, 0, bytes, cs);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return GDN_OK;
+  }
+  CUtensorMap mq, mk, mv;
+  const bool f32 = dims->dtype == GDN_F32;
+  if ((st = encode_map(&mq, q, dims->h_qk, T_total, f32)) != GDN_OK) return st;
+  if ((st = encode_map(&mk, k, dims->h_qk, T_total, f32)) != GDN_OK) return st;
+  if ((st = encode_map(&mv, v, dims->h_v, T_total, f32)) != GDN_OK) return st;
+
+  if (plan->mode == GDN_CP_OFF) {
+    if ((e = launch_scan_out(p, mq, mk, mv, plan->n_seg_total, cs)) != cudaSuccess) return cuda_fail(e);
+    return GDN_OK;
+  }
+  if (plan->mode == GDN_CP_WARMUP)
+    if ((e = launch_gate_bound(p, cs)) != cudaSuccess) return cuda_fail(e);
+  if ((e = launch_scan_prep(p, mq, mk, mv, cs)) != cudaSuccess) return cuda_fail(e);
+  if ((e = launch_combine(p, cs)) != cudaSuccess) return cuda_fail(e);
+  if ((e = launch_scan_out(p, mq, mk, mv, plan->n_seg_total, cs)) != cudaSuccess) return cuda_fail(e);
+  return GDN_OK;
+}
+
+gdn_status gdn_get_device_status(const void* workspace, void* stream, int* code, int* detail) {
+  if (!workspace || !code) return GDN_ERR_INVALID_ARG;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  int h[2] = {0, 0};
+  cudaError_t e = cudaMemcpyAsync(h, workspace, sizeof(h), cudaMemcpyDeviceToHost, cs);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  *code = h[0];
+  if (detail) *detail = h[1];
+  return GDN_OK;
+}
+
+gdn_status gdn_cp_head_modes(const void* workspace, const gdn_cp_plan_t* plan, int32_t* modes, float* bounds,
+                             void* stream) {
+  if (!workspace || !plan) return GDN_ERR_INVALID_ARG;
+  const size_t heads = (size_t)plan->n_seqs * plan->h_v;
+  if (plan->mode == GDN_CP_OFF) {
+    for (size_t i = 0; i < heads; ++i) {
+      if (modes) modes[i] = GDN_CP_OFF;
+      if (bounds) bounds[i] = -INFINITY;
+    }
+    return GDN_OK;
+  }
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const uint8_t* ws = reinterpret_cast<const uint8_t*>(workspace);
+  cudaError_t e = cudaSuccess;
+  if (modes) e = cudaMemcpyAsync(modes, ws + plan->off_head, heads * 4, cudaMemcpyDeviceToHost, cs);
+  if (e == cudaSuccess && bounds)
+    e = cudaMemcpyAsync(bounds, ws + plan->off_head + heads * 4, heads * 4, cudaMemcpyDeviceToHost, cs);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return GDN_OK;
+}
+
+}  // extern "C"

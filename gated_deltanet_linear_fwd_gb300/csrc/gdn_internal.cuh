@@ -1,0 +1,169 @@
+// Internal definitions shared by the kernels and the host entry points.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "gdn_plan_rule.cuh"
+
+namespace gdn {
+
+// Status word codes (first int of the workspace), mirrored in gdn_status.
+constexpr int kDevOk = 0;
+constexpr int kDevTimeout = 5;
+constexpr int kDevCheck = 7;
+
+// Detail words: which wait or check tripped.
+constexpr int kDetTmaWait = 1;
+constexpr int kDetMmaWait = 2;
+constexpr int kDetSegMismatch = 3;
+constexpr int kDetCombineOrder = 4;
+
+// Head mode words (workspace head-mode section).
+constexpr int kModeOff = 0;
+constexpr int kModeExact = 1;
+constexpr int kModeWarmup = 2;
+
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per bounded wait
+
+struct Problem {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta;
+  const float* h0;          // [n_seqs, h_v, d_k, d_v] or null
+  const int32_t* cu;        // device cu_seqlens or null
+  void* out;
+  float* hT;                // [n_seqs, h_v, d_k, d_v] or null
+  int T_row;                // tokens per batch row when cu == null
+  int n_seqs, h_qk, h_v;
+  float scale;
+  int elem_f32;             // q/k/v/out are fp32 (else bf16)
+  // plan
+  int plan_mode;            // kModeOff / kModeExact / kModeWarmup
+  int lambda_q8;
+  int warmup_chunks;
+  float log_tol;            // log(warmup_tol)
+  int n_seg_total;
+  // workspace sections
+  int* status;              // [0] code, [1] detail
+  int* head_mode;           // [n_seqs * h_v]
+  float* head_bound;        // [n_seqs * h_v]
+  float* seg_bound;         // [n_seg_total * h_v]
+  float* R;                 // [n_seg_total, h_v, 128, 128] row-major (row = d_k in)
+  float* Sloc;              // [n_seg_total, h_v, 128, 128] row = d_v
+  float* Sstart;            // [n_seg_total, h_v, 128, 128] row = d_v
+};
+
+__device__ __forceinline__ void report(int* status, int code, int detail) {
+  if (atomicCAS(status, 0, code) == 0) atomicExch(status + 1, detail);
+}
+
+struct SegInfo {
+  int n;         // sequence
+  int s;         // segment within the sequence
+  int n_seg;     // segments of the sequence
+  int seg_base;  // global index of segment 0 of this sequence
+  int n_chunks;  // chunks of the sequence
+  int cb, ce;    // chunk range of this segment
+  int64_t bos, eos;
+};
+
+// Segments of sequence n (cp_off: one).
+__device__ __forceinline__ int seq_seg_count(const Problem& p, int n, int64_t& bos, int64_t& eos,
+                                             int& n_chunks) {
+  if (p.cu) {
+    bos = p.cu[n];
+    eos = p.cu[n + 1];
+  } else {
+    bos = (int64_t)n * p.T_row;
+    eos = bos + p.T_row;
+  }
+  n_chunks = chunks_of(eos - bos);
+  return seg_count(n_chunks, p.lambda_q8, p.plan_mode == kModeOff);
+}
+
+// Locates global segment `seg` (warp-cooperative; call with a full warp,
+// every lane gets the result).  Returns false if seg is out of range.
+__device__ inline bool locate_segment(const Problem& p, int seg, SegInfo& out) {
+  const int lane = threadIdx.x & 31;
+  int base = 0;
+  for (int n0 = 0; n0 < p.n_seqs; n0 += 32) {
+    const int n = n0 + lane;
+    int cnt = 0, nch = 0;
+    int64_t bos = 0, eos = 0;
+    if (n < p.n_seqs) cnt = seq_seg_count(p, n, bos, eos, nch);
+    int incl = cnt;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += y;
+    }
+    const int excl = base + incl - cnt;
+    const bool mine = (n < p.n_seqs) && seg >= excl && seg < excl + cnt;
+    const unsigned hit = __ballot_sync(0xffffffffu, mine);
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      out.n = __shfl_sync(0xffffffffu, n, src);
+      out.seg_base = __shfl_sync(0xffffffffu, excl, src);
+      out.n_seg = __shfl_sync(0xffffffffu, cnt, src);
+      out.n_chunks = __shfl_sync(0xffffffffu, nch, src);
+      out.bos = __shfl_sync(0xffffffffu, bos, src);
+      out.eos = __shfl_sync(0xffffffffu, eos, src);
+      out.s = seg - out.seg_base;
+      out.cb = seg_first(out.s, out.n_chunks, out.n_seg);
+      out.ce = seg_first(out.s + 1, out.n_chunks, out.n_seg);
+      return true;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return false;
+}
+
+// Segment range of sequence n (warp-cooperative, every lane gets the result).
+__device__ inline void locate_sequence(const Problem& p, int n, SegInfo& out) {
+  const int lane = threadIdx.x & 31;
+  int base = 0;
+  for (int n0 = 0; n0 < n; n0 += 32) {
+    const int m = n0 + lane;
+    int cnt = 0, nch = 0;
+    int64_t bos, eos;
+    if (m < n) cnt = seq_seg_count(p, m, bos, eos, nch);
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, d);
+    base += cnt;
+  }
+  out.n = n;
+  out.seg_base = base;
+  out.n_seg = seq_seg_count(p, n, out.bos, out.eos, out.n_chunks);
+  out.s = 0;
+  out.cb = 0;
+  out.ce = out.n_chunks;
+}
+
+// Max of the per-segment warmup bounds of (sequence, head); -inf if none.
+__device__ inline float head_log_bound(const Problem& p, const SegInfo& si, int j) {
+  float m = -__int_as_float(0x7f800000);
+  for (int s = 1; s < si.n_seg; ++s) m = fmaxf(m, p.seg_bound[(size_t)(si.seg_base + s) * p.h_v + j]);
+  return m;
+}
+
+// Mode a (sequence, head) takes under the plan.
+__device__ inline int head_mode_of(const Problem& p, const SegInfo& si, int j) {
+  if (p.plan_mode == kModeOff) return kModeOff;
+  if (p.plan_mode == kModeExact) return kModeExact;
+  return head_log_bound(p, si, j) <= p.log_tol ? kModeWarmup : kModeExact;
+}
+
+// ---- kernel launchers (defined in the .cu files) ----
+cudaError_t launch_gate_bound(const Problem& p, cudaStream_t st);
+cudaError_t launch_scan_prep(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                             const CUtensorMap& mv, cudaStream_t st);
+cudaError_t launch_combine(const Problem& p, cudaStream_t st);
+cudaError_t launch_scan_out(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                            const CUtensorMap& mv, int grid_x, cudaStream_t st);
+cudaError_t scan_kernel_setup();
+cudaError_t combine_kernel_setup();
+
+}  // namespace gdn

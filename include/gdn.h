@@ -1,0 +1,192 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) Gated Delta Network chunked-prefill
+ * forward.
+ *
+ * Sources cited below:
+ *   [FlashQLA] the FlashQLA blog pages, "FlashQLA: fused linear-attention
+ *     kernels for CP/backward (GDN)" (Traditional Chinese and Korean
+ *     editions), sections "Optimising GDN chunked prefill", "AutoCP",
+ *     "TileLang warp-specialised kernels", "Benchmarks", "Implementation and
+ *     requirements"; and the Telegram post on FlashQLA (Russian) on the
+ *     fast-decaying heads and the 6-8 chunk warmup.
+ *   [GDN] Yang, Kautz, Hatamizadeh, "Gated Delta Networks: Improving Mamba2
+ *     with Delta Rule", ICLR 2025, section "Gated delta rule" (the recurrence).
+ *
+ * The layer (per sequence, per value head j, tokens t in order):
+ *   S_t = exp(g_t) * S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *   o_t = scale * S_t q_t
+ * with S_t a d_v x d_k fp32 matrix, q/k taken from query/key head
+ * floor(j * h_qk / h_v) (grouped heads) [GDN; FlashQLA, "Benchmarks" table
+ * columns h_qk, h_v].  It is evaluated over 64-token chunks, aligned to each
+ * sequence's own start, through the chunk-local WY form [FlashQLA,
+ * "Optimising GDN chunked prefill"], optionally split into context-parallel
+ * segments on one GPU [FlashQLA, "AutoCP"].
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are CUDA device addresses on the current device; host
+ *     pointers are ordinary host memory.  The caller owns all memory,
+ *     including the workspace; the library allocates nothing and keeps no
+ *     per-call state.  The only global state is a per-device cache of the
+ *     SM count and of the kernel attribute set-up.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Device
+ *     work is enqueued asynchronously; nothing synchronises except
+ *     gdn_get_device_status.
+ *   - Every entry point returns a gdn_status.  No exception crosses the ABI.
+ *     Kernels never trap: a kernel that fails its own bounds/consistency
+ *     check, or whose bounded wait runs out, records a code in the
+ *     workspace's status word (read it with gdn_get_device_status) and
+ *     returns.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn_status {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1,    /* null pointer, bad size, inconsistent dims/plan */
+  GDN_ERR_UNSUPPORTED = 2,    /* d_k or d_v != 128, unknown dtype or mode */
+  GDN_ERR_MISALIGNED = 3,     /* a device pointer not 16-byte (workspace: 256-byte) aligned */
+  GDN_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed; see gdn_last_cuda_error() */
+  GDN_ERR_DEVICE_TIMEOUT = 5, /* (from gdn_get_device_status) a bounded on-device wait ran out */
+  GDN_ERR_WORKSPACE = 6,      /* workspace missing or smaller than plan->workspace_bytes */
+  GDN_ERR_DEVICE_CHECK = 7    /* (from gdn_get_device_status) a kernel's own check failed */
+} gdn_status;
+
+/* Element types of q, k, v and out.  g, beta, states are always fp32. */
+enum { GDN_BF16 = 0, GDN_F32 = 1 };
+
+/* Intra-card context parallelism [FlashQLA, "AutoCP"]. */
+enum {
+  GDN_CP_OFF = 0,    /* one CTA-level scan per (sequence, value head) */
+  GDN_CP_EXACT = 1,  /* segments; start states combined exactly through M */
+  GDN_CP_WARMUP = 2, /* segments; a (sequence, head) whose gate bound is under
+                        warmup_tol restarts each segment from zero
+                        warmup_chunks chunks early and skips M; the others
+                        run exactly */
+  GDN_CP_AUTO = 3    /* WARMUP when n_seqs * h_v < sm_count, else OFF */
+};
+
+typedef struct gdn_dims {
+  int B;      /* batch; must be 1 when cu_seqlens is used */
+  int T;      /* tokens per batch row (varlen: total packed tokens) */
+  int h_qk;   /* query/key heads */
+  int h_v;    /* value heads (one recurrent state each) */
+  int d_k;    /* key dim; must be 128 */
+  int d_v;    /* value dim; must be 128 */
+  int n_seqs; /* varlen: number of sequences (len(cu_seqlens) - 1); fixed length: B */
+  float scale; /* output scale; 0 selects 1/sqrt(d_k) */
+  int dtype;   /* GDN_BF16 or GDN_F32 */
+} gdn_dims;
+
+typedef struct gdn_cp_opts {
+  int mode;          /* GDN_CP_* */
+  float lambda;      /* segment length L = round(lambda * sqrt(N)) chunks; <= 0 selects 1.0.
+                        lambda is used in steps of 1/256. */
+  int warmup_chunks; /* warmup restart depth w in chunks; <= 0 selects 8 */
+  float warmup_tol;  /* accept warmup for a (sequence, head) when its bound
+                        max over segments of exp(sum g over the window) *
+                        prod max(1, |1 - beta ||k||^2|) is <= this; <= 0 selects 1e-4 */
+  int sm_count;      /* SMs to plan for; <= 0 queries the current device */
+} gdn_cp_opts;
+
+/* Plain-data plan; fill with gdn_cp_plan, do not edit. */
+typedef struct gdn_cp_plan_t {
+  int mode;             /* resolved mode: GDN_CP_OFF, GDN_CP_EXACT or GDN_CP_WARMUP */
+  int n_seqs;           /* sequences the plan was made for */
+  int T_total;          /* B * T */
+  int h_v, h_qk, dtype; /* copied from dims, checked by gdn_chunk_fwd */
+  int lambda_q8;        /* lambda * 256, rounded */
+  int warmup_chunks;
+  float warmup_tol;
+  int sm_count;
+  int n_seg_total;      /* segments summed over sequences */
+  int max_seg_chunks;   /* longest segment, in chunks */
+  int max_chunks;       /* longest sequence, in chunks */
+  size_t workspace_bytes;
+  size_t off_head;      /* byte offsets of the workspace sections */
+  size_t off_seg_bound;
+  size_t off_R, off_Sloc, off_Sstart;
+} gdn_cp_plan_t;
+
+/*
+ * gdn_cp_plan -- host-only planning [FlashQLA, "AutoCP": L = lambda * sqrt(N),
+ * N = chunks, L = chunks per segment].  No device work.
+ *   dims              : problem sizes (see gdn_dims).
+ *   cu_seqlens_host   : n_seqs+1 non-decreasing token offsets starting at 0
+ *                       and ending at T, or NULL for B fixed-length rows of T.
+ *   opts              : may be NULL (all defaults, mode AUTO).
+ *   out_plan          : written on success.
+ * Segmentation of a sequence with N = ceil(len/64) chunks: L = max(1,
+ * floor((isqrt(lambda_q8^2 * N) + 128) / 256)), n_seg = max(1, ceil(N / L)),
+ * segment s = chunks [floor(s N / n_seg), floor((s+1) N / n_seg)).  Mode OFF
+ * uses one segment per sequence.  An empty sequence has one empty segment.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA (only when opts->sm_count <= 0 and
+ * the device query fails).
+ */
+gdn_status gdn_cp_plan(const gdn_dims* dims, const int32_t* cu_seqlens_host,
+                       const gdn_cp_opts* opts, gdn_cp_plan_t* out_plan);
+
+/*
+ * gdn_chunk_fwd -- the chunked-prefill forward [FlashQLA, "Optimising GDN
+ * chunked prefill", "AutoCP", "TileLang warp-specialised kernels" (forward
+ * pass: V', S and O)].  Asynchronous on `stream`.
+ *   q, k          : device, [B*T, h_qk, d_k] (token-major, heads interleaved), dims->dtype.
+ *   v             : device, [B*T, h_v, d_v], dims->dtype.
+ *   g             : device, [B*T, h_v] fp32, log of the decay gate (alpha = exp(g)).
+ *   beta          : device, [B*T, h_v] fp32, write strength.
+ *   initial_state : device, [n_seqs, h_v, d_k, d_v] fp32 (H = S^T), or NULL for zeros.
+ *   cu_seqlens_dev: device int32 [n_seqs+1], the same offsets given to gdn_cp_plan,
+ *                   or NULL for fixed-length rows.
+ *   out           : device, [B*T, h_v, d_v], dims->dtype (bf16 rounded to nearest even).
+ *   final_state   : device, [n_seqs, h_v, d_k, d_v] fp32, or NULL (not written).
+ *   dims, plan    : host; plan must come from gdn_cp_plan with these dims.
+ *   workspace     : device, 256-byte aligned; its contents on entry do not
+ *                   matter.  Must not be shared by calls that may run
+ *                   concurrently.
+ *   workspace_bytes: size of `workspace`; must be >= plan->workspace_bytes.
+ * All device pointers must be 16-byte aligned.  q/k/v/out may not overlap.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA (launch failure).
+ */
+gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, const float* initial_state,
+                         const int32_t* cu_seqlens_dev, void* out, float* final_state,
+                         const gdn_dims* dims, const gdn_cp_plan_t* plan, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* gdn_status_string(gdn_status status);
+
+/* The cudaError_t of the most recent GDN_ERR_CUDA on this thread (0 if none). */
+int gdn_last_cuda_error(void);
+
+/*
+ * gdn_get_device_status -- synchronises `stream`, then reads the status word
+ * the kernels of the last gdn_chunk_fwd on this workspace wrote.
+ *   workspace : device workspace passed to gdn_chunk_fwd.
+ *   code      : host; receives GDN_OK, GDN_ERR_DEVICE_TIMEOUT or GDN_ERR_DEVICE_CHECK.
+ *   detail    : host, may be NULL; receives a kernel-specific detail word.
+ * Returns CUDA on a failed copy/sync, INVALID_ARG on null pointers.
+ */
+gdn_status gdn_get_device_status(const void* workspace, void* stream, int* code, int* detail);
+
+/*
+ * gdn_cp_head_modes -- diagnostics: synchronises `stream` and copies, per
+ * (sequence, value head), the mode the last gdn_chunk_fwd on this workspace
+ * took (GDN_CP_EXACT or GDN_CP_WARMUP; GDN_CP_OFF for plans without CP) and
+ * the natural log of its warmup error bound (-inf when no segment needs one).
+ *   modes_host    : host int32 [n_seqs * h_v], or NULL.
+ *   log_bound_host: host fp32 [n_seqs * h_v], or NULL.
+ */
+gdn_status gdn_cp_head_modes(const void* workspace, const gdn_cp_plan_t* plan, int32_t* modes_host,
+                             float* log_bound_host, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDN_H_ */

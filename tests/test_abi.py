@@ -1,0 +1,143 @@
+"""CPU tests of the C ABI: the library loads, exports what include/gdn.h
+declares, and its host-side planner and argument checks behave (no GPU)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests import util
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_deltanet_linear_fwd_gb300 import _lib
+    if not os.path.exists(_lib.LIB_PATH):
+        from gated_deltanet_linear_fwd_gb300 import build
+        build.build()
+    return _lib.load()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_\w+)\s*\(", src)))
+
+
+def test_header_symbols_exported(lib):
+    names = header_functions()
+    assert {"gdn_cp_plan", "gdn_chunk_fwd", "gdn_status_string", "gdn_get_device_status"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"libgdn.so does not export {n}"
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert lib.gdn_status_string(s)
+    assert b"unknown" in lib.gdn_status_string(99)
+
+
+def plan(lib, T, h_qk=2, h_v=8, B=1, cu=None, mode=3, lam=1.0, w=8, tol=1e-4, sms=152, d=128, dtype=0):
+    from gated_deltanet_linear_fwd_gb300 import _lib as L
+    n_seqs = B if cu is None else len(cu) - 1
+    dims = L.gdn_dims(B, T, h_qk, h_v, d, d, n_seqs, 0.0, dtype)
+    opts = L.gdn_cp_opts(mode, lam, w, tol, sms)
+    out = L.gdn_cp_plan_t()
+    arr = None if cu is None else (ctypes.c_int32 * len(cu))(*cu)
+    st = lib.gdn_cp_plan(ctypes.byref(dims), arr, ctypes.byref(opts), ctypes.byref(out))
+    return st, out
+
+
+@pytest.mark.parametrize("cu,lam,mode", [
+    ([0, 32768], 1.0, 1), ([0, 262144, 327680, 344064, 348160], 1.0, 2),
+    ([0, 512], 1.0, 1), ([0, 100, 100, 165, 4000], 0.5, 1), ([0, 64 * 97 + 5], 2.25, 2),
+    ([0, 32768], 1.0, 0)])
+def test_plan_segments_follow_rule(lib, cu, lam, mode):
+    st, p = plan(lib, cu[-1], cu=cu, mode=mode, lam=lam)
+    assert st == 0
+    q8 = round(lam * 256)
+    assert p.lambda_q8 == q8
+    segs = [util.segments(cu[n + 1] - cu[n], q8, mode == 0) for n in range(len(cu) - 1)]
+    assert p.n_seg_total == sum(len(s) for s in segs)
+    assert p.max_seg_chunks == max(b - a for s in segs for (a, b) in s)
+    # segments cover each sequence in order, balanced to within one chunk
+    for s in segs:
+        assert s[0][0] == 0 and all(s[i][1] == s[i + 1][0] for i in range(len(s) - 1))
+        lens = [b - a for a, b in s]
+        assert max(lens) - min(lens) <= 1
+
+
+def test_plan_sqrt_model(lib):
+    # lambda = 1, N = 512 chunks -> L = round(sqrt(512)) = 23 -> 23 segments
+    st, p = plan(lib, 32768, mode=1)
+    assert st == 0 and p.n_seg_total == 23 and p.max_seg_chunks == 23
+
+
+def test_plan_auto_mode(lib):
+    st, p = plan(lib, 32768, h_v=8, mode=3, sms=152)
+    assert st == 0 and p.mode == 2  # 8 heads < 152 SMs -> warmup-with-exact-fallback CP
+    st, p = plan(lib, 4096, B=40, h_v=8, mode=3, sms=152)
+    assert st == 0 and p.mode == 0 and p.n_seg_total == 40  # 320 chains fill the GPU -> off
+
+
+def test_plan_workspace_layout(lib):
+    st, p = plan(lib, 32768, h_v=8, mode=1)
+    mat = 128 * 128 * 4
+    assert p.off_head % 256 == 0 and p.off_seg_bound % 256 == 0
+    assert p.off_Sloc - p.off_R == 23 * 8 * mat and p.off_Sstart - p.off_Sloc == 23 * 8 * mat
+    assert p.workspace_bytes == p.off_Sstart + 23 * 8 * mat
+    st, p0 = plan(lib, 32768, h_v=8, mode=0)
+    assert p0.workspace_bytes < 4096
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(d=64), 2), (dict(dtype=5), 2), (dict(mode=9), 2), (dict(h_v=0), 1),
+    (dict(cu=[0, 10, 5]), 1), (dict(cu=[1, 10]), 1), (dict(cu=[0, 9]), 1), (dict(B=2, cu=[0, 10]), 1)])
+def test_plan_rejects(lib, kw, expect):
+    T = kw.get("cu", [0, 10])[-1] if "cu" in kw else 10
+    if kw.get("cu") == [0, 9]:
+        T = 10  # cu does not end at T
+    st, _ = plan(lib, T, **kw)
+    assert st == expect
+
+
+def test_chunk_fwd_rejects_before_device_work(lib):
+    from gated_deltanet_linear_fwd_gb300 import _lib as L
+    st, p = plan(lib, 128, h_qk=1, h_v=1, mode=0)
+    assert st == 0
+    dims = L.gdn_dims(1, 128, 1, 1, 128, 128, 1, 0.0, 0)
+    A = ctypes.c_void_p(0x100000)  # never dereferenced: every case fails a host check first
+    U = ctypes.c_void_p(0x100008)  # not 16-byte aligned
+    f = lib.gdn_chunk_fwd
+    # null plan / dims
+    assert f(A, A, A, A, A, None, None, A, None, None, ctypes.byref(p), A, 4096, None) == 1
+    assert f(A, A, A, A, A, None, None, A, None, ctypes.byref(dims), None, A, 4096, None) == 1
+    # workspace missing or too small
+    assert f(A, A, A, A, A, None, None, A, None, ctypes.byref(dims), ctypes.byref(p), None, 4096, None) == 6
+    assert f(A, A, A, A, A, None, None, A, None, ctypes.byref(dims), ctypes.byref(p), A, 16, None) == 6
+    # misaligned
+    assert f(U, A, A, A, A, None, None, A, None, ctypes.byref(dims), ctypes.byref(p), A, 4096, None) == 3
+    assert f(A, A, A, A, A, None, None, A, None, ctypes.byref(dims), ctypes.byref(p), U, 4096, None) == 3
+    # null input
+    assert f(None, A, A, A, A, None, None, A, None, ctypes.byref(dims), ctypes.byref(p), A, 4096, None) == 1
+    # dims disagree with the plan
+    dims2 = L.gdn_dims(1, 128, 1, 2, 128, 128, 1, 0.0, 0)
+    assert f(A, A, A, A, A, None, None, A, None, ctypes.byref(dims2), ctypes.byref(p), A, 4096, None) == 1
+    # unsupported head dim
+    dims3 = L.gdn_dims(1, 128, 1, 1, 64, 128, 1, 0.0, 0)
+    assert f(A, A, A, A, A, None, None, A, None, ctypes.byref(dims3), ctypes.byref(p), A, 4096, None) == 2
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from gated_deltanet_linear_fwd_gb300 import _lib as L
+    saved = L._lib
+    try:
+        L._lib = None
+        with pytest.raises(RuntimeError, match="libgdn.so not found"):
+            L.load(str(tmp_path / "missing.so"))
+    finally:
+        L._lib = saved

@@ -1,0 +1,155 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Bar (bf16 I/O, fp32 accumulation): for o, max|diff| <= 2e-2 * RMS(ref) after
+allowing the half-ulp the bf16 store itself must add; for the fp32 final
+state, max|diff| <= 2e-2 * RMS(ref).  Small cases are compared element by
+element; the five standard workloads at full size in the bench's launch
+configuration are compared element by element as well (the oracle runs a
+1 x 32768 head in well under a second).
+"""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import chunked
+from tests import util
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU, skipped there
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from gated_deltanet_linear_fwd_gb300 import (gdn_chunk_fwd, gdn_cp_head_modes, gdn_cp_plan,  # noqa: E402
+                                             gdn_get_device_status)
+from gated_deltanet_linear_fwd_gb300.inputs import make_inputs, workload  # noqa: E402
+
+DEV = "cuda:0"
+
+
+def run(w, mode="off", lambda_=1.0, warmup_chunks=8, warmup_tol=1e-4, h0=True):
+    d = w.to(DEV)
+    plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, cu_seqlens=w.cu_seqlens, mode=mode, lambda_=lambda_,
+                       warmup_chunks=warmup_chunks, warmup_tol=warmup_tol)
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=DEV)
+    o, hT = gdn_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0 if h0 else None, d.cu_seqlens, plan=plan,
+                          workspace=ws)
+    code, detail = gdn_get_device_status(ws)
+    assert code == 0, f"device status {code} detail {detail}"
+    return o, hT, plan, ws
+
+
+@functools.lru_cache(maxsize=None)
+def ref_of(key):
+    w = CASES[key]()
+    f = util.to64
+    return oracle.recurrence(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0), w.seq_offsets())
+
+
+CASES = {
+    "tiny": lambda: workload("tiny_T512_h2x4"),
+    "ragged_gqa3": lambda: make_inputs(cu_seqlens=[0, 1, 65, 200, 200, 391, 1000], h_qk=2, h_v=6, seed=7,
+                                       with_h0=True),
+    "uneven_heads": lambda: make_inputs(300, h_qk=2, h_v=3, seed=8, with_h0=True),
+    "long_mix": lambda: make_inputs(4096 + 17, h_qk=1, h_v=4, seed=9, with_h0=True),
+}
+
+
+def check(o, hT, ref, tag):
+    ro, rh = ref
+    excess, raw = util.parity_bf16(o, ro)
+    err_h = util.parity_f32(hT, rh)
+    print(f"{tag}: o excess/rms {excess:.3e} (raw {raw:.3e})  hT {err_h:.3e}")
+    assert excess <= util.TOL_BF16, f"{tag}: o error {excess:.3e} * RMS"
+    assert err_h <= util.TOL_STATE, f"{tag}: final state error {err_h:.3e} * RMS"
+
+
+@pytest.mark.parametrize("key", sorted(CASES))
+@pytest.mark.parametrize("mode,lam", [("off", 1.0), ("exact", 1.0), ("exact", 0.3)])
+def test_parity_small(key, mode, lam):
+    w = CASES[key]()
+    o, hT, plan, _ = run(w, mode, lam)
+    check(o, hT, ref_of(key), f"{key}/{mode}/lambda={lam}/segments={plan.n_seg_total}")
+
+
+def test_exact_cp_invariant_to_segments():
+    w = CASES["long_mix"]()
+    outs = [run(w, "exact", lam)[:2] for lam in (0.2, 0.5, 1.0, 3.0)]
+    o0, h0 = run(w, "off")[:2]
+    ro, rh = ref_of("long_mix")
+    for o, h in outs:
+        check(o, h, (ro, rh), "cp-invariance")
+        # two bf16 results of the same value may differ by one ulp; beyond that they agree
+        a, b = util.to64(o), util.to64(o0)
+        excess = np.maximum(np.abs(a - b) - 2 * util.bf16_half_ulp(np.maximum(np.abs(a), np.abs(b))), 0)
+        assert excess.max() <= util.TOL_BF16 * np.sqrt(np.mean(ro ** 2))
+
+
+def test_warmup_mode_matches_warmup_expectation():
+    """Warmup heads equal the oracle's warmup restart, other heads the exact result."""
+    w = make_inputs(64 * 40 + 9, h_qk=1, h_v=4, seed=10, g_kind="mix", with_h0=True)
+    o, hT, plan, ws = run(w, "warmup", 0.5, warmup_chunks=2, warmup_tol=1e-4)
+    modes, bounds = gdn_cp_head_modes(ws, plan)
+    fast = set(w.fast_heads)
+    for jj in range(4):
+        assert int(modes[0, jj]) == (2 if jj in fast else 1), (modes, bounds, fast)
+    f = util.to64
+    segs = [util.segments(w.T, plan.raw.lambda_q8, False)]
+    warm_heads = {jj for jj in range(4) if int(modes[0, jj]) == 2}
+    ro, rh = chunked.gdn_fwd_chunked(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0), [0, w.T],
+                                     segments=segs, warmup_chunks=2, warmup_heads=warm_heads)
+    check(o, hT, (ro, rh), "warmup vs warmup-oracle")
+    check(o, hT, oracle.recurrence(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0)), "warmup vs exact")
+
+
+def test_resume_split_call():
+    w = CASES["long_mix"]()
+    d = w.to(DEV)
+    m = 64 * 30 + 5
+    o_full, h_full = gdn_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, mode="exact", lambda_=0.5)
+    o1, h1 = gdn_chunk_fwd(d.q[:m].contiguous(), d.k[:m].contiguous(), d.v[:m].contiguous(),
+                           d.g[:m].contiguous(), d.beta[:m].contiguous(), d.h0, mode="exact", lambda_=0.5)
+    o2, h2 = gdn_chunk_fwd(d.q[m:].contiguous(), d.k[m:].contiguous(), d.v[m:].contiguous(),
+                           d.g[m:].contiguous(), d.beta[m:].contiguous(), h1, mode="exact", lambda_=0.5)
+    ro, rh = ref_of("long_mix")
+    check(torch.cat([o1, o2]), h2, (ro, rh), "resume")
+
+
+def test_fixed_length_batch():
+    w = make_inputs(cu_seqlens=[0, 300, 600], h_qk=1, h_v=2, seed=11, with_h0=True)
+    d = w.to(DEV)
+    shape = lambda t, h: t.reshape(2, 300, h, -1) if t.dim() == 3 else t.reshape(2, 300, h)
+    o, hT = gdn_chunk_fwd(shape(d.q, 1), shape(d.k, 1), shape(d.v, 2), shape(d.g, 2), shape(d.beta, 2), d.h0,
+                          mode="exact", lambda_=0.5)
+    f = util.to64
+    ref = oracle.recurrence(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0), w.seq_offsets())
+    check(o.reshape(600, 2, 128), hT, ref, "batch B=2")
+
+
+def test_deterministic():
+    w = CASES["ragged_gqa3"]()
+    a = run(w, "exact", 0.3)
+    b = run(w, "exact", 0.3)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_empty_batch_copies_state():
+    w = make_inputs(cu_seqlens=[0, 0, 0], h_qk=1, h_v=2, seed=12, with_h0=True)
+    o, hT, _, _ = run(w, "exact")
+    assert torch.equal(hT.cpu(), w.h0)
+
+
+@pytest.mark.parametrize("name", ["tiny_T512_h2x4", "T32768_h2x8", "T32768_h8x24_h0", "T32768_h16x16",
+                                  "varlen4_T348160_h2x8"])
+def test_parity_standard_workloads(name):
+    """Full-size workloads in the bench's launch configuration (AutoCP)."""
+    w = workload(name)
+    o, hT, plan, ws = run(w, "auto")
+    modes, bounds = gdn_cp_head_modes(ws, plan)
+    f = util.to64
+    ref = oracle.recurrence(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0), w.seq_offsets())
+    check(o, hT, ref, f"{name} plan={plan.mode} segs={plan.n_seg_total} modes={modes.flatten().tolist()}")
