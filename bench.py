@@ -1,0 +1,398 @@
+"""Benchmark of the GDN chunked-prefill forward on GB300.
+
+`python bench.py --gpus N --steps K --warmup W` prints one JSON line.
+
+A step is one whole forward (every kernel of the path) over the 1 x 32768,
+h_qk = 2, h_v = 8 workload (the first row of the FlashQLA pages' forward
+benchmark table), seeded synthetic inputs resident in HBM, AutoCP planning.
+The L2 cache (129 MB) is flushed by writing a 256 MB buffer before every
+timed step; each step is timed with CUDA events on its stream.  `e2e`
+repeats the measurement through the public call with pinned host buffers,
+host-to-device copies of the inputs and device-to-host copies of o and the
+final state inside the timed region.  Under torchrun (N > 1) every rank runs
+an independent replica (the layer needs no collective) and the slowest
+rank's time is used.
+
+`--impl reference` times the float64 CPU oracle on the host cores instead,
+one bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GDN chunked-prefill fwd tokens/s at T=32768 (h_qk/h_v sweep); % of roofline"
+HEADLINE = "T32768_h2x8"
+SWEEP = ["T32768_h8x24_h0", "T32768_h16x16", "varlen4_T348160_h2x8"]
+# FlashQLA on an NVIDIA H200, same workloads (pages' benchmark table), ms per call.
+PAGES_H200_MS = {"T32768_h2x8": 0.310, "T32768_h8x24_h0": 0.659, "T32768_h16x16": 0.493}
+FLUSH_BYTES = 256 << 20
+C, D = 64, 128
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+def algorithmic(w):
+    """Bytes and FLOPs one forward must move / do: q,k,v,g,beta read, o and the
+    final state written (the initial state read when given); the chunked
+    algorithm's contractions counted once."""
+    T, hqk, hv, n = w.T, w.h_qk, w.h_v, w.n_seqs
+    by = T * (2 * hqk * D * 2 + 2 * hv * D * 2 + 2 * hv * 4) + n * hv * D * D * 4
+    if w.h0 is not None:
+        by += n * hv * D * D * 4
+    fl = T * (hv * (6 * C * D + 6 * D * D + C * C / 3) + hqk * 4 * C * D)
+    return by, fl
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.rows = []
+        self.proc = None
+        sel = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            pass
+        self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                    *sel]
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=5)
+        num = lambda x: x.replace(".", "", 1).isdigit()
+        sm = [float(r[1]) for r in self.rows if num(r[1])]
+        mx = [float(r[2]) for r in self.rows if num(r[2])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def time_gpu(name, steps, warmup, device, cp="auto", lambda_=1.0, trace=True):
+    """Times the forward on one workload; returns a dict of measurements."""
+    from gated_deltanet_linear_fwd_gb300 import (gdn_chunk_fwd, gdn_cp_head_modes, gdn_cp_plan,
+                                                 gdn_get_device_status, gdn_set_trace_events, gdn_trace_last)
+    from gated_deltanet_linear_fwd_gb300.inputs import workload
+    w = workload(name)
+    d = w.to(device)
+    plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, cu_seqlens=w.cu_seqlens, mode=cp, lambda_=lambda_)
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
+    out = torch.empty_like(d.v)
+    hT = torch.empty(w.n_seqs, w.h_v, D, D, dtype=torch.float32, device=device)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def fwd():
+        gdn_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, plan=plan, out=out, final_state=hT,
+                      workspace=ws)
+
+    for _ in range(warmup):
+        flush.zero_()
+        fwd()
+    torch.cuda.synchronize(device)
+    code, detail = gdn_get_device_status(ws)
+    names = gdn_trace_last()
+    n_k = len(names)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_k + 1)]
+    for e in ev:
+        e.record(stream)
+    torch.cuda.synchronize(device)
+    if trace:
+        gdn_set_trace_events(ev)
+    per_step, per_kernel = [], [0.0] * n_k
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(steps):
+        flush.zero_()
+        s0.record(stream)
+        fwd()
+        s1.record(stream)
+        s1.synchronize()
+        per_step.append(s0.elapsed_time(s1))
+        if trace:
+            for i in range(n_k):
+                per_kernel[i] += ev[i].elapsed_time(ev[i + 1])
+    if trace:
+        gdn_set_trace_events([])
+    code2, detail2 = gdn_get_device_status(ws)
+    modes, _ = gdn_cp_head_modes(ws, plan)
+    by, fl = algorithmic(w)
+    return {"workload": name, "w": w, "plan": plan, "ms": statistics.mean(per_step),
+            "ms_median": statistics.median(per_step),
+            "kernel_ms": {n: t / steps for n, t in zip(names, per_kernel)} if trace else {},
+            "launches": n_k, "status": (code, detail, code2, detail2), "bytes": by, "flops": fl,
+            "modes": modes.flatten().tolist(), "tokens": w.T}
+
+
+def time_e2e(name, steps, warmup, device, cp="auto"):
+    """The same forward through the public call from pinned host buffers."""
+    from gated_deltanet_linear_fwd_gb300 import gdn_chunk_fwd, gdn_cp_plan
+    from gated_deltanet_linear_fwd_gb300.inputs import workload
+    w = workload(name)
+    pin = lambda t: None if t is None else t.pin_memory()
+    hq, hk, hv_, hg, hb, hh0 = map(pin, (w.q, w.k, w.v, w.g, w.beta, w.h0))
+    dev = lambda t: None if t is None else torch.empty_like(t, device=device)
+    dq, dk, dv, dg, db, dh0 = map(dev, (hq, hk, hv_, hg, hb, hh0))
+    dcu = None if w.cu_seqlens is None else w.cu_seqlens.to(device)
+    plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, cu_seqlens=w.cu_seqlens, mode=cp)
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
+    out = torch.empty_like(dv)
+    hT = torch.empty(w.n_seqs, w.h_v, D, D, dtype=torch.float32, device=device)
+    ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hhT = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv_, hg, hb) + ((hh0,) if hh0 is not None else ()))
+    d2h = ho.numel() * ho.element_size() + hhT.numel() * hhT.element_size()
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        for src, dst in ((hq, dq), (hk, dk), (hv_, dv), (hg, dg), (hb, db), (hh0, dh0)):
+            if src is not None:
+                dst.copy_(src, non_blocking=True)
+        gdn_chunk_fwd(dq, dk, dv, dg, db, dh0, dcu, plan=plan, out=out, final_state=hT, workspace=ws)
+        ho.copy_(out, non_blocking=True)
+        hhT.copy_(hT, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(device)
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(steps):
+        step()
+    s1.record(stream)
+    s1.synchronize()
+    ms = s0.elapsed_time(s1) / steps
+    return {"ms": ms, "h2d": h2d, "d2h": d2h, "tokens": w.T}
+
+
+def cpu_baseline(name, budget_s=12.0):
+    """The float64 oracle, as it stands, on this host's cores: a bounded sample
+    (a prefix of the sequence, all heads) of the same workload."""
+    import oracle
+    from gated_deltanet_linear_fwd_gb300.inputs import workload
+    w = workload(name)
+    cores = oracle.default_threads()
+    f = lambda t: t.double().numpy()
+    tokens = 1024
+    while True:
+        t0 = time.perf_counter()
+        oracle.recurrence(f(w.q[:tokens]), f(w.k[:tokens]), f(w.v[:tokens]), f(w.g[:tokens]),
+                          f(w.beta[:tokens]), None if w.h0 is None else f(w.h0[:1]), [0, tokens])
+        dt = time.perf_counter() - t0
+        if dt * 4 > budget_s or tokens * 2 > w.T:
+            break
+        tokens *= 2
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {tokens} tokens of {name}, all {w.h_v} value heads, one pass ({dt:.2f} s)"}
+
+
+def traffic_from_profile(tag):
+    """DRAM bytes per launch from the committed ncu summary, when it was taken
+    on the current kernel source (its recorded source hash matches)."""
+    path = os.path.join(ROOT, "profiles", f"{tag}.md")
+    src = os.path.join(ROOT, "gated_deltanet_linear_fwd_gb300", "csrc", "gdn_scan.cu")
+    try:
+        txt = open(path).read()
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    vals = {}
+    for line in txt.splitlines():
+        line = line.strip()
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha256_16") != digest:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    from gated_deltanet_linear_fwd_gb300.inputs import workload
+    w = workload(HEADLINE)
+    f = lambda t: t.double().numpy()
+    tokens = 1024
+    arrays = [f(x[:tokens]) for x in (w.q, w.k, w.v, w.g, w.beta)]
+    for _ in range(args.warmup):
+        oracle.recurrence(*arrays, None, [0, tokens])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.recurrence(*arrays, None, [0, tokens])
+    dt = (time.perf_counter() - t0) / args.steps
+    value = tokens / dt
+    cores = oracle.default_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": HEADLINE, "B": 1, "T": 32768, "h_qk": 2, "h_v": 8, "d_k": 128, "d_v": 128},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"first {tokens} tokens of {HEADLINE}, all 8 value heads, per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cp", default="auto", choices=["off", "exact", "warmup", "auto"])
+    ap.add_argument("--lambda", dest="lambda_", type=float, default=1.0)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    hbm, tfl, peak_src = peaks()
+    barrier(world)
+    torch.cuda.synchronize(device)
+    clocks = ClockSampler(device)
+    clocks.start()
+    r = time_gpu(HEADLINE, args.steps, args.warmup, device, args.cp, args.lambda_)
+    clk = clocks.stop()
+    torch.cuda.synchronize(device)
+    barrier(world)
+    ms = max_over_ranks(r["ms"], world, device)
+    value = world * r["tokens"] / (ms * 1e-3)
+    kms = r["kernel_ms"]
+    t_hbm = r["bytes"] / (hbm * 1e9)
+    t_tc = r["flops"] / (tfl * 1e12)
+    roof = None
+    if "scan_out" in kms:
+        # the scan-output kernel moves every algorithmic byte of the layer
+        achieved = r["bytes"] / (kms["scan_out"] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": "scan_out", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": traffic_from_profile("scan_out_T32768_h2x8"),
+                "peak_source": peak_src, "algorithmic_bytes": r["bytes"], "kernel_ms": kms["scan_out"]}
+    e2e = time_e2e(HEADLINE, max(20, args.steps // 10), 3, device, args.cp)
+    e2e_ms = max_over_ranks(e2e["ms"], world, device)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": value / (32768 / (PAGES_H200_MS[HEADLINE] * 1e-3)),
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": HEADLINE, "B": 1, "T": 32768, "h_qk": 2, "h_v": 8, "d_k": 128, "d_v": 128,
+                   "chunk": 64, "cp": r["plan"].mode, "segments": r["plan"].n_seg_total,
+                   "head_modes": r["modes"], "l2": "flushed (256 MB write) before every timed step",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "layer_roofline": {"t_roofline_ms": max(t_hbm, t_tc) * 1e3, "bound": "hbm" if t_hbm >= t_tc else "tensor",
+                           "frac": max(t_hbm, t_tc) * 1e3 / r["ms"], "peak_source": peak_src,
+                           "bytes": r["bytes"], "flops": r["flops"]},
+        "kernels_ms": kms,
+        "gpu_launches": r["launches"] * args.steps,
+        "clocks": clk,
+        "e2e": {"value": world * e2e["tokens"] / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
+        "device_status": list(r["status"]),
+        "vs_baseline_note": "vs FlashQLA on an H200 (pages' table, 0.310 ms): another machine, context only",
+    }
+    if not args.no_sweep and rank == 0:
+        sweep = {}
+        for name in SWEEP:
+            s = time_gpu(name, max(20, args.steps // 20), 5, device, args.cp, args.lambda_)
+            t_r = max(s["bytes"] / (hbm * 1e9), s["flops"] / (tfl * 1e12))
+            sweep[name] = {"tokens_per_s": s["tokens"] / (s["ms"] * 1e-3), "ms": s["ms"], "cp": s["plan"].mode,
+                           "segments": s["plan"].n_seg_total, "roofline_frac": t_r * 1e3 / s["ms"],
+                           "kernels_ms": s["kernel_ms"], "head_modes": s["modes"]}
+            if name in PAGES_H200_MS:
+                sweep[name]["pages_h200_ms"] = PAGES_H200_MS[name]
+        line["sweep"] = sweep
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(HEADLINE)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

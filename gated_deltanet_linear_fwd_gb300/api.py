@@ -130,3 +130,19 @@ def gdn_cp_head_modes(workspace: torch.Tensor, plan: Plan, stream=None):
     shape = (plan.raw.n_seqs, plan.raw.h_v)
     return (torch.tensor(list(modes), dtype=torch.int32).reshape(shape),
             torch.tensor(list(bounds), dtype=torch.float32).reshape(shape))
+
+
+def gdn_set_trace_events(events) -> None:
+    """Register torch.cuda.Event objects (enable_timing=True, recorded once so
+    they exist) for per-kernel timing of this thread's next gdn_chunk_fwd
+    calls; [] turns it off."""
+    n = len(events)
+    arr = (ctypes.c_void_p * max(n, 1))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    L.check(L.load().gdn_set_trace_events(arr if n else None, n), "gdn_set_trace_events")
+
+
+def gdn_trace_last() -> list:
+    """Names of the kernels the last gdn_chunk_fwd on this thread launched."""
+    names = (ctypes.c_char_p * 16)()
+    n = L.load().gdn_trace_last(names, 16)
+    return [names[i].decode() for i in range(n)]

@@ -13,6 +13,27 @@ namespace {
 
 thread_local int g_last_cuda_error = 0;
 
+// ---- tracing: caller-provided events recorded around each launch ----
+constexpr int kMaxTrace = 16;
+thread_local cudaEvent_t g_trace_ev[kMaxTrace];
+thread_local int g_trace_n = 0;
+thread_local const char* g_last_names[kMaxTrace];
+thread_local int g_last_count = 0;
+
+struct LaunchLog {
+  cudaStream_t st;
+  int count = 0;
+  cudaError_t begin() {
+    g_last_count = 0;
+    return g_trace_n > 0 ? cudaEventRecord(g_trace_ev[0], st) : cudaSuccess;
+  }
+  cudaError_t after(const char* name) {
+    if (g_last_count < kMaxTrace) g_last_names[g_last_count++] = name;
+    ++count;
+    return count < g_trace_n ? cudaEventRecord(g_trace_ev[count], st) : cudaSuccess;
+  }
+};
+
 gdn_status cuda_fail(cudaError_t e) {
   g_last_cuda_error = (int)e;
   return GDN_ERR_CUDA;
@@ -265,16 +286,38 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
   if ((st = encode_map(&mk, k, dims->h_qk, T_total, f32)) != GDN_OK) return st;
   if ((st = encode_map(&mv, v, dims->h_v, T_total, f32)) != GDN_OK) return st;
 
-  if (plan->mode == GDN_CP_OFF) {
-    if ((e = launch_scan_out(p, mq, mk, mv, plan->n_seg_total, cs)) != cudaSuccess) return cuda_fail(e);
-    return GDN_OK;
+  LaunchLog log{cs};
+  if ((e = log.begin()) != cudaSuccess) return cuda_fail(e);
+  if (plan->mode != GDN_CP_OFF) {
+    if (plan->mode == GDN_CP_WARMUP) {
+      if ((e = launch_gate_bound(p, cs)) != cudaSuccess) return cuda_fail(e);
+      if ((e = log.after("gate_bound")) != cudaSuccess) return cuda_fail(e);
+    }
+    if ((e = launch_scan_prep(p, mq, mk, mv, cs)) != cudaSuccess) return cuda_fail(e);
+    if ((e = log.after("scan_prep")) != cudaSuccess) return cuda_fail(e);
+    if ((e = launch_combine(p, cs)) != cudaSuccess) return cuda_fail(e);
+    if ((e = log.after("combine")) != cudaSuccess) return cuda_fail(e);
   }
-  if (plan->mode == GDN_CP_WARMUP)
-    if ((e = launch_gate_bound(p, cs)) != cudaSuccess) return cuda_fail(e);
-  if ((e = launch_scan_prep(p, mq, mk, mv, cs)) != cudaSuccess) return cuda_fail(e);
-  if ((e = launch_combine(p, cs)) != cudaSuccess) return cuda_fail(e);
   if ((e = launch_scan_out(p, mq, mk, mv, plan->n_seg_total, cs)) != cudaSuccess) return cuda_fail(e);
+  if ((e = log.after("scan_out")) != cudaSuccess) return cuda_fail(e);
   return GDN_OK;
+}
+
+gdn_status gdn_set_trace_events(void* const* events, int n_events) {
+  if (n_events < 0 || n_events > kMaxTrace) return GDN_ERR_INVALID_ARG;
+  if (!events) n_events = 0;
+  for (int i = 0; i < n_events; ++i) {
+    if (!events[i]) return GDN_ERR_INVALID_ARG;
+    g_trace_ev[i] = reinterpret_cast<cudaEvent_t>(events[i]);
+  }
+  g_trace_n = n_events;
+  return GDN_OK;
+}
+
+int gdn_trace_last(const char** names, int max_names) {
+  if (names)
+    for (int i = 0; i < g_last_count && i < max_names; ++i) names[i] = g_last_names[i];
+  return g_last_count;
 }
 
 gdn_status gdn_get_device_status(const void* workspace, void* stream, int* code, int* detail) {

@@ -186,6 +186,26 @@ gdn_status gdn_get_device_status(const void* workspace, void* stream, int* code,
 gdn_status gdn_cp_head_modes(const void* workspace, const gdn_cp_plan_t* plan, int32_t* modes_host,
                              float* log_bound_host, void* stream);
 
+/*
+ * gdn_set_trace_events -- optional per-kernel timing (tracing).  Registers,
+ * for the calling host thread, up to 16 caller-created cudaEvent_t handles.
+ * While registered, each gdn_chunk_fwd on this thread records events[0] on
+ * its stream before its first kernel and events[i + 1] right after its i-th
+ * kernel launch, so cudaEventElapsedTime(events[i], events[i + 1]) is the
+ * device time of kernel i.  n_events = 0 (or events = NULL) turns tracing
+ * off.  The caller keeps ownership of the events.
+ * Errors: INVALID_ARG for n_events outside 0..16 or a NULL event.
+ */
+gdn_status gdn_set_trace_events(void* const* events, int n_events);
+
+/*
+ * gdn_trace_last -- names of the kernels the last gdn_chunk_fwd on this
+ * thread launched, in order (static strings), and their count.
+ *   names : host array of at least max_names pointers, or NULL.
+ * Returns the number of kernels launched (0 before any call).
+ */
+int gdn_trace_last(const char** names, int max_names);
+
 #ifdef __cplusplus
 }
 #endif
