@@ -146,3 +146,17 @@ def gdn_trace_last() -> list:
     names = (ctypes.c_char_p * 16)()
     n = L.load().gdn_trace_last(names, 16)
     return [names[i].decode() for i in range(n)]
+
+
+def gdn_chunk_fwd_static(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, plan: Plan, out, final_state=None,
+                         stream=None):
+    """gdn_chunk_fwd_static: the forward with the library's built-in 8 MiB
+    device workspace, for callers that cannot allocate device memory.  The
+    caller passes every input and output (nothing is allocated here)."""
+    dims = L.gdn_dims(q.shape[0] if q.dim() == 4 else 1, q.shape[-3], q.shape[-2], v.shape[-2], q.shape[-1],
+                      v.shape[-1], plan.raw.n_seqs, 0.0, _DT.get(q.dtype, -1))
+    st = L.load().gdn_chunk_fwd_static(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                                       _ptr(cu_seqlens), _ptr(out), _ptr(final_state), ctypes.byref(dims),
+                                       ctypes.byref(plan.raw), _stream_handle(stream))
+    L.check(st, "gdn_chunk_fwd_static")
+    return out, final_state

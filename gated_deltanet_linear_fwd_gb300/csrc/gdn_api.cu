@@ -106,6 +106,31 @@ gdn_status encode_map(CUtensorMap* m, const void* base, int heads, int64_t token
   return GDN_OK;
 }
 
+// ---- fixed device workspace for callers that cannot allocate ----
+// 8 MiB: every CP-off plan (status word, head modes and segment bounds only)
+// and CP plans of up to 42 (segment, value head) pairs (192 KiB each).
+constexpr size_t kStaticWorkspaceBytes = size_t(8) << 20;
+static __device__ __align__(256) uint8_t g_static_workspace[kStaticWorkspaceBytes];
+void* g_static_ws_dev[kMaxDevices] = {};
+
+// Device address of g_static_workspace on the current device, looked up once
+// per device (the host-side name is not a device address).
+gdn_status static_workspace(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_setup_mu);
+  if (!g_static_ws_dev[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_static_workspace);
+    if (e != cudaSuccess || !ptr) return cuda_fail(e == cudaSuccess ? cudaErrorInvalidSymbol : e);
+    g_static_ws_dev[dev] = ptr;
+  }
+  *out = g_static_ws_dev[dev];
+  return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -355,3 +380,16 @@ gdn_status gdn_cp_head_modes(const void* workspace, const gdn_cp_plan_t* plan, i
 }
 
 }  // extern "C"
+
+extern "C" gdn_status gdn_chunk_fwd_static(const void* q, const void* k, const void* v, const float* g,
+                                          const float* beta, const float* initial_state,
+                                          const int32_t* cu_seqlens_dev, void* out, float* final_state,
+                                          const gdn_dims* dims, const gdn_cp_plan_t* plan, void* stream) {
+  if (!plan) return GDN_ERR_INVALID_ARG;
+  if (plan->workspace_bytes > kStaticWorkspaceBytes) return GDN_ERR_WORKSPACE;
+  void* ws = nullptr;
+  gdn_status st = static_workspace(&ws);
+  if (st != GDN_OK) return st;
+  return gdn_chunk_fwd(q, k, v, g, beta, initial_state, cu_seqlens_dev, out, final_state, dims, plan, ws,
+                       kStaticWorkspaceBytes, stream);
+}

@@ -187,6 +187,36 @@ gdn_status gdn_cp_head_modes(const void* workspace, const gdn_cp_plan_t* plan, i
                              float* log_bound_host, void* stream);
 
 /*
+ * gdn_chunk_fwd_static -- gdn_chunk_fwd for callers that cannot allocate
+ * device memory.  The FlashQLA pages have no counterpart: this is a library
+ * convenience.  Some callers can't call cudaMalloc or hand out scratch: code
+ * running under a runtime that owns all device memory (an inference
+ * server's arena, a plugin interface that passes only its inputs and
+ * outputs), or code that must not allocate after start-up.  This entry point
+ * takes the same arguments as gdn_chunk_fwd minus the workspace and uses a
+ * fixed 8 MiB device array built into the library instead; every GPU that
+ * loads the library holds that array until the process exits.
+ *   - Fits every GDN_CP_OFF plan and context-parallel plans whose
+ *     plan->workspace_bytes is at most 8 MiB (about 42 (segment, value head)
+ *     pairs); larger plans are rejected with GDN_ERR_WORKSPACE before any
+ *     device work.
+ *   - Allocates nothing.  Its first call on a device looks up the array's
+ *     device address (cudaGetSymbolAddress) with that device current; make
+ *     that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     every part the forward reads is written or cleared within the call.
+ *     Calls that may overlap on the GPU (other streams, other host threads)
+ *     race on the array: serialise them.
+ *   - The device status word of these calls lives in the shared array and
+ *     is not readable through gdn_get_device_status.
+ * Errors: as gdn_chunk_fwd, plus WORKSPACE for plans above the limit.
+ */
+gdn_status gdn_chunk_fwd_static(const void* q, const void* k, const void* v, const float* g,
+                                const float* beta, const float* initial_state,
+                                const int32_t* cu_seqlens_dev, void* out, float* final_state,
+                                const gdn_dims* dims, const gdn_cp_plan_t* plan, void* stream);
+
+/*
  * gdn_set_trace_events -- optional per-kernel timing (tracing).  Registers,
  * for the calling host thread, up to 16 caller-created cudaEvent_t handles.
  * While registered, each gdn_chunk_fwd on this thread records events[0] on
