@@ -142,7 +142,7 @@ def barrier(world):
         dist.barrier()
 
 
-def time_gpu(name, steps, warmup, device, cp="auto", lambda_=1.0, trace=True):
+def time_gpu(name, steps, warmup, device, cp="auto", lambda_=0.0, trace=True):
     """Times the forward on one workload; returns a dict of measurements."""
     from gated_deltanet_linear_fwd_gb300 import (gdn_chunk_fwd, gdn_cp_head_modes, gdn_cp_plan,
                                                  gdn_get_device_status, gdn_set_trace_events, gdn_trace_last)
@@ -318,7 +318,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cp", default="auto", choices=["off", "exact", "warmup", "auto"])
-    ap.add_argument("--lambda", dest="lambda_", type=float, default=1.0)
+    ap.add_argument("--lambda", dest="lambda_", type=float, default=0.0,
+                    help="segment-length factor; 0 lets the planner choose")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

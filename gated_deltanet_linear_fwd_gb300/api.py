@@ -46,7 +46,7 @@ def _cu_list(cu_seqlens) -> Optional[list]:
 
 
 def gdn_cp_plan(*, T: int, h_qk: int, h_v: int, B: int = 1, cu_seqlens=None,
-                dtype: torch.dtype = torch.bfloat16, mode: str = "auto", lambda_: float = 1.0,
+                dtype: torch.dtype = torch.bfloat16, mode: str = "auto", lambda_: float = 0.0,
                 warmup_chunks: int = 8, warmup_tol: float = 1e-4, sm_count: int = 0,
                 scale: float = 0.0, d_k: int = 128, d_v: int = 128) -> Plan:
     """Host-only planning (gdn_cp_plan).  T = tokens per row (varlen: total)."""
@@ -75,7 +75,7 @@ def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
                   *, plan: Optional[Plan] = None, out: Optional[torch.Tensor] = None,
                   final_state: Optional[torch.Tensor] = None, output_final_state: bool = True,
                   workspace: Optional[torch.Tensor] = None, stream=None, scale: float = 0.0,
-                  mode: str = "auto", lambda_: float = 1.0, warmup_chunks: int = 8,
+                  mode: str = "auto", lambda_: float = 0.0, warmup_chunks: int = 8,
                   warmup_tol: float = 1e-4):
     """The chunked-prefill forward (gdn_chunk_fwd).
 

@@ -1,6 +1,8 @@
 // Host side of the C ABI declared in include/gdn.h: planning, argument
 // checks, TMA tensor maps, and the launch sequence of the forward.
 #include <cmath>
+#include <algorithm>
+#include <climits>
 #include <cstring>
 #include <mutex>
 
@@ -76,6 +78,37 @@ gdn_status device_setup(int* dev_out) {
   g_sm_count[dev] = sms;
   g_setup_done[dev] = true;
   return GDN_OK;
+}
+
+// AutoCP's choice of lambda (FlashQLA pages, section "AutoCP": the degree
+// of parallelism follows L = lambda sqrt(N)).  The scan kernel runs one CTA
+// per (segment, value head) and one CTA per SM, so its time is about
+// (waves of CTAs) x (longest segment, in chunks).  Among lambda = k/8 the
+// planner takes the one that minimises that product; ties go to fewer
+// segments (less warmup and combine work).
+int pick_lambda_q8(const gdn_dims* d, const int32_t* cu, int sm_count) {
+  int best_q8 = 256;
+  int64_t best_cost = INT64_MAX, best_segs = INT64_MAX;
+  for (int q8 = 32; q8 <= 4096; q8 += 32) {
+    int64_t segs = 0;
+    int longest = 0;
+    for (int n = 0; n < d->n_seqs; ++n) {
+      const int64_t len = cu ? (int64_t)cu[n + 1] - cu[n] : d->T;
+      const int N = chunks_of(len);
+      const int ns = seg_count(N, q8, false);
+      segs += ns;
+      for (int s = 0; s < ns; ++s) longest = std::max(longest, seg_first(s + 1, N, ns) - seg_first(s, N, ns));
+    }
+    const int64_t ctas = segs * d->h_v;
+    const int64_t waves = (ctas + sm_count - 1) / sm_count;
+    const int64_t cost = waves * (int64_t)(longest + 1);  // +1: a warmup chunk per segment
+    if (cost < best_cost || (cost == best_cost && segs < best_segs)) {
+      best_cost = cost;
+      best_segs = segs;
+      best_q8 = q8;
+    }
+  }
+  return best_q8;
 }
 
 gdn_status check_dims(const gdn_dims* d) {
@@ -167,7 +200,7 @@ gdn_status gdn_cp_plan(const gdn_dims* dims, const int32_t* cu, const gdn_cp_opt
   gdn_cp_opts o = {GDN_CP_AUTO, 1.0f, 8, 1e-4f, 0};
   if (opts) o = *opts;
   if (o.mode < GDN_CP_OFF || o.mode > GDN_CP_AUTO) return GDN_ERR_UNSUPPORTED;
-  if (!(o.lambda > 0.f)) o.lambda = 1.0f;
+  const bool auto_lambda = !(o.lambda > 0.f);
   if (o.lambda > 1000.f) return GDN_ERR_INVALID_ARG;
   if (o.warmup_chunks <= 0) o.warmup_chunks = 8;
   if (!(o.warmup_tol > 0.f)) o.warmup_tol = 1e-4f;
@@ -189,8 +222,12 @@ gdn_status gdn_cp_plan(const gdn_dims* dims, const int32_t* cu, const gdn_cp_opt
   p.h_v = dims->h_v;
   p.h_qk = dims->h_qk;
   p.dtype = dims->dtype;
-  p.lambda_q8 = (int)std::lround(o.lambda * 256.0);
-  if (p.lambda_q8 < 1) p.lambda_q8 = 1;
+  if (auto_lambda) {
+    p.lambda_q8 = mode == GDN_CP_OFF ? 256 : pick_lambda_q8(dims, cu, o.sm_count);
+  } else {
+    p.lambda_q8 = (int)std::lround(o.lambda * 256.0);
+    if (p.lambda_q8 < 1) p.lambda_q8 = 1;
+  }
   p.warmup_chunks = o.warmup_chunks;
   p.warmup_tol = o.warmup_tol;
   p.sm_count = o.sm_count;
@@ -214,8 +251,8 @@ gdn_status gdn_cp_plan(const gdn_dims* dims, const int32_t* cu, const gdn_cp_opt
   size_t off = 256;
   p.off_head = off;
   off = align_up(off + heads * 8, 256);
-  p.off_seg_bound = off;
-  off = align_up(off + segheads * 4, 256);
+  p.off_seg_bound = off;  // seg_bound (fp32) then seg_w (int32)
+  off = align_up(off + segheads * 8, 256);
   if (mode != GDN_CP_OFF) {
     const size_t mat = (size_t)kDim * kDim * 4;
     p.off_R = off;
@@ -287,6 +324,7 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
   p.head_mode = reinterpret_cast<int*>(ws + plan->off_head);
   p.head_bound = reinterpret_cast<float*>(ws + plan->off_head + (size_t)dims->n_seqs * dims->h_v * 4);
   p.seg_bound = reinterpret_cast<float*>(ws + plan->off_seg_bound);
+  p.seg_w = reinterpret_cast<int*>(ws + plan->off_seg_bound + (size_t)plan->n_seg_total * dims->h_v * 4);
   if (plan->mode != GDN_CP_OFF) {
     p.R = reinterpret_cast<float*>(ws + plan->off_R);
     p.Sloc = reinterpret_cast<float*>(ws + plan->off_Sloc);

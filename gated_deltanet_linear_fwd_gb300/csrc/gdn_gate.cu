@@ -10,9 +10,11 @@
 // beta k k^T) has spectral norm <= alpha * max(1, |1 - beta ||k||^2|), so
 // the relative error is at most
 //     exp( sum_{t in W} [ g_t + log max(1, |1 - beta_t ||k_t||^2|) ] ).
-// The kernel writes that exponent; a (sequence, head) takes warmup when the
-// largest exponent over its segments is <= log(tol).  Segment 0, and any
-// window that reaches the sequence start, needs no restart: -inf.
+// The kernel picks, per segment, the smallest depth w (at most the planned
+// maximum) whose exponent is <= log(tol), and writes w and that exponent; a
+// depth that reaches the sequence start runs exactly from the initial state
+// (exponent -inf).  No acceptable depth: w = -1, and the (sequence, head)
+// runs in exact mode.  Segment 0 needs no restart (w = 0).
 #include <cuda_bf16.h>
 
 #include "gdn_internal.cuh"
@@ -55,8 +57,9 @@ __device__ __forceinline__ float row_sq_norm<float>(const float* krow) {
 
 template <typename KT>
 __global__ void __launch_bounds__(256) gate_bound_kernel(const Problem p) {
+  constexpr int kMaxWin = 64;
   __shared__ SegInfo s_seg;
-  __shared__ float s_part[8];
+  __shared__ float s_chunk[kMaxWin];  // exponent contribution of window chunk cb-1-w
   __shared__ int s_ok;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int j = blockIdx.y;
@@ -75,30 +78,54 @@ __global__ void __launch_bounds__(256) gate_bound_kernel(const Problem p) {
   }
   const SegInfo si = s_seg;
   const float neg_inf = -__int_as_float(0x7f800000);
-  float* dst = p.seg_bound + (size_t)blockIdx.x * p.h_v + j;
-  const int ws = si.cb - p.warmup_chunks;
-  if (si.s == 0 || ws <= 0) {
-    if (tid == 0) *dst = neg_inf;
+  const size_t slot = (size_t)blockIdx.x * p.h_v + j;
+  if (si.s == 0) {
+    if (tid == 0) {
+      p.seg_bound[slot] = neg_inf;
+      p.seg_w[slot] = 0;
+    }
     return;
   }
+  const int wmax = min(p.warmup_chunks, kMaxWin);
+  const int nwin = min(wmax, si.cb);
   const int iq = (int)(((int64_t)j * p.h_qk) / p.h_v);
   const KT* kbase = reinterpret_cast<const KT*>(p.k);
-  const int64_t t_begin = si.bos + (int64_t)ws * kChunk, t_end = si.bos + (int64_t)si.cb * kChunk;
-  float acc = 0.f;
-  for (int64_t t = t_begin + tid; t < t_end; t += blockDim.x) {
-    const float gsum = p.g[(size_t)t * p.h_v + j];
-    const float b = p.beta[(size_t)t * p.h_v + j];
-    const float kk = row_sq_norm<KT>(kbase + ((size_t)t * p.h_qk + iq) * kDim);
-    acc += gsum + __logf(fmaxf(1.f, fabsf(1.f - b * kk)));
-  }
+  for (int w = warp; w < nwin; w += 8) {  // one warp per window chunk, two tokens per lane
+    const int64_t t0 = si.bos + (int64_t)(si.cb - 1 - w) * kChunk;
+    float acc = 0.f;
 #pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, d);
-  if (lane == 0) s_part[warp] = acc;
+    for (int e = 0; e < 2; ++e) {
+      const int64_t t = t0 + 2 * lane + e;
+      const float gsum = p.g[(size_t)t * p.h_v + j];
+      const float b = p.beta[(size_t)t * p.h_v + j];
+      const float kk = row_sq_norm<KT>(kbase + ((size_t)t * p.h_qk + iq) * kDim);
+      acc += gsum + __logf(fmaxf(1.f, fabsf(1.f - b * kk)));
+    }
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, d);
+    if (lane == 0) s_chunk[w] = acc;
+  }
   __syncthreads();
   if (tid == 0) {
-    float tot = 0.f;
-    for (int w = 0; w < 8; ++w) tot += s_part[w];
-    *dst = tot;
+    float acc = 0.f;
+    int wsel = -1;
+    float bsel = 0.f;
+    for (int w = 1; w <= nwin; ++w) {
+      acc += s_chunk[w - 1];
+      if (si.cb - w == 0) {  // reaches the sequence start: exact from the initial state
+        wsel = w;
+        bsel = neg_inf;
+        break;
+      }
+      if (acc <= p.log_tol) {
+        wsel = w;
+        bsel = acc;
+        break;
+      }
+    }
+    if (wsel < 0) bsel = acc;
+    p.seg_w[slot] = wsel;
+    p.seg_bound[slot] = bsel;
   }
 }
 

@@ -18,6 +18,7 @@ constexpr int kDetTmaWait = 1;
 constexpr int kDetMmaWait = 2;
 constexpr int kDetSegMismatch = 3;
 constexpr int kDetCombineOrder = 4;
+constexpr int kDetFp16Range = 5;  // a value outside the fp16 MMA operand range
 
 // Head mode words (workspace head-mode section).
 constexpr int kModeOff = 0;
@@ -50,7 +51,9 @@ struct Problem {
   int* status;              // [0] code, [1] detail
   int* head_mode;           // [n_seqs * h_v]
   float* head_bound;        // [n_seqs * h_v]
-  float* seg_bound;         // [n_seg_total * h_v]
+  float* seg_bound;         // [n_seg_total * h_v] log warmup error bound of the chosen depth
+  int* seg_w;               // [n_seg_total * h_v] warmup depth in chunks; -1: no depth up to the
+                            // planned maximum meets the tolerance (the head runs exactly)
   float* R;                 // [n_seg_total, h_v, 128, 128] row-major (row = d_k in)
   float* Sloc;              // [n_seg_total, h_v, 128, 128] row = d_v
   float* Sstart;            // [n_seg_total, h_v, 128, 128] row = d_v
@@ -149,11 +152,14 @@ __device__ inline float head_log_bound(const Problem& p, const SegInfo& si, int 
   return m;
 }
 
-// Mode a (sequence, head) takes under the plan.
+// Mode a (sequence, head) takes under the plan: warmup when every segment
+// found a restart depth whose bound meets the tolerance.
 __device__ inline int head_mode_of(const Problem& p, const SegInfo& si, int j) {
   if (p.plan_mode == kModeOff) return kModeOff;
   if (p.plan_mode == kModeExact) return kModeExact;
-  return head_log_bound(p, si, j) <= p.log_tol ? kModeWarmup : kModeExact;
+  for (int s = 1; s < si.n_seg; ++s)
+    if (p.seg_w[(size_t)(si.seg_base + s) * p.h_v + j] < 0) return kModeExact;
+  return kModeWarmup;
 }
 
 // ---- kernel launchers (defined in the .cu files) ----

@@ -86,8 +86,10 @@ typedef struct gdn_dims {
 
 typedef struct gdn_cp_opts {
   int mode;          /* GDN_CP_* */
-  float lambda;      /* segment length L = round(lambda * sqrt(N)) chunks; <= 0 selects 1.0.
-                        lambda is used in steps of 1/256. */
+  float lambda;      /* segment length L = round(lambda * sqrt(N)) chunks, lambda used in
+                        steps of 1/256; <= 0 lets the planner choose it: the lambda (a
+                        multiple of 1/8) minimising (waves of CTAs over sm_count) x (longest
+                        segment + 1) */
   int warmup_chunks; /* warmup restart depth w in chunks; <= 0 selects 8 */
   float warmup_tol;  /* accept warmup for a (sequence, head) when its bound
                         max over segments of exp(sum g over the window) *

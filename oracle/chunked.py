@@ -127,8 +127,9 @@ def gdn_fwd_chunked(q, k, v, g, beta, h0, cu_seqlens, scale=None, C=CHUNK,
     warmup_chunks / warmup_heads: segments after the first of a head in
       warmup_heads (a set of (seq, head) or of head indices; None: all heads)
       restart from a zero state warmup_chunks chunks before their start
-      instead of taking the exactly combined start state.  A restart clipped
-      at the sequence start runs exactly from h0.
+      instead of taking the exactly combined start state.  warmup_chunks is
+      an int, or a dict {(seq, head, segment): depth} giving each segment its
+      own depth.  A restart clipped at the sequence start runs exactly from h0.
     Returns (o [T, h_v, d_v], hT [N, h_v, d_k, d_v]).
     """
     T, h_qk, d_k = q.shape
@@ -153,11 +154,13 @@ def gdn_fwd_chunked(q, k, v, g, beta, h0, cu_seqlens, scale=None, C=CHUNK,
             if use_warm:
                 H = H0
                 for si, (cb, ce) in enumerate(segs):
-                    if si == 0 or cb - warmup_chunks <= 0:
+                    wd = (warmup_chunks[(n, j, si)] if isinstance(warmup_chunks, dict) and si > 0
+                          else warmup_chunks)
+                    if si == 0 or cb - wd <= 0:
                         Hs = scan_head(qs, ks, vs, gs, bs, H0, scale, C, (0, cb)) if cb > 0 else H0
                     else:
                         Hs = scan_head(qs, ks, vs, gs, bs, np.zeros((d_k, d_v)), scale, C,
-                                       (cb - warmup_chunks, cb))
+                                       (cb - wd, cb))
                     H = scan_head(qs, ks, vs, gs, bs, Hs, scale, C, (cb, ce), out=out)
             else:
                 # exact: local transitions, exact combine, then the scan per segment

@@ -141,3 +141,11 @@ def test_binding_fails_loudly_without_library(tmp_path):
             L.load(str(tmp_path / "missing.so"))
     finally:
         L._lib = saved
+
+
+@pytest.mark.parametrize("cu,h_v,sms", [([0, 32768], 8, 152), ([0, 32768], 24, 148),
+                                        ([0, 262144, 327680, 344064, 348160], 8, 152), ([0, 512], 4, 152)])
+def test_plan_automatic_lambda(lib, cu, h_v, sms):
+    st, p = plan(lib, cu[-1], h_v=h_v, cu=cu, mode=2, lam=0.0, sms=sms)
+    assert st == 0
+    assert p.lambda_q8 == util.auto_lambda_q8([cu[n + 1] - cu[n] for n in range(len(cu) - 1)], h_v, sms)

@@ -31,7 +31,7 @@ from gated_deltanet_linear_fwd_gb300.inputs import make_inputs, workload  # noqa
 DEV = "cuda:0"
 
 
-def run(w, mode="off", lambda_=1.0, warmup_chunks=8, warmup_tol=1e-4, h0=True):
+def run(w, mode="off", lambda_=0.0, warmup_chunks=8, warmup_tol=1e-4, h0=True):
     d = w.to(DEV)
     plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, cu_seqlens=w.cu_seqlens, mode=mode, lambda_=lambda_,
                        warmup_chunks=warmup_chunks, warmup_tol=warmup_tol)
@@ -90,18 +90,23 @@ def test_exact_cp_invariant_to_segments():
 
 
 def test_warmup_mode_matches_warmup_expectation():
-    """Warmup heads equal the oracle's warmup restart, other heads the exact result."""
+    """Warmup heads equal the oracle's warmup restart (per-segment depth by the
+    documented rule), other heads the exact result."""
     w = make_inputs(64 * 40 + 9, h_qk=1, h_v=4, seed=10, g_kind="mix", with_h0=True)
     o, hT, plan, ws = run(w, "warmup", 0.5, warmup_chunks=2, warmup_tol=1e-4)
     modes, bounds = gdn_cp_head_modes(ws, plan)
     fast = set(w.fast_heads)
+    depths = util.warmup_depths(w, plan.raw.lambda_q8, 2, 1e-4)
     for jj in range(4):
-        assert int(modes[0, jj]) == (2 if jj in fast else 1), (modes, bounds, fast)
+        expect_warm = all(depths[(0, jj, s)] is not None for s in range(1, plan.n_seg_total))
+        assert expect_warm == (jj in fast)
+        assert int(modes[0, jj]) == (2 if expect_warm else 1), (modes, bounds, fast)
     f = util.to64
     segs = [util.segments(w.T, plan.raw.lambda_q8, False)]
     warm_heads = {jj for jj in range(4) if int(modes[0, jj]) == 2}
+    wd = {key: (v if v is not None else 0) for key, v in depths.items()}
     ro, rh = chunked.gdn_fwd_chunked(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0), [0, w.T],
-                                     segments=segs, warmup_chunks=2, warmup_heads=warm_heads)
+                                     segments=segs, warmup_chunks=wd, warmup_heads=warm_heads)
     check(o, hT, (ro, rh), "warmup vs warmup-oracle")
     check(o, hT, oracle.recurrence(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0)), "warmup vs exact")
 

@@ -56,3 +56,50 @@ def parity_f32(out_gpu: torch.Tensor, ref: np.ndarray) -> float:
 
 def to64(t):
     return None if t is None else t.detach().double().cpu().numpy()
+
+
+def warmup_depths(w, lambda_q8, wmax, tol):
+    """Per (seq, head, segment) warmup depth by the documented rule: the
+    smallest w <= wmax with sum over the w chunks before the segment of
+    g + log max(1, |1 - beta ||k||^2|) <= log(tol); a window reaching the
+    sequence start runs exactly; None when no depth qualifies."""
+    f = to64
+    g, beta, k = f(w.g), f(w.beta), f(w.k)
+    offs = w.seq_offsets()
+    out = {}
+    for n in range(len(offs) - 1):
+        bos, eos = offs[n], offs[n + 1]
+        segs = segments(eos - bos, lambda_q8, False)
+        for j in range(w.h_v):
+            i = (j * w.h_qk) // w.h_v
+            kk = (k[bos:eos, i] ** 2).sum(-1)
+            term = g[bos:eos, j] + np.log(np.maximum(1.0, np.abs(1.0 - beta[bos:eos, j] * kk)))
+            for si, (cb, _) in enumerate(segs):
+                if si == 0:
+                    continue
+                acc, wsel = 0.0, None
+                for wd in range(1, min(wmax, cb) + 1):
+                    acc += term[(cb - wd) * 64:(cb - wd + 1) * 64].sum()
+                    if cb - wd == 0 or acc <= math.log(tol):
+                        wsel = wd
+                        break
+                out[(n, j, si)] = wsel
+    return out
+
+
+def auto_lambda_q8(T_list, h_v, sm_count):
+    """The planner's automatic lambda, restated from its documented rule:
+    among lambda = k/8 (k = 1..128) minimise waves x (longest segment + 1),
+    ties to fewer segments."""
+    best = None
+    for q8 in range(32, 4097, 32):
+        segs, longest = 0, 0
+        for n_tok in T_list:
+            sg = segments(n_tok, q8, False)
+            segs += len(sg)
+            longest = max(longest, max(b - a for a, b in sg))
+        waves = -(-segs * h_v // sm_count)
+        key = (waves * (longest + 1), segs)
+        if best is None or key < best[0]:
+            best = (key, q8)
+    return best[1]
