@@ -290,7 +290,6 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
   if ((initial_state && !aligned16(initial_state)) || (final_state && !aligned16(final_state)) ||
       (cu_dev && (reinterpret_cast<uintptr_t>(cu_dev) & 3u)))
     return GDN_ERR_MISALIGNED;
-  if (dims->dtype == GDN_F32) return GDN_ERR_UNSUPPORTED;  // fp32 path: see the fp32 kernels
 
   int dev = 0;
   st = device_setup(&dev);
@@ -343,8 +342,15 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
     }
     return GDN_OK;
   }
+  if (dims->dtype == GDN_F32) {  // fp32 inputs: the recurrence on the CUDA cores, in fp32
+    LaunchLog log{cs};
+    if ((e = log.begin()) != cudaSuccess) return cuda_fail(e);
+    if ((e = launch_recurrence_f32(p, cs)) != cudaSuccess) return cuda_fail(e);
+    if ((e = log.after("recurrence_f32")) != cudaSuccess) return cuda_fail(e);
+    return GDN_OK;
+  }
   CUtensorMap mq, mk, mv;
-  const bool f32 = dims->dtype == GDN_F32;
+  const bool f32 = false;
   if ((st = encode_map(&mq, q, dims->h_qk, T_total, f32)) != GDN_OK) return st;
   if ((st = encode_map(&mk, k, dims->h_qk, T_total, f32)) != GDN_OK) return st;
   if ((st = encode_map(&mv, v, dims->h_v, T_total, f32)) != GDN_OK) return st;
@@ -399,7 +405,7 @@ gdn_status gdn_cp_head_modes(const void* workspace, const gdn_cp_plan_t* plan, i
                              void* stream) {
   if (!workspace || !plan) return GDN_ERR_INVALID_ARG;
   const size_t heads = (size_t)plan->n_seqs * plan->h_v;
-  if (plan->mode == GDN_CP_OFF) {
+  if (plan->mode == GDN_CP_OFF || plan->dtype == GDN_F32) {  // no per-head modes taken
     for (size_t i = 0; i < heads; ++i) {
       if (modes) modes[i] = GDN_CP_OFF;
       if (bounds) bounds[i] = -INFINITY;

@@ -169,6 +169,7 @@ cudaError_t launch_scan_prep(const Problem& p, const CUtensorMap& mq, const CUte
 cudaError_t launch_combine(const Problem& p, cudaStream_t st);
 cudaError_t launch_scan_out(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
                             const CUtensorMap& mv, int grid_x, cudaStream_t st);
+cudaError_t launch_recurrence_f32(const Problem& p, cudaStream_t st);
 cudaError_t scan_kernel_setup();
 cudaError_t combine_kernel_setup();
 

@@ -58,7 +58,12 @@ typedef enum gdn_status {
   GDN_ERR_DEVICE_CHECK = 7    /* (from gdn_get_device_status) a kernel's own check failed */
 } gdn_status;
 
-/* Element types of q, k, v and out.  g, beta, states are always fp32. */
+/* Element types of q, k, v and out.  g, beta, states are always fp32.
+ *   GDN_BF16: the chunked tcgen05 path (fp16 MMA operands, fp32 accumulation),
+ *             with the plan's context parallelism.
+ *   GDN_F32:  fp32 throughout, on the CUDA cores: the recurrence itself,
+ *             parallel over (sequence, value head, 16 state rows); the plan's
+ *             segments are not used.  For results within 1e-4 of exact. */
 enum { GDN_BF16 = 0, GDN_F32 = 1 };
 
 /* Intra-card context parallelism [FlashQLA, "AutoCP"]. */

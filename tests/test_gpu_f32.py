@@ -1,0 +1,43 @@
+"""GPU parity of the fp32 path (q, k, v, o in fp32) against the float64
+oracle: max|diff| <= 1e-4 * RMS(ref) for o and for the final state."""
+from __future__ import annotations
+
+import pytest
+import torch
+
+import oracle
+from tests import util
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU, skipped there
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from gated_deltanet_linear_fwd_gb300 import gdn_chunk_fwd, gdn_cp_plan, gdn_get_device_status  # noqa: E402
+from gated_deltanet_linear_fwd_gb300.inputs import make_inputs, workload  # noqa: E402
+
+TOL_F32 = 1e-4
+
+CASES = {
+    "tiny": lambda: workload("tiny_T512_h2x4", dtype=torch.float32),
+    "ragged_gqa3_h0": lambda: make_inputs(cu_seqlens=[0, 1, 65, 200, 200, 391, 1000], h_qk=2, h_v=6, seed=7,
+                                          with_h0=True, dtype=torch.float32),
+    "long_mix_h0": lambda: make_inputs(8192 + 5, h_qk=2, h_v=8, seed=13, with_h0=True, dtype=torch.float32),
+}
+
+
+@pytest.mark.parametrize("key", sorted(CASES))
+@pytest.mark.parametrize("mode", ["off", "exact", "auto"])
+def test_f32_parity(key, mode):
+    w = CASES[key]()
+    d = w.to("cuda:0")
+    plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, cu_seqlens=w.cu_seqlens, dtype=torch.float32, mode=mode)
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device="cuda:0")
+    o, hT = gdn_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, plan=plan, workspace=ws)
+    assert gdn_get_device_status(ws)[0] == 0
+    f = util.to64
+    ro, rh = oracle.recurrence(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0), w.seq_offsets())
+    eo, eh = util.parity_f32(o, ro), util.parity_f32(hT, rh)
+    print(f"f32 {key}/{mode}: o {eo:.2e}  hT {eh:.2e}")
+    assert o.dtype == torch.float32
+    assert eo <= TOL_F32 and eh <= TOL_F32
