@@ -105,6 +105,18 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Named barrier that also ORs a predicate over the participating threads.
+__device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %3, 0;\n bar.red.or.pred po, %1, %2, pi;\n"
+      " selp.u32 %0, 1, 0, po;\n}"
+      : "=r"(r)
+      : "r"(id), "r"(count), "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
@@ -159,7 +171,7 @@ __device__ __forceinline__ bool want_out(const Chain& ch, int i) {
 // ----------------------------------------------------------------- producer
 // Loads each chunk's tiles (TMA) and gates (plain loads) into its stage.
 template <bool PREP>
-__device__ void producer_role(uint8_t* sm, Ctl* ctl, const Problem& p, const SegInfo& si, const Chain& ch,
+__device__ __noinline__ void producer_role(uint8_t* sm, Ctl* ctl, const Problem& p, const SegInfo& si, const Chain& ch,
                               const CUtensorMap* mq, const CUtensorMap* mk, const CUtensorMap* mv, int j) {
   const int lane = threadIdx.x & 31;
   const int n = ch.run_end - ch.run_begin;
@@ -201,7 +213,7 @@ __device__ void producer_role(uint8_t* sm, Ctl* ctl, const Problem& p, const Seg
 
 // ----------------------------------------------------------------- MMA issuer
 template <bool PREP>
-__device__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch, uint32_t tmem) {
+__device__ __noinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch, uint32_t tmem) {
   const int n = ch.run_end - ch.run_begin;
   const uint32_t sS = smem_u32(sm + kSmS), sVp = smem_u32(sm + kSmVp), sVd = smem_u32(sm + kSmVd);
   const uint32_t sWn = smem_u32(sm + kSmWn), sP = smem_u32(sm + kSmP), sA = smem_u32(sm + kSmA);
@@ -318,8 +330,11 @@ __device__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch, uint32_t tmem) 
 // Blocked inverse of the unit lower-triangular (I + L), L strictly lower in F.
 // A^T is written on and above the diagonal of F (block (j, i) holds A_ij^T);
 // the strict lower part of each diagonal block is cleared after phase 1, so
-// the products of phase 2 need no masks.
-__device__ void solve_unit_lower(float* F, float* T, int p) {
+// the products of phase 2 need no masks.  Threads 64-127, idle in phase 1,
+// run side() meanwhile; it returns false on a failed wait.  Returns false,
+// in every thread alike, if any thread's side() failed.
+template <class Side>
+__device__ __forceinline__ bool solve_unit_lower(float* F, float* T, int p, Side&& side) {
   // phase 1: diagonal 16x16 blocks, one column per thread; L rows are
   // broadcast float4 loads, four partial sums per row
   float x[16];
@@ -340,7 +355,8 @@ __device__ void solve_unit_lower(float* F, float* T, int p) {
       x[r] = (a[0] + a[1]) + (a[2] + a[3]);
     }
   }
-  named_bar_sync(2, kPrepThreads);
+  const bool side_ok = p < 64 ? true : side();
+  if (named_bar_or(2, kPrepThreads, !side_ok)) return false;
   if (p < 64) {  // row c of D_bb^T, zero below the block diagonal
     float* Dt = F + (16 * b + c) * kFStride + 16 * b;
 #pragma unroll
@@ -392,10 +408,11 @@ __device__ void solve_unit_lower(float* F, float* T, int p) {
     }
     named_bar_sync(2, kPrepThreads);
   }
+  return true;
 }
 
 template <bool PREP>
-__device__ void prep_role(uint8_t* sm, Ctl* ctl, const Chain& ch, uint32_t tmem) {
+__device__ __noinline__ void prep_role(uint8_t* sm, Ctl* ctl, const Chain& ch, uint32_t tmem) {
   const int p = threadIdx.x - kChainThreads;  // 0..127 = TMEM lane
   const int pw = p >> 5, lane = p & 31;
   const int n = ch.run_end - ch.run_begin;
@@ -440,49 +457,60 @@ __device__ void prep_role(uint8_t* sm, Ctl* ctl, const Chain& ch, uint32_t tmem)
     named_bar_sync(2, kPrepThreads);
     // exp(G_r - G_s) = exp(G_r) exp(-G_s) when no factor can overflow
     const bool factored = fabsf(sG[0]) < 80.f && fabsf(sG[63]) < 80.f;
-    // (c) L (rows 0-63 of D_kq) into F; P (rows 64-127) into its operand, once
-    //     the O2 of the previous chunk has consumed the old one
-    if (i >= 1 && !wait_bar(ctl, kO2Done, par ^ 1u)) break;
+    // (c) L (rows 0-63 of D_kq) into F
     if (!wait_bar(ctl, kKqDone, par)) break;
     tc_fence_after();
-    {
+    if (p < 64) {
       uint32_t rk[4][16];  // this lane's row of D_kq, loaded in one batch
 #pragma unroll
       for (int g4 = 0; g4 < 4; ++g4) tmem_ld16(tmem + lane_base + kTKQ + g4 * 16, rk[g4]);
       tmem_ld_wait(rk[0], rk[1]);
       tmem_ld_wait(rk[2], rk[3]);
-      if (p < 64) {
-        const int r = p;
-        const float br = sBeta[r], Gr = sG[r], brE = sBeta[r] * sEp[r];
-        float* Lr = F + r * kFStride;
-        if (factored) {
+      const int r = p;
+      const float br = sBeta[r], Gr = sG[r], brE = sBeta[r] * sEp[r];
+      float* Lr = F + r * kFStride;
+      if (factored) {
 #pragma unroll
-          for (int s4 = 0; s4 < 64; s4 += 4) {
-            const float4 em = *reinterpret_cast<const float4*>(sEm + s4);
-            const float* emv = &em.x;
-            float4 o4;
-            float* o = &o4.x;
+        for (int s4 = 0; s4 < 64; s4 += 4) {
+          const float4 em = *reinterpret_cast<const float4*>(sEm + s4);
+          const float* emv = &em.x;
+          float4 o4;
+          float* o = &o4.x;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int s = s4 + e;
-              o[e] = (s < r) ? brE * __uint_as_float(rk[s >> 4][s & 15]) * emv[e] : 0.f;
-            }
-            *reinterpret_cast<float4*>(Lr + s4) = o4;
+          for (int e = 0; e < 4; ++e) {
+            const int s = s4 + e;
+            o[e] = (s < r) ? brE * __uint_as_float(rk[s >> 4][s & 15]) * emv[e] : 0.f;
           }
-        } else {
-#pragma unroll
-          for (int s4 = 0; s4 < 64; s4 += 4) {
-            float4 o4;
-            float* o = &o4.x;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int s = s4 + e;
-              o[e] = (s < r) ? br * __uint_as_float(rk[s >> 4][s & 15]) * __expf(Gr - sG[s]) : 0.f;
-            }
-            *reinterpret_cast<float4*>(Lr + s4) = o4;
-          }
+          *reinterpret_cast<float4*>(Lr + s4) = o4;
         }
-      } else if (out) {
+      } else {
+#pragma unroll
+        for (int s4 = 0; s4 < 64; s4 += 4) {
+          float4 o4;
+          float* o = &o4.x;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int s = s4 + e;
+            o[e] = (s < r) ? br * __uint_as_float(rk[s >> 4][s & 15]) * __expf(Gr - sG[s]) : 0.f;
+          }
+          *reinterpret_cast<float4*>(Lr + s4) = o4;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&ctl->bar[kKqFree]);  // rows 0-63 of D_kq have been read
+    }
+    named_bar_sync(2, kPrepThreads);
+    // (d) A = (I + L)^{-1}.  Meanwhile threads 64-127 build P (rows 64-127 of
+    //     D_kq) into its operand, once the O2 of the previous chunk has
+    //     consumed the old one.
+    auto build_p = [&]() -> bool {
+      if (out) {
+        if (i >= 1 && !wait_bar(ctl, kO2Done, par ^ 1u)) return false;
+        uint32_t rk[4][16];
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) tmem_ld16(tmem + lane_base + kTKQ + g4 * 16, rk[g4]);
+        tmem_ld_wait(rk[0], rk[1]);
+        tmem_ld_wait(rk[2], rk[3]);
         const int r = p - 64;
         const float Gr = sG[r], Er = sEp[r];
 #pragma unroll
@@ -507,12 +535,11 @@ __device__ void prep_role(uint8_t* sm, Ctl* ctl, const Chain& ch, uint32_t tmem)
           store_f16x8(sP + sw128_offset(r, q), f, bad);
         }
       }
-    }
-    tc_fence_before();
-    mbar_arrive(&ctl->bar[kKqFree]);  // D_kq has been read
-    named_bar_sync(2, kPrepThreads);
-    // (d) A = (I + L)^{-1}; A operands: row s of A^T scaled by beta gamma / beta
-    solve_unit_lower(F, T, p);
+      tc_fence_before();
+      mbar_arrive(&ctl->bar[kKqFree]);  // rows 64-127 of D_kq have been read
+      return true;
+    };
+    if (!solve_unit_lower(F, T, p, build_p)) break;
     {
       const int s = p & 63, mat = p >> 6;
       const float sc = mat == 0 ? sBeta[s] * sGam[s] : sBeta[s];
@@ -532,9 +559,10 @@ __device__ void prep_role(uint8_t* sm, Ctl* ctl, const Chain& ch, uint32_t tmem)
     }
     fence_proxy_async_smem();
     mbar_arrive(&ctl->bar[kAReady]);
-    // (e) -W operand.  Waiting for the chain's V' hand-over of the previous
-    //     chunk both frees the old operand (its S W^T is complete) and keeps
-    //     this w_ready arrival from running two phases ahead of the chain.
+    // (e) -W operand (its proxy fence also covers the P stores).  Waiting
+    //     for the chain's V' hand-over of the previous chunk both frees the
+    //     old operand (its S W^T is complete) and keeps this w_ready arrival
+    //     from running two phases ahead of the chain.
     if (!wait_bar(ctl, kWuDone, par)) break;
     if (i >= 1 && !wait_bar(ctl, kVReady, par ^ 1u)) break;
     tc_fence_after();
@@ -561,10 +589,34 @@ __device__ void prep_role(uint8_t* sm, Ctl* ctl, const Chain& ch, uint32_t tmem)
 
 // ----------------------------------------------------------------- state (chain) warps
 template <bool PREP>
-__device__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p, const SegInfo& si, const Chain& ch,
-                           uint32_t tmem, float (&S)[64], int j) {
+__device__ __noinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p, const SegInfo& si, const Chain& ch,
+                           uint32_t tmem, int j, int chain) {
   const int tid = threadIdx.x, warp = tid >> 5;
   const int row = tid & 127, half = tid >> 7;
+  // The state lives only in these warps' registers (loading it outside this
+  // role would keep 64 registers busy in every other role too).
+  float S[64];
+  {
+    const size_t head_off = (size_t)(si.n * p.h_v + j) * kDim * kDim;
+    if (ch.init == kInitH0) {
+#pragma unroll
+      for (int e = 0; e < 64; ++e) S[e] = p.h0[head_off + (size_t)(half * 64 + e) * kDim + row];
+    } else if (ch.init == kInitStart) {
+      const float4* src = reinterpret_cast<const float4*>(
+          p.Sstart + ((size_t)(si.seg_base + si.s) * p.h_v + j) * kDim * kDim + (size_t)row * kDim + half * 64);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const float4 v4 = src[e];
+        S[4 * e] = v4.x;
+        S[4 * e + 1] = v4.y;
+        S[4 * e + 2] = v4.z;
+        S[4 * e + 3] = v4.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 64; ++e) S[e] = (ch.init == kInitIdentity && half * 64 + e == row) ? 1.f : 0.f;
+    }
+  }
   int n = ch.run_end - ch.run_begin;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   const uint32_t sS = smem_u32(sm + kSmS), sVp = smem_u32(sm + kSmVp), sVd = smem_u32(sm + kSmVd);
@@ -609,7 +661,8 @@ __device__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p, const SegInf
   store_state();
   fence_proxy_async_smem();
   mbar_arrive(&ctl->bar[kSReady]);
-  if (n > 0 && !convert_stage(0)) n = 0;
+  int done = 0;
+  if (n > 0 && !convert_stage(0)) n = -1;
   for (int i = 0; i < n; ++i) {
     if (i + 1 < n && !convert_stage(i + 1)) break;
     const uint32_t par = (uint32_t)(i & 1);
@@ -663,8 +716,7 @@ __device__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p, const SegInf
     store_state();
     if (!wait_bar(ctl, kO2Done, par)) break;
     tc_fence_after();
-    uint32_t ob[16];  // this thread's 32 outputs, bf16 pairs along the chunk rows
-    if (out) {
+    if (out) {  // stage this thread's 32 outputs (sO aliases V', which O2 has consumed)
 #pragma unroll
       for (int g2 = 0; g2 < 2; ++g2) {
         uint32_t yq[16], o2[16];
@@ -672,11 +724,10 @@ __device__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p, const SegInf
         tmem_ld16(tmem + lane_base + kTO2 + half * 32 + g2 * 16, o2);
         tmem_ld_wait(yq, o2);
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) {
+        for (int e = 0; e < 16; ++e) {
           const int c = half * 32 + g2 * 16 + e;
-          const float o0 = p.scale * fmaf(gts[64 + c], __uint_as_float(yq[e]), __uint_as_float(o2[e]));
-          const float o1 = p.scale * fmaf(gts[64 + c + 1], __uint_as_float(yq[e + 1]), __uint_as_float(o2[e + 1]));
-          ob[(g2 * 16 + e) / 2] = pack_bf16x2(o0, o1);
+          const float o = p.scale * fmaf(gts[64 + c], __uint_as_float(yq[e]), __uint_as_float(o2[e]));
+          sO[c * kDim + row] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
         }
       }
     }
@@ -684,12 +735,6 @@ __device__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p, const SegInf
     tc_fence_before();
     mbar_arrive(&ctl->bar[kSReady]);
     if (out) {
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int c = half * 32 + 2 * e;
-        sO[c * kDim + row] = (uint16_t)(ob[e] & 0xffffu);
-        sO[(c + 1) * kDim + row] = (uint16_t)(ob[e] >> 16);
-      }
       named_bar_sync(4, kChainThreads);
       __nv_bfloat16* outp = reinterpret_cast<__nv_bfloat16*>(p.out);
 #pragma unroll
@@ -704,8 +749,21 @@ __device__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p, const SegInf
       named_bar_sync(4, kChainThreads);
     }
     mbar_arrive(&ctl->bar[kChainDone0 + (i & 1)]);
+    done = i + 1;
   }
   if (bad) atomicExch(&ctl->range_bad, 1);
+  if (done < n || *reinterpret_cast<volatile int*>(&ctl->abort)) return;  // no results from an aborted chain
+  if (PREP) {
+    float* dst = (chain == 0 ? p.R : p.Sloc) + ((size_t)(si.seg_base + si.s) * p.h_v + j) * kDim * kDim +
+                 (size_t)row * kDim + half * 64;
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      reinterpret_cast<float4*>(dst)[e] = make_float4(S[4 * e], S[4 * e + 1], S[4 * e + 2], S[4 * e + 3]);
+  } else if (ch.write_final) {
+    float* dst = p.hT + (size_t)(si.n * p.h_v + j) * kDim * kDim;
+#pragma unroll
+    for (int e = 0; e < 64; ++e) dst[(size_t)(half * 64 + e) * kDim + row] = S[e];
+  }
 }
 
 template <bool PREP>
@@ -791,36 +849,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&ctl->tmem, 512);
     tmem_relinquish();
   }
-  float S[64];
-  if (warp < 8) {
-    const int row = tid & 127, half = tid >> 7;
-    const size_t head_off = (size_t)(si.n * p.h_v + j) * kDim * kDim;
-    if (ch.init == kInitH0) {
-#pragma unroll
-      for (int e = 0; e < 64; ++e) S[e] = p.h0[head_off + (size_t)(half * 64 + e) * kDim + row];
-    } else if (ch.init == kInitStart) {
-      const float4* src = reinterpret_cast<const float4*>(
-          p.Sstart + ((size_t)(si.seg_base + si.s) * p.h_v + j) * kDim * kDim + (size_t)row * kDim + half * 64);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float4 v4 = src[e];
-        S[4 * e] = v4.x;
-        S[4 * e + 1] = v4.y;
-        S[4 * e + 2] = v4.z;
-        S[4 * e + 3] = v4.w;
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 64; ++e) S[e] = (ch.init == kInitIdentity && half * 64 + e == row) ? 1.f : 0.f;
-    }
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
 
   if (warp < 8) {
-    chain_role<PREP>(sm, ctl, p, si, ch, tmem, S, j);
+    chain_role<PREP>(sm, ctl, p, si, ch, tmem, j, chain);
   } else if (warp < 12) {
     prep_role<PREP>(sm, ctl, ch, tmem);
   } else if (warp == kProducerWarp) {
@@ -838,22 +873,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t t0 = globaltimer_ns();
     while (globaltimer_ns() - t0 < 2000000ull) {
     }
-  } else {
-    if (tid == 0 && ctl->range_bad) report(p.status, kDevCheck, kDetFp16Range);
-    if (warp < 8) {
-      const int row = tid & 127, half = tid >> 7;
-      if (PREP) {
-        float* dst = (chain == 0 ? p.R : p.Sloc) + ((size_t)(si.seg_base + si.s) * p.h_v + j) * kDim * kDim +
-                     (size_t)row * kDim + half * 64;
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          reinterpret_cast<float4*>(dst)[e] = make_float4(S[4 * e], S[4 * e + 1], S[4 * e + 2], S[4 * e + 3]);
-      } else if (ch.write_final) {
-        float* dst = p.hT + (size_t)(si.n * p.h_v + j) * kDim * kDim;
-#pragma unroll
-        for (int e = 0; e < 64; ++e) dst[(size_t)(half * 64 + e) * kDim + row] = S[e];
-      }
-    }
+  } else if (tid == 0 && ctl->range_bad) {
+    report(p.status, kDevCheck, kDetFp16Range);
   }
   __syncthreads();
   if (warp == 0) {
