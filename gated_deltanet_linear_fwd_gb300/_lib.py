@@ -52,7 +52,9 @@ class gdn_cp_plan_t(ctypes.Structure):
                 ("n_seg_total", ctypes.c_int), ("max_seg_chunks", ctypes.c_int),
                 ("max_chunks", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
                 ("off_head", ctypes.c_size_t), ("off_seg_bound", ctypes.c_size_t),
-                ("off_R", ctypes.c_size_t), ("off_Sloc", ctypes.c_size_t), ("off_Sstart", ctypes.c_size_t)]
+                ("off_R", ctypes.c_size_t), ("off_Sloc", ctypes.c_size_t), ("off_Sstart", ctypes.c_size_t),
+                ("n_chunks_total", ctypes.c_int), ("off_chunk_map", ctypes.c_size_t),
+                ("off_wy", ctypes.c_size_t), ("off_kq16", ctypes.c_size_t)]
 
 
 _lock = threading.Lock()

@@ -72,6 +72,7 @@ gdn_status device_setup(int* dev_out) {
     g_encode = reinterpret_cast<EncodeTiledFn>(fn);
   }
   if ((e = scan_kernel_setup()) != cudaSuccess) return cuda_fail(e);
+  if ((e = wy_kernel_setup()) != cudaSuccess) return cuda_fail(e);
   if ((e = combine_kernel_setup()) != cudaSuccess) return cuda_fail(e);
   int sms = 0;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return cuda_fail(e);
@@ -231,10 +232,11 @@ gdn_status gdn_cp_plan(const gdn_dims* dims, const int32_t* cu, const gdn_cp_opt
   p.warmup_chunks = o.warmup_chunks;
   p.warmup_tol = o.warmup_tol;
   p.sm_count = o.sm_count;
-  int64_t n_seg_total = 0;
+  int64_t n_seg_total = 0, n_chunks_total = 0;
   for (int n = 0; n < dims->n_seqs; ++n) {
     const int64_t len = cu ? (int64_t)cu[n + 1] - cu[n] : dims->T;
     const int N = chunks_of(len);
+    n_chunks_total += N;
     const int ns = seg_count(N, p.lambda_q8, mode == GDN_CP_OFF);
     n_seg_total += ns;
     if (N > p.max_chunks) p.max_chunks = N;
@@ -244,8 +246,11 @@ gdn_status gdn_cp_plan(const gdn_dims* dims, const int32_t* cu, const gdn_cp_opt
     }
   }
   if (n_seg_total > 0x7fffffff) return GDN_ERR_INVALID_ARG;
+  if (n_chunks_total * std::max(dims->h_v, dims->h_qk) > 0x7fffffff) return GDN_ERR_INVALID_ARG;
   p.n_seg_total = (int)n_seg_total;
-  // workspace: status | head modes + bounds | segment bounds | R | S_loc | S_start
+  p.n_chunks_total = (int)n_chunks_total;
+  // workspace: status | head modes + bounds | segment bounds | R | S_loc | S_start |
+  //            chunk index | chunk records | fp16 K|Q tiles (the last three: bf16 path only)
   const size_t heads = (size_t)dims->n_seqs * dims->h_v;
   const size_t segheads = (size_t)n_seg_total * dims->h_v;
   size_t off = 256;
@@ -261,6 +266,14 @@ gdn_status gdn_cp_plan(const gdn_dims* dims, const int32_t* cu, const gdn_cp_opt
     off += segheads * mat;
     p.off_Sstart = off;
     off += segheads * mat;
+  }
+  if (dims->dtype == GDN_BF16) {
+    p.off_chunk_map = off;
+    off = align_up(off + ((size_t)dims->n_seqs + 1 + (size_t)n_chunks_total) * 4, 1024);
+    p.off_wy = off;
+    off += (size_t)n_chunks_total * dims->h_v * kRecBytes;
+    p.off_kq16 = off;
+    off += (size_t)n_chunks_total * dims->h_qk * kKqRecBytes;
   }
   p.workspace_bytes = off;
   *out = p;
@@ -329,6 +342,13 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
     p.Sloc = reinterpret_cast<float*>(ws + plan->off_Sloc);
     p.Sstart = reinterpret_cast<float*>(ws + plan->off_Sstart);
   }
+  p.n_chunks_total = plan->n_chunks_total;
+  if (dims->dtype == GDN_BF16) {
+    p.seq_chunk_base = reinterpret_cast<int32_t*>(ws + plan->off_chunk_map);
+    p.chunk_seq = p.seq_chunk_base + dims->n_seqs + 1;
+    p.wy = ws + plan->off_wy;
+    p.kq16 = ws + plan->off_kq16;
+  }
 
   cudaError_t e = cudaMemsetAsync(ws, 0, 256, cs);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -357,17 +377,21 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
 
   LaunchLog log{cs};
   if ((e = log.begin()) != cudaSuccess) return cuda_fail(e);
+  if ((e = launch_chunk_map(p, cs)) != cudaSuccess) return cuda_fail(e);
+  if ((e = log.after("chunk_map")) != cudaSuccess) return cuda_fail(e);
+  if (plan->mode == GDN_CP_WARMUP) {
+    if ((e = launch_gate_bound(p, cs)) != cudaSuccess) return cuda_fail(e);
+    if ((e = log.after("gate_bound")) != cudaSuccess) return cuda_fail(e);
+  }
+  if ((e = launch_wy(p, mq, mk, mv, cs)) != cudaSuccess) return cuda_fail(e);
+  if ((e = log.after("wy")) != cudaSuccess) return cuda_fail(e);
   if (plan->mode != GDN_CP_OFF) {
-    if (plan->mode == GDN_CP_WARMUP) {
-      if ((e = launch_gate_bound(p, cs)) != cudaSuccess) return cuda_fail(e);
-      if ((e = log.after("gate_bound")) != cudaSuccess) return cuda_fail(e);
-    }
-    if ((e = launch_scan_prep(p, mq, mk, mv, cs)) != cudaSuccess) return cuda_fail(e);
+    if ((e = launch_scan_prep(p, cs)) != cudaSuccess) return cuda_fail(e);
     if ((e = log.after("scan_prep")) != cudaSuccess) return cuda_fail(e);
     if ((e = launch_combine(p, cs)) != cudaSuccess) return cuda_fail(e);
     if ((e = log.after("combine")) != cudaSuccess) return cuda_fail(e);
   }
-  if ((e = launch_scan_out(p, mq, mk, mv, plan->n_seg_total, cs)) != cudaSuccess) return cuda_fail(e);
+  if ((e = launch_scan_out(p, plan->n_seg_total, cs)) != cudaSuccess) return cuda_fail(e);
   if ((e = log.after("scan_out")) != cudaSuccess) return cuda_fail(e);
   return GDN_OK;
 }

@@ -1,0 +1,99 @@
+// Device helpers shared by the tensor-core kernels: fp16 operand stores,
+// instruction descriptors for fp16 MMAs, named barriers, bulk copies and a
+// bounded mbarrier wait that gives up when another role has aborted.
+#pragma once
+#include <cstdint>
+
+#include "gdn_internal.cuh"
+#include "sm103_ptx.cuh"
+
+namespace gdn {
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 8 consecutive floats -> one 16-byte fp16 chunk; flags values outside the fp16 range.
+__device__ __forceinline__ void store_f16x8(uint32_t addr, const float* f, bool& bad) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) bad |= !(fabsf(f[e]) < 65504.f);
+  st_shared_v4(addr, pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
+               pack_f16x2(f[6], f[7]));
+}
+
+// Two packed bf16 -> two packed fp16 (round to nearest); flags out-of-range values.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool& bad) {
+  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+  bad |= !(fabsf(lo) < 65504.f) || !(fabsf(hi) < 65504.f);
+  return pack_f16x2(lo, hi);
+}
+
+// Instruction descriptor for kind::f16 with fp16 A/B and fp32 D.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named barrier that also ORs a predicate over the participating threads.
+__device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %3, 0;\n bar.red.or.pred po, %1, %2, pi;\n"
+      " selp.u32 %0, 1, 0, po;\n}"
+      : "=r"(r)
+      : "r"(id), "r"(count), "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
+}
+
+// ---- bulk (non-tensor) async copies ----
+// global -> shared, completing on an mbarrier (both addresses 16-byte aligned, bytes % 16 == 0).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+// shared -> global, tracked by this thread's bulk groups.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until every committed bulk store of this thread has read its source.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until every committed bulk store of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Bounded wait on an mbarrier phase; gives up (false) after the wall-clock
+// limit, recording `code` in *abort, or as soon as *abort is set by another
+// thread.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, int* abort, int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*reinterpret_cast<volatile int*>(abort)) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicCAS(abort, 0, code);
+      return false;
+    }
+  }
+}
+
+}  // namespace gdn

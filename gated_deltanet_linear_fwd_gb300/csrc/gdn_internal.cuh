@@ -27,6 +27,18 @@ constexpr int kModeWarmup = 2;
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per bounded wait
 
+// Chunk-local records written by the WY kernel and read by the scans: operand
+// tiles already in the 128-byte-swizzled shared-memory image the tcgen05 MMAs
+// read, so one bulk copy per tile brings them on chip.
+//   per (chunk, value head):
+constexpr uint32_t kRecWn = 0;        // fp16 -W, MN-major B tile: row d_k, 64 chunk rows (16 KB)
+constexpr uint32_t kRecU = 16384;     // fp16 U^T, K-major A tile: row d_v, 64 chunk rows (16 KB)
+constexpr uint32_t kRecP = 32768;     // fp16 P, K-major B tile: row r, columns s <= r (8 KB)
+constexpr uint32_t kRecGam = 40960;   // fp32 exp(G_r), then exp(G_63 - G_r) (2 x 64)
+constexpr uint32_t kRecBytes = 41472;
+//   per (chunk, query/key head):
+constexpr uint32_t kKqRecBytes = 32768;  // fp16 [K d0-63 | Q d0-63 | K d64-127 | Q d64-127], 8 KB each
+
 struct Problem {
   const void* q;
   const void* k;
@@ -57,6 +69,12 @@ struct Problem {
   float* R;                 // [n_seg_total, h_v, 128, 128] row-major (row = d_k in)
   float* Sloc;              // [n_seg_total, h_v, 128, 128] row = d_v
   float* Sstart;            // [n_seg_total, h_v, 128, 128] row = d_v
+  // chunk index: chunks are numbered over all sequences in order
+  int n_chunks_total;
+  int32_t* seq_chunk_base;  // [n_seqs + 1] global index of each sequence's first chunk
+  int32_t* chunk_seq;       // [n_chunks_total] sequence of each chunk
+  uint8_t* wy;              // [n_chunks_total, h_v] records of kRecBytes
+  uint8_t* kq16;            // [n_chunks_total, h_qk] records of kKqRecBytes
 };
 
 __device__ __forceinline__ void report(int* status, int code, int detail) {
@@ -163,14 +181,16 @@ __device__ inline int head_mode_of(const Problem& p, const SegInfo& si, int j) {
 }
 
 // ---- kernel launchers (defined in the .cu files) ----
+cudaError_t launch_chunk_map(const Problem& p, cudaStream_t st);
 cudaError_t launch_gate_bound(const Problem& p, cudaStream_t st);
-cudaError_t launch_scan_prep(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
-                             const CUtensorMap& mv, cudaStream_t st);
+cudaError_t launch_wy(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                      cudaStream_t st);
+cudaError_t launch_scan_prep(const Problem& p, cudaStream_t st);
 cudaError_t launch_combine(const Problem& p, cudaStream_t st);
-cudaError_t launch_scan_out(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk,
-                            const CUtensorMap& mv, int grid_x, cudaStream_t st);
+cudaError_t launch_scan_out(const Problem& p, int grid_x, cudaStream_t st);
 cudaError_t launch_recurrence_f32(const Problem& p, cudaStream_t st);
 cudaError_t scan_kernel_setup();
+cudaError_t wy_kernel_setup();
 cudaError_t combine_kernel_setup();
 
 }  // namespace gdn

@@ -1,0 +1,528 @@
+// The chunk-local WY/gate kernel (FlashQLA pages, section "Optimising GDN
+// chunked prefill": gate cumsum and the WY form of each 64-token chunk), and
+// the small chunk-index kernel it reads.
+//
+// Everything a chunk contributes that does not depend on the state is
+// computed here, for every (chunk, value head) at once, so that the scans
+// that carry the state from chunk to chunk do only the state-dependent
+// products.  Per chunk (G = inclusive cumsum of g, gamma = exp(G),
+// dec = exp(G_63 - G)):
+//   D    = [K;Q] K^T                       (bf16 MMA, exact inputs)
+//   L    = strict_lower(diag(beta) D_kk . exp(G_r - G_s))
+//   P    = lower(D_qk . exp(G_r - G_s))    (diagonal included)
+//   A    = (I + L)^{-1}                    (fp32, blocked)
+//   W^T  = K^T (A diag(beta gamma))^T,  U^T = V^T (A diag(beta))^T   (fp16 MMAs)
+// and writes -W, U^T, P and (gamma, dec) as one record per (chunk, value
+// head), plus the fp16 copy of K and Q per (chunk, query/key head), each
+// tile in the 128-byte-swizzled layout the scan's MMAs read.
+//
+// One CTA of 256 threads per (chunk, value head), two CTAs per SM.
+#include <cuda_bf16.h>
+
+#include "gdn_dev.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kWyThreads = 256;
+
+// ---- shared memory map (bytes from a 1024-byte aligned base) ----
+constexpr uint32_t kWyKQ = 0;         // [K d0-63 | Q d0-63 | K d64-127 | Q d64-127]: bf16 from TMA, then fp16
+constexpr uint32_t kWyV = 32768;      // [V d0-63 | V d64-127]: bf16, then fp16; finally the U^T tile
+constexpr uint32_t kWyA = 49152;      // solve scratch; then A diag(beta gamma) | A diag(beta); finally -W
+constexpr uint32_t kWyP = 65536;      // fp16 P
+constexpr uint32_t kWyF = 73728;      // fp32 [64][68]: L below the diagonal, A^T on and above it
+constexpr uint32_t kFStride = 68;
+constexpr uint32_t kWyGates = 91136;  // G | exp(G) | exp(G_63 - G) | beta | exp(-G), 64 floats each
+constexpr uint32_t kWyCtl = 92416;
+constexpr uint32_t kWySmemUse = 92480;
+constexpr uint32_t kWySmemAlloc = kWySmemUse + 1024;
+static_assert(2 * (kWySmemAlloc + 1024) <= 233472, "two CTAs per SM must fit");
+
+// ---- TMEM columns ----
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTD = 0;    // [K K^T ; Q K^T]   128 x 64
+constexpr uint32_t kTW = 64;   // W^T               128 x 64
+constexpr uint32_t kTU = 128;  // U^T               128 x 64
+
+struct WyCtl {
+  uint64_t full, kq, wu;
+  uint32_t tmem;
+  int abort;
+  float warp_total[2];
+};
+static_assert(sizeof(WyCtl) <= kWySmemUse - kWyCtl, "control block too large");
+
+// ---------------------------------------------------------------- solve
+// A = (I + L)^{-1} for the unit lower-triangular 64 x 64 matrix held
+// strictly below the diagonal of F.  A^T is written on and above the
+// diagonal (F[s][r] = A[r][s], r >= s).  Diagonal 16 x 16 blocks by forward
+// substitution (one column per thread), then two merge levels:
+//   A_10 = -D_1 L_10 D_0, A_32 = -D_3 L_32 D_2       (16 x 16 blocks)
+//   A_hl = -A_hh L_hl A_ll                           (32 x 32 blocks)
+// The strict lower parts of the diagonal 32 x 32 blocks are cleared once
+// consumed, so every product runs over full ranges without masks.  `side`
+// runs on threads 64-255 during the substitution.
+template <class Side>
+__device__ __forceinline__ void solve_unit_lower(float* F, float* scratch, int tid, Side&& side) {
+  // ---- diagonal blocks ----
+  {
+    float x[16];
+    const int b = tid >> 4, c = tid & 15;
+    if (tid < 64) {
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const float* Lr = F + (16 * b + r) * kFStride + 16 * b;
+        float a[4] = {(r == c) ? 1.f : 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int s4 = 0; s4 < r; s4 += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(Lr + s4);
+          const float* lv = &l4.x;
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (s4 + e < r) a[e] = fmaf(-lv[e], x[s4 + e], a[e]);
+        }
+        x[r] = (a[0] + a[1]) + (a[2] + a[3]);
+      }
+    } else {
+      side();
+    }
+    __syncthreads();
+    if (tid < 64) {  // row c of D_b^T; zero below the diagonal (L_bb has been consumed)
+      float* Dt = F + (16 * b + c) * kFStride + 16 * b;
+#pragma unroll
+      for (int r4 = 0; r4 < 16; r4 += 4)
+        *reinterpret_cast<float4*>(Dt + r4) =
+            make_float4(r4 + 0 >= c ? x[r4] : 0.f, r4 + 1 >= c ? x[r4 + 1] : 0.f,
+                        r4 + 2 >= c ? x[r4 + 2] : 0.f, r4 + 3 >= c ? x[r4 + 3] : 0.f);
+    }
+    __syncthreads();
+  }
+  // ---- level 1: T = L_{ib,jb} D_jb, then A_{ib,jb} = -D_ib T, for (ib, jb) = (1, 0), (3, 2) ----
+  {
+    const int mat = tid >> 7, idx = tid & 127;
+    const int r = idx >> 3, c0 = (idx & 7) * 2;
+    const int ib = 2 * mat + 1, jb = 2 * mat;
+    float* Ts = scratch + mat * 256;
+    {
+      const float* Lr = F + (16 * ib + r) * kFStride + 16 * jb;
+      const float* A0 = F + (16 * jb + c0) * kFStride + 16 * jb;  // D_jb column c0 (as a row of D^T)
+      float t0[2] = {0.f, 0.f}, t1[2] = {0.f, 0.f};
+#pragma unroll
+      for (int m = 0; m < 16; m += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(Lr + m);
+        const float4 a0 = *reinterpret_cast<const float4*>(A0 + m);
+        const float4 a1 = *reinterpret_cast<const float4*>(A0 + kFStride + m);
+        const int h = (m >> 2) & 1;
+        t0[h] = fmaf(l4.x, a0.x, fmaf(l4.y, a0.y, fmaf(l4.z, a0.z, fmaf(l4.w, a0.w, t0[h]))));
+        t1[h] = fmaf(l4.x, a1.x, fmaf(l4.y, a1.y, fmaf(l4.z, a1.z, fmaf(l4.w, a1.w, t1[h]))));
+      }
+      *reinterpret_cast<float2*>(Ts + r * 16 + c0) = make_float2(t0[0] + t0[1], t1[0] + t1[1]);
+    }
+    __syncthreads();
+    {
+      float a0[2] = {0.f, 0.f}, a1[2] = {0.f, 0.f};
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        const float d = F[(16 * ib + m) * kFStride + 16 * ib + r];  // D_ib[r][m], zero for m > r
+        const float2 t = *reinterpret_cast<const float2*>(Ts + m * 16 + c0);
+        a0[m & 1] = fmaf(d, t.x, a0[m & 1]);
+        a1[m & 1] = fmaf(d, t.y, a1[m & 1]);
+      }
+      F[(16 * jb + c0) * kFStride + 16 * ib + r] = -(a0[0] + a0[1]);  // A_{ib,jb}^T
+      F[(16 * jb + c0 + 1) * kFStride + 16 * ib + r] = -(a1[0] + a1[1]);
+      // L_{ib,jb} has been consumed: clear it
+      *reinterpret_cast<float2*>(F + (16 * ib + r) * kFStride + 16 * jb + c0) = make_float2(0.f, 0.f);
+    }
+    __syncthreads();
+  }
+  // ---- level 2: T = L_hl A_ll (32 x 32), then A_hl = -A_hh T ----
+  {
+    const int r0 = (tid >> 4) * 2, c0 = (tid & 15) * 2;
+    float* Tb = scratch;  // [32][32]
+    {
+      const float* L0 = F + (32 + r0) * kFStride;  // L[32 + r0][0..31]
+      const float* L1 = L0 + kFStride;
+      const float* A0 = F + c0 * kFStride;         // A_ll[.][c0] as row c0 of A^T
+      const float* A1 = A0 + kFStride;
+      float t00 = 0.f, t01 = 0.f, t10 = 0.f, t11 = 0.f;
+#pragma unroll
+      for (int m = 0; m < 32; m += 4) {
+        const float4 l0 = *reinterpret_cast<const float4*>(L0 + m);
+        const float4 l1 = *reinterpret_cast<const float4*>(L1 + m);
+        const float4 a0 = *reinterpret_cast<const float4*>(A0 + m);
+        const float4 a1 = *reinterpret_cast<const float4*>(A1 + m);
+        t00 = fmaf(l0.x, a0.x, fmaf(l0.y, a0.y, fmaf(l0.z, a0.z, fmaf(l0.w, a0.w, t00))));
+        t01 = fmaf(l0.x, a1.x, fmaf(l0.y, a1.y, fmaf(l0.z, a1.z, fmaf(l0.w, a1.w, t01))));
+        t10 = fmaf(l1.x, a0.x, fmaf(l1.y, a0.y, fmaf(l1.z, a0.z, fmaf(l1.w, a0.w, t10))));
+        t11 = fmaf(l1.x, a1.x, fmaf(l1.y, a1.y, fmaf(l1.z, a1.z, fmaf(l1.w, a1.w, t11))));
+      }
+      *reinterpret_cast<float2*>(Tb + r0 * 32 + c0) = make_float2(t00, t01);
+      *reinterpret_cast<float2*>(Tb + (r0 + 1) * 32 + c0) = make_float2(t10, t11);
+    }
+    __syncthreads();
+    {
+      float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
+      const int m_end = r0 + 2;  // A_hh[r][m] = 0 for m > r
+#pragma unroll 4
+      for (int m = 0; m < m_end; ++m) {
+        const float2 a = *reinterpret_cast<const float2*>(F + (32 + m) * kFStride + 32 + r0);  // A_hh[r0..r0+1][m]
+        const float2 t = *reinterpret_cast<const float2*>(Tb + m * 32 + c0);
+        x00 = fmaf(a.x, t.x, x00);
+        x01 = fmaf(a.x, t.y, x01);
+        x10 = fmaf(a.y, t.x, x10);
+        x11 = fmaf(a.y, t.y, x11);
+      }
+      *reinterpret_cast<float2*>(F + c0 * kFStride + 32 + r0) = make_float2(-x00, -x10);
+      *reinterpret_cast<float2*>(F + (c0 + 1) * kFStride + 32 + r0) = make_float2(-x01, -x11);
+    }
+    __syncthreads();
+  }
+}
+
+__device__ __forceinline__ void seq_bounds(const Problem& p, int n, int64_t& bos, int64_t& eos) {
+  if (p.cu) {
+    bos = p.cu[n];
+    eos = p.cu[n + 1];
+  } else {
+    bos = (int64_t)n * p.T_row;
+    eos = bos + p.T_row;
+  }
+}
+
+// Returns false (in every thread alike) when a wait gave up.
+__device__ __noinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& p, const CUtensorMap* mq,
+                                     const CUtensorMap* mk, const CUtensorMap* mv, uint32_t tmem, bool& bad) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gc = (int)(blockIdx.x / (unsigned)p.h_v), j = (int)(blockIdx.x % (unsigned)p.h_v);
+  const int n = p.chunk_seq[gc];
+  if (n < 0 || n >= p.n_seqs) {  // the chunk index disagrees with the plan
+    if (tid == 0) report(p.status, kDevCheck, kDetSegMismatch);
+    return false;
+  }
+  const int c = gc - p.seq_chunk_base[n];
+  int64_t bos, eos;
+  seq_bounds(p, n, bos, eos);
+  const int64_t t0 = bos + (int64_t)c * kChunk;
+  if (c < 0 || t0 >= eos) {
+    if (tid == 0) report(p.status, kDevCheck, kDetSegMismatch);
+    return false;
+  }
+  const int cv = (int)min((int64_t)kChunk, eos - t0);
+  const int iq = (int)(((int64_t)j * p.h_qk) / p.h_v);
+  const bool first_of_group = j == (int)(((int64_t)iq * p.h_v + p.h_qk - 1) / p.h_qk);
+  float* gts = reinterpret_cast<float*>(sm + kWyGates);
+  float* sG = gts;
+  float* sGam = gts + 64;
+  float* sDec = gts + 128;
+  float* sBeta = gts + 192;
+  float* sEm = gts + 256;
+  float* F = reinterpret_cast<float*>(sm + kWyF);
+  float* scratch = reinterpret_cast<float*>(sm + kWyA);
+  const uint32_t sKQ = smem_u32(sm + kWyKQ), sV = smem_u32(sm + kWyV), sA = smem_u32(sm + kWyA);
+  const uint32_t sP = smem_u32(sm + kWyP);
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+
+  // ---- loads; D = [K;Q] K^T as soon as they land ----
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&ctl->full, 49152u);
+    tma_load_3d(sm + kWyKQ, mk, &ctl->full, 0, iq, (int)t0);
+    tma_load_3d(sm + kWyKQ + 16384, mk, &ctl->full, 64, iq, (int)t0);
+    tma_load_3d(sm + kWyKQ + 8192, mq, &ctl->full, 0, iq, (int)t0);
+    tma_load_3d(sm + kWyKQ + 24576, mq, &ctl->full, 64, iq, (int)t0);
+    tma_load_3d(sm + kWyV, mv, &ctl->full, 0, j, (int)t0);
+    tma_load_3d(sm + kWyV + 8192, mv, &ctl->full, 64, j, (int)t0);
+  }
+  if (warp == 2 || warp == 3) {  // gate cumsum; rows past the sequence end act as g = beta = 0
+    const int r = tid - 64;
+    const bool ok = r < cv;
+    float x = ok ? p.g[(size_t)(t0 + r) * p.h_v + j] : 0.f;
+    const float b = ok ? p.beta[(size_t)(t0 + r) * p.h_v + j] : 0.f;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x += y;
+    }
+    if (lane == 31) ctl->warp_total[warp - 2] = x;
+    named_bar_sync(1, 64);
+    if (warp == 3) x += ctl->warp_total[0];
+    sG[r] = x;
+    sGam[r] = __expf(x);
+    sBeta[r] = b;
+    sEm[r] = __expf(-x);
+    named_bar_sync(1, 64);
+    sDec[r] = __expf(sG[63] - x);
+  }
+  if (tid == 32) {
+    if (wait_phase(&ctl->full, 0, &ctl->abort, 100)) {
+      tc_fence_after();
+      const uint32_t id = idesc_bf16_f32(128, 64, false, false);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t off = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+        mma_bf16(tmem + kTD, sdesc_sw128(sKQ + off, 16, 1024), sdesc_sw128(sKQ + off, 16, 1024), id, ks > 0);
+      }
+      mma_commit(&ctl->kq);
+    }
+  }
+  bool ok = wait_phase(&ctl->kq, 0, &ctl->abort, 101);
+  if (__syncthreads_or(!ok)) return false;
+  tc_fence_after();
+
+  // ---- L (TMEM lanes 0-63) into F and P (lanes 64-127) into its operand ----
+  {
+    const bool factored = fabsf(sG[0]) < 80.f && fabsf(sG[63]) < 80.f;  // exp(G_r) exp(-G_s) cannot overflow
+    const int R = (warp & 3) * 32 + lane, ch = warp >> 2;                 // columns 32 ch .. 32 ch + 31
+    uint32_t rk[2][16];
+    tmem_ld16(tmem + lane_base + kTD + ch * 32, rk[0]);
+    tmem_ld16(tmem + lane_base + kTD + ch * 32 + 16, rk[1]);
+    tmem_ld_wait(rk[0], rk[1]);
+    if (R < 64) {
+      const int r = R;
+      const float br = sBeta[r], Gr = sG[r], brE = sBeta[r] * sGam[r];
+      float* Lr = F + r * kFStride + ch * 32;
+#pragma unroll
+      for (int s4 = 0; s4 < 32; s4 += 4) {
+        float4 o4;
+        float* o = &o4.x;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int sl = s4 + e, s = ch * 32 + sl;
+          const float d = __uint_as_float(rk[sl >> 4][sl & 15]);
+          o[e] = (s < r) ? (factored ? brE * d * sEm[s] : br * d * __expf(Gr - sG[s])) : 0.f;
+        }
+        *reinterpret_cast<float4*>(Lr + s4) = o4;
+      }
+    } else {
+      const int r = R - 64;
+      const float Er = sGam[r], Gr = sG[r];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int sl = 8 * q + e, s = ch * 32 + sl;
+          const float d = __uint_as_float(rk[sl >> 4][sl & 15]);
+          f[e] = (s <= r) ? (factored ? d * Er * sEm[s] : d * __expf(Gr - sG[s])) : 0.f;
+        }
+        store_f16x8(sP + sw128_offset(r, ch * 4 + q), f, bad);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+
+  // ---- A = (I + L)^{-1}; meanwhile threads 64-255 convert K, Q, V to fp16 in place ----
+  solve_unit_lower(F, scratch, tid, [&]() {
+    uint4* b4 = reinterpret_cast<uint4*>(sm + kWyKQ);  // K|Q|K|Q then V: 3072 16-byte vectors
+#pragma unroll 4
+    for (int v = tid - 64; v < 3072; v += kWyThreads - 64) {
+      const uint4 u = b4[v];
+      b4[v] = make_uint4(bf16x2_to_f16x2(u.x, bad), bf16x2_to_f16x2(u.y, bad), bf16x2_to_f16x2(u.z, bad),
+                         bf16x2_to_f16x2(u.w, bad));
+    }
+  });
+
+  // ---- A operands: row s of A^T scaled by beta gamma (for W) / beta (for U) ----
+  {
+    const int row = tid >> 1, hs = tid & 1;
+    const int s = row & 63, mat = row >> 6;
+    const float sc = mat == 0 ? sBeta[s] * sGam[s] : sBeta[s];
+    const float* At = F + s * kFStride;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int qq = hs * 4 + q;
+      const float4 lo4 = *reinterpret_cast<const float4*>(At + 8 * qq);
+      const float4 hi4 = *reinterpret_cast<const float4*>(At + 8 * qq + 4);
+      const float v[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
+      float f[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = (8 * qq + e >= s) ? v[e] * sc : 0.f;
+      store_f16x8(sA + mat * 8192 + sw128_offset(s, qq), f, bad);
+    }
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  uint8_t* rec = p.wy + ((size_t)gc * p.h_v + j) * kRecBytes;
+  if (tid == 32) {  // W^T = K^T (A diag(beta gamma))^T, U^T = V^T (A diag(beta))^T
+    tc_fence_after();
+    const uint32_t id_mn = idesc_f16(128, 64, true, true);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      mma_bf16(tmem + kTW, sdesc_sw128(sKQ + ks * 2048, 16384, 1024), sdesc_sw128(sA + ks * 2048, 8192, 1024),
+               id_mn, ks > 0);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      mma_bf16(tmem + kTU, sdesc_sw128(sV + ks * 2048, 8192, 1024),
+               sdesc_sw128(sA + 8192 + ks * 2048, 8192, 1024), id_mn, ks > 0);
+    mma_commit(&ctl->wu);
+  } else if (tid == 64) {  // the parts of the record that are final already
+    bulk_store(rec + kRecP, sm + kWyP, 8192);
+    bulk_store(rec + kRecGam, sGam, 512);  // exp(G) then exp(G_63 - G)
+    if (first_of_group) bulk_store(p.kq16 + ((size_t)gc * p.h_qk + iq) * kKqRecBytes, sm + kWyKQ, kKqRecBytes);
+    bulk_commit();
+  }
+  ok = wait_phase(&ctl->wu, 0, &ctl->abort, 102);
+  if (__syncthreads_or(!ok)) return false;
+  tc_fence_after();
+
+  // ---- -W and U^T tiles (over the A operands and V, which the MMAs have consumed) ----
+  {
+    const int d = (warp & 3) * 32 + lane, ch = warp >> 2;
+    uint32_t ra[16], rb[16];
+    tmem_ld16(tmem + lane_base + kTW + ch * 32, ra);
+    tmem_ld16(tmem + lane_base + kTW + ch * 32 + 16, rb);
+    tmem_ld_wait(ra, rb);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float f[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = -__uint_as_float(q < 2 ? ra[8 * q + e] : rb[8 * (q - 2) + e]);
+      store_f16x8(sA + sw128_offset(d, ch * 4 + q), f, bad);
+    }
+    tmem_ld16(tmem + lane_base + kTU + ch * 32, ra);
+    tmem_ld16(tmem + lane_base + kTU + ch * 32 + 16, rb);
+    tmem_ld_wait(ra, rb);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float f[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(q < 2 ? ra[8 * q + e] : rb[8 * (q - 2) + e]);
+      store_f16x8(sV + sw128_offset(d, ch * 4 + q), f, bad);
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 64) {
+    bulk_store(rec + kRecWn, sm + kWyA, 16384);
+    bulk_store(rec + kRecU, sm + kWyV, 16384);
+    bulk_commit();
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(kWyThreads, 2)
+    wy_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+              const __grid_constant__ CUtensorMap mv, const Problem p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  WyCtl* ctl = reinterpret_cast<WyCtl*>(sm + kWyCtl);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (tid == 0) {
+    mbar_init(&ctl->full, 1);
+    mbar_init(&ctl->kq, 1);
+    mbar_init(&ctl->wu, 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&mk);
+    tma_prefetch_desc(&mq);
+    tma_prefetch_desc(&mv);
+  }
+  if (warp == 0) {
+    tmem_alloc(&ctl->tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem;
+  bool bad = false;
+  wy_body(sm, ctl, p, &mq, &mk, &mv, tmem, bad);
+  if (tid == 64) bulk_wait_all();  // the record's stores have landed (and read shared memory)
+  tc_fence_before();
+  __syncthreads();
+  if (ctl->abort) {
+    if (tid == 0) report(p.status, kDevTimeout, ctl->abort);
+    // let copies and MMAs already in flight land before the memory is released
+    const uint64_t t_start = globaltimer_ns();
+    while (globaltimer_ns() - t_start < 2000000ull) {
+    }
+    __syncthreads();
+  }
+  if (bad) report(p.status, kDevCheck, kDetFp16Range);
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- chunk index
+// seq_chunk_base[n] = chunks of sequences 0..n-1; chunk_seq[c] = the
+// sequence of global chunk c.  One CTA.
+constexpr int kMapThreads = 1024;
+
+__global__ void __launch_bounds__(kMapThreads) chunk_map_kernel(const Problem p) {
+  __shared__ int warp_sum[32];
+  __shared__ int carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int n0 = 0; n0 < p.n_seqs; n0 += kMapThreads) {
+    const int n = n0 + tid;
+    int cnt = 0;
+    if (n < p.n_seqs) {
+      int64_t bos, eos;
+      seq_bounds(p, n, bos, eos);
+      cnt = chunks_of(eos - bos);
+    }
+    int x = cnt;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x += y;
+    }
+    if (lane == 31) warp_sum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_sum[lane];
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, d);
+        if (lane >= d) w += y;
+      }
+      warp_sum[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const int incl = x + (warp > 0 ? warp_sum[warp - 1] : 0) + carry;
+    if (n < p.n_seqs) p.seq_chunk_base[n] = incl - cnt;
+    __syncthreads();
+    if (tid == kMapThreads - 1) carry = incl;
+    __syncthreads();
+  }
+  if (tid == 0) p.seq_chunk_base[p.n_seqs] = carry;
+  const int total = carry;
+  if (tid == 0 && total != p.n_chunks_total) report(p.status, kDevCheck, kDetSegMismatch);
+  __syncthreads();
+  for (int gc = tid; gc < total && gc < p.n_chunks_total; gc += kMapThreads) {
+    int lo = 0, hi = p.n_seqs - 1;  // last n with base[n] <= gc
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.seq_chunk_base[mid] <= gc) lo = mid;
+      else hi = mid - 1;
+    }
+    p.chunk_seq[gc] = lo;
+  }
+}
+
+}  // namespace
+
+cudaError_t wy_kernel_setup() {
+  return cudaFuncSetAttribute(wy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWySmemAlloc);
+}
+
+cudaError_t launch_chunk_map(const Problem& p, cudaStream_t st) {
+  chunk_map_kernel<<<1, kMapThreads, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wy(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                      cudaStream_t st) {
+  if (p.n_chunks_total == 0) return cudaSuccess;
+  const unsigned grid = (unsigned)p.n_chunks_total * (unsigned)p.h_v;
+  wy_kernel<<<grid, kWyThreads, kWySmemAlloc, st>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -119,6 +119,10 @@ typedef struct gdn_cp_plan_t {
   size_t off_head;      /* byte offsets of the workspace sections */
   size_t off_seg_bound;
   size_t off_R, off_Sloc, off_Sstart;
+  int n_chunks_total;   /* 64-token chunks summed over sequences */
+  size_t off_chunk_map; /* chunk index: first chunk of each sequence, sequence of each chunk */
+  size_t off_wy;        /* chunk-local records (-W, U, P, gates), 41472 bytes per (chunk, value head) */
+  size_t off_kq16;      /* fp16 K|Q tiles, 32768 bytes per (chunk, query/key head) */
 } gdn_cp_plan_t;
 
 /*

@@ -89,9 +89,15 @@ def test_plan_workspace_layout(lib):
     mat = 128 * 128 * 4
     assert p.off_head % 256 == 0 and p.off_seg_bound % 256 == 0
     assert p.off_Sloc - p.off_R == 23 * 8 * mat and p.off_Sstart - p.off_Sloc == 23 * 8 * mat
-    assert p.workspace_bytes == p.off_Sstart + 23 * 8 * mat
+    # chunk index (n_seqs + 1 + chunks int32), then the chunk records and fp16 K|Q tiles
+    assert p.n_chunks_total == 512
+    assert p.off_chunk_map == p.off_Sstart + 23 * 8 * mat
+    assert p.off_wy % 1024 == 0 and p.off_wy >= p.off_chunk_map + (1 + 1 + 512) * 4
+    assert p.off_kq16 == p.off_wy + 512 * 8 * 41472
+    assert p.workspace_bytes == p.off_kq16 + 512 * 2 * 32768
     st, p0 = plan(lib, 32768, h_v=8, mode=0)
-    assert p0.workspace_bytes < 4096
+    assert p0.off_R == p0.off_Sloc == p0.off_Sstart == 0  # no context parallelism: no segment states
+    assert p0.workspace_bytes == p0.off_kq16 + 512 * 2 * 32768
 
 
 @pytest.mark.parametrize("kw,expect", [
@@ -112,24 +118,25 @@ def test_chunk_fwd_rejects_before_device_work(lib):
     dims = L.gdn_dims(1, 128, 1, 1, 128, 128, 1, 0.0, 0)
     A = ctypes.c_void_p(0x100000)  # never dereferenced: every case fails a host check first
     U = ctypes.c_void_p(0x100008)  # not 16-byte aligned
+    ws = p.workspace_bytes
     f = lib.gdn_chunk_fwd
     # null plan / dims
-    assert f(A, A, A, A, A, None, None, A, None, None, ctypes.byref(p), A, 4096, None) == 1
-    assert f(A, A, A, A, A, None, None, A, None, ctypes.byref(dims), None, A, 4096, None) == 1
+    assert f(A, A, A, A, A, None, None, A, None, None, ctypes.byref(p), A, ws, None) == 1
+    assert f(A, A, A, A, A, None, None, A, None, ctypes.byref(dims), None, A, ws, None) == 1
     # workspace missing or too small
-    assert f(A, A, A, A, A, None, None, A, None, ctypes.byref(dims), ctypes.byref(p), None, 4096, None) == 6
+    assert f(A, A, A, A, A, None, None, A, None, ctypes.byref(dims), ctypes.byref(p), None, ws, None) == 6
     assert f(A, A, A, A, A, None, None, A, None, ctypes.byref(dims), ctypes.byref(p), A, 16, None) == 6
     # misaligned
-    assert f(U, A, A, A, A, None, None, A, None, ctypes.byref(dims), ctypes.byref(p), A, 4096, None) == 3
-    assert f(A, A, A, A, A, None, None, A, None, ctypes.byref(dims), ctypes.byref(p), U, 4096, None) == 3
+    assert f(U, A, A, A, A, None, None, A, None, ctypes.byref(dims), ctypes.byref(p), A, ws, None) == 3
+    assert f(A, A, A, A, A, None, None, A, None, ctypes.byref(dims), ctypes.byref(p), U, ws, None) == 3
     # null input
-    assert f(None, A, A, A, A, None, None, A, None, ctypes.byref(dims), ctypes.byref(p), A, 4096, None) == 1
+    assert f(None, A, A, A, A, None, None, A, None, ctypes.byref(dims), ctypes.byref(p), A, ws, None) == 1
     # dims disagree with the plan
     dims2 = L.gdn_dims(1, 128, 1, 2, 128, 128, 1, 0.0, 0)
-    assert f(A, A, A, A, A, None, None, A, None, ctypes.byref(dims2), ctypes.byref(p), A, 4096, None) == 1
+    assert f(A, A, A, A, A, None, None, A, None, ctypes.byref(dims2), ctypes.byref(p), A, ws, None) == 1
     # unsupported head dim
     dims3 = L.gdn_dims(1, 128, 1, 1, 64, 128, 1, 0.0, 0)
-    assert f(A, A, A, A, A, None, None, A, None, ctypes.byref(dims3), ctypes.byref(p), A, 4096, None) == 2
+    assert f(A, A, A, A, A, None, None, A, None, ctypes.byref(dims3), ctypes.byref(p), A, ws, None) == 2
 
 
 def test_binding_fails_loudly_without_library(tmp_path):
