@@ -7,8 +7,10 @@
 // so the start states follow by a serial scan over the segments of a
 // sequence:  S_start(0) = h0^T,  S_start(s+1) = S_start(s) R_s + S_loc,s.
 // Rows of S are independent, so each CTA owns 8 rows of one (sequence, head)
-// and streams R_s through shared memory (double-buffered cp.async) while it
-// does the fp32 vector-matrix products.  The CTA of row block 0 also
+// and streams R_s and its 8 rows of S_loc,s through shared memory (cp.async,
+// one segment ahead) while it does the fp32 products.  Each warp takes a
+// 16-row slice of R for all 8 rows (so R is read from shared memory once per
+// segment), and the 8 partial sums are added in a second pass.  The CTA of row block 0 also
 // records the mode the (sequence, head) takes and its warmup bound.
 #include "gdn_internal.cuh"
 
@@ -16,7 +18,8 @@ namespace gdn {
 namespace {
 
 constexpr int kRows = 8;  // state rows per CTA
-constexpr int kCombineSmem = 2 * kDim * kDim * 4 + kRows * kDim * 4;
+constexpr int kSlices = 8;  // k slices of 16 (one per warp)
+constexpr int kCombineSmem = 2 * kDim * kDim * 4 + 2 * kRows * kDim * 4 + kRows * kDim * 4 + kSlices * kRows * kDim * 4;
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)),
@@ -32,7 +35,9 @@ __device__ __forceinline__ void cp_async_wait() {
 __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
   extern __shared__ float4 csm4[];
   float* sR = reinterpret_cast<float*>(csm4);  // [2][128*128]
-  float* sX = sR + 2 * kDim * kDim;            // [kRows][128]
+  float* sL = sR + 2 * kDim * kDim;            // [2][kRows][128]: this block's rows of S_loc
+  float* sX = sL + 2 * kRows * kDim;           // [kRows][128]
+  float* sP = sX + kRows * kDim;               // [kSlices][kRows][128] partial sums
   __shared__ SegInfo s_seq;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int n = blockIdx.x, j = blockIdx.y, r0 = blockIdx.z * kRows;
@@ -59,41 +64,70 @@ __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
     const int r = i / kDim, c = i % kDim;
     sX[i] = p.h0 ? p.h0[(size_t)(n * p.h_v + j) * mat + (size_t)c * kDim + (r0 + r)] : 0.f;
   }
-  auto prefetch = [&](int s, int buf) {
-    const float* src = p.R + ((size_t)(si.seg_base + s) * p.h_v + j) * mat;
-    float* dst = sR + buf * mat;
-    for (int i = tid; i < kDim * kDim / 4; i += 256) cp_async16(dst + 4 * i, src + 4 * i);
+  // segment s's inputs into buffer s & 1: R_s (when its product is taken) and S_loc,s rows
+  const bool skip_first = p.h0 == nullptr;  // R_0 is not produced for a zero start: skip its product
+  const int first_product = skip_first ? 1 : 0;
+  const int last = si.n_seg - 2;  // produce S_start(1 .. n_seg-1)
+  auto prefetch = [&](int s) {
+    const int buf = s & 1;
+    if (s >= first_product) {
+      const float* src = p.R + ((size_t)(si.seg_base + s) * p.h_v + j) * mat;
+      float* dst = sR + buf * mat;
+      for (int i = tid; i < kDim * kDim / 4; i += 256) cp_async16(dst + 4 * i, src + 4 * i);
+    }
+    const float* lsrc = p.Sloc + ((size_t)(si.seg_base + s) * p.h_v + j) * mat + (size_t)r0 * kDim;
+    cp_async16(sL + buf * kRows * kDim + 4 * tid, lsrc + 4 * tid);  // kRows * kDim / 4 == 256 vectors
     cp_async_commit();
   };
-  // R_0 is not produced when the start state is zero (no h0): skip its product.
-  const bool skip_first = p.h0 == nullptr;
-  const int last = si.n_seg - 2;  // produce S_start(1 .. n_seg-1)
-  int first_product = skip_first ? 1 : 0;
-  if (first_product <= last) prefetch(first_product, first_product & 1);
-  __syncthreads();
+  prefetch(0);
   for (int s = 0; s <= last; ++s) {
     const bool product = s >= first_product;
-    if (product && s + 1 <= last) {
-      prefetch(s + 1, (s + 1) & 1);
+    if (s + 1 <= last) {
+      prefetch(s + 1);
       cp_async_wait<1>();
-    } else if (product) {
+    } else {
       cp_async_wait<0>();
     }
     __syncthreads();
-    const float4 l4 = *reinterpret_cast<const float4*>(
-        p.Sloc + ((size_t)(si.seg_base + s) * p.h_v + j) * mat + (size_t)(r0 + rr) * kDim + c4);
+    const float4 l4 = *reinterpret_cast<const float4*>(sL + (s & 1) * kRows * kDim + rr * kDim + c4);
     float a0 = l4.x, a1 = l4.y, a2 = l4.z, a3 = l4.w;
     if (product) {
-      const float* Rb = sR + (s & 1) * mat;
-      const float* xr = sX + rr * kDim;
-#pragma unroll 8
-      for (int k = 0; k < kDim; ++k) {
-        const float x = xr[k];
-        const float4 r4 = *reinterpret_cast<const float4*>(Rb + k * kDim + c4);
-        a0 = fmaf(x, r4.x, a0);
-        a1 = fmaf(x, r4.y, a1);
-        a2 = fmaf(x, r4.z, a2);
-        a3 = fmaf(x, r4.w, a3);
+      // partial products over k = 16 ks .. 16 ks + 15 for all rows, columns c4 .. c4 + 3
+      const int ks = tid >> 5;
+      const float* Rb = sR + (s & 1) * mat + (size_t)(16 * ks) * kDim + c4;
+      float acc[kRows][4];
+#pragma unroll
+      for (int r = 0; r < kRows; ++r) acc[r][0] = acc[r][1] = acc[r][2] = acc[r][3] = 0.f;
+#pragma unroll
+      for (int k4 = 0; k4 < 16; k4 += 4) {
+        float4 x4[kRows];
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) x4[r] = *reinterpret_cast<const float4*>(sX + r * kDim + 16 * ks + k4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float4 r4 = *reinterpret_cast<const float4*>(Rb + (k4 + e) * kDim);
+#pragma unroll
+          for (int r = 0; r < kRows; ++r) {
+            const float x = (&x4[r].x)[e];
+            acc[r][0] = fmaf(x, r4.x, acc[r][0]);
+            acc[r][1] = fmaf(x, r4.y, acc[r][1]);
+            acc[r][2] = fmaf(x, r4.z, acc[r][2]);
+            acc[r][3] = fmaf(x, r4.w, acc[r][3]);
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kRows; ++r)
+        *reinterpret_cast<float4*>(sP + (ks * kRows + r) * kDim + c4) =
+            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+      __syncthreads();
+#pragma unroll
+      for (int q = 0; q < kSlices; ++q) {
+        const float4 t4 = *reinterpret_cast<const float4*>(sP + (q * kRows + rr) * kDim + c4);
+        a0 += t4.x;
+        a1 += t4.y;
+        a2 += t4.z;
+        a3 += t4.w;
       }
     }
     __syncthreads();

@@ -14,6 +14,29 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// Explicit shared-memory accesses by 32-bit shared address (code that only
+// has a generic pointer would otherwise go through generic loads/stores).
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 lds_u32x4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -26,6 +49,44 @@ __device__ __forceinline__ void store_f16x8(uint32_t addr, const float* f, bool&
   for (int e = 0; e < 8; ++e) bad |= !(fabsf(f[e]) < 65504.f);
   st_shared_v4(addr, pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
                pack_f16x2(f[6], f[7]));
+}
+
+// max(m, |x|), NaN-propagating: a running bound on what went into fp16
+// operands (checked once against the fp16 range at the end).
+__device__ __forceinline__ float absmax_nan(float m, float x) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(m), "f"(fabsf(x)));
+  return r;
+}
+
+// 8 consecutive floats -> one 16-byte fp16 chunk; folds their magnitudes into mx.
+__device__ __forceinline__ void store_f16x8_m(uint32_t addr, const float* f, float& mx) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) mx = absmax_nan(mx, f[e]);
+  st_shared_v4(addr, pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
+               pack_f16x2(f[6], f[7]));
+}
+
+// 8 consecutive floats -> bf16 high parts and bf16 remainders (x = hi + lo to
+// about 16 significant bits), stored as two 16-byte chunks.
+__device__ __forceinline__ void store_bf16x8_hilo(uint32_t addr_hi, uint32_t addr_lo, const float* f) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    h[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
+    const float r0 = f[2 * e] - __uint_as_float(h[e] << 16);
+    const float r1 = f[2 * e + 1] - __uint_as_float(h[e] & 0xffff0000u);
+    l[e] = pack_bf16x2(r0, r1);
+  }
+  st_shared_v4(addr_hi, h[0], h[1], h[2], h[3]);
+  st_shared_v4(addr_lo, l[0], l[1], l[2], l[3]);
+}
+
+// Two packed bf16 -> two packed fp16 (round to nearest); folds their magnitudes into mx.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_m(uint32_t w, float& mx) {
+  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+  mx = absmax_nan(absmax_nan(mx, lo), hi);
+  return pack_f16x2(lo, hi);
 }
 
 // Two packed bf16 -> two packed fp16 (round to nearest); flags out-of-range values.

@@ -138,14 +138,17 @@ __device__ __noinline__ void producer_role(uint8_t* sm, Ctl* ctl, const Problem&
 }
 
 // ----------------------------------------------------------------- MMA issuer
-// Three groups per chunk i, each issued as soon as its inputs are ready (the
-// readiness probes never block, so one late input holds up nothing else):
+// Three groups per chunk i:
 //   U(i)  U^T . I into V' buffer i & 1, once the record has landed and the
 //         state warps have read that buffer's previous V' (C(i-2) issued)
 //   A(i)  V'^T += S (-W)^T and Y = S Q^T, after U(i) and s_ready(i), and
 //         once the output warps have read Y/O2 buffer i & 1 (yo_free(i-2))
 //   C(i)  D3 = V'^T diag(dec) K and O2 = V'^T P^T, after v_ready(i); then
 //         the record stage is released
+// issued in the order A(i), U(i+1), C(i): the chain's critical path runs
+// A(i) -> V' epilogue -> C(i) -> state epilogue -> A(i+1), and U(i+1) fits
+// in while the state warps work on V'(i).  Waits block (suspending the warp)
+// rather than spin, leaving the issue slots to the epilogue warps.
 template <bool PREP>
 __device__ __noinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch, uint32_t tmem) {
   const int n = ch.run_end - ch.run_begin;
@@ -154,79 +157,60 @@ __device__ __noinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch, ui
   const uint32_t id_k = idesc_f16(128, 64, false, false);
   const uint32_t id_sw = idesc_f16(128, 64, false, true);
   const uint32_t id_d3 = idesc_f16(128, 128, false, true);
-  if (n <= 0) return;
-  int nu = 0, na = 0, nc = 0;
-  uint64_t t_last = globaltimer_ns();
-  while (nc < n) {
-    bool progress = false;
-    // V' buffer nu & 1 is free once C(nu - 2) has been issued (it waited for
-    // v_ready(nu - 2)); probing v_ready itself here could miss that phase
-    // when v_ready(nu - 1) has completed too.
-    if (nu < n && (nu < 2 || nc >= nu - 1) &&
-        mbar_test_wait(&ctl->bar[kFull0 + (nu & 1)], (uint32_t)((nu >> 1) & 1))) {
-      if (ch.has_u) {
-        const uint32_t sU = smem_u32(sm + (nu & 1) * kStageBytes + kStU);
-        tc_fence_after();
+  auto issue_u = [&](int i) {
+    if (!ch.has_u) return;
+    const uint32_t sU = smem_u32(sm + (i & 1) * kStageBytes + kStU);
+    tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tmem + kTV + (nu & 1) * 64, sdesc_sw128(sU + ks * 32, 16, 1024),
-                   sdesc_sw128(sI + ks * 32, 16, 1024), id_k, ks > 0);
-      }
+    for (int ks = 0; ks < 4; ++ks)
+      mma_bf16(tmem + kTV + (i & 1) * 64, sdesc_sw128(sU + ks * 32, 16, 1024), sdesc_sw128(sI + ks * 32, 16, 1024),
+               id_k, ks > 0);
+  };
+  int nu = 0;  // U groups issued
+  for (int i = 0; i < n; ++i) {
+    const uint32_t stg = smem_u32(sm + (i & 1) * kStageBytes);
+    if (nu == i) {
+      if (!wait_bar(ctl, kFull0 + (i & 1), (uint32_t)((i >> 1) & 1))) return;
+      issue_u(i);
       ++nu;
-      progress = true;
     }
-    if (na < nu && mbar_test_wait(&ctl->bar[kSReady], (uint32_t)(na & 1)) &&
-        (na < 2 || mbar_test_wait(&ctl->bar[kYoFree0 + (na & 1)], (uint32_t)(((na - 2) >> 1) & 1)))) {
-      const int i = na;
-      const uint32_t stg = smem_u32(sm + (i & 1) * kStageBytes);
-      tc_fence_after();
+    if (!wait_bar(ctl, kSReady, (uint32_t)(i & 1))) return;
+    if (i >= 2 && !wait_bar(ctl, kYoFree0 + (i & 1), (uint32_t)(((i - 2) >> 1) & 1))) return;
+    tc_fence_after();
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {  // V'^T += S (-W)^T
-        const uint64_t a = sdesc_sw128(sS + (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u, 16, 1024);
-        mma_bf16(tmem + kTV + (i & 1) * 64, a, sdesc_sw128(stg + kStWn + ks * 2048, 8192, 1024), id_sw,
-                 (ch.has_u || ks > 0) ? 1u : 0u);
-      }
-      mma_commit(&ctl->bar[kVaDone]);
-      if (want_out<PREP>(ch, i)) {
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {  // Y = S Q^T
-          const uint32_t off = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
-          mma_bf16(tmem + kTY + (i & 1) * 64, sdesc_sw128(sS + off, 16, 1024),
-                   sdesc_sw128(stg + kStKQ + 8192 + off, 16, 1024), id_k, ks > 0);
-        }
-      }
-      ++na;
-      progress = true;
+    for (int ks = 0; ks < 8; ++ks) {  // V'^T += S (-W)^T
+      const uint64_t a = sdesc_sw128(sS + (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u, 16, 1024);
+      mma_bf16(tmem + kTV + (i & 1) * 64, a, sdesc_sw128(stg + kStWn + ks * 2048, 8192, 1024), id_sw,
+               (ch.has_u || ks > 0) ? 1u : 0u);
     }
-    if (nc < na && mbar_test_wait(&ctl->bar[kVReady], (uint32_t)(nc & 1))) {
-      const int i = nc;
-      const uint32_t stg = smem_u32(sm + (i & 1) * kStageBytes);
-      tc_fence_after();
+    mma_commit(&ctl->bar[kVaDone]);
+    if (want_out<PREP>(ch, i)) {
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)  // D3 = V'^T diag(dec) K
-        mma_bf16(tmem + kTD3, sdesc_sw128(sVd + ks * 32, 16, 1024),
-                 sdesc_sw128(stg + kStKQ + ks * 2048, 16384, 1024), id_d3, ks > 0);
-      mma_commit(&ctl->bar[kD3Done]);
-      if (want_out<PREP>(ch, i)) {
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)  // O2 = V'^T P^T
-          mma_bf16(tmem + kTO2 + (i & 1) * 64, sdesc_sw128(sVp + ks * 32, 16, 1024),
-                   sdesc_sw128(stg + kStP + ks * 32, 16, 1024), id_k, ks > 0);
-      }
-      mma_commit(&ctl->bar[kYoDone0 + (i & 1)]);
-      mma_commit(&ctl->bar[kEmpty0 + (i & 1)]);
-      ++nc;
-      progress = true;
-    }
-    if (progress) {
-      t_last = globaltimer_ns();
-    } else {
-      if (*reinterpret_cast<volatile int*>(&ctl->abort)) return;
-      if (globaltimer_ns() - t_last > kWaitLimitNs) {
-        atomicCAS(&ctl->abort, 0, 200);
-        return;
+      for (int ks = 0; ks < 8; ++ks) {  // Y = S Q^T
+        const uint32_t off = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+        mma_bf16(tmem + kTY + (i & 1) * 64, sdesc_sw128(sS + off, 16, 1024),
+                 sdesc_sw128(stg + kStKQ + 8192 + off, 16, 1024), id_k, ks > 0);
       }
     }
+    if (i + 1 < n && mbar_test_wait(&ctl->bar[kFull0 + ((i + 1) & 1)], (uint32_t)(((i + 1) >> 1) & 1))) {
+      issue_u(i + 1);  // its V' buffer was released by C(i - 1)
+      ++nu;
+    }
+    if (!wait_bar(ctl, kVReady, (uint32_t)(i & 1))) return;
+    tc_fence_after();
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)  // D3 = V'^T diag(dec) K
+      mma_bf16(tmem + kTD3, sdesc_sw128(sVd + ks * 32, 16, 1024), sdesc_sw128(stg + kStKQ + ks * 2048, 16384, 1024),
+               id_d3, ks > 0);
+    mma_commit(&ctl->bar[kD3Done]);
+    if (want_out<PREP>(ch, i)) {
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)  // O2 = V'^T P^T
+        mma_bf16(tmem + kTO2 + (i & 1) * 64, sdesc_sw128(sVp + ks * 32, 16, 1024),
+                 sdesc_sw128(stg + kStP + ks * 32, 16, 1024), id_k, ks > 0);
+    }
+    mma_commit(&ctl->bar[kYoDone0 + (i & 1)]);
+    mma_commit(&ctl->bar[kEmpty0 + (i & 1)]);
   }
 }
 
@@ -274,11 +258,10 @@ __device__ __noinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p,
   for (int i = 0; i < n; ++i) {
     const uint32_t par = (uint32_t)(i & 1);
     const bool out = want_out<PREP>(ch, i);
-    const float* gam = reinterpret_cast<const float*>(sm + (i & 1) * kStageBytes + kStGam);
-    const float* dec = gam + 64;
+    const uint32_t sGam = smem_u32(sm + (i & 1) * kStageBytes + kStGam);  // exp(G) [64], then dec [64]
     if (!wait_bar(ctl, kFull0 + (i & 1), (uint32_t)((i >> 1) & 1)) || !wait_bar(ctl, kVaDone, par)) break;
     tc_fence_after();
-    const float gC = gam[63];
+    const float gC = lds_f32(sGam + 63 * 4);
     // V' operands: plain (for O) and decayed to the chunk end (for S)
     {
       uint32_t va[16], vb[16];
@@ -289,7 +272,9 @@ __device__ __noinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p,
       for (int q4 = 0; q4 < 4; ++q4) {
         const int g2 = q4 >> 1, q = q4 & 1;
         const float* f = reinterpret_cast<const float*>(g2 == 0 ? &va[q * 8] : &vb[q * 8]);
-        const float* d = dec + half * 32 + g2 * 16 + q * 8;
+        const uint32_t da = sGam + (64 + half * 32 + g2 * 16 + q * 8) * 4;
+        const float4 d0 = lds_f32x4(da), d1 = lds_f32x4(da + 16);
+        const float d[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
         const uint32_t off = sw128_offset(row, half * 4 + g2 * 2 + q);
         if (out) store_f16x8(sVp + off, f, bad);
         float fd[8];
@@ -356,20 +341,29 @@ __device__ __noinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem& p
     if (!wait_bar(ctl, kYoDone0 + b, (uint32_t)((i >> 1) & 1))) break;
     if (out && !wait_bar(ctl, kFull0 + b, (uint32_t)((i >> 1) & 1))) break;
     tc_fence_after();
-    uint16_t* sO = reinterpret_cast<uint16_t*>(stg + kStU);
+    const uint32_t sO = smem_u32(stg + kStU);  // bf16 [64 tokens][128]
     if (out) {
-      const float* gam = reinterpret_cast<const float*>(stg + kStGam);
+      const uint32_t sGam = smem_u32(stg + kStGam);
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         uint32_t yq[16], o2[16];
         tmem_ld16(tmem + lane_base + kTY + b * 64 + g * 16, yq);
         tmem_ld16(tmem + lane_base + kTO2 + b * 64 + g * 16, o2);
         tmem_ld_wait(yq, o2);
+        float gm[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 g4 = lds_f32x4(sGam + (g * 16 + 4 * q) * 4);
+          gm[4 * q] = g4.x;
+          gm[4 * q + 1] = g4.y;
+          gm[4 * q + 2] = g4.z;
+          gm[4 * q + 3] = g4.w;
+        }
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int t = g * 16 + e;
-          const float o = p.scale * fmaf(gam[t], __uint_as_float(yq[e]), __uint_as_float(o2[e]));
-          sO[t * kDim + row] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+          const float o = p.scale * fmaf(gm[e], __uint_as_float(yq[e]), __uint_as_float(o2[e]));
+          sts_u16(sO + (uint32_t)(t * kDim + row) * 2u, __bfloat16_as_ushort(__float2bfloat16_rn(o)));
         }
       }
     }
@@ -384,7 +378,7 @@ __device__ __noinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem& p
         const int idx = ot + q * kOutThreads;
         const int r = idx >> 4, c16 = idx & 15;
         if (r < cv) {
-          const uint4 val = *reinterpret_cast<const uint4*>(sO + r * kDim + c16 * 8);
+          const uint4 val = lds_u32x4(sO + (uint32_t)(r * kDim + c16 * 8) * 2u);
           *reinterpret_cast<uint4*>(outp + ((size_t)(t0 + r) * p.h_v + j) * kDim + c16 * 8) = val;
         }
       }
@@ -396,7 +390,7 @@ __device__ __noinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem& p
 template <bool PREP>
 __global__ void __launch_bounds__(kThreads, 1) scan_kernel(const Problem p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1024-byte aligned
   Ctl* ctl = reinterpret_cast<Ctl*>(sm + kSmCtl);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int j = blockIdx.y;

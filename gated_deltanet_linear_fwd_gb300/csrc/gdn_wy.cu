@@ -11,7 +11,9 @@
 //   L    = strict_lower(diag(beta) D_kk . exp(G_r - G_s))
 //   P    = lower(D_qk . exp(G_r - G_s))    (diagonal included)
 //   A    = (I + L)^{-1}                    (fp32, blocked)
-//   W^T  = K^T (A diag(beta gamma))^T,  U^T = V^T (A diag(beta))^T   (fp16 MMAs)
+//   W^T  = K^T (A diag(beta gamma))^T,  U^T = V^T (A diag(beta))^T
+// (bf16 MMAs on the exact K and V, with the A operands split into bf16 high
+// parts and remainders, so W and U keep about 16 significant bits of A)
 // and writes -W, U^T, P and (gamma, dec) as one record per (chunk, value
 // head), plus the fp16 copy of K and Q per (chunk, query/key head), each
 // tile in the 128-byte-swizzled layout the scan's MMAs read.
@@ -27,15 +29,16 @@ namespace {
 constexpr int kWyThreads = 256;
 
 // ---- shared memory map (bytes from a 1024-byte aligned base) ----
-constexpr uint32_t kWyKQ = 0;         // [K d0-63 | Q d0-63 | K d64-127 | Q d64-127]: bf16 from TMA, then fp16
-constexpr uint32_t kWyV = 32768;      // [V d0-63 | V d64-127]: bf16, then fp16; finally the U^T tile
-constexpr uint32_t kWyA = 49152;      // solve scratch; then A diag(beta gamma) | A diag(beta); finally -W
-constexpr uint32_t kWyP = 65536;      // fp16 P
-constexpr uint32_t kWyF = 73728;      // fp32 [64][68]: L below the diagonal, A^T on and above it
+constexpr uint32_t kWyKQ = 0;          // bf16 [K d0-63 | Q d0-63 | K d64-127 | Q d64-127] (TMA)
+constexpr uint32_t kWyV = 32768;       // bf16 [V d0-63 | V d64-127] (TMA); finally the U^T tile
+constexpr uint32_t kWyA = 49152;       // solve scratch; then the A operands, bf16 MN-major B, 8 KB each:
+                                       // A diag(beta gamma) hi | lo, A diag(beta) hi | lo; finally -W
+constexpr uint32_t kWyP = 81920;       // fp16 P
+constexpr uint32_t kWyF = 90112;       // fp32 [64][68]: L below the diagonal, A^T on and above it
 constexpr uint32_t kFStride = 68;
-constexpr uint32_t kWyGates = 91136;  // G | exp(G) | exp(G_63 - G) | beta | exp(-G), 64 floats each
-constexpr uint32_t kWyCtl = 92416;
-constexpr uint32_t kWySmemUse = 92480;
+constexpr uint32_t kWyGates = 107520;  // G | exp(G) | exp(G_63 - G) | beta | exp(-G), 64 floats each
+constexpr uint32_t kWyCtl = 108800;
+constexpr uint32_t kWySmemUse = 108864;
 constexpr uint32_t kWySmemAlloc = kWySmemUse + 1024;
 static_assert(2 * (kWySmemAlloc + 1024) <= 233472, "two CTAs per SM must fit");
 
@@ -191,8 +194,8 @@ __device__ __forceinline__ void seq_bounds(const Problem& p, int n, int64_t& bos
 }
 
 // Returns false (in every thread alike) when a wait gave up.
-__device__ __noinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& p, const CUtensorMap* mq,
-                                     const CUtensorMap* mk, const CUtensorMap* mv, uint32_t tmem, bool& bad) {
+__device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& p, const CUtensorMap* mq,
+                                     const CUtensorMap* mk, const CUtensorMap* mv, uint32_t tmem, float& mx) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gc = (int)(blockIdx.x / (unsigned)p.h_v), j = (int)(blockIdx.x % (unsigned)p.h_v);
   const int n = p.chunk_seq[gc];
@@ -305,21 +308,25 @@ __device__ __noinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& p, 
           const float d = __uint_as_float(rk[sl >> 4][sl & 15]);
           f[e] = (s <= r) ? (factored ? d * Er * sEm[s] : d * __expf(Gr - sG[s])) : 0.f;
         }
-        store_f16x8(sP + sw128_offset(r, ch * 4 + q), f, bad);
+        store_f16x8_m(sP + sw128_offset(r, ch * 4 + q), f, mx);
       }
     }
   }
   tc_fence_before();
   __syncthreads();
 
-  // ---- A = (I + L)^{-1}; meanwhile threads 64-255 convert K, Q, V to fp16 in place ----
+  // ---- A = (I + L)^{-1}; meanwhile threads 64-255 of the group's first CTA
+  //      write the fp16 copy of K|Q (same byte layout, converted chunk by chunk) ----
+  uint8_t* kq_rec = p.kq16 + ((size_t)gc * p.h_qk + iq) * kKqRecBytes;
   solve_unit_lower(F, scratch, tid, [&]() {
-    uint4* b4 = reinterpret_cast<uint4*>(sm + kWyKQ);  // K|Q|K|Q then V: 3072 16-byte vectors
+    if (!first_of_group) return;
+    const uint4* b4 = reinterpret_cast<const uint4*>(sm + kWyKQ);
+    uint4* g4 = reinterpret_cast<uint4*>(kq_rec);
 #pragma unroll 4
-    for (int v = tid - 64; v < 3072; v += kWyThreads - 64) {
+    for (int v = tid - 64; v < 2048; v += kWyThreads - 64) {
       const uint4 u = b4[v];
-      b4[v] = make_uint4(bf16x2_to_f16x2(u.x, bad), bf16x2_to_f16x2(u.y, bad), bf16x2_to_f16x2(u.z, bad),
-                         bf16x2_to_f16x2(u.w, bad));
+      g4[v] = make_uint4(bf16x2_to_f16x2_m(u.x, mx), bf16x2_to_f16x2_m(u.y, mx), bf16x2_to_f16x2_m(u.z, mx),
+                         bf16x2_to_f16x2_m(u.w, mx));
     }
   });
 
@@ -338,29 +345,33 @@ __device__ __noinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& p, 
       float f[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) f[e] = (8 * qq + e >= s) ? v[e] * sc : 0.f;
-      store_f16x8(sA + mat * 8192 + sw128_offset(s, qq), f, bad);
+      const uint32_t a = sA + mat * 16384 + sw128_offset(s, qq);
+      store_bf16x8_hilo(a, a + 8192, f);
     }
   }
   fence_proxy_async_smem();
   __syncthreads();
 
   uint8_t* rec = p.wy + ((size_t)gc * p.h_v + j) * kRecBytes;
-  if (tid == 32) {  // W^T = K^T (A diag(beta gamma))^T, U^T = V^T (A diag(beta))^T
+  if (tid == 32) {  // W^T = K^T (A diag(beta gamma))^T, U^T = V^T (A diag(beta))^T, A = hi + lo
     tc_fence_after();
-    const uint32_t id_mn = idesc_f16(128, 64, true, true);
+    const uint32_t id_mn = idesc_bf16_f32(128, 64, true, true);
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks)
-      mma_bf16(tmem + kTW, sdesc_sw128(sKQ + ks * 2048, 16384, 1024), sdesc_sw128(sA + ks * 2048, 8192, 1024),
-               id_mn, ks > 0);
+    for (int part = 0; part < 2; ++part)
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks)
-      mma_bf16(tmem + kTU, sdesc_sw128(sV + ks * 2048, 8192, 1024),
-               sdesc_sw128(sA + 8192 + ks * 2048, 8192, 1024), id_mn, ks > 0);
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tmem + kTW, sdesc_sw128(sKQ + ks * 2048, 16384, 1024),
+                 sdesc_sw128(sA + part * 8192 + ks * 2048, 8192, 1024), id_mn, (part | ks) > 0);
+#pragma unroll
+    for (int part = 0; part < 2; ++part)
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tmem + kTU, sdesc_sw128(sV + ks * 2048, 8192, 1024),
+                 sdesc_sw128(sA + 16384 + part * 8192 + ks * 2048, 8192, 1024), id_mn, (part | ks) > 0);
     mma_commit(&ctl->wu);
   } else if (tid == 64) {  // the parts of the record that are final already
     bulk_store(rec + kRecP, sm + kWyP, 8192);
     bulk_store(rec + kRecGam, sGam, 512);  // exp(G) then exp(G_63 - G)
-    if (first_of_group) bulk_store(p.kq16 + ((size_t)gc * p.h_qk + iq) * kKqRecBytes, sm + kWyKQ, kKqRecBytes);
     bulk_commit();
   }
   ok = wait_phase(&ctl->wu, 0, &ctl->abort, 102);
@@ -379,7 +390,7 @@ __device__ __noinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& p, 
       float f[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) f[e] = -__uint_as_float(q < 2 ? ra[8 * q + e] : rb[8 * (q - 2) + e]);
-      store_f16x8(sA + sw128_offset(d, ch * 4 + q), f, bad);
+      store_f16x8_m(sA + sw128_offset(d, ch * 4 + q), f, mx);
     }
     tmem_ld16(tmem + lane_base + kTU + ch * 32, ra);
     tmem_ld16(tmem + lane_base + kTU + ch * 32 + 16, rb);
@@ -389,7 +400,7 @@ __device__ __noinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& p, 
       float f[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(q < 2 ? ra[8 * q + e] : rb[8 * (q - 2) + e]);
-      store_f16x8(sV + sw128_offset(d, ch * 4 + q), f, bad);
+      store_f16x8_m(sV + sw128_offset(d, ch * 4 + q), f, mx);
     }
   }
   fence_proxy_async_smem();
@@ -407,7 +418,7 @@ __global__ void __launch_bounds__(kWyThreads, 2)
     wy_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
               const __grid_constant__ CUtensorMap mv, const Problem p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1024-byte aligned
   WyCtl* ctl = reinterpret_cast<WyCtl*>(sm + kWyCtl);
   const int tid = threadIdx.x, warp = tid >> 5;
   if (tid == 0) {
@@ -428,8 +439,8 @@ __global__ void __launch_bounds__(kWyThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem;
-  bool bad = false;
-  wy_body(sm, ctl, p, &mq, &mk, &mv, tmem, bad);
+  float mx = 0.f;  // largest magnitude rounded to fp16 by this thread
+  wy_body(sm, ctl, p, &mq, &mk, &mv, tmem, mx);
   if (tid == 64) bulk_wait_all();  // the record's stores have landed (and read shared memory)
   tc_fence_before();
   __syncthreads();
@@ -441,7 +452,7 @@ __global__ void __launch_bounds__(kWyThreads, 2)
     }
     __syncthreads();
   }
-  if (bad) report(p.status, kDevCheck, kDetFp16Range);
+  if (!(mx < 65504.f)) report(p.status, kDevCheck, kDetFp16Range);
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
