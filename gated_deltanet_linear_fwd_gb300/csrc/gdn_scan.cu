@@ -51,7 +51,7 @@ constexpr int kProducerWarp = 12;
 constexpr uint32_t kStageBytes = 75776;   // per chunk stage (two stages)
 constexpr uint32_t kStKQ = 0;             // fp16 [K d0-63 | Q d0-63 | K d64-127 | Q d64-127], 8 KB each
 constexpr uint32_t kStWn = 32768;         // fp16 -W, MN-major B: rows d_k
-constexpr uint32_t kStU = 49152;          // fp16 U^T, K-major A: rows d_v; then the chunk's bf16 output tile
+constexpr uint32_t kStU = 49152;          // fp16 U^T, K-major A: rows d_v
 constexpr uint32_t kStP = 65536;          // fp16 P, K-major B: rows r
 constexpr uint32_t kStGam = 73728;        // fp32 exp(G) [64], then exp(G_63 - G) [64]
 constexpr uint32_t kSmI = 2 * kStageBytes;  // fp16 64x64 identity, K-major B
@@ -246,10 +246,10 @@ __device__ __noinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p,
   const int n = ch.run_end - ch.run_begin;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   const uint32_t sS = smem_u32(sm + kSmS), sVp = smem_u32(sm + kSmVp), sVd = smem_u32(sm + kSmVd);
-  bool bad = false;
+  float mx = 0.f;  // largest magnitude rounded to fp16 by this thread
   auto store_state = [&]() {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) store_f16x8(sS + half * 16384 + sw128_offset(row, q), &S[8 * q], bad);
+    for (int q = 0; q < 8; ++q) store_f16x8_m(sS + half * 16384 + sw128_offset(row, q), &S[8 * q], mx);
   };
   store_state();
   fence_proxy_async_smem();
@@ -276,11 +276,11 @@ __device__ __noinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p,
         const float4 d0 = lds_f32x4(da), d1 = lds_f32x4(da + 16);
         const float d[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
         const uint32_t off = sw128_offset(row, half * 4 + g2 * 2 + q);
-        if (out) store_f16x8(sVp + off, f, bad);
+        if (out) store_f16x8_m(sVp + off, f, mx);
         float fd[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) fd[e] = f[e] * d[e];
-        store_f16x8(sVd + off, fd, bad);
+        store_f16x8_m(sVd + off, fd, mx);
       }
     }
     fence_proxy_async_smem();
@@ -307,7 +307,7 @@ __device__ __noinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p,
     mbar_arrive(&ctl->bar[kSReady]);
     done = i + 1;
   }
-  if (bad) atomicExch(&ctl->range_bad, 1);
+  if (!(mx < 65504.f)) atomicExch(&ctl->range_bad, 1);
   if (done < n || *reinterpret_cast<volatile int*>(&ctl->abort)) return;  // no results from an aborted chain
   if (PREP) {
     float* dst = (chain == 0 ? p.R : p.Sloc) + ((size_t)(si.seg_base + si.s) * p.h_v + j) * kDim * kDim +
@@ -323,67 +323,67 @@ __device__ __noinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p,
 }
 
 // ----------------------------------------------------------------- output warps
-// O^T = scale (Y diag(gamma) + O2), staged as bf16 [token][d_v] over the
-// chunk's U^T tile (consumed by then) and written with 16-byte stores.
+// O^T = scale (Y diag(gamma) + O2): each thread holds one d_v row of the
+// chunk's outputs and writes it straight to global memory (a warp's 32
+// threads cover 64 contiguous bytes of each token's row).  The stage is
+// released as soon as the gates have been read, so the next record's load
+// does not wait for these stores.
 template <bool PREP>
 __device__ __noinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem& p, const SegInfo& si,
                                          const Chain& ch, uint32_t tmem, int j) {
-  const int ot = threadIdx.x - kChainThreads;  // 0..127
   const int warp = threadIdx.x >> 5;
   const int row = (warp & 3) * 32 + (threadIdx.x & 31);  // d_v = TMEM lane
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   const int n = ch.run_end - ch.run_begin;
-  __nv_bfloat16* outp = reinterpret_cast<__nv_bfloat16*>(p.out);
+  uint16_t* outp = reinterpret_cast<uint16_t*>(p.out);
   for (int i = 0; i < n; ++i) {
     const int b = i & 1;
     const bool out = want_out<PREP>(ch, i);
-    uint8_t* stg = sm + b * kStageBytes;
     if (!wait_bar(ctl, kYoDone0 + b, (uint32_t)((i >> 1) & 1))) break;
-    if (out && !wait_bar(ctl, kFull0 + b, (uint32_t)((i >> 1) & 1))) break;
+    if (!out) {
+      tc_fence_before();
+      mbar_arrive(&ctl->bar[kYoFree0 + b]);
+      mbar_arrive(&ctl->bar[kEmpty0 + b]);
+      continue;
+    }
+    if (!wait_bar(ctl, kFull0 + b, (uint32_t)((i >> 1) & 1))) break;
     tc_fence_after();
-    const uint32_t sO = smem_u32(stg + kStU);  // bf16 [64 tokens][128]
-    if (out) {
-      const uint32_t sGam = smem_u32(stg + kStGam);
+    const uint32_t sGam = smem_u32(sm + b * kStageBytes + kStGam);
+    const int64_t t0 = si.bos + (int64_t)(ch.run_begin + i) * kChunk;
+    const int cv = (int)min((int64_t)kChunk, si.eos - t0);
+    uint16_t* orow = outp + ((size_t)t0 * p.h_v + j) * kDim + row;
+    const size_t tstride = (size_t)p.h_v * kDim;
+    uint32_t yq[2][16], o2[2][16];
+    tmem_ld16(tmem + lane_base + kTY + b * 64, yq[0]);
+    tmem_ld16(tmem + lane_base + kTO2 + b * 64, o2[0]);
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        uint32_t yq[16], o2[16];
-        tmem_ld16(tmem + lane_base + kTY + b * 64 + g * 16, yq);
-        tmem_ld16(tmem + lane_base + kTO2 + b * 64 + g * 16, o2);
-        tmem_ld_wait(yq, o2);
-        float gm[16];
+    for (int g = 0; g < 4; ++g) {
+      const int cur = g & 1;
+      tmem_ld_wait(yq[cur], o2[cur]);
+      if (g + 1 < 4) {  // next 16 columns in flight while these are stored
+        tmem_ld16(tmem + lane_base + kTY + b * 64 + (g + 1) * 16, yq[cur ^ 1]);
+        tmem_ld16(tmem + lane_base + kTO2 + b * 64 + (g + 1) * 16, o2[cur ^ 1]);
+      } else {
+        tc_fence_before();
+        mbar_arrive(&ctl->bar[kYoFree0 + b]);  // Y/O2 buffer b read
+      }
+      float gm[16];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 g4 = lds_f32x4(sGam + (g * 16 + 4 * q) * 4);
-          gm[4 * q] = g4.x;
-          gm[4 * q + 1] = g4.y;
-          gm[4 * q + 2] = g4.z;
-          gm[4 * q + 3] = g4.w;
-        }
+      for (int q = 0; q < 4; ++q) {
+        const float4 g4 = lds_f32x4(sGam + (g * 16 + 4 * q) * 4);
+        gm[4 * q] = g4.x;
+        gm[4 * q + 1] = g4.y;
+        gm[4 * q + 2] = g4.z;
+        gm[4 * q + 3] = g4.w;
+      }
+      if (g == 3) mbar_arrive(&ctl->bar[kEmpty0 + b]);  // the stage's gates have been read
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int t = g * 16 + e;
-          const float o = p.scale * fmaf(gm[e], __uint_as_float(yq[e]), __uint_as_float(o2[e]));
-          sts_u16(sO + (uint32_t)(t * kDim + row) * 2u, __bfloat16_as_ushort(__float2bfloat16_rn(o)));
-        }
+      for (int e = 0; e < 16; ++e) {
+        const int t = g * 16 + e;
+        const float o = p.scale * fmaf(gm[e], __uint_as_float(yq[cur][e]), __uint_as_float(o2[cur][e]));
+        if (t < cv) orow[(size_t)t * tstride] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
       }
     }
-    tc_fence_before();
-    mbar_arrive(&ctl->bar[kYoFree0 + b]);
-    if (out) {
-      named_bar_sync(5, kOutThreads);
-      const int64_t t0 = si.bos + (int64_t)(ch.run_begin + i) * kChunk;
-      const int cv = (int)min((int64_t)kChunk, si.eos - t0);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int idx = ot + q * kOutThreads;
-        const int r = idx >> 4, c16 = idx & 15;
-        if (r < cv) {
-          const uint4 val = lds_u32x4(sO + (uint32_t)(r * kDim + c16 * 8) * 2u);
-          *reinterpret_cast<uint4*>(outp + ((size_t)(t0 + r) * p.h_v + j) * kDim + c16 * 8) = val;
-        }
-      }
-    }
-    mbar_arrive(&ctl->bar[kEmpty0 + b]);
   }
 }
 
