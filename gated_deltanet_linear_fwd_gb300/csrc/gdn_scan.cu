@@ -48,21 +48,21 @@ constexpr int kOutThreads = 128;
 constexpr int kProducerWarp = 12;
 
 // ---- shared memory map (bytes from a 1024-byte aligned base) ----
-constexpr uint32_t kStageBytes = 75776;   // per chunk stage (two stages)
+constexpr uint32_t kStageBytes = 73728;   // per chunk stage (two stages)
 constexpr uint32_t kStKQ = 0;             // fp16 [K d0-63 | Q d0-63 | K d64-127 | Q d64-127], 8 KB each
 constexpr uint32_t kStWn = 32768;         // fp16 -W, MN-major B: rows d_k
 constexpr uint32_t kStU = 49152;          // fp16 U^T, K-major A: rows d_v
 constexpr uint32_t kStP = 65536;          // fp16 P, K-major B: rows r
-constexpr uint32_t kStGam = 73728;        // fp32 exp(G) [64], then exp(G_63 - G) [64]
 constexpr uint32_t kSmI = 2 * kStageBytes;  // fp16 64x64 identity, K-major B
 constexpr uint32_t kSmS = kSmI + 8192;      // fp16 state, K-major A: two 64-column halves of 16 KB
 constexpr uint32_t kSmVp = kSmS + 32768;    // fp16 V'^T, K-major A
 constexpr uint32_t kSmVd = kSmVp + 16384;   // fp16 V'^T diag(decay to chunk end), K-major A
-constexpr uint32_t kSmCtl = kSmVd + 16384;  // barriers, TMEM base, flags
+constexpr uint32_t kSmG = kSmVd + 16384;    // 4 slots (chunk i in slot i & 3): fp32 exp(G) [64], exp(G_63 - G) [64]
+constexpr uint32_t kSmCtl = kSmG + 4 * 512; // barriers, TMEM base, flags
 constexpr uint32_t kSmemUse = kSmCtl + 256;
 constexpr uint32_t kSmemAlloc = kSmemUse + 1024;
 static_assert(kSmemAlloc <= 232448, "shared memory over the per-block limit");
-static_assert(kStGam + 512 <= kStageBytes && kStageBytes % 1024 == 0, "stage layout");
+static_assert(kStP + 8192 <= kStageBytes && kStageBytes % 1024 == 0, "stage layout");
 
 // ---- TMEM columns (512 allocated) ----
 constexpr uint32_t kTV = 0;     // U^T then V'^T, 2 buffers    128 x 64 each
@@ -75,6 +75,7 @@ enum InitKind { kInitZero = 0, kInitIdentity = 1, kInitH0 = 2, kInitStart = 3 };
 // mbarrier indices
 enum Bar {
   kFull0 = 0, kFull1, kEmpty0, kEmpty1,    // record stages
+  kGates0, kGates1, kGates2, kGates3,      // gates ring slots (loaded)
   kVaDone, kVReady, kD3Done, kSReady,      // state pipeline
   kYoDone0, kYoDone1, kYoFree0, kYoFree1,  // output pipeline (two Y/O2 buffers)
   kNumBars
@@ -121,8 +122,7 @@ __device__ __noinline__ void producer_role(uint8_t* sm, Ctl* ctl, const Problem&
     const bool out = want_out<PREP>(ch, i);
     uint8_t* stg = sm + st * kStageBytes;
     uint64_t* bar = &ctl->bar[kFull0 + st];
-    const uint32_t bytes =
-        (out ? 32768u : 16384u) + 16384u + (ch.has_u ? 16384u : 0u) + (out ? 8192u : 0u) + 512u;
+    const uint32_t bytes = (out ? 32768u : 16384u) + 16384u + (ch.has_u ? 16384u : 0u) + (out ? 8192u : 0u);
     mbar_arrive_expect_tx(bar, bytes);
     if (out) {
       bulk_load(stg + kStKQ, kq, 32768u, bar);
@@ -133,7 +133,13 @@ __device__ __noinline__ void producer_role(uint8_t* sm, Ctl* ctl, const Problem&
     bulk_load(stg + kStWn, rec + kRecWn, 16384u, bar);
     if (ch.has_u) bulk_load(stg + kStU, rec + kRecU, 16384u, bar);
     if (out) bulk_load(stg + kStP, rec + kRecP, 8192u, bar);
-    bulk_load(stg + kStGam, rec + kRecGam, 512u, bar);
+    // The gates go to ring slot i & 3.  Its previous readers, of chunk i - 4,
+    // are done: the output warps read those gates before yo_free(i - 4),
+    // which A(i - 2) waited for, and stage i & 1 is free only after C(i - 2),
+    // which followed the state warps' v_ready(i - 2).
+    uint64_t* gbar = &ctl->bar[kGates0 + (i & 3)];
+    mbar_arrive_expect_tx(gbar, 512u);
+    bulk_load(sm + kSmG + (i & 3) * 512, rec + kRecGam, 512u, gbar);
   }
 }
 
@@ -258,8 +264,8 @@ __device__ __noinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p,
   for (int i = 0; i < n; ++i) {
     const uint32_t par = (uint32_t)(i & 1);
     const bool out = want_out<PREP>(ch, i);
-    const uint32_t sGam = smem_u32(sm + (i & 1) * kStageBytes + kStGam);  // exp(G) [64], then dec [64]
-    if (!wait_bar(ctl, kFull0 + (i & 1), (uint32_t)((i >> 1) & 1)) || !wait_bar(ctl, kVaDone, par)) break;
+    const uint32_t sGam = smem_u32(sm + kSmG + (i & 3) * 512);  // exp(G) [64], then dec [64]
+    if (!wait_bar(ctl, kGates0 + (i & 3), (uint32_t)((i >> 2) & 1)) || !wait_bar(ctl, kVaDone, par)) break;
     tc_fence_after();
     const float gC = lds_f32(sGam + 63 * 4);
     // V' operands: plain (for O) and decayed to the chunk end (for S)
@@ -325,9 +331,9 @@ __device__ __noinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p,
 // ----------------------------------------------------------------- output warps
 // O^T = scale (Y diag(gamma) + O2): each thread holds one d_v row of the
 // chunk's outputs and writes it straight to global memory (a warp's 32
-// threads cover 64 contiguous bytes of each token's row).  The stage is
-// released as soon as the gates have been read, so the next record's load
-// does not wait for these stores.
+// threads cover 64 contiguous bytes of each token's row).  These warps read
+// nothing from the record stages (the gates sit in their own ring), so the
+// next record's load never waits for them.
 template <bool PREP>
 __device__ __noinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem& p, const SegInfo& si,
                                          const Chain& ch, uint32_t tmem, int j) {
@@ -343,12 +349,11 @@ __device__ __noinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem& p
     if (!out) {
       tc_fence_before();
       mbar_arrive(&ctl->bar[kYoFree0 + b]);
-      mbar_arrive(&ctl->bar[kEmpty0 + b]);
       continue;
     }
-    if (!wait_bar(ctl, kFull0 + b, (uint32_t)((i >> 1) & 1))) break;
+    if (!wait_bar(ctl, kGates0 + (i & 3), (uint32_t)((i >> 2) & 1))) break;
     tc_fence_after();
-    const uint32_t sGam = smem_u32(sm + b * kStageBytes + kStGam);
+    const uint32_t sGam = smem_u32(sm + kSmG + (i & 3) * 512);
     const int64_t t0 = si.bos + (int64_t)(ch.run_begin + i) * kChunk;
     const int cv = (int)min((int64_t)kChunk, si.eos - t0);
     uint16_t* orow = outp + ((size_t)t0 * p.h_v + j) * kDim + row;
@@ -363,9 +368,6 @@ __device__ __noinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem& p
       if (g + 1 < 4) {  // next 16 columns in flight while these are stored
         tmem_ld16(tmem + lane_base + kTY + b * 64 + (g + 1) * 16, yq[cur ^ 1]);
         tmem_ld16(tmem + lane_base + kTO2 + b * 64 + (g + 1) * 16, o2[cur ^ 1]);
-      } else {
-        tc_fence_before();
-        mbar_arrive(&ctl->bar[kYoFree0 + b]);  // Y/O2 buffer b read
       }
       float gm[16];
 #pragma unroll
@@ -376,7 +378,10 @@ __device__ __noinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem& p
         gm[4 * q + 2] = g4.z;
         gm[4 * q + 3] = g4.w;
       }
-      if (g == 3) mbar_arrive(&ctl->bar[kEmpty0 + b]);  // the stage's gates have been read
+      if (g == 3) {  // Y/O2 buffer b and the gates ring slot have been read
+        tc_fence_before();
+        mbar_arrive(&ctl->bar[kYoFree0 + b]);
+      }
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int t = g * 16 + e;
@@ -455,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(const Problem p) {
 
   // ---- set-up ----
   if (tid == 0) {
-    const int counts[kNumBars] = {1, 1, 1 + kOutThreads, 1 + kOutThreads, 1, kChainThreads, 1, kChainThreads,
+    const int counts[kNumBars] = {1, 1, 1, 1, 1, 1, 1, 1, 1, kChainThreads, 1, kChainThreads,
                                   1, 1, kOutThreads, kOutThreads};
     for (int b = 0; b < kNumBars; ++b) mbar_init(&ctl->bar[b], counts[b]);
     ctl->abort = 0;
