@@ -29,12 +29,12 @@
 // for its MMAs; V' likewise.  A value outside the fp16 range is reported
 // through the status word.
 //
-// Warp roles (448 threads): warps 0-7 hold the state (row = d_v lane, 64
+// Warp roles (320 threads): warps 0-7 hold the state (row = d_v lane, 64
 // columns each) and run the V' and state epilogues, the critical path from
-// one chunk to the next; warps 8-11 read Y and O2 and write the outputs;
-// warp 12 loads each chunk's record (bulk copies); lane 0 of warp 13 issues
-// every MMA as soon as its inputs are ready.  They hand over through
-// mbarriers whose waits are all bounded.
+// one chunk to the next, and then the chunk's output epilogue while the
+// tensor cores work on the next chunk's S W^T; warp 8 loads each chunk's
+// record (bulk copies); lane 0 of warp 9 issues every MMA.  They hand over
+// through mbarriers whose waits are all bounded.
 #include <cuda_bf16.h>
 
 #include "gdn_dev.cuh"
@@ -42,10 +42,9 @@
 namespace gdn {
 namespace {
 
-constexpr int kThreads = 448;
+constexpr int kThreads = 320;
 constexpr int kChainThreads = 256;
-constexpr int kOutThreads = 128;
-constexpr int kProducerWarp = 12;
+constexpr int kProducerWarp = 8;
 
 // ---- shared memory map (bytes from a 1024-byte aligned base) ----
 constexpr uint32_t kStageBytes = 73728;   // per chunk stage (two stages)
@@ -77,7 +76,7 @@ enum Bar {
   kFull0 = 0, kFull1, kEmpty0, kEmpty1,    // record stages
   kGates0, kGates1, kGates2, kGates3,      // gates ring slots (loaded)
   kVaDone, kVReady, kD3Done, kSReady,      // state pipeline
-  kYoDone0, kYoDone1, kYoFree0, kYoFree1,  // output pipeline (two Y/O2 buffers)
+  kYoDone0, kYoDone1, kYoFree0, kYoFree1,  // output epilogue (two Y/O2 buffers)
   kNumBars
 };
 
@@ -133,10 +132,9 @@ __device__ __noinline__ void producer_role(uint8_t* sm, Ctl* ctl, const Problem&
     bulk_load(stg + kStWn, rec + kRecWn, 16384u, bar);
     if (ch.has_u) bulk_load(stg + kStU, rec + kRecU, 16384u, bar);
     if (out) bulk_load(stg + kStP, rec + kRecP, 8192u, bar);
-    // The gates go to ring slot i & 3.  Its previous readers, of chunk i - 4,
-    // are done: the output warps read those gates before yo_free(i - 4),
-    // which A(i - 2) waited for, and stage i & 1 is free only after C(i - 2),
-    // which followed the state warps' v_ready(i - 2).
+    // The gates go to ring slot i & 3.  Its readers of chunk i - 4 are done:
+    // the state warps read those gates before yo_free(i - 4), which A(i - 2)
+    // waited for, and stage i & 1 is free only after C(i - 2).
     uint64_t* gbar = &ctl->bar[kGates0 + (i & 3)];
     mbar_arrive_expect_tx(gbar, 512u);
     bulk_load(sm + kSmG + (i & 3) * 512, rec + kRecGam, 512u, gbar);
@@ -148,7 +146,7 @@ __device__ __noinline__ void producer_role(uint8_t* sm, Ctl* ctl, const Problem&
 //   U(i)  U^T . I into V' buffer i & 1, once the record has landed and the
 //         state warps have read that buffer's previous V' (C(i-2) issued)
 //   A(i)  V'^T += S (-W)^T and Y = S Q^T, after U(i) and s_ready(i), and
-//         once the output warps have read Y/O2 buffer i & 1 (yo_free(i-2))
+//         once the output epilogue has read Y/O2 buffer i & 1 (yo_free(i-2))
 //   C(i)  D3 = V'^T diag(dec) K and O2 = V'^T P^T, after v_ready(i); then
 //         the record stage is released
 // issued in the order A(i), U(i+1), C(i): the chain's critical path runs
@@ -311,6 +309,42 @@ __device__ __noinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p,
     fence_proxy_async_smem();
     tc_fence_before();
     mbar_arrive(&ctl->bar[kSReady]);
+    // output epilogue of this chunk (its O2 follows D3 on the tensor cores):
+    // O^T = scale (Y diag(gamma) + O2) for this thread's d_v row and 32 tokens,
+    // written straight to global memory (a warp covers 64 contiguous bytes
+    // of each token's row)
+    if (out) {
+      if (!wait_bar(ctl, kYoDone0 + (i & 1), (uint32_t)((i >> 1) & 1))) break;
+      tc_fence_after();
+      const int64_t t0 = si.bos + (int64_t)(ch.run_begin + i) * kChunk;
+      const int cv = (int)min((int64_t)kChunk, si.eos - t0);
+      uint16_t* orow = reinterpret_cast<uint16_t*>(p.out) + ((size_t)t0 * p.h_v + j) * kDim + row;
+      const size_t tstride = (size_t)p.h_v * kDim;
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        const int tb = half * 32 + g * 16;
+        uint32_t yq[16], o2[16];
+        tmem_ld16(tmem + lane_base + kTY + (i & 1) * 64 + tb, yq);
+        tmem_ld16(tmem + lane_base + kTO2 + (i & 1) * 64 + tb, o2);
+        float gm[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 g4 = lds_f32x4(sGam + (tb + 4 * q) * 4);
+          gm[4 * q] = g4.x;
+          gm[4 * q + 1] = g4.y;
+          gm[4 * q + 2] = g4.z;
+          gm[4 * q + 3] = g4.w;
+        }
+        tmem_ld_wait(yq, o2);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float o = p.scale * fmaf(gm[e], __uint_as_float(yq[e]), __uint_as_float(o2[e]));
+          if (tb + e < cv) orow[(size_t)(tb + e) * tstride] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+        }
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(&ctl->bar[kYoFree0 + (i & 1)]);  // Y/O2 buffer i & 1 and gates slot i & 3 read
     done = i + 1;
   }
   if (!(mx < 65504.f)) atomicExch(&ctl->range_bad, 1);
@@ -325,70 +359,6 @@ __device__ __noinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p,
     float* dst = p.hT + (size_t)(si.n * p.h_v + j) * kDim * kDim;
 #pragma unroll
     for (int e = 0; e < 64; ++e) dst[(size_t)(half * 64 + e) * kDim + row] = S[e];
-  }
-}
-
-// ----------------------------------------------------------------- output warps
-// O^T = scale (Y diag(gamma) + O2): each thread holds one d_v row of the
-// chunk's outputs and writes it straight to global memory (a warp's 32
-// threads cover 64 contiguous bytes of each token's row).  These warps read
-// nothing from the record stages (the gates sit in their own ring), so the
-// next record's load never waits for them.
-template <bool PREP>
-__device__ __noinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem& p, const SegInfo& si,
-                                         const Chain& ch, uint32_t tmem, int j) {
-  const int warp = threadIdx.x >> 5;
-  const int row = (warp & 3) * 32 + (threadIdx.x & 31);  // d_v = TMEM lane
-  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-  const int n = ch.run_end - ch.run_begin;
-  uint16_t* outp = reinterpret_cast<uint16_t*>(p.out);
-  for (int i = 0; i < n; ++i) {
-    const int b = i & 1;
-    const bool out = want_out<PREP>(ch, i);
-    if (!wait_bar(ctl, kYoDone0 + b, (uint32_t)((i >> 1) & 1))) break;
-    if (!out) {
-      tc_fence_before();
-      mbar_arrive(&ctl->bar[kYoFree0 + b]);
-      continue;
-    }
-    if (!wait_bar(ctl, kGates0 + (i & 3), (uint32_t)((i >> 2) & 1))) break;
-    tc_fence_after();
-    const uint32_t sGam = smem_u32(sm + kSmG + (i & 3) * 512);
-    const int64_t t0 = si.bos + (int64_t)(ch.run_begin + i) * kChunk;
-    const int cv = (int)min((int64_t)kChunk, si.eos - t0);
-    uint16_t* orow = outp + ((size_t)t0 * p.h_v + j) * kDim + row;
-    const size_t tstride = (size_t)p.h_v * kDim;
-    uint32_t yq[2][16], o2[2][16];
-    tmem_ld16(tmem + lane_base + kTY + b * 64, yq[0]);
-    tmem_ld16(tmem + lane_base + kTO2 + b * 64, o2[0]);
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      const int cur = g & 1;
-      tmem_ld_wait(yq[cur], o2[cur]);
-      if (g + 1 < 4) {  // next 16 columns in flight while these are stored
-        tmem_ld16(tmem + lane_base + kTY + b * 64 + (g + 1) * 16, yq[cur ^ 1]);
-        tmem_ld16(tmem + lane_base + kTO2 + b * 64 + (g + 1) * 16, o2[cur ^ 1]);
-      }
-      float gm[16];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 g4 = lds_f32x4(sGam + (g * 16 + 4 * q) * 4);
-        gm[4 * q] = g4.x;
-        gm[4 * q + 1] = g4.y;
-        gm[4 * q + 2] = g4.z;
-        gm[4 * q + 3] = g4.w;
-      }
-      if (g == 3) {  // Y/O2 buffer b and the gates ring slot have been read
-        tc_fence_before();
-        mbar_arrive(&ctl->bar[kYoFree0 + b]);
-      }
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int t = g * 16 + e;
-        const float o = p.scale * fmaf(gm[e], __uint_as_float(yq[cur][e]), __uint_as_float(o2[cur][e]));
-        if (t < cv) orow[(size_t)t * tstride] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
-      }
-    }
   }
 }
 
@@ -461,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(const Problem p) {
   // ---- set-up ----
   if (tid == 0) {
     const int counts[kNumBars] = {1, 1, 1, 1, 1, 1, 1, 1, 1, kChainThreads, 1, kChainThreads,
-                                  1, 1, kOutThreads, kOutThreads};
+                                  1, 1, kChainThreads, kChainThreads};
     for (int b = 0; b < kNumBars; ++b) mbar_init(&ctl->bar[b], counts[b]);
     ctl->abort = 0;
     ctl->range_bad = 0;
@@ -488,8 +458,6 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(const Problem p) {
 
   if (warp < 8) {
     chain_role<PREP>(sm, ctl, p, si, ch, tmem, j, chain);
-  } else if (warp < 12) {
-    output_role<PREP>(sm, ctl, p, si, ch, tmem, j);
   } else if (warp == kProducerWarp) {
     producer_role<PREP>(sm, ctl, p, ch, j);
   } else if (lane == 0) {
