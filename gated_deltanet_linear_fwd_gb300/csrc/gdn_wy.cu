@@ -18,7 +18,9 @@
 // head), plus the fp16 copy of K and Q per (chunk, query/key head), each
 // tile in the 128-byte-swizzled layout the scan's MMAs read.
 //
-// One CTA of 256 threads per (chunk, value head), two CTAs per SM.
+// One CTA of 256 threads per (chunk, value head), three CTAs per SM: the
+// shared-memory regions are reused as the work moves on (the A operands
+// go where Q and L were), and P and the gates go straight to global memory.
 #include <cuda_bf16.h>
 
 #include "gdn_dev.cuh"
@@ -29,24 +31,24 @@ namespace {
 constexpr int kWyThreads = 256;
 
 // ---- shared memory map (bytes from a 1024-byte aligned base) ----
-constexpr uint32_t kWyKQ = 0;          // bf16 [K d0-63 | Q d0-63 | K d64-127 | Q d64-127] (TMA)
+constexpr uint32_t kWyKQ = 0;          // bf16 [K d0-63 | Q d0-63 | K d64-127 | Q d64-127] (TMA); once Q
+                                       // is consumed, its two slots hold A diag(beta gamma) hi | lo
 constexpr uint32_t kWyV = 32768;       // bf16 [V d0-63 | V d64-127] (TMA); finally the U^T tile
-constexpr uint32_t kWyA = 49152;       // solve scratch; then the A operands, bf16 MN-major B, 8 KB each:
-                                       // A diag(beta gamma) hi | lo, A diag(beta) hi | lo; finally -W
-constexpr uint32_t kWyP = 81920;       // fp16 P
-constexpr uint32_t kWyF = 90112;       // fp32 [64][68]: L below the diagonal, A^T on and above it
+constexpr uint32_t kWyF = 49152;       // fp32 [64][68]: L below the diagonal, A^T on and above it; then
+                                       // A diag(beta) hi | lo (8 KB each); finally the -W tile
 constexpr uint32_t kFStride = 68;
-constexpr uint32_t kWyGates = 107520;  // G | exp(G) | exp(G_63 - G) | beta | exp(-G), 64 floats each
-constexpr uint32_t kWyCtl = 108800;
-constexpr uint32_t kWySmemUse = 108864;
+constexpr uint32_t kWyScr = 66560;     // fp32 solve scratch (4 KB)
+constexpr uint32_t kWyGates = 70656;   // G | exp(G) | exp(G_63 - G) | beta | exp(-G), 64 floats each
+constexpr uint32_t kWyCtl = 71936;
+constexpr uint32_t kWySmemUse = 72000;
 constexpr uint32_t kWySmemAlloc = kWySmemUse + 1024;
-static_assert(2 * (kWySmemAlloc + 1024) <= 233472, "two CTAs per SM must fit");
+static_assert(3 * (kWySmemAlloc + 1024) <= 233472, "three CTAs per SM must fit");
 
 // ---- TMEM columns ----
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 128;
 constexpr uint32_t kTD = 0;    // [K K^T ; Q K^T]   128 x 64
 constexpr uint32_t kTW = 64;   // W^T               128 x 64
-constexpr uint32_t kTU = 128;  // U^T               128 x 64
+constexpr uint32_t kTU = 0;    // U^T               128 x 64 (over D, read by then)
 
 struct WyCtl {
   uint64_t full, kq, wu;
@@ -221,10 +223,10 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
   float* sBeta = gts + 192;
   float* sEm = gts + 256;
   float* F = reinterpret_cast<float*>(sm + kWyF);
-  float* scratch = reinterpret_cast<float*>(sm + kWyA);
-  const uint32_t sKQ = smem_u32(sm + kWyKQ), sV = smem_u32(sm + kWyV), sA = smem_u32(sm + kWyA);
-  const uint32_t sP = smem_u32(sm + kWyP);
+  float* scratch = reinterpret_cast<float*>(sm + kWyScr);
+  const uint32_t sKQ = smem_u32(sm + kWyKQ), sV = smem_u32(sm + kWyV), sF = smem_u32(sm + kWyF);
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+  uint8_t* rec = p.wy + ((size_t)gc * p.h_v + j) * kRecBytes;
 
   // ---- loads; D = [K;Q] K^T as soon as they land ----
   if (tid == 0) {
@@ -254,7 +256,10 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
     sBeta[r] = b;
     sEm[r] = __expf(-x);
     named_bar_sync(1, 64);
-    sDec[r] = __expf(sG[63] - x);
+    const float dec = __expf(sG[63] - x);
+    sDec[r] = dec;
+    reinterpret_cast<float*>(rec + kRecGam)[r] = sGam[r];  // the record's gates
+    reinterpret_cast<float*>(rec + kRecGam)[64 + r] = dec;
   }
   if (tid == 32) {
     if (wait_phase(&ctl->full, 0, &ctl->abort, 100)) {
@@ -272,7 +277,8 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
   if (__syncthreads_or(!ok)) return false;
   tc_fence_after();
 
-  // ---- L (TMEM lanes 0-63) into F and P (lanes 64-127) into its operand ----
+  // ---- L (TMEM lanes 0-63) into F; P (lanes 64-127) into the record, as its
+  //      swizzled operand tile ----
   {
     const bool factored = fabsf(sG[0]) < 80.f && fabsf(sG[63]) < 80.f;  // exp(G_r) exp(-G_s) cannot overflow
     const int R = (warp & 3) * 32 + lane, ch = warp >> 2;                 // columns 32 ch .. 32 ch + 31
@@ -308,7 +314,10 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
           const float d = __uint_as_float(rk[sl >> 4][sl & 15]);
           f[e] = (s <= r) ? (factored ? d * Er * sEm[s] : d * __expf(Gr - sG[s])) : 0.f;
         }
-        store_f16x8_m(sP + sw128_offset(r, ch * 4 + q), f, mx);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx = absmax_nan(mx, f[e]);
+        *reinterpret_cast<uint4*>(rec + kRecP + sw128_offset(r, ch * 4 + q)) =
+            make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]), pack_f16x2(f[6], f[7]));
       }
     }
   }
@@ -330,29 +339,38 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
     }
   });
 
-  // ---- A operands: row s of A^T scaled by beta gamma (for W) / beta (for U) ----
+  // ---- A operands: row s of A^T scaled by beta gamma (for W) / beta (for U),
+  //      split into bf16 high parts and remainders; A diag(beta gamma) goes to
+  //      the Q slots, A diag(beta) over F (read into registers first) ----
   {
     const int row = tid >> 1, hs = tid & 1;
     const int s = row & 63, mat = row >> 6;
     const float sc = mat == 0 ? sBeta[s] * sGam[s] : sBeta[s];
-    const float* At = F + s * kFStride;
+    const float* At = F + s * kFStride + 32 * hs;
+    float v[32];
+#pragma unroll
+    for (int q4 = 0; q4 < 8; ++q4) {
+      const float4 a4 = *reinterpret_cast<const float4*>(At + 4 * q4);
+      v[4 * q4] = a4.x;
+      v[4 * q4 + 1] = a4.y;
+      v[4 * q4 + 2] = a4.z;
+      v[4 * q4 + 3] = a4.w;
+    }
+    __syncthreads();  // F is read: its first 16 KB take A diag(beta)
+    const uint32_t hi_base = mat == 0 ? sKQ + 8192 : sF, lo_base = mat == 0 ? sKQ + 24576 : sF + 8192;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int qq = hs * 4 + q;
-      const float4 lo4 = *reinterpret_cast<const float4*>(At + 8 * qq);
-      const float4 hi4 = *reinterpret_cast<const float4*>(At + 8 * qq + 4);
-      const float v[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
       float f[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) f[e] = (8 * qq + e >= s) ? v[e] * sc : 0.f;
-      const uint32_t a = sA + mat * 16384 + sw128_offset(s, qq);
-      store_bf16x8_hilo(a, a + 8192, f);
+      for (int e = 0; e < 8; ++e) f[e] = (8 * qq + e >= s) ? v[8 * q + e] * sc : 0.f;
+      store_bf16x8_hilo(hi_base + sw128_offset(s, qq), lo_base + sw128_offset(s, qq), f);
     }
   }
   fence_proxy_async_smem();
+  tc_fence_before();
   __syncthreads();
 
-  uint8_t* rec = p.wy + ((size_t)gc * p.h_v + j) * kRecBytes;
   if (tid == 32) {  // W^T = K^T (A diag(beta gamma))^T, U^T = V^T (A diag(beta))^T, A = hi + lo
     tc_fence_after();
     const uint32_t id_mn = idesc_bf16_f32(128, 64, true, true);
@@ -361,24 +379,20 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
         mma_bf16(tmem + kTW, sdesc_sw128(sKQ + ks * 2048, 16384, 1024),
-                 sdesc_sw128(sA + part * 8192 + ks * 2048, 8192, 1024), id_mn, (part | ks) > 0);
+                 sdesc_sw128(sKQ + 8192 + part * 16384 + ks * 2048, 8192, 1024), id_mn, (part | ks) > 0);
 #pragma unroll
     for (int part = 0; part < 2; ++part)
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
         mma_bf16(tmem + kTU, sdesc_sw128(sV + ks * 2048, 8192, 1024),
-                 sdesc_sw128(sA + 16384 + part * 8192 + ks * 2048, 8192, 1024), id_mn, (part | ks) > 0);
+                 sdesc_sw128(sF + part * 8192 + ks * 2048, 8192, 1024), id_mn, (part | ks) > 0);
     mma_commit(&ctl->wu);
-  } else if (tid == 64) {  // the parts of the record that are final already
-    bulk_store(rec + kRecP, sm + kWyP, 8192);
-    bulk_store(rec + kRecGam, sGam, 512);  // exp(G) then exp(G_63 - G)
-    bulk_commit();
   }
   ok = wait_phase(&ctl->wu, 0, &ctl->abort, 102);
   if (__syncthreads_or(!ok)) return false;
   tc_fence_after();
 
-  // ---- -W and U^T tiles (over the A operands and V, which the MMAs have consumed) ----
+  // ---- -W and U^T tiles (over A diag(beta) and V, which the MMAs have consumed) ----
   {
     const int d = (warp & 3) * 32 + lane, ch = warp >> 2;
     uint32_t ra[16], rb[16];
@@ -390,7 +404,7 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
       float f[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) f[e] = -__uint_as_float(q < 2 ? ra[8 * q + e] : rb[8 * (q - 2) + e]);
-      store_f16x8_m(sA + sw128_offset(d, ch * 4 + q), f, mx);
+      store_f16x8_m(sF + sw128_offset(d, ch * 4 + q), f, mx);
     }
     tmem_ld16(tmem + lane_base + kTU + ch * 32, ra);
     tmem_ld16(tmem + lane_base + kTU + ch * 32 + 16, rb);
@@ -407,14 +421,14 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
   tc_fence_before();
   __syncthreads();
   if (tid == 64) {
-    bulk_store(rec + kRecWn, sm + kWyA, 16384);
+    bulk_store(rec + kRecWn, sm + kWyF, 16384);
     bulk_store(rec + kRecU, sm + kWyV, 16384);
     bulk_commit();
   }
   return true;
 }
 
-__global__ void __launch_bounds__(kWyThreads, 2)
+__global__ void __launch_bounds__(kWyThreads, 3)
     wy_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
               const __grid_constant__ CUtensorMap mv, const Problem p) {
   extern __shared__ uint8_t smem_raw[];
