@@ -7,12 +7,12 @@
 // so the start states follow by a serial scan over the segments of a
 // sequence:  S_start(0) = h0^T,  S_start(s+1) = S_start(s) R_s + S_loc,s.
 // Rows of S are independent, so each CTA owns 8 rows of one (sequence, head)
-// and streams R_s and its 8 rows of S_loc,s through shared memory (cp.async,
-// one segment ahead) while it does the fp32 products.  Each warp takes a
+// and streams R_s and its 8 rows of S_loc,s through shared memory (bulk
+// copies, one segment ahead) while it does the fp32 products.  Each warp takes a
 // 16-row slice of R for all 8 rows (so R is read from shared memory once per
 // segment), and the 8 partial sums are added in a second pass.  The CTA of row block 0 also
 // records the mode the (sequence, head) takes and its warmup bound.
-#include "gdn_internal.cuh"
+#include "gdn_dev.cuh"
 
 namespace gdn {
 namespace {
@@ -21,17 +21,6 @@ constexpr int kRows = 8;  // state rows per CTA
 constexpr int kSlices = 8;  // k slices of 16 (one per warp)
 constexpr int kCombineSmem = 2 * kDim * kDim * 4 + 2 * kRows * kDim * 4 + kRows * kDim * 4 + kSlices * kRows * kDim * 4;
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)),
-               "l"(gmem)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
   extern __shared__ float4 csm4[];
   float* sR = reinterpret_cast<float*>(csm4);  // [2][128*128]
@@ -39,6 +28,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
   float* sX = sL + 2 * kRows * kDim;           // [kRows][128]
   float* sP = sX + kRows * kDim;               // [kSlices][kRows][128] partial sums
   __shared__ SegInfo s_seq;
+  __shared__ uint64_t s_bar[2];
   const int tid = threadIdx.x, warp = tid >> 5;
   const int n = blockIdx.x, j = blockIdx.y, r0 = blockIdx.z * kRows;
   if (warp == 0) {
@@ -56,6 +46,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
   }
   if (mode != kModeExact || si.n_seg <= 1) return;
 
+  if (tid == 0) {
+    mbar_init(&s_bar[0], 1);
+    mbar_init(&s_bar[1], 1);
+    fence_mbar_init();
+  }
   const int rr = tid >> 5;         // row within the block
   const int c4 = (tid & 31) * 4;   // 4 output columns
   const size_t mat = (size_t)kDim * kDim;
@@ -68,27 +63,29 @@ __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
   const bool skip_first = p.h0 == nullptr;  // R_0 is not produced for a zero start: skip its product
   const int first_product = skip_first ? 1 : 0;
   const int last = si.n_seg - 2;  // produce S_start(1 .. n_seg-1)
-  auto prefetch = [&](int s) {
+  auto prefetch = [&](int s) {     // one thread; buffer s & 1 was last read in step s - 2
     const int buf = s & 1;
-    if (s >= first_product) {
-      const float* src = p.R + ((size_t)(si.seg_base + s) * p.h_v + j) * mat;
-      float* dst = sR + buf * mat;
-      for (int i = tid; i < kDim * kDim / 4; i += 256) cp_async16(dst + 4 * i, src + 4 * i);
-    }
-    const float* lsrc = p.Sloc + ((size_t)(si.seg_base + s) * p.h_v + j) * mat + (size_t)r0 * kDim;
-    cp_async16(sL + buf * kRows * kDim + 4 * tid, lsrc + 4 * tid);  // kRows * kDim / 4 == 256 vectors
-    cp_async_commit();
+    const bool product = s >= first_product;
+    mbar_arrive_expect_tx(&s_bar[buf], (uint32_t)(kRows * kDim * 4) + (product ? (uint32_t)(mat * 4) : 0u));
+    if (product)
+      bulk_load(sR + buf * mat, p.R + ((size_t)(si.seg_base + s) * p.h_v + j) * mat, (uint32_t)(mat * 4), &s_bar[buf]);
+    bulk_load(sL + buf * kRows * kDim, p.Sloc + ((size_t)(si.seg_base + s) * p.h_v + j) * mat + (size_t)r0 * kDim,
+              (uint32_t)(kRows * kDim * 4), &s_bar[buf]);
   };
-  prefetch(0);
+  __syncthreads();  // barriers initialised, S_start(0) rows in place
+  if (tid == 0) prefetch(0);
   for (int s = 0; s <= last; ++s) {
     const bool product = s >= first_product;
-    if (s + 1 <= last) {
-      prefetch(s + 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+    if (tid == 0 && s + 1 <= last) prefetch(s + 1);
+    const bool ok = mbar_wait(&s_bar[s & 1], (uint32_t)((s >> 1) & 1), kWaitLimitNs);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) report(p.status, kDevTimeout, kDetTmaWait);
+      // let copies already in flight land before the memory is released
+      const uint64_t t_start = globaltimer_ns();
+      while (globaltimer_ns() - t_start < 2000000ull) {
+      }
+      return;
     }
-    __syncthreads();
     const float4 l4 = *reinterpret_cast<const float4*>(sL + (s & 1) * kRows * kDim + rr * kDim + c4);
     float a0 = l4.x, a1 = l4.y, a2 = l4.z, a3 = l4.w;
     if (product) {
