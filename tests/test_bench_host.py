@@ -22,6 +22,15 @@ def test_algorithmic_counts_match_hand_figures():
     assert abs(fl / 1e9 - 41.16) < 0.05
 
 
+def test_kernel_bytes_partition_the_layer_bytes():
+    # the WY kernel's reads plus the output scan's writes are exactly the layer's algorithmic bytes
+    for kw in (dict(with_h0=False), dict(with_h0=True)):
+        w = make_inputs(4096, h_qk=2, h_v=8, seed=1, **kw)
+        by, _ = bench.algorithmic(w)
+        assert bench.kernel_bytes("wy", w) + bench.kernel_bytes("scan_out", w) == by
+        assert bench.kernel_bytes("combine", w) == bench.kernel_bytes("scan_prep", w) == 0
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))
