@@ -141,8 +141,8 @@ gdn_status encode_map(CUtensorMap* m, const void* base, int heads, int64_t token
 }
 
 // ---- fixed device workspace for callers that cannot allocate ----
-// 8 MiB: every CP-off plan (status word, head modes and segment bounds only)
-// and CP plans of up to 42 (segment, value head) pairs (192 KiB each).
+// 8 MiB: small problems only (the chunk records take 41472 bytes per
+// (chunk, value head) and 32768 per (chunk, query/key head)).
 constexpr size_t kStaticWorkspaceBytes = size_t(8) << 20;
 static __device__ __align__(256) uint8_t g_static_workspace[kStaticWorkspaceBytes];
 void* g_static_ws_dev[kMaxDevices] = {};

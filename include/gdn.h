@@ -207,9 +207,10 @@ gdn_status gdn_cp_head_modes(const void* workspace, const gdn_cp_plan_t* plan, i
  * takes the same arguments as gdn_chunk_fwd minus the workspace and uses a
  * fixed 8 MiB device array built into the library instead; every GPU that
  * loads the library holds that array until the process exits.
- *   - Fits every GDN_CP_OFF plan and context-parallel plans whose
- *     plan->workspace_bytes is at most 8 MiB (about 42 (segment, value head)
- *     pairs); larger plans are rejected with GDN_ERR_WORKSPACE before any
+ *   - Fits plans whose plan->workspace_bytes is at most 8 MiB: the chunk
+ *     records take 41472 bytes per (chunk, value head) and 32768 per (chunk,
+ *     query/key head), so about 150 chunk-heads (e.g. 1000 tokens with 6 value
+ *     heads); larger plans are rejected with GDN_ERR_WORKSPACE before any
  *     device work.
  *   - Allocates nothing.  Its first call on a device looks up the array's
  *     device address (cudaGetSymbolAddress) with that device current; make
