@@ -214,6 +214,40 @@ def time_gpu(name, steps, warmup, device, cp="auto", lambda_=0.0, trace=True):
             "modes": modes.flatten().tolist(), "tokens": w.T}
 
 
+DECODE_BATCH = (256, 2, 8)  # sequences, h_qk, h_v: one token each; 268 MB of state read and written per step
+
+
+def time_decode(steps, warmup, device, hbm):
+    """The one-token step over a batch of states (gdn_decode_step), L2 flushed
+    before each step; HBM roofline on its bytes (state read + written, q/k/v/o)."""
+    from gated_deltanet_linear_fwd_gb300 import gdn_decode_step
+    from gated_deltanet_linear_fwd_gb300.inputs import make_inputs
+    B, hqk, hv = DECODE_BATCH
+    w = make_inputs(cu_seqlens=list(range(B + 1)), h_qk=hqk, h_v=hv, seed=5, with_h0=True)
+    d = w.to(device)
+    state = d.h0.clone()
+    out = torch.empty_like(d.v)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(warmup):
+        flush.zero_()
+        gdn_decode_step(d.q, d.k, d.v, d.g, d.beta, state, out=out)
+    times = []
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(steps):
+        flush.zero_()
+        s0.record(stream)
+        gdn_decode_step(d.q, d.k, d.v, d.g, d.beta, state, out=out)
+        s1.record(stream)
+        s1.synchronize()
+        times.append(s0.elapsed_time(s1))
+    ms = statistics.mean(times)
+    by = B * hv * D * D * 4 * 2 + B * (2 * hqk * D + 2 * hv * D) * 2 + B * hv * 8
+    return {"batch": B, "h_qk": hqk, "h_v": hv, "ms": ms, "tokens_per_s": B / (ms * 1e-3), "bytes": by,
+            "achieved_gbs": by / (ms * 1e-3) / 1e9, "peak_gbs": hbm, "frac": by / (ms * 1e-3) / 1e9 / hbm,
+            "dtype": "bf16 q/k/v/o, fp32 state"}
+
+
 def time_e2e(name, steps, warmup, device, cp="auto"):
     """The same forward through the public call from pinned host buffers."""
     from gated_deltanet_linear_fwd_gb300 import gdn_chunk_fwd, gdn_cp_plan
@@ -405,6 +439,8 @@ def main(argv=None):
             if name in PAGES_H200_MS:
                 sweep[name]["pages_h200_ms"] = PAGES_H200_MS[name]
         line["sweep"] = sweep
+    if not args.no_sweep and rank == 0:
+        line["decode"] = time_decode(max(20, args.steps // 10), 5, device, hbm)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(HEADLINE)
     if rank == 0:

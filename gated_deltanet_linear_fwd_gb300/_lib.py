@@ -90,6 +90,8 @@ def load(path: str = LIB_PATH):
         lib.gdn_chunk_fwd_static.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(gdn_dims),
                                              ctypes.POINTER(gdn_cp_plan_t), vp]
         lib.gdn_chunk_fwd_static.restype = ctypes.c_int
+        lib.gdn_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(gdn_dims), vp]
+        lib.gdn_decode_step.restype = ctypes.c_int
         lib.gdn_set_trace_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
         lib.gdn_set_trace_events.restype = ctypes.c_int
         lib.gdn_trace_last.argtypes = [ctypes.POINTER(ctypes.c_char_p), ctypes.c_int]

@@ -112,6 +112,26 @@ def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
     return out, final_state
 
 
+def gdn_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+                    state: torch.Tensor, *, out: Optional[torch.Tensor] = None, scale: float = 0.0, stream=None):
+    """One new token per sequence (gdn_decode_step): q,k [B,h_qk,128], v [B,h_v,128]
+    (bf16 or fp32), g,beta [B,h_v] fp32, state [B,h_v,128,128] fp32 (H = S^T,
+    updated in place).  Returns o [B,h_v,128]."""
+    B, h_qk, h_v = q.shape[0], q.shape[1], v.shape[1]
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("state", state)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if g.dtype != torch.float32 or beta.dtype != torch.float32 or state.dtype != torch.float32:
+        raise ValueError("g, beta and state must be float32")
+    if out is None:
+        out = torch.empty_like(v)
+    dims = L.gdn_dims(B, 1, h_qk, h_v, q.shape[-1], v.shape[-1], B, scale, _DT.get(q.dtype, -1))
+    st = L.load().gdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(out),
+                                  ctypes.byref(dims), _stream_handle(stream))
+    L.check(st, "gdn_decode_step")
+    return out
+
+
 def gdn_get_device_status(workspace: torch.Tensor, stream=None):
     """(code, detail) of the status word of the last call on this workspace (synchronises)."""
     code, detail = ctypes.c_int(), ctypes.c_int()

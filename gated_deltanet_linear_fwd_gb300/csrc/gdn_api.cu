@@ -396,6 +396,36 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
   return GDN_OK;
 }
 
+gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                           float* state, void* out, const gdn_dims* dims, void* stream) {
+  gdn_status st = check_dims(dims);
+  if (st != GDN_OK) return st;
+  if (dims->T != 1 || dims->n_seqs != dims->B) return GDN_ERR_INVALID_ARG;
+  if (!q || !k || !v || !g || !beta || !state || !out) return GDN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) || !aligned16(state) ||
+      !aligned16(out))
+    return GDN_ERR_MISALIGNED;
+  if (dims->B > 65535 * 32768) return GDN_ERR_INVALID_ARG;
+  DecodeArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.g = g;
+  a.beta = beta;
+  a.state = state;
+  a.out = out;
+  a.n_seqs = dims->B;
+  a.h_qk = dims->h_qk;
+  a.h_v = dims->h_v;
+  a.scale = dims->scale != 0.f ? dims->scale : 1.0f / std::sqrt((float)dims->d_k);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  LaunchLog log{cs};
+  cudaError_t e = log.begin();
+  if (e == cudaSuccess) e = launch_decode(a, dims->dtype == GDN_F32, cs);
+  if (e == cudaSuccess) e = log.after("decode");
+  return e == cudaSuccess ? GDN_OK : cuda_fail(e);
+}
+
 gdn_status gdn_set_trace_events(void* const* events, int n_events) {
   if (n_events < 0 || n_events > kMaxTrace) return GDN_ERR_INVALID_ARG;
   if (!events) n_events = 0;

@@ -77,6 +77,19 @@ struct Problem {
   uint8_t* kq16;            // [n_chunks_total, h_qk] records of kKqRecBytes
 };
 
+// Arguments of the one-token step (gdn_decode_step).
+struct DecodeArgs {
+  const void* q;   // [n_seqs, h_qk, 128]
+  const void* k;   // [n_seqs, h_qk, 128]
+  const void* v;   // [n_seqs, h_v, 128]
+  const float* g;  // [n_seqs, h_v]
+  const float* beta;
+  float* state;    // [n_seqs, h_v, 128, 128] (H = S^T), updated in place
+  void* out;       // [n_seqs, h_v, 128]
+  int n_seqs, h_qk, h_v;
+  float scale;
+};
+
 __device__ __forceinline__ void report(int* status, int code, int detail) {
   if (atomicCAS(status, 0, code) == 0) atomicExch(status + 1, detail);
 }
@@ -189,6 +202,7 @@ cudaError_t launch_scan_prep(const Problem& p, cudaStream_t st);
 cudaError_t launch_combine(const Problem& p, cudaStream_t st);
 cudaError_t launch_scan_out(const Problem& p, int grid_x, cudaStream_t st);
 cudaError_t launch_recurrence_f32(const Problem& p, cudaStream_t st);
+cudaError_t launch_decode(const DecodeArgs& a, bool f32, cudaStream_t st);
 cudaError_t scan_kernel_setup();
 cudaError_t wy_kernel_setup();
 cudaError_t combine_kernel_setup();

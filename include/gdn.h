@@ -229,6 +229,29 @@ gdn_status gdn_chunk_fwd_static(const void* q, const void* k, const void* v, con
                                 const gdn_dims* dims, const gdn_cp_plan_t* plan, void* stream);
 
 /*
+ * gdn_decode_step -- one new token for each of a batch of sequences: the
+ * recurrence step itself [GDN, "Gated delta rule"], the generation-time
+ * counterpart of gdn_chunk_fwd.  Per sequence n and value head j (q/k head
+ * floor(j * h_qk / h_v)):
+ *   S <- exp(g) S (I - beta k k^T) + beta v k^T,   o = scale * S q,
+ * with the state stored as H = S^T like initial_state/final_state, so the
+ * final_state of a prefill continues here directly.  fp32 arithmetic on the
+ * CUDA cores; asynchronous on `stream`.
+ *   q, k  : device, [B, h_qk, d_k], dims->dtype.
+ *   v     : device, [B, h_v, d_v], dims->dtype.
+ *   g, beta: device, [B, h_v] fp32.
+ *   state : device, [B, h_v, d_k, d_v] fp32; read, then overwritten with the
+ *           new state.
+ *   out   : device, [B, h_v, d_v], dims->dtype (bf16 rounded to nearest even).
+ *   dims  : B sequences, T must be 1, n_seqs must equal B; d_k = d_v = 128.
+ * No workspace.  out may not overlap the inputs or the state.
+ * Errors: INVALID_ARG (null pointer, T != 1, n_seqs != B), UNSUPPORTED,
+ * MISALIGNED (16 bytes), CUDA (launch failure).
+ */
+gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                           float* state, void* out, const gdn_dims* dims, void* stream);
+
+/*
  * gdn_set_trace_events -- optional per-kernel timing (tracing).  Registers,
  * for the calling host thread, up to 16 caller-created cudaEvent_t handles.
  * While registered, each gdn_chunk_fwd on this thread records events[0] on

@@ -139,6 +139,20 @@ def test_chunk_fwd_rejects_before_device_work(lib):
     assert f(A, A, A, A, A, None, None, A, None, ctypes.byref(dims3), ctypes.byref(p), A, ws, None) == 2
 
 
+def test_decode_step_rejects_before_device_work(lib):
+    from gated_deltanet_linear_fwd_gb300 import _lib as L
+    A = ctypes.c_void_p(0x100000)  # never dereferenced: every case fails a host check first
+    U = ctypes.c_void_p(0x100008)  # not 16-byte aligned
+    f = lib.gdn_decode_step
+    ok = L.gdn_dims(4, 1, 2, 8, 128, 128, 4, 0.0, 0)
+    assert f(A, A, A, A, A, A, A, None, None) == 1                                    # null dims
+    assert f(A, A, A, A, A, A, A, ctypes.byref(L.gdn_dims(4, 2, 2, 8, 128, 128, 4, 0.0, 0)), None) == 1  # T != 1
+    assert f(A, A, A, A, A, A, A, ctypes.byref(L.gdn_dims(4, 1, 2, 8, 128, 128, 3, 0.0, 0)), None) == 1  # n_seqs != B
+    assert f(A, A, A, A, A, None, A, ctypes.byref(ok), None) == 1                     # null state
+    assert f(A, A, A, A, A, A, U, ctypes.byref(ok), None) == 3                        # misaligned out
+    assert f(A, A, A, A, A, A, A, ctypes.byref(L.gdn_dims(4, 1, 2, 8, 64, 128, 4, 0.0, 0)), None) == 2  # d_k
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     from gated_deltanet_linear_fwd_gb300 import _lib as L
     saved = L._lib
