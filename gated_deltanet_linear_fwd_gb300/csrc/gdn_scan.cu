@@ -250,10 +250,16 @@ __device__ __noinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p,
   const int n = ch.run_end - ch.run_begin;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   const uint32_t sS = smem_u32(sm + kSmS), sVp = smem_u32(sm + kSmVp), sVd = smem_u32(sm + kSmVd);
-  float mx = 0.f;  // largest magnitude rounded to fp16 by this thread
+  // Largest magnitude this thread rounds to fp16: V' is checked every chunk
+  // (|V' dec| <= |V'|); the state only at the end, since an fp16 overflow of
+  // its operand copy would turn the next V' and so the state into inf/NaN.
+  float mx = 0.f;
   auto store_state = [&]() {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) store_f16x8_m(sS + half * 16384 + sw128_offset(row, q), &S[8 * q], mx);
+    for (int q = 0; q < 8; ++q)
+      st_shared_v4(sS + half * 16384 + sw128_offset(row, q), pack_f16x2(S[8 * q], S[8 * q + 1]),
+                   pack_f16x2(S[8 * q + 2], S[8 * q + 3]), pack_f16x2(S[8 * q + 4], S[8 * q + 5]),
+                   pack_f16x2(S[8 * q + 6], S[8 * q + 7]));
   };
   store_state();
   fence_proxy_async_smem();
@@ -280,11 +286,13 @@ __device__ __noinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p,
         const float4 d0 = lds_f32x4(da), d1 = lds_f32x4(da + 16);
         const float d[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
         const uint32_t off = sw128_offset(row, half * 4 + g2 * 2 + q);
-        if (out) store_f16x8_m(sVp + off, f, mx);
-        float fd[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) fd[e] = f[e] * d[e];
-        store_f16x8_m(sVd + off, fd, mx);
+        for (int e = 0; e < 8; ++e) mx = absmax_nan(mx, f[e]);
+        if (out)
+          st_shared_v4(sVp + off, pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
+                       pack_f16x2(f[6], f[7]));
+        st_shared_v4(sVd + off, pack_f16x2(f[0] * d[0], f[1] * d[1]), pack_f16x2(f[2] * d[2], f[3] * d[3]),
+                     pack_f16x2(f[4] * d[4], f[5] * d[5]), pack_f16x2(f[6] * d[6], f[7] * d[7]));
       }
     }
     fence_proxy_async_smem();
@@ -347,6 +355,8 @@ __device__ __noinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p,
     mbar_arrive(&ctl->bar[kYoFree0 + (i & 1)]);  // Y/O2 buffer i & 1 and gates slot i & 3 read
     done = i + 1;
   }
+#pragma unroll
+  for (int e = 0; e < 64; ++e) mx = absmax_nan(mx, S[e]);
   if (!(mx < 65504.f)) atomicExch(&ctl->range_bad, 1);
   if (done < n || *reinterpret_cast<volatile int*>(&ctl->abort)) return;  // no results from an aborted chain
   if (PREP) {

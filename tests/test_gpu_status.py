@@ -1,0 +1,45 @@
+"""The device status word: values outside the fp16 range of the MMA
+operands are reported (status 7, detail 5) rather than silently rounded to
+inf, and ordinary inputs report nothing."""
+from __future__ import annotations
+
+import dataclasses
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU, skipped there
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from gated_deltanet_linear_fwd_gb300 import gdn_chunk_fwd, gdn_cp_plan, gdn_get_device_status  # noqa: E402
+from gated_deltanet_linear_fwd_gb300.inputs import make_inputs  # noqa: E402
+
+DEVICE_CHECK, FP16_RANGE = 7, 5
+
+
+def _status(w, mode="exact"):
+    d = w.to("cuda:0")
+    plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, cu_seqlens=w.cu_seqlens, mode=mode, lambda_=0.5)
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device="cuda:0")
+    gdn_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, plan=plan, workspace=ws)
+    return gdn_get_device_status(ws)
+
+
+@pytest.mark.parametrize("mode", ["off", "exact"])
+def test_ordinary_inputs_report_nothing(mode):
+    assert _status(make_inputs(700, h_qk=2, h_v=4, seed=3, with_h0=True), mode) == (0, 0)
+
+
+@pytest.mark.parametrize("mode", ["off", "exact"])
+def test_values_past_fp16_range_are_reported(mode):
+    w = make_inputs(700, h_qk=2, h_v=4, seed=3)
+    w = dataclasses.replace(w, v=(w.v.float() * 1e6).to(torch.bfloat16))  # U = A diag(beta) V far beyond 65504
+    assert _status(w, mode) == (DEVICE_CHECK, FP16_RANGE)
+
+
+def test_state_past_fp16_range_is_reported():
+    w = make_inputs(700, h_qk=2, h_v=4, seed=3, with_h0=True, g_kind="zero")
+    w = dataclasses.replace(w, h0=w.h0 * 1e7)  # the state's fp16 operand copy overflows
+    assert _status(w, "off") == (DEVICE_CHECK, FP16_RANGE)
