@@ -141,45 +141,41 @@ __device__ __forceinline__ void solve_unit_lower(float* F, float* scratch, int t
     }
     __syncthreads();
   }
-  // ---- level 2: T = L_hl A_ll (32 x 32), then A_hl = -A_hh T ----
+  // ---- level 2: T = L_hl A_ll (32 x 32), then A_hl = -A_hh T.  Each warp
+  //      takes four columns of T (four rows of A_hl), so the triangular
+  //      bounds of A_ll and A_hh are the same across the warp ----
   {
-    const int r0 = (tid >> 4) * 2, c0 = (tid & 15) * 2;
+    const int w = tid >> 5, lane = tid & 31;
     float* Tb = scratch;  // [32][32]
     {
-      const float* L0 = F + (32 + r0) * kFStride;  // L[32 + r0][0..31]
-      const float* L1 = L0 + kFStride;
-      const float* A0 = F + c0 * kFStride;         // A_ll[.][c0] as row c0 of A^T
-      const float* A1 = A0 + kFStride;
-      float t00 = 0.f, t01 = 0.f, t10 = 0.f, t11 = 0.f;
+      // T[lane][4w .. 4w+3] = sum_{m >= 4w} L[32 + lane][m] A_ll[m][c]   (A_ll[m][c] = 0 for m < c)
+      const float* Lr = F + (32 + lane) * kFStride;
+      float t[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+      for (int m = 4 * w; m < 32; m += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(Lr + m);
 #pragma unroll
-      for (int m = 0; m < 32; m += 4) {
-        const float4 l0 = *reinterpret_cast<const float4*>(L0 + m);
-        const float4 l1 = *reinterpret_cast<const float4*>(L1 + m);
-        const float4 a0 = *reinterpret_cast<const float4*>(A0 + m);
-        const float4 a1 = *reinterpret_cast<const float4*>(A1 + m);
-        t00 = fmaf(l0.x, a0.x, fmaf(l0.y, a0.y, fmaf(l0.z, a0.z, fmaf(l0.w, a0.w, t00))));
-        t01 = fmaf(l0.x, a1.x, fmaf(l0.y, a1.y, fmaf(l0.z, a1.z, fmaf(l0.w, a1.w, t01))));
-        t10 = fmaf(l1.x, a0.x, fmaf(l1.y, a0.y, fmaf(l1.z, a0.z, fmaf(l1.w, a0.w, t10))));
-        t11 = fmaf(l1.x, a1.x, fmaf(l1.y, a1.y, fmaf(l1.z, a1.z, fmaf(l1.w, a1.w, t11))));
+        for (int c = 0; c < 4; ++c) {
+          const float4 a4 = *reinterpret_cast<const float4*>(F + (4 * w + c) * kFStride + m);  // A_ll[m..m+3][4w+c]
+          t[c] = fmaf(l4.x, a4.x, fmaf(l4.y, a4.y, fmaf(l4.z, a4.z, fmaf(l4.w, a4.w, t[c]))));
+        }
       }
-      *reinterpret_cast<float2*>(Tb + r0 * 32 + c0) = make_float2(t00, t01);
-      *reinterpret_cast<float2*>(Tb + (r0 + 1) * 32 + c0) = make_float2(t10, t11);
+      *reinterpret_cast<float4*>(Tb + lane * 32 + 4 * w) = make_float4(t[0], t[1], t[2], t[3]);
     }
     __syncthreads();
     {
-      float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
-      const int m_end = r0 + 2;  // A_hh[r][m] = 0 for m > r
+      // A_hl[4w .. 4w+3][lane] = -sum_{m <= 4w+3} A_hh[r][m] T[m][lane]   (A_hh[r][m] = 0 for m > r)
+      float x[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
-      for (int m = 0; m < m_end; ++m) {
-        const float2 a = *reinterpret_cast<const float2*>(F + (32 + m) * kFStride + 32 + r0);  // A_hh[r0..r0+1][m]
-        const float2 t = *reinterpret_cast<const float2*>(Tb + m * 32 + c0);
-        x00 = fmaf(a.x, t.x, x00);
-        x01 = fmaf(a.x, t.y, x01);
-        x10 = fmaf(a.y, t.x, x10);
-        x11 = fmaf(a.y, t.y, x11);
+      for (int m = 0; m < 4 * w + 4; ++m) {
+        const float4 a4 = *reinterpret_cast<const float4*>(F + (32 + m) * kFStride + 32 + 4 * w);  // A_hh[4w..4w+3][m]
+        const float tv = Tb[m * 32 + lane];
+        x[0] = fmaf(a4.x, tv, x[0]);
+        x[1] = fmaf(a4.y, tv, x[1]);
+        x[2] = fmaf(a4.z, tv, x[2]);
+        x[3] = fmaf(a4.w, tv, x[3]);
       }
-      *reinterpret_cast<float2*>(F + c0 * kFStride + 32 + r0) = make_float2(-x00, -x10);
-      *reinterpret_cast<float2*>(F + (c0 + 1) * kFStride + 32 + r0) = make_float2(-x01, -x11);
+      *reinterpret_cast<float4*>(F + lane * kFStride + 32 + 4 * w) = make_float4(-x[0], -x[1], -x[2], -x[3]);
     }
     __syncthreads();
   }
@@ -290,17 +286,32 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
       const int r = R;
       const float br = sBeta[r], Gr = sG[r], brE = sBeta[r] * sGam[r];
       float* Lr = F + r * kFStride + ch * 32;
+      if (factored) {  // separate loops: a select between the two would evaluate both
 #pragma unroll
-      for (int s4 = 0; s4 < 32; s4 += 4) {
-        float4 o4;
-        float* o = &o4.x;
+        for (int s4 = 0; s4 < 32; s4 += 4) {
+          const float4 em = *reinterpret_cast<const float4*>(sEm + ch * 32 + s4);
+          const float* emv = &em.x;
+          float4 o4;
+          float* o = &o4.x;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int sl = s4 + e, s = ch * 32 + sl;
-          const float d = __uint_as_float(rk[sl >> 4][sl & 15]);
-          o[e] = (s < r) ? (factored ? brE * d * sEm[s] : br * d * __expf(Gr - sG[s])) : 0.f;
+          for (int e = 0; e < 4; ++e) {
+            const int sl = s4 + e;
+            o[e] = (ch * 32 + sl < r) ? brE * __uint_as_float(rk[sl >> 4][sl & 15]) * emv[e] : 0.f;
+          }
+          *reinterpret_cast<float4*>(Lr + s4) = o4;
         }
-        *reinterpret_cast<float4*>(Lr + s4) = o4;
+      } else {
+#pragma unroll
+        for (int s4 = 0; s4 < 32; s4 += 4) {
+          float4 o4;
+          float* o = &o4.x;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int sl = s4 + e, s = ch * 32 + sl;
+            o[e] = (s < r) ? br * __uint_as_float(rk[sl >> 4][sl & 15]) * __expf(Gr - sG[s]) : 0.f;
+          }
+          *reinterpret_cast<float4*>(Lr + s4) = o4;
+        }
       }
     } else {
       const int r = R - 64;
@@ -308,11 +319,21 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         float f[8];
+        if (factored) {
+          const float4 e0 = *reinterpret_cast<const float4*>(sEm + ch * 32 + 8 * q);
+          const float4 e1 = *reinterpret_cast<const float4*>(sEm + ch * 32 + 8 * q + 4);
+          const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int sl = 8 * q + e, s = ch * 32 + sl;
-          const float d = __uint_as_float(rk[sl >> 4][sl & 15]);
-          f[e] = (s <= r) ? (factored ? d * Er * sEm[s] : d * __expf(Gr - sG[s])) : 0.f;
+          for (int e = 0; e < 8; ++e) {
+            const int sl = 8 * q + e;
+            f[e] = (ch * 32 + sl <= r) ? __uint_as_float(rk[sl >> 4][sl & 15]) * Er * ev[e] : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int sl = 8 * q + e, s = ch * 32 + sl;
+            f[e] = (s <= r) ? __uint_as_float(rk[sl >> 4][sl & 15]) * __expf(Gr - sG[s]) : 0.f;
+          }
         }
 #pragma unroll
         for (int e = 0; e < 8; ++e) mx = absmax_nan(mx, f[e]);
