@@ -70,7 +70,7 @@ def algorithmic(w):
 # the WY kernel writes and the scans read back, the context-parallel
 # transitions and the combine are overhead and count zero.
 KERNEL_SOURCE = {"wy": "gdn_wy.cu", "scan_out": "gdn_scan.cu", "scan_prep": "gdn_scan.cu",
-                 "combine": "gdn_combine.cu", "gate_bound": "gdn_gate.cu", "chunk_map": "gdn_wy.cu"}
+                 "combine": "gdn_combine.cu", "chunk_map": "gdn_wy.cu"}
 
 
 def kernel_bytes(name, w):

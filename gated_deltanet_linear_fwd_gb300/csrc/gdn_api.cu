@@ -268,8 +268,9 @@ gdn_status gdn_cp_plan(const gdn_dims* dims, const int32_t* cu, const gdn_cp_opt
     off += segheads * mat;
   }
   if (dims->dtype == GDN_BF16) {
-    p.off_chunk_map = off;
-    off = align_up(off + ((size_t)dims->n_seqs + 1 + (size_t)n_chunks_total) * 4, 1024);
+    p.off_chunk_map = off;  // chunk index, then the chunk warmup exponents
+    off = align_up(off + ((size_t)dims->n_seqs + 1 + (size_t)n_chunks_total) * 4, 256);
+    off = align_up(off + (size_t)n_chunks_total * dims->h_v * 4, 1024);
     p.off_wy = off;
     off += (size_t)n_chunks_total * dims->h_v * kRecBytes;
     p.off_kq16 = off;
@@ -346,6 +347,8 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
   if (dims->dtype == GDN_BF16) {
     p.seq_chunk_base = reinterpret_cast<int32_t*>(ws + plan->off_chunk_map);
     p.chunk_seq = p.seq_chunk_base + dims->n_seqs + 1;
+    p.chunk_exp = reinterpret_cast<float*>(
+        ws + align_up(plan->off_chunk_map + ((size_t)dims->n_seqs + 1 + (size_t)plan->n_chunks_total) * 4, 256));
     p.wy = ws + plan->off_wy;
     p.kq16 = ws + plan->off_kq16;
   }
@@ -379,10 +382,6 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
   if ((e = log.begin()) != cudaSuccess) return cuda_fail(e);
   if ((e = launch_chunk_map(p, cs)) != cudaSuccess) return cuda_fail(e);
   if ((e = log.after("chunk_map")) != cudaSuccess) return cuda_fail(e);
-  if (plan->mode == GDN_CP_WARMUP) {
-    if ((e = launch_gate_bound(p, cs)) != cudaSuccess) return cuda_fail(e);
-    if ((e = log.after("gate_bound")) != cudaSuccess) return cuda_fail(e);
-  }
   if ((e = launch_wy(p, mq, mk, mv, cs)) != cudaSuccess) return cuda_fail(e);
   if ((e = log.after("wy")) != cudaSuccess) return cuda_fail(e);
   if (plan->mode != GDN_CP_OFF) {

@@ -73,6 +73,8 @@ struct Problem {
   int n_chunks_total;
   int32_t* seq_chunk_base;  // [n_seqs + 1] global index of each sequence's first chunk
   int32_t* chunk_seq;       // [n_chunks_total] sequence of each chunk
+  float* chunk_exp;         // [n_chunks_total, h_v] warmup exponent of each chunk:
+                            // sum over its tokens of g + log max(1, |1 - beta ||k||^2|)
   uint8_t* wy;              // [n_chunks_total, h_v] records of kRecBytes
   uint8_t* kq16;            // [n_chunks_total, h_qk] records of kKqRecBytes
 };
@@ -176,6 +178,35 @@ __device__ inline void locate_sequence(const Problem& p, int n, SegInfo& out) {
   out.ce = out.n_chunks;
 }
 
+// Warmup depth of segment `cb` (its first chunk) of the sequence whose first
+// global chunk is chunk0 (FlashQLA pages, section "AutoCP": a fast-decaying
+// head restarts each segment from a few preceding chunks).  A restart from
+// zero w chunks early errs, relative to the state there, by at most
+// exp(sum of the window's chunk exponents), since each token map
+// X -> alpha X (I - beta k k^T) has spectral norm <= alpha max(1, |1 - beta
+// ||k||^2|).  The depth is the smallest w <= the planned maximum whose bound
+// is <= tol; a window reaching the sequence start is exact (bound -inf); no
+// such w gives -1 (the head runs exactly) with the full window's exponent.
+__device__ inline void seg_warmup_depth(const Problem& p, int chunk0, int cb, int j, int& w_out, float& b_out) {
+  const int nwin = min(p.warmup_chunks, cb);
+  float acc = 0.f;
+  for (int w = 1; w <= nwin; ++w) {
+    acc += p.chunk_exp[(size_t)(chunk0 + cb - w) * p.h_v + j];
+    if (cb - w == 0) {
+      w_out = w;
+      b_out = -__int_as_float(0x7f800000);
+      return;
+    }
+    if (acc <= p.log_tol) {
+      w_out = w;
+      b_out = acc;
+      return;
+    }
+  }
+  w_out = -1;
+  b_out = acc;
+}
+
 // Max of the per-segment warmup bounds of (sequence, head); -inf if none.
 __device__ inline float head_log_bound(const Problem& p, const SegInfo& si, int j) {
   float m = -__int_as_float(0x7f800000);
@@ -195,7 +226,6 @@ __device__ inline int head_mode_of(const Problem& p, const SegInfo& si, int j) {
 
 // ---- kernel launchers (defined in the .cu files) ----
 cudaError_t launch_chunk_map(const Problem& p, cudaStream_t st);
-cudaError_t launch_gate_bound(const Problem& p, cudaStream_t st);
 cudaError_t launch_wy(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                       cudaStream_t st);
 cudaError_t launch_scan_prep(const Problem& p, cudaStream_t st);

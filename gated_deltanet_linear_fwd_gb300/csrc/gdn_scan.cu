@@ -407,7 +407,31 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(const Problem p) {
   ch.has_u = true;
   ch.write_final = false;
   if (PREP) {
-    if (head_mode_of(p, si, j) != kModeExact || si.s == si.n_seg - 1) return;
+    if (p.plan_mode == kModeWarmup) {
+      // warmup depths of every segment of this (sequence, head) from the chunk
+      // exponents; the head runs exactly unless all of them found a depth.  The
+      // first CTA of each segment records its depth for the combine and the scan.
+      __shared__ int s_exact;
+      if (warp == 0) {
+        const int chunk0 = p.seq_chunk_base[si.n];
+        bool none = false;
+        for (int s2 = lane; s2 < si.n_seg; s2 += 32) {
+          int w = 0;
+          float b = -__int_as_float(0x7f800000);
+          if (s2 > 0) seg_warmup_depth(p, chunk0, seg_first(s2, si.n_chunks, si.n_seg), j, w, b);
+          none |= w < 0;
+          if (s2 == si.s && chain == 0) {
+            p.seg_w[(size_t)(si.seg_base + s2) * p.h_v + j] = w;
+            p.seg_bound[(size_t)(si.seg_base + s2) * p.h_v + j] = b;
+          }
+        }
+        none = __any_sync(0xffffffffu, none);
+        if (lane == 0) s_exact = none;
+      }
+      __syncthreads();
+      if (!s_exact) return;
+    }
+    if (si.s == si.n_seg - 1) return;
     if (chain == 0 && si.s == 0 && p.h0 == nullptr) return;  // M of segment 0 unused for a zero start
     ch.init = chain == 0 ? kInitIdentity : kInitZero;
     ch.has_u = chain == 1;
