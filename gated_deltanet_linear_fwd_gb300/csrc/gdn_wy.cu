@@ -256,26 +256,6 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
     sDec[r] = dec;
     reinterpret_cast<float*>(rec + kRecGam)[r] = sGam[r];  // the record's gates
     reinterpret_cast<float*>(rec + kRecGam)[64 + r] = dec;
-    if (p.plan_mode == kModeWarmup && wait_phase(&ctl->full, 0, &ctl->abort, 100)) {
-      // the chunk's warmup exponent: G_63 + sum_r log max(1, |1 - beta_r ||k_r||^2|)
-      float kk = 0.f;
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {  // row r of K: 8 swizzled 16-byte chunks in each 64-column half
-        const uint4 u = *reinterpret_cast<const uint4*>(sm + kWyKQ + (c >> 3) * 16384 + sw128_offset(r, c & 7));
-        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float lo = __uint_as_float(wv[e] << 16), hi = __uint_as_float(wv[e] & 0xffff0000u);
-          kk = fmaf(lo, lo, fmaf(hi, hi, kk));
-        }
-      }
-      float t = __logf(fmaxf(1.f, fabsf(1.f - b * kk)));  // 0 past the sequence end (beta = 0)
-#pragma unroll
-      for (int d = 16; d >= 1; d >>= 1) t += __shfl_xor_sync(0xffffffffu, t, d);
-      if (lane == 0) ctl->warp_total[warp - 2] = t;
-      named_bar_sync(1, 64);
-      if (r == 0) p.chunk_exp[(size_t)gc * p.h_v + j] = sG[63] + ctl->warp_total[0] + ctl->warp_total[1];
-    }
   }
   if (tid == 32) {
     if (wait_phase(&ctl->full, 0, &ctl->abort, 100)) {
@@ -302,6 +282,17 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
     tmem_ld16(tmem + lane_base + kTD + ch * 32, rk[0]);
     tmem_ld16(tmem + lane_base + kTD + ch * 32 + 16, rk[1]);
     tmem_ld_wait(rk[0], rk[1]);
+    if (p.plan_mode == kModeWarmup && R < 64 && (R >> 5) == ch) {  // warps 0 and 5 hold the diagonal
+      // the chunk's warmup exponent: G_63 + sum_r log max(1, |1 - beta_r ||k_r||^2|), ||k_r||^2 = D[r][r]
+      float kk = 0.f;
+#pragma unroll
+      for (int sl = 0; sl < 32; ++sl)
+        if (sl == (R & 31)) kk = __uint_as_float(rk[sl >> 4][sl & 15]);
+      float t = __logf(fmaxf(1.f, fabsf(1.f - sBeta[R] * kk)));  // 0 past the sequence end (beta = 0)
+#pragma unroll
+      for (int d = 16; d >= 1; d >>= 1) t += __shfl_xor_sync(0xffffffffu, t, d);
+      if (lane == 0) ctl->warp_total[ch] = t;
+    }
     if (R < 64) {
       const int r = R;
       const float br = sBeta[r], Gr = sG[r], brE = sBeta[r] * sGam[r];
@@ -364,6 +355,8 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
   }
   tc_fence_before();
   __syncthreads();
+  if (tid == 0 && p.plan_mode == kModeWarmup)
+    p.chunk_exp[(size_t)gc * p.h_v + j] = sG[63] + ctl->warp_total[0] + ctl->warp_total[1];
 
   // ---- A = (I + L)^{-1}; meanwhile threads 64-255 of the group's first CTA
   //      write the fp16 copy of K|Q (same byte layout, converted chunk by chunk) ----
