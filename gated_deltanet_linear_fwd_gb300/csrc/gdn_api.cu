@@ -387,7 +387,7 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
   if (plan->mode != GDN_CP_OFF) {
     if ((e = launch_scan_prep(p, cs)) != cudaSuccess) return cuda_fail(e);
     if ((e = log.after("scan_prep")) != cudaSuccess) return cuda_fail(e);
-    if ((e = launch_combine(p, cs)) != cudaSuccess) return cuda_fail(e);
+    if ((e = launch_combine(p, g_sm_count[dev], cs)) != cudaSuccess) return cuda_fail(e);
     if ((e = log.after("combine")) != cudaSuccess) return cuda_fail(e);
   }
   if ((e = launch_scan_out(p, plan->n_seg_total, cs)) != cudaSuccess) return cuda_fail(e);

@@ -6,21 +6,26 @@
 //     S_end = S_start R + S_loc,     R = M^T (d_k x d_k),
 // so the start states follow by a serial scan over the segments of a
 // sequence:  S_start(0) = h0^T,  S_start(s+1) = S_start(s) R_s + S_loc,s.
-// Rows of S are independent, so each CTA owns 8 rows of one (sequence, head)
-// and streams R_s and its 8 rows of S_loc,s through shared memory (bulk
+// Rows of S are independent, so each CTA owns 4 or 8 rows of one (sequence,
+// head) and streams R_s and its rows of S_loc,s through shared memory (bulk
 // copies, one segment ahead) while it does the fp32 products.  Each warp takes a
-// 16-row slice of R for all 8 rows (so R is read from shared memory once per
-// segment), and the 8 partial sums are added in a second pass.  The CTA of row block 0 also
+// 16-row slice of R for all the CTA's rows (so R is read from shared memory once
+// per segment), and the 8 partial sums are added in a second pass.  Four rows
+// per CTA halve each segment's step when few (sequence, head) pairs exist.  The CTA of row block 0 also
 // records the mode the (sequence, head) takes and its warmup bound.
 #include "gdn_dev.cuh"
 
 namespace gdn {
 namespace {
 
-constexpr int kRows = 8;  // state rows per CTA
 constexpr int kSlices = 8;  // k slices of 16 (one per warp)
-constexpr int kCombineSmem = 2 * kDim * kDim * 4 + 2 * kRows * kDim * 4 + kRows * kDim * 4 + kSlices * kRows * kDim * 4;
+template <int kRows>
+constexpr int combine_smem() {
+  return 2 * kDim * kDim * 4 + 2 * kRows * kDim * 4 + kRows * kDim * 4 + kSlices * kRows * kDim * 4;
+}
 
+// kRows state rows per CTA (4 or 8)
+template <int kRows>
 __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
   extern __shared__ float4 csm4[];
   float* sR = reinterpret_cast<float*>(csm4);  // [2][128*128]
@@ -86,8 +91,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
       }
       return;
     }
-    const float4 l4 = *reinterpret_cast<const float4*>(sL + (s & 1) * kRows * kDim + rr * kDim + c4);
-    float a0 = l4.x, a1 = l4.y, a2 = l4.z, a3 = l4.w;
+    const bool own = rr < kRows;  // the threads that finish one output row each
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    if (own) {
+      const float4 l4 = *reinterpret_cast<const float4*>(sL + (s & 1) * kRows * kDim + rr * kDim + c4);
+      a0 = l4.x;
+      a1 = l4.y;
+      a2 = l4.z;
+      a3 = l4.w;
+    }
     if (product) {
       // partial products over k = 16 ks .. 16 ks + 15 for all rows, columns c4 .. c4 + 3
       const int ks = tid >> 5;
@@ -118,31 +130,42 @@ __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
         *reinterpret_cast<float4*>(sP + (ks * kRows + r) * kDim + c4) =
             make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
       __syncthreads();
+      if (own) {
 #pragma unroll
-      for (int q = 0; q < kSlices; ++q) {
-        const float4 t4 = *reinterpret_cast<const float4*>(sP + (q * kRows + rr) * kDim + c4);
-        a0 += t4.x;
-        a1 += t4.y;
-        a2 += t4.z;
-        a3 += t4.w;
+        for (int q = 0; q < kSlices; ++q) {
+          const float4 t4 = *reinterpret_cast<const float4*>(sP + (q * kRows + rr) * kDim + c4);
+          a0 += t4.x;
+          a1 += t4.y;
+          a2 += t4.z;
+          a3 += t4.w;
+        }
       }
     }
     __syncthreads();
-    *reinterpret_cast<float4*>(sX + rr * kDim + c4) = make_float4(a0, a1, a2, a3);
-    *reinterpret_cast<float4*>(p.Sstart + ((size_t)(si.seg_base + s + 1) * p.h_v + j) * mat +
-                               (size_t)(r0 + rr) * kDim + c4) = make_float4(a0, a1, a2, a3);
+    if (own) {
+      *reinterpret_cast<float4*>(sX + rr * kDim + c4) = make_float4(a0, a1, a2, a3);
+      *reinterpret_cast<float4*>(p.Sstart + ((size_t)(si.seg_base + s + 1) * p.h_v + j) * mat +
+                                 (size_t)(r0 + rr) * kDim + c4) = make_float4(a0, a1, a2, a3);
+    }
   }
 }
 
 }  // namespace
 
 cudaError_t combine_kernel_setup() {
-  return cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCombineSmem);
+  cudaError_t e =
+      cudaFuncSetAttribute(combine_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, combine_smem<4>());
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(combine_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, combine_smem<8>());
 }
 
-cudaError_t launch_combine(const Problem& p, cudaStream_t st) {
-  dim3 grid(p.n_seqs, p.h_v, kDim / kRows);
-  combine_kernel<<<grid, 256, kCombineSmem, st>>>(p);
+cudaError_t launch_combine(const Problem& p, int sm_count, cudaStream_t st) {
+  // 32 CTAs of 4 rows per exact (sequence, head) if even all pairs fit in about two waves
+  if ((int64_t)p.n_seqs * p.h_v * 32 <= 2 * (int64_t)sm_count) {
+    combine_kernel<4><<<dim3(p.n_seqs, p.h_v, kDim / 4), 256, combine_smem<4>(), st>>>(p);
+  } else {
+    combine_kernel<8><<<dim3(p.n_seqs, p.h_v, kDim / 8), 256, combine_smem<8>(), st>>>(p);
+  }
   return cudaGetLastError();
 }
 

@@ -103,41 +103,47 @@ __device__ __forceinline__ void solve_unit_lower(float* F, float* scratch, int t
     }
     __syncthreads();
   }
-  // ---- level 1: T = L_{ib,jb} D_jb, then A_{ib,jb} = -D_ib T, for (ib, jb) = (1, 0), (3, 2) ----
+  // ---- level 1: T = L_{ib,jb} D_jb, then A_{ib,jb} = -D_ib T, for (ib, jb) = (1, 0), (3, 2);
+  //      four warps per pair, each on four columns of T (four rows of A_{ib,jb}) ----
   {
-    const int mat = tid >> 7, idx = tid & 127;
-    const int r = idx >> 3, c0 = (idx & 7) * 2;
+    const int mat = tid >> 7, w = (tid >> 5) & 3, lane = tid & 31;
     const int ib = 2 * mat + 1, jb = 2 * mat;
-    float* Ts = scratch + mat * 256;
+    float* Ts = scratch + mat * 256;  // [16][16]
     {
+      // T[r][c], c = 4w + 2 (lane >> 4) + {0, 1}, r = lane & 15: sum over m >= 4w (D_jb[m][c] = 0 for m < c)
+      const int r = lane & 15, c = 4 * w + 2 * (lane >> 4);
       const float* Lr = F + (16 * ib + r) * kFStride + 16 * jb;
-      const float* A0 = F + (16 * jb + c0) * kFStride + 16 * jb;  // D_jb column c0 (as a row of D^T)
-      float t0[2] = {0.f, 0.f}, t1[2] = {0.f, 0.f};
+      const float* D0 = F + (16 * jb + c) * kFStride + 16 * jb;  // D_jb column c as a row of D^T
+      float t0 = 0.f, t1 = 0.f;
 #pragma unroll
       for (int m = 0; m < 16; m += 4) {
+        if (m < 4 * w) continue;
         const float4 l4 = *reinterpret_cast<const float4*>(Lr + m);
-        const float4 a0 = *reinterpret_cast<const float4*>(A0 + m);
-        const float4 a1 = *reinterpret_cast<const float4*>(A0 + kFStride + m);
-        const int h = (m >> 2) & 1;
-        t0[h] = fmaf(l4.x, a0.x, fmaf(l4.y, a0.y, fmaf(l4.z, a0.z, fmaf(l4.w, a0.w, t0[h]))));
-        t1[h] = fmaf(l4.x, a1.x, fmaf(l4.y, a1.y, fmaf(l4.z, a1.z, fmaf(l4.w, a1.w, t1[h]))));
+        const float4 a0 = *reinterpret_cast<const float4*>(D0 + m);
+        const float4 a1 = *reinterpret_cast<const float4*>(D0 + kFStride + m);
+        t0 = fmaf(l4.x, a0.x, fmaf(l4.y, a0.y, fmaf(l4.z, a0.z, fmaf(l4.w, a0.w, t0))));
+        t1 = fmaf(l4.x, a1.x, fmaf(l4.y, a1.y, fmaf(l4.z, a1.z, fmaf(l4.w, a1.w, t1))));
       }
-      *reinterpret_cast<float2*>(Ts + r * 16 + c0) = make_float2(t0[0] + t0[1], t1[0] + t1[1]);
+      *reinterpret_cast<float2*>(Ts + r * 16 + c) = make_float2(t0, t1);
     }
     __syncthreads();
     {
-      float a0[2] = {0.f, 0.f}, a1[2] = {0.f, 0.f};
+      // A_{ib,jb}[r][c], r = 4w + 2 (lane >> 4) + {0, 1}, c = lane & 15: sum over m <= 4w + 3
+      // (D_ib[r][m] = 0 for m > r)
+      const int r = 4 * w + 2 * (lane >> 4), c = lane & 15;
+      float x0 = 0.f, x1 = 0.f;
 #pragma unroll
       for (int m = 0; m < 16; ++m) {
-        const float d = F[(16 * ib + m) * kFStride + 16 * ib + r];  // D_ib[r][m], zero for m > r
-        const float2 t = *reinterpret_cast<const float2*>(Ts + m * 16 + c0);
-        a0[m & 1] = fmaf(d, t.x, a0[m & 1]);
-        a1[m & 1] = fmaf(d, t.y, a1[m & 1]);
+        if (m >= 4 * w + 4) break;
+        const float2 d = *reinterpret_cast<const float2*>(F + (16 * ib + m) * kFStride + 16 * ib + r);
+        const float tv = Ts[m * 16 + c];
+        x0 = fmaf(d.x, tv, x0);
+        x1 = fmaf(d.y, tv, x1);
       }
-      F[(16 * jb + c0) * kFStride + 16 * ib + r] = -(a0[0] + a0[1]);  // A_{ib,jb}^T
-      F[(16 * jb + c0 + 1) * kFStride + 16 * ib + r] = -(a1[0] + a1[1]);
+      *reinterpret_cast<float2*>(F + (16 * jb + c) * kFStride + 16 * ib + r) = make_float2(-x0, -x1);
       // L_{ib,jb} has been consumed: clear it
-      *reinterpret_cast<float2*>(F + (16 * ib + r) * kFStride + 16 * jb + c0) = make_float2(0.f, 0.f);
+      const int idx = tid & 127, rz = idx >> 3, cz = (idx & 7) * 2;
+      *reinterpret_cast<float2*>(F + (16 * ib + rz) * kFStride + 16 * jb + cz) = make_float2(0.f, 0.f);
     }
     __syncthreads();
   }
