@@ -268,8 +268,10 @@ gdn_status gdn_cp_plan(const gdn_dims* dims, const int32_t* cu, const gdn_cp_opt
     off += segheads * mat;
   }
   if (dims->dtype == GDN_BF16) {
-    p.off_chunk_map = off;  // chunk index, then the chunk warmup exponents
-    off = align_up(off + ((size_t)dims->n_seqs + 1 + (size_t)n_chunks_total) * 4, 256);
+    p.off_chunk_map = off;  // chunk index (sequence bases, then 16-byte chunk records), then the chunk
+                            // warmup exponents
+    off = align_up(off + ((size_t)dims->n_seqs + 1) * 4, 16) + (size_t)n_chunks_total * 16;
+    off = align_up(off, 256);
     off = align_up(off + (size_t)n_chunks_total * dims->h_v * 4, 1024);
     p.off_wy = off;
     off += (size_t)n_chunks_total * dims->h_v * kRecBytes;
@@ -345,10 +347,10 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
   }
   p.n_chunks_total = plan->n_chunks_total;
   if (dims->dtype == GDN_BF16) {
+    const size_t info_off = align_up(plan->off_chunk_map + ((size_t)dims->n_seqs + 1) * 4, 16);
     p.seq_chunk_base = reinterpret_cast<int32_t*>(ws + plan->off_chunk_map);
-    p.chunk_seq = p.seq_chunk_base + dims->n_seqs + 1;
-    p.chunk_exp = reinterpret_cast<float*>(
-        ws + align_up(plan->off_chunk_map + ((size_t)dims->n_seqs + 1 + (size_t)plan->n_chunks_total) * 4, 256));
+    p.chunk_info = reinterpret_cast<int4*>(ws + info_off);
+    p.chunk_exp = reinterpret_cast<float*>(ws + align_up(info_off + (size_t)plan->n_chunks_total * 16, 256));
     p.wy = ws + plan->off_wy;
     p.kq16 = ws + plan->off_kq16;
   }
@@ -380,8 +382,10 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
 
   LaunchLog log{cs};
   if ((e = log.begin()) != cudaSuccess) return cuda_fail(e);
-  if ((e = launch_chunk_map(p, cs)) != cudaSuccess) return cuda_fail(e);
-  if ((e = log.after("chunk_map")) != cudaSuccess) return cuda_fail(e);
+  if (cu_dev) {  // varlen chunk index (fixed-length rows compute it)
+    if ((e = launch_chunk_map(p, cs)) != cudaSuccess) return cuda_fail(e);
+    if ((e = log.after("chunk_map")) != cudaSuccess) return cuda_fail(e);
+  }
   if ((e = launch_wy(p, mq, mk, mv, cs)) != cudaSuccess) return cuda_fail(e);
   if ((e = log.after("wy")) != cudaSuccess) return cuda_fail(e);
   if (plan->mode != GDN_CP_OFF) {

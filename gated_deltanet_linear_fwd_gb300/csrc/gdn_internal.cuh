@@ -71,8 +71,8 @@ struct Problem {
   float* Sstart;            // [n_seg_total, h_v, 128, 128] row = d_v
   // chunk index: chunks are numbered over all sequences in order
   int n_chunks_total;
-  int32_t* seq_chunk_base;  // [n_seqs + 1] global index of each sequence's first chunk
-  int32_t* chunk_seq;       // [n_chunks_total] sequence of each chunk
+  int32_t* seq_chunk_base;  // varlen: [n_seqs + 1] global index of each sequence's first chunk
+  int4* chunk_info;         // varlen: [n_chunks_total] {sequence, valid tokens, first token (lo, hi)}
   float* chunk_exp;         // [n_chunks_total, h_v] warmup exponent of each chunk:
                             // sum over its tokens of g + log max(1, |1 - beta ||k||^2|)
   uint8_t* wy;              // [n_chunks_total, h_v] records of kRecBytes
@@ -105,6 +105,12 @@ struct SegInfo {
   int cb, ce;    // chunk range of this segment
   int64_t bos, eos;
 };
+
+// Global index of sequence n's first chunk: arithmetic for fixed-length rows,
+// else from the chunk index built by chunk_map_kernel.
+__device__ __forceinline__ int seq_first_chunk(const Problem& p, int n) {
+  return p.cu ? p.seq_chunk_base[n] : n * chunks_of(p.T_row);
+}
 
 // Segments of sequence n (cp_off: one).
 __device__ __forceinline__ int seq_seg_count(const Problem& p, int n, int64_t& bos, int64_t& eos,

@@ -413,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(const Problem p) {
       // first CTA of each segment records its depth for the combine and the scan.
       __shared__ int s_exact;
       if (warp == 0) {
-        const int chunk0 = p.seq_chunk_base[si.n];
+        const int chunk0 = seq_first_chunk(p, si.n);
         bool none = false;
         for (int s2 = lane; s2 < si.n_seg; s2 += 32) {
           int w = 0;
@@ -456,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(const Problem p) {
   }
   if (ch.init == kInitH0 && p.h0 == nullptr) ch.init = kInitZero;
   ch.iq = (int)(((int64_t)j * p.h_qk) / p.h_v);
-  ch.chunk0 = p.seq_chunk_base[si.n];
+  ch.chunk0 = seq_first_chunk(p, si.n);
   if (ch.chunk0 < 0 || ch.chunk0 + si.n_chunks > p.n_chunks_total) {  // the chunk index disagrees with the plan
     if (tid == 0) report(p.status, kDevCheck, kDetSegMismatch);
     return;

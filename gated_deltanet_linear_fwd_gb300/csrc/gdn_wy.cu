@@ -202,20 +202,23 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
                                      const CUtensorMap* mk, const CUtensorMap* mv, uint32_t tmem, float& mx) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gc = (int)(blockIdx.x / (unsigned)p.h_v), j = (int)(blockIdx.x % (unsigned)p.h_v);
-  const int n = p.chunk_seq[gc];
-  if (n < 0 || n >= p.n_seqs) {  // the chunk index disagrees with the plan
+  int n, cv;
+  int64_t t0;
+  if (p.cu) {  // one 16-byte load: {sequence, valid tokens, first token}
+    const int4 ci = p.chunk_info[gc];
+    n = ci.x;
+    cv = ci.y;
+    t0 = (int64_t)(((uint64_t)(uint32_t)ci.w << 32) | (uint32_t)ci.z);
+  } else {     // fixed-length rows
+    const int cps = chunks_of(p.T_row);
+    n = gc / cps;
+    t0 = (int64_t)n * p.T_row + (int64_t)(gc - n * cps) * kChunk;
+    cv = (int)min((int64_t)kChunk, (int64_t)(n + 1) * p.T_row - t0);
+  }
+  if (n < 0 || n >= p.n_seqs || cv <= 0 || cv > kChunk) {  // the chunk index disagrees with the plan
     if (tid == 0) report(p.status, kDevCheck, kDetSegMismatch);
     return false;
   }
-  const int c = gc - p.seq_chunk_base[n];
-  int64_t bos, eos;
-  seq_bounds(p, n, bos, eos);
-  const int64_t t0 = bos + (int64_t)c * kChunk;
-  if (c < 0 || t0 >= eos) {
-    if (tid == 0) report(p.status, kDevCheck, kDetSegMismatch);
-    return false;
-  }
-  const int cv = (int)min((int64_t)kChunk, eos - t0);
   const int iq = (int)(((int64_t)j * p.h_qk) / p.h_v);
   const bool first_of_group = j == (int)(((int64_t)iq * p.h_v + p.h_qk - 1) / p.h_qk);
   float* gts = reinterpret_cast<float*>(sm + kWyGates);
@@ -432,7 +435,9 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
   if (__syncthreads_or(!ok)) return false;
   tc_fence_after();
 
-  // ---- -W and U^T tiles (over A diag(beta) and V, which the MMAs have consumed) ----
+  // ---- -W and U^T tiles (over A diag(beta) and V, which the MMAs have consumed).
+  //      No range check here: an fp16 overflow of either becomes inf in the
+  //      scan's V' = U - W S, which the scan checks every chunk. ----
   {
     const int d = (warp & 3) * 32 + lane, ch = warp >> 2;
     uint32_t ra[16], rb[16];
@@ -444,7 +449,8 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
       float f[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) f[e] = -__uint_as_float(q < 2 ? ra[8 * q + e] : rb[8 * (q - 2) + e]);
-      store_f16x8_m(sF + sw128_offset(d, ch * 4 + q), f, mx);
+      st_shared_v4(sF + sw128_offset(d, ch * 4 + q), pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]),
+                   pack_f16x2(f[4], f[5]), pack_f16x2(f[6], f[7]));
     }
     tmem_ld16(tmem + lane_base + kTU + ch * 32, ra);
     tmem_ld16(tmem + lane_base + kTU + ch * 32 + 16, rb);
@@ -454,7 +460,8 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
       float f[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(q < 2 ? ra[8 * q + e] : rb[8 * (q - 2) + e]);
-      store_f16x8_m(sV + sw128_offset(d, ch * 4 + q), f, mx);
+      st_shared_v4(sV + sw128_offset(d, ch * 4 + q), pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]),
+                   pack_f16x2(f[4], f[5]), pack_f16x2(f[6], f[7]));
     }
   }
   fence_proxy_async_smem();
@@ -514,8 +521,9 @@ __global__ void __launch_bounds__(kWyThreads, 3)
 }
 
 // ---------------------------------------------------------------- chunk index
-// seq_chunk_base[n] = chunks of sequences 0..n-1; chunk_seq[c] = the
-// sequence of global chunk c.  One CTA.
+// Varlen chunk index: seq_chunk_base[n] = chunks of sequences 0..n-1;
+// chunk_info[c] = {sequence, valid tokens, first token} of global chunk c.
+// One CTA.  (Fixed-length rows need no index: it is arithmetic.)
 constexpr int kMapThreads = 1024;
 
 __global__ void __launch_bounds__(kMapThreads) chunk_map_kernel(const Problem p) {
@@ -567,7 +575,11 @@ __global__ void __launch_bounds__(kMapThreads) chunk_map_kernel(const Problem p)
       if (p.seq_chunk_base[mid] <= gc) lo = mid;
       else hi = mid - 1;
     }
-    p.chunk_seq[gc] = lo;
+    int64_t bos, eos;
+    seq_bounds(p, lo, bos, eos);
+    const int64_t t0 = bos + (int64_t)(gc - p.seq_chunk_base[lo]) * kChunk;
+    p.chunk_info[gc] = make_int4(lo, (int)min((int64_t)kChunk, eos - t0), (int)(uint32_t)(uint64_t)t0,
+                                 (int)(uint32_t)((uint64_t)t0 >> 32));
   }
 }
 

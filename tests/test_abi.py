@@ -89,10 +89,11 @@ def test_plan_workspace_layout(lib):
     mat = 128 * 128 * 4
     assert p.off_head % 256 == 0 and p.off_seg_bound % 256 == 0
     assert p.off_Sloc - p.off_R == 23 * 8 * mat and p.off_Sstart - p.off_Sloc == 23 * 8 * mat
-    # chunk index (n_seqs + 1 + chunks int32), then the chunk records and fp16 K|Q tiles
+    # chunk index (n_seqs + 1 int32, 16-byte chunk records) and the chunk warmup exponents,
+    # then the chunk records and fp16 K|Q tiles
     assert p.n_chunks_total == 512
     assert p.off_chunk_map == p.off_Sstart + 23 * 8 * mat
-    assert p.off_wy % 1024 == 0 and p.off_wy >= p.off_chunk_map + (1 + 1 + 512) * 4
+    assert p.off_wy % 1024 == 0 and p.off_wy >= p.off_chunk_map + 8 + 512 * 16 + 512 * 8 * 4
     assert p.off_kq16 == p.off_wy + 512 * 8 * 41472
     assert p.workspace_bytes == p.off_kq16 + 512 * 2 * 32768
     st, p0 = plan(lib, 32768, h_v=8, mode=0)
