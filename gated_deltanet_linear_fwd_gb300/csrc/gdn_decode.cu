@@ -6,10 +6,10 @@
 // rule").  The state is read and written once (64 KB each way per (n, j)), so
 // the step is bound by HBM bandwidth; it runs on the CUDA cores in fp32.
 //
-// One CTA of 512 threads per (n, j): thread (i, part) holds column i of H
-// (row i of S) for d_k = 32 part .. 32 part + 31, so a warp reads and writes
-// 128 contiguous bytes of H per instruction.  S k and S q are summed over
-// the four parts through shared memory.
+// One CTA of 256 threads per (n, j): thread (g, part) holds columns
+// 4g .. 4g + 3 of H (rows of S) for d_k = 16 part .. 16 part + 15, so a warp
+// reads and writes one 512-byte row of H per 16-byte instruction.  S k and
+// S q are summed over the eight parts through shared memory.
 #include <cuda_bf16.h>
 
 #include "gdn_internal.cuh"
@@ -17,7 +17,7 @@
 namespace gdn {
 namespace {
 
-constexpr int kDecThreads = 512;
+constexpr int kDecThreads = 256;
 
 template <typename T>
 __device__ __forceinline__ float load_elem(const T* p);
@@ -40,48 +40,84 @@ __device__ __forceinline__ void store_elem<__nv_bfloat16>(__nv_bfloat16* p, floa
   *p = __float2bfloat16_rn(x);
 }
 
+// Thread (g, part): columns 4g .. 4g + 3 of H (rows 4g .. 4g + 3 of S) for
+// d_k = 16 part .. 16 part + 15, 16-byte loads and stores (a warp covers one
+// 512-byte row of H per instruction).
 template <typename T>
-__global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kDecThreads, 3) decode_kernel(const DecodeArgs a) {
   __shared__ float sk[kDim], sq[kDim];
-  __shared__ float part_sum[4][kDim];
+  __shared__ float4 red[8][32];
   const int n = blockIdx.x, j = blockIdx.y;
-  const int tid = threadIdx.x, i = tid & (kDim - 1), part = tid >> 7;
+  const int tid = threadIdx.x, g = tid & 31, part = tid >> 5;
   const int iq = (int)(((int64_t)j * a.h_qk) / a.h_v);
-  const T* q = reinterpret_cast<const T*>(a.q) + ((size_t)n * a.h_qk + iq) * kDim;
-  const T* k = reinterpret_cast<const T*>(a.k) + ((size_t)n * a.h_qk + iq) * kDim;
-  if (part == 0) {
-    sk[i] = load_elem(k + i);
-    sq[i] = load_elem(q + i);
+  if (tid < kDim) {
+    sk[tid] = load_elem(reinterpret_cast<const T*>(a.k) + ((size_t)n * a.h_qk + iq) * kDim + tid);
+    sq[tid] = load_elem(reinterpret_cast<const T*>(a.q) + ((size_t)n * a.h_qk + iq) * kDim + tid);
   }
-  float* H = a.state + ((size_t)n * a.h_v + j) * kDim * kDim + (size_t)(part * 32) * kDim + i;
-  float h[32];
+  float4* H = reinterpret_cast<float4*>(a.state + ((size_t)n * a.h_v + j) * kDim * kDim + (size_t)(part * 16) * kDim) + g;
+  float4 h[16];
 #pragma unroll
-  for (int e = 0; e < 32; ++e) h[e] = H[(size_t)e * kDim];
+  for (int e = 0; e < 16; ++e) h[e] = H[(size_t)e * (kDim / 4)];
   __syncthreads();
-  // (S_{t-1} k)_i over this part's 32 columns
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  // (S_{t-1} k) for this thread's 4 rows of S over its 16 columns, then over all parts
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int e = 0; e < 32; ++e) acc[e & 3] = fmaf(h[e], sk[part * 32 + e], acc[e & 3]);
-  part_sum[part][i] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+  for (int e = 0; e < 16; ++e) {
+    const float kc = sk[part * 16 + e];
+    acc.x = fmaf(h[e].x, kc, acc.x);
+    acc.y = fmaf(h[e].y, kc, acc.y);
+    acc.z = fmaf(h[e].z, kc, acc.z);
+    acc.w = fmaf(h[e].w, kc, acc.w);
+  }
+  red[part][g] = acc;
   __syncthreads();
-  const float s_k = (part_sum[0][i] + part_sum[1][i]) + (part_sum[2][i] + part_sum[3][i]);
+  float4 s_k = red[0][g];
+#pragma unroll
+  for (int q = 1; q < 8; ++q) {
+    const float4 t = red[q][g];
+    s_k.x += t.x;
+    s_k.y += t.y;
+    s_k.z += t.z;
+    s_k.w += t.w;
+  }
   const float alpha = expf(a.g[(size_t)n * a.h_v + j]), beta = a.beta[(size_t)n * a.h_v + j];
-  const float vi = load_elem(reinterpret_cast<const T*>(a.v) + ((size_t)n * a.h_v + j) * kDim + i);
-  const float bsk = beta * s_k, bv = beta * vi;
-  float o[4] = {0.f, 0.f, 0.f, 0.f};
+  const T* vrow = reinterpret_cast<const T*>(a.v) + ((size_t)n * a.h_v + j) * kDim + 4 * g;
+  const float4 bsk = make_float4(beta * s_k.x, beta * s_k.y, beta * s_k.z, beta * s_k.w);
+  const float4 bv = make_float4(beta * load_elem(vrow), beta * load_elem(vrow + 1), beta * load_elem(vrow + 2),
+                                beta * load_elem(vrow + 3));
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    const float kc = sk[part * 32 + e];
-    const float hn = fmaf(alpha, fmaf(-bsk, kc, h[e]), bv * kc);
-    H[(size_t)e * kDim] = hn;
-    o[e & 3] = fmaf(hn, sq[part * 32 + e], o[e & 3]);
+  for (int e = 0; e < 16; ++e) {
+    const float kc = sk[part * 16 + e], qc = sq[part * 16 + e];
+    float4 hn;
+    hn.x = fmaf(alpha, fmaf(-bsk.x, kc, h[e].x), bv.x * kc);
+    hn.y = fmaf(alpha, fmaf(-bsk.y, kc, h[e].y), bv.y * kc);
+    hn.z = fmaf(alpha, fmaf(-bsk.z, kc, h[e].z), bv.z * kc);
+    hn.w = fmaf(alpha, fmaf(-bsk.w, kc, h[e].w), bv.w * kc);
+    H[(size_t)e * (kDim / 4)] = hn;
+    o.x = fmaf(hn.x, qc, o.x);
+    o.y = fmaf(hn.y, qc, o.y);
+    o.z = fmaf(hn.z, qc, o.z);
+    o.w = fmaf(hn.w, qc, o.w);
   }
-  __syncthreads();  // everyone has read part_sum
-  part_sum[part][i] = (o[0] + o[1]) + (o[2] + o[3]);
+  __syncthreads();  // everyone has read red
+  red[part][g] = o;
   __syncthreads();
   if (part == 0) {
-    const float oi = (part_sum[0][i] + part_sum[1][i]) + (part_sum[2][i] + part_sum[3][i]);
-    store_elem(reinterpret_cast<T*>(a.out) + ((size_t)n * a.h_v + j) * kDim + i, a.scale * oi);
+    float4 t = red[0][g];
+#pragma unroll
+    for (int q = 1; q < 8; ++q) {
+      const float4 u = red[q][g];
+      t.x += u.x;
+      t.y += u.y;
+      t.z += u.z;
+      t.w += u.w;
+    }
+    T* orow = reinterpret_cast<T*>(a.out) + ((size_t)n * a.h_v + j) * kDim + 4 * g;
+    store_elem(orow, a.scale * t.x);
+    store_elem(orow + 1, a.scale * t.y);
+    store_elem(orow + 2, a.scale * t.z);
+    store_elem(orow + 3, a.scale * t.w);
   }
 }
 
