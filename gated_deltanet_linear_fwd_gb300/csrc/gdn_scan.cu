@@ -93,6 +93,22 @@ __device__ __forceinline__ bool wait_bar(Ctl* ctl, int b, uint32_t parity) {
   return wait_phase(&ctl->bar[b], parity, &ctl->abort, 100 + b);
 }
 
+// Bounded wait that polls without suspending: the single MMA-issuing thread
+// uses it so that it reacts to a hand-over as soon as the phase completes.
+__device__ __forceinline__ bool spin_bar(Ctl* ctl, int b, uint32_t parity) {
+  if (mbar_test_wait(&ctl->bar[b], parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int k = 0; k < 64; ++k)
+      if (mbar_test_wait(&ctl->bar[b], parity)) return true;
+    if (*reinterpret_cast<volatile int*>(&ctl->abort)) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicCAS(&ctl->abort, 0, 100 + b);
+      return false;
+    }
+  }
+}
+
 struct Chain {
   int run_begin, run_end, out_begin;
   int init;
@@ -178,7 +194,7 @@ __device__ __noinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch, ui
       issue_u(i);
       ++nu;
     }
-    if (!wait_bar(ctl, kSReady, (uint32_t)(i & 1))) return;
+    if (!spin_bar(ctl, kSReady, (uint32_t)(i & 1))) return;
     if (i >= 2 && !wait_bar(ctl, kYoFree0 + (i & 1), (uint32_t)(((i - 2) >> 1) & 1))) return;
     tc_fence_after();
 #pragma unroll
@@ -200,7 +216,7 @@ __device__ __noinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch, ui
       issue_u(i + 1);  // its V' buffer was released by C(i - 1)
       ++nu;
     }
-    if (!wait_bar(ctl, kVReady, (uint32_t)(i & 1))) return;
+    if (!spin_bar(ctl, kVReady, (uint32_t)(i & 1))) return;
     tc_fence_after();
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)  // D3 = V'^T diag(dec) K
