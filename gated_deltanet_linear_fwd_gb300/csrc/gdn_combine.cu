@@ -36,19 +36,24 @@ __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
   __shared__ uint64_t s_bar[2];
   const int tid = threadIdx.x, warp = tid >> 5;
   const int n = blockIdx.x, j = blockIdx.y, r0 = blockIdx.z * kRows;
+  __shared__ int s_mode;
   if (warp == 0) {
     SegInfo si;
     locate_sequence(p, n, si);
-    if ((tid & 31) == 0) s_seq = si;
+    float bound;
+    const int mode = head_mode_warp(p, si, j, &bound);
+    if ((tid & 31) == 0) {
+      s_seq = si;
+      s_mode = mode;
+      if (blockIdx.z == 0) {
+        p.head_mode[n * p.h_v + j] = mode;
+        p.head_bound[n * p.h_v + j] = bound;
+      }
+    }
   }
   __syncthreads();
   const SegInfo si = s_seq;
-  const int mode = head_mode_of(p, si, j);
-  if (blockIdx.z == 0 && tid == 0) {
-    p.head_mode[n * p.h_v + j] = mode;
-    p.head_bound[n * p.h_v + j] =
-        p.plan_mode == kModeWarmup ? head_log_bound(p, si, j) : -__int_as_float(0x7f800000);
-  }
+  const int mode = s_mode;
   if (mode != kModeExact || si.n_seg <= 1) return;
 
   if (tid == 0) {

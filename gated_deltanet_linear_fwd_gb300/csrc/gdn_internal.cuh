@@ -195,9 +195,13 @@ __device__ inline void locate_sequence(const Problem& p, int n, SegInfo& out) {
 // such w gives -1 (the head runs exactly) with the full window's exponent.
 __device__ inline void seg_warmup_depth(const Problem& p, int chunk0, int cb, int j, int& w_out, float& b_out) {
   const int nwin = min(p.warmup_chunks, cb);
+  constexpr int kPre = 8;  // window exponents loaded together before the scan
+  float pre[kPre];
+#pragma unroll
+  for (int w = 1; w <= kPre; ++w) pre[w - 1] = w <= nwin ? p.chunk_exp[(size_t)(chunk0 + cb - w) * p.h_v + j] : 0.f;
   float acc = 0.f;
   for (int w = 1; w <= nwin; ++w) {
-    acc += p.chunk_exp[(size_t)(chunk0 + cb - w) * p.h_v + j];
+    acc += w <= kPre ? pre[w - 1] : p.chunk_exp[(size_t)(chunk0 + cb - w) * p.h_v + j];
     if (cb - w == 0) {
       w_out = w;
       b_out = -__int_as_float(0x7f800000);
@@ -213,20 +217,27 @@ __device__ inline void seg_warmup_depth(const Problem& p, int chunk0, int cb, in
   b_out = acc;
 }
 
-// Max of the per-segment warmup bounds of (sequence, head); -inf if none.
-__device__ inline float head_log_bound(const Problem& p, const SegInfo& si, int j) {
+// Warp-cooperative (call with a full warp; every lane gets the result): the
+// mode a (sequence, head) takes under the plan -- warmup when every segment
+// found a restart depth -- and the largest of its segments' warmup bounds.
+// The segments' words are read in parallel across the lanes.
+__device__ inline int head_mode_warp(const Problem& p, const SegInfo& si, int j, float* log_bound) {
+  const int lane = threadIdx.x & 31;
   float m = -__int_as_float(0x7f800000);
-  for (int s = 1; s < si.n_seg; ++s) m = fmaxf(m, p.seg_bound[(size_t)(si.seg_base + s) * p.h_v + j]);
-  return m;
-}
-
-// Mode a (sequence, head) takes under the plan: warmup when every segment
-// found a restart depth whose bound meets the tolerance.
-__device__ inline int head_mode_of(const Problem& p, const SegInfo& si, int j) {
+  bool none = false;
+  if (p.plan_mode == kModeWarmup) {
+    for (int s = 1 + lane; s < si.n_seg; s += 32) {
+      const size_t slot = (size_t)(si.seg_base + s) * p.h_v + j;
+      none |= p.seg_w[slot] < 0;
+      m = fmaxf(m, p.seg_bound[slot]);
+    }
+  }
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+  none = __any_sync(0xffffffffu, none);
+  if (log_bound) *log_bound = m;
   if (p.plan_mode == kModeOff) return kModeOff;
-  if (p.plan_mode == kModeExact) return kModeExact;
-  for (int s = 1; s < si.n_seg; ++s)
-    if (p.seg_w[(size_t)(si.seg_base + s) * p.h_v + j] < 0) return kModeExact;
+  if (p.plan_mode == kModeExact || none) return kModeExact;
   return kModeWarmup;
 }
 
