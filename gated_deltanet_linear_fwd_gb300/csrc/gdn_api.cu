@@ -5,6 +5,7 @@
 #include <climits>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "gdn.h"
 #include "gdn_internal.cuh"
@@ -83,33 +84,110 @@ gdn_status device_setup(int* dev_out) {
 
 // AutoCP's choice of lambda (FlashQLA pages, section "AutoCP": the degree
 // of parallelism follows L = lambda sqrt(N)).  The scan kernel runs one CTA
-// per (segment, value head) and one CTA per SM, so its time is about
-// (waves of CTAs) x (longest segment, in chunks).  Among lambda = k/8 the
-// planner takes the one that minimises that product; ties go to fewer
-// segments (less warmup and combine work).
-int pick_lambda_q8(const gdn_dims* d, const int32_t* cu, int sm_count) {
-  int best_q8 = 256;
-  int64_t best_cost = INT64_MAX, best_segs = INT64_MAX;
-  for (int q8 = 32; q8 <= 4096; q8 += 32) {
-    int64_t segs = 0;
-    int longest = 0;
+// per (segment, value head), one CTA per SM; a CTA takes about (segment
+// chunks + 3) chunk-times (start-up, pipeline fill and warmup chunks).  The
+// block scheduler hands CTAs out in launch order (the segments of sequence
+// 0, 1, ..., then the next value head) to whichever SM frees first, so the
+// planner replays that list schedule.  The combine then walks each
+// sequence's segments in order, about half a chunk-time per segment.  Among
+// lambda = k/8 the planner takes the smallest (schedule finish + half the
+// largest segment count of a sequence); ties go to fewer segments.
+namespace {
+
+constexpr int kCtaOverheadChunks = 3;
+
+struct SegStats {
+  int64_t segs = 0;
+  int longest = 0, most_segs = 0;
+  int64_t work = 0;  // sum of (chunks + overhead) over one head's segments
+};
+
+SegStats seg_stats(const gdn_dims* d, const int32_t* cu, int q8) {
+  SegStats r;
+  for (int n = 0; n < d->n_seqs; ++n) {
+    const int64_t len = cu ? (int64_t)cu[n + 1] - cu[n] : d->T;
+    const int N = chunks_of(len);
+    const int ns = seg_count(N, q8, false);
+    r.segs += ns;
+    r.work += N + (int64_t)ns * kCtaOverheadChunks;
+    r.longest = std::max(r.longest, (N + ns - 1) / ns);  // balanced split: ceil(N / ns) at most
+    r.most_segs = std::max(r.most_segs, ns);
+  }
+  return r;
+}
+
+// Finish time of the list schedule of the scan's CTAs on sm_count SMs.  The
+// earliest free time never decreases along the schedule, so SM free times
+// are kept as counts per time step and the earliest is found by a forward
+// scan; the finish is at most total / sm_count + the longest CTA (the list
+// scheduling bound), which sizes the count array.
+int64_t list_schedule(const gdn_dims* d, const int32_t* cu, int q8, int sm_count, const SegStats& st,
+                      std::vector<int32_t>& free_at) {
+  const int64_t horizon = st.work * d->h_v / sm_count + st.longest + kCtaOverheadChunks + 2;
+  free_at.assign((size_t)horizon, 0);
+  free_at[0] = sm_count;
+  int64_t t = 0, finish = 0;
+  for (int j = 0; j < d->h_v; ++j)
     for (int n = 0; n < d->n_seqs; ++n) {
       const int64_t len = cu ? (int64_t)cu[n + 1] - cu[n] : d->T;
       const int N = chunks_of(len);
       const int ns = seg_count(N, q8, false);
-      segs += ns;
-      for (int s = 0; s < ns; ++s) longest = std::max(longest, seg_first(s + 1, N, ns) - seg_first(s, N, ns));
+      for (int s = 0; s < ns; ++s) {
+        while (free_at[(size_t)t] == 0) ++t;
+        --free_at[(size_t)t];
+        const int64_t end = t + seg_first(s + 1, N, ns) - seg_first(s, N, ns) + kCtaOverheadChunks;
+        ++free_at[(size_t)end];
+        finish = std::max(finish, end);
+      }
     }
-    const int64_t ctas = segs * d->h_v;
-    const int64_t waves = (ctas + sm_count - 1) / sm_count;
-    const int64_t cost = waves * (int64_t)(longest + 1);  // +1: a warmup chunk per segment
-    if (cost < best_cost || (cost == best_cost && segs < best_segs)) {
+  return finish;
+}
+
+}  // namespace
+
+int pick_lambda_q8_uncached(const gdn_dims* d, const int32_t* cu, int sm_count) {
+  int best_q8 = 256;
+  int64_t best_cost = INT64_MAX, best_segs = INT64_MAX;
+  std::vector<int32_t> free_at;
+  for (int q8 = 32; q8 <= 4096; q8 += 32) {
+    const SegStats st = seg_stats(d, cu, q8);
+    // in half chunk-times; no schedule ends before its longest CTA or the average SM load
+    const int64_t total = st.work * d->h_v;
+    const int64_t lower =
+        2 * std::max<int64_t>(st.longest + kCtaOverheadChunks, (total + sm_count - 1) / sm_count) + st.most_segs;
+    if (lower > best_cost || (lower == best_cost && st.segs >= best_segs)) continue;
+    const int64_t cost = 2 * list_schedule(d, cu, q8, sm_count, st, free_at) + st.most_segs;
+    if (cost < best_cost || (cost == best_cost && st.segs < best_segs)) {
       best_cost = cost;
-      best_segs = segs;
+      best_segs = st.segs;
       best_q8 = q8;
     }
   }
   return best_q8;
+}
+
+// The choice depends only on the sequence lengths, h_v and the SM count; a
+// model plans the same lengths once per layer, so recent choices are kept.
+int pick_lambda_q8(const gdn_dims* d, const int32_t* cu, int sm_count) {
+  struct Entry {
+    int h_v, sm_count;
+    std::vector<int64_t> lens;
+    int q8;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> recent;  // most recent last
+  std::vector<int64_t> lens((size_t)d->n_seqs);
+  for (int n = 0; n < d->n_seqs; ++n) lens[(size_t)n] = cu ? (int64_t)cu[n + 1] - cu[n] : d->T;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (const Entry& e : recent)
+      if (e.h_v == d->h_v && e.sm_count == sm_count && e.lens == lens) return e.q8;
+  }
+  const int q8 = pick_lambda_q8_uncached(d, cu, sm_count);
+  std::lock_guard<std::mutex> lk(mu);
+  if (recent.size() >= 8) recent.erase(recent.begin());
+  recent.push_back(Entry{d->h_v, sm_count, std::move(lens), q8});
+  return q8;
 }
 
 gdn_status check_dims(const gdn_dims* d) {

@@ -93,8 +93,10 @@ typedef struct gdn_cp_opts {
   int mode;          /* GDN_CP_* */
   float lambda;      /* segment length L = round(lambda * sqrt(N)) chunks, lambda used in
                         steps of 1/256; <= 0 lets the planner choose it: the lambda (a
-                        multiple of 1/8) minimising (waves of CTAs over sm_count) x (longest
-                        segment + 1) */
+                        multiple of 1/8) minimising 2 x (finish of the list schedule of
+                        the scan's CTAs in launch order on sm_count SMs, each taking its
+                        segment's chunks + 3) + (most segments of one sequence); ties go
+                        to fewer segments */
   int warmup_chunks; /* warmup restart depth w in chunks; <= 0 selects 8 */
   float warmup_tol;  /* accept warmup for a (sequence, head) when its bound
                         max over segments of exp(sum g over the window) *

@@ -166,7 +166,9 @@ def test_binding_fails_loudly_without_library(tmp_path):
 
 
 @pytest.mark.parametrize("cu,h_v,sms", [([0, 32768], 8, 152), ([0, 32768], 24, 148),
-                                        ([0, 262144, 327680, 344064, 348160], 8, 152), ([0, 512], 4, 152)])
+                                        ([0, 262144, 327680, 344064, 348160], 8, 152), ([0, 512], 4, 152),
+                                        ([0, 4096, 20480, 86016, 348160], 8, 152),
+                                        ([0, 100000, 100100, 160000], 4, 148)])
 def test_plan_automatic_lambda(lib, cu, h_v, sms):
     st, p = plan(lib, cu[-1], h_v=h_v, cu=cu, mode=2, lam=0.0, sms=sms)
     assert st == 0

@@ -89,17 +89,21 @@ def warmup_depths(w, lambda_q8, wmax, tol):
 
 def auto_lambda_q8(T_list, h_v, sm_count):
     """The planner's automatic lambda, restated from its documented rule:
-    among lambda = k/8 (k = 1..128) minimise waves x (longest segment + 1),
-    ties to fewer segments."""
+    among lambda = k/8 (k = 1..128) take the smallest (finish of the list
+    schedule of the scan's CTAs + half the largest segment count of a
+    sequence), ties to fewer segments.  The schedule: launch order (the
+    segments of every sequence, head after head), each CTA taking segment
+    chunks + 3 on the first SM to free up."""
     best = None
     for q8 in range(32, 4097, 32):
-        segs, longest = 0, 0
-        for n_tok in T_list:
-            sg = segments(n_tok, q8, False)
-            segs += len(sg)
-            longest = max(longest, max(b - a for a, b in sg))
-        waves = -(-segs * h_v // sm_count)
-        key = (waves * (longest + 1), segs)
+        seglists = [segments(n_tok, q8, False) for n_tok in T_list]
+        free = [0] * sm_count
+        for _ in range(h_v):
+            for sg in seglists:
+                for a, b in sg:
+                    i = min(range(sm_count), key=free.__getitem__)
+                    free[i] += b - a + 3
+        key = (2 * max(free) + max(len(sg) for sg in seglists), sum(len(sg) for sg in seglists))
         if best is None or key < best[0]:
             best = (key, q8)
     return best[1]
