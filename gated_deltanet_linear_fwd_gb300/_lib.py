@@ -54,7 +54,7 @@ class gdn_cp_plan_t(ctypes.Structure):
                 ("off_head", ctypes.c_size_t), ("off_seg_bound", ctypes.c_size_t),
                 ("off_R", ctypes.c_size_t), ("off_Sloc", ctypes.c_size_t), ("off_Sstart", ctypes.c_size_t),
                 ("n_chunks_total", ctypes.c_int), ("off_chunk_map", ctypes.c_size_t),
-                ("off_wy", ctypes.c_size_t), ("off_kq16", ctypes.c_size_t)]
+                ("off_wy", ctypes.c_size_t)]
 
 
 _lock = threading.Lock()

@@ -328,7 +328,7 @@ gdn_status gdn_cp_plan(const gdn_dims* dims, const int32_t* cu, const gdn_cp_opt
   p.n_seg_total = (int)n_seg_total;
   p.n_chunks_total = (int)n_chunks_total;
   // workspace: status | head modes + bounds | segment bounds | R | S_loc | S_start |
-  //            chunk index | chunk records | fp16 K|Q tiles (the last three: bf16 path only)
+  //            chunk index | chunk records (the last two: bf16 path only)
   const size_t heads = (size_t)dims->n_seqs * dims->h_v;
   const size_t segheads = (size_t)n_seg_total * dims->h_v;
   size_t off = 256;
@@ -353,8 +353,6 @@ gdn_status gdn_cp_plan(const gdn_dims* dims, const int32_t* cu, const gdn_cp_opt
     off = align_up(off + (size_t)n_chunks_total * dims->h_v * 4, 1024);
     p.off_wy = off;
     off += (size_t)n_chunks_total * dims->h_v * kRecBytes;
-    p.off_kq16 = off;
-    off += (size_t)n_chunks_total * dims->h_qk * kKqRecBytes;
   }
   p.workspace_bytes = off;
   *out = p;
@@ -430,7 +428,6 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
     p.chunk_info = reinterpret_cast<int4*>(ws + info_off);
     p.chunk_exp = reinterpret_cast<float*>(ws + align_up(info_off + (size_t)plan->n_chunks_total * 16, 256));
     p.wy = ws + plan->off_wy;
-    p.kq16 = ws + plan->off_kq16;
   }
 
   cudaError_t e = cudaMemsetAsync(ws, 0, 256, cs);
@@ -467,12 +464,12 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
   if ((e = launch_wy(p, mq, mk, mv, cs)) != cudaSuccess) return cuda_fail(e);
   if ((e = log.after("wy")) != cudaSuccess) return cuda_fail(e);
   if (plan->mode != GDN_CP_OFF) {
-    if ((e = launch_scan_prep(p, cs)) != cudaSuccess) return cuda_fail(e);
+    if ((e = launch_scan_prep(p, mq, mk, cs)) != cudaSuccess) return cuda_fail(e);
     if ((e = log.after("scan_prep")) != cudaSuccess) return cuda_fail(e);
     if ((e = launch_combine(p, g_sm_count[dev], cs)) != cudaSuccess) return cuda_fail(e);
     if ((e = log.after("combine")) != cudaSuccess) return cuda_fail(e);
   }
-  if ((e = launch_scan_out(p, plan->n_seg_total, cs)) != cudaSuccess) return cuda_fail(e);
+  if ((e = launch_scan_out(p, mq, mk, plan->n_seg_total, cs)) != cudaSuccess) return cuda_fail(e);
   if ((e = log.after("scan_out")) != cudaSuccess) return cuda_fail(e);
   return GDN_OK;
 }

@@ -36,8 +36,6 @@ constexpr uint32_t kRecU = 16384;     // fp16 U^T, K-major A tile: row d_v, 64 c
 constexpr uint32_t kRecP = 32768;     // fp16 P, K-major B tile: row r, columns s <= r (8 KB)
 constexpr uint32_t kRecGam = 40960;   // fp32 exp(G_r), then exp(G_63 - G_r) (2 x 64)
 constexpr uint32_t kRecBytes = 41472;
-//   per (chunk, query/key head):
-constexpr uint32_t kKqRecBytes = 32768;  // fp16 [K d0-63 | Q d0-63 | K d64-127 | Q d64-127], 8 KB each
 
 struct Problem {
   const void* q;
@@ -76,7 +74,6 @@ struct Problem {
   float* chunk_exp;         // [n_chunks_total, h_v] warmup exponent of each chunk:
                             // sum over its tokens of g + log max(1, |1 - beta ||k||^2|)
   uint8_t* wy;              // [n_chunks_total, h_v] records of kRecBytes
-  uint8_t* kq16;            // [n_chunks_total, h_qk] records of kKqRecBytes
 };
 
 // Arguments of the one-token step (gdn_decode_step).
@@ -245,9 +242,10 @@ __device__ inline int head_mode_warp(const Problem& p, const SegInfo& si, int j,
 cudaError_t launch_chunk_map(const Problem& p, cudaStream_t st);
 cudaError_t launch_wy(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                       cudaStream_t st);
-cudaError_t launch_scan_prep(const Problem& p, cudaStream_t st);
+cudaError_t launch_scan_prep(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, cudaStream_t st);
 cudaError_t launch_combine(const Problem& p, int sm_count, cudaStream_t st);
-cudaError_t launch_scan_out(const Problem& p, int grid_x, cudaStream_t st);
+cudaError_t launch_scan_out(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, int grid_x,
+                            cudaStream_t st);
 cudaError_t launch_recurrence_f32(const Problem& p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, bool f32, cudaStream_t st);
 cudaError_t scan_kernel_setup();

@@ -18,7 +18,8 @@
 //     state (started at zero).
 //
 // Everything chunk-local (the gate cumsum, the WY form, P) comes from the
-// WY kernel's records as ready-made operand tiles.  Here, in the S
+// WY kernel's records as ready-made operand tiles; K and Q come straight
+// from the inputs (bf16, rounded to fp16 in shared memory).  Here, in the S
 // orientation (rows = d_v, columns = d_k), per chunk:
 //   V'^T = U^T - S W^T        (U^T enters the accumulator as U^T . I)
 //   Y    = S Q^T
@@ -29,12 +30,17 @@
 // for its MMAs; V' likewise.  A value outside the fp16 range is reported
 // through the status word.
 //
-// Warp roles (320 threads): warps 0-7 hold the state (row = d_v lane, 64
-// columns each) and run the V' and state epilogues, the critical path from
-// one chunk to the next, and then the chunk's output epilogue while the
-// tensor cores work on the next chunk's S W^T; warp 8 loads each chunk's
-// record (bulk copies); lane 0 of warp 9 issues every MMA.  They hand over
-// through mbarriers whose waits are all bounded.
+// Warp roles (512 threads, four warpgroups): warps 0-7 hold the state (row =
+// d_v lane, 64 columns each) and run the V' and state epilogues, the
+// critical path from one chunk to the next; warps 8-11 read Y and O2 and
+// write the chunk's outputs while the state warps go on to the next chunk;
+// warp 12 loads each chunk's record (bulk copies) and its K and Q tiles
+// (TMA); lane 0 of warp 13 issues every MMA; warps 14-15 round the bf16 K
+// and Q tiles to fp16 in place, a chunk ahead of the MMAs that read them.
+// The state warpgroups raise their register limit to 168 (the state takes
+// 64 per thread) and the others lower theirs to 88, within the 128 per
+// thread the block is launched with.  The roles hand over through
+// mbarriers whose waits are all bounded.
 #include <cuda_bf16.h>
 
 #include "gdn_dev.cuh"
@@ -42,13 +48,22 @@
 namespace gdn {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 512;
 constexpr int kChainThreads = 256;
-constexpr int kProducerWarp = 8;
+constexpr int kOutWarp = 8;        // warps 8-11
+constexpr int kOutThreads = 128;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr int kConvertWarp = 14;   // warps 14-15
+constexpr int kConvertWarps = 2;
+constexpr uint32_t kChainRegs = 168, kOtherRegs = 88;
+static_assert(2 * 128 * kChainRegs + 2 * 128 * kOtherRegs <= 65536 && kThreads * 128 == 65536,
+              "register split over the launch's 128 per thread");
 
 // ---- shared memory map (bytes from a 1024-byte aligned base) ----
 constexpr uint32_t kStageBytes = 73728;   // per chunk stage (two stages)
-constexpr uint32_t kStKQ = 0;             // fp16 [K d0-63 | Q d0-63 | K d64-127 | Q d64-127], 8 KB each
+constexpr uint32_t kStKQ = 0;             // [K d0-63 | Q d0-63 | K d64-127 | Q d64-127], 8 KB each:
+                                          // bf16 as loaded, then fp16 in place
 constexpr uint32_t kStWn = 32768;         // fp16 -W, MN-major B: rows d_k
 constexpr uint32_t kStU = 49152;          // fp16 U^T, K-major A: rows d_v
 constexpr uint32_t kStP = 65536;          // fp16 P, K-major B: rows r
@@ -77,6 +92,7 @@ enum Bar {
   kGates0, kGates1, kGates2, kGates3,      // gates ring slots (loaded)
   kVaDone, kVReady, kD3Done, kSReady,      // state pipeline
   kYoDone0, kYoDone1, kYoFree0, kYoFree1,  // output epilogue (two Y/O2 buffers)
+  kKqFull0, kKqFull1, kKqReady0, kKqReady1,  // K|Q tiles loaded (bf16) / rounded to fp16
   kNumBars
 };
 
@@ -110,6 +126,7 @@ __device__ __forceinline__ bool spin_bar(Ctl* ctl, int b, uint32_t parity) {
 }
 
 struct Chain {
+  int64_t bos;  // the sequence's first token
   int run_begin, run_end, out_begin;
   int init;
   bool has_u, write_final;
@@ -123,9 +140,12 @@ __device__ __forceinline__ bool want_out(const Chain& ch, int i) {
 }
 
 // ----------------------------------------------------------------- producer
-// Loads each chunk's record tiles (bulk copies) into its stage.
+// Loads each chunk's K and Q tiles (TMA, 64 tokens x 64 dims per box, rows
+// past the end of the input read as zero) and its record tiles (bulk
+// copies) into its stage.
 template <bool PREP>
-__device__ __noinline__ void producer_role(uint8_t* sm, Ctl* ctl, const Problem& p, const Chain& ch, int j) {
+__device__ __forceinline__ void producer_role(uint8_t* sm, Ctl* ctl, const Problem& p, const Chain& ch, int j,
+                                           const CUtensorMap* mq, const CUtensorMap* mk) {
   if ((threadIdx.x & 31) != 0) return;
   const int n = ch.run_end - ch.run_begin;
   for (int i = 0; i < n; ++i) {
@@ -133,28 +153,68 @@ __device__ __noinline__ void producer_role(uint8_t* sm, Ctl* ctl, const Problem&
     if (i >= 2 && !wait_bar(ctl, kEmpty0 + st, (uint32_t)(((i - 2) >> 1) & 1))) return;
     const size_t gc = (size_t)ch.chunk0 + ch.run_begin + i;
     const uint8_t* rec = p.wy + (gc * p.h_v + j) * kRecBytes;
-    const uint8_t* kq = p.kq16 + (gc * p.h_qk + ch.iq) * kKqRecBytes;
     const bool out = want_out<PREP>(ch, i);
     uint8_t* stg = sm + st * kStageBytes;
-    uint64_t* bar = &ctl->bar[kFull0 + st];
-    const uint32_t bytes = (out ? 32768u : 16384u) + 16384u + (ch.has_u ? 16384u : 0u) + (out ? 8192u : 0u);
-    mbar_arrive_expect_tx(bar, bytes);
-    if (out) {
-      bulk_load(stg + kStKQ, kq, 32768u, bar);
-    } else {  // K halves only
-      bulk_load(stg + kStKQ, kq, 8192u, bar);
-      bulk_load(stg + kStKQ + 16384, kq + 16384, 8192u, bar);
+    const int t0 = (int)(ch.bos + (int64_t)(ch.run_begin + i) * kChunk);
+    uint64_t* kbar = &ctl->bar[kKqFull0 + st];
+    mbar_arrive_expect_tx(kbar, out ? 32768u : 16384u);
+    tma_load_3d(stg + kStKQ, mk, kbar, 0, ch.iq, t0);
+    tma_load_3d(stg + kStKQ + 16384, mk, kbar, 64, ch.iq, t0);
+    if (out) {  // Q only where the chunk's output is written
+      tma_load_3d(stg + kStKQ + 8192, mq, kbar, 0, ch.iq, t0);
+      tma_load_3d(stg + kStKQ + 24576, mq, kbar, 64, ch.iq, t0);
     }
+    uint64_t* bar = &ctl->bar[kFull0 + st];
+    const uint32_t bytes = 16384u + (ch.has_u ? 16384u : 0u) + (out ? 8192u : 0u);
+    mbar_arrive_expect_tx(bar, bytes);
     bulk_load(stg + kStWn, rec + kRecWn, 16384u, bar);
     if (ch.has_u) bulk_load(stg + kStU, rec + kRecU, 16384u, bar);
     if (out) bulk_load(stg + kStP, rec + kRecP, 8192u, bar);
     // The gates go to ring slot i & 3.  Its readers of chunk i - 4 are done:
-    // the state warps read those gates before yo_free(i - 4), which A(i - 2)
-    // waited for, and stage i & 1 is free only after C(i - 2).
+    // the state warps read those gates in the V' epilogue of chunk i - 4, the
+    // output warps before yo_free(i - 4), which A(i - 2) waited for, and
+    // stage i & 1 is free only after C(i - 2).
     uint64_t* gbar = &ctl->bar[kGates0 + (i & 3)];
     mbar_arrive_expect_tx(gbar, 512u);
     bulk_load(sm + kSmG + (i & 3) * 512, rec + kRecGam, 512u, gbar);
   }
+}
+
+// ----------------------------------------------------------------- K|Q rounding
+// Rounds each stage's bf16 K (and Q) tiles to fp16 in place (same byte
+// layout), then hands the stage to the MMA issuer.  The state's fp16 operand
+// copy keeps 11 significant bits, so the MMAs with K and Q run in fp16.
+// Values outside the fp16 range are reported through the status word.
+template <bool PREP>
+__device__ __forceinline__ void convert_role(uint8_t* sm, Ctl* ctl, const Chain& ch) {
+  const int lane = threadIdx.x & 31, part = (threadIdx.x >> 5) - kConvertWarp;
+  const int n = ch.run_end - ch.run_begin;
+  float mx = 0.f;
+  for (int i = 0; i < n; ++i) {
+    const int st = i & 1;
+    if (!wait_bar(ctl, kKqFull0 + st, (uint32_t)((i >> 1) & 1))) break;
+    const uint32_t base = smem_u32(sm + st * kStageBytes + kStKQ);
+    if (want_out<PREP>(ch, i)) {
+#pragma unroll 8
+      for (int v = lane + 32 * part; v < 2048; v += 32 * kConvertWarps) {
+        const uint4 u = lds_u32x4(base + v * 16);
+        st_shared_v4(base + v * 16, bf16x2_to_f16x2_m(u.x, mx), bf16x2_to_f16x2_m(u.y, mx),
+                     bf16x2_to_f16x2_m(u.z, mx), bf16x2_to_f16x2_m(u.w, mx));
+      }
+    } else {  // the K halves, at 0 and 16 KB
+#pragma unroll 8
+      for (int v = lane + 32 * part; v < 1024; v += 32 * kConvertWarps) {
+        const uint32_t a = base + (uint32_t)(v & 511) * 16 + (uint32_t)(v >> 9) * 16384;
+        const uint4 u = lds_u32x4(a);
+        st_shared_v4(a, bf16x2_to_f16x2_m(u.x, mx), bf16x2_to_f16x2_m(u.y, mx), bf16x2_to_f16x2_m(u.z, mx),
+                     bf16x2_to_f16x2_m(u.w, mx));
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->bar[kKqReady0 + st]);
+  }
+  if (!(mx < 65504.f)) atomicExch(&ctl->range_bad, 1);
 }
 
 // ----------------------------------------------------------------- MMA issuer
@@ -162,7 +222,9 @@ __device__ __noinline__ void producer_role(uint8_t* sm, Ctl* ctl, const Problem&
 //   U(i)  U^T . I into V' buffer i & 1, once the record has landed and the
 //         state warps have read that buffer's previous V' (C(i-2) issued)
 //   A(i)  V'^T += S (-W)^T and Y = S Q^T, after U(i) and s_ready(i), and
-//         once the output epilogue has read Y/O2 buffer i & 1 (yo_free(i-2))
+//         once the output epilogue has read Y/O2 buffer i & 1 (yo_free(i-2));
+//         Y (and everything after it that reads K or Q) also waits for the
+//         stage's fp16 K|Q (kq_ready(i))
 //   C(i)  D3 = V'^T diag(dec) K and O2 = V'^T P^T, after v_ready(i); then
 //         the record stage is released
 // issued in the order A(i), U(i+1), C(i): the chain's critical path runs
@@ -170,7 +232,7 @@ __device__ __noinline__ void producer_role(uint8_t* sm, Ctl* ctl, const Problem&
 // in while the state warps work on V'(i).  Waits block (suspending the warp)
 // rather than spin, leaving the issue slots to the epilogue warps.
 template <bool PREP>
-__device__ __noinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch, uint32_t tmem) {
+__device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch, uint32_t tmem) {
   const int n = ch.run_end - ch.run_begin;
   const uint32_t sS = smem_u32(sm + kSmS), sVp = smem_u32(sm + kSmVp), sVd = smem_u32(sm + kSmVd);
   const uint32_t sI = smem_u32(sm + kSmI);
@@ -204,6 +266,8 @@ __device__ __noinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch, ui
                (ch.has_u || ks > 0) ? 1u : 0u);
     }
     mma_commit(&ctl->bar[kVaDone]);
+    if (!wait_bar(ctl, kKqReady0 + (i & 1), (uint32_t)((i >> 1) & 1))) return;
+    tc_fence_after();
     if (want_out<PREP>(ch, i)) {
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {  // Y = S Q^T
@@ -234,9 +298,59 @@ __device__ __noinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch, ui
   }
 }
 
+// ----------------------------------------------------------------- output warps
+// O^T = scale (Y diag(gamma) + O2) for each chunk whose output is written:
+// thread (warp w, lane) takes d_v row 32 (w & 3) + lane and all 64 tokens,
+// 16 at a time, and writes them straight to global memory (a warp covers 64
+// contiguous bytes of each token's row).  Every chunk, written or not, ends
+// with yo_free, which releases Y/O2 buffer i & 1 to the MMA issuer.
+template <bool PREP>
+__device__ __forceinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem& p, const SegInfo& si,
+                                            const Chain& ch, uint32_t tmem, int j) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = (warp & 3) * 32 + lane;
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+  const int n = ch.run_end - ch.run_begin;
+  const size_t tstride = (size_t)p.h_v * kDim;
+  for (int i = 0; i < n; ++i) {
+    if (!wait_bar(ctl, kYoDone0 + (i & 1), (uint32_t)((i >> 1) & 1))) break;
+    if (want_out<PREP>(ch, i)) {
+      if (!wait_bar(ctl, kGates0 + (i & 3), (uint32_t)((i >> 2) & 1))) break;
+      tc_fence_after();
+      const uint32_t sGam = smem_u32(sm + kSmG + (i & 3) * 512);  // exp(G) [64]
+      const int64_t t0 = si.bos + (int64_t)(ch.run_begin + i) * kChunk;
+      const int cv = (int)min((int64_t)kChunk, si.eos - t0);
+      uint16_t* orow = reinterpret_cast<uint16_t*>(p.out) + ((size_t)t0 * p.h_v + j) * kDim + row;
+#pragma unroll 1
+      for (int tb = 0; tb < kChunk; tb += 16) {
+        uint32_t yq[16], o2[16];
+        tmem_ld16(tmem + lane_base + kTY + (i & 1) * 64 + tb, yq);
+        tmem_ld16(tmem + lane_base + kTO2 + (i & 1) * 64 + tb, o2);
+        float gm[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 g4 = lds_f32x4(sGam + (tb + 4 * q) * 4);
+          gm[4 * q] = g4.x;
+          gm[4 * q + 1] = g4.y;
+          gm[4 * q + 2] = g4.z;
+          gm[4 * q + 3] = g4.w;
+        }
+        tmem_ld_wait(yq, o2);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float o = p.scale * fmaf(gm[e], __uint_as_float(yq[e]), __uint_as_float(o2[e]));
+          if (tb + e < cv) orow[(size_t)(tb + e) * tstride] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+        }
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(&ctl->bar[kYoFree0 + (i & 1)]);  // Y/O2 buffer i & 1 read
+  }
+}
+
 // ----------------------------------------------------------------- state (chain) warps
 template <bool PREP>
-__device__ __noinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p, const SegInfo& si,
+__device__ __forceinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p, const SegInfo& si,
                                         const Chain& ch, uint32_t tmem, int j, int chain) {
   const int tid = threadIdx.x, warp = tid >> 5;
   const int row = tid & 127, half = tid >> 7;
@@ -333,42 +447,6 @@ __device__ __noinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p,
     fence_proxy_async_smem();
     tc_fence_before();
     mbar_arrive(&ctl->bar[kSReady]);
-    // output epilogue of this chunk (its O2 follows D3 on the tensor cores):
-    // O^T = scale (Y diag(gamma) + O2) for this thread's d_v row and 32 tokens,
-    // written straight to global memory (a warp covers 64 contiguous bytes
-    // of each token's row)
-    if (out) {
-      if (!wait_bar(ctl, kYoDone0 + (i & 1), (uint32_t)((i >> 1) & 1))) break;
-      tc_fence_after();
-      const int64_t t0 = si.bos + (int64_t)(ch.run_begin + i) * kChunk;
-      const int cv = (int)min((int64_t)kChunk, si.eos - t0);
-      uint16_t* orow = reinterpret_cast<uint16_t*>(p.out) + ((size_t)t0 * p.h_v + j) * kDim + row;
-      const size_t tstride = (size_t)p.h_v * kDim;
-#pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        const int tb = half * 32 + g * 16;
-        uint32_t yq[16], o2[16];
-        tmem_ld16(tmem + lane_base + kTY + (i & 1) * 64 + tb, yq);
-        tmem_ld16(tmem + lane_base + kTO2 + (i & 1) * 64 + tb, o2);
-        float gm[16];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 g4 = lds_f32x4(sGam + (tb + 4 * q) * 4);
-          gm[4 * q] = g4.x;
-          gm[4 * q + 1] = g4.y;
-          gm[4 * q + 2] = g4.z;
-          gm[4 * q + 3] = g4.w;
-        }
-        tmem_ld_wait(yq, o2);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float o = p.scale * fmaf(gm[e], __uint_as_float(yq[e]), __uint_as_float(o2[e]));
-          if (tb + e < cv) orow[(size_t)(tb + e) * tstride] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
-        }
-      }
-    }
-    tc_fence_before();
-    mbar_arrive(&ctl->bar[kYoFree0 + (i & 1)]);  // Y/O2 buffer i & 1 and gates slot i & 3 read
     done = i + 1;
   }
 #pragma unroll
@@ -389,7 +467,8 @@ __device__ __noinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p,
 }
 
 template <bool PREP>
-__global__ void __launch_bounds__(kThreads, 1) scan_kernel(const Problem p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    scan_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk, const Problem p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1024-byte aligned
   Ctl* ctl = reinterpret_cast<Ctl*>(sm + kSmCtl);
@@ -416,6 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(const Problem p) {
     if (tid == 0 && blockIdx.y == 0 && blockIdx.z == 0) report(p.status, kDevCheck, kDetSegMismatch);
   }
   Chain ch;
+  ch.bos = si.bos;
   ch.run_begin = si.cb;
   ch.run_end = si.ce;
   ch.out_begin = si.cb;
@@ -481,11 +561,13 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(const Problem p) {
   // ---- set-up ----
   if (tid == 0) {
     const int counts[kNumBars] = {1, 1, 1, 1, 1, 1, 1, 1, 1, kChainThreads, 1, kChainThreads,
-                                  1, 1, kChainThreads, kChainThreads};
+                                  1, 1, kOutThreads, kOutThreads, 1, 1, kConvertWarps, kConvertWarps};
     for (int b = 0; b < kNumBars; ++b) mbar_init(&ctl->bar[b], counts[b]);
     ctl->abort = 0;
     ctl->range_bad = 0;
     fence_mbar_init();
+    tma_prefetch_desc(&mq);
+    tma_prefetch_desc(&mk);
   }
   {  // 64 x 64 fp16 identity: row r has its 1 at column r
     const uint32_t sI = smem_u32(sm + kSmI);
@@ -507,11 +589,19 @@ __global__ void __launch_bounds__(kThreads, 1) scan_kernel(const Problem p) {
   const uint32_t tmem = ctl->tmem;
 
   if (warp < 8) {
+    setmaxnreg_inc<kChainRegs>();
     chain_role<PREP>(sm, ctl, p, si, ch, tmem, j, chain);
-  } else if (warp == kProducerWarp) {
-    producer_role<PREP>(sm, ctl, p, ch, j);
-  } else if (lane == 0) {
-    mma_role<PREP>(sm, ctl, ch, tmem);
+  } else {
+    setmaxnreg_dec<kOtherRegs>();
+    if (warp < kOutWarp + 4) {
+      output_role<PREP>(sm, ctl, p, si, ch, tmem, j);
+    } else if (warp == kProducerWarp) {
+      producer_role<PREP>(sm, ctl, p, ch, j, &mq, &mk);
+    } else if (warp >= kConvertWarp) {
+      convert_role<PREP>(sm, ctl, ch);
+    } else if (warp == kMmaWarp && lane == 0) {
+      mma_role<PREP>(sm, ctl, ch, tmem);
+    }
   }
   __syncwarp();
   tc_fence_before();
@@ -542,15 +632,16 @@ cudaError_t scan_kernel_setup() {
   return cudaFuncSetAttribute(scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
 }
 
-cudaError_t launch_scan_prep(const Problem& p, cudaStream_t st) {
+cudaError_t launch_scan_prep(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, cudaStream_t st) {
   dim3 grid(p.n_seg_total, p.h_v, 2);
-  scan_kernel<true><<<grid, kThreads, kSmemAlloc, st>>>(p);
+  scan_kernel<true><<<grid, kThreads, kSmemAlloc, st>>>(mq, mk, p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_scan_out(const Problem& p, int grid_x, cudaStream_t st) {
+cudaError_t launch_scan_out(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, int grid_x,
+                            cudaStream_t st) {
   dim3 grid(grid_x, p.h_v, 1);
-  scan_kernel<false><<<grid, kThreads, kSmemAlloc, st>>>(p);
+  scan_kernel<false><<<grid, kThreads, kSmemAlloc, st>>>(mq, mk, p);
   return cudaGetLastError();
 }
 

@@ -15,8 +15,7 @@
 // (bf16 MMAs on the exact K and V, with the A operands split into bf16 high
 // parts and remainders, so W and U keep about 16 significant bits of A)
 // and writes -W, U^T, P and (gamma, dec) as one record per (chunk, value
-// head), plus the fp16 copy of K and Q per (chunk, query/key head), each
-// tile in the 128-byte-swizzled layout the scan's MMAs read.
+// head), each tile in the 128-byte-swizzled layout the scan's MMAs read.
 //
 // One CTA of 256 threads per (chunk, value head), three CTAs per SM: the
 // shared-memory regions are reused as the work moves on (the A operands
@@ -66,10 +65,8 @@ static_assert(sizeof(WyCtl) <= kWySmemUse - kWyCtl, "control block too large");
 //   A_10 = -D_1 L_10 D_0, A_32 = -D_3 L_32 D_2       (16 x 16 blocks)
 //   A_hl = -A_hh L_hl A_ll                           (32 x 32 blocks)
 // The strict lower parts of the diagonal 32 x 32 blocks are cleared once
-// consumed, so every product runs over full ranges without masks.  `side`
-// runs on threads 64-255 during the substitution.
-template <class Side>
-__device__ __forceinline__ void solve_unit_lower(float* F, float* scratch, int tid, Side&& side) {
+// consumed, so every product runs over full ranges without masks.
+__device__ __forceinline__ void solve_unit_lower(float* F, float* scratch, int tid) {
   // ---- diagonal blocks ----
   {
     float x[16];
@@ -89,8 +86,6 @@ __device__ __forceinline__ void solve_unit_lower(float* F, float* scratch, int t
         }
         x[r] = (a[0] + a[1]) + (a[2] + a[3]);
       }
-    } else {
-      side();
     }
     __syncthreads();
     if (tid < 64) {  // row c of D_b^T; zero below the diagonal (L_bb has been consumed)
@@ -220,7 +215,6 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
     return false;
   }
   const int iq = (int)(((int64_t)j * p.h_qk) / p.h_v);
-  const bool first_of_group = j == (int)(((int64_t)iq * p.h_v + p.h_qk - 1) / p.h_qk);
   float* gts = reinterpret_cast<float*>(sm + kWyGates);
   float* sG = gts;
   float* sGam = gts + 64;
@@ -367,20 +361,8 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
   if (tid == 0 && p.plan_mode == kModeWarmup)
     p.chunk_exp[(size_t)gc * p.h_v + j] = sG[63] + ctl->warp_total[0] + ctl->warp_total[1];
 
-  // ---- A = (I + L)^{-1}; meanwhile threads 64-255 of the group's first CTA
-  //      write the fp16 copy of K|Q (same byte layout, converted chunk by chunk) ----
-  uint8_t* kq_rec = p.kq16 + ((size_t)gc * p.h_qk + iq) * kKqRecBytes;
-  solve_unit_lower(F, scratch, tid, [&]() {
-    if (!first_of_group) return;
-    const uint4* b4 = reinterpret_cast<const uint4*>(sm + kWyKQ);
-    uint4* g4 = reinterpret_cast<uint4*>(kq_rec);
-#pragma unroll 4
-    for (int v = tid - 64; v < 2048; v += kWyThreads - 64) {
-      const uint4 u = b4[v];
-      g4[v] = make_uint4(bf16x2_to_f16x2_m(u.x, mx), bf16x2_to_f16x2_m(u.y, mx), bf16x2_to_f16x2_m(u.z, mx),
-                         bf16x2_to_f16x2_m(u.w, mx));
-    }
-  });
+  // ---- A = (I + L)^{-1} ----
+  solve_unit_lower(F, scratch, tid);
 
   // ---- A operands: row s of A^T scaled by beta gamma (for W) / beta (for U),
   //      split into bf16 high parts and remainders; A diag(beta gamma) goes to

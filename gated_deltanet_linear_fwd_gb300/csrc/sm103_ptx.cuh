@@ -93,6 +93,16 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
 
 // ---------------------------------------------------------------- TMEM
 // Allocation is warp-collective; the base column address lands in *dst.
+// Per-warpgroup register limit (all threads of the warpgroup execute it).
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
                "r"(ncols)

@@ -124,7 +124,6 @@ typedef struct gdn_cp_plan_t {
   int n_chunks_total;   /* 64-token chunks summed over sequences */
   size_t off_chunk_map; /* chunk index: first chunk of each sequence, sequence of each chunk */
   size_t off_wy;        /* chunk-local records (-W, U, P, gates), 41472 bytes per (chunk, value head) */
-  size_t off_kq16;      /* fp16 K|Q tiles, 32768 bytes per (chunk, query/key head) */
 } gdn_cp_plan_t;
 
 /*
@@ -210,10 +209,9 @@ gdn_status gdn_cp_head_modes(const void* workspace, const gdn_cp_plan_t* plan, i
  * fixed 8 MiB device array built into the library instead; every GPU that
  * loads the library holds that array until the process exits.
  *   - Fits plans whose plan->workspace_bytes is at most 8 MiB: the chunk
- *     records take 41472 bytes per (chunk, value head) and 32768 per (chunk,
- *     query/key head), so about 150 chunk-heads (e.g. 1000 tokens with 6 value
- *     heads); larger plans are rejected with GDN_ERR_WORKSPACE before any
- *     device work.
+ *     records take 41472 bytes per (chunk, value head), so about 200
+ *     chunk-heads (e.g. 1000 tokens with 12 value heads); larger plans are
+ *     rejected with GDN_ERR_WORKSPACE before any device work.
  *   - Allocates nothing.  Its first call on a device looks up the array's
  *     device address (cudaGetSymbolAddress) with that device current; make
  *     that first call before any stream capture.

@@ -90,15 +90,14 @@ def test_plan_workspace_layout(lib):
     assert p.off_head % 256 == 0 and p.off_seg_bound % 256 == 0
     assert p.off_Sloc - p.off_R == 23 * 8 * mat and p.off_Sstart - p.off_Sloc == 23 * 8 * mat
     # chunk index (n_seqs + 1 int32, 16-byte chunk records) and the chunk warmup exponents,
-    # then the chunk records and fp16 K|Q tiles
+    # then the chunk records
     assert p.n_chunks_total == 512
     assert p.off_chunk_map == p.off_Sstart + 23 * 8 * mat
     assert p.off_wy % 1024 == 0 and p.off_wy >= p.off_chunk_map + 8 + 512 * 16 + 512 * 8 * 4
-    assert p.off_kq16 == p.off_wy + 512 * 8 * 41472
-    assert p.workspace_bytes == p.off_kq16 + 512 * 2 * 32768
+    assert p.workspace_bytes == p.off_wy + 512 * 8 * 41472
     st, p0 = plan(lib, 32768, h_v=8, mode=0)
     assert p0.off_R == p0.off_Sloc == p0.off_Sstart == 0  # no context parallelism: no segment states
-    assert p0.workspace_bytes == p0.off_kq16 + 512 * 2 * 32768
+    assert p0.workspace_bytes == p0.off_wy + 512 * 8 * 41472
 
 
 @pytest.mark.parametrize("kw,expect", [

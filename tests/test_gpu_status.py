@@ -43,3 +43,10 @@ def test_state_past_fp16_range_is_reported():
     w = make_inputs(700, h_qk=2, h_v=4, seed=3, with_h0=True, g_kind="zero")
     w = dataclasses.replace(w, h0=w.h0 * 1e7)  # the state's fp16 operand copy overflows
     assert _status(w, "off") == (DEVICE_CHECK, FP16_RANGE)
+
+
+@pytest.mark.parametrize("mode", ["off", "exact"])
+def test_query_past_fp16_range_is_reported(mode):
+    w = make_inputs(700, h_qk=2, h_v=4, seed=3)
+    w = dataclasses.replace(w, q=(w.q.float() * 1e6).to(torch.bfloat16))  # q itself has no fp16 image
+    assert _status(w, mode) == (DEVICE_CHECK, FP16_RANGE)
