@@ -210,8 +210,10 @@ gdn_status gdn_cp_head_modes(const void* workspace, const gdn_cp_plan_t* plan, i
  * loads the library holds that array until the process exits.
  *   - Fits plans whose plan->workspace_bytes is at most 8 MiB: the chunk
  *     records take 41472 bytes per (chunk, value head), so about 200
- *     chunk-heads (e.g. 1000 tokens with 12 value heads); larger plans are
- *     rejected with GDN_ERR_WORKSPACE before any device work.
+ *     chunk-heads (e.g. 1000 tokens with 12 value heads, context parallelism
+ *     off; with it, each segment adds 192 KB per value head of segment
+ *     states); larger plans are rejected with GDN_ERR_WORKSPACE before any
+ *     device work.
  *   - Allocates nothing.  Its first call on a device looks up the array's
  *     device address (cudaGetSymbolAddress) with that device current; make
  *     that first call before any stream capture.
