@@ -218,6 +218,23 @@ gdn_status encode_map(CUtensorMap* m, const void* base, int heads, int64_t token
   return GDN_OK;
 }
 
+// o: [tokens, h_v, 128] bf16 -> 3-D (d, head, token), whole 128 x 1 x 64 boxes, no swizzle
+// (the scan stores each chunk's o from a plain [64][128] shared-memory tile).
+gdn_status encode_out_map(CUtensorMap* m, void* base, int heads, int64_t tokens) {
+  cuuint64_t dims[3] = {(cuuint64_t)kDim, (cuuint64_t)heads, (cuuint64_t)(tokens > 0 ? tokens : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)kDim * 2, (cuuint64_t)heads * kDim * 2};
+  cuuint32_t box[3] = {(cuuint32_t)kDim, 1, (cuuint32_t)kChunk};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    g_last_cuda_error = (int)r;
+    return GDN_ERR_CUDA;
+  }
+  return GDN_OK;
+}
+
 // ---- fixed device workspace for callers that cannot allocate ----
 // 8 MiB: small problems only (the chunk records take 41472 bytes per
 // (chunk, value head) and 32768 per (chunk, query/key head)).
@@ -449,11 +466,12 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
     if ((e = log.after("recurrence_f32")) != cudaSuccess) return cuda_fail(e);
     return GDN_OK;
   }
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   const bool f32 = false;
   if ((st = encode_map(&mq, q, dims->h_qk, T_total, f32)) != GDN_OK) return st;
   if ((st = encode_map(&mk, k, dims->h_qk, T_total, f32)) != GDN_OK) return st;
   if ((st = encode_map(&mv, v, dims->h_v, T_total, f32)) != GDN_OK) return st;
+  if ((st = encode_out_map(&mo, out, dims->h_v, T_total)) != GDN_OK) return st;
 
   LaunchLog log{cs};
   if ((e = log.begin()) != cudaSuccess) return cuda_fail(e);
@@ -469,7 +487,7 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
     if ((e = launch_combine(p, g_sm_count[dev], cs)) != cudaSuccess) return cuda_fail(e);
     if ((e = log.after("combine")) != cudaSuccess) return cuda_fail(e);
   }
-  if ((e = launch_scan_out(p, mq, mk, plan->n_seg_total, cs)) != cudaSuccess) return cuda_fail(e);
+  if ((e = launch_scan_out(p, mq, mk, mo, plan->n_seg_total, cs)) != cudaSuccess) return cuda_fail(e);
   if ((e = log.after("scan_out")) != cudaSuccess) return cuda_fail(e);
   return GDN_OK;
 }

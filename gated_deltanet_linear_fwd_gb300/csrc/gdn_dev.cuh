@@ -89,6 +89,14 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2_m(uint32_t w, float& mx) {
   return pack_f16x2(lo, hi);
 }
 
+// Two packed bf16 times d -> two packed fp16 (round to nearest); folds the
+// magnitudes of the rounded values into mx.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled_m(uint32_t w, float d, float& mx) {
+  const float lo = __uint_as_float(w << 16) * d, hi = __uint_as_float(w & 0xffff0000u) * d;
+  mx = absmax_nan(absmax_nan(mx, lo), hi);
+  return pack_f16x2(lo, hi);
+}
+
 // Two packed bf16 -> two packed fp16 (round to nearest); flags out-of-range values.
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool& bad) {
   const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);

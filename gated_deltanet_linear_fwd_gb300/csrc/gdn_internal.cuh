@@ -244,8 +244,8 @@ cudaError_t launch_wy(const Problem& p, const CUtensorMap& mq, const CUtensorMap
                       cudaStream_t st);
 cudaError_t launch_scan_prep(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, cudaStream_t st);
 cudaError_t launch_combine(const Problem& p, int sm_count, cudaStream_t st);
-cudaError_t launch_scan_out(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, int grid_x,
-                            cudaStream_t st);
+cudaError_t launch_scan_out(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mo,
+                            int grid_x, cudaStream_t st);
 cudaError_t launch_recurrence_f32(const Problem& p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, bool f32, cudaStream_t st);
 cudaError_t scan_kernel_setup();

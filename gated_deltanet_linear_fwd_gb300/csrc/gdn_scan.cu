@@ -19,11 +19,12 @@
 //
 // Everything chunk-local (the gate cumsum, the WY form, P) comes from the
 // WY kernel's records as ready-made operand tiles; K and Q come straight
-// from the inputs (bf16, rounded to fp16 in shared memory).  Here, in the S
-// orientation (rows = d_v, columns = d_k), per chunk:
+// from the inputs (bf16, rounded to fp16 in shared memory, K scaled by the
+// decay to the chunk end on the way).  Here, in the S orientation (rows =
+// d_v, columns = d_k), per chunk:
 //   V'^T = U^T - S W^T        (U^T enters the accumulator as U^T . I)
 //   Y    = S Q^T
-//   S    = gamma_C S + V'^T diag(exp(G_last - G)) K
+//   S    = gamma_C S + V'^T (diag(exp(G_last - G)) K)
 //   O^T  = scale (Y diag(gamma) + V'^T P^T)
 // All are M = 128 tcgen05 MMAs (fp16 operands, fp32 accumulation in TMEM).
 // The state is kept fp32 in registers and rounded to fp16 once per chunk
@@ -33,10 +34,12 @@
 // Warp roles (512 threads, four warpgroups): warps 0-7 hold the state (row =
 // d_v lane, 64 columns each) and run the V' and state epilogues, the
 // critical path from one chunk to the next; warps 8-11 read Y and O2 and
-// write the chunk's outputs while the state warps go on to the next chunk;
+// stage the chunk's outputs in shared memory and store them (TMA) while
+// the state warps go on to the next chunk;
 // warp 12 loads each chunk's record (bulk copies) and its K and Q tiles
 // (TMA); lane 0 of warp 13 issues every MMA; warps 14-15 round the bf16 K
-// and Q tiles to fp16 in place, a chunk ahead of the MMAs that read them.
+// (times the decay to the chunk end) and Q tiles to fp16 in place, a chunk
+// ahead of the MMAs that read them.
 // The state warpgroups raise their register limit to 168 (the state takes
 // 64 per thread) and the others lower theirs to 88, within the 128 per
 // thread the block is launched with.  The roles hand over through
@@ -57,21 +60,22 @@ constexpr int kMmaWarp = 13;
 constexpr int kConvertWarp = 14;   // warps 14-15
 constexpr int kConvertWarps = 2;
 constexpr uint32_t kChainRegs = 168, kOtherRegs = 88;
+constexpr int kOutBarrier = 1;     // named barrier of the output warps
 static_assert(2 * 128 * kChainRegs + 2 * 128 * kOtherRegs <= 65536 && kThreads * 128 == 65536,
               "register split over the launch's 128 per thread");
 
 // ---- shared memory map (bytes from a 1024-byte aligned base) ----
 constexpr uint32_t kStageBytes = 73728;   // per chunk stage (two stages)
 constexpr uint32_t kStKQ = 0;             // [K d0-63 | Q d0-63 | K d64-127 | Q d64-127], 8 KB each:
-                                          // bf16 as loaded, then fp16 in place
+                                          // bf16 as loaded, then fp16 in place (K times dec)
 constexpr uint32_t kStWn = 32768;         // fp16 -W, MN-major B: rows d_k
 constexpr uint32_t kStU = 49152;          // fp16 U^T, K-major A: rows d_v
 constexpr uint32_t kStP = 65536;          // fp16 P, K-major B: rows r
 constexpr uint32_t kSmI = 2 * kStageBytes;  // fp16 64x64 identity, K-major B
 constexpr uint32_t kSmS = kSmI + 8192;      // fp16 state, K-major A: two 64-column halves of 16 KB
 constexpr uint32_t kSmVp = kSmS + 32768;    // fp16 V'^T, K-major A
-constexpr uint32_t kSmVd = kSmVp + 16384;   // fp16 V'^T diag(decay to chunk end), K-major A
-constexpr uint32_t kSmG = kSmVd + 16384;    // 4 slots (chunk i in slot i & 3): fp32 exp(G) [64], exp(G_63 - G) [64]
+constexpr uint32_t kSmO = kSmVp + 16384;    // bf16 o of one chunk, [64 tokens][128 d_v] rows of 256 bytes
+constexpr uint32_t kSmG = kSmO + 16384;     // 4 slots (chunk i in slot i & 3): fp32 exp(G) [64], exp(G_63 - G) [64]
 constexpr uint32_t kSmCtl = kSmG + 4 * 512; // barriers, TMEM base, flags
 constexpr uint32_t kSmemUse = kSmCtl + 256;
 constexpr uint32_t kSmemAlloc = kSmemUse + 1024;
@@ -181,10 +185,12 @@ __device__ __forceinline__ void producer_role(uint8_t* sm, Ctl* ctl, const Probl
 }
 
 // ----------------------------------------------------------------- K|Q rounding
-// Rounds each stage's bf16 K (and Q) tiles to fp16 in place (same byte
-// layout), then hands the stage to the MMA issuer.  The state's fp16 operand
-// copy keeps 11 significant bits, so the MMAs with K and Q run in fp16.
-// Values outside the fp16 range are reported through the status word.
+// Rounds each stage's bf16 tiles to fp16 in place (same byte layout): K
+// times dec = exp(G_63 - G) of its row (so D3 needs only the plain V'), and
+// Q where the chunk's output is written; then hands the stage to the MMA
+// issuer.  The state's fp16 operand copy keeps 11 significant bits, so the
+// MMAs with K and Q run in fp16.  Values outside the fp16 range are
+// reported through the status word.
 template <bool PREP>
 __device__ __forceinline__ void convert_role(uint8_t* sm, Ctl* ctl, const Chain& ch) {
   const int lane = threadIdx.x & 31, part = (threadIdx.x >> 5) - kConvertWarp;
@@ -192,19 +198,24 @@ __device__ __forceinline__ void convert_role(uint8_t* sm, Ctl* ctl, const Chain&
   float mx = 0.f;
   for (int i = 0; i < n; ++i) {
     const int st = i & 1;
-    if (!wait_bar(ctl, kKqFull0 + st, (uint32_t)((i >> 1) & 1))) break;
+    if (!wait_bar(ctl, kKqFull0 + st, (uint32_t)((i >> 1) & 1)) ||
+        !wait_bar(ctl, kGates0 + (i & 3), (uint32_t)((i >> 2) & 1)))
+      break;
     const uint32_t base = smem_u32(sm + st * kStageBytes + kStKQ);
-    if (want_out<PREP>(ch, i)) {
-#pragma unroll 8
-      for (int v = lane + 32 * part; v < 2048; v += 32 * kConvertWarps) {
-        const uint4 u = lds_u32x4(base + v * 16);
-        st_shared_v4(base + v * 16, bf16x2_to_f16x2_m(u.x, mx), bf16x2_to_f16x2_m(u.y, mx),
-                     bf16x2_to_f16x2_m(u.z, mx), bf16x2_to_f16x2_m(u.w, mx));
-      }
-    } else {  // the K halves, at 0 and 16 KB
-#pragma unroll 8
+    const uint32_t sDec = smem_u32(sm + kSmG + (i & 3) * 512 + 256);
+    // K halves at 0 and 16 KB: 16-byte vector v holds 8 dims of token row (v & 511) >> 3
+#pragma unroll 4
+    for (int v = lane + 32 * part; v < 1024; v += 32 * kConvertWarps) {
+      const uint32_t a = base + (uint32_t)(v & 511) * 16 + (uint32_t)(v >> 9) * 16384;
+      const float d = lds_f32(sDec + (uint32_t)((v & 511) >> 3) * 4);
+      const uint4 u = lds_u32x4(a);
+      st_shared_v4(a, bf16x2_to_f16x2_scaled_m(u.x, d, mx), bf16x2_to_f16x2_scaled_m(u.y, d, mx),
+                   bf16x2_to_f16x2_scaled_m(u.z, d, mx), bf16x2_to_f16x2_scaled_m(u.w, d, mx));
+    }
+    if (want_out<PREP>(ch, i)) {  // Q halves at 8 and 24 KB
+#pragma unroll 4
       for (int v = lane + 32 * part; v < 1024; v += 32 * kConvertWarps) {
-        const uint32_t a = base + (uint32_t)(v & 511) * 16 + (uint32_t)(v >> 9) * 16384;
+        const uint32_t a = base + 8192 + (uint32_t)(v & 511) * 16 + (uint32_t)(v >> 9) * 16384;
         const uint4 u = lds_u32x4(a);
         st_shared_v4(a, bf16x2_to_f16x2_m(u.x, mx), bf16x2_to_f16x2_m(u.y, mx), bf16x2_to_f16x2_m(u.z, mx),
                      bf16x2_to_f16x2_m(u.w, mx));
@@ -234,7 +245,7 @@ __device__ __forceinline__ void convert_role(uint8_t* sm, Ctl* ctl, const Chain&
 template <bool PREP>
 __device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch, uint32_t tmem) {
   const int n = ch.run_end - ch.run_begin;
-  const uint32_t sS = smem_u32(sm + kSmS), sVp = smem_u32(sm + kSmVp), sVd = smem_u32(sm + kSmVd);
+  const uint32_t sS = smem_u32(sm + kSmS), sVp = smem_u32(sm + kSmVp);
   const uint32_t sI = smem_u32(sm + kSmI);
   const uint32_t id_k = idesc_f16(128, 64, false, false);
   const uint32_t id_sw = idesc_f16(128, 64, false, true);
@@ -284,7 +295,7 @@ __device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch,
     tc_fence_after();
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)  // D3 = V'^T diag(dec) K
-      mma_bf16(tmem + kTD3, sdesc_sw128(sVd + ks * 32, 16, 1024), sdesc_sw128(stg + kStKQ + ks * 2048, 16384, 1024),
+      mma_bf16(tmem + kTD3, sdesc_sw128(sVp + ks * 32, 16, 1024), sdesc_sw128(stg + kStKQ + ks * 2048, 16384, 1024),
                id_d3, ks > 0);
     mma_commit(&ctl->bar[kD3Done]);
     if (want_out<PREP>(ch, i)) {
@@ -301,26 +312,32 @@ __device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch,
 // ----------------------------------------------------------------- output warps
 // O^T = scale (Y diag(gamma) + O2) for each chunk whose output is written:
 // thread (warp w, lane) takes d_v row 32 (w & 3) + lane and all 64 tokens,
-// 16 at a time, and writes them straight to global memory (a warp covers 64
-// contiguous bytes of each token's row).  Every chunk, written or not, ends
-// with yo_free, which releases Y/O2 buffer i & 1 to the MMA issuer.
+// 16 at a time, into the staging tile o[token][d_v] (a warp writes 64
+// contiguous bytes of a token row).  One thread then stores the tile: a
+// tensor store for a full chunk, one 256-byte bulk copy per token for a
+// sequence's partial last chunk (whose other rows belong to the next
+// sequence).  Every chunk, written or not, ends with yo_free, which
+// releases Y/O2 buffer i & 1 to the MMA issuer.
 template <bool PREP>
 __device__ __forceinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem& p, const SegInfo& si,
-                                            const Chain& ch, uint32_t tmem, int j) {
+                                            const Chain& ch, uint32_t tmem, int j, const CUtensorMap* mo) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool issuer = threadIdx.x == kOutWarp * 32;
   const int row = (warp & 3) * 32 + lane;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+  const uint32_t sO = smem_u32(sm + kSmO);
   const int n = ch.run_end - ch.run_begin;
-  const size_t tstride = (size_t)p.h_v * kDim;
   for (int i = 0; i < n; ++i) {
-    if (!wait_bar(ctl, kYoDone0 + (i & 1), (uint32_t)((i >> 1) & 1))) break;
-    if (want_out<PREP>(ch, i)) {
-      if (!wait_bar(ctl, kGates0 + (i & 3), (uint32_t)((i >> 2) & 1))) break;
+    const bool out = want_out<PREP>(ch, i);
+    bool ok = wait_bar(ctl, kYoDone0 + (i & 1), (uint32_t)((i >> 1) & 1));
+    if (ok && out) ok = wait_bar(ctl, kGates0 + (i & 3), (uint32_t)((i >> 2) & 1));
+    if (!out && !ok) break;
+    if (out) {
+      if (issuer) bulk_wait_read_all();  // the previous chunk's stores have read the tile
+      // the four warps pass the tile's barriers together or leave together
+      if (named_bar_or(kOutBarrier, kOutThreads, !ok)) break;
       tc_fence_after();
       const uint32_t sGam = smem_u32(sm + kSmG + (i & 3) * 512);  // exp(G) [64]
-      const int64_t t0 = si.bos + (int64_t)(ch.run_begin + i) * kChunk;
-      const int cv = (int)min((int64_t)kChunk, si.eos - t0);
-      uint16_t* orow = reinterpret_cast<uint16_t*>(p.out) + ((size_t)t0 * p.h_v + j) * kDim + row;
 #pragma unroll 1
       for (int tb = 0; tb < kChunk; tb += 16) {
         uint32_t yq[16], o2[16];
@@ -339,13 +356,27 @@ __device__ __forceinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const float o = p.scale * fmaf(gm[e], __uint_as_float(yq[e]), __uint_as_float(o2[e]));
-          if (tb + e < cv) orow[(size_t)(tb + e) * tstride] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+          sts_u16(sO + (uint32_t)(tb + e) * 256u + (uint32_t)row * 2u, __bfloat16_as_ushort(__float2bfloat16_rn(o)));
         }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(kOutBarrier, kOutThreads);
+      if (issuer) {
+        const int64_t t0 = si.bos + (int64_t)(ch.run_begin + i) * kChunk;
+        const int cv = (int)min((int64_t)kChunk, si.eos - t0);
+        if (cv == kChunk) {
+          tma_store_3d(mo, sm + kSmO, 0, j, (int)t0);
+        } else {
+          uint8_t* orow = reinterpret_cast<uint8_t*>(p.out) + ((size_t)t0 * p.h_v + j) * kDim * 2;
+          for (int r = 0; r < cv; ++r) bulk_store(orow + (size_t)r * p.h_v * kDim * 2, sm + kSmO + r * 256, 256u);
+        }
+        bulk_commit();
       }
     }
     tc_fence_before();
     mbar_arrive(&ctl->bar[kYoFree0 + (i & 1)]);  // Y/O2 buffer i & 1 read
   }
+  if (issuer) bulk_wait_all();  // the stores have landed before the block exits
 }
 
 // ----------------------------------------------------------------- state (chain) warps
@@ -379,7 +410,7 @@ __device__ __forceinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem&
   }
   const int n = ch.run_end - ch.run_begin;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-  const uint32_t sS = smem_u32(sm + kSmS), sVp = smem_u32(sm + kSmVp), sVd = smem_u32(sm + kSmVd);
+  const uint32_t sS = smem_u32(sm + kSmS), sVp = smem_u32(sm + kSmVp);
   // Largest magnitude this thread rounds to fp16: V' is checked every chunk
   // (|V' dec| <= |V'|); the state only at the end, since an fp16 overflow of
   // its operand copy would turn the next V' and so the state into inf/NaN.
@@ -397,12 +428,11 @@ __device__ __forceinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem&
   int done = 0;
   for (int i = 0; i < n; ++i) {
     const uint32_t par = (uint32_t)(i & 1);
-    const bool out = want_out<PREP>(ch, i);
     const uint32_t sGam = smem_u32(sm + kSmG + (i & 3) * 512);  // exp(G) [64], then dec [64]
     if (!wait_bar(ctl, kGates0 + (i & 3), (uint32_t)((i >> 2) & 1)) || !wait_bar(ctl, kVaDone, par)) break;
     tc_fence_after();
     const float gC = lds_f32(sGam + 63 * 4);
-    // V' operands: plain (for O) and decayed to the chunk end (for S)
+    // V' as the fp16 operand of D3 and O2 (the decay to the chunk end is in K)
     {
       uint32_t va[16], vb[16];
       tmem_ld16(tmem + lane_base + kTV + (i & 1) * 64 + half * 32, va);
@@ -412,17 +442,10 @@ __device__ __forceinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem&
       for (int q4 = 0; q4 < 4; ++q4) {
         const int g2 = q4 >> 1, q = q4 & 1;
         const float* f = reinterpret_cast<const float*>(g2 == 0 ? &va[q * 8] : &vb[q * 8]);
-        const uint32_t da = sGam + (64 + half * 32 + g2 * 16 + q * 8) * 4;
-        const float4 d0 = lds_f32x4(da), d1 = lds_f32x4(da + 16);
-        const float d[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-        const uint32_t off = sw128_offset(row, half * 4 + g2 * 2 + q);
 #pragma unroll
         for (int e = 0; e < 8; ++e) mx = absmax_nan(mx, f[e]);
-        if (out)
-          st_shared_v4(sVp + off, pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
-                       pack_f16x2(f[6], f[7]));
-        st_shared_v4(sVd + off, pack_f16x2(f[0] * d[0], f[1] * d[1]), pack_f16x2(f[2] * d[2], f[3] * d[3]),
-                     pack_f16x2(f[4] * d[4], f[5] * d[5]), pack_f16x2(f[6] * d[6], f[7] * d[7]));
+        st_shared_v4(sVp + sw128_offset(row, half * 4 + g2 * 2 + q), pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]),
+                     pack_f16x2(f[4], f[5]), pack_f16x2(f[6], f[7]));
       }
     }
     fence_proxy_async_smem();
@@ -468,7 +491,8 @@ __device__ __forceinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem&
 
 template <bool PREP>
 __global__ void __launch_bounds__(kThreads, 1)
-    scan_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk, const Problem p) {
+    scan_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                const __grid_constant__ CUtensorMap mo, const Problem p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1024-byte aligned
   Ctl* ctl = reinterpret_cast<Ctl*>(sm + kSmCtl);
@@ -568,6 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     tma_prefetch_desc(&mq);
     tma_prefetch_desc(&mk);
+    if (!PREP) tma_prefetch_desc(&mo);
   }
   {  // 64 x 64 fp16 identity: row r has its 1 at column r
     const uint32_t sI = smem_u32(sm + kSmI);
@@ -594,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     setmaxnreg_dec<kOtherRegs>();
     if (warp < kOutWarp + 4) {
-      output_role<PREP>(sm, ctl, p, si, ch, tmem, j);
+      output_role<PREP>(sm, ctl, p, si, ch, tmem, j, &mo);
     } else if (warp == kProducerWarp) {
       producer_role<PREP>(sm, ctl, p, ch, j, &mq, &mk);
     } else if (warp >= kConvertWarp) {
@@ -634,14 +659,14 @@ cudaError_t scan_kernel_setup() {
 
 cudaError_t launch_scan_prep(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, cudaStream_t st) {
   dim3 grid(p.n_seg_total, p.h_v, 2);
-  scan_kernel<true><<<grid, kThreads, kSmemAlloc, st>>>(mq, mk, p);
+  scan_kernel<true><<<grid, kThreads, kSmemAlloc, st>>>(mq, mk, mq, p);  // writes no output: o's map unused
   return cudaGetLastError();
 }
 
-cudaError_t launch_scan_out(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, int grid_x,
-                            cudaStream_t st) {
+cudaError_t launch_scan_out(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mo,
+                            int grid_x, cudaStream_t st) {
   dim3 grid(grid_x, p.h_v, 1);
-  scan_kernel<false><<<grid, kThreads, kSmemAlloc, st>>>(mq, mk, p);
+  scan_kernel<false><<<grid, kThreads, kSmemAlloc, st>>>(mq, mk, mo, p);
   return cudaGetLastError();
 }
 
