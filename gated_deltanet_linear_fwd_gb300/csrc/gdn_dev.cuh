@@ -43,28 +43,12 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return r;
 }
 
-// 8 consecutive floats -> one 16-byte fp16 chunk; flags values outside the fp16 range.
-__device__ __forceinline__ void store_f16x8(uint32_t addr, const float* f, bool& bad) {
-#pragma unroll
-  for (int e = 0; e < 8; ++e) bad |= !(fabsf(f[e]) < 65504.f);
-  st_shared_v4(addr, pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
-               pack_f16x2(f[6], f[7]));
-}
-
 // max(m, |x|), NaN-propagating: a running bound on what went into fp16
 // operands (checked once against the fp16 range at the end).
 __device__ __forceinline__ float absmax_nan(float m, float x) {
   float r;
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(m), "f"(fabsf(x)));
   return r;
-}
-
-// 8 consecutive floats -> one 16-byte fp16 chunk; folds their magnitudes into mx.
-__device__ __forceinline__ void store_f16x8_m(uint32_t addr, const float* f, float& mx) {
-#pragma unroll
-  for (int e = 0; e < 8; ++e) mx = absmax_nan(mx, f[e]);
-  st_shared_v4(addr, pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
-               pack_f16x2(f[6], f[7]));
 }
 
 // 8 consecutive floats -> bf16 high parts and bf16 remainders (x = hi + lo to
@@ -82,26 +66,12 @@ __device__ __forceinline__ void store_bf16x8_hilo(uint32_t addr_hi, uint32_t add
   st_shared_v4(addr_lo, l[0], l[1], l[2], l[3]);
 }
 
-// Two packed bf16 -> two packed fp16 (round to nearest); folds their magnitudes into mx.
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2_m(uint32_t w, float& mx) {
-  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
-  mx = absmax_nan(absmax_nan(mx, lo), hi);
-  return pack_f16x2(lo, hi);
+// Two packed bf16 (times d) -> two packed fp16, round to nearest.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
-
-// Two packed bf16 times d -> two packed fp16 (round to nearest); folds the
-// magnitudes of the rounded values into mx.
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled_m(uint32_t w, float d, float& mx) {
-  const float lo = __uint_as_float(w << 16) * d, hi = __uint_as_float(w & 0xffff0000u) * d;
-  mx = absmax_nan(absmax_nan(mx, lo), hi);
-  return pack_f16x2(lo, hi);
-}
-
-// Two packed bf16 -> two packed fp16 (round to nearest); flags out-of-range values.
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool& bad) {
-  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
-  bad |= !(fabsf(lo) < 65504.f) || !(fabsf(hi) < 65504.f);
-  return pack_f16x2(lo, hi);
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float d) {
+  return pack_f16x2(__uint_as_float(w << 16) * d, __uint_as_float(w & 0xffff0000u) * d);
 }
 
 // Instruction descriptor for kind::f16 with fp16 A/B and fp32 D.

@@ -65,22 +65,31 @@ static_assert(2 * 128 * kChainRegs + 2 * 128 * kOtherRegs <= 65536 && kThreads *
               "register split over the launch's 128 per thread");
 
 // ---- shared memory map (bytes from a 1024-byte aligned base) ----
-constexpr uint32_t kStageBytes = 73728;   // per chunk stage (two stages)
-constexpr uint32_t kStKQ = 0;             // [K d0-63 | Q d0-63 | K d64-127 | Q d64-127], 8 KB each:
-                                          // bf16 as loaded, then fp16 in place (K times dec)
-constexpr uint32_t kStWn = 32768;         // fp16 -W, MN-major B: rows d_k
-constexpr uint32_t kStU = 49152;          // fp16 U^T, K-major A: rows d_v
-constexpr uint32_t kStP = 65536;          // fp16 P, K-major B: rows r
+// Two rings of two slots each: ring A holds what the chunk's first MMAs
+// read (-W, U^T) and is released as soon as A(i) has run; ring B holds K, Q
+// and P, read up to the end of the chunk.  So the loads for chunk i + 2 of
+// ring A start about a chunk earlier than they could if one stage held all.
+constexpr uint32_t kRingA = 0;            // 2 slots of 32 KB:
+constexpr uint32_t kSlotA = 32768;
+constexpr uint32_t kAWn = 0;              //   fp16 -W, MN-major B: rows d_k
+constexpr uint32_t kAU = 16384;           //   fp16 U^T, K-major A: rows d_v
+constexpr uint32_t kRingB = 2 * kSlotA;   // 2 slots of 40 KB:
+constexpr uint32_t kSlotB = 40960;
+constexpr uint32_t kBKQ = 0;              //   [K d0-63 | Q d0-63 | K d64-127 | Q d64-127], 8 KB each: bf16 as
+                                          //   loaded, then fp16 in place (K times dec)
+constexpr uint32_t kBP = 32768;           //   fp16 P, K-major B: rows r
+constexpr uint32_t kStageBytes = 73728;   // per chunk over both rings
 constexpr uint32_t kSmI = 2 * kStageBytes;  // fp16 64x64 identity, K-major B
 constexpr uint32_t kSmS = kSmI + 8192;      // fp16 state, K-major A: two 64-column halves of 16 KB
 constexpr uint32_t kSmVp = kSmS + 32768;    // fp16 V'^T, K-major A
 constexpr uint32_t kSmO = kSmVp + 16384;    // bf16 o of one chunk, [64 tokens][128 d_v] rows of 256 bytes
 constexpr uint32_t kSmG = kSmO + 16384;     // 4 slots (chunk i in slot i & 3): fp32 exp(G) [64], exp(G_63 - G) [64]
 constexpr uint32_t kSmCtl = kSmG + 4 * 512; // barriers, TMEM base, flags
-constexpr uint32_t kSmemUse = kSmCtl + 256;
+constexpr uint32_t kSmemUse = kSmCtl + 512;
 constexpr uint32_t kSmemAlloc = kSmemUse + 1024;
 static_assert(kSmemAlloc <= 232448, "shared memory over the per-block limit");
-static_assert(kStP + 8192 <= kStageBytes && kStageBytes % 1024 == 0, "stage layout");
+static_assert(kRingB + 2 * kSlotB == 2 * kStageBytes && kSlotB % 1024 == 0 && kBP + 8192 <= kSlotB,
+              "ring layout");
 
 // ---- TMEM columns (512 allocated) ----
 constexpr uint32_t kTV = 0;     // U^T then V'^T, 2 buffers    128 x 64 each
@@ -92,11 +101,14 @@ enum InitKind { kInitZero = 0, kInitIdentity = 1, kInitH0 = 2, kInitStart = 3 };
 
 // mbarrier indices
 enum Bar {
-  kFull0 = 0, kFull1, kEmpty0, kEmpty1,    // record stages
+  kFull0 = 0, kFull1, kEmpty0, kEmpty1,    // ring A slots (-W, U^T): loaded / released
   kGates0, kGates1, kGates2, kGates3,      // gates ring slots (loaded)
   kVaDone, kVReady, kD3Done, kSReady,      // state pipeline
   kYoDone0, kYoDone1, kYoFree0, kYoFree1,  // output epilogue (two Y/O2 buffers)
-  kKqFull0, kKqFull1, kKqReady0, kKqReady1,  // K|Q tiles loaded (bf16) / rounded to fp16
+  kKqFull0, kKqFull1,                      // ring B slots loaded (K|Q bf16, P)
+  kKReady0, kKReady1, kQReady0, kQReady1,  // K, then Q, rounded to fp16
+  kYDone,                                  // Y read the state's fp16 copy
+  kEmptyB0, kEmptyB1,                      // ring B slots released
   kNumBars
 };
 
@@ -144,64 +156,81 @@ __device__ __forceinline__ bool want_out(const Chain& ch, int i) {
 }
 
 // ----------------------------------------------------------------- producer
-// Loads each chunk's K and Q tiles (TMA, 64 tokens x 64 dims per box, rows
-// past the end of the input read as zero) and its record tiles (bulk
-// copies) into its stage.
+// Loads each chunk's ring B tiles (K and Q by TMA, 64 tokens x 64 dims per
+// box, rows past the end of the input read as zero; P by a bulk copy) and
+// gates, and, a chunk ahead, its ring A tiles (-W, U^T; bulk copies).  The
+// waits come in the order the slots are released: ring B of chunk i - 2
+// (end of that chunk), then ring A of chunk i - 1 (after its A).
 template <bool PREP>
 __device__ __forceinline__ void producer_role(uint8_t* sm, Ctl* ctl, const Problem& p, const Chain& ch, int j,
                                            const CUtensorMap* mq, const CUtensorMap* mk) {
   if ((threadIdx.x & 31) != 0) return;
   const int n = ch.run_end - ch.run_begin;
+  auto rec_of = [&](int i) { return p.wy + (((size_t)ch.chunk0 + ch.run_begin + i) * p.h_v + j) * kRecBytes; };
+  auto load_a = [&](int i) {
+    uint8_t* slot = sm + kRingA + (i & 1) * kSlotA;
+    uint64_t* bar = &ctl->bar[kFull0 + (i & 1)];
+    mbar_arrive_expect_tx(bar, ch.has_u ? 32768u : 16384u);
+    bulk_load(slot + kAWn, rec_of(i) + kRecWn, 16384u, bar);
+    if (ch.has_u) bulk_load(slot + kAU, rec_of(i) + kRecU, 16384u, bar);
+  };
+  if (n > 0) load_a(0);
   for (int i = 0; i < n; ++i) {
-    const int st = i & 1;
-    if (i >= 2 && !wait_bar(ctl, kEmpty0 + st, (uint32_t)(((i - 2) >> 1) & 1))) return;
-    const size_t gc = (size_t)ch.chunk0 + ch.run_begin + i;
-    const uint8_t* rec = p.wy + (gc * p.h_v + j) * kRecBytes;
+    if (i >= 2 && !wait_bar(ctl, kEmptyB0 + (i & 1), (uint32_t)(((i - 2) >> 1) & 1))) return;
     const bool out = want_out<PREP>(ch, i);
-    uint8_t* stg = sm + st * kStageBytes;
+    uint8_t* slot = sm + kRingB + (i & 1) * kSlotB;
     const int t0 = (int)(ch.bos + (int64_t)(ch.run_begin + i) * kChunk);
-    uint64_t* kbar = &ctl->bar[kKqFull0 + st];
-    mbar_arrive_expect_tx(kbar, out ? 32768u : 16384u);
-    tma_load_3d(stg + kStKQ, mk, kbar, 0, ch.iq, t0);
-    tma_load_3d(stg + kStKQ + 16384, mk, kbar, 64, ch.iq, t0);
-    if (out) {  // Q only where the chunk's output is written
-      tma_load_3d(stg + kStKQ + 8192, mq, kbar, 0, ch.iq, t0);
-      tma_load_3d(stg + kStKQ + 24576, mq, kbar, 64, ch.iq, t0);
+    uint64_t* kbar = &ctl->bar[kKqFull0 + (i & 1)];
+    mbar_arrive_expect_tx(kbar, out ? 40960u : 16384u);
+    tma_load_3d(slot + kBKQ, mk, kbar, 0, ch.iq, t0);
+    tma_load_3d(slot + kBKQ + 16384, mk, kbar, 64, ch.iq, t0);
+    if (out) {  // Q and P only where the chunk's output is written
+      tma_load_3d(slot + kBKQ + 8192, mq, kbar, 0, ch.iq, t0);
+      tma_load_3d(slot + kBKQ + 24576, mq, kbar, 64, ch.iq, t0);
+      bulk_load(slot + kBP, rec_of(i) + kRecP, 8192u, kbar);
     }
-    uint64_t* bar = &ctl->bar[kFull0 + st];
-    const uint32_t bytes = 16384u + (ch.has_u ? 16384u : 0u) + (out ? 8192u : 0u);
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_load(stg + kStWn, rec + kRecWn, 16384u, bar);
-    if (ch.has_u) bulk_load(stg + kStU, rec + kRecU, 16384u, bar);
-    if (out) bulk_load(stg + kStP, rec + kRecP, 8192u, bar);
     // The gates go to ring slot i & 3.  Its readers of chunk i - 4 are done:
-    // the state warps read those gates in the V' epilogue of chunk i - 4, the
-    // output warps before yo_free(i - 4), which A(i - 2) waited for, and
-    // stage i & 1 is free only after C(i - 2).
+    // the converter before k_ready(i - 4), the state warps in the V' epilogue
+    // of chunk i - 4 (before v_ready(i - 4)), both waited for before D3(i - 4)
+    // was issued, and the output warps before yo_free(i - 4), which A(i - 2)
+    // waited for; ring B of chunk i - 2 is released after all of these.
     uint64_t* gbar = &ctl->bar[kGates0 + (i & 3)];
     mbar_arrive_expect_tx(gbar, 512u);
-    bulk_load(sm + kSmG + (i & 3) * 512, rec + kRecGam, 512u, gbar);
+    bulk_load(sm + kSmG + (i & 3) * 512, rec_of(i) + kRecGam, 512u, gbar);
+    if (i + 1 < n) {
+      if (i + 1 >= 2 && !wait_bar(ctl, kEmpty0 + ((i + 1) & 1), (uint32_t)(((i - 1) >> 1) & 1))) return;
+      load_a(i + 1);
+    }
   }
 }
 
-// ----------------------------------------------------------------- K|Q rounding
-// Rounds each stage's bf16 tiles to fp16 in place (same byte layout): K
-// times dec = exp(G_63 - G) of its row (so D3 needs only the plain V'), and
-// Q where the chunk's output is written; then hands the stage to the MMA
-// issuer.  The state's fp16 operand copy keeps 11 significant bits, so the
-// MMAs with K and Q run in fp16.  Values outside the fp16 range are
-// reported through the status word.
+// ----------------------------------------------------------------- K and Q rounding
+// bf16 tiles are rounded to fp16 in place (same byte layout): the state's
+// fp16 operand copy keeps 11 significant bits, so the MMAs with K and Q run
+// in fp16.  K is multiplied by dec = exp(G_63 - G) of its row on the way (so
+// D3 needs only the plain V'); the converter warps do K and hand it over by
+// k_ready, the output warps do Q (two chunks ahead, between their output
+// tiles) and hand it over by q_ready.  A value outside the fp16 range turns
+// into inf in V', the state or o, which are checked.
+__device__ __forceinline__ void round_q_tile(uint32_t base, int t, int nthreads) {
+#pragma unroll 2
+  for (int v = t; v < 1024; v += nthreads) {  // Q halves at 8 and 24 KB
+    const uint32_t a = base + 8192 + (uint32_t)(v & 511) * 16 + (uint32_t)(v >> 9) * 16384;
+    const uint4 u = lds_u32x4(a);
+    st_shared_v4(a, bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
+  }
+}
+
 template <bool PREP>
 __device__ __forceinline__ void convert_role(uint8_t* sm, Ctl* ctl, const Chain& ch) {
   const int lane = threadIdx.x & 31, part = (threadIdx.x >> 5) - kConvertWarp;
   const int n = ch.run_end - ch.run_begin;
-  float mx = 0.f;
   for (int i = 0; i < n; ++i) {
     const int st = i & 1;
     if (!wait_bar(ctl, kKqFull0 + st, (uint32_t)((i >> 1) & 1)) ||
         !wait_bar(ctl, kGates0 + (i & 3), (uint32_t)((i >> 2) & 1)))
       break;
-    const uint32_t base = smem_u32(sm + st * kStageBytes + kStKQ);
+    const uint32_t base = smem_u32(sm + kRingB + st * kSlotB + kBKQ);
     const uint32_t sDec = smem_u32(sm + kSmG + (i & 3) * 512 + 256);
     // K halves at 0 and 16 KB: 16-byte vector v holds 8 dims of token row (v & 511) >> 3
 #pragma unroll 4
@@ -209,39 +238,30 @@ __device__ __forceinline__ void convert_role(uint8_t* sm, Ctl* ctl, const Chain&
       const uint32_t a = base + (uint32_t)(v & 511) * 16 + (uint32_t)(v >> 9) * 16384;
       const float d = lds_f32(sDec + (uint32_t)((v & 511) >> 3) * 4);
       const uint4 u = lds_u32x4(a);
-      st_shared_v4(a, bf16x2_to_f16x2_scaled_m(u.x, d, mx), bf16x2_to_f16x2_scaled_m(u.y, d, mx),
-                   bf16x2_to_f16x2_scaled_m(u.z, d, mx), bf16x2_to_f16x2_scaled_m(u.w, d, mx));
-    }
-    if (want_out<PREP>(ch, i)) {  // Q halves at 8 and 24 KB
-#pragma unroll 4
-      for (int v = lane + 32 * part; v < 1024; v += 32 * kConvertWarps) {
-        const uint32_t a = base + 8192 + (uint32_t)(v & 511) * 16 + (uint32_t)(v >> 9) * 16384;
-        const uint4 u = lds_u32x4(a);
-        st_shared_v4(a, bf16x2_to_f16x2_m(u.x, mx), bf16x2_to_f16x2_m(u.y, mx), bf16x2_to_f16x2_m(u.z, mx),
-                     bf16x2_to_f16x2_m(u.w, mx));
-      }
+      st_shared_v4(a, bf16x2_to_f16x2_scaled(u.x, d), bf16x2_to_f16x2_scaled(u.y, d), bf16x2_to_f16x2_scaled(u.z, d),
+                   bf16x2_to_f16x2_scaled(u.w, d));
     }
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&ctl->bar[kKqReady0 + st]);
+    if (lane == 0) mbar_arrive(&ctl->bar[kKReady0 + st]);
   }
-  if (!(mx < 65504.f)) atomicExch(&ctl->range_bad, 1);
 }
 
 // ----------------------------------------------------------------- MMA issuer
-// Three groups per chunk i:
-//   U(i)  U^T . I into V' buffer i & 1, once the record has landed and the
-//         state warps have read that buffer's previous V' (C(i-2) issued)
-//   A(i)  V'^T += S (-W)^T and Y = S Q^T, after U(i) and s_ready(i), and
-//         once the output epilogue has read Y/O2 buffer i & 1 (yo_free(i-2));
-//         Y (and everything after it that reads K or Q) also waits for the
-//         stage's fp16 K|Q (kq_ready(i))
-//   C(i)  D3 = V'^T diag(dec) K and O2 = V'^T P^T, after v_ready(i); then
-//         the record stage is released
-// issued in the order A(i), U(i+1), C(i): the chain's critical path runs
-// A(i) -> V' epilogue -> C(i) -> state epilogue -> A(i+1), and U(i+1) fits
-// in while the state warps work on V'(i).  Waits block (suspending the warp)
-// rather than spin, leaving the issue slots to the epilogue warps.
+// Per chunk i, in this order:
+//   A(i)  V'^T += S (-W)^T, once s_ready(i) has published the state's fp16
+//         copy and the output warps have read O buffer i & 1 (yo_free(i-2));
+//         commits va_done
+//   D3(i) V'^T (diag(dec) K), after v_ready(i) and k_ready(i); commits d3_done
+//   Y(i)  S Q^T into O buffer i & 1, after q_ready(i); commits y_done, after
+//         which the state warps may overwrite the state's copy
+//   O2(i) V'^T P^T; commits yo_done(i)
+//   then ring B of chunk i is released (ring A was, right after A(i)), and
+//   U(i+1) U^T . I into V' buffer (i+1) & 1 (read by the state warps for
+//         chunk i-1) once the next record has landed
+// The chain's critical path runs A(i) -> V' epilogue -> D3(i) -> state
+// epilogue -> A(i+1); Y, O2 and U run on the tensor cores while the state
+// warps work on the state, never between A(i) and D3(i).
 template <bool PREP>
 __device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch, uint32_t tmem) {
   const int n = ch.run_end - ch.run_begin;
@@ -250,62 +270,60 @@ __device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch,
   const uint32_t id_k = idesc_f16(128, 64, false, false);
   const uint32_t id_sw = idesc_f16(128, 64, false, true);
   const uint32_t id_d3 = idesc_f16(128, 128, false, true);
-  auto issue_u = [&](int i) {
-    if (!ch.has_u) return;
-    const uint32_t sU = smem_u32(sm + (i & 1) * kStageBytes + kStU);
+  auto issue_u = [&](int i) -> bool {
+    if (!wait_bar(ctl, kFull0 + (i & 1), (uint32_t)((i >> 1) & 1))) return false;
+    if (!ch.has_u) return true;
+    const uint32_t sU = smem_u32(sm + kRingA + (i & 1) * kSlotA + kAU);
     tc_fence_after();
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
       mma_bf16(tmem + kTV + (i & 1) * 64, sdesc_sw128(sU + ks * 32, 16, 1024), sdesc_sw128(sI + ks * 32, 16, 1024),
                id_k, ks > 0);
+    return true;
   };
-  int nu = 0;  // U groups issued
+  if (n > 0 && !issue_u(0)) return;
   for (int i = 0; i < n; ++i) {
-    const uint32_t stg = smem_u32(sm + (i & 1) * kStageBytes);
-    if (nu == i) {
-      if (!wait_bar(ctl, kFull0 + (i & 1), (uint32_t)((i >> 1) & 1))) return;
-      issue_u(i);
-      ++nu;
-    }
+    const uint32_t sA = smem_u32(sm + kRingA + (i & 1) * kSlotA), sB = smem_u32(sm + kRingB + (i & 1) * kSlotB);
+    const bool out = want_out<PREP>(ch, i);
     if (!spin_bar(ctl, kSReady, (uint32_t)(i & 1))) return;
     if (i >= 2 && !wait_bar(ctl, kYoFree0 + (i & 1), (uint32_t)(((i - 2) >> 1) & 1))) return;
     tc_fence_after();
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {  // V'^T += S (-W)^T
       const uint64_t a = sdesc_sw128(sS + (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u, 16, 1024);
-      mma_bf16(tmem + kTV + (i & 1) * 64, a, sdesc_sw128(stg + kStWn + ks * 2048, 8192, 1024), id_sw,
+      mma_bf16(tmem + kTV + (i & 1) * 64, a, sdesc_sw128(sA + kAWn + ks * 2048, 8192, 1024), id_sw,
                (ch.has_u || ks > 0) ? 1u : 0u);
     }
     mma_commit(&ctl->bar[kVaDone]);
-    if (!wait_bar(ctl, kKqReady0 + (i & 1), (uint32_t)((i >> 1) & 1))) return;
-    tc_fence_after();
-    if (want_out<PREP>(ch, i)) {
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {  // Y = S Q^T
-        const uint32_t off = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
-        mma_bf16(tmem + kTY + (i & 1) * 64, sdesc_sw128(sS + off, 16, 1024),
-                 sdesc_sw128(stg + kStKQ + 8192 + off, 16, 1024), id_k, ks > 0);
-      }
-    }
-    if (i + 1 < n && mbar_test_wait(&ctl->bar[kFull0 + ((i + 1) & 1)], (uint32_t)(((i + 1) >> 1) & 1))) {
-      issue_u(i + 1);  // its V' buffer was released by C(i - 1)
-      ++nu;
-    }
+    mma_commit(&ctl->bar[kEmpty0 + (i & 1)]);  // ring A slot read (U(i), A(i))
+    if (!wait_bar(ctl, kKReady0 + (i & 1), (uint32_t)((i >> 1) & 1))) return;
     if (!spin_bar(ctl, kVReady, (uint32_t)(i & 1))) return;
     tc_fence_after();
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)  // D3 = V'^T diag(dec) K
-      mma_bf16(tmem + kTD3, sdesc_sw128(sVp + ks * 32, 16, 1024), sdesc_sw128(stg + kStKQ + ks * 2048, 16384, 1024),
+      mma_bf16(tmem + kTD3, sdesc_sw128(sVp + ks * 32, 16, 1024), sdesc_sw128(sB + kBKQ + ks * 2048, 16384, 1024),
                id_d3, ks > 0);
     mma_commit(&ctl->bar[kD3Done]);
-    if (want_out<PREP>(ch, i)) {
+    if (out) {
+      if (!wait_bar(ctl, kQReady0 + (i & 1), (uint32_t)((i >> 1) & 1))) return;
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {  // Y = S Q^T
+        const uint32_t off = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+        mma_bf16(tmem + kTY + (i & 1) * 64, sdesc_sw128(sS + off, 16, 1024),
+                 sdesc_sw128(sB + kBKQ + 8192 + off, 16, 1024), id_k, ks > 0);
+      }
+    }
+    mma_commit(&ctl->bar[kYDone]);
+    if (out) {
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)  // O2 = V'^T P^T
         mma_bf16(tmem + kTO2 + (i & 1) * 64, sdesc_sw128(sVp + ks * 32, 16, 1024),
-                 sdesc_sw128(stg + kStP + ks * 32, 16, 1024), id_k, ks > 0);
+                 sdesc_sw128(sB + kBP + ks * 32, 16, 1024), id_k, ks > 0);
     }
     mma_commit(&ctl->bar[kYoDone0 + (i & 1)]);
-    mma_commit(&ctl->bar[kEmpty0 + (i & 1)]);
+    mma_commit(&ctl->bar[kEmptyB0 + (i & 1)]);  // ring B slot read
+    if (i + 1 < n && !issue_u(i + 1)) return;  // its V' buffer was read in the V' epilogue of chunk i - 1
   }
 }
 
@@ -327,6 +345,21 @@ __device__ __forceinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   const uint32_t sO = smem_u32(sm + kSmO);
   const int n = ch.run_end - ch.run_begin;
+  float mx = 0.f;  // largest |o| (inf or NaN when an fp16 operand overflowed)
+  // Q of chunk c rounded to fp16 (chunks with no output: nothing to round),
+  // then q_ready(c); every chunk gets its q_ready, so its phases follow c.
+  auto round_q = [&](int c) -> bool {
+    if (want_out<PREP>(ch, c)) {
+      if (!wait_bar(ctl, kKqFull0 + (c & 1), (uint32_t)((c >> 1) & 1))) return false;
+      round_q_tile(smem_u32(sm + kRingB + (c & 1) * kSlotB + kBKQ), threadIdx.x - kOutWarp * 32, kOutThreads);
+      fence_proxy_async_smem();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->bar[kQReady0 + (c & 1)]);
+    return true;
+  };
+  for (int c = 0; c < 2 && c < n; ++c)
+    if (!round_q(c)) return;
   for (int i = 0; i < n; ++i) {
     const bool out = want_out<PREP>(ch, i);
     bool ok = wait_bar(ctl, kYoDone0 + (i & 1), (uint32_t)((i >> 1) & 1));
@@ -356,6 +389,7 @@ __device__ __forceinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const float o = p.scale * fmaf(gm[e], __uint_as_float(yq[e]), __uint_as_float(o2[e]));
+          mx = absmax_nan(mx, o);
           sts_u16(sO + (uint32_t)(tb + e) * 256u + (uint32_t)row * 2u, __bfloat16_as_ushort(__float2bfloat16_rn(o)));
         }
       }
@@ -375,8 +409,10 @@ __device__ __forceinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem
     }
     tc_fence_before();
     mbar_arrive(&ctl->bar[kYoFree0 + (i & 1)]);  // Y/O2 buffer i & 1 read
+    if (i + 2 < n && !round_q(i + 2)) break;  // its ring B slot was released with yo_done(i)
   }
   if (issuer) bulk_wait_all();  // the stores have landed before the block exits
+  if (!(mx <= 3.4028235e38f)) atomicExch(&ctl->range_bad, 1);
 }
 
 // ----------------------------------------------------------------- state (chain) warps
@@ -466,6 +502,7 @@ __device__ __forceinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem&
         S[g8 * 32 + 16 + e] = fmaf(gC, S[g8 * 32 + 16 + e], __uint_as_float(rb[e]));
       }
     }
+    if (!wait_bar(ctl, kYDone, par)) break;  // Y(i) has read the state's copy
     store_state();
     fence_proxy_async_smem();
     tc_fence_before();
@@ -585,7 +622,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- set-up ----
   if (tid == 0) {
     const int counts[kNumBars] = {1, 1, 1, 1, 1, 1, 1, 1, 1, kChainThreads, 1, kChainThreads,
-                                  1, 1, kOutThreads, kOutThreads, 1, 1, kConvertWarps, kConvertWarps};
+                                  1, 1, kOutThreads, kOutThreads, 1, 1, kConvertWarps, kConvertWarps,
+                                  kOutThreads / 32, kOutThreads / 32, 1, 1, 1};
     for (int b = 0; b < kNumBars; ++b) mbar_init(&ctl->bar[b], counts[b]);
     ctl->abort = 0;
     ctl->range_bad = 0;
