@@ -65,19 +65,19 @@ static_assert(2 * 128 * kChainRegs + 2 * 128 * kOtherRegs <= 65536 && kThreads *
               "register split over the launch's 128 per thread");
 
 // ---- shared memory map (bytes from a 1024-byte aligned base) ----
-// Two rings of two slots each: ring A holds what the chunk's first MMAs
-// read (-W, U^T) and is released as soon as A(i) has run; ring B holds K, Q
-// and P, read up to the end of the chunk.  So the loads for chunk i + 2 of
-// ring A start about a chunk earlier than they could if one stage held all.
+// Three rings of two slots each, each released as soon as its last reader
+// has run: ring A (-W, U^T) after A(i), ring K after D3(i), ring B (Q, P)
+// after O2(i).  So the loads for chunk i + 2 start as early as they can.
 constexpr uint32_t kRingA = 0;            // 2 slots of 32 KB:
 constexpr uint32_t kSlotA = 32768;
 constexpr uint32_t kAWn = 0;              //   fp16 -W, MN-major B: rows d_k
 constexpr uint32_t kAU = 16384;           //   fp16 U^T, K-major A: rows d_v
-constexpr uint32_t kRingB = 2 * kSlotA;   // 2 slots of 40 KB:
-constexpr uint32_t kSlotB = 40960;
-constexpr uint32_t kBKQ = 0;              //   [K d0-63 | Q d0-63 | K d64-127 | Q d64-127], 8 KB each: bf16 as
-                                          //   loaded, then fp16 in place (K times dec)
-constexpr uint32_t kBP = 32768;           //   fp16 P, K-major B: rows r
+constexpr uint32_t kRingK = 2 * kSlotA;   // 2 slots of 16 KB: [K d0-63 | K d64-127], 8 KB each, bf16 as
+constexpr uint32_t kSlotK = 16384;        //   loaded, then fp16 in place (K times dec)
+constexpr uint32_t kRingB = kRingK + 2 * kSlotK;  // 2 slots of 24 KB:
+constexpr uint32_t kSlotB = 24576;
+constexpr uint32_t kBQ = 0;               //   [Q d0-63 | Q d64-127], 8 KB each, bf16 then fp16 in place
+constexpr uint32_t kBP = 16384;           //   fp16 P, K-major B: rows r
 constexpr uint32_t kStageBytes = 73728;   // per chunk over both rings
 constexpr uint32_t kSmI = 2 * kStageBytes;  // fp16 64x64 identity, K-major B
 constexpr uint32_t kSmS = kSmI + 8192;      // fp16 state, K-major A: two 64-column halves of 16 KB
@@ -105,10 +105,12 @@ enum Bar {
   kGates0, kGates1, kGates2, kGates3,      // gates ring slots (loaded)
   kVaDone, kVReady, kD3Done, kSReady,      // state pipeline
   kYoDone0, kYoDone1, kYoFree0, kYoFree1,  // output epilogue (two Y/O2 buffers)
-  kKqFull0, kKqFull1,                      // ring B slots loaded (K|Q bf16, P)
+  kKqFull0, kKqFull1,                      // ring K slots loaded (bf16)
   kKReady0, kKReady1, kQReady0, kQReady1,  // K, then Q, rounded to fp16
   kYDone,                                  // Y read the state's fp16 copy
   kEmptyB0, kEmptyB1,                      // ring B slots released
+  kQFull0, kQFull1,                        // ring B slots loaded (Q bf16, P)
+  kEmptyK0, kEmptyK1,                      // ring K slots released
   kNumBars
 };
 
@@ -156,11 +158,12 @@ __device__ __forceinline__ bool want_out(const Chain& ch, int i) {
 }
 
 // ----------------------------------------------------------------- producer
-// Loads each chunk's ring B tiles (K and Q by TMA, 64 tokens x 64 dims per
-// box, rows past the end of the input read as zero; P by a bulk copy) and
-// gates, and, a chunk ahead, its ring A tiles (-W, U^T; bulk copies).  The
-// waits come in the order the slots are released: ring B of chunk i - 2
-// (end of that chunk), then ring A of chunk i - 1 (after its A).
+// Loads each chunk's K (ring K) and Q (ring B) tiles by TMA, 64 tokens x 64
+// dims per box (rows past the end of the input read as zero), its P (ring
+// B) and gates by bulk copies, and, a chunk ahead, its ring A tiles (-W,
+// U^T; bulk copies).  The waits come in the order the slots are released:
+// ring K of chunk i - 2 (after its D3), ring B of chunk i - 2 (after its
+// O2), ring A of chunk i - 1 (after its A).
 template <bool PREP>
 __device__ __forceinline__ void producer_role(uint8_t* sm, Ctl* ctl, const Problem& p, const Chain& ch, int j,
                                            const CUtensorMap* mq, const CUtensorMap* mk) {
@@ -176,27 +179,35 @@ __device__ __forceinline__ void producer_role(uint8_t* sm, Ctl* ctl, const Probl
   };
   if (n > 0) load_a(0);
   for (int i = 0; i < n; ++i) {
-    if (i >= 2 && !wait_bar(ctl, kEmptyB0 + (i & 1), (uint32_t)(((i - 2) >> 1) & 1))) return;
     const bool out = want_out<PREP>(ch, i);
-    uint8_t* slot = sm + kRingB + (i & 1) * kSlotB;
     const int t0 = (int)(ch.bos + (int64_t)(ch.run_begin + i) * kChunk);
+    // ring K and the gates
+    if (i >= 2 && !wait_bar(ctl, kEmptyK0 + (i & 1), (uint32_t)(((i - 2) >> 1) & 1))) return;
+    uint8_t* kslot = sm + kRingK + (i & 1) * kSlotK;
     uint64_t* kbar = &ctl->bar[kKqFull0 + (i & 1)];
-    mbar_arrive_expect_tx(kbar, out ? 40960u : 16384u);
-    tma_load_3d(slot + kBKQ, mk, kbar, 0, ch.iq, t0);
-    tma_load_3d(slot + kBKQ + 16384, mk, kbar, 64, ch.iq, t0);
-    if (out) {  // Q and P only where the chunk's output is written
-      tma_load_3d(slot + kBKQ + 8192, mq, kbar, 0, ch.iq, t0);
-      tma_load_3d(slot + kBKQ + 24576, mq, kbar, 64, ch.iq, t0);
-      bulk_load(slot + kBP, rec_of(i) + kRecP, 8192u, kbar);
-    }
+    mbar_arrive_expect_tx(kbar, 16384u);
+    tma_load_3d(kslot, mk, kbar, 0, ch.iq, t0);
+    tma_load_3d(kslot + 8192, mk, kbar, 64, ch.iq, t0);
     // The gates go to ring slot i & 3.  Its readers of chunk i - 4 are done:
     // the converter before k_ready(i - 4), the state warps in the V' epilogue
     // of chunk i - 4 (before v_ready(i - 4)), both waited for before D3(i - 4)
     // was issued, and the output warps before yo_free(i - 4), which A(i - 2)
-    // waited for; ring B of chunk i - 2 is released after all of these.
+    // waited for; ring K of chunk i - 2 is released after D3(i - 2).
     uint64_t* gbar = &ctl->bar[kGates0 + (i & 3)];
     mbar_arrive_expect_tx(gbar, 512u);
     bulk_load(sm + kSmG + (i & 3) * 512, rec_of(i) + kRecGam, 512u, gbar);
+    // ring B: Q and P, only where the chunk's output is written
+    if (i >= 2 && !wait_bar(ctl, kEmptyB0 + (i & 1), (uint32_t)(((i - 2) >> 1) & 1))) return;
+    uint8_t* bslot = sm + kRingB + (i & 1) * kSlotB;
+    uint64_t* qbar = &ctl->bar[kQFull0 + (i & 1)];
+    if (out) {
+      mbar_arrive_expect_tx(qbar, 24576u);
+      tma_load_3d(bslot + kBQ, mq, qbar, 0, ch.iq, t0);
+      tma_load_3d(bslot + kBQ + 8192, mq, qbar, 64, ch.iq, t0);
+      bulk_load(bslot + kBP, rec_of(i) + kRecP, 8192u, qbar);
+    } else {
+      mbar_arrive(qbar);  // nothing to load: the phase completes, keeping the slot's phases per chunk
+    }
     if (i + 1 < n) {
       if (i + 1 >= 2 && !wait_bar(ctl, kEmpty0 + ((i + 1) & 1), (uint32_t)(((i - 1) >> 1) & 1))) return;
       load_a(i + 1);
@@ -212,13 +223,16 @@ __device__ __forceinline__ void producer_role(uint8_t* sm, Ctl* ctl, const Probl
 // k_ready, the output warps do Q (two chunks ahead, between their output
 // tiles) and hand it over by q_ready.  A value outside the fp16 range turns
 // into inf in V', the state or o, which are checked.
-__device__ __forceinline__ void round_q_tile(uint32_t base, int t, int nthreads) {
-#pragma unroll 2
-  for (int v = t; v < 1024; v += nthreads) {  // Q halves at 8 and 24 KB
-    const uint32_t a = base + 8192 + (uint32_t)(v & 511) * 16 + (uint32_t)(v >> 9) * 16384;
-    const uint4 u = lds_u32x4(a);
-    st_shared_v4(a, bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
-  }
+// The 16 KB Q tile, 16-byte vectors t, t + 128, ... (128 threads): all eight
+// loads first, then the stores.
+__device__ __forceinline__ void round_q_tile(uint32_t base, int t) {
+  uint4 u[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) u[k] = lds_u32x4(base + (uint32_t)(t + 128 * k) * 16);
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    st_shared_v4(base + (uint32_t)(t + 128 * k) * 16, bf16x2_to_f16x2(u[k].x), bf16x2_to_f16x2(u[k].y),
+                 bf16x2_to_f16x2(u[k].z), bf16x2_to_f16x2(u[k].w));
 }
 
 template <bool PREP>
@@ -230,16 +244,27 @@ __device__ __forceinline__ void convert_role(uint8_t* sm, Ctl* ctl, const Chain&
     if (!wait_bar(ctl, kKqFull0 + st, (uint32_t)((i >> 1) & 1)) ||
         !wait_bar(ctl, kGates0 + (i & 3), (uint32_t)((i >> 2) & 1)))
       break;
-    const uint32_t base = smem_u32(sm + kRingB + st * kSlotB + kBKQ);
+    const uint32_t base = smem_u32(sm + kRingK + st * kSlotK);
     const uint32_t sDec = smem_u32(sm + kSmG + (i & 3) * 512 + 256);
-    // K halves at 0 and 16 KB: 16-byte vector v holds 8 dims of token row (v & 511) >> 3
-#pragma unroll 4
-    for (int v = lane + 32 * part; v < 1024; v += 32 * kConvertWarps) {
-      const uint32_t a = base + (uint32_t)(v & 511) * 16 + (uint32_t)(v >> 9) * 16384;
-      const float d = lds_f32(sDec + (uint32_t)((v & 511) >> 3) * 4);
-      const uint4 u = lds_u32x4(a);
-      st_shared_v4(a, bf16x2_to_f16x2_scaled(u.x, d), bf16x2_to_f16x2_scaled(u.y, d), bf16x2_to_f16x2_scaled(u.z, d),
-                   bf16x2_to_f16x2_scaled(u.w, d));
+    // K halves at 0 and 8 KB: 16-byte vector v holds 8 dims of token row (v & 511) >> 3;
+    // eight vectors per thread at a time, loads first
+#pragma unroll 1
+    for (int v0 = lane + 32 * part; v0 < 1024; v0 += 8 * 32 * kConvertWarps) {
+      uint4 u[8];
+      float d[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int v = v0 + k * 32 * kConvertWarps;
+        u[k] = lds_u32x4(base + (uint32_t)v * 16);
+        d[k] = lds_f32(sDec + (uint32_t)((v & 511) >> 3) * 4);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int v = v0 + k * 32 * kConvertWarps;
+        st_shared_v4(base + (uint32_t)v * 16, bf16x2_to_f16x2_scaled(u[k].x, d[k]),
+                     bf16x2_to_f16x2_scaled(u[k].y, d[k]), bf16x2_to_f16x2_scaled(u[k].z, d[k]),
+                     bf16x2_to_f16x2_scaled(u[k].w, d[k]));
+      }
     }
     fence_proxy_async_smem();
     __syncwarp();
@@ -256,7 +281,8 @@ __device__ __forceinline__ void convert_role(uint8_t* sm, Ctl* ctl, const Chain&
 //   Y(i)  S Q^T into O buffer i & 1, after q_ready(i); commits y_done, after
 //         which the state warps may overwrite the state's copy
 //   O2(i) V'^T P^T; commits yo_done(i)
-//   then ring B of chunk i is released (ring A was, right after A(i)), and
+//   then ring B of chunk i is released (ring A was, right after A(i), and
+//         ring K right after D3(i)), and
 //   U(i+1) U^T . I into V' buffer (i+1) & 1 (read by the state warps for
 //         chunk i-1) once the next record has landed
 // The chain's critical path runs A(i) -> V' epilogue -> D3(i) -> state
@@ -283,7 +309,8 @@ __device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch,
   };
   if (n > 0 && !issue_u(0)) return;
   for (int i = 0; i < n; ++i) {
-    const uint32_t sA = smem_u32(sm + kRingA + (i & 1) * kSlotA), sB = smem_u32(sm + kRingB + (i & 1) * kSlotB);
+    const uint32_t sA = smem_u32(sm + kRingA + (i & 1) * kSlotA), sK = smem_u32(sm + kRingK + (i & 1) * kSlotK);
+    const uint32_t sB = smem_u32(sm + kRingB + (i & 1) * kSlotB);
     const bool out = want_out<PREP>(ch, i);
     if (!spin_bar(ctl, kSReady, (uint32_t)(i & 1))) return;
     if (i >= 2 && !wait_bar(ctl, kYoFree0 + (i & 1), (uint32_t)(((i - 2) >> 1) & 1))) return;
@@ -301,17 +328,19 @@ __device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch,
     tc_fence_after();
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)  // D3 = V'^T diag(dec) K
-      mma_bf16(tmem + kTD3, sdesc_sw128(sVp + ks * 32, 16, 1024), sdesc_sw128(sB + kBKQ + ks * 2048, 16384, 1024),
+      mma_bf16(tmem + kTD3, sdesc_sw128(sVp + ks * 32, 16, 1024), sdesc_sw128(sK + ks * 2048, 8192, 1024),
                id_d3, ks > 0);
     mma_commit(&ctl->bar[kD3Done]);
+    mma_commit(&ctl->bar[kEmptyK0 + (i & 1)]);  // ring K slot read
     if (out) {
       if (!wait_bar(ctl, kQReady0 + (i & 1), (uint32_t)((i >> 1) & 1))) return;
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {  // Y = S Q^T
-        const uint32_t off = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
-        mma_bf16(tmem + kTY + (i & 1) * 64, sdesc_sw128(sS + off, 16, 1024),
-                 sdesc_sw128(sB + kBKQ + 8192 + off, 16, 1024), id_k, ks > 0);
+        mma_bf16(tmem + kTY + (i & 1) * 64,
+                 sdesc_sw128(sS + (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u, 16, 1024),
+                 sdesc_sw128(sB + kBQ + (uint32_t)(ks >> 2) * 8192u + (uint32_t)(ks & 3) * 32u, 16, 1024), id_k,
+                 ks > 0);
       }
     }
     mma_commit(&ctl->bar[kYDone]);
@@ -322,7 +351,7 @@ __device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch,
                  sdesc_sw128(sB + kBP + ks * 32, 16, 1024), id_k, ks > 0);
     }
     mma_commit(&ctl->bar[kYoDone0 + (i & 1)]);
-    mma_commit(&ctl->bar[kEmptyB0 + (i & 1)]);  // ring B slot read
+    mma_commit(&ctl->bar[kEmptyB0 + (i & 1)]);  // ring B slot read (Y, O2)
     if (i + 1 < n && !issue_u(i + 1)) return;  // its V' buffer was read in the V' epilogue of chunk i - 1
   }
 }
@@ -350,8 +379,8 @@ __device__ __forceinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem
   // then q_ready(c); every chunk gets its q_ready, so its phases follow c.
   auto round_q = [&](int c) -> bool {
     if (want_out<PREP>(ch, c)) {
-      if (!wait_bar(ctl, kKqFull0 + (c & 1), (uint32_t)((c >> 1) & 1))) return false;
-      round_q_tile(smem_u32(sm + kRingB + (c & 1) * kSlotB + kBKQ), threadIdx.x - kOutWarp * 32, kOutThreads);
+      if (!wait_bar(ctl, kQFull0 + (c & 1), (uint32_t)((c >> 1) & 1))) return false;
+      round_q_tile(smem_u32(sm + kRingB + (c & 1) * kSlotB + kBQ), threadIdx.x - kOutWarp * 32);
       fence_proxy_async_smem();
     }
     __syncwarp();
@@ -623,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     const int counts[kNumBars] = {1, 1, 1, 1, 1, 1, 1, 1, 1, kChainThreads, 1, kChainThreads,
                                   1, 1, kOutThreads, kOutThreads, 1, 1, kConvertWarps, kConvertWarps,
-                                  kOutThreads / 32, kOutThreads / 32, 1, 1, 1};
+                                  kOutThreads / 32, kOutThreads / 32, 1, 1, 1, 1, 1, 1, 1};
     for (int b = 0; b < kNumBars; ++b) mbar_init(&ctl->bar[b], counts[b]);
     ctl->abort = 0;
     ctl->range_bad = 0;
