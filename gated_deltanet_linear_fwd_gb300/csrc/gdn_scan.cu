@@ -23,12 +23,12 @@
 // decay to the chunk end on the way).  Here, in the S orientation (rows =
 // d_v, columns = d_k), per chunk:
 //   V'^T = U^T - S W^T        (U^T enters the accumulator as U^T . I)
-//   Y    = S Q^T
 //   S    = gamma_C S + V'^T (diag(exp(G_last - G)) K)
-//   O^T  = scale (Y diag(gamma) + V'^T P^T)
+//   O^T  = scale (S (diag(gamma) Q)^T + V'^T P^T)   (one accumulator)
 // All are M = 128 tcgen05 MMAs (fp16 operands, fp32 accumulation in TMEM).
 // The state is kept fp32 in registers and rounded to fp16 once per chunk
-// for its MMAs; V' likewise.  A value outside the fp16 range is reported
+// into TMEM (two buffers), where the MMAs read it as their A operand; V' is
+// rounded to fp16 into shared memory.  A value outside the fp16 range is reported
 // through the status word.
 //
 // Warp roles (512 threads, four warpgroups): warps 0-7 hold the state (row =
@@ -80,8 +80,7 @@ constexpr uint32_t kBQ = 0;               //   [Q d0-63 | Q d64-127], 8 KB each,
 constexpr uint32_t kBP = 16384;           //   fp16 P, K-major B: rows r
 constexpr uint32_t kStageBytes = 73728;   // per chunk over both rings
 constexpr uint32_t kSmI = 2 * kStageBytes;  // fp16 64x64 identity, K-major B
-constexpr uint32_t kSmS = kSmI + 8192;      // fp16 state, K-major A: two 64-column halves of 16 KB
-constexpr uint32_t kSmVp = kSmS + 32768;    // fp16 V'^T, K-major A
+constexpr uint32_t kSmVp = kSmI + 8192;     // fp16 V'^T, K-major A
 constexpr uint32_t kSmO = kSmVp + 16384;    // bf16 o of one chunk, [64 tokens][128 d_v] rows of 256 bytes
 constexpr uint32_t kSmG = kSmO + 16384;     // 4 slots (chunk i in slot i & 3): fp32 exp(G) [64], exp(G_63 - G) [64]
 constexpr uint32_t kSmCtl = kSmG + 4 * 512; // barriers, TMEM base, flags
@@ -94,8 +93,8 @@ static_assert(kRingB + 2 * kSlotB == 2 * kStageBytes && kSlotB % 1024 == 0 && kB
 // ---- TMEM columns (512 allocated) ----
 constexpr uint32_t kTV = 0;     // U^T then V'^T, 2 buffers    128 x 64 each
 constexpr uint32_t kTD3 = 128;  // V'^T diag(dec) K            128 x 128
-constexpr uint32_t kTY = 256;   // S Q^T, 2 buffers            128 x 64 each
-constexpr uint32_t kTO2 = 384;  // V'^T P^T, 2 buffers         128 x 64 each
+constexpr uint32_t kTO = 256;   // S (gamma Q)^T + V'^T P^T, 2 buffers   128 x 64 each
+constexpr uint32_t kTS = 384;   // fp16 state, 2 buffers: 128 x 128 packed in 64 columns each
 
 enum InitKind { kInitZero = 0, kInitIdentity = 1, kInitH0 = 2, kInitStart = 3 };
 
@@ -104,10 +103,9 @@ enum Bar {
   kFull0 = 0, kFull1, kEmpty0, kEmpty1,    // ring A slots (-W, U^T): loaded / released
   kGates0, kGates1, kGates2, kGates3,      // gates ring slots (loaded)
   kVaDone, kVReady, kD3Done, kSReady,      // state pipeline
-  kYoDone0, kYoDone1, kYoFree0, kYoFree1,  // output epilogue (two Y/O2 buffers)
+  kYoDone0, kYoDone1, kYoFree0, kYoFree1,  // output epilogue (two O buffers)
   kKqFull0, kKqFull1,                      // ring K slots loaded (bf16)
   kKReady0, kKReady1, kQReady0, kQReady1,  // K, then Q, rounded to fp16
-  kYDone,                                  // Y read the state's fp16 copy
   kEmptyB0, kEmptyB1,                      // ring B slots released
   kQFull0, kQFull1,                        // ring B slots loaded (Q bf16, P)
   kEmptyK0, kEmptyK1,                      // ring K slots released
@@ -223,16 +221,23 @@ __device__ __forceinline__ void producer_role(uint8_t* sm, Ctl* ctl, const Probl
 // k_ready, the output warps do Q (two chunks ahead, between their output
 // tiles) and hand it over by q_ready.  A value outside the fp16 range turns
 // into inf in V', the state or o, which are checked.
-// The 16 KB Q tile, 16-byte vectors t, t + 128, ... (128 threads): all eight
-// loads first, then the stores.
-__device__ __forceinline__ void round_q_tile(uint32_t base, int t) {
+// The 16 KB Q tile times gamma (sGam: exp(G) of the 64 rows), 16-byte
+// vectors t, t + 128, ... (128 threads; vector v holds 8 dims of row
+// (v & 511) >> 3): all eight loads first, then the stores.
+__device__ __forceinline__ void round_q_tile(uint32_t base, uint32_t sGam, int t) {
   uint4 u[8];
+  float gm[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) u[k] = lds_u32x4(base + (uint32_t)(t + 128 * k) * 16);
+  for (int k = 0; k < 8; ++k) {
+    const int v = t + 128 * k;
+    u[k] = lds_u32x4(base + (uint32_t)v * 16);
+    gm[k] = lds_f32(sGam + (uint32_t)((v & 511) >> 3) * 4);
+  }
 #pragma unroll
   for (int k = 0; k < 8; ++k)
-    st_shared_v4(base + (uint32_t)(t + 128 * k) * 16, bf16x2_to_f16x2(u[k].x), bf16x2_to_f16x2(u[k].y),
-                 bf16x2_to_f16x2(u[k].z), bf16x2_to_f16x2(u[k].w));
+    st_shared_v4(base + (uint32_t)(t + 128 * k) * 16, bf16x2_to_f16x2_scaled(u[k].x, gm[k]),
+                 bf16x2_to_f16x2_scaled(u[k].y, gm[k]), bf16x2_to_f16x2_scaled(u[k].z, gm[k]),
+                 bf16x2_to_f16x2_scaled(u[k].w, gm[k]));
 }
 
 template <bool PREP>
@@ -275,12 +280,13 @@ __device__ __forceinline__ void convert_role(uint8_t* sm, Ctl* ctl, const Chain&
 // ----------------------------------------------------------------- MMA issuer
 // Per chunk i, in this order:
 //   A(i)  V'^T += S (-W)^T, once s_ready(i) has published the state's fp16
-//         copy and the output warps have read O buffer i & 1 (yo_free(i-2));
-//         commits va_done
-//   D3(i) V'^T (diag(dec) K), after v_ready(i) and k_ready(i); commits d3_done
-//   Y(i)  S Q^T into O buffer i & 1, after q_ready(i); commits y_done, after
-//         which the state warps may overwrite the state's copy
-//   O2(i) V'^T P^T; commits yo_done(i)
+//         copy (TMEM buffer i & 1) and the output warps have read O buffer
+//         i & 1 (yo_free(i-2)); commits va_done
+//   D3(i) V'^T (diag(dec) K), after v_ready(i) and k_ready(i); commits
+//         d3_done, which also tells the state warps that Y(i-1), issued
+//         before it, has read state buffer (i+1) & 1
+//   Y(i)  O = S (gamma Q)^T into O buffer i & 1, after q_ready(i)
+//   O2(i) O += V'^T P^T; commits yo_done(i)
 //   then ring B of chunk i is released (ring A was, right after A(i), and
 //         ring K right after D3(i)), and
 //   U(i+1) U^T . I into V' buffer (i+1) & 1 (read by the state warps for
@@ -291,7 +297,7 @@ __device__ __forceinline__ void convert_role(uint8_t* sm, Ctl* ctl, const Chain&
 template <bool PREP>
 __device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch, uint32_t tmem) {
   const int n = ch.run_end - ch.run_begin;
-  const uint32_t sS = smem_u32(sm + kSmS), sVp = smem_u32(sm + kSmVp);
+  const uint32_t sVp = smem_u32(sm + kSmVp);
   const uint32_t sI = smem_u32(sm + kSmI);
   const uint32_t id_k = idesc_f16(128, 64, false, false);
   const uint32_t id_sw = idesc_f16(128, 64, false, true);
@@ -315,12 +321,11 @@ __device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch,
     if (!spin_bar(ctl, kSReady, (uint32_t)(i & 1))) return;
     if (i >= 2 && !wait_bar(ctl, kYoFree0 + (i & 1), (uint32_t)(((i - 2) >> 1) & 1))) return;
     tc_fence_after();
+    const uint32_t tS = tmem + kTS + (i & 1) * 64;  // the state's fp16 copy, 8 columns per K = 16 step
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {  // V'^T += S (-W)^T
-      const uint64_t a = sdesc_sw128(sS + (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u, 16, 1024);
-      mma_bf16(tmem + kTV + (i & 1) * 64, a, sdesc_sw128(sA + kAWn + ks * 2048, 8192, 1024), id_sw,
-               (ch.has_u || ks > 0) ? 1u : 0u);
-    }
+    for (int ks = 0; ks < 8; ++ks)  // V'^T += S (-W)^T
+      mma_f16_ts(tmem + kTV + (i & 1) * 64, tS + ks * 8, sdesc_sw128(sA + kAWn + ks * 2048, 8192, 1024), id_sw,
+                 (ch.has_u || ks > 0) ? 1u : 0u);
     mma_commit(&ctl->bar[kVaDone]);
     mma_commit(&ctl->bar[kEmpty0 + (i & 1)]);  // ring A slot read (U(i), A(i))
     if (!wait_bar(ctl, kKReady0 + (i & 1), (uint32_t)((i >> 1) & 1))) return;
@@ -336,19 +341,14 @@ __device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch,
       if (!wait_bar(ctl, kQReady0 + (i & 1), (uint32_t)((i >> 1) & 1))) return;
       tc_fence_after();
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {  // Y = S Q^T
-        mma_bf16(tmem + kTY + (i & 1) * 64,
-                 sdesc_sw128(sS + (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u, 16, 1024),
-                 sdesc_sw128(sB + kBQ + (uint32_t)(ks >> 2) * 8192u + (uint32_t)(ks & 3) * 32u, 16, 1024), id_k,
-                 ks > 0);
-      }
-    }
-    mma_commit(&ctl->bar[kYDone]);
-    if (out) {
+      for (int ks = 0; ks < 8; ++ks)  // O = S (gamma Q)^T
+        mma_f16_ts(tmem + kTO + (i & 1) * 64, tS + ks * 8,
+                   sdesc_sw128(sB + kBQ + (uint32_t)(ks >> 2) * 8192u + (uint32_t)(ks & 3) * 32u, 16, 1024), id_k,
+                   ks > 0);
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)  // O2 = V'^T P^T
-        mma_bf16(tmem + kTO2 + (i & 1) * 64, sdesc_sw128(sVp + ks * 32, 16, 1024),
-                 sdesc_sw128(sB + kBP + ks * 32, 16, 1024), id_k, ks > 0);
+      for (int ks = 0; ks < 4; ++ks)  // O += V'^T P^T
+        mma_bf16(tmem + kTO + (i & 1) * 64, sdesc_sw128(sVp + ks * 32, 16, 1024),
+                 sdesc_sw128(sB + kBP + ks * 32, 16, 1024), id_k, 1u);
     }
     mma_commit(&ctl->bar[kYoDone0 + (i & 1)]);
     mma_commit(&ctl->bar[kEmptyB0 + (i & 1)]);  // ring B slot read (Y, O2)
@@ -357,7 +357,7 @@ __device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch,
 }
 
 // ----------------------------------------------------------------- output warps
-// O^T = scale (Y diag(gamma) + O2) for each chunk whose output is written:
+// o = scale O for each chunk whose output is written:
 // thread (warp w, lane) takes d_v row 32 (w & 3) + lane and all 64 tokens,
 // 16 at a time, into the staging tile o[token][d_v] (a warp writes 64
 // contiguous bytes of a token row).  One thread then stores the tile: a
@@ -375,12 +375,16 @@ __device__ __forceinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem
   const uint32_t sO = smem_u32(sm + kSmO);
   const int n = ch.run_end - ch.run_begin;
   float mx = 0.f;  // largest |o| (inf or NaN when an fp16 operand overflowed)
-  // Q of chunk c rounded to fp16 (chunks with no output: nothing to round),
-  // then q_ready(c); every chunk gets its q_ready, so its phases follow c.
+  // Q of chunk c times gamma = exp(G) of its row, rounded to fp16 (chunks
+  // with no output: nothing to round), then q_ready(c); every chunk gets its
+  // q_ready, so its phases follow c.
   auto round_q = [&](int c) -> bool {
     if (want_out<PREP>(ch, c)) {
-      if (!wait_bar(ctl, kQFull0 + (c & 1), (uint32_t)((c >> 1) & 1))) return false;
-      round_q_tile(smem_u32(sm + kRingB + (c & 1) * kSlotB + kBQ), threadIdx.x - kOutWarp * 32);
+      if (!wait_bar(ctl, kQFull0 + (c & 1), (uint32_t)((c >> 1) & 1)) ||
+          !wait_bar(ctl, kGates0 + (c & 3), (uint32_t)((c >> 2) & 1)))
+        return false;
+      round_q_tile(smem_u32(sm + kRingB + (c & 1) * kSlotB + kBQ), smem_u32(sm + kSmG + (c & 3) * 512),
+                   threadIdx.x - kOutWarp * 32);
       fence_proxy_async_smem();
     }
     __syncwarp();
@@ -391,35 +395,25 @@ __device__ __forceinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem
     if (!round_q(c)) return;
   for (int i = 0; i < n; ++i) {
     const bool out = want_out<PREP>(ch, i);
-    bool ok = wait_bar(ctl, kYoDone0 + (i & 1), (uint32_t)((i >> 1) & 1));
-    if (ok && out) ok = wait_bar(ctl, kGates0 + (i & 3), (uint32_t)((i >> 2) & 1));
+    const bool ok = wait_bar(ctl, kYoDone0 + (i & 1), (uint32_t)((i >> 1) & 1));
     if (!out && !ok) break;
     if (out) {
       if (issuer) bulk_wait_read_all();  // the previous chunk's stores have read the tile
       // the four warps pass the tile's barriers together or leave together
       if (named_bar_or(kOutBarrier, kOutThreads, !ok)) break;
       tc_fence_after();
-      const uint32_t sGam = smem_u32(sm + kSmG + (i & 3) * 512);  // exp(G) [64]
-#pragma unroll 1
-      for (int tb = 0; tb < kChunk; tb += 16) {
-        uint32_t yq[16], o2[16];
-        tmem_ld16(tmem + lane_base + kTY + (i & 1) * 64 + tb, yq);
-        tmem_ld16(tmem + lane_base + kTO2 + (i & 1) * 64 + tb, o2);
-        float gm[16];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 g4 = lds_f32x4(sGam + (tb + 4 * q) * 4);
-          gm[4 * q] = g4.x;
-          gm[4 * q + 1] = g4.y;
-          gm[4 * q + 2] = g4.z;
-          gm[4 * q + 3] = g4.w;
-        }
-        tmem_ld_wait(yq, o2);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t oa[16], ob[16];
+        tmem_ld16(tmem + lane_base + kTO + (i & 1) * 64 + h * 32, oa);
+        tmem_ld16(tmem + lane_base + kTO + (i & 1) * 64 + h * 32 + 16, ob);
+        tmem_ld_wait(oa, ob);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float o = p.scale * fmaf(gm[e], __uint_as_float(yq[e]), __uint_as_float(o2[e]));
+        for (int e = 0; e < 32; ++e) {
+          const float o = p.scale * __uint_as_float(e < 16 ? oa[e] : ob[e - 16]);
           mx = absmax_nan(mx, o);
-          sts_u16(sO + (uint32_t)(tb + e) * 256u + (uint32_t)row * 2u, __bfloat16_as_ushort(__float2bfloat16_rn(o)));
+          sts_u16(sO + (uint32_t)(h * 32 + e) * 256u + (uint32_t)row * 2u,
+                  __bfloat16_as_ushort(__float2bfloat16_rn(o)));
         }
       }
       fence_proxy_async_smem();
@@ -437,7 +431,7 @@ __device__ __forceinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem
       }
     }
     tc_fence_before();
-    mbar_arrive(&ctl->bar[kYoFree0 + (i & 1)]);  // Y/O2 buffer i & 1 read
+    mbar_arrive(&ctl->bar[kYoFree0 + (i & 1)]);  // O buffer i & 1 read
     if (i + 2 < n && !round_q(i + 2)) break;  // its ring B slot was released with yo_done(i)
   }
   if (issuer) bulk_wait_all();  // the stores have landed before the block exits
@@ -475,20 +469,22 @@ __device__ __forceinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem&
   }
   const int n = ch.run_end - ch.run_begin;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-  const uint32_t sS = smem_u32(sm + kSmS), sVp = smem_u32(sm + kSmVp);
-  // Largest magnitude this thread rounds to fp16: V' is checked every chunk
-  // (|V' dec| <= |V'|); the state only at the end, since an fp16 overflow of
-  // its operand copy would turn the next V' and so the state into inf/NaN.
+  const uint32_t sVp = smem_u32(sm + kSmVp);
+  // Largest magnitude this thread rounds to fp16: V' is checked every chunk;
+  // the state only at the end, since an fp16 overflow of its operand copy
+  // would turn the next V' and so the state into inf/NaN.
   float mx = 0.f;
-  auto store_state = [&]() {
+  // The state's fp16 copy for chunk c into TMEM buffer c & 1: this thread's
+  // row, its 64 columns packed into 32 (columns 32 half .. 32 half + 31).
+  auto store_state = [&](int c) {
+    uint32_t w[32];
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
-      st_shared_v4(sS + half * 16384 + sw128_offset(row, q), pack_f16x2(S[8 * q], S[8 * q + 1]),
-                   pack_f16x2(S[8 * q + 2], S[8 * q + 3]), pack_f16x2(S[8 * q + 4], S[8 * q + 5]),
-                   pack_f16x2(S[8 * q + 6], S[8 * q + 7]));
+    for (int q = 0; q < 32; ++q) w[q] = pack_f16x2(S[2 * q], S[2 * q + 1]);
+    tmem_st32(tmem + lane_base + kTS + (c & 1) * 64 + half * 32, w);
+    tmem_st_wait();
   };
-  store_state();
-  fence_proxy_async_smem();
+  store_state(0);
+  tc_fence_before();
   mbar_arrive(&ctl->bar[kSReady]);
   int done = 0;
   for (int i = 0; i < n; ++i) {
@@ -531,9 +527,9 @@ __device__ __forceinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem&
         S[g8 * 32 + 16 + e] = fmaf(gC, S[g8 * 32 + 16 + e], __uint_as_float(rb[e]));
       }
     }
-    if (!wait_bar(ctl, kYDone, par)) break;  // Y(i) has read the state's copy
-    store_state();
-    fence_proxy_async_smem();
+    // buffer (i + 1) & 1 was last read by A(i - 1) and Y(i - 1), both issued
+    // before D3(i), whose completion this thread has seen
+    store_state(i + 1);
     tc_fence_before();
     mbar_arrive(&ctl->bar[kSReady]);
     done = i + 1;
@@ -652,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     const int counts[kNumBars] = {1, 1, 1, 1, 1, 1, 1, 1, 1, kChainThreads, 1, kChainThreads,
                                   1, 1, kOutThreads, kOutThreads, 1, 1, kConvertWarps, kConvertWarps,
-                                  kOutThreads / 32, kOutThreads / 32, 1, 1, 1, 1, 1, 1, 1};
+                                  kOutThreads / 32, kOutThreads / 32, 1, 1, 1, 1, 1, 1};
     for (int b = 0; b < kNumBars; ++b) mbar_init(&ctl->bar[b], counts[b]);
     ctl->abort = 0;
     ctl->range_bad = 0;
