@@ -22,13 +22,13 @@
 // from the inputs (bf16, rounded to fp16 in shared memory, K scaled by the
 // decay to the chunk end on the way).  Here, in the S orientation (rows =
 // d_v, columns = d_k), per chunk:
-//   V'^T = U^T - S W^T        (U^T enters the accumulator as U^T . I)
+//   V'^T = U^T - S W^T        (U^T added by the state warps)
 //   S    = gamma_C S + V'^T (diag(exp(G_last - G)) K)
 //   O^T  = scale (S (diag(gamma) Q)^T + V'^T P^T)   (one accumulator)
 // All are M = 128 tcgen05 MMAs (fp16 operands, fp32 accumulation in TMEM).
 // The state is kept fp32 in registers and rounded to fp16 once per chunk
-// into TMEM (two buffers), where the MMAs read it as their A operand; V' is
-// rounded to fp16 into shared memory.  A value outside the fp16 range is reported
+// into TMEM (two buffers), where the MMAs read it as their A operand; V'
+// likewise (two buffers of its fp16 copy beside its fp32 accumulator).  A value outside the fp16 range is reported
 // through the status word.
 //
 // Warp roles (512 threads, four warpgroups): warps 0-7 hold the state (row =
@@ -45,6 +45,7 @@
 // thread the block is launched with.  The roles hand over through
 // mbarriers whose waits are all bounded.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "gdn_dev.cuh"
 
@@ -79,9 +80,7 @@ constexpr uint32_t kSlotB = 24576;
 constexpr uint32_t kBQ = 0;               //   [Q d0-63 | Q d64-127], 8 KB each, bf16 then fp16 in place
 constexpr uint32_t kBP = 16384;           //   fp16 P, K-major B: rows r
 constexpr uint32_t kStageBytes = 73728;   // per chunk over both rings
-constexpr uint32_t kSmI = 2 * kStageBytes;  // fp16 64x64 identity, K-major B
-constexpr uint32_t kSmVp = kSmI + 8192;     // fp16 V'^T, K-major A
-constexpr uint32_t kSmO = kSmVp + 16384;    // bf16 o of one chunk, [64 tokens][128 d_v] rows of 256 bytes
+constexpr uint32_t kSmO = 2 * kStageBytes;  // bf16 o of one chunk, [64 tokens][128 d_v] rows of 256 bytes
 constexpr uint32_t kSmG = kSmO + 16384;     // 4 slots (chunk i in slot i & 3): fp32 exp(G) [64], exp(G_63 - G) [64]
 constexpr uint32_t kSmCtl = kSmG + 4 * 512; // barriers, TMEM base, flags
 constexpr uint32_t kSmemUse = kSmCtl + 512;
@@ -91,7 +90,8 @@ static_assert(kRingB + 2 * kSlotB == 2 * kStageBytes && kSlotB % 1024 == 0 && kB
               "ring layout");
 
 // ---- TMEM columns (512 allocated) ----
-constexpr uint32_t kTV = 0;     // U^T then V'^T, 2 buffers    128 x 64 each
+constexpr uint32_t kTV = 0;     // -S W^T                      128 x 64
+constexpr uint32_t kTV16 = 64;  // fp16 V'^T, 2 buffers: 128 x 64 packed in 32 columns each
 constexpr uint32_t kTD3 = 128;  // V'^T diag(dec) K            128 x 128
 constexpr uint32_t kTO = 256;   // S (gamma Q)^T + V'^T P^T, 2 buffers   128 x 64 each
 constexpr uint32_t kTS = 384;   // fp16 state, 2 buffers: 128 x 128 packed in 64 columns each
@@ -279,66 +279,50 @@ __device__ __forceinline__ void convert_role(uint8_t* sm, Ctl* ctl, const Chain&
 
 // ----------------------------------------------------------------- MMA issuer
 // Per chunk i, in this order:
-//   A(i)  V'^T += S (-W)^T, once s_ready(i) has published the state's fp16
-//         copy (TMEM buffer i & 1) and the output warps have read O buffer
-//         i & 1 (yo_free(i-2)); commits va_done
+//   A(i)  -S W^T, once ring A of chunk i has landed and s_ready(i) has
+//         published the state's fp16 copy (TMEM buffer i & 1); commits
+//         va_done (the state warps add U^T and write V'(i) in fp16 to TMEM
+//         buffer i & 1)
 //   D3(i) V'^T (diag(dec) K), after v_ready(i) and k_ready(i); commits
-//         d3_done, which also tells the state warps that Y(i-1), issued
-//         before it, has read state buffer (i+1) & 1
-//   Y(i)  O = S (gamma Q)^T into O buffer i & 1, after q_ready(i)
-//   O2(i) O += V'^T P^T; commits yo_done(i)
-//   then ring B of chunk i is released (ring A was, right after A(i), and
-//         ring K right after D3(i)), and
-//   U(i+1) U^T . I into V' buffer (i+1) & 1 (read by the state warps for
-//         chunk i-1) once the next record has landed
+//         d3_done (which also tells the state warps that Y(i-1), issued
+//         before it, has read state buffer (i+1) & 1) and releases rings K
+//         and A (the state warps read U^T before v_ready(i))
+//   Y(i)  O = S (gamma Q)^T into O buffer i & 1, after q_ready(i) and
+//         yo_free(i-2), then O2(i) O += V'^T P^T; commits yo_done(i) and
+//         releases ring B
 // The chain's critical path runs A(i) -> V' epilogue -> D3(i) -> state
-// epilogue -> A(i+1); Y, O2 and U run on the tensor cores while the state
-// warps work on the state, never between A(i) and D3(i).
+// epilogue -> A(i+1).  A(i+2), issued after O2(i), tells the state warps
+// through va_done that V' buffer i & 1 has been read.
 template <bool PREP>
 __device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch, uint32_t tmem) {
   const int n = ch.run_end - ch.run_begin;
-  const uint32_t sVp = smem_u32(sm + kSmVp);
-  const uint32_t sI = smem_u32(sm + kSmI);
   const uint32_t id_k = idesc_f16(128, 64, false, false);
   const uint32_t id_sw = idesc_f16(128, 64, false, true);
   const uint32_t id_d3 = idesc_f16(128, 128, false, true);
-  auto issue_u = [&](int i) -> bool {
-    if (!wait_bar(ctl, kFull0 + (i & 1), (uint32_t)((i >> 1) & 1))) return false;
-    if (!ch.has_u) return true;
-    const uint32_t sU = smem_u32(sm + kRingA + (i & 1) * kSlotA + kAU);
-    tc_fence_after();
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks)
-      mma_bf16(tmem + kTV + (i & 1) * 64, sdesc_sw128(sU + ks * 32, 16, 1024), sdesc_sw128(sI + ks * 32, 16, 1024),
-               id_k, ks > 0);
-    return true;
-  };
-  if (n > 0 && !issue_u(0)) return;
+  if (n > 0 && !wait_bar(ctl, kFull0, 0u)) return;  // ring A of chunk 0
   for (int i = 0; i < n; ++i) {
     const uint32_t sA = smem_u32(sm + kRingA + (i & 1) * kSlotA), sK = smem_u32(sm + kRingK + (i & 1) * kSlotK);
     const uint32_t sB = smem_u32(sm + kRingB + (i & 1) * kSlotB);
-    const bool out = want_out<PREP>(ch, i);
+    const uint32_t tS = tmem + kTS + (i & 1) * 64;    // the state's fp16 copy, 8 columns per K = 16 step
+    const uint32_t tV = tmem + kTV16 + (i & 1) * 32;  // V''s fp16 copy, 8 columns per K = 16 step
     if (!spin_bar(ctl, kSReady, (uint32_t)(i & 1))) return;
-    if (i >= 2 && !wait_bar(ctl, kYoFree0 + (i & 1), (uint32_t)(((i - 2) >> 1) & 1))) return;
     tc_fence_after();
-    const uint32_t tS = tmem + kTS + (i & 1) * 64;  // the state's fp16 copy, 8 columns per K = 16 step
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks)  // V'^T += S (-W)^T
-      mma_f16_ts(tmem + kTV + (i & 1) * 64, tS + ks * 8, sdesc_sw128(sA + kAWn + ks * 2048, 8192, 1024), id_sw,
-                 (ch.has_u || ks > 0) ? 1u : 0u);
+    for (int ks = 0; ks < 8; ++ks)  // -S W^T
+      mma_f16_ts(tmem + kTV, tS + ks * 8, sdesc_sw128(sA + kAWn + ks * 2048, 8192, 1024), id_sw, ks > 0 ? 1u : 0u);
     mma_commit(&ctl->bar[kVaDone]);
-    mma_commit(&ctl->bar[kEmpty0 + (i & 1)]);  // ring A slot read (U(i), A(i))
     if (!wait_bar(ctl, kKReady0 + (i & 1), (uint32_t)((i >> 1) & 1))) return;
     if (!spin_bar(ctl, kVReady, (uint32_t)(i & 1))) return;
     tc_fence_after();
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)  // D3 = V'^T diag(dec) K
-      mma_bf16(tmem + kTD3, sdesc_sw128(sVp + ks * 32, 16, 1024), sdesc_sw128(sK + ks * 2048, 8192, 1024),
-               id_d3, ks > 0);
+      mma_f16_ts(tmem + kTD3, tV + ks * 8, sdesc_sw128(sK + ks * 2048, 8192, 1024), id_d3, ks > 0);
     mma_commit(&ctl->bar[kD3Done]);
     mma_commit(&ctl->bar[kEmptyK0 + (i & 1)]);  // ring K slot read
-    if (out) {
+    mma_commit(&ctl->bar[kEmpty0 + (i & 1)]);   // ring A slot read (A(i); U^T before v_ready(i))
+    if (want_out<PREP>(ch, i)) {
       if (!wait_bar(ctl, kQReady0 + (i & 1), (uint32_t)((i >> 1) & 1))) return;
+      if (i >= 2 && !wait_bar(ctl, kYoFree0 + (i & 1), (uint32_t)(((i - 2) >> 1) & 1))) return;
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)  // O = S (gamma Q)^T
@@ -347,12 +331,11 @@ __device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch,
                    ks > 0);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)  // O += V'^T P^T
-        mma_bf16(tmem + kTO + (i & 1) * 64, sdesc_sw128(sVp + ks * 32, 16, 1024),
-                 sdesc_sw128(sB + kBP + ks * 32, 16, 1024), id_k, 1u);
+        mma_f16_ts(tmem + kTO + (i & 1) * 64, tV + ks * 8, sdesc_sw128(sB + kBP + ks * 32, 16, 1024), id_k, 1u);
     }
     mma_commit(&ctl->bar[kYoDone0 + (i & 1)]);
     mma_commit(&ctl->bar[kEmptyB0 + (i & 1)]);  // ring B slot read (Y, O2)
-    if (i + 1 < n && !issue_u(i + 1)) return;  // its V' buffer was read in the V' epilogue of chunk i - 1
+    if (i + 1 < n && !wait_bar(ctl, kFull0 + ((i + 1) & 1), (uint32_t)(((i + 1) >> 1) & 1))) return;  // ring A
   }
 }
 
@@ -469,7 +452,6 @@ __device__ __forceinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem&
   }
   const int n = ch.run_end - ch.run_begin;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-  const uint32_t sVp = smem_u32(sm + kSmVp);
   // Largest magnitude this thread rounds to fp16: V' is checked every chunk;
   // the state only at the end, since an fp16 overflow of its operand copy
   // would turn the next V' and so the state into inf/NaN.
@@ -490,26 +472,42 @@ __device__ __forceinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem&
   for (int i = 0; i < n; ++i) {
     const uint32_t par = (uint32_t)(i & 1);
     const uint32_t sGam = smem_u32(sm + kSmG + (i & 3) * 512);  // exp(G) [64], then dec [64]
-    if (!wait_bar(ctl, kGates0 + (i & 3), (uint32_t)((i >> 2) & 1)) || !wait_bar(ctl, kVaDone, par)) break;
+    if (!wait_bar(ctl, kGates0 + (i & 3), (uint32_t)((i >> 2) & 1))) break;
+    // U^T of this thread's row and 32 tokens (16-byte chunks half * 4 .. + 3 of
+    // the row in ring A), read while A(i) runs
+    uint4 uq[4] = {};
+    if (ch.has_u) {
+      if (!wait_bar(ctl, kFull0 + (i & 1), (uint32_t)((i >> 1) & 1))) break;
+      const uint32_t sU = smem_u32(sm + kRingA + (i & 1) * kSlotA + kAU);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) uq[c] = lds_u32x4(sU + sw128_offset(row, half * 4 + c));
+    }
+    if (!wait_bar(ctl, kVaDone, par)) break;
     tc_fence_after();
     const float gC = lds_f32(sGam + 63 * 4);
-    // V' as the fp16 operand of D3 and O2 (the decay to the chunk end is in K)
+    // V' = U^T - S W^T, its fp16 copy into TMEM buffer i & 1 (columns 16 half ..
+    // 16 half + 15: this thread's 32 tokens), the A operand of D3 and O2 (the
+    // decay to the chunk end is in K)
     {
-      uint32_t va[16], vb[16];
-      tmem_ld16(tmem + lane_base + kTV + (i & 1) * 64 + half * 32, va);
-      tmem_ld16(tmem + lane_base + kTV + (i & 1) * 64 + half * 32 + 16, vb);
+      uint32_t va[16], vb[16], w[16];
+      tmem_ld16(tmem + lane_base + kTV + half * 32, va);
+      tmem_ld16(tmem + lane_base + kTV + half * 32 + 16, vb);
       tmem_ld_wait(va, vb);
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
-        const int g2 = q4 >> 1, q = q4 & 1;
-        const float* f = reinterpret_cast<const float*>(g2 == 0 ? &va[q * 8] : &vb[q * 8]);
+        const uint32_t* acc = q4 < 2 ? &va[q4 * 8] : &vb[(q4 - 2) * 8];
+        const uint32_t uw[4] = {uq[q4].x, uq[q4].y, uq[q4].z, uq[q4].w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mx = absmax_nan(mx, f[e]);
-        st_shared_v4(sVp + sw128_offset(row, half * 4 + g2 * 2 + q), pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]),
-                     pack_f16x2(f[4], f[5]), pack_f16x2(f[6], f[7]));
+        for (int e = 0; e < 4; ++e) {
+          const float2 u2 = __half22float2(*reinterpret_cast<const __half2*>(&uw[e]));
+          const float f0 = __uint_as_float(acc[2 * e]) + u2.x, f1 = __uint_as_float(acc[2 * e + 1]) + u2.y;
+          mx = absmax_nan(absmax_nan(mx, f0), f1);
+          w[q4 * 4 + e] = pack_f16x2(f0, f1);
+        }
       }
+      tmem_st16(tmem + lane_base + kTV16 + (i & 1) * 32 + half * 16, w);
+      tmem_st_wait();
     }
-    fence_proxy_async_smem();
     tc_fence_before();
     mbar_arrive(&ctl->bar[kVReady]);
     // S = gamma_C S + D3
@@ -656,15 +654,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&mq);
     tma_prefetch_desc(&mk);
     if (!PREP) tma_prefetch_desc(&mo);
-  }
-  {  // 64 x 64 fp16 identity: row r has its 1 at column r
-    const uint32_t sI = smem_u32(sm + kSmI);
-    for (int idx = tid; idx < 512; idx += kThreads) {
-      const int r = idx >> 3, q = idx & 7;
-      uint32_t w[4] = {0u, 0u, 0u, 0u};
-      if (q == (r >> 3)) w[(r & 7) >> 1] = 0x3C00u << (16 * (r & 1));
-      st_shared_v4(sI + sw128_offset(r, q), w[0], w[1], w[2], w[3]);
-    }
   }
   fence_proxy_async_smem();
   if (warp == 0) {
