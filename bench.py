@@ -184,13 +184,9 @@ def time_gpu(name, steps, warmup, device, cp="auto", lambda_=0.0, trace=True):
     code, detail = gdn_get_device_status(ws)
     names = gdn_trace_last()
     n_k = len(names)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_k + 1)]
-    for e in ev:
-        e.record(stream)
-    torch.cuda.synchronize(device)
-    if trace:
-        gdn_set_trace_events(ev)
-    per_step, per_kernel = [], [0.0] * n_k
+    # the timed steps run without events between the kernels (they would keep
+    # each kernel from starting before the one before it has drained)
+    per_step = []
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for _ in range(steps):
         flush.zero_()
@@ -199,17 +195,28 @@ def time_gpu(name, steps, warmup, device, cp="auto", lambda_=0.0, trace=True):
         s1.record(stream)
         s1.synchronize()
         per_step.append(s0.elapsed_time(s1))
-        if trace:
+    # the per-kernel split: separate steps with an event after every kernel
+    per_kernel = [0.0] * n_k
+    trace_steps = max(5, steps // 4) if trace else 0
+    if trace:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_k + 1)]
+        for e in ev:
+            e.record(stream)
+        torch.cuda.synchronize(device)
+        gdn_set_trace_events(ev)
+        for _ in range(trace_steps):
+            flush.zero_()
+            fwd()
+            ev[-1].synchronize()
             for i in range(n_k):
                 per_kernel[i] += ev[i].elapsed_time(ev[i + 1])
-    if trace:
         gdn_set_trace_events([])
     code2, detail2 = gdn_get_device_status(ws)
     modes, _ = gdn_cp_head_modes(ws, plan)
     by, fl = algorithmic(w)
     return {"workload": name, "w": w, "plan": plan, "ms": statistics.mean(per_step),
             "ms_median": statistics.median(per_step),
-            "kernel_ms": {n: t / steps for n, t in zip(names, per_kernel)} if trace else {},
+            "kernel_ms": {n: t / trace_steps for n, t in zip(names, per_kernel)} if trace else {},
             "launches": n_k, "status": (code, detail, code2, detail2), "bytes": by, "flops": fl,
             "modes": modes.flatten().tolist(), "tokens": w.T}
 

@@ -479,7 +479,7 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
     if ((e = launch_chunk_map(p, cs)) != cudaSuccess) return cuda_fail(e);
     if ((e = log.after("chunk_map")) != cudaSuccess) return cuda_fail(e);
   }
-  if ((e = launch_wy(p, mq, mk, mv, cs)) != cudaSuccess) return cuda_fail(e);
+  if ((e = launch_wy(p, mq, mk, mv, cs, cu_dev != nullptr)) != cudaSuccess) return cuda_fail(e);
   if ((e = log.after("wy")) != cudaSuccess) return cuda_fail(e);
   if (plan->mode != GDN_CP_OFF) {
     if ((e = launch_scan_prep(p, mq, mk, cs)) != cudaSuccess) return cuda_fail(e);

@@ -34,6 +34,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
   float* sP = sX + kRows * kDim;               // [kSlices][kRows][128] partial sums
   __shared__ SegInfo s_seq;
   __shared__ uint64_t s_bar[2];
+  grid_dependency_wait();  // the segment transitions and local states: written by the kernel before
+  grid_launch_dependents();
   const int tid = threadIdx.x, warp = tid >> 5;
   const int n = blockIdx.x, j = blockIdx.y, r0 = blockIdx.z * kRows;
   __shared__ int s_mode;
@@ -166,12 +168,9 @@ cudaError_t combine_kernel_setup() {
 
 cudaError_t launch_combine(const Problem& p, int sm_count, cudaStream_t st) {
   // 32 CTAs of 4 rows per exact (sequence, head) if even all pairs fit in about two waves
-  if ((int64_t)p.n_seqs * p.h_v * 32 <= 2 * (int64_t)sm_count) {
-    combine_kernel<4><<<dim3(p.n_seqs, p.h_v, kDim / 4), 256, combine_smem<4>(), st>>>(p);
-  } else {
-    combine_kernel<8><<<dim3(p.n_seqs, p.h_v, kDim / 8), 256, combine_smem<8>(), st>>>(p);
-  }
-  return cudaGetLastError();
+  if ((int64_t)p.n_seqs * p.h_v * 32 <= 2 * (int64_t)sm_count)
+    return launch_kernel(combine_kernel<4>, dim3(p.n_seqs, p.h_v, kDim / 4), dim3(256), combine_smem<4>(), st, true, p);
+  return launch_kernel(combine_kernel<8>, dim3(p.n_seqs, p.h_v, kDim / 8), dim3(256), combine_smem<8>(), st, true, p);
 }
 
 }  // namespace gdn

@@ -238,10 +238,32 @@ __device__ inline int head_mode_warp(const Problem& p, const SegInfo& si, int j,
   return kModeWarmup;
 }
 
+// Launches kernel<<<grid, block, smem, st>>>(args...); with `dependent`, as a
+// programmatic dependent launch: its blocks may start while the previous
+// kernel in the stream finishes, and wait for it (grid_dependency_wait) at
+// their start.  Every kernel of the forward waits first thing, so each one
+// also sees the results of all kernels before its predecessor.
+template <typename... Params, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                          bool dependent, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = dependent ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // ---- kernel launchers (defined in the .cu files) ----
+// `dependent`: launched as a programmatic dependent of the kernel before it.
 cudaError_t launch_chunk_map(const Problem& p, cudaStream_t st);
 cudaError_t launch_wy(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                      cudaStream_t st);
+                      cudaStream_t st, bool dependent);
 cudaError_t launch_scan_prep(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, cudaStream_t st);
 cudaError_t launch_combine(const Problem& p, int sm_count, cudaStream_t st);
 cudaError_t launch_scan_out(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mo,

@@ -559,6 +559,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int j = blockIdx.y;
   const int chain = PREP ? (int)blockIdx.z : 0;
+  grid_dependency_wait();  // records, chunk index, segment states: written by the kernels before
+  grid_launch_dependents();
 
   // ---- which chain this CTA runs ----
   if (warp == 0) {
@@ -711,15 +713,14 @@ cudaError_t scan_kernel_setup() {
 
 cudaError_t launch_scan_prep(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, cudaStream_t st) {
   dim3 grid(p.n_seg_total, p.h_v, 2);
-  scan_kernel<true><<<grid, kThreads, kSmemAlloc, st>>>(mq, mk, mq, p);  // writes no output: o's map unused
-  return cudaGetLastError();
+  return launch_kernel(scan_kernel<true>, grid, dim3(kThreads), kSmemAlloc, st, true, mq, mk, mq,
+                       p);  // writes no output: o's map unused
 }
 
 cudaError_t launch_scan_out(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mo,
                             int grid_x, cudaStream_t st) {
   dim3 grid(grid_x, p.h_v, 1);
-  scan_kernel<false><<<grid, kThreads, kSmemAlloc, st>>>(mq, mk, mo, p);
-  return cudaGetLastError();
+  return launch_kernel(scan_kernel<false>, grid, dim3(kThreads), kSmemAlloc, st, true, mq, mk, mo, p);
 }
 
 }  // namespace gdn

@@ -464,6 +464,8 @@ __global__ void __launch_bounds__(kWyThreads, 3)
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1024-byte aligned
   WyCtl* ctl = reinterpret_cast<WyCtl*>(sm + kWyCtl);
   const int tid = threadIdx.x, warp = tid >> 5;
+  grid_dependency_wait();  // the chunk index (varlen) is written by the kernel before
+  grid_launch_dependents();
   if (tid == 0) {
     mbar_init(&ctl->full, 1);
     mbar_init(&ctl->kq, 1);
@@ -512,6 +514,7 @@ __global__ void __launch_bounds__(kMapThreads) chunk_map_kernel(const Problem p)
   __shared__ int warp_sum[32];
   __shared__ int carry;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  grid_launch_dependents();
   if (tid == 0) carry = 0;
   __syncthreads();
   for (int n0 = 0; n0 < p.n_seqs; n0 += kMapThreads) {
@@ -577,11 +580,10 @@ cudaError_t launch_chunk_map(const Problem& p, cudaStream_t st) {
 }
 
 cudaError_t launch_wy(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                      cudaStream_t st) {
+                      cudaStream_t st, bool dependent) {
   if (p.n_chunks_total == 0) return cudaSuccess;
   const unsigned grid = (unsigned)p.n_chunks_total * (unsigned)p.h_v;
-  wy_kernel<<<grid, kWyThreads, kWySmemAlloc, st>>>(mq, mk, mv, p);
-  return cudaGetLastError();
+  return launch_kernel(wy_kernel, dim3(grid), dim3(kWyThreads), kWySmemAlloc, st, dependent, mq, mk, mv, p);
 }
 
 }  // namespace gdn

@@ -101,6 +101,14 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
 
 // ---------------------------------------------------------------- TMEM
 // Allocation is warp-collective; the base column address lands in *dst.
+// Programmatic dependent launch: wait until the grid this one depends on has
+// completed and its writes are visible (returns at once for a grid launched
+// without the dependency), then let the next grid start launching its blocks.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Per-warpgroup register limit (all threads of the warpgroup execute it).
 template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_inc() {
