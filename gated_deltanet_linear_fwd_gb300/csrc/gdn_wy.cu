@@ -36,10 +36,11 @@ constexpr uint32_t kWyV = 32768;       // bf16 [V d0-63 | V d64-127] (TMA); fina
 constexpr uint32_t kWyF = 49152;       // fp32 [64][68]: L below the diagonal, A^T on and above it; then
                                        // A diag(beta) hi | lo (8 KB each); finally the -W tile
 constexpr uint32_t kFStride = 68;
-constexpr uint32_t kWyScr = 66560;     // fp32 solve scratch (4 KB)
-constexpr uint32_t kWyGates = 70656;   // G | exp(G) | exp(G_63 - G) | beta | exp(-G), 64 floats each
-constexpr uint32_t kWyCtl = 71936;
-constexpr uint32_t kWySmemUse = 72000;
+constexpr uint32_t kWyScr = 66560;     // fp32 solve scratch (4.5 KB): T blocks, rows padded against
+                                       // bank conflicts
+constexpr uint32_t kWyGates = 71168;   // G | exp(G) | exp(G_63 - G) | beta | exp(-G), 64 floats each
+constexpr uint32_t kWyCtl = 72448;
+constexpr uint32_t kWySmemUse = 72512;
 constexpr uint32_t kWySmemAlloc = kWySmemUse + 1024;
 static_assert(3 * (kWySmemAlloc + 1024) <= 233472, "three CTAs per SM must fit");
 
@@ -66,6 +67,12 @@ static_assert(sizeof(WyCtl) <= kWySmemUse - kWyCtl, "control block too large");
 //   A_hl = -A_hh L_hl A_ll                           (32 x 32 blocks)
 // The strict lower parts of the diagonal 32 x 32 blocks are cleared once
 // consumed, so every product runs over full ranges without masks.
+// Row strides of the T blocks in the scratch: 18 (16 x 16, float2 stores of
+// 16 rows hit 16 different bank pairs) and 36 (32 x 32, float4 stores of 32
+// rows spread over all 32 banks).
+constexpr int kTs1 = 18, kTs2 = 36;
+static_assert(2 * 16 * kTs1 * 4 <= 4608 && 32 * kTs2 * 4 <= 4608, "solve scratch");
+
 __device__ __forceinline__ void solve_unit_lower(float* F, float* scratch, int tid) {
   // ---- diagonal blocks ----
   {
@@ -103,7 +110,7 @@ __device__ __forceinline__ void solve_unit_lower(float* F, float* scratch, int t
   {
     const int mat = tid >> 7, w = (tid >> 5) & 3, lane = tid & 31;
     const int ib = 2 * mat + 1, jb = 2 * mat;
-    float* Ts = scratch + mat * 256;  // [16][16]
+    float* Ts = scratch + mat * 16 * kTs1;  // [16][kTs1]
     {
       // T[r][c], c = 4w + 2 (lane >> 4) + {0, 1}, r = lane & 15: sum over m >= 4w (D_jb[m][c] = 0 for m < c)
       const int r = lane & 15, c = 4 * w + 2 * (lane >> 4);
@@ -119,7 +126,7 @@ __device__ __forceinline__ void solve_unit_lower(float* F, float* scratch, int t
         t0 = fmaf(l4.x, a0.x, fmaf(l4.y, a0.y, fmaf(l4.z, a0.z, fmaf(l4.w, a0.w, t0))));
         t1 = fmaf(l4.x, a1.x, fmaf(l4.y, a1.y, fmaf(l4.z, a1.z, fmaf(l4.w, a1.w, t1))));
       }
-      *reinterpret_cast<float2*>(Ts + r * 16 + c) = make_float2(t0, t1);
+      *reinterpret_cast<float2*>(Ts + r * kTs1 + c) = make_float2(t0, t1);
     }
     __syncthreads();
     {
@@ -131,7 +138,7 @@ __device__ __forceinline__ void solve_unit_lower(float* F, float* scratch, int t
       for (int m = 0; m < 16; ++m) {
         if (m >= 4 * w + 4) break;
         const float2 d = *reinterpret_cast<const float2*>(F + (16 * ib + m) * kFStride + 16 * ib + r);
-        const float tv = Ts[m * 16 + c];
+        const float tv = Ts[m * kTs1 + c];
         x0 = fmaf(d.x, tv, x0);
         x1 = fmaf(d.y, tv, x1);
       }
@@ -147,7 +154,7 @@ __device__ __forceinline__ void solve_unit_lower(float* F, float* scratch, int t
   //      bounds of A_ll and A_hh are the same across the warp ----
   {
     const int w = tid >> 5, lane = tid & 31;
-    float* Tb = scratch;  // [32][32]
+    float* Tb = scratch;  // [32][kTs2]
     {
       // T[lane][4w .. 4w+3] = sum_{m >= 4w} L[32 + lane][m] A_ll[m][c]   (A_ll[m][c] = 0 for m < c)
       const float* Lr = F + (32 + lane) * kFStride;
@@ -161,7 +168,7 @@ __device__ __forceinline__ void solve_unit_lower(float* F, float* scratch, int t
           t[c] = fmaf(l4.x, a4.x, fmaf(l4.y, a4.y, fmaf(l4.z, a4.z, fmaf(l4.w, a4.w, t[c]))));
         }
       }
-      *reinterpret_cast<float4*>(Tb + lane * 32 + 4 * w) = make_float4(t[0], t[1], t[2], t[3]);
+      *reinterpret_cast<float4*>(Tb + lane * kTs2 + 4 * w) = make_float4(t[0], t[1], t[2], t[3]);
     }
     __syncthreads();
     {
@@ -170,7 +177,7 @@ __device__ __forceinline__ void solve_unit_lower(float* F, float* scratch, int t
 #pragma unroll 4
       for (int m = 0; m < 4 * w + 4; ++m) {
         const float4 a4 = *reinterpret_cast<const float4*>(F + (32 + m) * kFStride + 32 + 4 * w);  // A_hh[4w..4w+3][m]
-        const float tv = Tb[m * 32 + lane];
+        const float tv = Tb[m * kTs2 + lane];
         x[0] = fmaf(a4.x, tv, x[0]);
         x[1] = fmaf(a4.y, tv, x[1]);
         x[2] = fmaf(a4.z, tv, x[2]);
