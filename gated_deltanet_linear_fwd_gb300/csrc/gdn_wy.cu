@@ -51,7 +51,7 @@ constexpr uint32_t kTW = 64;   // W^T               128 x 64
 constexpr uint32_t kTU = 0;    // U^T               128 x 64 (over D, read by then)
 
 struct WyCtl {
-  uint64_t full, kq, wu;
+  uint64_t full, vfull, kq, wu;  // K|Q landed, V landed, D done, W and U done
   uint32_t tmem;
   int abort;
   float warp_total[2];
@@ -236,13 +236,14 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
 
   // ---- loads; D = [K;Q] K^T as soon as they land ----
   if (tid == 0) {
-    mbar_arrive_expect_tx(&ctl->full, 49152u);
+    mbar_arrive_expect_tx(&ctl->full, 32768u);
+    mbar_arrive_expect_tx(&ctl->vfull, 16384u);
     tma_load_3d(sm + kWyKQ, mk, &ctl->full, 0, iq, (int)t0);
     tma_load_3d(sm + kWyKQ + 16384, mk, &ctl->full, 64, iq, (int)t0);
     tma_load_3d(sm + kWyKQ + 8192, mq, &ctl->full, 0, iq, (int)t0);
     tma_load_3d(sm + kWyKQ + 24576, mq, &ctl->full, 64, iq, (int)t0);
-    tma_load_3d(sm + kWyV, mv, &ctl->full, 0, j, (int)t0);
-    tma_load_3d(sm + kWyV + 8192, mv, &ctl->full, 64, j, (int)t0);
+    tma_load_3d(sm + kWyV, mv, &ctl->vfull, 0, j, (int)t0);  // needed only by U, near the end
+    tma_load_3d(sm + kWyV + 8192, mv, &ctl->vfull, 64, j, (int)t0);
   }
   if (warp == 2 || warp == 3) {  // gate cumsum; rows past the sequence end act as g = beta = 0
     const int r = tid - 64;
@@ -412,12 +413,15 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
       for (int ks = 0; ks < 4; ++ks)
         mma_bf16(tmem + kTW, sdesc_sw128(sKQ + ks * 2048, 16384, 1024),
                  sdesc_sw128(sKQ + 8192 + part * 16384 + ks * 2048, 8192, 1024), id_mn, (part | ks) > 0);
+    if (wait_phase(&ctl->vfull, 0, &ctl->abort, 103)) {
+      tc_fence_after();
 #pragma unroll
-    for (int part = 0; part < 2; ++part)
+      for (int part = 0; part < 2; ++part)
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + kTU, sdesc_sw128(sV + ks * 2048, 8192, 1024),
-                 sdesc_sw128(sF + part * 8192 + ks * 2048, 8192, 1024), id_mn, (part | ks) > 0);
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tmem + kTU, sdesc_sw128(sV + ks * 2048, 8192, 1024),
+                   sdesc_sw128(sF + part * 8192 + ks * 2048, 8192, 1024), id_mn, (part | ks) > 0);
+    }
     mma_commit(&ctl->wu);
   }
   ok = wait_phase(&ctl->wu, 0, &ctl->abort, 102);
@@ -475,6 +479,7 @@ __global__ void __launch_bounds__(kWyThreads, 3)
   grid_launch_dependents();
   if (tid == 0) {
     mbar_init(&ctl->full, 1);
+    mbar_init(&ctl->vfull, 1);
     mbar_init(&ctl->kq, 1);
     mbar_init(&ctl->wu, 1);
     ctl->abort = 0;
@@ -493,7 +498,9 @@ __global__ void __launch_bounds__(kWyThreads, 3)
   const uint32_t tmem = ctl->tmem;
   float mx = 0.f;  // largest magnitude rounded to fp16 by this thread
   wy_body(sm, ctl, p, &mq, &mk, &mv, tmem, mx);
-  if (tid == 64) bulk_wait_all();  // the record's stores have landed (and read shared memory)
+  // the record's bulk stores have read shared memory before it is released (the
+  // grid completes only once they have landed)
+  if (tid == 64) bulk_wait_read_all();
   tc_fence_before();
   __syncthreads();
   if (ctl->abort) {
