@@ -221,6 +221,33 @@ def time_gpu(name, steps, warmup, device, cp="auto", lambda_=0.0, trace=True):
             "modes": modes.flatten().tolist(), "tokens": w.T}
 
 
+VARLEN = "varlen4_T348160_h2x8"
+
+
+def compare_cp_modes(name, steps, device):
+    """The same workload without context parallelism, with every head
+    combined exactly, and in the automatic mode (warmup restarts where the
+    gate bound allows): time of each, and how far each mode's o and final
+    state are from the exact ones (max |diff| / RMS of the exact result)."""
+    from gated_deltanet_linear_fwd_gb300 import gdn_chunk_fwd, gdn_cp_plan
+    from gated_deltanet_linear_fwd_gb300.inputs import workload
+    res = {}
+    for cp in ("off", "exact", "auto"):
+        t = time_gpu(name, steps, 3, device, cp, 0.0, trace=False)
+        res[cp] = {"ms": t["ms"], "segments": t["plan"].n_seg_total, "head_modes": t["modes"]}
+    w = workload(name)
+    d = w.to(device)
+    outs = {}
+    for cp in ("off", "exact", "auto"):
+        plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, cu_seqlens=w.cu_seqlens, mode=cp)
+        outs[cp] = gdn_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, plan=plan)
+    rel = lambda a, b: float((a.float() - b.float()).abs().max() / b.float().pow(2).mean().sqrt())
+    for cp in ("off", "auto"):
+        res[cp + "_vs_exact"] = {"o": rel(outs[cp][0], outs["exact"][0]),
+                                 "final_state": rel(outs[cp][1], outs["exact"][1])}
+    return res
+
+
 DECODE_BATCH = (256, 2, 8)  # sequences, h_qk, h_v: one token each; 268 MB of state read and written per step
 
 
@@ -445,6 +472,8 @@ def main(argv=None):
                            "kernels_ms": s["kernel_ms"], "head_modes": s["modes"]}
             if name in PAGES_H200_MS:
                 sweep[name]["pages_h200_ms"] = PAGES_H200_MS[name]
+            if name == VARLEN:  # AutoCP: exact combine for every head against the automatic warmup mode
+                sweep[name]["modes"] = compare_cp_modes(name, max(20, args.steps // 20), device)
         line["sweep"] = sweep
     if not args.no_sweep and rank == 0:
         line["decode"] = time_decode(max(20, args.steps // 10), 5, device, hbm)

@@ -293,7 +293,7 @@ gdn_status gdn_cp_plan(const gdn_dims* dims, const int32_t* cu, const gdn_cp_opt
   } else if (dims->n_seqs != dims->B) {
     return GDN_ERR_INVALID_ARG;
   }
-  gdn_cp_opts o = {GDN_CP_AUTO, 1.0f, 8, 1e-4f, 0};
+  gdn_cp_opts o = {GDN_CP_AUTO, 0.0f, 8, 1e-4f, 0};  // NULL opts: the planner picks lambda
   if (opts) o = *opts;
   if (o.mode < GDN_CP_OFF || o.mode > GDN_CP_AUTO) return GDN_ERR_UNSUPPORTED;
   const bool auto_lambda = !(o.lambda > 0.f);

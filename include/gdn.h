@@ -132,7 +132,8 @@ typedef struct gdn_cp_plan_t {
  *   dims              : problem sizes (see gdn_dims).
  *   cu_seqlens_host   : n_seqs+1 non-decreasing token offsets starting at 0
  *                       and ending at T, or NULL for B fixed-length rows of T.
- *   opts              : may be NULL (all defaults, mode AUTO).
+ *   opts              : may be NULL (all defaults: mode AUTO, lambda chosen by
+ *                       the planner, warmup 8 chunks at 1e-4, SMs of the device).
  *   out_plan          : written on success.
  * Segmentation of a sequence with N = ceil(len/64) chunks: L = max(1,
  * floor((isqrt(lambda_q8^2 * N) + 128) / 256)), n_seg = max(1, ceil(N / L)),
