@@ -17,9 +17,11 @@
 // and writes -W, U^T, P and (gamma, dec) as one record per (chunk, value
 // head), each tile in the 128-byte-swizzled layout the scan's MMAs read.
 //
-// One CTA of 256 threads per (chunk, value head), three CTAs per SM: the
-// shared-memory regions are reused as the work moves on (the A operands
-// go where Q and L were), and P and the gates go straight to global memory.
+// One CTA of 256 threads per (chunk, value head), four CTAs per SM: the
+// shared-memory regions are reused as the work moves on (V lands where Q
+// was once D has read it, the A operands of W and then of U go where L was,
+// -W and U^T go where K and V were), and P and the gates go straight to
+// global memory.
 #include <cuda_bf16.h>
 
 #include "gdn_dev.cuh"
@@ -30,19 +32,22 @@ namespace {
 constexpr int kWyThreads = 256;
 
 // ---- shared memory map (bytes from a 1024-byte aligned base) ----
-constexpr uint32_t kWyKQ = 0;          // bf16 [K d0-63 | Q d0-63 | K d64-127 | Q d64-127] (TMA); once Q
-                                       // is consumed, its two slots hold A diag(beta gamma) hi | lo
-constexpr uint32_t kWyV = 32768;       // bf16 [V d0-63 | V d64-127] (TMA); finally the U^T tile
-constexpr uint32_t kWyF = 49152;       // fp32 [64][68]: L below the diagonal, A^T on and above it; then
-                                       // A diag(beta) hi | lo (8 KB each); finally the -W tile
+constexpr uint32_t kWyKQ = 0;          // bf16 [K d0-63 | Q d0-63 | K d64-127 | Q d64-127] (TMA).  Once D
+                                       // has read Q, V d0-63 | V d64-127 land in the Q slots; once W and
+                                       // U are computed, the K slots take the two row halves of the -W
+                                       // tile and the Q slots those of the U^T tile
+constexpr uint32_t kWyV0 = 8192, kWyV1 = 24576;
+constexpr uint32_t kWyF = 32768;       // fp32 [64][68]: L below the diagonal, A^T on and above it; then
+                                       // the A operand hi | lo (8 KB each): A diag(beta gamma) for W,
+                                       // then A diag(beta) for U
 constexpr uint32_t kFStride = 68;
-constexpr uint32_t kWyScr = 66560;     // fp32 solve scratch (4.5 KB): T blocks, rows padded against
-                                       // bank conflicts
-constexpr uint32_t kWyGates = 71168;   // G | exp(G) | exp(G_63 - G) | beta | exp(-G), 64 floats each
-constexpr uint32_t kWyCtl = 72448;
-constexpr uint32_t kWySmemUse = 72512;
+constexpr uint32_t kWyScr = kWyF + 64 * kFStride * 4;  // fp32 solve scratch (4.5 KB): T blocks, rows
+                                                        // padded against bank conflicts
+constexpr uint32_t kWyGates = kWyScr + 4608;  // G | exp(G) | exp(G_63 - G) | beta | exp(-G), 64 floats each
+constexpr uint32_t kWyCtl = kWyGates + 1280;
+constexpr uint32_t kWySmemUse = kWyCtl + 64;
 constexpr uint32_t kWySmemAlloc = kWySmemUse + 1024;
-static_assert(3 * (kWySmemAlloc + 1024) <= 233472, "three CTAs per SM must fit");
+static_assert(4 * (kWySmemAlloc + 1024) <= 233472, "four CTAs per SM must fit");
 
 // ---- TMEM columns ----
 constexpr uint32_t kTmemCols = 128;
@@ -51,7 +56,7 @@ constexpr uint32_t kTW = 64;   // W^T               128 x 64
 constexpr uint32_t kTU = 0;    // U^T               128 x 64 (over D, read by then)
 
 struct WyCtl {
-  uint64_t full, vfull, kq, wu;  // K|Q landed, V landed, D done, W and U done
+  uint64_t full, vfull, kq, w, u;  // K|Q landed, V landed, D done, W done, U done
   uint32_t tmem;
   int abort;
   float warp_total[2];
@@ -230,20 +235,17 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
   float* sEm = gts + 256;
   float* F = reinterpret_cast<float*>(sm + kWyF);
   float* scratch = reinterpret_cast<float*>(sm + kWyScr);
-  const uint32_t sKQ = smem_u32(sm + kWyKQ), sV = smem_u32(sm + kWyV), sF = smem_u32(sm + kWyF);
+  const uint32_t sKQ = smem_u32(sm + kWyKQ), sF = smem_u32(sm + kWyF);
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   uint8_t* rec = p.wy + ((size_t)gc * p.h_v + j) * kRecBytes;
 
   // ---- loads; D = [K;Q] K^T as soon as they land ----
   if (tid == 0) {
     mbar_arrive_expect_tx(&ctl->full, 32768u);
-    mbar_arrive_expect_tx(&ctl->vfull, 16384u);
     tma_load_3d(sm + kWyKQ, mk, &ctl->full, 0, iq, (int)t0);
     tma_load_3d(sm + kWyKQ + 16384, mk, &ctl->full, 64, iq, (int)t0);
     tma_load_3d(sm + kWyKQ + 8192, mq, &ctl->full, 0, iq, (int)t0);
     tma_load_3d(sm + kWyKQ + 24576, mq, &ctl->full, 64, iq, (int)t0);
-    tma_load_3d(sm + kWyV, mv, &ctl->vfull, 0, j, (int)t0);  // needed only by U, near the end
-    tma_load_3d(sm + kWyV + 8192, mv, &ctl->vfull, 64, j, (int)t0);
   }
   if (warp == 2 || warp == 3) {  // gate cumsum; rows past the sequence end act as g = beta = 0
     const int r = tid - 64;
@@ -283,6 +285,11 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
   bool ok = wait_phase(&ctl->kq, 0, &ctl->abort, 101);
   if (__syncthreads_or(!ok)) return false;
   tc_fence_after();
+  if (tid == 0) {  // D has read Q: V into its slots (needed only by U, after the inverse)
+    mbar_arrive_expect_tx(&ctl->vfull, 16384u);
+    tma_load_3d(sm + kWyV0, mv, &ctl->vfull, 0, j, (int)t0);
+    tma_load_3d(sm + kWyV1, mv, &ctl->vfull, 64, j, (int)t0);
+  }
 
   // ---- L (TMEM lanes 0-63) into F; P (lanes 64-127) into the record, as its
   //      swizzled operand tile ----
@@ -372,67 +379,75 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
   // ---- A = (I + L)^{-1} ----
   solve_unit_lower(F, scratch, tid);
 
-  // ---- A operands: row s of A^T scaled by beta gamma (for W) / beta (for U),
-  //      split into bf16 high parts and remainders; A diag(beta gamma) goes to
-  //      the Q slots, A diag(beta) over F (read into registers first) ----
+  // ---- A operands: quarter c of row s of A^T, scaled by beta gamma (for W),
+  //      then by beta (for U), split into bf16 high parts and remainders, in
+  //      the hi | lo buffer over F; W^T = K^T (A diag(beta gamma))^T and
+  //      U^T = V^T (A diag(beta))^T take it in turn (A = hi + lo) ----
+  const int s = tid >> 2, qc = tid & 3;  // columns 16 qc .. 16 qc + 15 of row s
+  float a[16];
   {
-    const int row = tid >> 1, hs = tid & 1;
-    const int s = row & 63, mat = row >> 6;
-    const float sc = mat == 0 ? sBeta[s] * sGam[s] : sBeta[s];
-    const float* At = F + s * kFStride + 32 * hs;
-    float v[32];
+    const float* At = F + s * kFStride + 16 * qc;
 #pragma unroll
-    for (int q4 = 0; q4 < 8; ++q4) {
+    for (int q4 = 0; q4 < 4; ++q4) {
       const float4 a4 = *reinterpret_cast<const float4*>(At + 4 * q4);
-      v[4 * q4] = a4.x;
-      v[4 * q4 + 1] = a4.y;
-      v[4 * q4 + 2] = a4.z;
-      v[4 * q4 + 3] = a4.w;
-    }
-    __syncthreads();  // F is read: its first 16 KB take A diag(beta)
-    const uint32_t hi_base = mat == 0 ? sKQ + 8192 : sF, lo_base = mat == 0 ? sKQ + 24576 : sF + 8192;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int qq = hs * 4 + q;
-      float f[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) f[e] = (8 * qq + e >= s) ? v[8 * q + e] * sc : 0.f;
-      store_bf16x8_hilo(hi_base + sw128_offset(s, qq), lo_base + sw128_offset(s, qq), f);
+      a[4 * q4] = (16 * qc + 4 * q4 + 0 >= s) ? a4.x : 0.f;
+      a[4 * q4 + 1] = (16 * qc + 4 * q4 + 1 >= s) ? a4.y : 0.f;
+      a[4 * q4 + 2] = (16 * qc + 4 * q4 + 2 >= s) ? a4.z : 0.f;
+      a[4 * q4 + 3] = (16 * qc + 4 * q4 + 3 >= s) ? a4.w : 0.f;
     }
   }
+  auto store_operand = [&](float sc) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float f[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = a[8 * h + e] * sc;
+      store_bf16x8_hilo(sF + sw128_offset(s, 2 * qc + h), sF + 8192 + sw128_offset(s, 2 * qc + h), f);
+    }
+  };
+  const uint32_t id_mn = idesc_bf16_f32(128, 64, true, true);
+  __syncthreads();  // F is read: its first 16 KB take the operand
+  store_operand(sBeta[s] * sGam[s]);
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
-
-  if (tid == 32) {  // W^T = K^T (A diag(beta gamma))^T, U^T = V^T (A diag(beta))^T, A = hi + lo
+  if (tid == 32) {
     tc_fence_after();
-    const uint32_t id_mn = idesc_bf16_f32(128, 64, true, true);
 #pragma unroll
     for (int part = 0; part < 2; ++part)
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
         mma_bf16(tmem + kTW, sdesc_sw128(sKQ + ks * 2048, 16384, 1024),
-                 sdesc_sw128(sKQ + 8192 + part * 16384 + ks * 2048, 8192, 1024), id_mn, (part | ks) > 0);
+                 sdesc_sw128(sF + part * 8192 + ks * 2048, 8192, 1024), id_mn, (part | ks) > 0);
+    mma_commit(&ctl->w);
+  }
+  ok = wait_phase(&ctl->w, 0, &ctl->abort, 102);
+  if (__syncthreads_or(!ok)) return false;
+  tc_fence_after();
+  store_operand(sBeta[s]);
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 32) {
     if (wait_phase(&ctl->vfull, 0, &ctl->abort, 103)) {
       tc_fence_after();
 #pragma unroll
       for (int part = 0; part < 2; ++part)
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tmem + kTU, sdesc_sw128(sV + ks * 2048, 8192, 1024),
+          mma_bf16(tmem + kTU, sdesc_sw128(sKQ + kWyV0 + ks * 2048, 16384, 1024),
                    sdesc_sw128(sF + part * 8192 + ks * 2048, 8192, 1024), id_mn, (part | ks) > 0);
     }
-    mma_commit(&ctl->wu);
+    mma_commit(&ctl->u);
   }
-  ok = wait_phase(&ctl->wu, 0, &ctl->abort, 102);
-  if (__syncthreads_or(!ok)) return false;
-  tc_fence_after();
 
-  // ---- -W and U^T tiles (over A diag(beta) and V, which the MMAs have consumed).
-  //      No range check here: an fp16 overflow of either becomes inf in the
-  //      scan's V' = U - W S, which the scan checks every chunk. ----
+  // ---- -W and U^T tiles, row halves d 0-63 | 64-127 in the slots of K (read
+  //      by W) and of V (read by U).  No range check here: an fp16 overflow of
+  //      either becomes inf in the scan's V' = U - W S, which the scan checks
+  //      every chunk. ----
   {
     const int d = (warp & 3) * 32 + lane, ch = warp >> 2;
+    const uint32_t half = (uint32_t)(d >> 6) * 16384u;
     uint32_t ra[16], rb[16];
     tmem_ld16(tmem + lane_base + kTW + ch * 32, ra);
     tmem_ld16(tmem + lane_base + kTW + ch * 32 + 16, rb);
@@ -442,9 +457,12 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
       float f[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) f[e] = -__uint_as_float(q < 2 ? ra[8 * q + e] : rb[8 * (q - 2) + e]);
-      st_shared_v4(sF + sw128_offset(d, ch * 4 + q), pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]),
+      st_shared_v4(sKQ + half + sw128_offset(d & 63, ch * 4 + q), pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]),
                    pack_f16x2(f[4], f[5]), pack_f16x2(f[6], f[7]));
     }
+    ok = wait_phase(&ctl->u, 0, &ctl->abort, 104);
+    if (__syncthreads_or(!ok)) return false;
+    tc_fence_after();
     tmem_ld16(tmem + lane_base + kTU + ch * 32, ra);
     tmem_ld16(tmem + lane_base + kTU + ch * 32 + 16, rb);
     tmem_ld_wait(ra, rb);
@@ -453,22 +471,24 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
       float f[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(q < 2 ? ra[8 * q + e] : rb[8 * (q - 2) + e]);
-      st_shared_v4(sV + sw128_offset(d, ch * 4 + q), pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]),
-                   pack_f16x2(f[4], f[5]), pack_f16x2(f[6], f[7]));
+      st_shared_v4(sKQ + kWyV0 + half + sw128_offset(d & 63, ch * 4 + q), pack_f16x2(f[0], f[1]),
+                   pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]), pack_f16x2(f[6], f[7]));
     }
   }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   if (tid == 64) {
-    bulk_store(rec + kRecWn, sm + kWyF, 16384);
-    bulk_store(rec + kRecU, sm + kWyV, 16384);
+    bulk_store(rec + kRecWn, sm + kWyKQ, 8192);
+    bulk_store(rec + kRecWn + 8192, sm + kWyKQ + 16384, 8192);
+    bulk_store(rec + kRecU, sm + kWyV0, 8192);
+    bulk_store(rec + kRecU + 8192, sm + kWyV1, 8192);
     bulk_commit();
   }
   return true;
 }
 
-__global__ void __launch_bounds__(kWyThreads, 3)
+__global__ void __launch_bounds__(kWyThreads, 4)
     wy_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
               const __grid_constant__ CUtensorMap mv, const Problem p) {
   extern __shared__ uint8_t smem_raw[];
@@ -481,7 +501,8 @@ __global__ void __launch_bounds__(kWyThreads, 3)
     mbar_init(&ctl->full, 1);
     mbar_init(&ctl->vfull, 1);
     mbar_init(&ctl->kq, 1);
-    mbar_init(&ctl->wu, 1);
+    mbar_init(&ctl->w, 1);
+    mbar_init(&ctl->u, 1);
     ctl->abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&mk);
