@@ -66,28 +66,27 @@ static_assert(2 * 128 * kChainRegs + 2 * 128 * kOtherRegs <= 65536 && kThreads *
               "register split over the launch's 128 per thread");
 
 // ---- shared memory map (bytes from a 1024-byte aligned base) ----
-// Three rings of two slots each, each released as soon as its last reader
-// has run: ring A (-W, U^T) after A(i), ring K after D3(i), ring B (Q, P)
-// after O2(i).  So the loads for chunk i + 2 start as early as they can.
+// Three rings, each slot released as soon as its last reader has run: ring
+// A (-W, U^T; two slots) and ring K (two slots) after D3(i), ring B (Q, P;
+// three slots) after O2(i).  So the loads of chunk i + 2 (rings A, K) and
+// i + 3 (ring B) start as early as they can.
 constexpr uint32_t kRingA = 0;            // 2 slots of 32 KB:
 constexpr uint32_t kSlotA = 32768;
 constexpr uint32_t kAWn = 0;              //   fp16 -W, MN-major B: rows d_k
 constexpr uint32_t kAU = 16384;           //   fp16 U^T, K-major A: rows d_v
 constexpr uint32_t kRingK = 2 * kSlotA;   // 2 slots of 16 KB: [K d0-63 | K d64-127], 8 KB each, bf16 as
 constexpr uint32_t kSlotK = 16384;        //   loaded, then fp16 in place (K times dec)
-constexpr uint32_t kRingB = kRingK + 2 * kSlotK;  // 2 slots of 24 KB:
+constexpr uint32_t kRingB = kRingK + 2 * kSlotK;  // 3 slots of 24 KB (chunk i in slot i % 3):
 constexpr uint32_t kSlotB = 24576;
 constexpr uint32_t kBQ = 0;               //   [Q d0-63 | Q d64-127], 8 KB each, bf16 then fp16 in place
 constexpr uint32_t kBP = 16384;           //   fp16 P, K-major B: rows r
-constexpr uint32_t kStageBytes = 73728;   // per chunk over both rings
-constexpr uint32_t kSmO = 2 * kStageBytes;  // bf16 o of one chunk, [64 tokens][128 d_v] rows of 256 bytes
+constexpr uint32_t kSmO = kRingB + 3 * kSlotB;  // bf16 o of one chunk, [64 tokens][128 d_v] rows of 256 bytes
 constexpr uint32_t kSmG = kSmO + 16384;     // 4 slots (chunk i in slot i & 3): fp32 exp(G) [64], exp(G_63 - G) [64]
 constexpr uint32_t kSmCtl = kSmG + 4 * 512; // barriers, TMEM base, flags
 constexpr uint32_t kSmemUse = kSmCtl + 512;
 constexpr uint32_t kSmemAlloc = kSmemUse + 1024;
 static_assert(kSmemAlloc <= 232448, "shared memory over the per-block limit");
-static_assert(kRingB + 2 * kSlotB == 2 * kStageBytes && kSlotB % 1024 == 0 && kBP + 8192 <= kSlotB,
-              "ring layout");
+static_assert(kSlotB % 1024 == 0 && kBP + 8192 <= kSlotB, "ring layout");
 
 // ---- TMEM columns (512 allocated) ----
 constexpr uint32_t kTV = 0;     // -S W^T                      128 x 64
@@ -106,8 +105,8 @@ enum Bar {
   kYoDone0, kYoDone1, kYoFree0, kYoFree1,  // output epilogue (two O buffers)
   kKqFull0, kKqFull1,                      // ring K slots loaded (bf16)
   kKReady0, kKReady1, kQReady0, kQReady1,  // K, then Q, rounded to fp16
-  kEmptyB0, kEmptyB1,                      // ring B slots released
-  kQFull0, kQFull1,                        // ring B slots loaded (Q bf16, P)
+  kEmptyB0, kEmptyB1, kEmptyB2,            // ring B slots released
+  kQFull0, kQFull1, kQFull2,               // ring B slots loaded (Q bf16, P)
   kEmptyK0, kEmptyK1,                      // ring K slots released
   kNumBars
 };
@@ -160,8 +159,8 @@ __device__ __forceinline__ bool want_out(const Chain& ch, int i) {
 // dims per box (rows past the end of the input read as zero), its P (ring
 // B) and gates by bulk copies, and, a chunk ahead, its ring A tiles (-W,
 // U^T; bulk copies).  The waits come in the order the slots are released:
-// ring K of chunk i - 2 (after its D3), ring B of chunk i - 2 (after its
-// O2), ring A of chunk i - 1 (after its A).
+// ring B of chunk i - 3 (after its O2), ring K of chunk i - 2 (after its
+// D3), ring A of chunk i - 1 (after its D3).
 template <bool PREP>
 __device__ __forceinline__ void producer_role(uint8_t* sm, Ctl* ctl, const Problem& p, const Chain& ch, int j,
                                            const CUtensorMap* mq, const CUtensorMap* mk) {
@@ -177,28 +176,13 @@ __device__ __forceinline__ void producer_role(uint8_t* sm, Ctl* ctl, const Probl
   };
   if (n > 0) load_a(0);
   for (int i = 0; i < n; ++i) {
-    const bool out = want_out<PREP>(ch, i);
     const int t0 = (int)(ch.bos + (int64_t)(ch.run_begin + i) * kChunk);
-    // ring K and the gates
-    if (i >= 2 && !wait_bar(ctl, kEmptyK0 + (i & 1), (uint32_t)(((i - 2) >> 1) & 1))) return;
-    uint8_t* kslot = sm + kRingK + (i & 1) * kSlotK;
-    uint64_t* kbar = &ctl->bar[kKqFull0 + (i & 1)];
-    mbar_arrive_expect_tx(kbar, 16384u);
-    tma_load_3d(kslot, mk, kbar, 0, ch.iq, t0);
-    tma_load_3d(kslot + 8192, mk, kbar, 64, ch.iq, t0);
-    // The gates go to ring slot i & 3.  Its readers of chunk i - 4 are done:
-    // the converter before k_ready(i - 4), the state warps in the V' epilogue
-    // of chunk i - 4 (before v_ready(i - 4)), both waited for before D3(i - 4)
-    // was issued, and the output warps before yo_free(i - 4), which A(i - 2)
-    // waited for; ring K of chunk i - 2 is released after D3(i - 2).
-    uint64_t* gbar = &ctl->bar[kGates0 + (i & 3)];
-    mbar_arrive_expect_tx(gbar, 512u);
-    bulk_load(sm + kSmG + (i & 3) * 512, rec_of(i) + kRecGam, 512u, gbar);
-    // ring B: Q and P, only where the chunk's output is written
-    if (i >= 2 && !wait_bar(ctl, kEmptyB0 + (i & 1), (uint32_t)(((i - 2) >> 1) & 1))) return;
-    uint8_t* bslot = sm + kRingB + (i & 1) * kSlotB;
-    uint64_t* qbar = &ctl->bar[kQFull0 + (i & 1)];
-    if (out) {
+    // ring B (Q and P, only where the chunk's output is written) and the gates
+    const int sb = i % 3;
+    if (i >= 3 && !wait_bar(ctl, kEmptyB0 + sb, (uint32_t)(((i - 3) / 3) & 1))) return;
+    uint8_t* bslot = sm + kRingB + sb * kSlotB;
+    uint64_t* qbar = &ctl->bar[kQFull0 + sb];
+    if (want_out<PREP>(ch, i)) {
       mbar_arrive_expect_tx(qbar, 24576u);
       tma_load_3d(bslot + kBQ, mq, qbar, 0, ch.iq, t0);
       tma_load_3d(bslot + kBQ + 8192, mq, qbar, 64, ch.iq, t0);
@@ -206,6 +190,21 @@ __device__ __forceinline__ void producer_role(uint8_t* sm, Ctl* ctl, const Probl
     } else {
       mbar_arrive(qbar);  // nothing to load: the phase completes, keeping the slot's phases per chunk
     }
+    // The gates go to ring slot i & 3.  Its readers of chunk i - 4 are done:
+    // the converter before k_ready(i - 4), the state warps in the V' epilogue
+    // of chunk i - 4 (before v_ready(i - 4)), the output warps before
+    // q_ready(i - 4), all waited for before O2(i - 3) was issued, and ring B
+    // of chunk i - 3 is released after O2(i - 3).
+    uint64_t* gbar = &ctl->bar[kGates0 + (i & 3)];
+    mbar_arrive_expect_tx(gbar, 512u);
+    bulk_load(sm + kSmG + (i & 3) * 512, rec_of(i) + kRecGam, 512u, gbar);
+    // ring K
+    if (i >= 2 && !wait_bar(ctl, kEmptyK0 + (i & 1), (uint32_t)(((i - 2) >> 1) & 1))) return;
+    uint8_t* kslot = sm + kRingK + (i & 1) * kSlotK;
+    uint64_t* kbar = &ctl->bar[kKqFull0 + (i & 1)];
+    mbar_arrive_expect_tx(kbar, 16384u);
+    tma_load_3d(kslot, mk, kbar, 0, ch.iq, t0);
+    tma_load_3d(kslot + 8192, mk, kbar, 64, ch.iq, t0);
     if (i + 1 < n) {
       if (i + 1 >= 2 && !wait_bar(ctl, kEmpty0 + ((i + 1) & 1), (uint32_t)(((i - 1) >> 1) & 1))) return;
       load_a(i + 1);
@@ -283,16 +282,19 @@ __device__ __forceinline__ void convert_role(uint8_t* sm, Ctl* ctl, const Chain&
 //         published the state's fp16 copy (TMEM buffer i & 1); commits
 //         va_done (the state warps add U^T and write V'(i) in fp16 to TMEM
 //         buffer i & 1)
-//   D3(i) V'^T (diag(dec) K), after v_ready(i) and k_ready(i); commits
-//         d3_done (which also tells the state warps that Y(i-1), issued
-//         before it, has read state buffer (i+1) & 1) and releases rings K
-//         and A (the state warps read U^T before v_ready(i))
 //   Y(i)  O = S (gamma Q)^T into O buffer i & 1, after q_ready(i) and
-//         yo_free(i-2), then O2(i) O += V'^T P^T; commits yo_done(i) and
-//         releases ring B
+//         yo_free(i-2), issued while the state warps run the V' epilogue
+//   D3(i) V'^T (diag(dec) K), after v_ready(i) and k_ready(i); commits
+//         d3_done (which also tells the state warps that Y(i), issued
+//         before it, has read state buffer i & 1 before the state of chunk
+//         i + 2 goes there) and releases rings K and A (the state warps
+//         read U^T before v_ready(i))
+//   O2(i) O += V'^T P^T, issued while the state warps update the state;
+//         commits yo_done(i) and releases ring B.
 // The chain's critical path runs A(i) -> V' epilogue -> D3(i) -> state
-// epilogue -> A(i+1).  A(i+2), issued after O2(i), tells the state warps
-// through va_done that V' buffer i & 1 has been read.
+// epilogue -> A(i+1); the output products fill the issuer's time in between.
+// A(i+2), issued after O2(i), tells the state warps through va_done that V'
+// buffer i & 1 has been read.
 template <bool PREP>
 __device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch, uint32_t tmem) {
   const int n = ch.run_end - ch.run_begin;
@@ -301,16 +303,29 @@ __device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch,
   const uint32_t id_d3 = idesc_f16(128, 128, false, true);
   if (n > 0 && !wait_bar(ctl, kFull0, 0u)) return;  // ring A of chunk 0
   for (int i = 0; i < n; ++i) {
+    const int sb = i % 3;
     const uint32_t sA = smem_u32(sm + kRingA + (i & 1) * kSlotA), sK = smem_u32(sm + kRingK + (i & 1) * kSlotK);
-    const uint32_t sB = smem_u32(sm + kRingB + (i & 1) * kSlotB);
+    const uint32_t sB = smem_u32(sm + kRingB + sb * kSlotB);
     const uint32_t tS = tmem + kTS + (i & 1) * 64;    // the state's fp16 copy, 8 columns per K = 16 step
     const uint32_t tV = tmem + kTV16 + (i & 1) * 32;  // V''s fp16 copy, 8 columns per K = 16 step
+    const uint32_t tO = tmem + kTO + (i & 1) * 64;
+    const bool out = want_out<PREP>(ch, i);
     if (!spin_bar(ctl, kSReady, (uint32_t)(i & 1))) return;
     tc_fence_after();
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks)  // -S W^T
       mma_f16_ts(tmem + kTV, tS + ks * 8, sdesc_sw128(sA + kAWn + ks * 2048, 8192, 1024), id_sw, ks > 0 ? 1u : 0u);
     mma_commit(&ctl->bar[kVaDone]);
+    if (out) {
+      if (!wait_bar(ctl, kQReady0 + (i & 1), (uint32_t)((i >> 1) & 1))) return;
+      if (i >= 2 && !wait_bar(ctl, kYoFree0 + (i & 1), (uint32_t)(((i - 2) >> 1) & 1))) return;
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)  // O = S (gamma Q)^T
+        mma_f16_ts(tO, tS + ks * 8,
+                   sdesc_sw128(sB + kBQ + (uint32_t)(ks >> 2) * 8192u + (uint32_t)(ks & 3) * 32u, 16, 1024), id_k,
+                   ks > 0);
+    }
     if (!wait_bar(ctl, kKReady0 + (i & 1), (uint32_t)((i >> 1) & 1))) return;
     if (!spin_bar(ctl, kVReady, (uint32_t)(i & 1))) return;
     tc_fence_after();
@@ -320,21 +335,13 @@ __device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch,
     mma_commit(&ctl->bar[kD3Done]);
     mma_commit(&ctl->bar[kEmptyK0 + (i & 1)]);  // ring K slot read
     mma_commit(&ctl->bar[kEmpty0 + (i & 1)]);   // ring A slot read (A(i); U^T before v_ready(i))
-    if (want_out<PREP>(ch, i)) {
-      if (!wait_bar(ctl, kQReady0 + (i & 1), (uint32_t)((i >> 1) & 1))) return;
-      if (i >= 2 && !wait_bar(ctl, kYoFree0 + (i & 1), (uint32_t)(((i - 2) >> 1) & 1))) return;
-      tc_fence_after();
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks)  // O = S (gamma Q)^T
-        mma_f16_ts(tmem + kTO + (i & 1) * 64, tS + ks * 8,
-                   sdesc_sw128(sB + kBQ + (uint32_t)(ks >> 2) * 8192u + (uint32_t)(ks & 3) * 32u, 16, 1024), id_k,
-                   ks > 0);
+    if (out) {
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)  // O += V'^T P^T
-        mma_f16_ts(tmem + kTO + (i & 1) * 64, tV + ks * 8, sdesc_sw128(sB + kBP + ks * 32, 16, 1024), id_k, 1u);
+        mma_f16_ts(tO, tV + ks * 8, sdesc_sw128(sB + kBP + ks * 32, 16, 1024), id_k, 1u);
     }
     mma_commit(&ctl->bar[kYoDone0 + (i & 1)]);
-    mma_commit(&ctl->bar[kEmptyB0 + (i & 1)]);  // ring B slot read (Y, O2)
+    mma_commit(&ctl->bar[kEmptyB0 + sb]);  // ring B slot read (Y, O2)
     if (i + 1 < n && !wait_bar(ctl, kFull0 + ((i + 1) & 1), (uint32_t)(((i + 1) >> 1) & 1))) return;  // ring A
   }
 }
@@ -363,10 +370,10 @@ __device__ __forceinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem
   // q_ready, so its phases follow c.
   auto round_q = [&](int c) -> bool {
     if (want_out<PREP>(ch, c)) {
-      if (!wait_bar(ctl, kQFull0 + (c & 1), (uint32_t)((c >> 1) & 1)) ||
+      if (!wait_bar(ctl, kQFull0 + c % 3, (uint32_t)((c / 3) & 1)) ||
           !wait_bar(ctl, kGates0 + (c & 3), (uint32_t)((c >> 2) & 1)))
         return false;
-      round_q_tile(smem_u32(sm + kRingB + (c & 1) * kSlotB + kBQ), smem_u32(sm + kSmG + (c & 3) * 512),
+      round_q_tile(smem_u32(sm + kRingB + (c % 3) * kSlotB + kBQ), smem_u32(sm + kSmG + (c & 3) * 512),
                    threadIdx.x - kOutWarp * 32);
       fence_proxy_async_smem();
     }
@@ -415,7 +422,7 @@ __device__ __forceinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem
     }
     tc_fence_before();
     mbar_arrive(&ctl->bar[kYoFree0 + (i & 1)]);  // O buffer i & 1 read
-    if (i + 2 < n && !round_q(i + 2)) break;  // its ring B slot was released with yo_done(i)
+    if (i + 2 < n && !round_q(i + 2)) break;  // its ring B slot was loaded after O2(i - 1)
   }
   if (issuer) bulk_wait_all();  // the stores have landed before the block exits
   if (!(mx <= 3.4028235e38f)) atomicExch(&ctl->range_bad, 1);
@@ -526,7 +533,7 @@ __device__ __forceinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem&
       }
     }
     // buffer (i + 1) & 1 was last read by A(i - 1) and Y(i - 1), both issued
-    // before D3(i), whose completion this thread has seen
+    // before D3(i - 1), whose completion this thread has seen
     store_state(i + 1);
     tc_fence_before();
     mbar_arrive(&ctl->bar[kSReady]);
@@ -648,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     const int counts[kNumBars] = {1, 1, 1, 1, 1, 1, 1, 1, 1, kChainThreads, 1, kChainThreads,
                                   1, 1, kOutThreads, kOutThreads, 1, 1, kConvertWarps, kConvertWarps,
-                                  kOutThreads / 32, kOutThreads / 32, 1, 1, 1, 1, 1, 1};
+                                  kOutThreads / 32, kOutThreads / 32, 1, 1, 1, 1, 1, 1, 1, 1};
     for (int b = 0; b < kNumBars; ++b) mbar_init(&ctl->bar[b], counts[b]);
     ctl->abort = 0;
     ctl->range_bad = 0;
