@@ -158,3 +158,22 @@ def test_parity_standard_workloads(name):
     f = util.to64
     ref = oracle.recurrence(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0), w.seq_offsets())
     check(o, hT, ref, f"{name} plan={plan.mode} segs={plan.n_seg_total} modes={modes.flatten().tolist()}")
+
+
+def test_null_plan_options_are_the_documented_defaults():
+    """gdn_cp_plan with NULL options: mode AUTO, lambda chosen by the planner,
+    warmup 8 chunks at 1e-4, the current device's SM count."""
+    import ctypes
+    from gated_deltanet_linear_fwd_gb300 import _lib as L
+    lib = L.load()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for cu in ([0, 32768], [0, 100, 100, 165, 4000], [0, 262144, 327680, 344064, 348160]):
+        dims = L.gdn_dims(1, cu[-1], 2, 8, 128, 128, len(cu) - 1, 0.0, L.GDN_BF16)
+        arr = (ctypes.c_int32 * len(cu))(*cu)
+        got, want = L.gdn_cp_plan_t(), L.gdn_cp_plan_t()
+        assert lib.gdn_cp_plan(ctypes.byref(dims), arr, None, ctypes.byref(got)) == 0
+        opts = L.gdn_cp_opts(L.GDN_CP_AUTO, 0.0, 8, 1e-4, sms)
+        assert lib.gdn_cp_plan(ctypes.byref(dims), arr, ctypes.byref(opts), ctypes.byref(want)) == 0
+        for f in ("mode", "lambda_q8", "n_seg_total", "warmup_chunks", "sm_count", "workspace_bytes"):
+            assert getattr(got, f) == getattr(want, f), (cu, f)
+        assert abs(got.warmup_tol - 1e-4) < 1e-9 and got.sm_count == sms
