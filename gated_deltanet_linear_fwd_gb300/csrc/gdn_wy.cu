@@ -460,9 +460,15 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
       st_shared_v4(sKQ + half + sw128_offset(d & 63, ch * 4 + q), pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]),
                    pack_f16x2(f[4], f[5]), pack_f16x2(f[6], f[7]));
     }
+    fence_proxy_async_smem();
     ok = wait_phase(&ctl->u, 0, &ctl->abort, 104);
-    if (__syncthreads_or(!ok)) return false;
+    if (__syncthreads_or(!ok)) return false;  // also: every thread's -W rows are written
     tc_fence_after();
+    if (tid == 64) {  // -W into the record while U is read back
+      bulk_store(rec + kRecWn, sm + kWyKQ, 8192);
+      bulk_store(rec + kRecWn + 8192, sm + kWyKQ + 16384, 8192);
+      bulk_commit();
+    }
     tmem_ld16(tmem + lane_base + kTU + ch * 32, ra);
     tmem_ld16(tmem + lane_base + kTU + ch * 32 + 16, rb);
     tmem_ld_wait(ra, rb);
@@ -479,8 +485,6 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
   tc_fence_before();
   __syncthreads();
   if (tid == 64) {
-    bulk_store(rec + kRecWn, sm + kWyKQ, 8192);
-    bulk_store(rec + kRecWn + 8192, sm + kWyKQ + 16384, 8192);
     bulk_store(rec + kRecU, sm + kWyV0, 8192);
     bulk_store(rec + kRecU + 8192, sm + kWyV1, 8192);
     bulk_commit();
