@@ -283,41 +283,71 @@ def time_decode(steps, warmup, device, hbm):
 
 
 def time_e2e(name, steps, warmup, device, cp="auto"):
-    """The same forward through the public call from pinned host buffers."""
+    """The same forward through the public call from pinned host buffers, as
+    a serving loop would run it: every step copies its inputs host -> device,
+    runs the forward and reads o and the final state back, with the copies of
+    one step overlapping the forward of its neighbours (an input stream, the
+    compute stream and an output stream; device and host buffers alternate
+    between two sets).  The timed region starts before the first step's first
+    copy and ends after the last step's last read."""
     from gated_deltanet_linear_fwd_gb300 import gdn_chunk_fwd, gdn_cp_plan
     from gated_deltanet_linear_fwd_gb300.inputs import workload
     w = workload(name)
     pin = lambda t: None if t is None else t.pin_memory()
-    hq, hk, hv_, hg, hb, hh0 = map(pin, (w.q, w.k, w.v, w.g, w.beta, w.h0))
+    hin = [t for t in map(pin, (w.q, w.k, w.v, w.g, w.beta, w.h0))]
     dev = lambda t: None if t is None else torch.empty_like(t, device=device)
-    dq, dk, dv, dg, db, dh0 = map(dev, (hq, hk, hv_, hg, hb, hh0))
+    din = [[dev(t) for t in hin] for _ in range(2)]
     dcu = None if w.cu_seqlens is None else w.cu_seqlens.to(device)
     plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, cu_seqlens=w.cu_seqlens, mode=cp)
     ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
-    out = torch.empty_like(dv)
-    hT = torch.empty(w.n_seqs, w.h_v, D, D, dtype=torch.float32, device=device)
-    ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    hhT = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv_, hg, hb) + ((hh0,) if hh0 is not None else ()))
-    d2h = ho.numel() * ho.element_size() + hhT.numel() * hhT.element_size()
-    stream = torch.cuda.current_stream(device)
+    dout = [torch.empty_like(din[0][2]) for _ in range(2)]
+    dhT = [torch.empty(w.n_seqs, w.h_v, D, D, dtype=torch.float32, device=device) for _ in range(2)]
+    hout = [torch.empty(dout[0].shape, dtype=dout[0].dtype).pin_memory() for _ in range(2)]
+    hhT = [torch.empty(dhT[0].shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in hin if t is not None)
+    d2h = hout[0].numel() * hout[0].element_size() + hhT[0].numel() * hhT[0].element_size()
+    comp = torch.cuda.current_stream(device)
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ev = lambda: torch.cuda.Event()
+    in_ready, in_free, done, out_free = ([ev(), ev()] for _ in range(4))
+    used = [False, False]
 
-    def step():
-        for src, dst in ((hq, dq), (hk, dk), (hv_, dv), (hg, dg), (hb, db), (hh0, dh0)):
-            if src is not None:
-                dst.copy_(src, non_blocking=True)
-        gdn_chunk_fwd(dq, dk, dv, dg, db, dh0, dcu, plan=plan, out=out, final_state=hT, workspace=ws)
-        ho.copy_(out, non_blocking=True)
-        hhT.copy_(hT, non_blocking=True)
+    def step(k):
+        b = k & 1
+        with torch.cuda.stream(s_in):
+            if used[b]:
+                s_in.wait_event(in_free[b])  # the forward two steps back has read this set
+            for src, dst in zip(hin, din[b]):
+                if src is not None:
+                    dst.copy_(src, non_blocking=True)
+            in_ready[b].record(s_in)
+        comp.wait_event(in_ready[b])
+        if used[b]:
+            comp.wait_event(out_free[b])  # its outputs two steps back have been read
+        q, k_, v, g, beta, h0 = din[b]
+        gdn_chunk_fwd(q, k_, v, g, beta, h0, dcu, plan=plan, out=dout[b], final_state=dhT[b], workspace=ws,
+                      stream=comp)
+        done[b].record(comp)
+        in_free[b].record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(done[b])
+            hout[b].copy_(dout[b], non_blocking=True)
+            hhT[b].copy_(dhT[b], non_blocking=True)
+            out_free[b].record(s_out)
+        used[b] = True
 
-    for _ in range(warmup):
-        step()
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize(device)
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s0.record(stream)
-    for _ in range(steps):
-        step()
-    s1.record(stream)
+    s0.record(comp)
+    s_in.wait_event(s0)
+    s_out.wait_event(s0)
+    for i in range(steps):
+        step(warmup + i)
+    for b in range(2):
+        comp.wait_event(out_free[b])
+    s1.record(comp)
     s1.synchronize()
     ms = s0.elapsed_time(s1) / steps
     return {"ms": ms, "h2d": h2d, "d2h": d2h, "tokens": w.T}

@@ -33,13 +33,14 @@
 //
 // Warp roles (512 threads, four warpgroups): warps 0-7 hold the state (row =
 // d_v lane, 64 columns each) and run the V' and state epilogues, the
-// critical path from one chunk to the next; warps 8-11 read Y and O2 and
-// stage the chunk's outputs in shared memory and store them (TMA) while
-// the state warps go on to the next chunk;
-// warp 12 loads each chunk's record (bulk copies) and its K and Q tiles
-// (TMA); lane 0 of warp 13 issues every MMA; warps 14-15 round the bf16 K
-// (times the decay to the chunk end) and Q tiles to fp16 in place, a chunk
-// ahead of the MMAs that read them.
+// critical path from one chunk to the next; warps 8-11 read the output
+// accumulator (Y + O2) and stage the chunk's outputs in shared memory and
+// store them (TMA) while the state warps go on to the next chunk, and round
+// the bf16 Q tiles (times gamma) to fp16 in place two chunks ahead; warp 12
+// loads each chunk's record (bulk copies) and its K and Q tiles (TMA); lane
+// 0 of warp 13 issues every MMA, in the order A, Y, D3, O2; warps 14-15
+// round the bf16 K tiles (times the decay to the chunk end) to fp16 in
+// place ahead of the D3 that reads them.
 // The state warpgroups raise their register limit to 168 (the state takes
 // 64 per thread) and the others lower theirs to 88, within the 128 per
 // thread the block is launched with.  The roles hand over through
