@@ -21,12 +21,6 @@ __device__ __forceinline__ float lds_f32(uint32_t addr) {
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
   return v;
 }
-__device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
-               : "memory");
-  return v;
-}
 __device__ __forceinline__ uint4 lds_u32x4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
@@ -67,9 +61,6 @@ __device__ __forceinline__ void store_bf16x8_hilo(uint32_t addr_hi, uint32_t add
 }
 
 // Two packed bf16 (times d) -> two packed fp16, round to nearest.
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-  return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float d) {
   return pack_f16x2(__uint_as_float(w << 16) * d, __uint_as_float(w & 0xffff0000u) * d);
 }
