@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
       for (int r = 0; r < kRows; ++r)
         *reinterpret_cast<float4*>(sP + (ks * kRows + r) * kDim + c4) =
             make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-      __syncthreads();
+      __syncthreads();  // partial sums written; R, S_loc and sX read for this step
       if (own) {
 #pragma unroll
         for (int q = 0; q < kSlices; ++q) {
@@ -147,8 +147,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
           a3 += t4.w;
         }
       }
+    } else {
+      __syncthreads();  // S_loc read before its buffer is refilled
     }
-    __syncthreads();
+    // The new rows go to sX once every thread has read it (the barrier above);
+    // the next step reads them, and overwrites sP, only after its own barrier.
     if (own) {
       *reinterpret_cast<float4*>(sX + rr * kDim + c4) = make_float4(a0, a1, a2, a3);
       *reinterpret_cast<float4*>(p.Sstart + ((size_t)(si.seg_base + s + 1) * p.h_v + j) * mat +
