@@ -9,6 +9,7 @@ configuration are compared element by element as well (the oracle runs a
 """
 from __future__ import annotations
 
+import dataclasses
 import functools
 
 import numpy as np
@@ -50,8 +51,25 @@ def ref_of(key):
     return oracle.recurrence(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0), w.seq_offsets())
 
 
+def _strong_decay():
+    # g about -3 per token: a chunk's cumulative gate reaches about -190, past the range
+    # where exp(G_r) exp(-G_s) can be formed as a product, and exp(G) underflows in fp32
+    w = make_inputs(cu_seqlens=[0, 70, 333, 700], h_qk=1, h_v=2, seed=13, with_h0=True)
+    gen = torch.Generator().manual_seed(14)
+    return dataclasses.replace(w, g=(-3.0 + 0.5 * torch.randn(w.g.shape, generator=gen)).float())
+
+
+def _no_write():
+    # beta = 0: nothing is written, the state only decays (W, U and L vanish, A = I)
+    w = make_inputs(cu_seqlens=[0, 129, 400], h_qk=2, h_v=4, seed=15, with_h0=True)
+    return dataclasses.replace(w, beta=torch.zeros_like(w.beta))
+
+
 CASES = {
     "tiny": lambda: workload("tiny_T512_h2x4"),
+    "no_gate": lambda: make_inputs(cu_seqlens=[0, 200, 777], h_qk=1, h_v=3, seed=16, with_h0=True, g_kind="zero"),
+    "strong_decay": _strong_decay,
+    "no_write": _no_write,
     "ragged_gqa3": lambda: make_inputs(cu_seqlens=[0, 1, 65, 200, 200, 391, 1000], h_qk=2, h_v=6, seed=7,
                                        with_h0=True),
     "uneven_heads": lambda: make_inputs(300, h_qk=2, h_v=3, seed=8, with_h0=True),
