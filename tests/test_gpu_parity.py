@@ -195,3 +195,23 @@ def test_null_plan_options_are_the_documented_defaults():
         for f in ("mode", "lambda_q8", "n_seg_total", "warmup_chunks", "sm_count", "workspace_bytes"):
             assert getattr(got, f) == getattr(want, f), (cu, f)
         assert abs(got.warmup_tol - 1e-4) < 1e-9 and got.sm_count == sms
+
+
+@functools.lru_cache(maxsize=None)
+def _many_short():
+    gen = np.random.default_rng(17)
+    lens = gen.integers(0, 131, size=2500)
+    lens[::97] = 0
+    w = make_inputs(cu_seqlens=[0] + np.cumsum(lens).tolist(), h_qk=1, h_v=2, seed=18, with_h0=True)
+    f = util.to64
+    return w, oracle.recurrence(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0), w.seq_offsets())
+
+
+@pytest.mark.parametrize("mode,lam", [("off", 1.0), ("exact", 0.5), ("auto", 0.0)])
+def test_many_short_sequences(mode, lam):
+    """2500 sequences of 0 to 130 tokens (every 97th empty): the chunk index's
+    prefix sum runs over several blocks of sequences, and most CTAs find their
+    sequence past the first warp-sized group."""
+    w, ref = _many_short()
+    o, hT, plan, _ = run(w, mode, lam)
+    check(o, hT, ref, f"many/{mode}/segments={plan.n_seg_total}")
