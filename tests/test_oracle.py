@@ -132,3 +132,105 @@ def test_warmup_error_within_gate_bound():
         H_warm = chunked.scan_head(q, k, v, g, beta, np.zeros((16, 16)), 0.25, chunk_range=(cb - w, cb))
         bound = np.exp(g[(cb - w) * 64: cb * 64].sum()) * np.linalg.norm(H_exact_early, 2)
         assert np.linalg.norm(H_exact - H_warm, 2) <= bound * (1 + 1e-9)
+
+
+# ---- the warmup restart branch of the chunked form (pages, section "AutoCP":
+#      a segment restarts from a zero state a few chunks before its start) ----
+#
+# Pinned against the token recurrence, which knows nothing of chunks or
+# segments: a warm segment [cb, ce) must equal the recurrence run from a zero
+# state over the tokens [(cb - w) * 64, ce * 64) (from h0 over [0, ce * 64)
+# when the window reaches the sequence start), read from chunk cb on.
+
+WARM_SEGS = [[(0, 3), (3, 7), (7, 10), (10, 15)]]
+WARM_T = 64 * 14 + 23  # 15 chunks, the last one partial
+WARM_DEPTHS = [
+    2,  # one depth for every segment: windows start at chunks 1, 5, 8 (none clipped)
+    {(0, 0, 1): 3, (0, 0, 2): 1, (0, 0, 3): 4,    # head 0: clipped exactly at chunk 0, then 6, 6
+     (0, 1, 1): 1, (0, 1, 2): 5, (0, 1, 3): 2},   # head 1: 2, 2, 8
+]
+
+
+def _depth(wc, n, j, s):
+    if s == 0:
+        return 0  # the first segment starts from h0 at the sequence start
+    return wc[(n, j, s)] if isinstance(wc, dict) else wc
+
+
+def _warm_case(seed, zero_before_windows=None):
+    # slow decay (g in [-0.01, 0]): a window's history stays far above rounding
+    c = P.rand_case([WARM_T], h_qk=1, h_v=2, d=16, seed=seed, g_scale=0.01)
+    if zero_before_windows is not None:
+        # alpha = 0 and beta = 0 at the last token before every window: the
+        # state entering the window is exactly zero, so nothing is dropped
+        for j, starts in zero_before_windows.items():
+            for st in starts:
+                t = st * 64 - 1
+                c["g"][t, j] = -800.0  # exp(-800) is 0 in float64
+                c["beta"][t, j] = 0.0
+    return c
+
+
+def _warm_violation(mod, c, wc):
+    """Largest |chunked warmup - recurrence on the restarted slice| over the
+    warm segments of both heads (o of every segment, the final state)."""
+    args = (c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"], c["cu"])
+    o, hT = mod.gdn_fwd_chunked(*args, segments=WARM_SEGS, warmup_chunks=wc)
+    worst = 0.0
+    for j in range(2):
+        for si, (cb, ce) in enumerate(WARM_SEGS[0]):
+            wd = _depth(wc, 0, j, si)
+            start = 0 if si == 0 or cb - wd <= 0 else cb - wd
+            a, b = start * 64, min(ce * 64, WARM_T)
+            h_init = np.zeros_like(c["h0"]) if start > 0 else c["h0"]
+            ro, rh = oracle.recurrence(c["q"][a:b], c["k"][a:b], c["v"][a:b], c["g"][a:b], c["beta"][a:b],
+                                       h_init, [0, b - a], heads=[j], n_threads=2)
+            worst = max(worst, np.abs(o[cb * 64:b, j] - ro[(cb - start) * 64:, j]).max())
+            if si == len(WARM_SEGS[0]) - 1:
+                worst = max(worst, np.abs(hT[0, j] - rh[0, j]).max())
+    return worst
+
+
+@pytest.mark.parametrize("wc", WARM_DEPTHS, ids=["int", "per-segment"])
+def test_warmup_branch_equals_restarted_recurrence(wc):
+    assert _warm_violation(chunked, _warm_case(31), wc) < 1e-11
+
+
+@pytest.mark.parametrize("wc", WARM_DEPTHS, ids=["int", "per-segment"])
+def test_warmup_is_exact_when_history_before_window_is_zero(wc):
+    """With the state wiped (alpha = beta = 0) at the token before every
+    window, the warmup result is the full recurrence itself."""
+    starts = {j: [cb - _depth(wc, 0, j, si) for si, (cb, _) in enumerate(WARM_SEGS[0])
+                  if si > 0 and cb - _depth(wc, 0, j, si) > 0] for j in range(2)}
+    c = _warm_case(32, starts)
+    args = (c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"], c["cu"])
+    o, hT = chunked.gdn_fwd_chunked(*args, segments=WARM_SEGS, warmup_chunks=wc)
+    ro, rh = oracle.recurrence(*args, n_threads=2)
+    assert np.abs(o - ro).max() < 1e-11 and np.abs(hT - rh).max() < 1e-11
+    # and without the wipe the same windows do drop history (the pin is not vacuous)
+    c2 = _warm_case(32)
+    o2, _ = chunked.gdn_fwd_chunked(c2["q"], c2["k"], c2["v"], c2["g"], c2["beta"], c2["h0"], c2["cu"],
+                                    segments=WARM_SEGS, warmup_chunks=wc)
+    ro2, _ = oracle.recurrence(c2["q"], c2["k"], c2["v"], c2["g"], c2["beta"], c2["h0"], c2["cu"], n_threads=2)
+    assert np.abs(o2 - ro2).max() > 1e-6
+
+
+# Off-by-one windows planted in a copy of the chunked form: each must break the pin.
+WARM_MUTANTS = {
+    "window_one_late": ("(cb - wd, cb))", "(cb - wd + 1, cb))"),
+    "window_one_early": ("(cb - wd, cb))", "(cb - wd - 1, cb))"),
+    "clip_strict": ("cb - wd <= 0", "cb - wd < 0"),
+    "depth_of_next_segment": ("warmup_chunks[(n, j, si)]", "warmup_chunks.get((n, j, si + 1), 1)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(WARM_MUTANTS))
+def test_planted_warmup_mistake_is_caught(name):
+    import types
+    src = open(chunked.__file__).read()
+    old, new = WARM_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mod = types.ModuleType(f"chunked_{name}")
+    exec(compile(src.replace(old, new), f"<{name}>", "exec"), mod.__dict__)
+    worst = max(_warm_violation(mod, _warm_case(31), wc) for wc in WARM_DEPTHS)
+    assert not worst < 1e-11, f"the warmup pin misses the planted mistake {name}"
