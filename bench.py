@@ -13,6 +13,15 @@ final state inside the timed region.  Under torchrun (N > 1) every rank runs
 an independent replica (the layer needs no collective) and the slowest
 rank's time is used.
 
+The line also carries, for every workload: its time and roofline fraction;
+the fp32 path's time on the headline workload; the host planning time; and,
+from the CPU-baseline leg (which runs the float64 oracle on the host cores
+anyway), the raw max|diff|/RMS of o and of the final state against the
+oracle and the excess over bf16's half-ulp store rounding.
+
+`--only NAME` times just one case (a workload name, `decode` or `f32`) and
+prints a short line: the entry point of the ncu captures under profiles/.
+
 `--impl reference` times the float64 CPU oracle on the host cores instead,
 one bounded sample of the same workload per step.
 """
@@ -66,19 +75,31 @@ def algorithmic(w):
 
 
 # Each kernel's share of the layer's algorithmic bytes (the inputs it reads
-# and outputs it writes that the layer must move anyway); the chunk records
-# the WY kernel writes and the scans read back, the context-parallel
+# and outputs it writes that the layer must move anyway): the WY kernel reads
+# q, k, v, g and beta, the output scans write o and the states.  The chunk
+# records the WY kernel writes and the scans read back, the context-parallel
 # transitions and the combine are overhead and count zero.
-KERNEL_SOURCE = {"wy": "gdn_wy.cu", "scan_out": "gdn_scan.cu", "scan_prep": "gdn_scan.cu",
-                 "combine": "gdn_combine.cu", "chunk_map": "gdn_wy.cu"}
+KERNEL_SOURCE = {"wy": "gdn_wy.cu", "scan_out": "gdn_scan.cu", "scan_out_warm": "gdn_scan.cu",
+                 "scan_out_exact": "gdn_scan.cu", "scan_prep": "gdn_scan.cu", "combine": "gdn_combine.cu",
+                 "modes": "gdn_combine.cu", "chunk_map": "gdn_wy.cu"}
 
 
-def kernel_bytes(name, w):
+def kernel_bytes(name, w, modes=None):
+    """name's share of the algorithmic bytes.  The output scan reads v and
+    writes o and the final state of the heads it runs: every head, or with
+    warmup heads split off (modes: per (sequence, head) 1 = exact, 2 =
+    warmup), those of its mode."""
     T, hqk, hv, n = w.T, w.h_qk, w.h_v, w.n_seqs
     if name == "wy":  # q, k (once per query/key head), v, g, beta
         return T * (2 * hqk * D * 2 + hv * D * 2 + 2 * hv * 4)
-    if name == "scan_out":  # o, the final state, and the initial state when given
-        return T * hv * D * 2 + n * hv * D * D * 4 * (2 if w.h0 is not None else 1)
+    per_head_state = D * D * 4 * (2 if w.h0 is not None else 1)
+    if name == "scan_out":  # o out, the final state, and the initial state when given
+        return T * hv * D * 2 + n * hv * per_head_state
+    if name in ("scan_out_warm", "scan_out_exact") and modes is not None:
+        want = 2 if name == "scan_out_warm" else 1
+        offs = w.seq_offsets()
+        return sum(((offs[s + 1] - offs[s]) * D * 2 + per_head_state)
+                   for s in range(n) for j in range(hv) if modes[s * hv + j] == want)
     return 0
 
 
@@ -195,11 +216,13 @@ def time_gpu(name, steps, warmup, device, cp="auto", lambda_=0.0, trace=True):
         s1.record(stream)
         s1.synchronize()
         per_step.append(s0.elapsed_time(s1))
-    # the per-kernel split: separate steps with an event after every kernel
+    # the per-kernel split: separate steps with a pair of events around every
+    # kernel, on the stream it runs on (with warmup heads, the output scan of
+    # those heads runs beside the exact heads' kernels, so the times overlap)
     per_kernel = [0.0] * n_k
     trace_steps = max(5, steps // 4) if trace else 0
     if trace:
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_k + 1)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_k)]
         for e in ev:
             e.record(stream)
         torch.cuda.synchronize(device)
@@ -207,9 +230,9 @@ def time_gpu(name, steps, warmup, device, cp="auto", lambda_=0.0, trace=True):
         for _ in range(trace_steps):
             flush.zero_()
             fwd()
-            ev[-1].synchronize()
+            torch.cuda.synchronize(device)
             for i in range(n_k):
-                per_kernel[i] += ev[i].elapsed_time(ev[i + 1])
+                per_kernel[i] += ev[2 * i].elapsed_time(ev[2 * i + 1])
         gdn_set_trace_events([])
     code2, detail2 = gdn_get_device_status(ws)
     modes, _ = gdn_cp_head_modes(ws, plan)
@@ -353,6 +376,82 @@ def time_e2e(name, steps, warmup, device, cp="auto"):
     return {"ms": ms, "h2d": h2d, "d2h": d2h, "tokens": w.T}
 
 
+def time_f32(name, steps, warmup, device):
+    """The fp32 path (q, k, v, o in fp32) on a workload, L2 flushed before each step."""
+    from gated_deltanet_linear_fwd_gb300 import gdn_chunk_fwd, gdn_cp_plan
+    from gated_deltanet_linear_fwd_gb300.inputs import workload
+    w = workload(name, dtype=torch.float32)
+    d = w.to(device)
+    plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, cu_seqlens=w.cu_seqlens, dtype=torch.float32)
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
+    out = torch.empty_like(d.v)
+    hT = torch.empty(w.n_seqs, w.h_v, D, D, dtype=torch.float32, device=device)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    fwd = lambda: gdn_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, plan=plan, out=out,
+                                final_state=hT, workspace=ws)
+    for _ in range(warmup):
+        flush.zero_()
+        fwd()
+    times = []
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(steps):
+        flush.zero_()
+        s0.record(stream)
+        fwd()
+        s1.record(stream)
+        s1.synchronize()
+        times.append(s0.elapsed_time(s1))
+    ms = statistics.mean(times)
+    return {"workload": name, "ms": ms, "tokens_per_s": w.T / (ms * 1e-3), "dtype": "f32 q/k/v/o",
+            "kernel": "recurrence_f32"}
+
+
+def planning_ms(name, repeats=20):
+    """Host time of gdn_cp_plan with automatic lambda: the first call for these
+    sequence lengths (the planner's search) and later calls (its cache)."""
+    from gated_deltanet_linear_fwd_gb300 import gdn_cp_plan
+    from gated_deltanet_linear_fwd_gb300.inputs import WORKLOADS
+    spec = WORKLOADS[name]
+    cu = spec.get("cu_seqlens")
+    T = cu[-1] if cu else spec["n_tokens"]
+    # an SM count no other call of this process plans for, so the first call searches
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count - 1
+    t0 = time.perf_counter()
+    gdn_cp_plan(T=T, h_qk=spec["h_qk"], h_v=spec["h_v"], cu_seqlens=cu, sm_count=sms)
+    first = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        gdn_cp_plan(T=T, h_qk=spec["h_qk"], h_v=spec["h_v"], cu_seqlens=cu, sm_count=sms)
+    return {"workload": name, "first_ms": first * 1e3, "cached_ms": (time.perf_counter() - t0) / repeats * 1e3}
+
+
+def gpu_outputs(name, device, cp="auto"):
+    """o and the final state of one forward on a workload, on the host."""
+    from gated_deltanet_linear_fwd_gb300 import gdn_chunk_fwd
+    from gated_deltanet_linear_fwd_gb300.inputs import workload
+    w = workload(name)
+    d = w.to(device)
+    o, hT = gdn_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, mode=cp)
+    torch.cuda.synchronize(device)
+    return o.cpu(), hT.cpu()
+
+
+def compare(o_gpu, hT_gpu, ref):
+    """max|diff| / RMS(ref) for o (raw, and beyond bf16's half-ulp store
+    rounding) and for the final state."""
+    import numpy as np
+    ro, rh = ref
+    g = o_gpu.double().numpy()
+    rms = float(np.sqrt(np.mean(ro ** 2)))
+    diff = np.abs(g - ro)
+    a = np.maximum(np.maximum(np.abs(ro), np.abs(g)), np.finfo(np.float32).tiny)
+    half_ulp = np.exp2(np.floor(np.log2(a)) - 8)
+    hs = hT_gpu.double().numpy()
+    return {"o_raw": float(diff.max()) / rms, "o_excess": float(np.maximum(diff - half_ulp, 0).max()) / rms,
+            "final_state": float(np.abs(hs - rh).max() / np.sqrt(np.mean(rh ** 2))), "bar": 2e-2}
+
+
 def cpu_baseline(name, budget_s=12.0):
     """The float64 oracle, as it stands, on this host's cores: a bounded sample
     (a prefix of the sequence, all heads) of the same workload."""
@@ -372,6 +471,22 @@ def cpu_baseline(name, budget_s=12.0):
         tokens *= 2
     return {"value": tokens / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"first {tokens} tokens of {name}, all {w.h_v} value heads, one pass ({dt:.2f} s)"}
+
+
+def oracle_accuracy(outputs):
+    """The oracle over each whole workload (float64, host cores), against the
+    GPU outputs taken from the same seeded inputs."""
+    import oracle
+    from gated_deltanet_linear_fwd_gb300.inputs import workload
+    res = {}
+    for name, (o, hT) in outputs.items():
+        w = workload(name)
+        f = lambda t: None if t is None else t.double().numpy()
+        t0 = time.perf_counter()
+        ref = oracle.recurrence(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0), w.seq_offsets())
+        res[name] = compare(o, hT, ref)
+        res[name]["oracle_s"] = time.perf_counter() - t0
+    return res
 
 
 def traffic_from_profile(tag, source):
@@ -426,6 +541,20 @@ def run_reference(args, world, rank):
     return 0
 
 
+def run_only(args, device, hbm):
+    """One case alone, few steps: the command the ncu captures run."""
+    if args.only == "decode":
+        r = time_decode(args.steps, args.warmup, device, hbm)
+    elif args.only == "f32":
+        r = time_f32(HEADLINE, args.steps, args.warmup, device)
+    else:
+        t = time_gpu(args.only, args.steps, args.warmup, device, args.cp, args.lambda_)
+        r = {"workload": args.only, "ms": t["ms"], "kernels_ms": t["kernel_ms"], "segments": t["plan"].n_seg_total,
+             "status": list(t["status"])}
+    print(json.dumps({"only": args.only, **r}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -437,6 +566,8 @@ def main(argv=None):
                     help="segment-length factor; 0 lets the planner choose")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default=None,
+                    help="time just this case (a workload name, 'decode' or 'f32') and print a short line")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()
@@ -446,6 +577,9 @@ def main(argv=None):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     hbm, tfl, peak_src = peaks()
+    if args.only:
+        return run_only(args, device, hbm)
+    plan_t = planning_ms(HEADLINE) if rank == 0 else None
     barrier(world)
     torch.cuda.synchronize(device)
     clocks = ClockSampler(device)
@@ -462,8 +596,8 @@ def main(argv=None):
     roof = None
     if kms:
         # the dominant kernel: its share of the algorithmic bytes over its average launch time
-        top = max((k for k in kms if kernel_bytes(k, r["w"]) > 0), key=lambda k: kms[k])
-        kb = kernel_bytes(top, r["w"])
+        top = max((k for k in kms if kernel_bytes(k, r["w"], r["modes"]) > 0), key=lambda k: kms[k])
+        kb = kernel_bytes(top, r["w"], r["modes"])
         achieved = kb / (kms[top] * 1e-3) / 1e9
         roof = {"bound": "hbm", "kernel": top, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": achieved / hbm, "traffic": traffic_from_profile(f"{top}_T32768_h2x8", KERNEL_SOURCE[top]),
@@ -507,8 +641,15 @@ def main(argv=None):
         line["sweep"] = sweep
     if not args.no_sweep and rank == 0:
         line["decode"] = time_decode(max(20, args.steps // 10), 5, device, hbm)
+        f32 = time_f32(HEADLINE, max(5, args.steps // 50), 3, device)
+        f32["vs_bf16_path"] = f32["ms"] / ms
+        line["f32"] = f32
+    if rank == 0:
+        line["planning"] = plan_t
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(HEADLINE)
+        names = [HEADLINE] + ([] if args.no_sweep else SWEEP)
+        line["accuracy"] = oracle_accuracy({n: gpu_outputs(n, device, args.cp) for n in names})
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -30,7 +30,8 @@ GDN_CP_WARMUP = 2
 GDN_CP_AUTO = 3
 
 EXPORTED = ["gdn_cp_plan", "gdn_chunk_fwd", "gdn_status_string", "gdn_last_cuda_error",
-            "gdn_get_device_status", "gdn_cp_head_modes", "gdn_set_trace_events", "gdn_trace_last", "gdn_chunk_fwd_static"]
+            "gdn_get_device_status", "gdn_cp_head_modes", "gdn_set_trace_events", "gdn_trace_last", "gdn_chunk_fwd_static",
+            "gdn_get_static_device_status", "gdn_decode_step", "gdn_debug_stall_ns"]
 
 
 class gdn_dims(ctypes.Structure):
@@ -90,12 +91,16 @@ def load(path: str = LIB_PATH):
         lib.gdn_chunk_fwd_static.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(gdn_dims),
                                              ctypes.POINTER(gdn_cp_plan_t), vp]
         lib.gdn_chunk_fwd_static.restype = ctypes.c_int
+        lib.gdn_get_static_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
+        lib.gdn_get_static_device_status.restype = ctypes.c_int
         lib.gdn_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(gdn_dims), vp]
         lib.gdn_decode_step.restype = ctypes.c_int
         lib.gdn_set_trace_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
         lib.gdn_set_trace_events.restype = ctypes.c_int
         lib.gdn_trace_last.argtypes = [ctypes.POINTER(ctypes.c_char_p), ctypes.c_int]
         lib.gdn_trace_last.restype = ctypes.c_int
+        lib.gdn_debug_stall_ns.argtypes = [ctypes.c_uint32]
+        lib.gdn_debug_stall_ns.restype = ctypes.c_int
         _lib = lib
         return lib
 

@@ -140,6 +140,41 @@ def gdn_get_device_status(workspace: torch.Tensor, stream=None):
     return code.value, detail.value
 
 
+_DETAILS = {1: "a bulk copy's wait", 2: "an MMA's wait", 3: "the chunk index or segments disagree with the plan",
+            4: "segments combined out of order", 5: "a value outside the fp16 range of the MMA operands",
+            6: "the test hook's stall"}
+
+
+def describe_device_status(code: int, detail: int) -> str:
+    """Text for a (code, detail) pair read from the status word: code is a
+    gdn_status (0, 5 timeout or 7 check); detail says which check or wait
+    tripped (100 + b: a bounded wait on mbarrier b of the kernel)."""
+    if code == L.GDN_OK:
+        return "ok"
+    what = {L.GDN_ERR_DEVICE_TIMEOUT: "timeout", L.GDN_ERR_DEVICE_CHECK: "check failed"}.get(code, f"code {code}")
+    if detail >= 100:
+        where = f"the bounded wait on barrier {detail - 100}"
+    else:
+        where = _DETAILS.get(detail, f"detail {detail}")
+    return f"{what}: {where}"
+
+
+def gdn_debug_stall_ns(ns: int) -> None:
+    """Test hook (gdn_debug_stall_ns): while ns > 0 every later forward's
+    chunk-local kernel waits ns nanoseconds on a barrier nothing arrives on,
+    so the call takes its timeout path; 0 turns it off."""
+    L.check(L.load().gdn_debug_stall_ns(int(ns)), "gdn_debug_stall_ns")
+
+
+def gdn_get_static_device_status(stream=None):
+    """(code, detail) of the status word of the last gdn_chunk_fwd_static call
+    on the current device (synchronises)."""
+    code, detail = ctypes.c_int(), ctypes.c_int()
+    L.check(L.load().gdn_get_static_device_status(_stream_handle(stream), ctypes.byref(code), ctypes.byref(detail)),
+            "gdn_get_static_device_status")
+    return code.value, detail.value
+
+
 def gdn_cp_head_modes(workspace: torch.Tensor, plan: Plan, stream=None):
     """Per (sequence, head): the mode taken (1 exact, 2 warmup, 0 off) and log warmup bound."""
     n = plan.raw.n_seqs * plan.raw.h_v

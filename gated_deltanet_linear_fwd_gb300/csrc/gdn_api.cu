@@ -1,7 +1,8 @@
 // Host side of the C ABI declared in include/gdn.h: planning, argument
 // checks, TMA tensor maps, and the launch sequence of the forward.
-#include <cmath>
 #include <algorithm>
+#include <atomic>
+#include <cmath>
 #include <climits>
 #include <cstring>
 #include <mutex>
@@ -15,25 +16,29 @@ using namespace gdn;
 namespace {
 
 thread_local int g_last_cuda_error = 0;
+std::atomic<uint32_t> g_debug_stall_ns{0};  // test hook of the timeout path (gdn_debug_stall_ns)
 
 // ---- tracing: caller-provided events recorded around each launch ----
+// Kernel i of a call is bracketed by events 2i and 2i + 1, recorded on the
+// stream it is launched on.
 constexpr int kMaxTrace = 16;
 thread_local cudaEvent_t g_trace_ev[kMaxTrace];
 thread_local int g_trace_n = 0;
-thread_local const char* g_last_names[kMaxTrace];
+thread_local const char* g_last_names[kMaxTrace / 2];
 thread_local int g_last_count = 0;
 
 struct LaunchLog {
-  cudaStream_t st;
-  int count = 0;
-  cudaError_t begin() {
-    g_last_count = 0;
-    return g_trace_n > 0 ? cudaEventRecord(g_trace_ev[0], st) : cudaSuccess;
+  LaunchLog() { g_last_count = 0; }
+  // Records the start event of the next kernel on st.
+  cudaError_t before(cudaStream_t st) {
+    const int k = 2 * g_last_count;
+    return k < g_trace_n ? cudaEventRecord(g_trace_ev[k], st) : cudaSuccess;
   }
-  cudaError_t after(const char* name) {
-    if (g_last_count < kMaxTrace) g_last_names[g_last_count++] = name;
-    ++count;
-    return count < g_trace_n ? cudaEventRecord(g_trace_ev[count], st) : cudaSuccess;
+  // Names the kernel just launched on st and records its end event.
+  cudaError_t after(const char* name, cudaStream_t st) {
+    const int k = 2 * g_last_count + 1;
+    if (g_last_count < kMaxTrace / 2) g_last_names[g_last_count++] = name;
+    return k < g_trace_n ? cudaEventRecord(g_trace_ev[k], st) : cudaSuccess;
   }
 };
 
@@ -51,7 +56,6 @@ constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
 bool g_setup_done[kMaxDevices] = {};
 int g_sm_count[kMaxDevices] = {};
-
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -75,6 +79,7 @@ gdn_status device_setup(int* dev_out) {
   if ((e = scan_kernel_setup()) != cudaSuccess) return cuda_fail(e);
   if ((e = wy_kernel_setup()) != cudaSuccess) return cuda_fail(e);
   if ((e = combine_kernel_setup()) != cudaSuccess) return cuda_fail(e);
+  if ((e = f32_kernel_setup()) != cudaSuccess) return cuda_fail(e);
   int sms = 0;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return cuda_fail(e);
   g_sm_count[dev] = sms;
@@ -237,7 +242,8 @@ gdn_status encode_out_map(CUtensorMap* m, void* base, int heads, int64_t tokens)
 
 // ---- fixed device workspace for callers that cannot allocate ----
 // 8 MiB: small problems only (the chunk records take 41472 bytes per
-// (chunk, value head) and 32768 per (chunk, query/key head)).
+// (chunk, value head); context parallelism adds three 64 KB states per
+// (segment, value head)).
 constexpr size_t kStaticWorkspaceBytes = size_t(8) << 20;
 static __device__ __align__(256) uint8_t g_static_workspace[kStaticWorkspaceBytes];
 void* g_static_ws_dev[kMaxDevices] = {};
@@ -446,6 +452,7 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
     p.chunk_exp = reinterpret_cast<float*>(ws + align_up(info_off + (size_t)plan->n_chunks_total * 16, 256));
     p.wy = ws + plan->off_wy;
   }
+  p.stall_ns = g_debug_stall_ns.load(std::memory_order_relaxed);
 
   cudaError_t e = cudaMemsetAsync(ws, 0, 256, cs);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -459,11 +466,23 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
     }
     return GDN_OK;
   }
-  if (dims->dtype == GDN_F32) {  // fp32 inputs: the recurrence on the CUDA cores, in fp32
-    LaunchLog log{cs};
-    if ((e = log.begin()) != cudaSuccess) return cuda_fail(e);
-    if ((e = launch_recurrence_f32(p, cs)) != cudaSuccess) return cuda_fail(e);
-    if ((e = log.after("recurrence_f32")) != cudaSuccess) return cuda_fail(e);
+  if (dims->dtype == GDN_F32) {
+    // fp32 inputs: the recurrence on the CUDA cores, in fp32; a context-parallel
+    // plan always combines its segments exactly (no warmup restarts)
+    LaunchLog log;
+    if (plan->mode != GDN_CP_OFF) {
+      p.plan_mode = kModeExact;
+      if ((e = log.before(cs)) != cudaSuccess || (e = launch_f32_prep(p, cs)) != cudaSuccess ||
+          (e = log.after("recurrence_f32_prep", cs)) != cudaSuccess)
+        return cuda_fail(e);
+      if ((e = log.before(cs)) != cudaSuccess || (e = launch_combine(p, g_sm_count[dev], cs)) != cudaSuccess ||
+          (e = log.after("combine", cs)) != cudaSuccess)
+        return cuda_fail(e);
+    }
+    if ((e = log.before(cs)) != cudaSuccess ||
+        (e = launch_recurrence_f32(p, cs, plan->mode != GDN_CP_OFF)) != cudaSuccess ||
+        (e = log.after("recurrence_f32", cs)) != cudaSuccess)
+      return cuda_fail(e);
     return GDN_OK;
   }
   CUtensorMap mq, mk, mv, mo;
@@ -473,22 +492,28 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
   if ((st = encode_map(&mv, v, dims->h_v, T_total, f32)) != GDN_OK) return st;
   if ((st = encode_out_map(&mo, out, dims->h_v, T_total)) != GDN_OK) return st;
 
-  LaunchLog log{cs};
-  if ((e = log.begin()) != cudaSuccess) return cuda_fail(e);
+  // chunk index (varlen) -> WY -> [context parallel: preprocessing -> combine]
+  // -> output scan
+  LaunchLog log;
   if (cu_dev) {  // varlen chunk index (fixed-length rows compute it)
-    if ((e = launch_chunk_map(p, cs)) != cudaSuccess) return cuda_fail(e);
-    if ((e = log.after("chunk_map")) != cudaSuccess) return cuda_fail(e);
+    if ((e = log.before(cs)) != cudaSuccess || (e = launch_chunk_map(p, cs)) != cudaSuccess ||
+        (e = log.after("chunk_map", cs)) != cudaSuccess)
+      return cuda_fail(e);
   }
-  if ((e = launch_wy(p, mq, mk, mv, cs, cu_dev != nullptr)) != cudaSuccess) return cuda_fail(e);
-  if ((e = log.after("wy")) != cudaSuccess) return cuda_fail(e);
+  if ((e = log.before(cs)) != cudaSuccess || (e = launch_wy(p, mq, mk, mv, cs, cu_dev != nullptr)) != cudaSuccess ||
+      (e = log.after("wy", cs)) != cudaSuccess)
+    return cuda_fail(e);
   if (plan->mode != GDN_CP_OFF) {
-    if ((e = launch_scan_prep(p, mq, mk, cs)) != cudaSuccess) return cuda_fail(e);
-    if ((e = log.after("scan_prep")) != cudaSuccess) return cuda_fail(e);
-    if ((e = launch_combine(p, g_sm_count[dev], cs)) != cudaSuccess) return cuda_fail(e);
-    if ((e = log.after("combine")) != cudaSuccess) return cuda_fail(e);
+    if ((e = log.before(cs)) != cudaSuccess || (e = launch_scan_prep(p, mq, mk, cs)) != cudaSuccess ||
+        (e = log.after("scan_prep", cs)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = log.before(cs)) != cudaSuccess || (e = launch_combine(p, g_sm_count[dev], cs)) != cudaSuccess ||
+        (e = log.after("combine", cs)) != cudaSuccess)
+      return cuda_fail(e);
   }
-  if ((e = launch_scan_out(p, mq, mk, mo, plan->n_seg_total, cs)) != cudaSuccess) return cuda_fail(e);
-  if ((e = log.after("scan_out")) != cudaSuccess) return cuda_fail(e);
+  if ((e = log.before(cs)) != cudaSuccess || (e = launch_scan_out(p, mq, mk, mo, plan->n_seg_total, cs)) != cudaSuccess ||
+      (e = log.after("scan_out", cs)) != cudaSuccess)
+    return cuda_fail(e);
   return GDN_OK;
 }
 
@@ -515,11 +540,16 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const fl
   a.h_v = dims->h_v;
   a.scale = dims->scale != 0.f ? dims->scale : 1.0f / std::sqrt((float)dims->d_k);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  LaunchLog log{cs};
-  cudaError_t e = log.begin();
+  LaunchLog log;
+  cudaError_t e = log.before(cs);
   if (e == cudaSuccess) e = launch_decode(a, dims->dtype == GDN_F32, cs);
-  if (e == cudaSuccess) e = log.after("decode");
+  if (e == cudaSuccess) e = log.after("decode", cs);
   return e == cudaSuccess ? GDN_OK : cuda_fail(e);
+}
+
+gdn_status gdn_debug_stall_ns(uint32_t ns) {
+  g_debug_stall_ns.store(ns, std::memory_order_relaxed);
+  return GDN_OK;
 }
 
 gdn_status gdn_set_trace_events(void* const* events, int n_events) {
@@ -555,9 +585,9 @@ gdn_status gdn_cp_head_modes(const void* workspace, const gdn_cp_plan_t* plan, i
                              void* stream) {
   if (!workspace || !plan) return GDN_ERR_INVALID_ARG;
   const size_t heads = (size_t)plan->n_seqs * plan->h_v;
-  if (plan->mode == GDN_CP_OFF || plan->dtype == GDN_F32) {  // no per-head modes taken
+  if (plan->mode == GDN_CP_OFF || plan->dtype == GDN_F32) {  // no warmup decision taken
     for (size_t i = 0; i < heads; ++i) {
-      if (modes) modes[i] = GDN_CP_OFF;
+      if (modes) modes[i] = plan->mode == GDN_CP_OFF ? GDN_CP_OFF : GDN_CP_EXACT;
       if (bounds) bounds[i] = -INFINITY;
     }
     return GDN_OK;
@@ -586,4 +616,12 @@ extern "C" gdn_status gdn_chunk_fwd_static(const void* q, const void* k, const v
   if (st != GDN_OK) return st;
   return gdn_chunk_fwd(q, k, v, g, beta, initial_state, cu_seqlens_dev, out, final_state, dims, plan, ws,
                        kStaticWorkspaceBytes, stream);
+}
+
+extern "C" gdn_status gdn_get_static_device_status(void* stream, int* code, int* detail) {
+  if (!code) return GDN_ERR_INVALID_ARG;
+  void* ws = nullptr;
+  gdn_status st = static_workspace(&ws);
+  if (st != GDN_OK) return st;
+  return gdn_get_device_status(ws, stream, code, detail);
 }

@@ -11,8 +11,9 @@
 // copies, one segment ahead) while it does the fp32 products.  Each warp takes a
 // 16-row slice of R for all the CTA's rows (so R is read from shared memory once
 // per segment), and the 8 partial sums are added in a second pass.  Four rows
-// per CTA halve each segment's step when few (sequence, head) pairs exist.  The CTA of row block 0 also
-// records the mode the (sequence, head) takes and its warmup bound.
+// per CTA halve each segment's step when few (sequence, head) pairs exist.
+// The CTA of row block 0 also records the mode the (sequence, head) takes and
+// its warmup bound.
 #include "gdn_dev.cuh"
 
 namespace gdn {
@@ -38,7 +39,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
   grid_launch_dependents();
   const int tid = threadIdx.x, warp = tid >> 5;
   const int n = blockIdx.x, j = blockIdx.y, r0 = blockIdx.z * kRows;
-  __shared__ int s_mode;
+  __shared__ int s_mode, s_skip;
+  if (tid == 0) s_skip = earlier_failure(p.status);
+  __syncthreads();
+  if (s_skip) return;  // an earlier kernel failed: its results are incomplete
   if (warp == 0) {
     SegInfo si;
     locate_sequence(p, n, si);

@@ -4,92 +4,261 @@
 // delta rule itself in fp32 on the CUDA cores:
 //   S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
 //   o_t = scale S_t q_t.
-// Chunking and context parallelism are exact re-associations of this same
-// recurrence (FlashQLA pages, sections "Optimising GDN chunked prefill" and
-// "AutoCP"); here the parallelism comes instead from the d_v rows of the
-// state, which evolve independently given k, g and beta.  One CTA owns 16 rows
-// of one (sequence, value head): 16 threads per row, 8 columns each.
-#include "gdn_internal.cuh"
+// Each row s of S (one d_v index) evolves on its own given k, g and beta:
+//   s <- a s + c k,   a = exp(g_t),  c = beta_t (v_t[row] - a (s . k)),
+// so two neighbouring threads of a warp hold one row (64 fp32 registers each,
+// their dot products joined by one shuffle) and a CTA of 256 threads holds a
+// whole state.
+//
+// Context parallelism (FlashQLA pages, section "AutoCP": segments whose start
+// states are combined exactly through the correction term M) supplies the
+// parallelism the token loop lacks: over a segment the map s_start -> s_end
+// is affine, s_end = s_start R + s_loc, so
+//   transition  (role 0): rows of the identity run with no value input -> R
+//   local       (role 1): rows from zero with the value input          -> S_loc
+// run for every segment but each sequence's last at once, the fp32 combine
+// kernel chains the segments' start states, and
+//   output      (role 2): each segment from its start state (h0 for the
+//                         first) writes o, and the last segment the final
+//                         state.
+// Without context parallelism only the output role runs, one CTA per
+// (sequence, value head).
+//
+// Tokens are staged through shared memory in blocks of 16 (k, q, v rows by
+// cp.async, the gates by plain loads), double buffered, so each thread reads
+// k and q as broadcasts.
+#include "gdn_dev.cuh"
 
 namespace gdn {
 namespace {
 
-constexpr int kRowsPerCta = 16;
+constexpr int kF32Threads = 256;
+constexpr int kHalf = kDim / 2;  // columns per thread
+constexpr int kTokBlock = 16;
+constexpr int kBufFloats = 3 * kTokBlock * kDim + 2 * kTokBlock;  // k, q, v rows, then exp(g), beta
+constexpr int kF32Smem = 2 * kBufFloats * 4;
 
-__global__ void __launch_bounds__(256) recurrence_f32_kernel(const Problem p) {
-  const int tid = threadIdx.x;
-  const int rr = tid >> 4;         // row within the CTA
-  const int cg = tid & 15;         // column group: columns 8 cg .. 8 cg + 7
-  const int n = blockIdx.x, j = blockIdx.y;
-  const int dv = blockIdx.z * kRowsPerCta + rr;
-  const int iq = (int)(((int64_t)j * p.h_qk) / p.h_v);
-  int64_t bos, eos;
-  if (p.cu) {
-    bos = p.cu[n];
-    eos = p.cu[n + 1];
-  } else {
-    bos = (int64_t)n * p.T_row;
-    eos = bos + p.T_row;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// A shared-memory float4 read the compiler may not merge with an earlier read
+// of the same address: the update pass reads k again rather than keep all of
+// it in registers across the dot product.
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+
+// OUT: the output role; else blockIdx.z = 0 runs the transition and 1 the
+// local state.
+template <bool OUT>
+__global__ void __launch_bounds__(kF32Threads, 2) recurrence_f32_kernel(const Problem p) {
+  extern __shared__ float4 f32_smem4[];
+  float* smem = reinterpret_cast<float*>(f32_smem4);
+  __shared__ SegInfo s_seg;
+  __shared__ int s_skip;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = tid >> 1, half = tid & 1, c0 = half * kHalf;  // this thread: row, columns c0 .. c0 + 63
+  const int j = blockIdx.y;
+  const bool transition = !OUT && blockIdx.z == 0;  // rows of the identity, no value input
+  const bool with_v = !transition;
+  grid_dependency_wait();  // start states (output role): written by the combine before
+  grid_launch_dependents();
+  if (warp == 0) {
+    SegInfo si;
+    const bool ok = locate_segment(p, blockIdx.x, si);
+    if (lane == 0) {
+      if (!ok) si.n = -1;
+      s_seg = si;
+      s_skip = earlier_failure(p.status);
+    }
   }
+  __syncthreads();
+  if (s_skip) return;
+  const SegInfo si = s_seg;
+  if (si.n < 0) {
+    if (tid == 0) report(p.status, kDevCheck, kDetSegMismatch);
+    return;
+  }
+  if (!OUT) {
+    if (si.s == si.n_seg - 1) return;                    // the last segment's map is not needed
+    if (transition && si.s == 0 && p.h0 == nullptr) return;  // nor R_0 for a zero start
+  }
+  const int iq = (int)(((int64_t)j * p.h_qk) / p.h_v);
+  const int64_t t_begin = si.bos + (int64_t)si.cb * kChunk;
+  const int64_t t_end = min(si.bos + (int64_t)si.ce * kChunk, si.eos);
+  const size_t mat = (size_t)kDim * kDim;
+  const size_t seg_off = ((size_t)(si.seg_base + si.s) * p.h_v + j) * mat;
+
+  float s[kHalf];
+  if (!OUT) {
+#pragma unroll
+    for (int i = 0; i < kHalf; ++i) s[i] = (transition && c0 + i == row) ? 1.f : 0.f;
+  } else if (si.s > 0) {  // the combined start state, rows = d_v
+    const float4* src = reinterpret_cast<const float4*>(p.Sstart + seg_off + (size_t)row * kDim + c0);
+#pragma unroll
+    for (int i = 0; i < kHalf / 4; ++i) {
+      const float4 v4 = src[i];
+      s[4 * i] = v4.x;
+      s[4 * i + 1] = v4.y;
+      s[4 * i + 2] = v4.z;
+      s[4 * i + 3] = v4.w;
+    }
+  } else if (p.h0) {  // H = S^T: S[row][i] = h0[i][row]
+    const float* h0 = p.h0 + (size_t)(si.n * p.h_v + j) * mat;
+#pragma unroll
+    for (int i = 0; i < kHalf; ++i) s[i] = h0[(size_t)(c0 + i) * kDim + row];
+  } else {
+#pragma unroll
+    for (int i = 0; i < kHalf; ++i) s[i] = 0.f;
+  }
+
   const float* q = reinterpret_cast<const float*>(p.q);
   const float* k = reinterpret_cast<const float*>(p.k);
   const float* v = reinterpret_cast<const float*>(p.v);
   float* o = reinterpret_cast<float*>(p.out);
-  const size_t head_off = (size_t)(n * p.h_v + j) * kDim * kDim;
-
-  float S[8];
+  const int n_blocks = (int)((t_end - t_begin + kTokBlock - 1) / kTokBlock);
+  const uint32_t sm0 = smem_u32(smem);
+  // Block b's rows into buffer b & 1: 16 tokens x 512 bytes for each of k,
+  // (q, v where used); thread tid copies 16-byte piece tid % 32 of token
+  // 8 r + tid / 32, r = 0..1.  Tokens past the range are filled with zeros.
+  auto stage = [&](int b) {
+    const uint32_t buf = sm0 + (uint32_t)((b & 1) * kBufFloats) * 4u;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) S[e] = p.h0 ? p.h0[head_off + (size_t)(8 * cg + e) * kDim + dv] : 0.f;
-
-  auto load = [&](int64_t t, float4& k0, float4& k1, float4& q0, float4& q1, float& vv, float& a, float& b) {
-    const float4* kr = reinterpret_cast<const float4*>(k + ((size_t)t * p.h_qk + iq) * kDim + 8 * cg);
-    const float4* qr = reinterpret_cast<const float4*>(q + ((size_t)t * p.h_qk + iq) * kDim + 8 * cg);
-    k0 = kr[0];
-    k1 = kr[1];
-    q0 = qr[0];
-    q1 = qr[1];
-    vv = v[((size_t)t * p.h_v + j) * kDim + dv];
-    a = p.g[(size_t)t * p.h_v + j];
-    b = p.beta[(size_t)t * p.h_v + j];
-  };
-  float4 k0, k1, q0, q1;
-  float vv = 0.f, gg = 0.f, bb = 0.f;
-  if (bos < eos) load(bos, k0, k1, q0, q1, vv, gg, bb);
-  for (int64_t t = bos; t < eos; ++t) {
-    const float kc[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-    const float qc[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-    const float vt = vv, alpha = expf(gg), beta = bb;
-    if (t + 1 < eos) load(t + 1, k0, k1, q0, q1, vv, gg, bb);  // next token in flight
-    // S_{t-1} k_t, reduced over the 16 column groups of this row
-    float sk = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) sk = fmaf(S[e], kc[e], sk);
-#pragma unroll
-    for (int d = 8; d >= 1; d >>= 1) sk += __shfl_xor_sync(0xffffffffu, sk, d);
-    // S_t = alpha (S_{t-1} - beta (S_{t-1} k) k^T) + beta v k^T
-    const float bsk = beta * sk, bv = beta * vt;
-    float so = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      S[e] = fmaf(alpha, fmaf(-bsk, kc[e], S[e]), bv * kc[e]);
-      so = fmaf(S[e], qc[e], so);
+    for (int r = 0; r < kTokBlock / 8; ++r) {
+      const int tt = 8 * r + warp, piece = lane * 4;
+      const int64_t t = t_begin + (int64_t)b * kTokBlock + tt;
+      const bool valid = t < t_end;
+      const int64_t tc = valid ? t : t_begin;  // a valid address even for the zero fill
+      const uint32_t off = (uint32_t)(tt * kDim + piece) * 4u;
+      cp_async16(buf + off, k + ((size_t)tc * p.h_qk + iq) * kDim + piece, valid);
+      if (OUT)
+        cp_async16(buf + (uint32_t)(kTokBlock * kDim) * 4u + off, q + ((size_t)tc * p.h_qk + iq) * kDim + piece, valid);
+      if (with_v)
+        cp_async16(buf + (uint32_t)(2 * kTokBlock * kDim) * 4u + off, v + ((size_t)tc * p.h_v + j) * kDim + piece, valid);
     }
-#pragma unroll
-    for (int d = 8; d >= 1; d >>= 1) so += __shfl_xor_sync(0xffffffffu, so, d);
-    if (cg == 0) o[((size_t)t * p.h_v + j) * kDim + dv] = p.scale * so;
+    cp_async_commit();
+  };
+  // The gates of block b (threads 0..15, one token each) into registers.
+  auto gates = [&](int b, float& a, float& be) {
+    const int64_t t = t_begin + (int64_t)b * kTokBlock + tid;
+    a = 0.f;
+    be = 0.f;
+    if (tid < kTokBlock && t < t_end) {
+      a = expf(p.g[(size_t)t * p.h_v + j]);
+      be = p.beta[(size_t)t * p.h_v + j];
+    }
+  };
+  auto put_gates = [&](int b, float a, float be) {
+    if (tid < kTokBlock) {
+      smem[(b & 1) * kBufFloats + 3 * kTokBlock * kDim + tid] = a;
+      smem[(b & 1) * kBufFloats + 3 * kTokBlock * kDim + kTokBlock + tid] = be;
+    }
+  };
+  if (n_blocks > 0) {
+    float a0, b0;
+    stage(0);
+    gates(0, a0, b0);
+    put_gates(0, a0, b0);
   }
-  if (p.hT) {
+  for (int b = 0; b < n_blocks; ++b) {
+    float a1 = 0.f, b1 = 0.f;
+    if (b + 1 < n_blocks) {  // buffer (b + 1) & 1 was last read in block b - 1
+      stage(b + 1);
+      gates(b + 1, a1, b1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();  // block b's rows and gates are in buffer b & 1
+    const float* buf = smem + (b & 1) * kBufFloats;
+    const int nt = (int)min((int64_t)kTokBlock, t_end - t_begin - (int64_t)b * kTokBlock);
+    for (int tt = 0; tt < nt; ++tt) {
+      const float4* kr = reinterpret_cast<const float4*>(buf + tt * kDim + c0);
+      const float a = buf[3 * kTokBlock * kDim + tt], be = buf[3 * kTokBlock * kDim + kTokBlock + tt];
+      // s . k over four partial sums
+      float sk[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int e = 0; e < 8; ++e) p.hT[head_off + (size_t)(8 * cg + e) * kDim + dv] = S[e];
+      for (int i = 0; i < kHalf / 4; ++i) {
+        const float4 k4 = kr[i];
+        sk[i & 3] = fmaf(s[4 * i], k4.x, sk[i & 3]);
+        sk[i & 3] = fmaf(s[4 * i + 1], k4.y, sk[i & 3]);
+        sk[i & 3] = fmaf(s[4 * i + 2], k4.z, sk[i & 3]);
+        sk[i & 3] = fmaf(s[4 * i + 3], k4.w, sk[i & 3]);
+      }
+      float skv = (sk[0] + sk[1]) + (sk[2] + sk[3]);
+      skv += __shfl_xor_sync(0xffffffffu, skv, 1);  // the row's other half
+      const float vr = with_v ? buf[2 * kTokBlock * kDim + tt * kDim + row] : 0.f;
+      const float c = be * (vr - a * skv);
+      const uint32_t kaddr = smem_u32(kr);
+#pragma unroll
+      for (int i = 0; i < kHalf / 4; ++i) {
+        const float4 k4 = lds_f4(kaddr + 16u * i);
+        s[4 * i] = fmaf(c, k4.x, a * s[4 * i]);
+        s[4 * i + 1] = fmaf(c, k4.y, a * s[4 * i + 1]);
+        s[4 * i + 2] = fmaf(c, k4.z, a * s[4 * i + 2]);
+        s[4 * i + 3] = fmaf(c, k4.w, a * s[4 * i + 3]);
+      }
+      if (OUT) {
+        const float4* qr = reinterpret_cast<const float4*>(buf + kTokBlock * kDim + tt * kDim + c0);
+        float so[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < kHalf / 4; ++i) {
+          const float4 q4 = qr[i];
+          so[i & 3] = fmaf(s[4 * i], q4.x, so[i & 3]);
+          so[i & 3] = fmaf(s[4 * i + 1], q4.y, so[i & 3]);
+          so[i & 3] = fmaf(s[4 * i + 2], q4.z, so[i & 3]);
+          so[i & 3] = fmaf(s[4 * i + 3], q4.w, so[i & 3]);
+        }
+        float sov = (so[0] + so[1]) + (so[2] + so[3]);
+        sov += __shfl_xor_sync(0xffffffffu, sov, 1);
+        const int64_t t = t_begin + (int64_t)b * kTokBlock + tt;
+        if (half == 0) o[((size_t)t * p.h_v + j) * kDim + row] = p.scale * sov;
+      }
+    }
+    put_gates(b + 1, a1, b1);  // buffer (b + 1) & 1's gates: read from the next block on
+    __syncthreads();           // buffer b & 1 is read before block b + 2 is staged into it
+  }
+  if (OUT) {
+    if (p.hT && si.s == si.n_seg - 1) {  // H = S^T
+      float* hT = p.hT + (size_t)(si.n * p.h_v + j) * mat;
+#pragma unroll
+      for (int i = 0; i < kHalf; ++i) hT[(size_t)(c0 + i) * kDim + row] = s[i];
+    }
+  } else {
+    float4* dst = reinterpret_cast<float4*>((transition ? p.R : p.Sloc) + seg_off + (size_t)row * kDim + c0);
+#pragma unroll
+    for (int i = 0; i < kHalf / 4; ++i) dst[i] = make_float4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_recurrence_f32(const Problem& p, cudaStream_t st) {
-  dim3 grid(p.n_seqs, p.h_v, kDim / kRowsPerCta);
-  recurrence_f32_kernel<<<grid, 256, 0, st>>>(p);
-  return cudaGetLastError();
+cudaError_t f32_kernel_setup() {
+  cudaError_t e = cudaFuncSetAttribute(recurrence_f32_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kF32Smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(recurrence_f32_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kF32Smem);
+}
+
+// The segments' transitions and local states (context-parallel plans only).
+cudaError_t launch_f32_prep(const Problem& p, cudaStream_t st) {
+  return launch_kernel(recurrence_f32_kernel<false>, dim3(p.n_seg_total, p.h_v, 2), dim3(kF32Threads), kF32Smem, st,
+                       true, p);
+}
+
+// The output pass: every segment from its start state.
+cudaError_t launch_recurrence_f32(const Problem& p, cudaStream_t st, bool dependent) {
+  return launch_kernel(recurrence_f32_kernel<true>, dim3(p.n_seg_total, p.h_v), dim3(kF32Threads), kF32Smem, st,
+                       dependent, p);
 }
 
 }  // namespace gdn

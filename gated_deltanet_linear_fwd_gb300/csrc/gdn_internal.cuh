@@ -19,6 +19,7 @@ constexpr int kDetMmaWait = 2;
 constexpr int kDetSegMismatch = 3;
 constexpr int kDetCombineOrder = 4;
 constexpr int kDetFp16Range = 5;  // a value outside the fp16 MMA operand range
+constexpr int kDetStallTest = 6;  // the test hook's wait ran out (Problem::stall_ns)
 
 // Head mode words (workspace head-mode section).
 constexpr int kModeOff = 0;
@@ -74,6 +75,10 @@ struct Problem {
   float* chunk_exp;         // [n_chunks_total, h_v] warmup exponent of each chunk:
                             // sum over its tokens of g + log max(1, |1 - beta ||k||^2|)
   uint8_t* wy;              // [n_chunks_total, h_v] records of kRecBytes
+  // Test hook (0 in normal use): the WY kernel's CTAs first wait this many
+  // nanoseconds on an mbarrier nothing arrives on, so the bounded wait runs
+  // out and the call takes its timeout path.
+  uint32_t stall_ns;
 };
 
 // Arguments of the one-token step (gdn_decode_step).
@@ -91,6 +96,14 @@ struct DecodeArgs {
 
 __device__ __forceinline__ void report(int* status, int code, int detail) {
   if (atomicCAS(status, 0, code) == 0) atomicExch(status + 1, detail);
+}
+
+// The status word as the kernels before this one left it.  Each kernel of
+// the forward after the chunk-local one reads it once (one thread, after
+// grid_dependency_wait) and, if an earlier kernel reported a failure, does no
+// work: its inputs would be incomplete.
+__device__ __forceinline__ int earlier_failure(const int* status) {
+  return *reinterpret_cast<const volatile int*>(status);
 }
 
 struct SegInfo {
@@ -268,7 +281,9 @@ cudaError_t launch_scan_prep(const Problem& p, const CUtensorMap& mq, const CUte
 cudaError_t launch_combine(const Problem& p, int sm_count, cudaStream_t st);
 cudaError_t launch_scan_out(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mo,
                             int grid_x, cudaStream_t st);
-cudaError_t launch_recurrence_f32(const Problem& p, cudaStream_t st);
+cudaError_t launch_recurrence_f32(const Problem& p, cudaStream_t st, bool dependent);
+cudaError_t launch_f32_prep(const Problem& p, cudaStream_t st);
+cudaError_t f32_kernel_setup();
 cudaError_t launch_decode(const DecodeArgs& a, bool f32, cudaStream_t st);
 cudaError_t scan_kernel_setup();
 cudaError_t wy_kernel_setup();

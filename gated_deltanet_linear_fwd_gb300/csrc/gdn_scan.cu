@@ -28,8 +28,8 @@
 // All are M = 128 tcgen05 MMAs (fp16 operands, fp32 accumulation in TMEM).
 // The state is kept fp32 in registers and rounded to fp16 once per chunk
 // into TMEM (two buffers), where the MMAs read it as their A operand; V'
-// likewise (two buffers of its fp16 copy beside its fp32 accumulator).  A value outside the fp16 range is reported
-// through the status word.
+// likewise (two buffers of its fp16 copy beside its fp32 accumulator).  A
+// value outside the fp16 range is reported through the status word.
 //
 // Warp roles (512 threads, four warpgroups): warps 0-7 hold the state (row =
 // d_v lane, 64 columns each) and run the V' and state epilogues, the
@@ -44,7 +44,10 @@
 // The state warpgroups raise their register limit to 168 (the state takes
 // 64 per thread) and the others lower theirs to 88, within the 128 per
 // thread the block is launched with.  The roles hand over through
-// mbarriers whose waits are all bounded.
+// mbarriers whose waits are all bounded; every decision to stop after a wait
+// gave up is taken alike by all threads that share a warp-collective
+// instruction or a named barrier, so a timeout ends in the kernel's own
+// exit path.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -117,6 +120,7 @@ struct Ctl {
   uint32_t tmem;
   int abort;
   int range_bad;
+  int skip;
   SegInfo seg;
 };
 static_assert(sizeof(Ctl) <= kSmemUse - kSmCtl, "control block too large");
@@ -124,6 +128,10 @@ static_assert(sizeof(Ctl) <= kSmemUse - kSmCtl, "control block too large");
 __device__ __forceinline__ bool wait_bar(Ctl* ctl, int b, uint32_t parity) {
   return wait_phase(&ctl->bar[b], parity, &ctl->abort, 100 + b);
 }
+
+// A warp's verdict on a wait: true only if every lane's wait succeeded, so
+// the warp stays converged for its warp-collective instructions.
+__device__ __forceinline__ bool warp_ok(bool ok) { return __all_sync(0xffffffffu, ok); }
 
 // Bounded wait that polls without suspending: the single MMA-issuing thread
 // uses it so that it reacts to a hand-over as soon as the phase completes.
@@ -246,8 +254,8 @@ __device__ __forceinline__ void convert_role(uint8_t* sm, Ctl* ctl, const Chain&
   const int n = ch.run_end - ch.run_begin;
   for (int i = 0; i < n; ++i) {
     const int st = i & 1;
-    if (!wait_bar(ctl, kKqFull0 + st, (uint32_t)((i >> 1) & 1)) ||
-        !wait_bar(ctl, kGates0 + (i & 3), (uint32_t)((i >> 2) & 1)))
+    if (!warp_ok(wait_bar(ctl, kKqFull0 + st, (uint32_t)((i >> 1) & 1)) &&
+                 wait_bar(ctl, kGates0 + (i & 3), (uint32_t)((i >> 2) & 1))))
       break;
     const uint32_t base = smem_u32(sm + kRingK + st * kSlotK);
     const uint32_t sDec = smem_u32(sm + kSmG + (i & 3) * 512 + 256);
@@ -296,17 +304,29 @@ __device__ __forceinline__ void convert_role(uint8_t* sm, Ctl* ctl, const Chain&
 // epilogue -> A(i+1); the output products fill the issuer's time in between.
 // A(i+2), issued after O2(i), tells the state warps through va_done that V'
 // buffer i & 1 has been read.
+// The descriptor of the tile at byte offset off from the tile whose
+// descriptor is d: the start-address field holds the shared-memory address
+// >> 4 in its low 14 bits, and every tile here lies below 256 KB, so adding
+// off >> 4 never carries out of the field.  With every descriptor derived
+// this way from a few computed once, issuing an MMA costs one add.
+__device__ __forceinline__ uint64_t desc_at(uint64_t d, uint32_t off) { return d + (uint64_t)(off >> 4); }
+
 template <bool PREP>
 __device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch, uint32_t tmem) {
   const int n = ch.run_end - ch.run_begin;
   const uint32_t id_k = idesc_f16(128, 64, false, false);
   const uint32_t id_sw = idesc_f16(128, 64, false, true);
   const uint32_t id_d3 = idesc_f16(128, 128, false, true);
+  // SW128 descriptors of the first slot of each ring
+  const uint64_t dW0 = sdesc_sw128(smem_u32(sm + kRingA + kAWn), 8192, 1024);
+  const uint64_t dK0 = sdesc_sw128(smem_u32(sm + kRingK), 8192, 1024);
+  const uint64_t dQ0 = sdesc_sw128(smem_u32(sm + kRingB + kBQ), 16, 1024);
+  const uint64_t dP0 = sdesc_sw128(smem_u32(sm + kRingB + kBP), 16, 1024);
   if (n > 0 && !wait_bar(ctl, kFull0, 0u)) return;  // ring A of chunk 0
   for (int i = 0; i < n; ++i) {
     const int sb = i % 3;
-    const uint32_t sA = smem_u32(sm + kRingA + (i & 1) * kSlotA), sK = smem_u32(sm + kRingK + (i & 1) * kSlotK);
-    const uint32_t sB = smem_u32(sm + kRingB + sb * kSlotB);
+    const uint64_t dW = desc_at(dW0, (uint32_t)(i & 1) * kSlotA), dK = desc_at(dK0, (uint32_t)(i & 1) * kSlotK);
+    const uint64_t dQ = desc_at(dQ0, (uint32_t)sb * kSlotB), dP = desc_at(dP0, (uint32_t)sb * kSlotB);
     const uint32_t tS = tmem + kTS + (i & 1) * 64;    // the state's fp16 copy, 8 columns per K = 16 step
     const uint32_t tV = tmem + kTV16 + (i & 1) * 32;  // V''s fp16 copy, 8 columns per K = 16 step
     const uint32_t tO = tmem + kTO + (i & 1) * 64;
@@ -315,7 +335,7 @@ __device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch,
     tc_fence_after();
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks)  // -S W^T
-      mma_f16_ts(tmem + kTV, tS + ks * 8, sdesc_sw128(sA + kAWn + ks * 2048, 8192, 1024), id_sw, ks > 0 ? 1u : 0u);
+      mma_f16_ts(tmem + kTV, tS + ks * 8, desc_at(dW, ks * 2048), id_sw, ks > 0 ? 1u : 0u);
     mma_commit(&ctl->bar[kVaDone]);
     if (out) {
       if (!wait_bar(ctl, kQReady0 + (i & 1), (uint32_t)((i >> 1) & 1))) return;
@@ -323,23 +343,21 @@ __device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch,
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)  // O = S (gamma Q)^T
-        mma_f16_ts(tO, tS + ks * 8,
-                   sdesc_sw128(sB + kBQ + (uint32_t)(ks >> 2) * 8192u + (uint32_t)(ks & 3) * 32u, 16, 1024), id_k,
-                   ks > 0);
+        mma_f16_ts(tO, tS + ks * 8, desc_at(dQ, (ks >> 2) * 8192 + (ks & 3) * 32), id_k, ks > 0 ? 1u : 0u);
     }
     if (!wait_bar(ctl, kKReady0 + (i & 1), (uint32_t)((i >> 1) & 1))) return;
     if (!spin_bar(ctl, kVReady, (uint32_t)(i & 1))) return;
     tc_fence_after();
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)  // D3 = V'^T diag(dec) K
-      mma_f16_ts(tmem + kTD3, tV + ks * 8, sdesc_sw128(sK + ks * 2048, 8192, 1024), id_d3, ks > 0);
+      mma_f16_ts(tmem + kTD3, tV + ks * 8, desc_at(dK, ks * 2048), id_d3, ks > 0 ? 1u : 0u);
     mma_commit(&ctl->bar[kD3Done]);
     mma_commit(&ctl->bar[kEmptyK0 + (i & 1)]);  // ring K slot read
     mma_commit(&ctl->bar[kEmpty0 + (i & 1)]);   // ring A slot read (A(i); U^T before v_ready(i))
     if (out) {
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)  // O += V'^T P^T
-        mma_f16_ts(tO, tV + ks * 8, sdesc_sw128(sB + kBP + ks * 32, 16, 1024), id_k, 1u);
+        mma_f16_ts(tO, tV + ks * 8, desc_at(dP, ks * 32), id_k, 1u);
     }
     mma_commit(&ctl->bar[kYoDone0 + (i & 1)]);
     mma_commit(&ctl->bar[kEmptyB0 + sb]);  // ring B slot read (Y, O2)
@@ -355,7 +373,9 @@ __device__ __forceinline__ void mma_role(uint8_t* sm, Ctl* ctl, const Chain& ch,
 // tensor store for a full chunk, one 256-byte bulk copy per token for a
 // sequence's partial last chunk (whose other rows belong to the next
 // sequence).  Every chunk, written or not, ends with yo_free, which
-// releases Y/O2 buffer i & 1 to the MMA issuer.
+// releases Y/O2 buffer i & 1 to the MMA issuer.  The four warps decide
+// together (a named barrier with an OR) whether to go on after each wait, so
+// none is left behind at the next named barrier.
 template <bool PREP>
 __device__ __forceinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem& p, const SegInfo& si,
                                             const Chain& ch, uint32_t tmem, int j, const CUtensorMap* mo) {
@@ -366,14 +386,15 @@ __device__ __forceinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem
   const uint32_t sO = smem_u32(sm + kSmO);
   const int n = ch.run_end - ch.run_begin;
   float mx = 0.f;  // largest |o| (inf or NaN when an fp16 operand overflowed)
+  auto all_ok = [&](bool ok) { return !named_bar_or(kOutBarrier, kOutThreads, !ok); };
   // Q of chunk c times gamma = exp(G) of its row, rounded to fp16 (chunks
   // with no output: nothing to round), then q_ready(c); every chunk gets its
   // q_ready, so its phases follow c.
   auto round_q = [&](int c) -> bool {
     if (want_out<PREP>(ch, c)) {
-      if (!wait_bar(ctl, kQFull0 + c % 3, (uint32_t)((c / 3) & 1)) ||
-          !wait_bar(ctl, kGates0 + (c & 3), (uint32_t)((c >> 2) & 1)))
-        return false;
+      const bool ok = wait_bar(ctl, kQFull0 + c % 3, (uint32_t)((c / 3) & 1)) &&
+                      wait_bar(ctl, kGates0 + (c & 3), (uint32_t)((c >> 2) & 1));
+      if (!all_ok(ok)) return false;
       round_q_tile(smem_u32(sm + kRingB + (c % 3) * kSlotB + kBQ), smem_u32(sm + kSmG + (c & 3) * 512),
                    threadIdx.x - kOutWarp * 32);
       fence_proxy_async_smem();
@@ -386,12 +407,10 @@ __device__ __forceinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem
     if (!round_q(c)) return;
   for (int i = 0; i < n; ++i) {
     const bool out = want_out<PREP>(ch, i);
-    const bool ok = wait_bar(ctl, kYoDone0 + (i & 1), (uint32_t)((i >> 1) & 1));
-    if (!out && !ok) break;
+    if (!all_ok(wait_bar(ctl, kYoDone0 + (i & 1), (uint32_t)((i >> 1) & 1)))) break;
     if (out) {
       if (issuer) bulk_wait_read_all();  // the previous chunk's stores have read the tile
-      // the four warps pass the tile's barriers together or leave together
-      if (named_bar_or(kOutBarrier, kOutThreads, !ok)) break;
+      named_bar_sync(kOutBarrier, kOutThreads);
       tc_fence_after();
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -480,17 +499,17 @@ __device__ __forceinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem&
   for (int i = 0; i < n; ++i) {
     const uint32_t par = (uint32_t)(i & 1);
     const uint32_t sGam = smem_u32(sm + kSmG + (i & 3) * 512);  // exp(G) [64], then dec [64]
-    if (!wait_bar(ctl, kGates0 + (i & 3), (uint32_t)((i >> 2) & 1))) break;
+    if (!warp_ok(wait_bar(ctl, kGates0 + (i & 3), (uint32_t)((i >> 2) & 1)))) break;
     // U^T of this thread's row and 32 tokens (16-byte chunks half * 4 .. + 3 of
     // the row in ring A), read while A(i) runs
     uint4 uq[4] = {};
     if (ch.has_u) {
-      if (!wait_bar(ctl, kFull0 + (i & 1), (uint32_t)((i >> 1) & 1))) break;
+      if (!warp_ok(wait_bar(ctl, kFull0 + (i & 1), (uint32_t)((i >> 1) & 1)))) break;
       const uint32_t sU = smem_u32(sm + kRingA + (i & 1) * kSlotA + kAU);
 #pragma unroll
       for (int c = 0; c < 4; ++c) uq[c] = lds_u32x4(sU + sw128_offset(row, half * 4 + c));
     }
-    if (!wait_bar(ctl, kVaDone, par)) break;
+    if (!warp_ok(wait_bar(ctl, kVaDone, par))) break;
     tc_fence_after();
     const float gC = lds_f32(sGam + 63 * 4);
     // V' = U^T - S W^T, its fp16 copy into TMEM buffer i & 1 (columns 16 half ..
@@ -519,7 +538,7 @@ __device__ __forceinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem&
     tc_fence_before();
     mbar_arrive(&ctl->bar[kVReady]);
     // S = gamma_C S + D3
-    if (!wait_bar(ctl, kD3Done, par)) break;
+    if (!warp_ok(wait_bar(ctl, kD3Done, par))) break;
     tc_fence_after();
 #pragma unroll
     for (int g8 = 0; g8 < 2; ++g8) {
@@ -577,9 +596,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       if (!ok) si.n = -1;
       ctl->seg = si;
+      ctl->skip = earlier_failure(p.status);
     }
   }
   __syncthreads();
+  if (ctl->skip) return;  // an earlier kernel failed: its results are incomplete
   const SegInfo si = ctl->seg;
   if (si.n < 0) {
     if (tid == 0) report(p.status, kDevCheck, kDetSegMismatch);
@@ -647,7 +668,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (ch.init == kInitH0 && p.h0 == nullptr) ch.init = kInitZero;
   ch.iq = (int)(((int64_t)j * p.h_qk) / p.h_v);
   ch.chunk0 = seq_first_chunk(p, si.n);
-  if (ch.chunk0 < 0 || ch.chunk0 + si.n_chunks > p.n_chunks_total) {  // the chunk index disagrees with the plan
+  if (ch.chunk0 < 0 || ch.chunk0 + si.n_chunks > p.n_chunks_total || ch.run_begin < 0 ||
+      ch.run_begin > ch.run_end) {  // the chunk index or the warmup depth disagrees with the plan
     if (tid == 0) report(p.status, kDevCheck, kDetSegMismatch);
     return;
   }

@@ -57,6 +57,7 @@ constexpr uint32_t kTU = 0;    // U^T               128 x 64 (over D, read by th
 
 struct WyCtl {
   uint64_t full, vfull, kq, w, u;  // K|Q landed, V landed, D done, W done, U done
+  uint64_t stall;                  // the test hook's barrier (nothing arrives on it)
   uint32_t tmem;
   int abort;
   float warp_total[2];
@@ -209,6 +210,14 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
                                      const CUtensorMap* mk, const CUtensorMap* mv, uint32_t tmem, float& mx) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gc = (int)(blockIdx.x / (unsigned)p.h_v), j = (int)(blockIdx.x % (unsigned)p.h_v);
+  if (p.stall_ns) {  // test hook: a wait that nothing ends, bounded by stall_ns
+    bool ok = true;
+    if (tid == 0 && !mbar_wait(&ctl->stall, 0, p.stall_ns)) {
+      atomicCAS(&ctl->abort, 0, kDetStallTest);
+      ok = false;
+    }
+    if (__syncthreads_or(!ok)) return false;
+  }
   int n, cv;
   int64_t t0;
   if (p.cu) {  // one 16-byte load: {sequence, valid tokens, first token}
@@ -502,6 +511,7 @@ __global__ void __launch_bounds__(kWyThreads, 4)
   grid_dependency_wait();  // the chunk index (varlen) is written by the kernel before
   grid_launch_dependents();
   if (tid == 0) {
+    mbar_init(&ctl->stall, 1);
     mbar_init(&ctl->full, 1);
     mbar_init(&ctl->vfull, 1);
     mbar_init(&ctl->kq, 1);

@@ -62,8 +62,9 @@ typedef enum gdn_status {
  *   GDN_BF16: the chunked tcgen05 path (fp16 MMA operands, fp32 accumulation),
  *             with the plan's context parallelism.
  *   GDN_F32:  fp32 throughout, on the CUDA cores: the recurrence itself,
- *             parallel over (sequence, value head, 16 state rows); the plan's
- *             segments are not used.  For results within 1e-4 of exact. */
+ *             one state row per thread pair, with the plan's segments always
+ *             combined exactly (a WARMUP plan runs as EXACT).  For results
+ *             within 1e-4 of exact. */
 enum { GDN_BF16 = 0, GDN_F32 = 1 };
 
 /* Intra-card context parallelism [FlashQLA, "AutoCP"]. */
@@ -191,7 +192,8 @@ gdn_status gdn_get_device_status(const void* workspace, void* stream, int* code,
 /*
  * gdn_cp_head_modes -- diagnostics: synchronises `stream` and copies, per
  * (sequence, value head), the mode the last gdn_chunk_fwd on this workspace
- * took (GDN_CP_EXACT or GDN_CP_WARMUP; GDN_CP_OFF for plans without CP) and
+ * took (GDN_CP_EXACT or GDN_CP_WARMUP; GDN_CP_OFF for plans without CP; always
+ * GDN_CP_EXACT on the fp32 path with CP) and
  * the natural log of its warmup error bound (-inf when no segment needs one).
  *   modes_host    : host int32 [n_seqs * h_v], or NULL.
  *   log_bound_host: host fp32 [n_seqs * h_v], or NULL.
@@ -222,14 +224,27 @@ gdn_status gdn_cp_head_modes(const void* workspace, const gdn_cp_plan_t* plan, i
  *     every part the forward reads is written or cleared within the call.
  *     Calls that may overlap on the GPU (other streams, other host threads)
  *     race on the array: serialise them.
- *   - The device status word of these calls lives in the shared array and
- *     is not readable through gdn_get_device_status.
+ *   - The device status word of these calls lives in the shared array;
+ *     read it with gdn_get_static_device_status.
  * Errors: as gdn_chunk_fwd, plus WORKSPACE for plans above the limit.
  */
 gdn_status gdn_chunk_fwd_static(const void* q, const void* k, const void* v, const float* g,
                                 const float* beta, const float* initial_state,
                                 const int32_t* cu_seqlens_dev, void* out, float* final_state,
                                 const gdn_dims* dims, const gdn_cp_plan_t* plan, void* stream);
+
+/*
+ * gdn_get_static_device_status -- gdn_get_device_status for the calls of
+ * gdn_chunk_fwd_static on the current device: synchronises `stream`, then
+ * reads the status word the kernels of the last such call wrote into the
+ * library's built-in array (no counterpart on the FlashQLA pages).  The
+ * first use on a device looks up the array's address like
+ * gdn_chunk_fwd_static does.
+ *   code   : host; receives GDN_OK, GDN_ERR_DEVICE_TIMEOUT or GDN_ERR_DEVICE_CHECK.
+ *   detail : host, may be NULL; receives the kernel-specific detail word.
+ * Errors: INVALID_ARG (code NULL), CUDA (address lookup, copy or sync failed).
+ */
+gdn_status gdn_get_static_device_status(void* stream, int* code, int* detail);
 
 /*
  * gdn_decode_step -- one new token for each of a batch of sequences: the
@@ -255,11 +270,26 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const fl
                            float* state, void* out, const gdn_dims* dims, void* stream);
 
 /*
+ * gdn_debug_stall_ns -- test hook of the failure path (no counterpart on the
+ * FlashQLA pages).  While ns > 0, each later gdn_chunk_fwd of this process on
+ * the bf16 path makes the blocks of its chunk-local kernel first wait ns
+ * nanoseconds on an mbarrier that nothing arrives on.  That bounded wait
+ * runs out: the blocks record GDN_ERR_DEVICE_TIMEOUT with detail 6 in the
+ * workspace's status word, free their tensor memory and return, and every
+ * kernel after them sees the recorded failure and does no work, so o and
+ * final_state are left unwritten.  ns = 0 (the default) turns it off.  A
+ * process-wide setting for tests; not for production calls.
+ * Errors: none.
+ */
+gdn_status gdn_debug_stall_ns(uint32_t ns);
+
+/*
  * gdn_set_trace_events -- optional per-kernel timing (tracing).  Registers,
  * for the calling host thread, up to 16 caller-created cudaEvent_t handles.
- * While registered, each gdn_chunk_fwd on this thread records events[0] on
- * its stream before its first kernel and events[i + 1] right after its i-th
- * kernel launch, so cudaEventElapsedTime(events[i], events[i + 1]) is the
+ * While registered, each gdn_chunk_fwd (and gdn_decode_step) on this thread
+ * brackets its i-th kernel launch with events[2i] (recorded right before the
+ * launch) and events[2i + 1] (right after it), both on the stream the kernel
+ * is launched on, so cudaEventElapsedTime(events[2i], events[2i + 1]) is the
  * device time of kernel i.  n_events = 0 (or events = NULL) turns tracing
  * off.  The caller keeps ownership of the events.
  * Errors: INVALID_ARG for n_events outside 0..16 or a NULL event.
@@ -267,8 +297,9 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const fl
 gdn_status gdn_set_trace_events(void* const* events, int n_events);
 
 /*
- * gdn_trace_last -- names of the kernels the last gdn_chunk_fwd on this
- * thread launched, in order (static strings), and their count.
+ * gdn_trace_last -- names of the kernels the last gdn_chunk_fwd (or
+ * gdn_decode_step) on this thread launched, in launch order (static
+ * strings), and their count (at most 8).
  *   names : host array of at least max_names pointers, or NULL.
  * Returns the number of kernels launched (0 before any call).
  */

@@ -172,3 +172,19 @@ def test_plan_automatic_lambda(lib, cu, h_v, sms):
     st, p = plan(lib, cu[-1], h_v=h_v, cu=cu, mode=2, lam=0.0, sms=sms)
     assert st == 0
     assert p.lambda_q8 == util.auto_lambda_q8([cu[n + 1] - cu[n] for n in range(len(cu) - 1)], h_v, sms)
+
+
+def test_device_status_decoding():
+    """The host's reading of the status word's (code, detail) pairs."""
+    from gated_deltanet_linear_fwd_gb300 import describe_device_status
+    assert describe_device_status(0, 0) == "ok"
+    assert describe_device_status(5, 6) == "timeout: the test hook's stall"
+    assert describe_device_status(7, 5).startswith("check failed: a value outside the fp16 range")
+    assert describe_device_status(7, 3).endswith("disagree with the plan")
+    assert describe_device_status(5, 108) == "timeout: the bounded wait on barrier 8"
+
+
+def test_debug_stall_hook_is_exported_and_settable(lib):
+    assert lib.gdn_debug_stall_ns(0) == 0
+    assert lib.gdn_debug_stall_ns(1000) == 0
+    assert lib.gdn_debug_stall_ns(0) == 0

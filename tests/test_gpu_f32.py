@@ -1,5 +1,7 @@
 """GPU parity of the fp32 path (q, k, v, o in fp32) against the float64
-oracle: max|diff| <= 1e-4 * RMS(ref) for o and for the final state."""
+oracle: max|diff| <= 1e-4 * RMS(ref) for o and for the final state, on small
+ragged cases in every context-parallel mode (the fp32 path combines segments
+exactly in all of them) and on the 1 x 32768, h 2/8 workload at full size."""
 from __future__ import annotations
 
 import pytest
@@ -23,6 +25,8 @@ CASES = {
     "ragged_gqa3_h0": lambda: make_inputs(cu_seqlens=[0, 1, 65, 200, 200, 391, 1000], h_qk=2, h_v=6, seed=7,
                                           with_h0=True, dtype=torch.float32),
     "long_mix_h0": lambda: make_inputs(8192 + 5, h_qk=2, h_v=8, seed=13, with_h0=True, dtype=torch.float32),
+    "many_short": lambda: make_inputs(cu_seqlens=[0, 5, 5, 70, 200, 201, 330, 640, 641, 700], h_qk=1, h_v=2, seed=19,
+                                      with_h0=True, dtype=torch.float32),
 }
 
 
@@ -40,4 +44,19 @@ def test_f32_parity(key, mode):
     eo, eh = util.parity_f32(o, ro), util.parity_f32(hT, rh)
     print(f"f32 {key}/{mode}: o {eo:.2e}  hT {eh:.2e}")
     assert o.dtype == torch.float32
+    assert eo <= TOL_F32 and eh <= TOL_F32
+
+
+def test_f32_parity_full_size():
+    """The 1 x 32768, h 2/8 workload in fp32 with the planner's defaults."""
+    w = workload("T32768_h2x8", dtype=torch.float32)
+    d = w.to("cuda:0")
+    plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, dtype=torch.float32)
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device="cuda:0")
+    o, hT = gdn_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, None, plan=plan, workspace=ws)
+    assert gdn_get_device_status(ws)[0] == 0
+    f = util.to64
+    ro, rh = oracle.recurrence(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), None)
+    eo, eh = util.parity_f32(o, ro), util.parity_f32(hT, rh)
+    print(f"f32 full size ({plan.n_seg_total} segments): o {eo:.2e}  hT {eh:.2e}")
     assert eo <= TOL_F32 and eh <= TOL_F32

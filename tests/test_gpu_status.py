@@ -1,6 +1,8 @@
 """The device status word: values outside the fp16 range of the MMA
 operands are reported (status 7, detail 5) rather than silently rounded to
-inf, and ordinary inputs report nothing."""
+inf, ordinary inputs report nothing, and a bounded wait that runs out (the
+test hook's wait on a barrier nothing arrives on) ends the call through its
+timeout path (status 5) without disturbing the next call."""
 from __future__ import annotations
 
 import dataclasses
@@ -13,7 +15,10 @@ pytestmark = pytest.mark.gpu
 if not torch.cuda.is_available():  # pragma: no cover - collected on CPU, skipped there
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
-from gated_deltanet_linear_fwd_gb300 import gdn_chunk_fwd, gdn_cp_plan, gdn_get_device_status  # noqa: E402
+import oracle  # noqa: E402
+from gated_deltanet_linear_fwd_gb300 import (describe_device_status, gdn_chunk_fwd, gdn_cp_plan,  # noqa: E402
+                                             gdn_debug_stall_ns, gdn_get_device_status)
+from tests import util  # noqa: E402
 from gated_deltanet_linear_fwd_gb300.inputs import make_inputs  # noqa: E402
 
 DEVICE_CHECK, FP16_RANGE = 7, 5
@@ -50,3 +55,30 @@ def test_query_past_fp16_range_is_reported(mode):
     w = make_inputs(700, h_qk=2, h_v=4, seed=3)
     w = dataclasses.replace(w, q=(w.q.float() * 1e6).to(torch.bfloat16))  # q itself has no fp16 image
     assert _status(w, mode) == (DEVICE_CHECK, FP16_RANGE)
+
+
+@pytest.mark.parametrize("mode", ["off", "exact"])
+def test_timeout_path_reports_and_the_next_call_is_clean(mode):
+    """The chunk-local kernel's blocks wait on an mbarrier nothing arrives on,
+    20 us at most: the wait runs out, the status word reads (5, 6), the
+    kernels after it do no work (o and the final state stay NaN), and the next
+    ordinary call on the same workspace matches the oracle."""
+    w = make_inputs(700, h_qk=2, h_v=4, seed=3, with_h0=True)
+    d = w.to("cuda:0")
+    plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, mode=mode, lambda_=0.5)
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device="cuda:0")
+    out = torch.full_like(d.v, float("nan"))
+    hT = torch.full((1, w.h_v, 128, 128), float("nan"), device="cuda:0")
+    try:
+        gdn_debug_stall_ns(20000)
+        gdn_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, plan=plan, out=out, final_state=hT, workspace=ws)
+        status = gdn_get_device_status(ws)
+    finally:
+        gdn_debug_stall_ns(0)
+    assert status == (5, 6), describe_device_status(*status)
+    assert torch.isnan(out).all() and torch.isnan(hT).all()
+    o, h = gdn_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, plan=plan, workspace=ws)
+    assert gdn_get_device_status(ws) == (0, 0)
+    f = util.to64
+    ro, rh = oracle.recurrence(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0))
+    assert util.parity_bf16(o, ro)[0] <= util.TOL_BF16 and util.parity_f32(h, rh) <= util.TOL_STATE
