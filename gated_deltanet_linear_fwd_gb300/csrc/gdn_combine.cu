@@ -35,30 +35,32 @@ __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
   float* sP = sX + kRows * kDim;               // [kSlices][kRows][128] partial sums
   __shared__ SegInfo s_seq;
   __shared__ uint64_t s_bar[2];
-  grid_dependency_wait();  // the segment transitions and local states: written by the kernel before
-  grid_launch_dependents();
   const int tid = threadIdx.x, warp = tid >> 5;
   const int n = blockIdx.x, j = blockIdx.y, r0 = blockIdx.z * kRows;
   __shared__ int s_mode, s_skip;
-  if (tid == 0) s_skip = earlier_failure(p.status);
-  __syncthreads();
-  if (s_skip) return;  // an earlier kernel failed: its results are incomplete
-  if (warp == 0) {
-    SegInfo si;
-    locate_sequence(p, n, si);
+  // the sequence's segments come from the plan's arithmetic and the sequence
+  // bounds (an input): located while the kernel before this one finishes
+  SegInfo si;
+  if (warp == 0) locate_sequence(p, n, si);
+  grid_dependency_wait();  // the segment transitions and local states: written by the kernel before
+  grid_launch_dependents();
+  if (warp == 0) {  // the status word is fetched beside the segments' depths
+    const int st = (tid == 0) ? earlier_failure(p.status) : 0;
     float bound;
     const int mode = head_mode_warp(p, si, j, &bound);
-    if ((tid & 31) == 0) {
+    if (tid == 0) {
+      s_skip = st;
       s_seq = si;
       s_mode = mode;
-      if (blockIdx.z == 0) {
+      if (blockIdx.z == 0 && !st) {
         p.head_mode[n * p.h_v + j] = mode;
         p.head_bound[n * p.h_v + j] = bound;
       }
     }
   }
   __syncthreads();
-  const SegInfo si = s_seq;
+  if (s_skip) return;  // an earlier kernel failed: its results are incomplete
+  si = s_seq;
   const int mode = s_mode;
   if (mode != kModeExact || si.n_seg <= 1) return;
 

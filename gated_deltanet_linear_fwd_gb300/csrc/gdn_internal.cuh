@@ -210,19 +210,26 @@ __device__ inline void seg_warmup_depth(const Problem& p, int chunk0, int cb, in
 #pragma unroll
   for (int w = 1; w <= kPre; ++w) pre[w - 1] = w <= nwin ? p.chunk_exp[(size_t)(chunk0 + cb - w) * p.h_v + j] : 0.f;
   float acc = 0.f;
-  for (int w = 1; w <= nwin; ++w) {
-    acc += w <= kPre ? pre[w - 1] : p.chunk_exp[(size_t)(chunk0 + cb - w) * p.h_v + j];
+  // true when depth w ends the search (w_out, b_out set)
+  auto accept = [&](int w, float e) {
+    acc += e;
     if (cb - w == 0) {
       w_out = w;
       b_out = -__int_as_float(0x7f800000);
-      return;
+      return true;
     }
     if (acc <= p.log_tol) {
       w_out = w;
       b_out = acc;
-      return;
+      return true;
     }
-  }
+    return false;
+  };
+#pragma unroll
+  for (int w = 1; w <= kPre; ++w)  // constant indices keep pre[] in registers
+    if (w <= nwin && accept(w, pre[w - 1])) return;
+  for (int w = kPre + 1; w <= nwin; ++w)
+    if (accept(w, p.chunk_exp[(size_t)(chunk0 + cb - w) * p.h_v + j])) return;
   w_out = -1;
   b_out = acc;
 }
@@ -253,9 +260,10 @@ __device__ inline int head_mode_warp(const Problem& p, const SegInfo& si, int j,
 
 // Launches kernel<<<grid, block, smem, st>>>(args...); with `dependent`, as a
 // programmatic dependent launch: its blocks may start while the previous
-// kernel in the stream finishes, and wait for it (grid_dependency_wait) at
-// their start.  Every kernel of the forward waits first thing, so each one
-// also sees the results of all kernels before its predecessor.
+// kernel in the stream finishes, and wait for it (grid_dependency_wait)
+// before they read anything an earlier kernel wrote.  Each kernel lets its
+// dependents launch only after its own wait, so a kernel's blocks start only
+// once every kernel before its predecessor has completed.
 template <typename... Params, typename... Args>
 cudaError_t launch_kernel(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                           bool dependent, Args&&... args) {

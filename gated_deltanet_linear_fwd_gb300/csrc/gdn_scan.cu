@@ -586,18 +586,72 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int j = blockIdx.y;
   const int chain = PREP ? (int)blockIdx.z : 0;
+  // ---- which chain this CTA runs ----
+  // The segment comes from the plan's arithmetic and the sequence bounds (an
+  // input), so warps 0 and 1 locate it before waiting for the kernel before
+  // this one: while that kernel finishes on other SMs.  After the wait, warp
+  // 0 fetches the words the set-up depends on together, so that their
+  // latencies overlap: the status word, and for the output scan the head's
+  // mode and the segment's warmup depth; warp 1 of the preprocessing
+  // computes the warmup depths of the head's segments.
+  __shared__ int s_mode, s_w, s_exact;
+  SegInfo si0;
+  bool ok0 = false;
+  if (warp < 2) ok0 = locate_segment(p, blockIdx.x, si0);
+  if (tid == 64) {  // the barriers and tensor maps, also before the wait
+    const int counts[kNumBars] = {1, 1, 1, 1, 1, 1, 1, 1, 1, kChainThreads, 1, kChainThreads,
+                                  1, 1, kOutThreads, kOutThreads, 1, 1, kConvertWarps, kConvertWarps,
+                                  kOutThreads / 32, kOutThreads / 32, 1, 1, 1, 1, 1, 1, 1, 1};
+    for (int b = 0; b < kNumBars; ++b) mbar_init(&ctl->bar[b], counts[b]);
+    ctl->abort = 0;
+    ctl->range_bad = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&mq);
+    tma_prefetch_desc(&mk);
+    if (!PREP) tma_prefetch_desc(&mo);
+  }
   grid_dependency_wait();  // records, chunk index, segment states: written by the kernels before
   grid_launch_dependents();
-
-  // ---- which chain this CTA runs ----
   if (warp == 0) {
-    SegInfo si;
-    const bool ok = locate_segment(p, blockIdx.x, si);
+    SegInfo si = si0;
+    const bool ok = ok0;
+    int v = 0;
+    if (lane == 0) v = earlier_failure(p.status);
+    if (!PREP && ok && p.plan_mode != kModeOff) {
+      if (lane == 1) v = p.head_mode[si.n * p.h_v + j];
+      if (lane == 2 && p.plan_mode == kModeWarmup) v = p.seg_w[(size_t)(si.seg_base + si.s) * p.h_v + j];
+    }
+    const int mode = __shfl_sync(0xffffffffu, v, 1), w = __shfl_sync(0xffffffffu, v, 2);
     if (lane == 0) {
       if (!ok) si.n = -1;
       ctl->seg = si;
-      ctl->skip = earlier_failure(p.status);
+      ctl->skip = v;
+      s_mode = mode;
+      s_w = w;
     }
+  } else if (warp == 1) {
+    // warmup depths of every segment of this (sequence, head) from the chunk
+    // exponents; the head runs exactly unless all of them found a depth.  The
+    // first CTA of each segment records its depth for the combine and the scan.
+    bool none = false;
+    if (PREP && p.plan_mode == kModeWarmup) {
+      const SegInfo si = si0;
+      if (ok0) {
+        const int chunk0 = seq_first_chunk(p, si.n);
+        for (int s2 = lane; s2 < si.n_seg; s2 += 32) {
+          int w = 0;
+          float b = -__int_as_float(0x7f800000);
+          if (s2 > 0) seg_warmup_depth(p, chunk0, seg_first(s2, si.n_chunks, si.n_seg), j, w, b);
+          none |= w < 0;
+          if (s2 == si.s && chain == 0) {
+            p.seg_w[(size_t)(si.seg_base + s2) * p.h_v + j] = w;
+            p.seg_bound[(size_t)(si.seg_base + s2) * p.h_v + j] = b;
+          }
+        }
+      }
+    }
+    none = __any_sync(0xffffffffu, none);
+    if (lane == 0) s_exact = !PREP || p.plan_mode != kModeWarmup || none;
   }
   __syncthreads();
   if (ctl->skip) return;  // an earlier kernel failed: its results are incomplete
@@ -618,41 +672,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   ch.has_u = true;
   ch.write_final = false;
   if (PREP) {
-    if (p.plan_mode == kModeWarmup) {
-      // warmup depths of every segment of this (sequence, head) from the chunk
-      // exponents; the head runs exactly unless all of them found a depth.  The
-      // first CTA of each segment records its depth for the combine and the scan.
-      __shared__ int s_exact;
-      if (warp == 0) {
-        const int chunk0 = seq_first_chunk(p, si.n);
-        bool none = false;
-        for (int s2 = lane; s2 < si.n_seg; s2 += 32) {
-          int w = 0;
-          float b = -__int_as_float(0x7f800000);
-          if (s2 > 0) seg_warmup_depth(p, chunk0, seg_first(s2, si.n_chunks, si.n_seg), j, w, b);
-          none |= w < 0;
-          if (s2 == si.s && chain == 0) {
-            p.seg_w[(size_t)(si.seg_base + s2) * p.h_v + j] = w;
-            p.seg_bound[(size_t)(si.seg_base + s2) * p.h_v + j] = b;
-          }
-        }
-        none = __any_sync(0xffffffffu, none);
-        if (lane == 0) s_exact = none;
-      }
-      __syncthreads();
-      if (!s_exact) return;
-    }
+    if (!s_exact) return;  // a warmup head: no transition or local state needed
     if (si.s == si.n_seg - 1) return;
     if (chain == 0 && si.s == 0 && p.h0 == nullptr) return;  // M of segment 0 unused for a zero start
     ch.init = chain == 0 ? kInitIdentity : kInitZero;
     ch.has_u = chain == 1;
   } else {
-    const int mode = p.plan_mode == kModeOff ? kModeOff : p.head_mode[si.n * p.h_v + j];
+    const int mode = p.plan_mode == kModeOff ? kModeOff : s_mode;
     if (si.s == 0) {
       ch.init = kInitH0;
     } else if (mode == kModeWarmup) {
-      const int w = p.seg_w[(size_t)(si.seg_base + si.s) * p.h_v + j];
-      const int ws = si.cb - w;
+      const int ws = si.cb - s_w;
       if (ws <= 0) {
         ch.run_begin = 0;
         ch.init = kInitH0;
@@ -675,18 +705,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---- set-up ----
-  if (tid == 0) {
-    const int counts[kNumBars] = {1, 1, 1, 1, 1, 1, 1, 1, 1, kChainThreads, 1, kChainThreads,
-                                  1, 1, kOutThreads, kOutThreads, 1, 1, kConvertWarps, kConvertWarps,
-                                  kOutThreads / 32, kOutThreads / 32, 1, 1, 1, 1, 1, 1, 1, 1};
-    for (int b = 0; b < kNumBars; ++b) mbar_init(&ctl->bar[b], counts[b]);
-    ctl->abort = 0;
-    ctl->range_bad = 0;
-    fence_mbar_init();
-    tma_prefetch_desc(&mq);
-    tma_prefetch_desc(&mk);
-    if (!PREP) tma_prefetch_desc(&mo);
-  }
   fence_proxy_async_smem();
   if (warp == 0) {
     tmem_alloc(&ctl->tmem, 512);
