@@ -79,27 +79,20 @@ def algorithmic(w):
 # q, k, v, g and beta, the output scans write o and the states.  The chunk
 # records the WY kernel writes and the scans read back, the context-parallel
 # transitions and the combine are overhead and count zero.
-KERNEL_SOURCE = {"wy": "gdn_wy.cu", "scan_out": "gdn_scan.cu", "scan_out_warm": "gdn_scan.cu",
-                 "scan_out_exact": "gdn_scan.cu", "scan_prep": "gdn_scan.cu", "combine": "gdn_combine.cu",
-                 "modes": "gdn_combine.cu", "chunk_map": "gdn_wy.cu"}
+KERNEL_SOURCE = {"wy": "gdn_wy.cu", "scan_out": "gdn_scan.cu", "scan_prep": "gdn_scan.cu",
+                 "combine": "gdn_combine.cu", "chunk_map": "gdn_wy.cu"}
 
 
-def kernel_bytes(name, w, modes=None):
-    """name's share of the algorithmic bytes.  The output scan reads v and
-    writes o and the final state of the heads it runs: every head, or with
-    warmup heads split off (modes: per (sequence, head) 1 = exact, 2 =
-    warmup), those of its mode."""
+def kernel_bytes(name, w):
+    """name's share of the algorithmic bytes: the WY kernel reads q, k, v, g
+    and beta, the output scan writes o and the final state (and reads the
+    initial state); the other kernels move only intermediate data."""
     T, hqk, hv, n = w.T, w.h_qk, w.h_v, w.n_seqs
     if name == "wy":  # q, k (once per query/key head), v, g, beta
         return T * (2 * hqk * D * 2 + hv * D * 2 + 2 * hv * 4)
     per_head_state = D * D * 4 * (2 if w.h0 is not None else 1)
     if name == "scan_out":  # o out, the final state, and the initial state when given
         return T * hv * D * 2 + n * hv * per_head_state
-    if name in ("scan_out_warm", "scan_out_exact") and modes is not None:
-        want = 2 if name == "scan_out_warm" else 1
-        offs = w.seq_offsets()
-        return sum(((offs[s + 1] - offs[s]) * D * 2 + per_head_state)
-                   for s in range(n) for j in range(hv) if modes[s * hv + j] == want)
     return 0
 
 
@@ -596,8 +589,8 @@ def main(argv=None):
     roof = None
     if kms:
         # the dominant kernel: its share of the algorithmic bytes over its average launch time
-        top = max((k for k in kms if kernel_bytes(k, r["w"], r["modes"]) > 0), key=lambda k: kms[k])
-        kb = kernel_bytes(top, r["w"], r["modes"])
+        top = max((k for k in kms if kernel_bytes(k, r["w"]) > 0), key=lambda k: kms[k])
+        kb = kernel_bytes(top, r["w"])
         achieved = kb / (kms[top] * 1e-3) / 1e9
         roof = {"bound": "hbm", "kernel": top, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": achieved / hbm, "traffic": traffic_from_profile(f"{top}_T32768_h2x8", KERNEL_SOURCE[top]),
