@@ -173,14 +173,15 @@ def barrier(world):
         dist.barrier()
 
 
-def time_gpu(name, steps, warmup, device, cp="auto", lambda_=0.0, trace=True):
+def time_gpu(name, steps, warmup, device, cp="auto", lambda_=0.0, trace=True, tol_rule="noise"):
     """Times the forward on one workload; returns a dict of measurements."""
     from gated_deltanet_linear_fwd_gb300 import (gdn_chunk_fwd, gdn_cp_head_modes, gdn_cp_plan,
                                                  gdn_get_device_status, gdn_set_trace_events, gdn_trace_last)
     from gated_deltanet_linear_fwd_gb300.inputs import workload
     w = workload(name)
     d = w.to(device)
-    plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, cu_seqlens=w.cu_seqlens, mode=cp, lambda_=lambda_)
+    plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, cu_seqlens=w.cu_seqlens, mode=cp, lambda_=lambda_,
+                       tol_rule=tol_rule)
     ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
     out = torch.empty_like(d.v)
     hT = torch.empty(w.n_seqs, w.h_v, D, D, dtype=torch.float32, device=device)
@@ -243,22 +244,25 @@ VARLEN = "varlen4_T348160_h2x8"
 def compare_cp_modes(name, steps, device):
     """The same workload without context parallelism, with every head
     combined exactly, and in the automatic mode (warmup restarts where the
-    gate bound allows): time of each, and how far each mode's o and final
-    state are from the exact ones (max |diff| / RMS of the exact result)."""
+    gate bound allows) with the noise-floor tolerance (the default) and with
+    the fixed one: time of each, and how far each mode's o and final state
+    are from the exact ones (max |diff| / RMS of the exact result)."""
     from gated_deltanet_linear_fwd_gb300 import gdn_chunk_fwd, gdn_cp_plan
     from gated_deltanet_linear_fwd_gb300.inputs import workload
+    cases = {"off": ("off", "noise"), "exact": ("exact", "noise"), "auto": ("auto", "noise"),
+             "auto_fixed_tol": ("auto", "fixed")}
     res = {}
-    for cp in ("off", "exact", "auto"):
-        t = time_gpu(name, steps, 3, device, cp, 0.0, trace=False)
-        res[cp] = {"ms": t["ms"], "segments": t["plan"].n_seg_total, "head_modes": t["modes"]}
+    for key, (cp, rule) in cases.items():
+        t = time_gpu(name, steps, 3, device, cp, 0.0, trace=False, tol_rule=rule)
+        res[key] = {"ms": t["ms"], "segments": t["plan"].n_seg_total, "head_modes": t["modes"]}
     w = workload(name)
     d = w.to(device)
     outs = {}
-    for cp in ("off", "exact", "auto"):
-        plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, cu_seqlens=w.cu_seqlens, mode=cp)
-        outs[cp] = gdn_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, plan=plan)
+    for key, (cp, rule) in cases.items():
+        plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, cu_seqlens=w.cu_seqlens, mode=cp, tol_rule=rule)
+        outs[key] = gdn_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, plan=plan)
     rel = lambda a, b: float((a.float() - b.float()).abs().max() / b.float().pow(2).mean().sqrt())
-    for cp in ("off", "auto"):
+    for cp in ("off", "auto", "auto_fixed_tol"):
         res[cp + "_vs_exact"] = {"o": rel(outs[cp][0], outs["exact"][0]),
                                  "final_state": rel(outs[cp][1], outs["exact"][1])}
     return res
@@ -604,7 +608,7 @@ def main(argv=None):
         "vs_baseline": value / (32768 / (PAGES_H200_MS[HEADLINE] * 1e-3)),
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": HEADLINE, "B": 1, "T": 32768, "h_qk": 2, "h_v": 8, "d_k": 128, "d_v": 128,
-                   "chunk": 64, "cp": r["plan"].mode, "segments": r["plan"].n_seg_total,
+                   "chunk": 64, "cp": r["plan"].mode, "warmup_tol_rule": "noise", "segments": r["plan"].n_seg_total,
                    "head_modes": r["modes"], "l2": "flushed (256 MB write) before every timed step",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roof,

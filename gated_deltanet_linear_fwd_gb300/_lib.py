@@ -23,6 +23,8 @@ GDN_ERR_DEVICE_CHECK = 7
 
 GDN_BF16 = 0
 GDN_F32 = 1
+GDN_TOL_FIXED = 0
+GDN_TOL_NOISE = 1
 
 GDN_CP_OFF = 0
 GDN_CP_EXACT = 1
@@ -42,14 +44,14 @@ class gdn_dims(ctypes.Structure):
 
 class gdn_cp_opts(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int), ("lambda_", ctypes.c_float), ("warmup_chunks", ctypes.c_int),
-                ("warmup_tol", ctypes.c_float), ("sm_count", ctypes.c_int)]
+                ("warmup_tol", ctypes.c_float), ("sm_count", ctypes.c_int), ("tol_rule", ctypes.c_int)]
 
 
 class gdn_cp_plan_t(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int), ("n_seqs", ctypes.c_int), ("T_total", ctypes.c_int),
                 ("h_v", ctypes.c_int), ("h_qk", ctypes.c_int), ("dtype", ctypes.c_int),
                 ("lambda_q8", ctypes.c_int), ("warmup_chunks", ctypes.c_int),
-                ("warmup_tol", ctypes.c_float), ("sm_count", ctypes.c_int),
+                ("warmup_tol", ctypes.c_float), ("sm_count", ctypes.c_int), ("tol_rule", ctypes.c_int),
                 ("n_seg_total", ctypes.c_int), ("max_seg_chunks", ctypes.c_int),
                 ("max_chunks", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
                 ("off_head", ctypes.c_size_t), ("off_seg_bound", ctypes.c_size_t),

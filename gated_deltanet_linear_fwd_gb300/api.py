@@ -15,6 +15,7 @@ from . import _lib as L
 
 _MODES = {"off": L.GDN_CP_OFF, "exact": L.GDN_CP_EXACT, "warmup": L.GDN_CP_WARMUP, "auto": L.GDN_CP_AUTO}
 _DT = {torch.bfloat16: L.GDN_BF16, torch.float32: L.GDN_F32}
+_TOL_RULES = {"fixed": L.GDN_TOL_FIXED, "noise": L.GDN_TOL_NOISE}
 
 
 @dataclasses.dataclass
@@ -48,12 +49,14 @@ def _cu_list(cu_seqlens) -> Optional[list]:
 def gdn_cp_plan(*, T: int, h_qk: int, h_v: int, B: int = 1, cu_seqlens=None,
                 dtype: torch.dtype = torch.bfloat16, mode: str = "auto", lambda_: float = 0.0,
                 warmup_chunks: int = 8, warmup_tol: float = 1e-4, sm_count: int = 0,
-                scale: float = 0.0, d_k: int = 128, d_v: int = 128) -> Plan:
-    """Host-only planning (gdn_cp_plan).  T = tokens per row (varlen: total)."""
+                scale: float = 0.0, d_k: int = 128, d_v: int = 128, tol_rule: str = "noise") -> Plan:
+    """Host-only planning (gdn_cp_plan).  T = tokens per row (varlen: total).
+    tol_rule: "noise" (a warmup's tolerance is at least the exact path's noise
+    floor at the segment start) or "fixed" (warmup_tol alone)."""
     cu = _cu_list(cu_seqlens)
     n_seqs = B if cu is None else len(cu) - 1
     dims = L.gdn_dims(B, T, h_qk, h_v, d_k, d_v, n_seqs, scale, _DT.get(dtype, -1))
-    opts = L.gdn_cp_opts(_MODES[mode], lambda_, warmup_chunks, warmup_tol, sm_count)
+    opts = L.gdn_cp_opts(_MODES[mode], lambda_, warmup_chunks, warmup_tol, sm_count, _TOL_RULES[tol_rule])
     raw = L.gdn_cp_plan_t()
     cu_arr = None if cu is None else (ctypes.c_int32 * len(cu))(*cu)
     L.check(L.load().gdn_cp_plan(ctypes.byref(dims), cu_arr, ctypes.byref(opts), ctypes.byref(raw)),
@@ -76,7 +79,7 @@ def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
                   final_state: Optional[torch.Tensor] = None, output_final_state: bool = True,
                   workspace: Optional[torch.Tensor] = None, stream=None, scale: float = 0.0,
                   mode: str = "auto", lambda_: float = 0.0, warmup_chunks: int = 8,
-                  warmup_tol: float = 1e-4):
+                  warmup_tol: float = 1e-4, tol_rule: str = "noise"):
     """The chunked-prefill forward (gdn_chunk_fwd).
 
     q,k [B,T,h_qk,128] or [T,h_qk,128]; v [.., h_v, 128]; g,beta [.., h_v] fp32;
@@ -94,7 +97,8 @@ def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
         raise ValueError("g and beta must be float32")
     if plan is None:
         plan = gdn_cp_plan(T=T, h_qk=h_qk, h_v=h_v, B=B, cu_seqlens=cu_seqlens, dtype=q.dtype, mode=mode,
-                           lambda_=lambda_, warmup_chunks=warmup_chunks, warmup_tol=warmup_tol, scale=scale)
+                           lambda_=lambda_, warmup_chunks=warmup_chunks, warmup_tol=warmup_tol, scale=scale,
+                           tol_rule=tol_rule)
     dims = L.gdn_dims(B, T, h_qk, h_v, q.shape[-1], v.shape[-1], plan.raw.n_seqs, scale, _DT.get(q.dtype, -1))
     if out is None:
         out = torch.empty_like(v)

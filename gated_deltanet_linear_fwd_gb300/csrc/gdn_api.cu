@@ -299,9 +299,10 @@ gdn_status gdn_cp_plan(const gdn_dims* dims, const int32_t* cu, const gdn_cp_opt
   } else if (dims->n_seqs != dims->B) {
     return GDN_ERR_INVALID_ARG;
   }
-  gdn_cp_opts o = {GDN_CP_AUTO, 0.0f, 8, 1e-4f, 0};  // NULL opts: the planner picks lambda
+  gdn_cp_opts o = {GDN_CP_AUTO, 0.0f, 8, 1e-4f, 0, GDN_TOL_NOISE};  // NULL opts: the planner picks lambda
   if (opts) o = *opts;
   if (o.mode < GDN_CP_OFF || o.mode > GDN_CP_AUTO) return GDN_ERR_UNSUPPORTED;
+  if (o.tol_rule != GDN_TOL_FIXED && o.tol_rule != GDN_TOL_NOISE) return GDN_ERR_UNSUPPORTED;
   const bool auto_lambda = !(o.lambda > 0.f);
   if (o.lambda > 1000.f) return GDN_ERR_INVALID_ARG;
   if (o.warmup_chunks <= 0) o.warmup_chunks = 8;
@@ -333,6 +334,7 @@ gdn_status gdn_cp_plan(const gdn_dims* dims, const int32_t* cu, const gdn_cp_opt
   p.warmup_chunks = o.warmup_chunks;
   p.warmup_tol = o.warmup_tol;
   p.sm_count = o.sm_count;
+  p.tol_rule = o.tol_rule;
   int64_t n_seg_total = 0, n_chunks_total = 0;
   for (int n = 0; n < dims->n_seqs; ++n) {
     const int64_t len = cu ? (int64_t)cu[n + 1] - cu[n] : dims->T;
@@ -433,6 +435,7 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
   p.lambda_q8 = plan->lambda_q8;
   p.warmup_chunks = plan->warmup_chunks;
   p.log_tol = std::log(plan->warmup_tol);
+  p.tol_noise = plan->tol_rule == GDN_TOL_NOISE;
   p.n_seg_total = plan->n_seg_total;
   p.status = reinterpret_cast<int*>(ws);
   p.head_mode = reinterpret_cast<int*>(ws + plan->off_head);

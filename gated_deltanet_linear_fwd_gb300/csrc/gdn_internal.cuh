@@ -57,6 +57,7 @@ struct Problem {
   int lambda_q8;
   int warmup_chunks;
   float log_tol;            // log(warmup_tol)
+  int tol_noise;            // the tolerance of a segment is at least the noise floor at its start
   int n_seg_total;
   // workspace sections
   int* status;              // [0] code, [1] detail
@@ -196,19 +197,38 @@ __device__ inline void locate_sequence(const Problem& p, int n, SegInfo& out) {
 
 // Warmup depth of segment `cb` (its first chunk) of the sequence whose first
 // global chunk is chunk0 (FlashQLA pages, section "AutoCP": a fast-decaying
-// head restarts each segment from a few preceding chunks).  A restart from
-// zero w chunks early errs, relative to the state there, by at most
-// exp(sum of the window's chunk exponents), since each token map
-// X -> alpha X (I - beta k k^T) has spectral norm <= alpha max(1, |1 - beta
-// ||k||^2|).  The depth is the smallest w <= the planned maximum whose bound
-// is <= tol; a window reaching the sequence start is exact (bound -inf); no
-// such w gives -1 (the head runs exactly) with the full window's exponent.
+// head restarts each segment from a few preceding chunks, which brings the
+// state error below the noise floor).  A restart from zero w chunks early
+// errs, relative to the state there, by at most exp(sum of the window's
+// chunk exponents), since each token map X -> alpha X (I - beta k k^T) has
+// spectral norm <= alpha max(1, |1 - beta ||k||^2|).  The tolerance is
+// exp(log_tol), or with tol_noise the larger of that and the noise floor of
+// the exact path at the segment start: each chunk rounds the state operand to
+// fp16 (relative 2^-11), and that rounding m chunks back reaches the start
+// scaled by at most the bound of the last m chunks, so the floor is 2^-11 (1
+// + sum over the window's depths of their bounds, each capped at 1) -- a
+// lower bound, since chunks before the window also contribute, and at most
+// 9 x 2^-11 whatever the gates.  The depth is the smallest w <=
+// the planned maximum whose bound is <= the tolerance; a window reaching the
+// sequence start is exact (bound -inf); no such w gives -1 (the head runs
+// exactly) with the full window's exponent.
 __device__ inline void seg_warmup_depth(const Problem& p, int chunk0, int cb, int j, int& w_out, float& b_out) {
   const int nwin = min(p.warmup_chunks, cb);
   constexpr int kPre = 8;  // window exponents loaded together before the scan
   float pre[kPre];
 #pragma unroll
   for (int w = 1; w <= kPre; ++w) pre[w - 1] = w <= nwin ? p.chunk_exp[(size_t)(chunk0 + cb - w) * p.h_v + j] : 0.f;
+  float log_thr = p.log_tol;
+  if (p.tol_noise) {
+    float acc = 0.f, floor_sum = 1.f;
+#pragma unroll
+    for (int w = 1; w <= kPre; ++w)
+      if (w <= nwin) {
+        acc += pre[w - 1];
+        floor_sum += __expf(fminf(acc, 0.f));
+      }
+    log_thr = fmaxf(log_thr, __logf(floor_sum) - 11.f * 0.69314718f);
+  }
   float acc = 0.f;
   // true when depth w ends the search (w_out, b_out set)
   auto accept = [&](int w, float e) {
@@ -218,7 +238,7 @@ __device__ inline void seg_warmup_depth(const Problem& p, int chunk0, int cb, in
       b_out = -__int_as_float(0x7f800000);
       return true;
     }
-    if (acc <= p.log_tol) {
+    if (acc <= log_thr) {
       w_out = w;
       b_out = acc;
       return true;

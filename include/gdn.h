@@ -72,11 +72,25 @@ enum {
   GDN_CP_OFF = 0,    /* one CTA-level scan per (sequence, value head) */
   GDN_CP_EXACT = 1,  /* segments; start states combined exactly through M */
   GDN_CP_WARMUP = 2, /* segments; a (sequence, head) whose gate bound is under
-                        warmup_tol restarts each segment from zero
-                        warmup_chunks chunks early and skips M; the others
-                        run exactly */
+                        its tolerance (see tol_rule) restarts each segment
+                        from zero up to warmup_chunks chunks early and skips
+                        M; the others run exactly */
   GDN_CP_AUTO = 3    /* WARMUP when n_seqs * h_v < sm_count, else OFF */
 };
+
+/* How a warmup restart's tolerance is set [FlashQLA, "AutoCP": a restart is
+ * good once the state error it leaves is under the noise floor].
+ *   GDN_TOL_FIXED: warmup_tol, the same for every head and segment.
+ *   GDN_TOL_NOISE: per (sequence, value head) and segment, the larger of
+ *     warmup_tol and the noise floor of the exact bf16 path at the segment
+ *     start: the fp16 rounding of the state operand in every chunk (relative
+ *     2^-11) carried to the start, 2^-11 * (1 + sum over m = 1..w of
+ *     min(1, the bound of the last m chunks before the start)), w =
+ *     min(warmup_chunks, 8, chunks before the start); so at most 9 * 2^-11.  A head whose gates decay slowly carries more
+ *     of that rounding, so its floor, and the depth error it tolerates, is
+ *     higher; the warmup error stays below the error the exact path makes
+ *     anyway.  The fp32 path always combines exactly. */
+enum { GDN_TOL_FIXED = 0, GDN_TOL_NOISE = 1 };
 
 typedef struct gdn_dims {
   int B;      /* batch; must be 1 when cu_seqlens is used */
@@ -99,10 +113,12 @@ typedef struct gdn_cp_opts {
                         segment's chunks + 3) + (most segments of one sequence); ties go
                         to fewer segments */
   int warmup_chunks; /* warmup restart depth w in chunks; <= 0 selects 8 */
-  float warmup_tol;  /* accept warmup for a (sequence, head) when its bound
-                        max over segments of exp(sum g over the window) *
-                        prod max(1, |1 - beta ||k||^2|) is <= this; <= 0 selects 1e-4 */
+  float warmup_tol;  /* accept warmup for a (sequence, head) when, for every segment,
+                        some depth w <= warmup_chunks has its bound exp(sum over the w
+                        chunks before the segment of g + log max(1, |1 - beta ||k||^2|))
+                        <= the segment's tolerance (see tol_rule); <= 0 selects 1e-4 */
   int sm_count;      /* SMs to plan for; <= 0 queries the current device */
+  int tol_rule;      /* GDN_TOL_FIXED or GDN_TOL_NOISE (NULL opts: GDN_TOL_NOISE) */
 } gdn_cp_opts;
 
 /* Plain-data plan; fill with gdn_cp_plan, do not edit. */
@@ -115,6 +131,7 @@ typedef struct gdn_cp_plan_t {
   int warmup_chunks;
   float warmup_tol;
   int sm_count;
+  int tol_rule;         /* GDN_TOL_FIXED or GDN_TOL_NOISE */
   int n_seg_total;      /* segments summed over sequences */
   int max_seg_chunks;   /* longest segment, in chunks */
   int max_chunks;       /* longest sequence, in chunks */
@@ -134,7 +151,10 @@ typedef struct gdn_cp_plan_t {
  *   cu_seqlens_host   : n_seqs+1 non-decreasing token offsets starting at 0
  *                       and ending at T, or NULL for B fixed-length rows of T.
  *   opts              : may be NULL (all defaults: mode AUTO, lambda chosen by
- *                       the planner, warmup 8 chunks at 1e-4, SMs of the device).
+ *                       the planner, warmup up to 8 chunks at 1e-4 or the noise
+ *                       floor (GDN_TOL_NOISE), SMs of the device).  A tol_rule
+ *                       other than GDN_TOL_FIXED or GDN_TOL_NOISE is refused
+ *                       with GDN_ERR_UNSUPPORTED.
  *   out_plan          : written on success.
  * Segmentation of a sequence with N = ceil(len/64) chunks: L = max(1,
  * floor((isqrt(lambda_q8^2 * N) + 128) / 256)), n_seg = max(1, ceil(N / L)),

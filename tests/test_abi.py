@@ -41,11 +41,11 @@ def test_status_strings(lib):
     assert b"unknown" in lib.gdn_status_string(99)
 
 
-def plan(lib, T, h_qk=2, h_v=8, B=1, cu=None, mode=3, lam=1.0, w=8, tol=1e-4, sms=152, d=128, dtype=0):
+def plan(lib, T, h_qk=2, h_v=8, B=1, cu=None, mode=3, lam=1.0, w=8, tol=1e-4, sms=152, d=128, dtype=0, rule=1):
     from gated_deltanet_linear_fwd_gb300 import _lib as L
     n_seqs = B if cu is None else len(cu) - 1
     dims = L.gdn_dims(B, T, h_qk, h_v, d, d, n_seqs, 0.0, dtype)
-    opts = L.gdn_cp_opts(mode, lam, w, tol, sms)
+    opts = L.gdn_cp_opts(mode, lam, w, tol, sms, rule)
     out = L.gdn_cp_plan_t()
     arr = None if cu is None else (ctypes.c_int32 * len(cu))(*cu)
     st = lib.gdn_cp_plan(ctypes.byref(dims), arr, ctypes.byref(opts), ctypes.byref(out))
@@ -84,6 +84,12 @@ def test_plan_auto_mode(lib):
     assert st == 0 and p.mode == 0 and p.n_seg_total == 40  # 320 chains fill the GPU -> off
 
 
+def test_plan_records_the_tolerance_rule(lib):
+    for rule in (0, 1):
+        st, p = plan(lib, 32768, mode=2, rule=rule, tol=3e-4)
+        assert st == 0 and p.tol_rule == rule and abs(p.warmup_tol - 3e-4) < 1e-9
+
+
 def test_plan_workspace_layout(lib):
     st, p = plan(lib, 32768, h_v=8, mode=1)
     mat = 128 * 128 * 4
@@ -101,7 +107,7 @@ def test_plan_workspace_layout(lib):
 
 
 @pytest.mark.parametrize("kw,expect", [
-    (dict(d=64), 2), (dict(dtype=5), 2), (dict(mode=9), 2), (dict(h_v=0), 1),
+    (dict(d=64), 2), (dict(dtype=5), 2), (dict(mode=9), 2), (dict(rule=2), 2), (dict(rule=-1), 2), (dict(h_v=0), 1),
     (dict(cu=[0, 10, 5]), 1), (dict(cu=[1, 10]), 1), (dict(cu=[0, 9]), 1), (dict(B=2, cu=[0, 10]), 1)])
 def test_plan_rejects(lib, kw, expect):
     T = kw.get("cu", [0, 10])[-1] if "cu" in kw else 10

@@ -32,10 +32,10 @@ from gated_deltanet_linear_fwd_gb300.inputs import make_inputs, workload  # noqa
 DEV = "cuda:0"
 
 
-def run(w, mode="off", lambda_=0.0, warmup_chunks=8, warmup_tol=1e-4, h0=True):
+def run(w, mode="off", lambda_=0.0, warmup_chunks=8, warmup_tol=1e-4, h0=True, tol_rule="noise"):
     d = w.to(DEV)
     plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, cu_seqlens=w.cu_seqlens, mode=mode, lambda_=lambda_,
-                       warmup_chunks=warmup_chunks, warmup_tol=warmup_tol)
+                       warmup_chunks=warmup_chunks, warmup_tol=warmup_tol, tol_rule=tol_rule)
     ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=DEV)
     o, hT = gdn_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0 if h0 else None, d.cu_seqlens, plan=plan,
                           workspace=ws)
@@ -107,26 +107,47 @@ def test_exact_cp_invariant_to_segments():
         assert excess.max() <= util.TOL_BF16 * np.sqrt(np.mean(ro ** 2))
 
 
-def test_warmup_mode_matches_warmup_expectation():
-    """Warmup heads equal the oracle's warmup restart (per-segment depth by the
-    documented rule), other heads the exact result."""
-    w = make_inputs(64 * 40 + 9, h_qk=1, h_v=4, seed=10, g_kind="mix", with_h0=True)
-    o, hT, plan, ws = run(w, "warmup", 0.5, warmup_chunks=2, warmup_tol=1e-4)
+def _check_warmup(w, o, hT, plan, ws, wmax, rule):
+    """The head modes follow the documented rule; warmup heads equal the
+    oracle's warmup restart (per-segment depths by the rule), the others the
+    exact result; and all of it is within the tolerance of the exact oracle.
+    Returns the heads that took warmup."""
     modes, bounds = gdn_cp_head_modes(ws, plan)
-    fast = set(w.fast_heads)
-    depths = util.warmup_depths(w, plan.raw.lambda_q8, 2, 1e-4)
-    for jj in range(4):
+    depths = util.warmup_depths(w, plan.raw.lambda_q8, wmax, 1e-4, rule)
+    for jj in range(w.h_v):
         expect_warm = all(depths[(0, jj, s)] is not None for s in range(1, plan.n_seg_total))
-        assert expect_warm == (jj in fast)
-        assert int(modes[0, jj]) == (2 if expect_warm else 1), (modes, bounds, fast)
+        assert int(modes[0, jj]) == (2 if expect_warm else 1), (modes, bounds)
     f = util.to64
     segs = [util.segments(w.T, plan.raw.lambda_q8, False)]
-    warm_heads = {jj for jj in range(4) if int(modes[0, jj]) == 2}
+    warm_heads = {jj for jj in range(w.h_v) if int(modes[0, jj]) == 2}
     wd = {key: (v if v is not None else 0) for key, v in depths.items()}
     ro, rh = chunked.gdn_fwd_chunked(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0), [0, w.T],
                                      segments=segs, warmup_chunks=wd, warmup_heads=warm_heads)
     check(o, hT, (ro, rh), "warmup vs warmup-oracle")
     check(o, hT, oracle.recurrence(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0)), "warmup vs exact")
+    return warm_heads
+
+
+@pytest.mark.parametrize("rule", ["fixed", "noise"])
+def test_warmup_mode_matches_warmup_expectation(rule):
+    """Fast-decay heads take warmup under either tolerance rule, slow ones run
+    exactly."""
+    w = make_inputs(64 * 40 + 9, h_qk=1, h_v=4, seed=10, g_kind="mix", with_h0=True)
+    o, hT, plan, ws = run(w, "warmup", 0.5, warmup_chunks=2, warmup_tol=1e-4, tol_rule=rule)
+    assert _check_warmup(w, o, hT, plan, ws, 2, rule) == set(w.fast_heads)
+
+
+def test_noise_floor_tolerance_accepts_a_moderate_decay():
+    """A decay of 0.02 a token (1.28 a chunk): six chunks bound the dropped
+    history by exp(-7.68) = 4.6e-4, over the fixed 1e-4 (which would need
+    eight) but under the noise floor 2^-11 (1 + sum of exp(-1.28 m), m = 1..6)
+    = 6.8e-4.  With a six-chunk window the fixed rule runs every head exactly,
+    the noise rule restarts them all, and both match the oracle."""
+    base = make_inputs(64 * 40 + 9, h_qk=1, h_v=3, seed=12, with_h0=True)
+    w = dataclasses.replace(base, g=torch.full_like(base.g, -0.02))
+    for rule, expect in (("fixed", set()), ("noise", {0, 1, 2})):
+        o, hT, plan, ws = run(w, "warmup", 0.5, warmup_chunks=6, warmup_tol=1e-4, tol_rule=rule)
+        assert _check_warmup(w, o, hT, plan, ws, 6, rule) == expect, rule
 
 
 def test_resume_split_call():
@@ -180,7 +201,8 @@ def test_parity_standard_workloads(name):
 
 def test_null_plan_options_are_the_documented_defaults():
     """gdn_cp_plan with NULL options: mode AUTO, lambda chosen by the planner,
-    warmup 8 chunks at 1e-4, the current device's SM count."""
+    warmup up to 8 chunks at 1e-4 or the noise floor, the current device's SM
+    count."""
     import ctypes
     from gated_deltanet_linear_fwd_gb300 import _lib as L
     lib = L.load()
@@ -190,9 +212,9 @@ def test_null_plan_options_are_the_documented_defaults():
         arr = (ctypes.c_int32 * len(cu))(*cu)
         got, want = L.gdn_cp_plan_t(), L.gdn_cp_plan_t()
         assert lib.gdn_cp_plan(ctypes.byref(dims), arr, None, ctypes.byref(got)) == 0
-        opts = L.gdn_cp_opts(L.GDN_CP_AUTO, 0.0, 8, 1e-4, sms)
+        opts = L.gdn_cp_opts(L.GDN_CP_AUTO, 0.0, 8, 1e-4, sms, L.GDN_TOL_NOISE)
         assert lib.gdn_cp_plan(ctypes.byref(dims), arr, ctypes.byref(opts), ctypes.byref(want)) == 0
-        for f in ("mode", "lambda_q8", "n_seg_total", "warmup_chunks", "sm_count", "workspace_bytes"):
+        for f in ("mode", "lambda_q8", "n_seg_total", "warmup_chunks", "sm_count", "workspace_bytes", "tol_rule"):
             assert getattr(got, f) == getattr(want, f), (cu, f)
         assert abs(got.warmup_tol - 1e-4) < 1e-9 and got.sm_count == sms
 

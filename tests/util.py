@@ -58,11 +58,14 @@ def to64(t):
     return None if t is None else t.detach().double().cpu().numpy()
 
 
-def warmup_depths(w, lambda_q8, wmax, tol):
+def warmup_depths(w, lambda_q8, wmax, tol, rule="fixed"):
     """Per (seq, head, segment) warmup depth by the documented rule: the
     smallest w <= wmax with sum over the w chunks before the segment of
-    g + log max(1, |1 - beta ||k||^2|) <= log(tol); a window reaching the
-    sequence start runs exactly; None when no depth qualifies."""
+    g + log max(1, |1 - beta ||k||^2|) <= log(the segment's tolerance); a
+    window reaching the sequence start runs exactly; None when no depth
+    qualifies.  The tolerance is tol ("fixed"), or ("noise") the larger of
+    tol and 2^-11 (1 + sum over m = 1..min(wmax, 8, chunks before) of
+    min(1, exp(sum over the last m chunks)))."""
     f = to64
     g, beta, k = f(w.g), f(w.beta), f(w.k)
     offs = w.seq_offsets()
@@ -74,13 +77,21 @@ def warmup_depths(w, lambda_q8, wmax, tol):
             i = (j * w.h_qk) // w.h_v
             kk = (k[bos:eos, i] ** 2).sum(-1)
             term = g[bos:eos, j] + np.log(np.maximum(1.0, np.abs(1.0 - beta[bos:eos, j] * kk)))
+            chunk = lambda c: term[c * 64:(c + 1) * 64].sum()
             for si, (cb, _) in enumerate(segs):
                 if si == 0:
                     continue
+                thr = math.log(tol)
+                if rule == "noise":
+                    acc, fl = 0.0, 1.0
+                    for m in range(1, min(wmax, 8, cb) + 1):
+                        acc += chunk(cb - m)
+                        fl += min(1.0, math.exp(acc))
+                    thr = max(thr, math.log(fl) - 11 * math.log(2.0))
                 acc, wsel = 0.0, None
                 for wd in range(1, min(wmax, cb) + 1):
-                    acc += term[(cb - wd) * 64:(cb - wd + 1) * 64].sum()
-                    if cb - wd == 0 or acc <= math.log(tol):
+                    acc += chunk(cb - wd)
+                    if cb - wd == 0 or acc <= thr:
                         wsel = wd
                         break
                 out[(n, j, si)] = wsel
