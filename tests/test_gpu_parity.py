@@ -237,3 +237,59 @@ def test_many_short_sequences(mode, lam):
     w, ref = _many_short()
     o, hT, plan, _ = run(w, mode, lam)
     check(o, hT, ref, f"many/{mode}/segments={plan.n_seg_total}")
+
+
+def _agree(a, b, scale, tag, tol):
+    """Two GPU results of the same value: at most one bf16 ulp apart (for bf16
+    outputs) plus tol * scale (computed on the device: these are large)."""
+    a, b = a.double(), b.double()
+    diff = (a - b).abs()
+    if tol == util.TOL_BF16:  # two bf16 half ulps at the larger magnitude (8 significant bits)
+        mag = torch.maximum(a.abs(), b.abs()).clamp_min(float(np.finfo(np.float32).tiny))
+        diff = (diff - 2 * torch.exp2(torch.floor(torch.log2(mag)) - 8)).clamp_min(0.0)
+    excess = float(diff.max()) / scale
+    print(f"{tag}: {excess:.3e}")
+    assert excess <= tol, f"{tag}: {excess:.3e}"
+
+
+def test_long_sequence_at_size():
+    """One sequence of 2^20 tokens (16384 chunks, h 1/2, h0 given), the
+    longest here: the prefix the oracle can follow token by token matches it in
+    every mode, the modes agree with each other on all of o and on the final
+    state, and a call split at an unaligned token resumes to the same result."""
+    T, P = 1 << 20, 64 * 64 + 13
+    w = make_inputs(T, h_qk=1, h_v=2, seed=31, with_h0=True)
+    f = util.to64
+    ro, _ = oracle.recurrence(f(w.q[:P]), f(w.k[:P]), f(w.v[:P]), f(w.g[:P]), f(w.beta[:P]), f(w.h0),
+                              want_state=False)
+    outs = {}
+    for mode in ("off", "exact", "auto"):
+        o, hT, plan, _ = run(w, mode)
+        excess, raw = util.parity_bf16(o[:P], ro)
+        print(f"2^20 {mode} (segments {plan.n_seg_total}): prefix excess {excess:.3e} raw {raw:.3e}")
+        assert excess <= util.TOL_BF16, (mode, excess)
+        outs[mode] = (o, hT)
+    o0, h0 = outs["off"]
+    so = float(o0.double().pow(2).mean().sqrt())
+    sh = float(h0.double().pow(2).mean().sqrt())
+    for mode in ("exact", "auto"):
+        _agree(outs[mode][0], o0, so, f"o {mode} vs off", util.TOL_BF16)
+        _agree(outs[mode][1], h0, sh, f"final state {mode} vs off", util.TOL_STATE)
+    d = w.to(DEV)
+    m = 64 * 9000 + 29  # copies: a slice starting at an odd token is not 16-byte aligned for g, beta
+    o1, h1 = gdn_chunk_fwd(d.q[:m].clone(), d.k[:m].clone(), d.v[:m].clone(), d.g[:m].clone(),
+                           d.beta[:m].clone(), d.h0)
+    o2, h2 = gdn_chunk_fwd(d.q[m:].clone(), d.k[m:].clone(), d.v[m:].clone(), d.g[m:].clone(),
+                           d.beta[m:].clone(), h1)
+    _agree(torch.cat([o1, o2]), o0, so, "o resumed vs one call", util.TOL_BF16)
+    _agree(h2, h0, sh, "final state resumed vs one call", util.TOL_STATE)
+
+
+@pytest.mark.parametrize("mode", ["off", "exact", "auto"])
+def test_many_heads(mode):
+    """64 value heads on 32 query/key heads, two ragged sequences."""
+    w = make_inputs(cu_seqlens=[0, 300, 1037], h_qk=32, h_v=64, seed=32, with_h0=True)
+    o, hT, plan, _ = run(w, mode)
+    f = util.to64
+    ref = oracle.recurrence(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0), w.seq_offsets())
+    check(o, hT, ref, f"h 32/64 {mode} segments={plan.n_seg_total}")
