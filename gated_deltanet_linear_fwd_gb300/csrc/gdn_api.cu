@@ -101,20 +101,29 @@ namespace {
 
 constexpr int kCtaOverheadChunks = 3;
 
+// The model's constants per path.  The bf16 scan: a CTA costs its chunks + 3
+// (start-up, pipeline fill, warmup) and a combine step about half a chunk.
+// The fp32 path: a chunk is ~40x a combine step and the start-up is small
+// against a chunk, so both count zero; its chains run two CTAs per SM.
+struct PlanModel {
+  int overhead;     // chunk-times a CTA costs beyond its chunks
+  bool combine;     // count the combine's serial steps
+};
+
 struct SegStats {
   int64_t segs = 0;
   int longest = 0, most_segs = 0;
   int64_t work = 0;  // sum of (chunks + overhead) over one head's segments
 };
 
-SegStats seg_stats(const gdn_dims* d, const int32_t* cu, int q8) {
+SegStats seg_stats(const gdn_dims* d, const int32_t* cu, int q8, const PlanModel& m) {
   SegStats r;
   for (int n = 0; n < d->n_seqs; ++n) {
     const int64_t len = cu ? (int64_t)cu[n + 1] - cu[n] : d->T;
     const int N = chunks_of(len);
     const int ns = seg_count(N, q8, false);
     r.segs += ns;
-    r.work += N + (int64_t)ns * kCtaOverheadChunks;
+    r.work += N + (int64_t)ns * m.overhead;
     r.longest = std::max(r.longest, (N + ns - 1) / ns);  // balanced split: ceil(N / ns) at most
     r.most_segs = std::max(r.most_segs, ns);
   }
@@ -127,8 +136,8 @@ SegStats seg_stats(const gdn_dims* d, const int32_t* cu, int q8) {
 // scan; the finish is at most total / sm_count + the longest CTA (the list
 // scheduling bound), which sizes the count array.
 int64_t list_schedule(const gdn_dims* d, const int32_t* cu, int q8, int sm_count, const SegStats& st,
-                      std::vector<int32_t>& free_at) {
-  const int64_t horizon = st.work * d->h_v / sm_count + st.longest + kCtaOverheadChunks + 2;
+                      const PlanModel& m, std::vector<int32_t>& free_at) {
+  const int64_t horizon = st.work * d->h_v / sm_count + st.longest + m.overhead + 2;
   free_at.assign((size_t)horizon, 0);
   free_at[0] = sm_count;
   int64_t t = 0, finish = 0;
@@ -140,7 +149,7 @@ int64_t list_schedule(const gdn_dims* d, const int32_t* cu, int q8, int sm_count
       for (int s = 0; s < ns; ++s) {
         while (free_at[(size_t)t] == 0) ++t;
         --free_at[(size_t)t];
-        const int64_t end = t + seg_first(s + 1, N, ns) - seg_first(s, N, ns) + kCtaOverheadChunks;
+        const int64_t end = t + seg_first(s + 1, N, ns) - seg_first(s, N, ns) + m.overhead;
         ++free_at[(size_t)end];
         finish = std::max(finish, end);
       }
@@ -150,18 +159,18 @@ int64_t list_schedule(const gdn_dims* d, const int32_t* cu, int q8, int sm_count
 
 }  // namespace
 
-int pick_lambda_q8_uncached(const gdn_dims* d, const int32_t* cu, int sm_count) {
+int pick_lambda_q8_uncached(const gdn_dims* d, const int32_t* cu, int slots, const PlanModel& m) {
   int best_q8 = 256;
   int64_t best_cost = INT64_MAX, best_segs = INT64_MAX;
   std::vector<int32_t> free_at;
   for (int q8 = 32; q8 <= 4096; q8 += 32) {
-    const SegStats st = seg_stats(d, cu, q8);
-    // in half chunk-times; no schedule ends before its longest CTA or the average SM load
+    const SegStats st = seg_stats(d, cu, q8, m);
+    const int64_t comb = m.combine ? st.most_segs : 0;
+    // in half chunk-times; no schedule ends before its longest CTA or the average slot load
     const int64_t total = st.work * d->h_v;
-    const int64_t lower =
-        2 * std::max<int64_t>(st.longest + kCtaOverheadChunks, (total + sm_count - 1) / sm_count) + st.most_segs;
+    const int64_t lower = 2 * std::max<int64_t>(st.longest + m.overhead, (total + slots - 1) / slots) + comb;
     if (lower > best_cost || (lower == best_cost && st.segs >= best_segs)) continue;
-    const int64_t cost = 2 * list_schedule(d, cu, q8, sm_count, st, free_at) + st.most_segs;
+    const int64_t cost = 2 * list_schedule(d, cu, q8, slots, st, m, free_at) + comb;
     if (cost < best_cost || (cost == best_cost && st.segs < best_segs)) {
       best_cost = cost;
       best_segs = st.segs;
@@ -171,11 +180,12 @@ int pick_lambda_q8_uncached(const gdn_dims* d, const int32_t* cu, int sm_count) 
   return best_q8;
 }
 
-// The choice depends only on the sequence lengths, h_v and the SM count; a
-// model plans the same lengths once per layer, so recent choices are kept.
+// The choice depends only on the sequence lengths, h_v, the SM count and the
+// path; a model plans the same lengths once per layer, so recent choices are
+// kept.
 int pick_lambda_q8(const gdn_dims* d, const int32_t* cu, int sm_count) {
   struct Entry {
-    int h_v, sm_count;
+    int h_v, sm_count, dtype;
     std::vector<int64_t> lens;
     int q8;
   };
@@ -186,12 +196,14 @@ int pick_lambda_q8(const gdn_dims* d, const int32_t* cu, int sm_count) {
   {
     std::lock_guard<std::mutex> lk(mu);
     for (const Entry& e : recent)
-      if (e.h_v == d->h_v && e.sm_count == sm_count && e.lens == lens) return e.q8;
+      if (e.h_v == d->h_v && e.sm_count == sm_count && e.dtype == d->dtype && e.lens == lens) return e.q8;
   }
-  const int q8 = pick_lambda_q8_uncached(d, cu, sm_count);
+  const bool f32 = d->dtype == GDN_F32;
+  const PlanModel m = f32 ? PlanModel{0, false} : PlanModel{kCtaOverheadChunks, true};
+  const int q8 = pick_lambda_q8_uncached(d, cu, f32 ? 2 * sm_count : sm_count, m);
   std::lock_guard<std::mutex> lk(mu);
   if (recent.size() >= 8) recent.erase(recent.begin());
-  recent.push_back(Entry{d->h_v, sm_count, std::move(lens), q8});
+  recent.push_back(Entry{d->h_v, sm_count, d->dtype, std::move(lens), q8});
   return q8;
 }
 

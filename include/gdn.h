@@ -111,7 +111,10 @@ typedef struct gdn_cp_opts {
                         multiple of 1/8) minimising 2 x (finish of the list schedule of
                         the scan's CTAs in launch order on sm_count SMs, each taking its
                         segment's chunks + 3) + (most segments of one sequence); ties go
-                        to fewer segments */
+                        to fewer segments.  For GDN_F32, whose chains run two CTAs per
+                        SM and whose chunks dwarf a combine step, the schedule has 2 x
+                        sm_count slots, a CTA takes its chunks alone, and the score is
+                        2 x the finish */
   int warmup_chunks; /* warmup restart depth w in chunks; <= 0 selects 8 */
   float warmup_tol;  /* accept warmup for a (sequence, head) when, for every segment,
                         some depth w <= warmup_chunks has its bound exp(sum over the w

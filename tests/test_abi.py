@@ -175,9 +175,14 @@ def test_binding_fails_loudly_without_library(tmp_path):
                                         ([0, 4096, 20480, 86016, 348160], 8, 152),
                                         ([0, 100000, 100100, 160000], 4, 148)])
 def test_plan_automatic_lambda(lib, cu, h_v, sms):
+    lens = [cu[n + 1] - cu[n] for n in range(len(cu) - 1)]
     st, p = plan(lib, cu[-1], h_v=h_v, cu=cu, mode=2, lam=0.0, sms=sms)
     assert st == 0
-    assert p.lambda_q8 == util.auto_lambda_q8([cu[n + 1] - cu[n] for n in range(len(cu) - 1)], h_v, sms)
+    assert p.lambda_q8 == util.auto_lambda_q8(lens, h_v, sms)
+    # the fp32 path: two CTAs per SM, no per-CTA overhead, no combine term
+    st, p = plan(lib, cu[-1], h_v=h_v, cu=cu, mode=1, lam=0.0, sms=sms, dtype=1)
+    assert st == 0
+    assert p.lambda_q8 == util.auto_lambda_q8(lens, h_v, 2 * sms, overhead=0, combine=False)
 
 
 def test_device_status_decoding():

@@ -98,13 +98,14 @@ def warmup_depths(w, lambda_q8, wmax, tol, rule="fixed"):
     return out
 
 
-def auto_lambda_q8(T_list, h_v, sm_count):
+def auto_lambda_q8(T_list, h_v, sm_count, overhead=3, combine=True):
     """The planner's automatic lambda, restated from its documented rule:
-    among lambda = k/8 (k = 1..128) take the smallest (finish of the list
-    schedule of the scan's CTAs + half the largest segment count of a
-    sequence), ties to fewer segments.  The schedule: launch order (the
-    segments of every sequence, head after head), each CTA taking segment
-    chunks + 3 on the first SM to free up."""
+    among lambda = k/8 (k = 1..128) take the smallest (2 x finish of the list
+    schedule of the scan's CTAs + the largest segment count of a sequence),
+    ties to fewer segments.  The schedule: launch order (the segments of every
+    sequence, head after head), each CTA taking segment chunks + overhead on
+    the first of sm_count slots to free up.  The fp32 path: 2 x SMs slots, no
+    overhead, no combine term."""
     best = None
     for q8 in range(32, 4097, 32):
         seglists = [segments(n_tok, q8, False) for n_tok in T_list]
@@ -113,8 +114,9 @@ def auto_lambda_q8(T_list, h_v, sm_count):
             for sg in seglists:
                 for a, b in sg:
                     i = min(range(sm_count), key=free.__getitem__)
-                    free[i] += b - a + 3
-        key = (2 * max(free) + max(len(sg) for sg in seglists), sum(len(sg) for sg in seglists))
+                    free[i] += b - a + overhead
+        comb = max(len(sg) for sg in seglists) if combine else 0
+        key = (2 * max(free) + comb, sum(len(sg) for sg in seglists))
         if best is None or key < best[0]:
             best = (key, q8)
     return best[1]
