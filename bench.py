@@ -14,7 +14,9 @@ an independent replica (the layer needs no collective) and the slowest
 rank's time is used.
 
 The line also carries, for every workload: its time and roofline fraction;
-the fp32 path's time on the headline workload; the host planning time; and,
+the AutoCP modes of the varlen workload (time and distance from exact); the
+decode step over a batch of 256 states; the fp32 path's time on the headline
+workload; the host planning time; and,
 from the CPU-baseline leg (which runs the float64 oracle on the host cores
 anyway), the raw max|diff|/RMS of o and of the final state against the
 oracle and the excess over bf16's half-ulp store rounding.
