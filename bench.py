@@ -47,7 +47,7 @@ if ROOT not in sys.path:
 
 METRIC = "GDN chunked-prefill fwd tokens/s at T=32768 (h_qk/h_v sweep); % of roofline"
 HEADLINE = "T32768_h2x8"
-SWEEP = ["T32768_h8x24_h0", "T32768_h16x16", "varlen4_T348160_h2x8"]
+SWEEP = ["T32768_h8x24_h0", "T32768_h16x16", "varlen4_T348160_h2x8", "batch8_T4096_h8x32"]
 # FlashQLA on an NVIDIA H200, same workloads (pages' benchmark table), ms per call.
 PAGES_H200_MS = {"T32768_h2x8": 0.310, "T32768_h8x24_h0": 0.659, "T32768_h16x16": 0.493}
 FLUSH_BYTES = 256 << 20

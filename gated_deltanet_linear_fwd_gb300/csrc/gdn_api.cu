@@ -444,6 +444,10 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
   p.scale = dims->scale != 0.f ? dims->scale : 1.0f / std::sqrt((float)dims->d_k);
   p.elem_f32 = dims->dtype == GDN_F32;
   p.plan_mode = plan->mode == GDN_CP_OFF ? kModeOff : (plan->mode == GDN_CP_EXACT ? kModeExact : kModeWarmup);
+  // a plan in which every sequence is one segment has nothing to combine: it
+  // runs without the preprocessing and the combine
+  const bool cp = plan->mode != GDN_CP_OFF && plan->n_seg_total > plan->n_seqs;
+  if (!cp) p.plan_mode = kModeOff;
   p.lambda_q8 = plan->lambda_q8;
   p.warmup_chunks = plan->warmup_chunks;
   p.log_tol = std::log(plan->warmup_tol);
@@ -485,7 +489,7 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
     // fp32 inputs: the recurrence on the CUDA cores, in fp32; a context-parallel
     // plan always combines its segments exactly (no warmup restarts)
     LaunchLog log;
-    if (plan->mode != GDN_CP_OFF) {
+    if (cp) {
       p.plan_mode = kModeExact;
       if ((e = log.before(cs)) != cudaSuccess || (e = launch_f32_prep(p, cs)) != cudaSuccess ||
           (e = log.after("recurrence_f32_prep", cs)) != cudaSuccess)
@@ -495,7 +499,7 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
         return cuda_fail(e);
     }
     if ((e = log.before(cs)) != cudaSuccess ||
-        (e = launch_recurrence_f32(p, cs, plan->mode != GDN_CP_OFF)) != cudaSuccess ||
+        (e = launch_recurrence_f32(p, cs, cp)) != cudaSuccess ||
         (e = log.after("recurrence_f32", cs)) != cudaSuccess)
       return cuda_fail(e);
     return GDN_OK;
@@ -518,7 +522,7 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
   if ((e = log.before(cs)) != cudaSuccess || (e = launch_wy(p, mq, mk, mv, cs, cu_dev != nullptr)) != cudaSuccess ||
       (e = log.after("wy", cs)) != cudaSuccess)
     return cuda_fail(e);
-  if (plan->mode != GDN_CP_OFF) {
+  if (cp) {
     if ((e = log.before(cs)) != cudaSuccess || (e = launch_scan_prep(p, mq, mk, cs)) != cudaSuccess ||
         (e = log.after("scan_prep", cs)) != cudaSuccess)
       return cuda_fail(e);
@@ -600,9 +604,11 @@ gdn_status gdn_cp_head_modes(const void* workspace, const gdn_cp_plan_t* plan, i
                              void* stream) {
   if (!workspace || !plan) return GDN_ERR_INVALID_ARG;
   const size_t heads = (size_t)plan->n_seqs * plan->h_v;
-  if (plan->mode == GDN_CP_OFF || plan->dtype == GDN_F32) {  // no warmup decision taken
+  if (plan->mode == GDN_CP_OFF || plan->dtype == GDN_F32 || plan->n_seg_total <= plan->n_seqs) {
+    // no warmup decision taken: no context parallelism, the fp32 path (always
+    // exact), or one segment per sequence (nothing to combine or restart)
     for (size_t i = 0; i < heads; ++i) {
-      if (modes) modes[i] = plan->mode == GDN_CP_OFF ? GDN_CP_OFF : GDN_CP_EXACT;
+      if (modes) modes[i] = plan->mode == GDN_CP_OFF ? GDN_CP_OFF : plan->dtype == GDN_F32 ? GDN_CP_EXACT : plan->mode;
       if (bounds) bounds[i] = -INFINITY;
     }
     return GDN_OK;

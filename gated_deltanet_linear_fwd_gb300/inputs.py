@@ -105,8 +105,9 @@ def make_inputs(n_tokens: int | None = None, h_qk: int = 2, h_v: int = 4, seed: 
                     h_qk, h_v, fast)
 
 
-# The five standard workloads: the tiny parity case, the three 1 x 32768 rows
-# of the pages' benchmark table, and a long packed varlen batch.
+# The standard workloads: the tiny parity case, the three 1 x 32768 rows of
+# the pages' benchmark table, a long packed varlen batch, and a batch of 8
+# sequences x 32 value heads that fills the GPU without context parallelism.
 WORKLOADS = {
     "tiny_T512_h2x4": dict(n_tokens=512, h_qk=2, h_v=4, seed=0, g_kind="tiny"),
     "T32768_h2x8": dict(n_tokens=32768, h_qk=2, h_v=8, seed=1, g_kind="mix"),
@@ -114,6 +115,8 @@ WORKLOADS = {
     "T32768_h16x16": dict(n_tokens=32768, h_qk=16, h_v=16, seed=3, g_kind="mix"),
     "varlen4_T348160_h2x8": dict(cu_seqlens=[0, 262144, 327680, 344064, 348160], h_qk=2, h_v=8,
                                  seed=4, g_kind="mix"),
+    # a batch wide enough to fill the GPU without context parallelism (8 x 32 = 256 chains)
+    "batch8_T4096_h8x32": dict(cu_seqlens=[4096 * i for i in range(9)], h_qk=8, h_v=32, seed=5, g_kind="mix"),
 }
 
 

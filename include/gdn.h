@@ -216,7 +216,8 @@ gdn_status gdn_get_device_status(const void* workspace, void* stream, int* code,
  * gdn_cp_head_modes -- diagnostics: synchronises `stream` and copies, per
  * (sequence, value head), the mode the last gdn_chunk_fwd on this workspace
  * took (GDN_CP_EXACT or GDN_CP_WARMUP; GDN_CP_OFF for plans without CP; always
- * GDN_CP_EXACT on the fp32 path with CP) and
+ * GDN_CP_EXACT on the fp32 path with CP; the plan's mode when every sequence
+ * is a single segment, where nothing is combined or restarted) and
  * the natural log of its warmup error bound (-inf when no segment needs one).
  *   modes_host    : host int32 [n_seqs * h_v], or NULL.
  *   log_bound_host: host fp32 [n_seqs * h_v], or NULL.

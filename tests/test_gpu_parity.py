@@ -3,7 +3,7 @@
 Bar (bf16 I/O, fp32 accumulation): for o, max|diff| <= 2e-2 * RMS(ref) after
 allowing the half-ulp the bf16 store itself must add; for the fp32 final
 state, max|diff| <= 2e-2 * RMS(ref).  Small cases are compared element by
-element; the five standard workloads at full size in the bench's launch
+element; the standard workloads at full size in the bench's launch
 configuration are compared element by element as well (the oracle runs a
 1 x 32768 head in well under a second).
 """
@@ -188,7 +188,7 @@ def test_empty_batch_copies_state():
 
 
 @pytest.mark.parametrize("name", ["tiny_T512_h2x4", "T32768_h2x8", "T32768_h8x24_h0", "T32768_h16x16",
-                                  "varlen4_T348160_h2x8"])
+                                  "varlen4_T348160_h2x8", "batch8_T4096_h8x32"])
 def test_parity_standard_workloads(name):
     """Full-size workloads in the bench's launch configuration (AutoCP)."""
     w = workload(name)
