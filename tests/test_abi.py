@@ -199,3 +199,26 @@ def test_debug_stall_hook_is_exported_and_settable(lib):
     assert lib.gdn_debug_stall_ns(0) == 0
     assert lib.gdn_debug_stall_ns(1000) == 0
     assert lib.gdn_debug_stall_ns(0) == 0
+
+
+def test_head_modes_without_a_device_decision(lib):
+    """Plans whose heads take no on-device decision report their modes from the
+    plan alone, without touching the workspace (a dummy, never-dereferenced
+    pointer here): no context parallelism (off), the fp32 path (exact), and a
+    plan in which every sequence is one segment (the plan's mode)."""
+    from gated_deltanet_linear_fwd_gb300 import _lib as L
+    A = ctypes.c_void_p(0x100000)
+    cases = [(dict(mode=0), 0), (dict(mode=1, dtype=1, lam=0.5), 1),
+             (dict(mode=1, cu=[0, 60, 120]), 1), (dict(mode=2, cu=[0, 60, 120]), 2)]
+    for kw, want in cases:
+        cu = kw.pop("cu", None)
+        T = cu[-1] if cu else 32768
+        st, p = plan(lib, T, h_v=4, cu=cu, **kw)
+        assert st == 0
+        if cu:
+            assert p.n_seg_total == p.n_seqs  # one chunk a sequence: one segment each
+        n = p.n_seqs * p.h_v
+        modes, bounds = (ctypes.c_int32 * n)(), (ctypes.c_float * n)()
+        assert lib.gdn_cp_head_modes(A, ctypes.byref(p), modes, bounds, None) == 0
+        assert list(modes) == [want] * n, (kw, list(modes))
+        assert all(b == float("-inf") for b in bounds)

@@ -293,3 +293,17 @@ def test_many_heads(mode):
     f = util.to64
     ref = oracle.recurrence(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0), w.seq_offsets())
     check(o, hT, ref, f"h 32/64 {mode} segments={plan.n_seg_total}")
+
+
+def test_single_segment_plans_run_as_off():
+    """When every sequence is one segment, exact and warmup plans have nothing
+    to combine or restart: they run the same kernels as no context parallelism
+    and give the same bits, and the oracle's result."""
+    w = make_inputs(cu_seqlens=[0, 60, 100, 164, 164], h_qk=1, h_v=2, seed=33, with_h0=True)
+    runs = {mode: run(w, mode, 1.0) for mode in ("off", "exact", "warmup")}
+    for mode in ("exact", "warmup"):
+        assert runs[mode][2].n_seg_total == w.n_seqs
+        assert torch.equal(runs[mode][0], runs["off"][0]) and torch.equal(runs[mode][1], runs["off"][1])
+    f = util.to64
+    check(*runs["off"][:2], oracle.recurrence(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0), w.seq_offsets()),
+          "single-segment plans")
