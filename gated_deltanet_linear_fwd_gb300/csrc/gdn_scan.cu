@@ -13,8 +13,8 @@
 //     writes o and, for a sequence's last segment, the final state.
 //   scan_kernel<true>   (context-parallel preprocessing, section "AutoCP",
 //     the correction term M): for an exact-mode (sequence, head) segment,
-//     blockIdx.z = 0 runs the segment's transition (the state started at the
-//     identity with no value input, giving M^T) and blockIdx.z = 1 its local
+//     chain 0 runs the segment's transition (the state started at the
+//     identity with no value input, giving M^T) and chain 1 its local
 //     state (started at zero).
 //
 // Everything chunk-local (the gate cumsum, the WY form, P) comes from the
@@ -584,8 +584,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1024-byte aligned
   Ctl* ctl = reinterpret_cast<Ctl*>(sm + kSmCtl);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the preprocessing's two chains of a segment are neighbouring blocks
+  // (x = 2 segment + chain), so both of a head's chains come in the same wave
   const int j = blockIdx.y;
-  const int chain = PREP ? (int)blockIdx.z : 0;
+  const int chain = PREP ? (int)(blockIdx.x & 1) : 0;
+  const int seg = PREP ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int n_segs = PREP ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   // ---- which chain this CTA runs ----
   // The segment comes from the plan's arithmetic and the sequence bounds (an
   // input), so warps 0 and 1 locate it before waiting for the kernel before
@@ -597,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_mode, s_w, s_exact;
   SegInfo si0;
   bool ok0 = false;
-  if (warp < 2) ok0 = locate_segment(p, blockIdx.x, si0);
+  if (warp < 2) ok0 = locate_segment(p, seg, si0);
   if (tid == 64) {  // the barriers and tensor maps, also before the wait
     const int counts[kNumBars] = {1, 1, 1, 1, 1, 1, 1, 1, 1, kChainThreads, 1, kChainThreads,
                                   1, 1, kOutThreads, kOutThreads, 1, 1, kConvertWarps, kConvertWarps,
@@ -660,8 +664,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) report(p.status, kDevCheck, kDetSegMismatch);
     return;
   }
-  if (blockIdx.x == gridDim.x - 1 && !(si.n == p.n_seqs - 1 && si.s == si.n_seg - 1)) {
-    if (tid == 0 && blockIdx.y == 0 && blockIdx.z == 0) report(p.status, kDevCheck, kDetSegMismatch);
+  if (seg == n_segs - 1 && !(si.n == p.n_seqs - 1 && si.s == si.n_seg - 1)) {
+    if (tid == 0 && blockIdx.y == 0 && chain == 0) report(p.status, kDevCheck, kDetSegMismatch);
   }
   Chain ch;
   ch.bos = si.bos;
@@ -760,7 +764,7 @@ cudaError_t scan_kernel_setup() {
 }
 
 cudaError_t launch_scan_prep(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, cudaStream_t st) {
-  dim3 grid(p.n_seg_total, p.h_v, 2);
+  dim3 grid(2 * p.n_seg_total, p.h_v);
   return launch_kernel(scan_kernel<true>, grid, dim3(kThreads), kSmemAlloc, st, true, mq, mk, mq,
                        p);  // writes no output: o's map unused
 }
