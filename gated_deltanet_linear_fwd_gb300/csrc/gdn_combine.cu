@@ -36,7 +36,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
   __shared__ SegInfo s_seq;
   __shared__ uint64_t s_bar[2];
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int n = blockIdx.x, j = blockIdx.y, r0 = blockIdx.z * kRows;
+  // x = row block + (kDim / kRows) * sequence: a (sequence, head)'s row blocks
+  // are neighbouring blocks, so they come in the same wave
+  constexpr int kBlocks = kDim / kRows;
+  const int n = (int)(blockIdx.x / kBlocks), j = blockIdx.y, rb = (int)(blockIdx.x % kBlocks), r0 = rb * kRows;
   __shared__ int s_mode, s_skip;
   // the sequence's segments come from the plan's arithmetic and the sequence
   // bounds (an input): located while the kernel before this one finishes
@@ -52,7 +55,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
       s_skip = st;
       s_seq = si;
       s_mode = mode;
-      if (blockIdx.z == 0 && !st) {
+      if (rb == 0 && !st) {
         p.head_mode[n * p.h_v + j] = mode;
         p.head_bound[n * p.h_v + j] = bound;
       }
@@ -178,8 +181,10 @@ cudaError_t combine_kernel_setup() {
 cudaError_t launch_combine(const Problem& p, int sm_count, cudaStream_t st) {
   // 32 CTAs of 4 rows per exact (sequence, head) if even all pairs fit in about two waves
   if ((int64_t)p.n_seqs * p.h_v * 32 <= 2 * (int64_t)sm_count)
-    return launch_kernel(combine_kernel<4>, dim3(p.n_seqs, p.h_v, kDim / 4), dim3(256), combine_smem<4>(), st, true, p);
-  return launch_kernel(combine_kernel<8>, dim3(p.n_seqs, p.h_v, kDim / 8), dim3(256), combine_smem<8>(), st, true, p);
+    return launch_kernel(combine_kernel<4>, dim3(p.n_seqs * (kDim / 4), p.h_v), dim3(256), combine_smem<4>(), st, true,
+                         p);
+  return launch_kernel(combine_kernel<8>, dim3(p.n_seqs * (kDim / 8), p.h_v), dim3(256), combine_smem<8>(), st, true,
+                       p);
 }
 
 }  // namespace gdn
