@@ -8,6 +8,9 @@ it.
 * ``chunked``          -- the chunked closed form and the context-parallel
                           combine (numpy), used to pin the recurrence and to
                           give warmup-mode expectations.
+* ``backward``         -- gradients of the forward: autograd of the token
+                          recurrence (the definition) and the chunk-level
+                          derivation the GPU backward follows (numpy).
 """
 from __future__ import annotations
 
