@@ -116,6 +116,59 @@ def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
     return out, final_state
 
 
+def gdn_bwd_workspace_bytes(plan: Plan) -> int:
+    """Device workspace bytes gdn_chunk_bwd needs for `plan` (gdn_bwd_workspace_bytes)."""
+    n = ctypes.c_size_t(0)
+    L.check(L.load().gdn_bwd_workspace_bytes(ctypes.byref(plan.raw), ctypes.byref(n)), "gdn_bwd_workspace_bytes")
+    return int(n.value)
+
+
+def gdn_chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+                  d_out: torch.Tensor, initial_state: Optional[torch.Tensor] = None,
+                  d_final_state: Optional[torch.Tensor] = None, cu_seqlens: Optional[torch.Tensor] = None,
+                  *, plan: Optional[Plan] = None, grads=None, workspace: Optional[torch.Tensor] = None,
+                  stream=None, scale: float = 0.0, mode: str = "auto", lambda_: float = 0.0,
+                  want_initial_state_grad: bool = True):
+    """Gradients of sum(o * d_out) + sum(final_state * d_final_state) (gdn_chunk_bwd).
+
+    Inputs as gdn_chunk_fwd (bf16 q/k/v); d_out like v (bf16); d_final_state
+    [N, h_v, 128, 128] fp32 or None.  grads: optional preallocated
+    (dq, dk, dv, dg, dbeta, dh0).  Returns (dq, dk, dv, dg, dbeta, dh0 or None).
+    """
+    batched = q.dim() == 4
+    B = q.shape[0] if batched else 1
+    T = q.shape[-3]
+    h_qk, h_v = q.shape[-2], v.shape[-2]
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("d_out", d_out)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if q.dtype != torch.bfloat16 or d_out.dtype != torch.bfloat16:
+        raise ValueError("the backward takes bf16 q/k/v and d_out")
+    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise ValueError("g and beta must be float32")
+    for name, t in (("initial_state", initial_state), ("d_final_state", d_final_state)):
+        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
+            raise ValueError(f"{name} must be contiguous float32")
+    if plan is None:
+        plan = gdn_cp_plan(T=T, h_qk=h_qk, h_v=h_v, B=B, cu_seqlens=cu_seqlens, dtype=q.dtype, mode=mode,
+                           lambda_=lambda_, scale=scale)
+    dims = L.gdn_dims(B, T, h_qk, h_v, q.shape[-1], v.shape[-1], plan.raw.n_seqs, scale, _DT.get(q.dtype, -1))
+    if grads is None:
+        dh0 = (torch.empty(plan.raw.n_seqs, h_v, 128, 128, dtype=torch.float32, device=q.device)
+               if want_initial_state_grad else None)
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(g),
+                 torch.empty_like(beta), dh0)
+    dq, dk, dv, dg, dbeta, dh0 = grads
+    if workspace is None:
+        workspace = torch.empty(max(gdn_bwd_workspace_bytes(plan), 256), dtype=torch.uint8, device=q.device)
+    st = L.load().gdn_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                                _ptr(cu_seqlens), _ptr(d_out), _ptr(d_final_state), _ptr(dq), _ptr(dk), _ptr(dv),
+                                _ptr(dg), _ptr(dbeta), _ptr(dh0), ctypes.byref(dims), ctypes.byref(plan.raw),
+                                _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    L.check(st, "gdn_chunk_bwd")
+    return dq, dk, dv, dg, dbeta, dh0
+
+
 def gdn_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
                     state: torch.Tensor, *, out: Optional[torch.Tensor] = None, scale: float = 0.0, stream=None):
     """One new token per sequence (gdn_decode_step): q,k [B,h_qk,128], v [B,h_v,128]

@@ -28,7 +28,10 @@ thread_local const char* g_last_names[kMaxTrace / 2];
 thread_local int g_last_count = 0;
 
 struct LaunchLog {
-  LaunchLog() { g_last_count = 0; }
+  // keep: continue the list of the call's kernels (the backward after its forward)
+  explicit LaunchLog(bool keep = false) {
+    if (!keep) g_last_count = 0;
+  }
   // Records the start event of the next kernel on st.
   cudaError_t before(cudaStream_t st) {
     const int k = 2 * g_last_count;
@@ -396,10 +399,15 @@ gdn_status gdn_cp_plan(const gdn_dims* dims, const int32_t* cu, const gdn_cp_opt
   return GDN_OK;
 }
 
-gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                         const float* initial_state, const int32_t* cu_dev, void* out, float* final_state,
-                         const gdn_dims* dims, const gdn_cp_plan_t* plan, void* workspace,
-                         size_t workspace_bytes, void* stream) {
+// The forward.  For the backward's recompute (hchunk != null) a context-
+// parallel plan combines every head exactly, and the WY and output-scan kernels
+// also write A^T (wyA) and every chunk's start state (hchunk); *p_out receives
+// the problem the kernels ran with.
+static gdn_status forward_impl(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                               const float* initial_state, const int32_t* cu_dev, void* out, float* final_state,
+                               const gdn_dims* dims, const gdn_cp_plan_t* plan, void* workspace,
+                               size_t workspace_bytes, void* stream, uint8_t* wyA, uint8_t* hchunk,
+                               Problem* p_out) {
   gdn_status st = check_dims(dims);
   if (st != GDN_OK) return st;
   if (!plan) return GDN_ERR_INVALID_ARG;
@@ -448,6 +456,9 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
   // runs without the preprocessing and the combine
   const bool cp = plan->mode != GDN_CP_OFF && plan->n_seg_total > plan->n_seqs;
   if (!cp) p.plan_mode = kModeOff;
+  if (hchunk && cp) p.plan_mode = kModeExact;
+  p.wyA = wyA;
+  p.hchunk = hchunk;
   p.lambda_q8 = plan->lambda_q8;
   p.warmup_chunks = plan->warmup_chunks;
   p.log_tol = std::log(plan->warmup_tol);
@@ -532,6 +543,114 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
   }
   if ((e = log.before(cs)) != cudaSuccess || (e = launch_scan_out(p, mq, mk, mo, plan->n_seg_total, cs)) != cudaSuccess ||
       (e = log.after("scan_out", cs)) != cudaSuccess)
+    return cuda_fail(e);
+  if (p_out) *p_out = p;
+  return GDN_OK;
+}
+
+gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                         const float* initial_state, const int32_t* cu_dev, void* out, float* final_state,
+                         const gdn_dims* dims, const gdn_cp_plan_t* plan, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  return forward_impl(q, k, v, g, beta, initial_state, cu_dev, out, final_state, dims, plan, workspace,
+                      workspace_bytes, stream, nullptr, nullptr, nullptr);
+}
+
+// ---- backward ----
+// Sections after the forward's workspace, per (chunk, value head): A^T (8 KB),
+// the chunk-start state, T', E and D (32 KB each); then a bf16 o the recompute
+// writes and nobody reads.
+struct BwdLayout {
+  size_t wyA, hchunk, tmat, emat, dstate, out, end;
+};
+static BwdLayout bwd_layout(const gdn_cp_plan_t* plan) {
+  BwdLayout L;
+  const size_t ch = (size_t)plan->n_chunks_total * plan->h_v;
+  size_t off = align_up(plan->workspace_bytes, 1024);
+  L.wyA = off;
+  off += ch * 8192;
+  L.hchunk = off;
+  off += ch * 32768;
+  L.tmat = off;
+  off += ch * 32768;
+  L.emat = off;
+  off += ch * 32768;
+  L.dstate = off;
+  off += ch * 32768;
+  L.out = off;
+  off = align_up(off + (size_t)plan->T_total * plan->h_v * kDim * 2, 256);
+  L.end = off;
+  return L;
+}
+
+gdn_status gdn_bwd_workspace_bytes(const gdn_cp_plan_t* plan, size_t* bytes) {
+  if (!plan || !bytes) return GDN_ERR_INVALID_ARG;
+  if (plan->dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+  *bytes = bwd_layout(plan).end;
+  return GDN_OK;
+}
+
+gdn_status gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                         const float* initial_state, const int32_t* cu_dev, const void* d_out,
+                         const float* d_final_state, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                         float* d_initial_state, const gdn_dims* dims, const gdn_cp_plan_t* plan, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  gdn_status st = check_dims(dims);
+  if (st != GDN_OK) return st;
+  if (!plan) return GDN_ERR_INVALID_ARG;
+  if (dims->dtype != GDN_BF16 || plan->dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+  const BwdLayout L = bwd_layout(plan);
+  if (!workspace || workspace_bytes < L.end) return GDN_ERR_WORKSPACE;
+  const int64_t T_total = (int64_t)dims->B * dims->T;
+  if (T_total > 0) {
+    if (!d_out || !dq || !dk || !dv || !dg || !dbeta) return GDN_ERR_INVALID_ARG;
+    if (!aligned16(d_out) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(dg) ||
+        !aligned16(dbeta))
+      return GDN_ERR_MISALIGNED;
+  }
+  if ((d_final_state && !aligned16(d_final_state)) || (d_initial_state && !aligned16(d_initial_state)))
+    return GDN_ERR_MISALIGNED;
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (T_total == 0) {
+    // no tokens: h_T = h0, so the gradient of h0 is that of h_T
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_MISALIGNED;
+    int dev = 0;
+    if ((st = device_setup(&dev)) != GDN_OK) return st;
+    cudaError_t e = cudaMemsetAsync(ws, 0, 256, cs);
+    if (e == cudaSuccess && d_initial_state) {
+      const size_t bytes = (size_t)dims->n_seqs * dims->h_v * kDim * kDim * 4;
+      e = d_final_state ? cudaMemcpyAsync(d_initial_state, d_final_state, bytes, cudaMemcpyDeviceToDevice, cs)
+                        : cudaMemsetAsync(d_initial_state, 0, bytes, cs);
+    }
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e);
+  }
+  Problem p;
+  st = forward_impl(q, k, v, g, beta, initial_state, cu_dev, ws + L.out, nullptr, dims, plan, workspace,
+                    workspace_bytes, stream, ws + L.wyA, ws + L.hchunk, &p);
+  if (st != GDN_OK) return st;
+  BwdArgs b;
+  b.dout = d_out;
+  b.dhT = d_final_state;
+  b.dq = dq;
+  b.dk = dk;
+  b.dv = dv;
+  b.dg = dg;
+  b.dbeta = dbeta;
+  b.dh0 = d_initial_state;
+  b.tmat = ws + L.tmat;
+  b.emat = ws + L.emat;
+  b.dstate = ws + L.dstate;
+  LaunchLog log(true);
+  cudaError_t e;
+  if ((e = log.before(cs)) != cudaSuccess || (e = launch_bwd_pre(p, b, cs)) != cudaSuccess ||
+      (e = log.after("bwd_pre", cs)) != cudaSuccess)
+    return cuda_fail(e);
+  if ((e = log.before(cs)) != cudaSuccess || (e = launch_bwd_chain(p, b, cs)) != cudaSuccess ||
+      (e = log.after("bwd_chain", cs)) != cudaSuccess)
+    return cuda_fail(e);
+  if ((e = log.before(cs)) != cudaSuccess || (e = launch_bwd_local(p, b, cs)) != cudaSuccess ||
+      (e = log.after("bwd_local", cs)) != cudaSuccess)
     return cuda_fail(e);
   return GDN_OK;
 }

@@ -76,10 +76,31 @@ struct Problem {
   float* chunk_exp;         // [n_chunks_total, h_v] warmup exponent of each chunk:
                             // sum over its tokens of g + log max(1, |1 - beta ||k||^2|)
   uint8_t* wy;              // [n_chunks_total, h_v] records of kRecBytes
+  // Written for the backward only (null in a plain forward):
+  uint8_t* wyA;             // [n_chunks_total, h_v] fp16 A^T = ((I + L)^{-1})^T, 64 x 64 in the
+                            // 128-byte-swizzled image (8 KB each)
+  uint8_t* hchunk;          // [n_chunks_total, h_v] fp16 chunk-start state S = H^T (rows d_v), two
+                            // 128 x 64 panels (d_k 0-63 | 64-127) in the swizzled image (32 KB each)
   // Test hook (0 in normal use): the WY kernel's CTAs first wait this many
   // nanoseconds on an mbarrier nothing arrives on, so the bounded wait runs
   // out and the call takes its timeout path.
   uint32_t stall_ns;
+};
+
+// Backward arguments (gdn_chunk_bwd) beside the forward's Problem.
+struct BwdArgs {
+  const void* dout;    // [T, h_v, 128] bf16: gradient of o
+  const float* dhT;    // [n_seqs, h_v, 128, 128] gradient of the final state, or null (zero)
+  void* dq;            // [T, h_qk, 128] bf16
+  void* dk;            // [T, h_qk, 128] bf16
+  void* dv;            // [T, h_v, 128] bf16
+  float* dg;           // [T, h_v]
+  float* dbeta;        // [T, h_v]
+  float* dh0;          // [n_seqs, h_v, 128, 128] or null (not written)
+  // workspace, per (chunk, value head), fp16 in the 128-byte-swizzled image, 32 KB each:
+  uint8_t* tmat;       // T' = -W^T Ktil (rows d_k out, panels d_k in)
+  uint8_t* emat;       // E = scale (diag(gamma) Q)^T dO - W^T scale P^T dO (rows d_k, panels d_v)
+  uint8_t* dstate;     // D = gradient of the chunk's end state (rows d_k, panels d_v)
 };
 
 // Arguments of the one-token step (gdn_decode_step).
@@ -313,6 +334,9 @@ cudaError_t launch_recurrence_f32(const Problem& p, cudaStream_t st, bool depend
 cudaError_t launch_f32_prep(const Problem& p, cudaStream_t st);
 cudaError_t f32_kernel_setup();
 cudaError_t launch_decode(const DecodeArgs& a, bool f32, cudaStream_t st);
+cudaError_t launch_bwd_pre(const Problem& p, const BwdArgs& b, cudaStream_t st);
+cudaError_t launch_bwd_chain(const Problem& p, const BwdArgs& b, cudaStream_t st);
+cudaError_t launch_bwd_local(const Problem& p, const BwdArgs& b, cudaStream_t st);
 cudaError_t scan_kernel_setup();
 cudaError_t wy_kernel_setup();
 cudaError_t combine_kernel_setup();

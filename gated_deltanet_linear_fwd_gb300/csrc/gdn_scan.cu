@@ -485,11 +485,23 @@ __device__ __forceinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem&
   float mx = 0.f;
   // The state's fp16 copy for chunk c into TMEM buffer c & 1: this thread's
   // row, its 64 columns packed into 32 (columns 32 half .. 32 half + 31).
+  // For the backward, the copy of each output chunk's start state also goes to
+  // p.hchunk (row = this thread's d_v, panel = half).
+  uint8_t* const hdump = (!PREP && p.hchunk)
+                             ? p.hchunk + ((size_t)(ch.chunk0 + ch.run_begin) * p.h_v + j) * 32768u +
+                                   (size_t)half * 16384u
+                             : nullptr;
   auto store_state = [&](int c) {
     uint32_t w[32];
 #pragma unroll
     for (int q = 0; q < 32; ++q) w[q] = pack_f16x2(S[2 * q], S[2 * q + 1]);
     tmem_st32(tmem + lane_base + kTS + (c & 1) * 64 + half * 32, w);
+    if (hdump && c < n && ch.run_begin + c >= ch.out_begin) {
+      uint8_t* dst = hdump + (size_t)c * p.h_v * 32768u;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<uint4*>(dst + sw128_offset(row, q)) = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    }
     tmem_st_wait();
   };
   store_state(0);

@@ -405,6 +405,17 @@ __device__ __forceinline__ bool wy_body(uint8_t* sm, WyCtl* ctl, const Problem& 
       a[4 * q4 + 3] = (16 * qc + 4 * q4 + 3 >= s) ? a4.w : 0.f;
     }
   }
+  if (p.wyA) {  // A^T for the backward: row s, columns 16 qc .. 16 qc + 15, fp16
+    uint8_t* dst = p.wyA + ((size_t)gc * p.h_v + j) * 8192u;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mx = absmax_nan(mx, a[8 * h + e]);
+      *reinterpret_cast<uint4*>(dst + sw128_offset(s, 2 * qc + h)) =
+          make_uint4(pack_f16x2(a[8 * h], a[8 * h + 1]), pack_f16x2(a[8 * h + 2], a[8 * h + 3]),
+                     pack_f16x2(a[8 * h + 4], a[8 * h + 5]), pack_f16x2(a[8 * h + 6], a[8 * h + 7]));
+    }
+  }
   auto store_operand = [&](float sc) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {

@@ -122,3 +122,15 @@ WORKLOADS = {
 
 def workload(name: str, dtype: torch.dtype = torch.bfloat16) -> Workload:
     return make_inputs(name=name, dtype=dtype, **WORKLOADS[name])
+
+
+def make_output_grads(w: Workload, seed: int = 100, with_dhT: bool = True, dhT_std: float = 0.1,
+                      dtype: torch.dtype = torch.bfloat16):
+    """Seeded upstream gradients for the backward: d_out ~ N(0, 1) like v (cast),
+    d_final_state ~ dhT_std * N(0, 1) fp32 [N, h_v, d_k, d_v] (or None)."""
+    gen = torch.Generator().manual_seed(seed)
+    d_out = torch.randn(w.v.shape, generator=gen).to(dtype)
+    dhT = None
+    if with_dhT:
+        dhT = dhT_std * torch.randn(w.n_seqs, w.h_v, w.q.shape[-1], w.v.shape[-1], generator=gen)
+    return d_out, dhT

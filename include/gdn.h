@@ -294,6 +294,46 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const fl
                            float* state, void* out, const gdn_dims* dims, void* stream);
 
 /*
+ * gdn_bwd_workspace_bytes -- device workspace gdn_chunk_bwd needs for `plan`:
+ * the forward's plan->workspace_bytes, then, per (chunk, value head), 136 KB
+ * (A^T, the chunk-start state and three 32 KB backward tiles), then a bf16
+ * copy of o.  Host only.  Errors: INVALID_ARG (NULL), UNSUPPORTED (fp32 plan).
+ */
+gdn_status gdn_bwd_workspace_bytes(const gdn_cp_plan_t* plan, size_t* bytes);
+
+/*
+ * gdn_chunk_bwd -- gradients of the chunked-prefill forward [FlashQLA,
+ * "TileLang warp-specialised kernels" (backward pass: the dv, state-gradient,
+ * dq/dk/dw/dg and WY gradient steps); the pages give no formulas: these are
+ * the exact gradients of gdn_chunk_fwd's function].  For the scalar
+ *   sum(o * d_out) + sum(final_state * d_final_state),
+ * writes its gradient with respect to q, k, v, g, beta and initial_state.
+ * Asynchronous on `stream`.  The forward is recomputed inside the call (no
+ * forward state is kept between calls); a context-parallel plan combines every
+ * head exactly there (no warmup restarts), so the gradients are those of the
+ * exact forward.  bf16 only.
+ *   q, k, v, g, beta, initial_state, cu_seqlens_dev, dims, plan: as gdn_chunk_fwd.
+ *   d_out         : device, [B*T, h_v, d_v] bf16.
+ *   d_final_state : device, [n_seqs, h_v, d_k, d_v] fp32, or NULL (zero).
+ *   dq, dk        : device, [B*T, h_qk, d_k] bf16 (summed over each q/k head's value heads).
+ *   dv            : device, [B*T, h_v, d_v] bf16.
+ *   dg, dbeta     : device, [B*T, h_v] fp32.
+ *   d_initial_state: device, [n_seqs, h_v, d_k, d_v] fp32, or NULL (not written);
+ *                   written also when initial_state is NULL (the gradient at zero).
+ *   workspace     : device, 256-byte aligned, at least gdn_bwd_workspace_bytes(plan).
+ * All device pointers 16-byte aligned; outputs may not overlap inputs.
+ * Kernels report through the workspace status word like the forward's
+ * (gdn_get_device_status), including GDN_ERR_DEVICE_CHECK when an fp16
+ * operand of the backward left the fp16 range.
+ * Errors: INVALID_ARG, UNSUPPORTED (fp32 dtype), MISALIGNED, WORKSPACE, CUDA.
+ */
+gdn_status gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                         const float* initial_state, const int32_t* cu_seqlens_dev, const void* d_out,
+                         const float* d_final_state, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                         float* d_initial_state, const gdn_dims* dims, const gdn_cp_plan_t* plan,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * gdn_debug_stall_ns -- test hook of the failure path (no counterpart on the
  * FlashQLA pages).  While ns > 0, each later gdn_chunk_fwd of this process on
  * the bf16 path makes the blocks of its chunk-local kernel first wait ns

@@ -177,10 +177,11 @@ def chunk_backward(H, D, qc, kc, vc, gc, bc, doc, scale):
     return dq, dk, dv, dg, dbeta, D_prev
 
 
-def grad_chunked(q, k, v, g, beta, h0, cu_seqlens, do, dhT=None, scale=None, C=CHUNK):
+def grad_chunked(q, k, v, g, beta, h0, cu_seqlens, do, dhT=None, scale=None, C=CHUNK, heads=None):
     """Gradients of sum(o * do) + sum(h_T * dh_T) through the chunked form.
 
-    Same arguments and results as ``grad_recurrence``.  Per sequence and value
+    Same arguments and results as ``grad_recurrence`` (heads: the value heads
+    to differentiate, None: all).  Per sequence and value
     head: a forward pass of the chunked scan keeps every chunk-start state, then
     the chunks are differentiated in reverse with ``chunk_backward``.
     """
@@ -198,7 +199,7 @@ def grad_chunked(q, k, v, g, beta, h0, cu_seqlens, do, dhT=None, scale=None, C=C
     for n in range(n_seqs):
         bos, eos = int(cu_seqlens[n]), int(cu_seqlens[n + 1])
         bounds = [(a + bos, b + bos) for a, b in chunk_bounds(eos - bos, C)]
-        for j in range(h_v):
+        for j in (range(h_v) if heads is None else sorted(heads)):
             i = (j * h_qk) // h_v
             H = np.zeros((d_k, d_v)) if h0 is None else np.asarray(h0, dtype=np.float64)[n, j].copy()
             states = []

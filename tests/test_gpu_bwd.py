@@ -1,0 +1,157 @@
+"""GPU parity of the backward (gdn_chunk_bwd) against the float64 oracle gradients.
+
+The oracle is ``oracle.backward``: the autograd definition on small cases and
+the chunk-level derivation (pinned to it on the CPU) on the larger ones, both
+on the exact bf16/fp32 values the GPU receives.  Bar, per gradient tensor:
+max|diff| <= 2e-2 * RMS(ref), the forward's bf16 rule; dq, dk and dv are bf16
+outputs, so their half-ulp rounding is allowed on top, as for o.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import backward as OB
+from tests import util
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU, skipped there
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from gated_deltanet_linear_fwd_gb300 import gdn_chunk_bwd, gdn_cp_plan, gdn_get_device_status  # noqa: E402
+from gated_deltanet_linear_fwd_gb300.api import gdn_bwd_workspace_bytes  # noqa: E402
+from gated_deltanet_linear_fwd_gb300.inputs import make_inputs, make_output_grads, workload  # noqa: E402
+
+DEV = "cuda:0"
+NAMES = ("dq", "dk", "dv", "dg", "dbeta", "dh0")
+TOL = 2e-2
+
+
+def run_bwd(w, d_out, dhT, mode="off", h0=True):
+    d = w.to(DEV)
+    plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, cu_seqlens=w.cu_seqlens, mode=mode)
+    ws = torch.empty(gdn_bwd_workspace_bytes(plan), dtype=torch.uint8, device=DEV)
+    grads = gdn_chunk_bwd(d.q, d.k, d.v, d.g, d.beta, d_out.to(DEV), d.h0 if h0 else None,
+                          None if dhT is None else dhT.to(DEV), d.cu_seqlens, plan=plan, workspace=ws)
+    code, detail = gdn_get_device_status(ws)
+    assert code == 0, f"device status {code} detail {detail}"
+    return dict(zip(NAMES, grads)), plan
+
+
+def ref_grads(w, d_out, dhT, h0=True, fn=OB.grad_chunked, heads=None):
+    f = util.to64
+    kw = {} if heads is None else {"heads": heads}
+    return dict(zip(NAMES, fn(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0) if h0 else None,
+                              w.seq_offsets(), f(d_out), None if dhT is None else f(dhT), **kw)))
+
+
+def check(got, ref, names=NAMES, tol=TOL):
+    worst = {}
+    for n in names:
+        r = ref[n]
+        x = got[n].double().cpu().numpy()
+        rms = float(np.sqrt(np.mean(r * r)))
+        err = np.abs(x - r)
+        if n in ("dq", "dk", "dv"):
+            err = np.maximum(err - util.bf16_half_ulp(r), 0.0)
+        worst[n] = float(err.max()) / max(rms, 1e-30)
+    bad = {n: e for n, e in worst.items() if not e <= tol}
+    assert not bad, f"over {tol}: {bad} (all: {worst})"
+    return worst
+
+
+@pytest.mark.parametrize("mode", ["off", "auto"])
+def test_bwd_small_against_definition(mode):
+    """Several chunks and a partial one, h0 and dhT given; the autograd oracle."""
+    w = make_inputs(200, h_qk=1, h_v=2, seed=21, with_h0=True)
+    d_out, dhT = make_output_grads(w, seed=22)
+    got, _ = run_bwd(w, d_out, dhT, mode=mode)
+    check(got, ref_grads(w, d_out, dhT, fn=OB.grad_recurrence))
+
+
+@pytest.mark.parametrize("mode", ["off", "exact", "auto"])
+def test_bwd_varlen_gqa(mode):
+    """Varlen with a one-token and an exactly-one-chunk sequence, GQA 2/4, CP modes."""
+    w = make_inputs(cu_seqlens=[0, 70, 330, 394, 395, 700], h_qk=2, h_v=4, seed=23, with_h0=True)
+    d_out, dhT = make_output_grads(w, seed=24)
+    got, _ = run_bwd(w, d_out, dhT, mode=mode)
+    check(got, ref_grads(w, d_out, dhT))
+
+
+def test_bwd_without_h0_or_dhT():
+    w = make_inputs(300, h_qk=2, h_v=2, seed=25)
+    d_out, _ = make_output_grads(w, seed=26, with_dhT=False)
+    got, _ = run_bwd(w, d_out, None, h0=False)
+    check(got, ref_grads(w, d_out, None, h0=False))
+
+
+def test_bwd_batch_rows():
+    """B fixed-length rows (no cu_seqlens) of a partial last chunk."""
+    w = make_inputs(2 * 150, h_qk=1, h_v=3, seed=27, with_h0=True)
+    d = w.to(DEV)
+    B, T = 2, 150
+    q, k, v = (t.view(B, T, *t.shape[1:]) for t in (d.q, d.k, d.v))
+    g, beta = d.g.view(B, T, -1), d.beta.view(B, T, -1)
+    h0 = d.h0.repeat(2, 1, 1, 1).contiguous()
+    d_out, dhT = make_output_grads(w, seed=28)
+    dhT = dhT.repeat(2, 1, 1, 1).contiguous()
+    plan = gdn_cp_plan(T=T, h_qk=1, h_v=3, B=B, mode="off")
+    ws = torch.empty(gdn_bwd_workspace_bytes(plan), dtype=torch.uint8, device=DEV)
+    grads = gdn_chunk_bwd(q, k, v, g, beta, d_out.to(DEV).view(B, T, 3, 128), h0, dhT.to(DEV), plan=plan,
+                          workspace=ws)
+    assert gdn_get_device_status(ws)[0] == 0
+    got = {n: x.reshape(-1, *x.shape[2:]) if n != "dh0" else x for n, x in zip(NAMES, grads)}
+    f = util.to64
+    h0_np = np.concatenate([f(w.h0)] * 2)
+    ref = dict(zip(NAMES, OB.grad_chunked(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), h0_np, [0, 150, 300],
+                                          f(d_out), f(dhT))))
+    check(got, ref)
+
+
+def test_bwd_more_qk_heads_than_value_heads():
+    """h_qk 4 / h_v 2: q/k heads 1 and 3 feed no value head; their gradients are zero."""
+    w = make_inputs(130, h_qk=4, h_v=2, seed=29, with_h0=True)
+    d_out, dhT = make_output_grads(w, seed=30)
+    got, _ = run_bwd(w, d_out, dhT)
+    check(got, ref_grads(w, d_out, dhT))
+    for n in ("dq", "dk"):
+        assert float(got[n][:, 1::2].abs().max()) == 0.0
+
+
+def test_bwd_no_tokens():
+    """T = 0: the gradient of h0 is that of h_T."""
+    d = make_inputs(64, h_qk=1, h_v=2, seed=31, with_h0=True).to(DEV)
+    e = lambda t: t[:0].contiguous()
+    plan = gdn_cp_plan(T=0, h_qk=1, h_v=2, mode="off")
+    dhT = torch.randn(1, 2, 128, 128, device=DEV)
+    ws = torch.empty(max(gdn_bwd_workspace_bytes(plan), 256), dtype=torch.uint8, device=DEV)
+    grads = gdn_chunk_bwd(e(d.q), e(d.k), e(d.v), e(d.g), e(d.beta), e(d.v), d.h0, dhT, plan=plan, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(grads[5], dhT)
+
+
+def test_bwd_strong_decay():
+    """g about -3 a token: exp(G) underflows in fp32 within a chunk."""
+    w = make_inputs(cu_seqlens=[0, 70, 333], h_qk=1, h_v=2, seed=32, with_h0=True)
+    gen = torch.Generator().manual_seed(33)
+    w.g = (-3.0 + 0.5 * torch.randn(w.g.shape, generator=gen)).float()
+    d_out, dhT = make_output_grads(w, seed=34)
+    got, _ = run_bwd(w, d_out, dhT)
+    check(got, ref_grads(w, d_out, dhT))
+
+
+@pytest.mark.parametrize("name,heads", [("T32768_h2x8", None), ("T32768_h16x16", [0, 7, 15])])
+def test_bwd_full_size(name, heads):
+    """The benchmark's 1 x 32768 workloads at full size, in the bench's launch
+    configuration (auto plan); every head, or a sample of heads, element by element."""
+    w = workload(name)
+    d_out, dhT = make_output_grads(w, seed=35)
+    got, plan = run_bwd(w, d_out, dhT, mode="auto", h0=w.h0 is not None)
+    ref = ref_grads(w, d_out, dhT, h0=w.h0 is not None, heads=heads)
+    if heads is None:
+        check(got, ref)
+    else:  # the sampled heads' own gradients (dq and dk sum over every head of a group)
+        names = ("dv", "dg", "dbeta", "dh0")
+        check({n: got[n][:, heads] for n in names}, {n: ref[n][:, heads] for n in names}, names=names)
