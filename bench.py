@@ -76,6 +76,22 @@ def algorithmic(w):
     return by, fl
 
 
+def algorithmic_bwd(w):
+    """Bytes and FLOPs the backward must move / do: q, k, v, g, beta and d_out
+    read, dq, dk, dv, dg, dbeta written (h0, dh_T read and dh0 written per
+    state); the forward's contractions once more (the recompute) plus the
+    chunked backward's: per token and value head 12 d^2 + 14 C d + 2 C^2
+    (K~D, Q^T dO, W^T dV', dO H^T, V' D^T, Y_U H^T; P^T dO, dO V'^T, (dP*Gam) K,
+    (dP*Gam)^T Q, A^T dV', dV' V'^T, the symmetrised dKK K; A^T (dV' V'^T))."""
+    T, hqk, hv, n = w.T, w.h_qk, w.h_v, w.n_seqs
+    by = T * (2 * (2 * hqk * D * 2) + 3 * hv * D * 2 + 4 * hv * 4) + n * hv * D * D * 4 * 2
+    if w.h0 is not None:
+        by += n * hv * D * D * 4
+    _, fl_fwd = algorithmic(w)
+    fl = fl_fwd + T * hv * (12 * D * D + 14 * C * D + 2 * C * C)
+    return by, fl
+
+
 # Each kernel's share of the layer's algorithmic bytes (the inputs it reads
 # and outputs it writes that the layer must move anyway): the WY kernel reads
 # q, k, v, g and beta, the output scans write o and the states.  The chunk
@@ -241,6 +257,91 @@ def time_gpu(name, steps, warmup, device, cp="auto", lambda_=0.0, trace=True, to
 
 
 VARLEN = "varlen4_T348160_h2x8"
+BWD_SWEEP = ["T32768_h8x24_h0", "T32768_h16x16", "batch8_T4096_h8x32"]
+
+
+def time_bwd(name, steps, warmup, device, cp="auto"):
+    """Times the backward (gdn_chunk_bwd, its forward recompute included) on one
+    workload with seeded upstream gradients d_out and d_final_state."""
+    from gated_deltanet_linear_fwd_gb300 import (gdn_bwd_workspace_bytes, gdn_chunk_bwd, gdn_cp_plan,
+                                                 gdn_get_device_status, gdn_set_trace_events, gdn_trace_last)
+    from gated_deltanet_linear_fwd_gb300.inputs import make_output_grads, workload
+    w = workload(name)
+    d = w.to(device)
+    d_out, dhT = make_output_grads(w)
+    d_out, dhT = d_out.to(device), dhT.to(device)
+    plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, cu_seqlens=w.cu_seqlens, mode=cp)
+    ws = torch.empty(gdn_bwd_workspace_bytes(plan), dtype=torch.uint8, device=device)
+    grads = (torch.empty_like(d.q), torch.empty_like(d.k), torch.empty_like(d.v), torch.empty_like(d.g),
+             torch.empty_like(d.beta), torch.empty(w.n_seqs, w.h_v, D, D, dtype=torch.float32, device=device))
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def bwd():
+        gdn_chunk_bwd(d.q, d.k, d.v, d.g, d.beta, d_out, d.h0, dhT, d.cu_seqlens, plan=plan, grads=grads,
+                      workspace=ws)
+
+    for _ in range(warmup):
+        flush.zero_()
+        bwd()
+    torch.cuda.synchronize(device)
+    names = gdn_trace_last()
+    per_step = []
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(steps):
+        flush.zero_()
+        s0.record(stream)
+        bwd()
+        s1.record(stream)
+        s1.synchronize()
+        per_step.append(s0.elapsed_time(s1))
+    n_k, trace_steps = len(names), max(3, steps // 4)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_k)]
+    for e in ev:
+        e.record(stream)
+    torch.cuda.synchronize(device)
+    gdn_set_trace_events(ev)
+    per_kernel = [0.0] * n_k
+    for _ in range(trace_steps):
+        flush.zero_()
+        bwd()
+        torch.cuda.synchronize(device)
+        for i in range(n_k):
+            per_kernel[i] += ev[2 * i].elapsed_time(ev[2 * i + 1])
+    gdn_set_trace_events([])
+    code, detail = gdn_get_device_status(ws)
+    by, fl = algorithmic_bwd(w)
+    return {"workload": name, "ms": statistics.mean(per_step), "ms_median": statistics.median(per_step),
+            "kernel_ms": {n: t / trace_steps for n, t in zip(names, per_kernel)}, "status": [code, detail],
+            "bytes": by, "flops": fl, "tokens": w.T, "segments": plan.n_seg_total,
+            "grads": [x.cpu() for x in grads]}
+
+
+def backward_report(r, hbm, tfl):
+    t_roof = max(r["bytes"] / (hbm * 1e9), r["flops"] / (tfl * 1e12))
+    return {"workload": r["workload"], "ms": r["ms"], "tokens_per_s": r["tokens"] / (r["ms"] * 1e-3),
+            "roofline_frac": t_roof * 1e3 / r["ms"], "roofline_ms": t_roof * 1e3,
+            "bound": "tensor" if r["flops"] / (tfl * 1e12) > r["bytes"] / (hbm * 1e9) else "hbm",
+            "kernels_ms": r["kernel_ms"], "segments": r["segments"], "device_status": r["status"]}
+
+
+def backward_accuracy(r):
+    """The float64 oracle's gradients (chunk-level derivation, pinned on the CPU to
+    the autograd definition) against the GPU's, max|diff| / RMS(ref) per tensor."""
+    import numpy as np
+    from oracle import backward as OB
+    from gated_deltanet_linear_fwd_gb300.inputs import make_output_grads, workload
+    w = workload(r["workload"])
+    d_out, dhT = make_output_grads(w)
+    f = lambda t: None if t is None else t.double().numpy()
+    t0 = time.perf_counter()
+    ref = OB.grad_chunked(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0), w.seq_offsets(), f(d_out), f(dhT))
+    res = {}
+    for n, x, y in zip(("dq", "dk", "dv", "dg", "dbeta", "dh0"), r["grads"], ref):
+        res[n] = float(np.abs(x.double().numpy() - y).max() / np.sqrt(np.mean(y * y)))
+    res["bar"] = 2e-2
+    res["oracle_s"] = time.perf_counter() - t0
+    return res
 
 
 def compare_cp_modes(name, steps, device):
@@ -546,6 +647,11 @@ def run_only(args, device, hbm):
         r = time_decode(args.steps, args.warmup, device, hbm)
     elif args.only == "f32":
         r = time_f32(HEADLINE, args.steps, args.warmup, device)
+    elif args.only.startswith("bwd"):
+        name = args.only.split(":", 1)[1] if ":" in args.only else HEADLINE
+        t = time_bwd(name, args.steps, args.warmup, device, args.cp)
+        r = {"workload": name, "ms": t["ms"], "kernels_ms": t["kernel_ms"], "segments": t["segments"],
+             "status": t["status"]}
     else:
         t = time_gpu(args.only, args.steps, args.warmup, device, args.cp, args.lambda_)
         r = {"workload": args.only, "ms": t["ms"], "kernels_ms": t["kernel_ms"], "segments": t["plan"].n_seg_total,
@@ -643,6 +749,14 @@ def main(argv=None):
         f32 = time_f32(HEADLINE, max(5, args.steps // 50), 3, device)
         f32["vs_bf16_path"] = f32["ms"] / ms
         line["f32"] = f32
+    if not args.no_sweep and rank == 0:
+        rb = time_bwd(HEADLINE, max(10, args.steps // 50), 3, device, args.cp)
+        line["backward"] = backward_report(rb, hbm, tfl)
+        line["backward"]["vs_forward"] = rb["ms"] / ms
+        line["backward"]["sweep"] = {n: backward_report(time_bwd(n, 5, 2, device, args.cp), hbm, tfl)
+                                     for n in BWD_SWEEP}
+        if not args.no_cpu_baseline:
+            line["backward"]["accuracy"] = backward_accuracy(rb)
     if rank == 0:
         line["planning"] = plan_t
     if rank == 0 and not args.no_cpu_baseline:

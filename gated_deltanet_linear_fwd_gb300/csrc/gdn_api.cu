@@ -21,7 +21,7 @@ std::atomic<uint32_t> g_debug_stall_ns{0};  // test hook of the timeout path (gd
 // ---- tracing: caller-provided events recorded around each launch ----
 // Kernel i of a call is bracketed by events 2i and 2i + 1, recorded on the
 // stream it is launched on.
-constexpr int kMaxTrace = 16;
+constexpr int kMaxTrace = 32;
 thread_local cudaEvent_t g_trace_ev[kMaxTrace];
 thread_local int g_trace_n = 0;
 thread_local const char* g_last_names[kMaxTrace / 2];
@@ -629,6 +629,8 @@ gdn_status gdn_chunk_bwd(const void* q, const void* k, const void* v, const floa
   st = forward_impl(q, k, v, g, beta, initial_state, cu_dev, ws + L.out, nullptr, dims, plan, workspace,
                     workspace_bytes, stream, ws + L.wyA, ws + L.hchunk, &p);
   if (st != GDN_OK) return st;
+  int dev = 0;
+  if ((st = device_setup(&dev)) != GDN_OK) return st;
   BwdArgs b;
   b.dout = d_out;
   b.dhT = d_final_state;
@@ -646,7 +648,19 @@ gdn_status gdn_chunk_bwd(const void* q, const void* k, const void* v, const floa
   if ((e = log.before(cs)) != cudaSuccess || (e = launch_bwd_pre(p, b, cs)) != cudaSuccess ||
       (e = log.after("bwd_pre", cs)) != cudaSuccess)
     return cuda_fail(e);
-  if ((e = log.before(cs)) != cudaSuccess || (e = launch_bwd_chain(p, b, cs)) != cudaSuccess ||
+  if (p.plan_mode != kModeOff) {
+    // context parallel: per segment the transition and the local offset, then
+    // the segments' end-state gradients by the combine run backwards
+    if ((e = log.before(cs)) != cudaSuccess || (e = launch_bwd_chain(p, b, true, cs)) != cudaSuccess ||
+        (e = log.after("bwd_chain_prep", cs)) != cudaSuccess)
+      return cuda_fail(e);
+    Problem pc = p;
+    pc.h0 = d_final_state;
+    if ((e = log.before(cs)) != cudaSuccess || (e = launch_combine_bwd(pc, g_sm_count[dev], cs)) != cudaSuccess ||
+        (e = log.after("bwd_combine", cs)) != cudaSuccess)
+      return cuda_fail(e);
+  }
+  if ((e = log.before(cs)) != cudaSuccess || (e = launch_bwd_chain(p, b, false, cs)) != cudaSuccess ||
       (e = log.after("bwd_chain", cs)) != cudaSuccess)
     return cuda_fail(e);
   if ((e = log.before(cs)) != cudaSuccess || (e = launch_bwd_local(p, b, cs)) != cudaSuccess ||

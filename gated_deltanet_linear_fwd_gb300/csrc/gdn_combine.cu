@@ -14,6 +14,14 @@
 // per CTA halve each segment's step when few (sequence, head) pairs exist.
 // The CTA of row block 0 also records the mode the (sequence, head) takes and
 // its warmup bound.
+//
+// BWD: the same scan run backwards for the gradient of the state.  With
+// D_end(s) the gradient of segment s's end state (rows d_v after transposing)
+// and R_s, S_loc,s the transposed transition and local offset of the
+// backward chain over segment s,
+//     D_end(n_seg-1) = dh_T^T,   D_end(s-1) = D_end(s) R_s + S_loc,s,
+// taking h0's place by dh_T and writing D_end(s-1) where the forward writes
+// S_start(s+1).
 #include "gdn_dev.cuh"
 
 namespace gdn {
@@ -26,7 +34,7 @@ constexpr int combine_smem() {
 }
 
 // kRows state rows per CTA (4 or 8)
-template <int kRows>
+template <int kRows, bool BWD>
 __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
   extern __shared__ float4 csm4[];
   float* sR = reinterpret_cast<float*>(csm4);  // [2][128*128]
@@ -55,7 +63,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
       s_skip = st;
       s_seq = si;
       s_mode = mode;
-      if (rb == 0 && !st) {
+      if (!BWD && rb == 0 && !st) {
         p.head_mode[n * p.h_v + j] = mode;
         p.head_bound[n * p.h_v + j] = bound;
       }
@@ -84,9 +92,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
   const bool skip_first = p.h0 == nullptr;  // R_0 is not produced for a zero start: skip its product
   const int first_product = skip_first ? 1 : 0;
   const int last = si.n_seg - 2;  // produce S_start(1 .. n_seg-1)
-  auto prefetch = [&](int s) {     // one thread; buffer s & 1 was last read in step s - 2
-    const int buf = s & 1;
-    const bool product = s >= first_product;
+  // step i reads segment seg_of(i) and writes the state of out_of(i)
+  auto seg_of = [&](int i) { return BWD ? si.n_seg - 1 - i : i; };
+  auto prefetch = [&](int i) {     // one thread; buffer i & 1 was last read in step i - 2
+    const int buf = i & 1;
+    const bool product = i >= first_product;
+    const int s = seg_of(i);
     mbar_arrive_expect_tx(&s_bar[buf], (uint32_t)(kRows * kDim * 4) + (product ? (uint32_t)(mat * 4) : 0u));
     if (product)
       bulk_load(sR + buf * mat, p.R + ((size_t)(si.seg_base + s) * p.h_v + j) * mat, (uint32_t)(mat * 4), &s_bar[buf]);
@@ -163,7 +174,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
     // the next step reads them, and overwrites sP, only after its own barrier.
     if (own) {
       *reinterpret_cast<float4*>(sX + rr * kDim + c4) = make_float4(a0, a1, a2, a3);
-      *reinterpret_cast<float4*>(p.Sstart + ((size_t)(si.seg_base + s + 1) * p.h_v + j) * mat +
+      const int out_seg = BWD ? seg_of(s) - 1 : s + 1;
+      *reinterpret_cast<float4*>(p.Sstart + ((size_t)(si.seg_base + out_seg) * p.h_v + j) * mat +
                                  (size_t)(r0 + rr) * kDim + c4) = make_float4(a0, a1, a2, a3);
     }
   }
@@ -173,18 +185,34 @@ __global__ void __launch_bounds__(256) combine_kernel(const Problem p) {
 
 cudaError_t combine_kernel_setup() {
   cudaError_t e =
-      cudaFuncSetAttribute(combine_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, combine_smem<4>());
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(combine_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, combine_smem<8>());
+      cudaFuncSetAttribute(combine_kernel<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, combine_smem<4>());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(combine_kernel<8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, combine_smem<8>());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(combine_kernel<4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, combine_smem<4>());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(combine_kernel<8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, combine_smem<8>());
+  return e;
+}
+
+template <bool BWD>
+static cudaError_t launch_combine_dir(const Problem& p, int sm_count, cudaStream_t st) {
+  // 32 CTAs of 4 rows per exact (sequence, head) if even all pairs fit in about two waves
+  if ((int64_t)p.n_seqs * p.h_v * 32 <= 2 * (int64_t)sm_count)
+    return launch_kernel(combine_kernel<4, BWD>, dim3(p.n_seqs * (kDim / 4), p.h_v), dim3(256), combine_smem<4>(), st,
+                         true, p);
+  return launch_kernel(combine_kernel<8, BWD>, dim3(p.n_seqs * (kDim / 8), p.h_v), dim3(256), combine_smem<8>(), st,
+                       true, p);
 }
 
 cudaError_t launch_combine(const Problem& p, int sm_count, cudaStream_t st) {
-  // 32 CTAs of 4 rows per exact (sequence, head) if even all pairs fit in about two waves
-  if ((int64_t)p.n_seqs * p.h_v * 32 <= 2 * (int64_t)sm_count)
-    return launch_kernel(combine_kernel<4>, dim3(p.n_seqs * (kDim / 4), p.h_v), dim3(256), combine_smem<4>(), st, true,
-                         p);
-  return launch_kernel(combine_kernel<8>, dim3(p.n_seqs * (kDim / 8), p.h_v), dim3(256), combine_smem<8>(), st, true,
-                       p);
+  return launch_combine_dir<false>(p, sm_count, st);
+}
+
+// The backward's combine: p.h0 = dh_T, p.R / p.Sloc = the backward chain's
+// transposed transitions and local offsets, p.Sstart receives D_end.
+cudaError_t launch_combine_bwd(const Problem& p, int sm_count, cudaStream_t st) {
+  return launch_combine_dir<true>(p, sm_count, st);
 }
 
 }  // namespace gdn

@@ -349,21 +349,21 @@ gdn_status gdn_debug_stall_ns(uint32_t ns);
 
 /*
  * gdn_set_trace_events -- optional per-kernel timing (tracing).  Registers,
- * for the calling host thread, up to 16 caller-created cudaEvent_t handles.
- * While registered, each gdn_chunk_fwd (and gdn_decode_step) on this thread
+ * for the calling host thread, up to 32 caller-created cudaEvent_t handles.
+ * While registered, each gdn_chunk_fwd (gdn_chunk_bwd, gdn_decode_step) on this thread
  * brackets its i-th kernel launch with events[2i] (recorded right before the
  * launch) and events[2i + 1] (right after it), both on the stream the kernel
  * is launched on, so cudaEventElapsedTime(events[2i], events[2i + 1]) is the
  * device time of kernel i.  n_events = 0 (or events = NULL) turns tracing
  * off.  The caller keeps ownership of the events.
- * Errors: INVALID_ARG for n_events outside 0..16 or a NULL event.
+ * Errors: INVALID_ARG for n_events outside 0..32 or a NULL event.
  */
 gdn_status gdn_set_trace_events(void* const* events, int n_events);
 
 /*
- * gdn_trace_last -- names of the kernels the last gdn_chunk_fwd (or
+ * gdn_trace_last -- names of the kernels the last gdn_chunk_fwd (gdn_chunk_bwd,
  * gdn_decode_step) on this thread launched, in launch order (static
- * strings), and their count (at most 8).
+ * strings), and their count (at most 16).
  *   names : host array of at least max_names pointers, or NULL.
  * Returns the number of kernels launched (0 before any call).
  */
