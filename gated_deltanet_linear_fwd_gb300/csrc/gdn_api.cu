@@ -663,7 +663,7 @@ gdn_status gdn_chunk_bwd(const void* q, const void* k, const void* v, const floa
   if ((e = log.before(cs)) != cudaSuccess || (e = launch_bwd_chain(p, b, false, cs)) != cudaSuccess ||
       (e = log.after("bwd_chain", cs)) != cudaSuccess)
     return cuda_fail(e);
-  if ((e = log.before(cs)) != cudaSuccess || (e = launch_bwd_local(p, b, cs)) != cudaSuccess ||
+  if ((e = log.before(cs)) != cudaSuccess || (e = launch_bwd_local_tc(p, b, cs)) != cudaSuccess ||
       (e = log.after("bwd_local", cs)) != cudaSuccess)
     return cuda_fail(e);
   return GDN_OK;

@@ -19,12 +19,11 @@
 //   bwd_pre_kernel    per (chunk, value head): T' and E            (chunk-parallel)
 //   bwd_chain_kernel  per (sequence, value head): D over the chunks in reverse,
 //                     D kept in fp32; writes every chunk's D (fp16) and dh0
-//   bwd_local_kernel  per (chunk, q/k head), over the value heads of the group:
-//                     every other gradient; dq and dk summed over the group in
-//                     registers (deterministic, no atomics)
-// Products run on the tensor cores through mma.sync m16n8k16 (fp16 operands in
-// the forward's 128-byte-swizzled tile image, fp32 accumulators); tiles arrive
-// by bulk copies on an mbarrier with a bounded wait.
+//   bwd_local_tc_kernel (gdn_bwd_tc.cu) per (chunk, q/k head), over the value
+//                     heads of the group: every other gradient on tcgen05
+// The two kernels here run their products on the tensor cores through mma.sync
+// m16n8k16 (fp16 operands in the forward's 128-byte-swizzled tile image, fp32
+// accumulators); tiles arrive by bulk copies on an mbarrier with a bounded wait.
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 
@@ -149,12 +148,20 @@ __device__ __forceinline__ bool chunk_rows(const Problem& p, int gc, int& n, int
 // panels), row r scaled by row_scale[r] (null: 1); rows >= cv are zero.
 __device__ __forceinline__ void load_rows_f16(const Tile& t, const __nv_bfloat16* src, int64_t t0, int heads, int head,
                                               int cv, const float* row_scale, float& mx) {
-  for (int idx = threadIdx.x; idx < 64 * 16; idx += kBwdThreads) {
-    const int r = idx >> 4, c = idx & 15;
-    uint4 raw = make_uint4(0, 0, 0, 0);
-    if (r < cv) raw = *reinterpret_cast<const uint4*>(src + ((size_t)(t0 + r) * heads + head) * kDim + c * 8);
+  // all loads in flight before the first store (the stores are ordered memory operations)
+  constexpr int kPer = 64 * 16 / kBwdThreads;
+  uint4 raw[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int idx = threadIdx.x + u * kBwdThreads, r = idx >> 4, c = idx & 15;
+    raw[u] = make_uint4(0, 0, 0, 0);
+    if (r < cv) raw[u] = *reinterpret_cast<const uint4*>(src + ((size_t)(t0 + r) * heads + head) * kDim + c * 8);
+  }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int idx = threadIdx.x + u * kBwdThreads, r = idx >> 4, c = idx & 15;
     const float sc = row_scale ? row_scale[r] : 1.f;
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
     uint32_t o[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -448,425 +455,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_chain_kernel(const Problem
   if (!(mx < 65504.f)) report(p.status, kDevCheck, kDetFp16Range);
 }
 
-// ---------------------------------------------------------------- bwd_local
-// One (chunk, q/k head); its value heads one after the other.  Warp w owns
-// rows 16 (w & 3) .. + 15 (tokens) and the column half w >> 2 of every
-// 64-row product (64 of 128 columns, or 32 of 64).
-constexpr uint32_t kLQ = 0;                  // Q: 64 x 128
-constexpr uint32_t kLK = kLQ + 16384;        // K: 64 x 128
-constexpr uint32_t kLWt = kLK + 16384;       // -W^T record tile (128 x 64), then dV' (64 x 128)
-constexpr uint32_t kLUt = kLWt + 16384;      // U^T record tile (128 x 64), then V' (64 x 128)
-constexpr uint32_t kLP = kLUt + 16384;       // P record tile (64 x 64), then dP * Gam
-constexpr uint32_t kLA = kLP + 8192;         // A^T (64 x 64)
-constexpr uint32_t kLH = kLA + 8192;         // chunk-start state S = H^T: 128 (d_v) x 128 (d_k)
-constexpr uint32_t kLD = kLH + 32768;        // chunk-end state gradient D: 128 (d_k) x 128 (d_v)
-constexpr uint32_t kLV = kLD + 32768;        // V: 64 x 128
-constexpr uint32_t kLDo = kLV + 16384;       // dO, then Y_U: 64 x 128
-constexpr uint32_t kLX = kLDo + 16384;       // dV' V'^T (64 x 64)
-constexpr uint32_t kLY = kLX + 8192;         // dKK (64 x 64)
-constexpr uint32_t kLF = kLY + 8192;         // fp32: G, exp(G), dec, beta [64 each]
-constexpr uint32_t kLRow = kLF + 1024;       // fp32 row partial sums [6 kinds][2 halves][64]
-constexpr uint32_t kLCol = kLRow + 3072;     // fp32 column sums of dGam * Gam [4 strips][64]
-constexpr uint32_t kLRed = kLCol + 1024;     // fp32 [16]: <D, H> per warp, scan carry
-constexpr uint32_t kLBar = kLRed + 64;
-constexpr uint32_t kLocalSmem = kLBar + 64 + 1024;
-enum RowKind { kRowDgam = 0, kRowDdec, kRowT1, kRowT2, kRowErow, kRowDbL, kRowKinds };
-
-// Sum over the four lanes of a quad (the lanes holding one accumulator row).
-__device__ __forceinline__ float quad_sum(float x) {
-  x += __shfl_xor_sync(0xffffffffu, x, 1);
-  return x + __shfl_xor_sync(0xffffffffu, x, 2);
-}
-
-__global__ void __launch_bounds__(kBwdThreads, 1) bwd_local_kernel(const Problem p, const BwdArgs b) {
-  uint8_t* sm = smem_base();
-  const uint32_t s0 = smem_u32(sm);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kLBar);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int gc = (int)(blockIdx.x / (unsigned)p.h_qk), iq = (int)(blockIdx.x % (unsigned)p.h_qk);
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-  }
-  grid_dependency_wait();
-  grid_launch_dependents();
-  int n, cv;
-  int64_t t0;
-  if (!chunk_rows(p, gc, n, t0, cv)) {
-    if (tid == 0) report(p.status, kDevCheck, kDetSegMismatch);
-    return;
-  }
-  if (__syncthreads_or(tid == 0 && earlier_failure(p.status))) return;
-  float* sG = reinterpret_cast<float*>(sm + kLF);
-  float* sGam = sG + 64;
-  float* sDec = sG + 128;
-  float* sBeta = sG + 192;
-  float* sRow = reinterpret_cast<float*>(sm + kLRow);  // [kind][half][64]
-  float* sCol = reinterpret_cast<float*>(sm + kLCol);  // [strip][64]
-  float* sRed = reinterpret_cast<float*>(sm + kLRed);
-  const Tile tQ{s0 + kLQ, 8192}, tK{s0 + kLK, 8192}, tWt{s0 + kLWt, 16384}, tUt{s0 + kLUt, 16384},
-      tP{s0 + kLP, 8192}, tA{s0 + kLA, 8192}, tH{s0 + kLH, 16384}, tD{s0 + kLD, 16384}, tV{s0 + kLV, 8192},
-      tDo{s0 + kLDo, 8192}, tX{s0 + kLX, 8192}, tY{s0 + kLY, 8192};
-  const Tile tVp{s0 + kLUt, 8192}, tdVp{s0 + kLWt, 8192}, tdPG{s0 + kLP, 8192}, tYU{s0 + kLDo, 8192};
-  float mx = 0.f;
-  load_rows_f16(tQ, reinterpret_cast<const __nv_bfloat16*>(p.q), t0, p.h_qk, iq, cv, nullptr, mx);
-  load_rows_f16(tK, reinterpret_cast<const __nv_bfloat16*>(p.k), t0, p.h_qk, iq, cv, nullptr, mx);
-  __syncthreads();
-  const int rs = warp & 3, hf = warp >> 2, m0 = 16 * rs;
-  const int r_lo = m0 + (lane >> 2), cq = 2 * (lane & 3);
-  // Q K^T and K K^T of this warp's 16 x 32 block (shared by the group's heads)
-  float qk[4][4], kk[4][4];
-  zero(qk);
-  zero(kk);
-  warp_mma<4, 8, false, false>(qk, tQ, tK, m0, 32 * hf, 0);
-  warp_mma<4, 8, false, false>(kk, tK, tK, m0, 32 * hf, 0);
-  float dq[8][4], dk[8][4];
-  zero(dq);
-  zero(dk);
-  const int j_lo = (int)(((int64_t)iq * p.h_v + p.h_qk - 1) / p.h_qk);
-  const int j_hi = (int)(((int64_t)(iq + 1) * p.h_v + p.h_qk - 1) / p.h_qk);
-  for (int j = j_lo; j < j_hi; ++j) {
-    const int it = j - j_lo;
-    const size_t slot = (size_t)gc * p.h_v + j;
-    __syncthreads();  // the previous head's reads of every tile are done
-    if (tid == 0) {
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar, 2 * 16384u + 2 * 8192u + 2 * 32768u);
-      const uint8_t* rec = p.wy + slot * kRecBytes;
-      bulk_load(sm + kLWt, rec + kRecWn, 16384u, bar);
-      bulk_load(sm + kLUt, rec + kRecU, 16384u, bar);
-      bulk_load(sm + kLP, rec + kRecP, 8192u, bar);
-      bulk_load(sm + kLA, p.wyA + slot * 8192u, 8192u, bar);
-      bulk_load(sm + kLH, p.hchunk + slot * 32768u, 32768u, bar);
-      bulk_load(sm + kLD, b.dstate + slot * 32768u, 32768u, bar);
-    }
-    load_rows_f16(tV, reinterpret_cast<const __nv_bfloat16*>(p.v), t0, p.h_v, j, cv, nullptr, mx);
-    load_rows_f16(tDo, reinterpret_cast<const __nv_bfloat16*>(b.dout), t0, p.h_v, j, cv, nullptr, mx);
-    if (tid < 64) {  // G = inclusive cumulative gate (two warps, as the forward)
-      const int r = tid;
-      float x = r < cv ? p.g[(size_t)(t0 + r) * p.h_v + j] : 0.f;
-      sBeta[r] = r < cv ? p.beta[(size_t)(t0 + r) * p.h_v + j] : 0.f;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, x, d);
-        if (lane >= d) x += y;
-      }
-      if (lane == 31 && warp == 0) sRed[8] = x;
-      named_bar_sync(1, 64);
-      if (warp == 1) x += sRed[8];
-      sG[r] = x;
-      sGam[r] = __expf(x);
-    }
-    if (!loads_landed(bar, (uint32_t)(it & 1), p)) return;
-    if (tid < 64) sDec[tid] = __expf(sG[63] - sG[tid]);
-    // <D, H> (the gradient of gamma_C): thread: d_k row tid / 2, half of d_v
-    float dh = 0.f;
-    {
-      const int kd = tid >> 1, v0 = 64 * (tid & 1);
-#pragma unroll 2
-      for (int c = 0; c < 8; ++c) {
-        const uint4 dw = lds_u32x4(tD.at(kd, v0 + 8 * c));
-        const uint32_t dd[4] = {dw.x, dw.y, dw.z, dw.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 d2 = h2f(dd[e]);
-          const int v = v0 + 8 * c + 2 * e;
-          const float h0v = __half2float(__ushort_as_half((unsigned short)(lds_u32(tH.at(v, kd) & ~3u) >> (16 * (kd & 1)))));
-          const float h1v = __half2float(__ushort_as_half((unsigned short)(lds_u32(tH.at(v + 1, kd) & ~3u) >> (16 * (kd & 1)))));
-          dh = fmaf(d2.x, h0v, fmaf(d2.y, h1v, dh));
-        }
-      }
-#pragma unroll
-      for (int d = 16; d >= 1; d >>= 1) dh += __shfl_xor_sync(0xffffffffu, dh, d);
-      if (lane == 0) sRed[warp] = dh;
-    }
-    // ---- V' = U - W H ----
-    {
-      float acc[8][4];
-      zero(acc);
-      warp_mma<8, 8, true, false>(acc, tWt, tH, m0, 64 * hf, 0);
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int c = 64 * hf + 8 * t + cq;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int r = r_lo + 8 * (e >> 1), v = c + (e & 1);
-          const uint32_t w = lds_u32(tUt.at(v, r) & ~3u);
-          acc[t][e] += __half2float(__ushort_as_half((unsigned short)(w >> (16 * (r & 1)))));
-        }
-      }
-      __syncthreads();  // -W^T and U^T are read
-      store_frag(tVp, acc, m0, 64 * hf, mx);
-    }
-    // ---- dV' = scale P^T dO + diag(dec) K D ----
-    {
-      float acc[8][4];
-      zero(acc);
-      warp_mma<8, 8, false, true>(acc, tK, tD, m0, 64 * hf, 0);
-      const float f0 = sDec[r_lo] / p.scale, f1 = sDec[r_lo + 8] / p.scale;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        acc[t][0] *= f0;
-        acc[t][1] *= f0;
-        acc[t][2] *= f1;
-        acc[t][3] *= f1;
-      }
-      warp_mma<8, 4, true, true>(acc, tP, tDo, m0, 64 * hf, 0);
-#pragma unroll
-      for (int t = 0; t < 8; ++t)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[t][e] *= p.scale;
-      store_frag(tdVp, acc, m0, 64 * hf, mx);
-    }
-    __syncthreads();  // V', dV' stored; P is read
-    // ---- dP = scale dO V'^T (s <= r); dGam * Gam from it; dP * Gam ----
-    float Eg[4][4];
-    {
-      float acc[4][4];
-      zero(acc);
-      warp_mma<4, 8, false, false>(acc, tDo, tVp, m0, 32 * hf, 0);
-#pragma unroll
-      for (int t = 0; t < 4; ++t)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int r = r_lo + 8 * (e >> 1), s = 32 * hf + 8 * t + cq + (e & 1);
-          const float gam = s <= r ? __expf(sG[r] - sG[s]) : 0.f;
-          const float dP = s <= r ? p.scale * acc[t][e] : 0.f;
-          Eg[t][e] = dP * qk[t][e] * gam;
-          acc[t][e] = dP * gam;
-        }
-      store_frag(tdPG, acc, m0, 32 * hf, mx);
-    }
-    // ---- dQs = scale dO H^T: dq += diag(gamma) dQs; dgamma_r = <Q_r, dQs_r> ----
-    {
-      float acc[8][4];
-      zero(acc);
-      warp_mma<8, 8, false, true>(acc, tDo, tH, m0, 64 * hf, 0);
-      float p0 = 0.f, p1 = 0.f;
-      const float g0 = sGam[r_lo], g1 = sGam[r_lo + 8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int c = 64 * hf + 8 * t + cq;
-        const float2 q0 = h2f(lds_u32(tQ.at(r_lo, c))), q1 = h2f(lds_u32(tQ.at(r_lo + 8, c)));
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[t][e] *= p.scale;
-        p0 += q0.x * acc[t][0] + q0.y * acc[t][1];
-        p1 += q1.x * acc[t][2] + q1.y * acc[t][3];
-        dq[t][0] = fmaf(g0, acc[t][0], dq[t][0]);
-        dq[t][1] = fmaf(g0, acc[t][1], dq[t][1]);
-        dq[t][2] = fmaf(g1, acc[t][2], dq[t][2]);
-        dq[t][3] = fmaf(g1, acc[t][3], dq[t][3]);
-      }
-      p0 = quad_sum(p0);
-      p1 = quad_sum(p1);
-      if ((lane & 3) == 0) {
-        sRow[(kRowDgam * 2 + hf) * 64 + r_lo] = p0;
-        sRow[(kRowDgam * 2 + hf) * 64 + r_lo + 8] = p1;
-      }
-    }
-    __syncthreads();  // dP * Gam stored; dO is read
-    // ---- dq += (dP * Gam) K;  dk += (dP * Gam)^T Q ----
-    warp_mma<8, 4, false, true>(dq, tdPG, tK, m0, 64 * hf, 0);
-    warp_mma<8, 4, true, true>(dk, tdPG, tQ, m0, 64 * hf, 0);
-    // ---- Z = V' D^T: dk += diag(dec) Z; ddec_r = <K_r, Z_r> ----
-    {
-      float acc[8][4];
-      zero(acc);
-      warp_mma<8, 8, false, false>(acc, tVp, tD, m0, 64 * hf, 0);
-      const float d0 = sDec[r_lo], d1 = sDec[r_lo + 8];
-      float p0 = 0.f, p1 = 0.f;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int c = 64 * hf + 8 * t + cq;
-        const float2 k0 = h2f(lds_u32(tK.at(r_lo, c))), k1 = h2f(lds_u32(tK.at(r_lo + 8, c)));
-        p0 += k0.x * acc[t][0] + k0.y * acc[t][1];
-        p1 += k1.x * acc[t][2] + k1.y * acc[t][3];
-        dk[t][0] = fmaf(d0, acc[t][0], dk[t][0]);
-        dk[t][1] = fmaf(d0, acc[t][1], dk[t][1]);
-        dk[t][2] = fmaf(d1, acc[t][2], dk[t][2]);
-        dk[t][3] = fmaf(d1, acc[t][3], dk[t][3]);
-      }
-      p0 = quad_sum(p0);
-      p1 = quad_sum(p1);
-      if ((lane & 3) == 0) {
-        sRow[(kRowDdec * 2 + hf) * 64 + r_lo] = p0;
-        sRow[(kRowDdec * 2 + hf) * 64 + r_lo + 8] = p1;
-      }
-    }
-    // ---- Y_U = A^T dV': dv = diag(beta) Y_U; t1_r = <Y_U_r, V_r> ----
-    {
-      float acc[8][4];
-      zero(acc);
-      warp_mma<8, 4, false, true>(acc, tA, tdVp, m0, 64 * hf, 0);
-      const float b0 = sBeta[r_lo], b1 = sBeta[r_lo + 8];
-      float p0 = 0.f, p1 = 0.f;
-      __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(b.dv);
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int c = 64 * hf + 8 * t + cq;
-        const float2 v0 = h2f(lds_u32(tV.at(r_lo, c))), v1 = h2f(lds_u32(tV.at(r_lo + 8, c)));
-        p0 += v0.x * acc[t][0] + v0.y * acc[t][1];
-        p1 += v1.x * acc[t][2] + v1.y * acc[t][3];
-        if (r_lo < cv)
-          *reinterpret_cast<__nv_bfloat162*>(dv + ((size_t)(t0 + r_lo) * p.h_v + j) * kDim + c) =
-              __floats2bfloat162_rn(b0 * acc[t][0], b0 * acc[t][1]);
-        if (r_lo + 8 < cv)
-          *reinterpret_cast<__nv_bfloat162*>(dv + ((size_t)(t0 + r_lo + 8) * p.h_v + j) * kDim + c) =
-              __floats2bfloat162_rn(b1 * acc[t][2], b1 * acc[t][3]);
-      }
-      p0 = quad_sum(p0);
-      p1 = quad_sum(p1);
-      if ((lane & 3) == 0) {
-        sRow[(kRowT1 * 2 + hf) * 64 + r_lo] = p0;
-        sRow[(kRowT1 * 2 + hf) * 64 + r_lo + 8] = p1;
-      }
-      store_frag(tYU, acc, m0, 64 * hf, mx);
-    }
-    // ---- dV' V'^T ----
-    {
-      float acc[4][4];
-      zero(acc);
-      warp_mma<4, 8, false, false>(acc, tdVp, tVp, m0, 32 * hf, 0);
-      store_frag(tX, acc, m0, 32 * hf, mx);
-    }
-    __syncthreads();  // Y_U and dV' V'^T stored
-    // ---- Y_W = -Y_U H^T: dk += diag(beta gamma) Y_W; t2_r = <Y_W_r, K_r> ----
-    {
-      float acc[8][4];
-      zero(acc);
-      warp_mma<8, 8, false, true>(acc, tYU, tH, m0, 64 * hf, 0);
-      const float bg0 = sBeta[r_lo] * sGam[r_lo], bg1 = sBeta[r_lo + 8] * sGam[r_lo + 8];
-      float p0 = 0.f, p1 = 0.f;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int c = 64 * hf + 8 * t + cq;
-        const float2 k0 = h2f(lds_u32(tK.at(r_lo, c))), k1 = h2f(lds_u32(tK.at(r_lo + 8, c)));
-        p0 -= k0.x * acc[t][0] + k0.y * acc[t][1];
-        p1 -= k1.x * acc[t][2] + k1.y * acc[t][3];
-        dk[t][0] = fmaf(-bg0, acc[t][0], dk[t][0]);
-        dk[t][1] = fmaf(-bg0, acc[t][1], dk[t][1]);
-        dk[t][2] = fmaf(-bg1, acc[t][2], dk[t][2]);
-        dk[t][3] = fmaf(-bg1, acc[t][3], dk[t][3]);
-      }
-      p0 = quad_sum(p0);
-      p1 = quad_sum(p1);
-      if ((lane & 3) == 0) {
-        sRow[(kRowT2 * 2 + hf) * 64 + r_lo] = p0;
-        sRow[(kRowT2 * 2 + hf) * 64 + r_lo + 8] = p1;
-      }
-    }
-    // ---- dL = -A^T (dV' V'^T), s < r: dKK = dL beta Gam; dbeta, dGam from L ----
-    {
-      float acc[4][4];
-      zero(acc);
-      warp_mma<4, 4, false, true>(acc, tA, tX, m0, 32 * hf, 0);
-      const float b0 = sBeta[r_lo], b1 = sBeta[r_lo + 8];
-      float p0 = 0.f, p1 = 0.f;
-#pragma unroll
-      for (int t = 0; t < 4; ++t)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int r = r_lo + 8 * (e >> 1), s = 32 * hf + 8 * t + cq + (e & 1);
-          const float gam = s < r ? __expf(sG[r] - sG[s]) : 0.f;
-          const float dL = s < r ? -acc[t][e] : 0.f;
-          const float br = (e >> 1) ? b1 : b0;
-          const float x = dL * kk[t][e] * gam;
-          if (e >> 1) p1 += x; else p0 += x;
-          Eg[t][e] += br * x;
-          acc[t][e] = dL * br * gam;
-        }
-      p0 = quad_sum(p0);
-      p1 = quad_sum(p1);
-      if ((lane & 3) == 0) {
-        sRow[(kRowDbL * 2 + hf) * 64 + r_lo] = p0;
-        sRow[(kRowDbL * 2 + hf) * 64 + r_lo + 8] = p1;
-      }
-      store_frag(tY, acc, m0, 32 * hf, mx);
-      // row and column sums of dGam * Gam
-      float e0 = 0.f, e1 = 0.f;
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        e0 += Eg[t][0] + Eg[t][1];
-        e1 += Eg[t][2] + Eg[t][3];
-      }
-      e0 = quad_sum(e0);
-      e1 = quad_sum(e1);
-      if ((lane & 3) == 0) {
-        sRow[(kRowErow * 2 + hf) * 64 + r_lo] = e0;
-        sRow[(kRowErow * 2 + hf) * 64 + r_lo + 8] = e1;
-      }
-#pragma unroll
-      for (int t = 0; t < 4; ++t)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float c = Eg[t][h] + Eg[t][2 + h];
-          c += __shfl_xor_sync(0xffffffffu, c, 4);
-          c += __shfl_xor_sync(0xffffffffu, c, 8);
-          c += __shfl_xor_sync(0xffffffffu, c, 16);
-          if (lane < 4) sCol[rs * 64 + 32 * hf + 8 * t + cq + h] = c;
-        }
-    }
-    __syncthreads();  // dKK stored; the partial sums are in
-    // ---- dk += (dKK + dKK^T) K ----
-    warp_mma<8, 4, false, true>(dk, tY, tK, m0, 64 * hf, 0);
-    warp_mma<8, 4, true, true>(dk, tY, tK, m0, 64 * hf, 0);
-    // ---- the gates: dG, then dg = its reverse cumulative sum; dbeta ----
-    if (tid < 64) {
-      const int r = tid;
-      auto row = [&](int kind) { return sRow[(kind * 2) * 64 + r] + sRow[(kind * 2 + 1) * 64 + r]; };
-      const float t2 = row(kRowT2);
-      const float dgam = row(kRowDgam) + sBeta[r] * t2;
-      const float dbeta = row(kRowT1) + sGam[r] * t2 + row(kRowDbL);
-      const float ddec = row(kRowDdec);
-      const float ecol = sCol[r] + sCol[64 + r] + sCol[128 + r] + sCol[192 + r];
-      float dG = dgam * sGam[r] + row(kRowErow) - ecol - ddec * sDec[r];
-      float dd = ddec * sDec[r];  // sum over the chunk of ddec dec, added to the last row
-#pragma unroll
-      for (int d = 16; d >= 1; d >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, d);
-      if (lane == 0) sRed[9 + warp] = dd;
-      named_bar_sync(1, 64);
-      if (r == 63) {
-        float dgc = 0.f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) dgc += sRed[w];
-        dG += dgc * sGam[63] + sRed[9] + sRed[10];
-      }
-      // reverse cumulative sum over the 64 rows (warp 1 holds rows 32-63)
-      float x = dG;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const float y = __shfl_down_sync(0xffffffffu, x, d);
-        if (lane + d < 32) x += y;
-      }
-      if (warp == 1 && lane == 0) sRed[11] = x;
-      named_bar_sync(1, 64);
-      if (warp == 0) x += sRed[11];
-      if (r < cv) {
-        b.dg[(size_t)(t0 + r) * p.h_v + j] = x;
-        b.dbeta[(size_t)(t0 + r) * p.h_v + j] = dbeta;
-      }
-    }
-  }
-  // ---- dq, dk of the q/k head (summed over its value heads), bf16 ----
-  __nv_bfloat16* dqo = reinterpret_cast<__nv_bfloat16*>(b.dq);
-  __nv_bfloat16* dko = reinterpret_cast<__nv_bfloat16*>(b.dk);
-#pragma unroll
-  for (int t = 0; t < 8; ++t) {
-    const int c = 64 * hf + 8 * t + cq;
-    if (r_lo < cv) {
-      const size_t o = ((size_t)(t0 + r_lo) * p.h_qk + iq) * kDim + c;
-      *reinterpret_cast<__nv_bfloat162*>(dqo + o) = __floats2bfloat162_rn(dq[t][0], dq[t][1]);
-      *reinterpret_cast<__nv_bfloat162*>(dko + o) = __floats2bfloat162_rn(dk[t][0], dk[t][1]);
-    }
-    if (r_lo + 8 < cv) {
-      const size_t o = ((size_t)(t0 + r_lo + 8) * p.h_qk + iq) * kDim + c;
-      *reinterpret_cast<__nv_bfloat162*>(dqo + o) = __floats2bfloat162_rn(dq[t][2], dq[t][3]);
-      *reinterpret_cast<__nv_bfloat162*>(dko + o) = __floats2bfloat162_rn(dk[t][2], dk[t][3]);
-    }
-  }
-  if (!(mx < 65504.f)) report(p.status, kDevCheck, kDetFp16Range);
-}
-
 }  // namespace
 
 namespace {
@@ -877,8 +465,6 @@ cudaError_t bwd_attrs() {
       e = cudaFuncSetAttribute(bwd_chain_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kChSmem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(bwd_chain_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kChSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(bwd_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLocalSmem);
     return e;
   }();
   return once;
@@ -899,9 +485,5 @@ cudaError_t launch_bwd_chain(const Problem& p, const BwdArgs& b, bool prep, cuda
   return launch_kernel(bwd_chain_kernel<false>, dim3(p.n_seg_total, p.h_v), dim3(kBwdThreads), kChSmem, st, true, p, b);
 }
 
-cudaError_t launch_bwd_local(const Problem& p, const BwdArgs& b, cudaStream_t st) {
-  const unsigned grid = (unsigned)p.n_chunks_total * (unsigned)p.h_qk;
-  return launch_kernel(bwd_local_kernel, dim3(grid), dim3(kBwdThreads), kLocalSmem, st, true, p, b);
-}
 
 }  // namespace gdn
