@@ -449,7 +449,7 @@ __device__ __forceinline__ void output_role(uint8_t* sm, Ctl* ctl, const Problem
 }
 
 // ----------------------------------------------------------------- state (chain) warps
-template <bool PREP>
+template <bool PREP, bool DUMP>
 __device__ __forceinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem& p, const SegInfo& si,
                                         const Chain& ch, uint32_t tmem, int j, int chain) {
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -485,9 +485,9 @@ __device__ __forceinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem&
   float mx = 0.f;
   // The state's fp16 copy for chunk c into TMEM buffer c & 1: this thread's
   // row, its 64 columns packed into 32 (columns 32 half .. 32 half + 31).
-  // For the backward, the copy of each output chunk's start state also goes to
-  // p.hchunk (row = this thread's d_v, panel = half).
-  uint8_t* const hdump = (!PREP && p.hchunk)
+  // DUMP (the backward's recompute): the copy of each output chunk's start
+  // state also goes to p.hchunk (row = this thread's d_v, panel = half).
+  uint8_t* const hdump = (DUMP && !PREP)
                              ? p.hchunk + ((size_t)(ch.chunk0 + ch.run_begin) * p.h_v + j) * 32768u +
                                    (size_t)half * 16384u
                              : nullptr;
@@ -496,7 +496,7 @@ __device__ __forceinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem&
 #pragma unroll
     for (int q = 0; q < 32; ++q) w[q] = pack_f16x2(S[2 * q], S[2 * q + 1]);
     tmem_st32(tmem + lane_base + kTS + (c & 1) * 64 + half * 32, w);
-    if (hdump && c < n && ch.run_begin + c >= ch.out_begin) {
+    if (DUMP && c < n && ch.run_begin + c >= ch.out_begin) {
       uint8_t* dst = hdump + (size_t)c * p.h_v * 32768u;
 #pragma unroll
       for (int q = 0; q < 8; ++q)
@@ -588,7 +588,7 @@ __device__ __forceinline__ void chain_role(uint8_t* sm, Ctl* ctl, const Problem&
   }
 }
 
-template <bool PREP>
+template <bool PREP, bool DUMP = false>
 __global__ void __launch_bounds__(kThreads, 1)
     scan_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                 const __grid_constant__ CUtensorMap mo, const Problem p) {
@@ -733,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 8) {
     setmaxnreg_inc<kChainRegs>();
-    chain_role<PREP>(sm, ctl, p, si, ch, tmem, j, chain);
+    chain_role<PREP, DUMP>(sm, ctl, p, si, ch, tmem, j, chain);
   } else {
     setmaxnreg_dec<kOtherRegs>();
     if (warp < kOutWarp + 4) {
@@ -772,6 +772,8 @@ cudaError_t scan_kernel_setup() {
   cudaError_t e = cudaFuncSetAttribute(scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemAlloc);
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(scan_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+  if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
 }
 
@@ -784,6 +786,8 @@ cudaError_t launch_scan_prep(const Problem& p, const CUtensorMap& mq, const CUte
 cudaError_t launch_scan_out(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mo,
                             int grid_x, cudaStream_t st) {
   dim3 grid(grid_x, p.h_v, 1);
+  if (p.hchunk)  // the backward's recompute: also keeps every chunk's start state
+    return launch_kernel(scan_kernel<false, true>, grid, dim3(kThreads), kSmemAlloc, st, true, mq, mk, mo, p);
   return launch_kernel(scan_kernel<false>, grid, dim3(kThreads), kSmemAlloc, st, true, mq, mk, mo, p);
 }
 
