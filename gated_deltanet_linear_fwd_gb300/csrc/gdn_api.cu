@@ -651,7 +651,7 @@ gdn_status gdn_chunk_bwd(const void* q, const void* k, const void* v, const floa
   if (p.plan_mode != kModeOff) {
     // context parallel: per segment the transition and the local offset, then
     // the segments' end-state gradients by the combine run backwards
-    if ((e = log.before(cs)) != cudaSuccess || (e = launch_bwd_chain(p, b, true, cs)) != cudaSuccess ||
+    if ((e = log.before(cs)) != cudaSuccess || (e = launch_bwd_chain_tc(p, b, true, cs)) != cudaSuccess ||
         (e = log.after("bwd_chain_prep", cs)) != cudaSuccess)
       return cuda_fail(e);
     Problem pc = p;
@@ -660,7 +660,7 @@ gdn_status gdn_chunk_bwd(const void* q, const void* k, const void* v, const floa
         (e = log.after("bwd_combine", cs)) != cudaSuccess)
       return cuda_fail(e);
   }
-  if ((e = log.before(cs)) != cudaSuccess || (e = launch_bwd_chain(p, b, false, cs)) != cudaSuccess ||
+  if ((e = log.before(cs)) != cudaSuccess || (e = launch_bwd_chain_tc(p, b, false, cs)) != cudaSuccess ||
       (e = log.after("bwd_chain", cs)) != cudaSuccess)
     return cuda_fail(e);
   if ((e = log.before(cs)) != cudaSuccess || (e = launch_bwd_local_tc(p, b, cs)) != cudaSuccess ||

@@ -17,11 +17,12 @@
 // Three kernels after a forward pass that also leaves each chunk's start state
 // and A^T (fp16):
 //   bwd_pre_kernel    per (chunk, value head): T' and E            (chunk-parallel)
-//   bwd_chain_kernel  per (sequence, value head): D over the chunks in reverse,
-//                     D kept in fp32; writes every chunk's D (fp16) and dh0
+//   bwd_chain_tc_kernel (gdn_bwd_tc.cu) per segment and value head: D over the
+//                     chunks in reverse, D kept in fp32; writes every chunk's D
+//                     (fp16) and dh0; context parallel like the forward
 //   bwd_local_tc_kernel (gdn_bwd_tc.cu) per (chunk, q/k head), over the value
 //                     heads of the group: every other gradient on tcgen05
-// The two kernels here run their products on the tensor cores through mma.sync
+// bwd_pre_kernel runs its products on the tensor cores through mma.sync
 // m16n8k16 (fp16 operands in the forward's 128-byte-swizzled tile image, fp32
 // accumulators); tiles arrive by bulk copies on an mbarrier with a bounded wait.
 #include <cuda_fp16.h>
@@ -295,176 +296,12 @@ __global__ void __launch_bounds__(kBwdThreads, 2) bwd_pre_kernel(const Problem p
   if (!(mx < 65504.f)) report(p.status, kDevCheck, kDetFp16Range);
 }
 
-// ---------------------------------------------------------------- bwd_chain
-// The gradient of the state over one segment's chunks, in reverse: per chunk
-// c, D <- gamma_C D + E_c + T'_c D (D in fp32 accumulators; the product reads
-// its fp16 copy; T' and E arrive a step ahead).
-//   final (PREP = false; grid x = segment): D starts from the gradient of the
-//     segment's end state (dh_T for a sequence's last segment, else the
-//     combine's D_end), writes every chunk's D before its step (fp16, rows
-//     d_k, panels d_v 0-63 | 64-127) and, for a sequence's first segment, dh0.
-//   preprocessing (PREP; grid x = 2 segment + chain): chain 0 runs the
-//     transition (D from I, no E), chain 1 the local offset (D from 0); both
-//     are stored transposed for the backward combine (p.R, p.Sloc).
-// Without context parallelism every sequence is one segment.
-constexpr uint32_t kChT = 0;                  // 2 x T' (32 KB)
-constexpr uint32_t kChE = 65536;              // 2 x E (32 KB)
-constexpr uint32_t kChD = 131072;             // 2 x D, fp16 (32 KB)
-constexpr uint32_t kChBar = 196608;           // 2 load barriers
-constexpr uint32_t kChSmem = kChBar + 64 + 1024;
-
-template <bool PREP>
-__global__ void __launch_bounds__(kBwdThreads, 1) bwd_chain_kernel(const Problem p, const BwdArgs b) {
-  uint8_t* sm = smem_base();
-  const uint32_t s0 = smem_u32(sm);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kChBar);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int j = blockIdx.y;
-  const int chain = PREP ? (int)(blockIdx.x & 1) : 0;
-  const int seg = PREP ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  __shared__ SegInfo s_si;
-  __shared__ int s_ok;
-  if (warp == 0) {
-    SegInfo si;
-    const bool ok = locate_segment(p, seg, si);
-    if (lane == 0) {
-      s_si = si;
-      s_ok = ok;
-    }
-  }
-  if (tid == 32) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
-    fence_mbar_init();
-  }
-  grid_dependency_wait();
-  grid_launch_dependents();
-  if (__syncthreads_or(tid == 0 && earlier_failure(p.status))) return;
-  const SegInfo si = s_si;
-  if (!s_ok) {
-    if (tid == 0) report(p.status, kDevCheck, kDetSegMismatch);
-    return;
-  }
-  const bool last_seg = si.s == si.n_seg - 1;
-  if (PREP) {
-    if (si.s == 0) return;                                        // segment 0 is taken by the final pass
-    if (chain == 0 && last_seg && b.dhT == nullptr) return;       // its transition would act on zero
-  }
-  const int c0 = seq_first_chunk(p, si.n) + si.cb, nc = si.ce - si.cb;
-  const size_t mat = (size_t)kDim * kDim;
-  const size_t head_seg = ((size_t)(si.seg_base + si.s) * p.h_v + j) * mat;
-  // D: rows 16 warp + lane/4 (+8) of d_k, columns 8 t + 2 (lane % 4) of d_v
-  const int m0 = 16 * warp, r = m0 + (lane >> 2), cq = 2 * (lane & 3);
-  float acc[16][4];
-  if (PREP) {
-#pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      acc[t][0] = (chain == 0 && r == 8 * t + cq) ? 1.f : 0.f;
-      acc[t][1] = (chain == 0 && r == 8 * t + cq + 1) ? 1.f : 0.f;
-      acc[t][2] = (chain == 0 && r + 8 == 8 * t + cq) ? 1.f : 0.f;
-      acc[t][3] = (chain == 0 && r + 8 == 8 * t + cq + 1) ? 1.f : 0.f;
-    }
-  } else if (!last_seg) {  // D_end of this segment from the combine, stored transposed (rows d_v)
-    const float* src = p.Sstart + head_seg;
-#pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      const int c = 8 * t + cq;
-      acc[t][0] = src[(size_t)c * kDim + r];
-      acc[t][1] = src[(size_t)(c + 1) * kDim + r];
-      acc[t][2] = src[(size_t)c * kDim + r + 8];
-      acc[t][3] = src[(size_t)(c + 1) * kDim + r + 8];
-    }
-  } else if (b.dhT) {
-    const float* src = b.dhT + ((size_t)si.n * p.h_v + j) * mat;
-#pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      const float2 lo = *reinterpret_cast<const float2*>(src + (size_t)r * kDim + 8 * t + cq);
-      const float2 hi = *reinterpret_cast<const float2*>(src + (size_t)(r + 8) * kDim + 8 * t + cq);
-      acc[t][0] = lo.x;
-      acc[t][1] = lo.y;
-      acc[t][2] = hi.x;
-      acc[t][3] = hi.y;
-    }
-  } else {
-    zero(acc);
-  }
-  const bool with_e = !(PREP && chain == 0);
-  float mx = 0.f;
-  const Tile tD0{s0 + kChD, 16384}, tD1{s0 + kChD + 32768, 16384};
-  store_frag(tD0, acc, m0, 0, mx);
-  auto issue = [&](int it) {  // T' (and E) of step it into buffer it & 1
-    const int c = c0 + nc - 1 - it;
-    const size_t slot = ((size_t)c * p.h_v + j) * 32768u;
-    const uint32_t buf = (uint32_t)(it & 1) * 32768u;
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(&bar[it & 1], with_e ? 65536u : 32768u);
-    bulk_load(sm + kChT + buf, b.tmat + slot, 32768u, &bar[it & 1]);
-    if (with_e) bulk_load(sm + kChE + buf, b.emat + slot, 32768u, &bar[it & 1]);
-  };
-  if (tid == 0 && nc > 0) issue(0);
-  for (int it = 0; it < nc; ++it) {
-    const int c = c0 + nc - 1 - it;
-    const float gC = reinterpret_cast<const float*>(p.wy + ((size_t)c * p.h_v + j) * kRecBytes + kRecGam)[63];
-    __syncthreads();  // buffer (it + 1) & 1 and D tile (it + 1) & 1 were last read in step it - 1
-    if (tid == 0 && it + 1 < nc) issue(it + 1);
-    if (!loads_landed(&bar[it & 1], (uint32_t)((it >> 1) & 1), p)) return;
-    const Tile tD = (it & 1) ? tD1 : tD0, tDn = (it & 1) ? tD0 : tD1;
-    const uint32_t buf = (uint32_t)(it & 1) * 32768u;
-    const Tile tT{s0 + kChT + buf, 16384}, tE{s0 + kChE + buf, 16384};
-    if (!PREP) {  // D_c (the gradient of chunk c's end state) for the per-chunk gradients
-      uint8_t* dst = b.dstate + ((size_t)c * p.h_v + j) * 32768u;
-      for (int idx = tid; idx < 2048; idx += kBwdThreads)
-        *reinterpret_cast<uint4*>(dst + idx * 16) = lds_u32x4(tD.base + idx * 16);
-    }
-    if (with_e) {
-#pragma unroll
-      for (int t = 0; t < 16; ++t) {
-        const float2 e0 = h2f(lds_u32(tE.at(r, 8 * t + cq))), e1 = h2f(lds_u32(tE.at(r + 8, 8 * t + cq)));
-        acc[t][0] = fmaf(gC, acc[t][0], e0.x);
-        acc[t][1] = fmaf(gC, acc[t][1], e0.y);
-        acc[t][2] = fmaf(gC, acc[t][2], e1.x);
-        acc[t][3] = fmaf(gC, acc[t][3], e1.y);
-      }
-    } else {
-#pragma unroll
-      for (int t = 0; t < 16; ++t)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[t][e] *= gC;
-    }
-    warp_mma<16, 8, false, true>(acc, tT, tD, m0, 0, 0);
-    store_frag(tDn, acc, m0, 0, mx);
-  }
-  if (PREP) {  // transposed (rows d_v, or the transition's column index) for the combine
-    float* dst = (chain == 0 ? p.R : p.Sloc) + head_seg;
-#pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      const int c = 8 * t + cq;
-      dst[(size_t)c * kDim + r] = acc[t][0];
-      dst[(size_t)(c + 1) * kDim + r] = acc[t][1];
-      dst[(size_t)c * kDim + r + 8] = acc[t][2];
-      dst[(size_t)(c + 1) * kDim + r + 8] = acc[t][3];
-    }
-  } else if (si.s == 0 && b.dh0) {
-    float* dst = b.dh0 + ((size_t)si.n * p.h_v + j) * mat;
-#pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      *reinterpret_cast<float2*>(dst + (size_t)r * kDim + 8 * t + cq) = make_float2(acc[t][0], acc[t][1]);
-      *reinterpret_cast<float2*>(dst + (size_t)(r + 8) * kDim + 8 * t + cq) = make_float2(acc[t][2], acc[t][3]);
-    }
-  }
-  if (!(mx < 65504.f)) report(p.status, kDevCheck, kDetFp16Range);
-}
-
 }  // namespace
 
 namespace {
 cudaError_t bwd_attrs() {
   static cudaError_t once = [] {
     cudaError_t e = cudaFuncSetAttribute(bwd_pre_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPreSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(bwd_chain_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kChSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(bwd_chain_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kChSmem);
     return e;
   }();
   return once;
@@ -478,12 +315,6 @@ cudaError_t launch_bwd_pre(const Problem& p, const BwdArgs& b, cudaStream_t st) 
   return launch_kernel(bwd_pre_kernel, dim3(grid), dim3(kBwdThreads), kPreSmem, st, true, p, b);
 }
 
-cudaError_t launch_bwd_chain(const Problem& p, const BwdArgs& b, bool prep, cudaStream_t st) {
-  if (prep)
-    return launch_kernel(bwd_chain_kernel<true>, dim3(2 * p.n_seg_total, p.h_v), dim3(kBwdThreads), kChSmem, st, true,
-                         p, b);
-  return launch_kernel(bwd_chain_kernel<false>, dim3(p.n_seg_total, p.h_v), dim3(kBwdThreads), kChSmem, st, true, p, b);
-}
 
 
 }  // namespace gdn

@@ -694,7 +694,236 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_local_tc_kernel(const Probl
   }
 }
 
+
+// ------------------------------------------------------------ state-gradient chain
+// One chain over one segment's chunks in reverse, D <- gamma_C D + E_c + T'_c D_c:
+// the product on tcgen05 (M = d_k out, N = d_v, K = d_k in; A = T' from the
+// record, B = D's fp16 copy in shared memory), D itself in fp32 registers
+// (thread: TMEM lane = row d_k, 64 of the 128 columns).  Modes as the
+// mma.sync chain in gdn_bwd.cu: final (PREP = false) writes every chunk's D
+// before its step (fp16 tile image) and dh0 for a sequence's first segment;
+// preprocessing (PREP) runs the transition (chain 0, from I, no E) or the
+// local offset (chain 1, from 0) and stores it transposed for the combine.
+constexpr uint32_t cT = 0;          // 2 x T' (32 KB): rows d_k out, panels d_k in 0-63 | 64-127
+constexpr uint32_t cE = 65536;      // 2 x E (32 KB): rows d_k, panels d_v
+constexpr uint32_t cD = 131072;     // D's fp16 copy: rows d_k (K), panels d_v 0-63 | 64-127
+constexpr uint32_t cCtl = 163840;
+constexpr uint32_t kChainSmem = cCtl + 128 + 1024;
+
+struct ChCtl {
+  uint64_t load[2], mma;
+  uint32_t tmem;
+  int abort;
+  SegInfo si;
+  int ok;
+};
+
+template <bool PREP>
+__global__ void __launch_bounds__(kTcThreads, 1) bwd_chain_tc_kernel(const Problem p, const BwdArgs b) {
+  uint8_t* sm = tc_smem_base();
+  const uint32_t s0 = smem_u32(sm);
+  ChCtl* ctl = reinterpret_cast<ChCtl*>(sm + cCtl);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q = warp & 3, h = warp >> 2, k = 32 * q + lane;
+  const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+  const int j = blockIdx.y;
+  const int chain = PREP ? (int)(blockIdx.x & 1) : 0;
+  const int seg = PREP ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  if (warp == 1) {
+    SegInfo si;
+    const bool okseg = locate_segment(p, seg, si);
+    if (lane == 0) {
+      ctl->si = si;
+      ctl->ok = okseg;
+    }
+  }
+  if (tid == 0) {
+    mbar_init(&ctl->load[0], 1);
+    mbar_init(&ctl->load[1], 1);
+    mbar_init(&ctl->mma, 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&ctl->tmem, 128);
+    tmem_relinquish();
+  }
+  grid_dependency_wait();
+  grid_launch_dependents();
+  tc_fence_before();
+  const bool failed = __syncthreads_or(tid == 0 && earlier_failure(p.status));
+  tc_fence_after();
+  const uint32_t tm = ctl->tmem;
+  const SegInfo si = ctl->si;
+  bool run = !failed && ctl->ok;
+  if (!failed && !ctl->ok && tid == 0) report(p.status, kDevCheck, kDetSegMismatch);
+  const bool last_seg = si.s == si.n_seg - 1;
+  if (PREP && run) {
+    if (si.s == 0) run = false;                                   // segment 0 is taken by the final pass
+    if (chain == 0 && last_seg && b.dhT == nullptr) run = false;  // its transition would act on zero
+  }
+  const int c0 = run ? seq_first_chunk(p, si.n) + si.cb : 0, nc = run ? si.ce - si.cb : 0;
+  const size_t mat = (size_t)kDim * kDim;
+  const size_t head_seg = ((size_t)(si.seg_base + si.s) * p.h_v + j) * mat;
+  const bool with_e = !(PREP && chain == 0);
+  float D[64];  // row k, columns 64 h .. 64 h + 63
+  if (run) {
+    if (PREP) {
+#pragma unroll
+      for (int e = 0; e < 64; ++e) D[e] = (chain == 0 && 64 * h + e == k) ? 1.f : 0.f;
+    } else if (!last_seg) {  // D_end of this segment from the combine, stored transposed (rows d_v)
+      const float* src = p.Sstart + head_seg;
+#pragma unroll
+      for (int e = 0; e < 64; ++e) D[e] = src[(size_t)(64 * h + e) * kDim + k];
+    } else if (b.dhT) {
+      const float4* src = reinterpret_cast<const float4*>(b.dhT + ((size_t)si.n * p.h_v + j) * mat + (size_t)k * kDim + 64 * h);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const float4 v4 = src[e];
+        D[4 * e] = v4.x;
+        D[4 * e + 1] = v4.y;
+        D[4 * e + 2] = v4.z;
+        D[4 * e + 3] = v4.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 64; ++e) D[e] = 0.f;
+    }
+  }
+  float mx = 0.f;
+  // D's fp16 copy as row k of the tile (panel h), and as chunk c's record when asked
+  auto store_d = [&](uint8_t* global_row) {
+    uint32_t w[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      mx = absmax_nan(absmax_nan(mx, D[2 * e]), D[2 * e + 1]);
+      w[e] = pack_f16x2(D[2 * e], D[2 * e + 1]);
+    }
+    const uint32_t panel = s0 + cD + (uint32_t)h * 16384u;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      st_shared_v4(panel + sw128_offset((uint32_t)k, (uint32_t)c), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+      if (global_row)
+        *reinterpret_cast<uint4*>(global_row + sw128_offset((uint32_t)k, (uint32_t)c)) =
+            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    }
+  };
+  auto issue = [&](int it) {  // T' (and E) of step it into buffer it & 1 (one thread)
+    const int c = c0 + nc - 1 - it;
+    const size_t slot = ((size_t)c * p.h_v + j) * 32768u;
+    const uint32_t buf = (uint32_t)(it & 1) * 32768u;
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(&ctl->load[it & 1], with_e ? 65536u : 32768u);
+    bulk_load(sm + cT + buf, b.tmat + slot, 32768u, &ctl->load[it & 1]);
+    if (with_e) bulk_load(sm + cE + buf, b.emat + slot, 32768u, &ctl->load[it & 1]);
+  };
+  if (tid == 0 && nc > 0) issue(0);
+  bool ok = true;
+  if (nc > 0) {
+    // the first step's D_c is D itself
+    store_d(PREP ? nullptr : b.dstate + ((size_t)(c0 + nc - 1) * p.h_v + j) * 32768u + (size_t)h * 16384u);
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  for (int it = 0; it < nc && ok; ++it) {
+    const int c = c0 + nc - 1 - it;
+    const uint32_t buf = (uint32_t)(it & 1) * 32768u;
+    const float gC = reinterpret_cast<const float*>(p.wy + ((size_t)c * p.h_v + j) * kRecBytes + kRecGam)[63];
+    if (!mbar_wait(&ctl->load[it & 1], (uint32_t)((it >> 1) & 1), kWaitLimitNs)) atomicCAS(&ctl->abort, 0, kDetTmaWait);
+    if (tid == 0 && !ctl->abort) {  // T'_c D_c
+      tc_fence_after();
+      const uint32_t id = idesc_f16(128, 128, false, true);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_bf16(tm, dk_(s0 + cT + buf, ks, 16384), dmn_(s0 + cD, ks, 16384), id, ks > 0);
+      mma_commit(&ctl->mma);
+      if (it + 1 < nc) issue(it + 1);  // buffer (it + 1) & 1 was last read in step it - 1
+    }
+    // E_c and gamma_C D while the product runs
+    if (with_e) {
+      const uint32_t epanel = s0 + cE + buf + (uint32_t)h * 16384u;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        const uint4 w = lds_u32x4(epanel + sw128_offset((uint32_t)k, (uint32_t)c8));
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[e]));
+          D[8 * c8 + 2 * e] = fmaf(gC, D[8 * c8 + 2 * e], f.x);
+          D[8 * c8 + 2 * e + 1] = fmaf(gC, D[8 * c8 + 2 * e + 1], f.y);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 64; ++e) D[e] *= gC;
+    }
+    if (!wait_phase(&ctl->mma, (uint32_t)(it & 1), &ctl->abort, 210)) ok = false;
+    tc_fence_after();
+    if (__syncthreads_or(!ok || ctl->abort)) {
+      ok = false;
+      break;
+    }
+    {
+      float a[32];
+      ld32(tm + lane_base + 64 * h, a);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) D[e] += a[e];
+      ld32(tm + lane_base + 64 * h + 32, a);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) D[32 + e] += a[e];
+    }
+    // D_{c-1} for the next step (and as the previous chunk's record)
+    if (it + 1 < nc)
+      store_d(PREP ? nullptr : b.dstate + ((size_t)(c - 1) * p.h_v + j) * 32768u + (size_t)h * 16384u);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+  }
+  if (run && ok && !ctl->abort) {
+    if (PREP) {  // transposed (rows d_v, or the transition's column index) for the combine
+      float* dst = (chain == 0 ? p.R : p.Sloc) + head_seg;
+#pragma unroll
+      for (int e = 0; e < 64; ++e) dst[(size_t)(64 * h + e) * kDim + k] = D[e];
+    } else if (si.s == 0 && b.dh0) {
+      float4* dst = reinterpret_cast<float4*>(b.dh0 + ((size_t)si.n * p.h_v + j) * mat + (size_t)k * kDim + 64 * h);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) dst[e] = make_float4(D[4 * e], D[4 * e + 1], D[4 * e + 2], D[4 * e + 3]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (ctl->abort || !ok) {
+    if (tid == 0) report(p.status, kDevTimeout, ctl->abort ? ctl->abort : kDetMmaWait);
+    const uint64_t t_start = globaltimer_ns();
+    while (globaltimer_ns() - t_start < 2000000ull) {
+    }
+    __syncthreads();
+  }
+  if (!(mx < 65504.f)) report(p.status, kDevCheck, kDetFp16Range);
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tm, 128);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_bwd_chain_tc(const Problem& p, const BwdArgs& b, bool prep, cudaStream_t st) {
+  static const cudaError_t attr = [] {
+    cudaError_t e = cudaFuncSetAttribute(bwd_chain_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kChainSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(bwd_chain_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kChainSmem);
+    return e;
+  }();
+  if (attr != cudaSuccess) return attr;
+  if (prep)
+    return launch_kernel(bwd_chain_tc_kernel<true>, dim3(2 * p.n_seg_total, p.h_v), dim3(kTcThreads), kChainSmem, st,
+                         true, p, b);
+  return launch_kernel(bwd_chain_tc_kernel<false>, dim3(p.n_seg_total, p.h_v), dim3(kTcThreads), kChainSmem, st, true,
+                       p, b);
+}
 
 cudaError_t launch_bwd_local_tc(const Problem& p, const BwdArgs& b, cudaStream_t st) {
   static const cudaError_t attr =

@@ -197,8 +197,10 @@ cudaError_t combine_kernel_setup() {
 
 template <bool BWD>
 static cudaError_t launch_combine_dir(const Problem& p, int sm_count, cudaStream_t st) {
-  // 32 CTAs of 4 rows per exact (sequence, head) if even all pairs fit in about two waves
-  if ((int64_t)p.n_seqs * p.h_v * 32 <= 2 * (int64_t)sm_count)
+  // 32 CTAs of 4 rows per exact (sequence, head) if they fit in about two waves when
+  // all pairs are launched (the forward: only the exact heads' blocks stay), in one
+  // wave for the backward (every head is exact there)
+  if ((int64_t)p.n_seqs * p.h_v * 32 <= (BWD ? 1 : 2) * (int64_t)sm_count)
     return launch_kernel(combine_kernel<4, BWD>, dim3(p.n_seqs * (kDim / 4), p.h_v), dim3(256), combine_smem<4>(), st,
                          true, p);
   return launch_kernel(combine_kernel<8, BWD>, dim3(p.n_seqs * (kDim / 8), p.h_v), dim3(256), combine_smem<8>(), st,
