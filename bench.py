@@ -317,6 +317,51 @@ def time_bwd(name, steps, warmup, device, cp="auto"):
             "grads": [x.cpu() for x in grads]}
 
 
+def time_train_step(name, steps, warmup, device, cp="auto"):
+    """A training step as a user runs it: gdn_chunk_fwd(for_backward=True), then
+    gdn_chunk_bwd(reuse_forward=True) on the same plan and workspace (no recompute);
+    also the training forward alone."""
+    from gated_deltanet_linear_fwd_gb300 import gdn_bwd_workspace_bytes, gdn_chunk_bwd, gdn_chunk_fwd, gdn_cp_plan
+    from gated_deltanet_linear_fwd_gb300.inputs import make_output_grads, workload
+    w = workload(name)
+    d = w.to(device)
+    d_out, dhT = make_output_grads(w)
+    d_out, dhT = d_out.to(device), dhT.to(device)
+    plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, cu_seqlens=w.cu_seqlens, mode=cp)
+    ws = torch.empty(gdn_bwd_workspace_bytes(plan), dtype=torch.uint8, device=device)
+    o, hT = torch.empty_like(d.v), torch.empty(w.n_seqs, w.h_v, D, D, dtype=torch.float32, device=device)
+    grads = (torch.empty_like(d.q), torch.empty_like(d.k), torch.empty_like(d.v), torch.empty_like(d.g),
+             torch.empty_like(d.beta), torch.empty(w.n_seqs, w.h_v, D, D, dtype=torch.float32, device=device))
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def fwd():
+        gdn_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, plan=plan, out=o, final_state=hT,
+                      workspace=ws, for_backward=True)
+
+    def step():
+        fwd()
+        gdn_chunk_bwd(d.q, d.k, d.v, d.g, d.beta, d_out, d.h0, dhT, d.cu_seqlens, plan=plan, grads=grads,
+                      workspace=ws, reuse_forward=True)
+
+    res = {}
+    for key, f in (("forward_train_ms", fwd), ("train_step_ms", step)):
+        for _ in range(warmup):
+            flush.zero_()
+            f()
+        ts = []
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(steps):
+            flush.zero_()
+            s0.record(stream)
+            f()
+            s1.record(stream)
+            s1.synchronize()
+            ts.append(s0.elapsed_time(s1))
+        res[key] = statistics.mean(ts)
+    return res
+
+
 def backward_report(r, hbm, tfl):
     t_roof = max(r["bytes"] / (hbm * 1e9), r["flops"] / (tfl * 1e12))
     return {"workload": r["workload"], "ms": r["ms"], "tokens_per_s": r["tokens"] / (r["ms"] * 1e-3),
@@ -753,6 +798,7 @@ def main(argv=None):
         rb = time_bwd(HEADLINE, max(10, args.steps // 50), 3, device, args.cp)
         line["backward"] = backward_report(rb, hbm, tfl)
         line["backward"]["vs_forward"] = rb["ms"] / ms
+        line["backward"]["training"] = time_train_step(HEADLINE, max(10, args.steps // 50), 3, device, args.cp)
         line["backward"]["sweep"] = {n: backward_report(time_bwd(n, 5, 2, device, args.cp), hbm, tfl)
                                      for n in BWD_SWEEP}
         if not args.no_cpu_baseline:

@@ -34,7 +34,7 @@ GDN_CP_AUTO = 3
 EXPORTED = ["gdn_cp_plan", "gdn_chunk_fwd", "gdn_status_string", "gdn_last_cuda_error",
             "gdn_get_device_status", "gdn_cp_head_modes", "gdn_set_trace_events", "gdn_trace_last", "gdn_chunk_fwd_static",
             "gdn_get_static_device_status", "gdn_decode_step", "gdn_debug_stall_ns", "gdn_bwd_workspace_bytes",
-            "gdn_chunk_bwd"]
+            "gdn_chunk_bwd", "gdn_chunk_fwd_train"]
 
 
 class gdn_dims(ctypes.Structure):
@@ -105,7 +105,10 @@ def load(path: str = LIB_PATH):
         lib.gdn_bwd_workspace_bytes.argtypes = [ctypes.POINTER(gdn_cp_plan_t), ctypes.POINTER(ctypes.c_size_t)]
         lib.gdn_bwd_workspace_bytes.restype = ctypes.c_int
         lib.gdn_chunk_bwd.argtypes = [vp] * 15 + [ctypes.POINTER(gdn_dims), ctypes.POINTER(gdn_cp_plan_t), vp,
-                                                  ctypes.c_size_t, vp]
+                                                  ctypes.c_size_t, ctypes.c_int, vp]
+        lib.gdn_chunk_fwd_train.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(gdn_dims),
+                                            ctypes.POINTER(gdn_cp_plan_t), vp, ctypes.c_size_t, vp]
+        lib.gdn_chunk_fwd_train.restype = ctypes.c_int
         lib.gdn_chunk_bwd.restype = ctypes.c_int
         lib.gdn_debug_stall_ns.argtypes = [ctypes.c_uint32]
         lib.gdn_debug_stall_ns.restype = ctypes.c_int

@@ -79,12 +79,14 @@ def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
                   final_state: Optional[torch.Tensor] = None, output_final_state: bool = True,
                   workspace: Optional[torch.Tensor] = None, stream=None, scale: float = 0.0,
                   mode: str = "auto", lambda_: float = 0.0, warmup_chunks: int = 8,
-                  warmup_tol: float = 1e-4, tol_rule: str = "noise"):
+                  warmup_tol: float = 1e-4, tol_rule: str = "noise", for_backward: bool = False):
     """The chunked-prefill forward (gdn_chunk_fwd).
 
     q,k [B,T,h_qk,128] or [T,h_qk,128]; v [.., h_v, 128]; g,beta [.., h_v] fp32;
     initial_state [N,h_v,128,128] fp32 or None; cu_seqlens int32 [N+1] on the
     device (varlen, B = 1) or None.  Returns (o, final_state or None).
+    for_backward: gdn_chunk_fwd_train -- the workspace (of gdn_bwd_workspace_bytes)
+    keeps what gdn_chunk_bwd(..., reuse_forward=True) needs with the same plan.
     """
     batched = q.dim() == 4
     B = q.shape[0] if batched else 1
@@ -105,14 +107,15 @@ def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
     if final_state is None and output_final_state:
         final_state = torch.empty(plan.raw.n_seqs, h_v, 128, 128, dtype=torch.float32, device=q.device)
     if workspace is None:
-        workspace = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=q.device)
+        n_ws = gdn_bwd_workspace_bytes(plan) if for_backward else plan.workspace_bytes
+        workspace = torch.empty(max(n_ws, 256), dtype=torch.uint8, device=q.device)
     if initial_state is not None and (initial_state.dtype != torch.float32 or not initial_state.is_contiguous()):
         raise ValueError("initial_state must be contiguous float32")
-    st = L.load().gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
-                                _ptr(cu_seqlens), _ptr(out), _ptr(final_state), ctypes.byref(dims),
-                                ctypes.byref(plan.raw), _ptr(workspace), workspace.numel(),
-                                _stream_handle(stream))
-    L.check(st, "gdn_chunk_fwd")
+    fn = L.load().gdn_chunk_fwd_train if for_backward else L.load().gdn_chunk_fwd
+    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
+            _ptr(final_state), ctypes.byref(dims), ctypes.byref(plan.raw), _ptr(workspace), workspace.numel(),
+            _stream_handle(stream))
+    L.check(st, "gdn_chunk_fwd_train" if for_backward else "gdn_chunk_fwd")
     return out, final_state
 
 
@@ -128,12 +131,14 @@ def gdn_chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
                   d_final_state: Optional[torch.Tensor] = None, cu_seqlens: Optional[torch.Tensor] = None,
                   *, plan: Optional[Plan] = None, grads=None, workspace: Optional[torch.Tensor] = None,
                   stream=None, scale: float = 0.0, mode: str = "auto", lambda_: float = 0.0,
-                  want_initial_state_grad: bool = True):
+                  want_initial_state_grad: bool = True, reuse_forward: bool = False):
     """Gradients of sum(o * d_out) + sum(final_state * d_final_state) (gdn_chunk_bwd).
 
     Inputs as gdn_chunk_fwd (bf16 q/k/v); d_out like v (bf16); d_final_state
     [N, h_v, 128, 128] fp32 or None.  grads: optional preallocated
     (dq, dk, dv, dg, dbeta, dh0).  Returns (dq, dk, dv, dg, dbeta, dh0 or None).
+    reuse_forward: `workspace` and `plan` are those of a gdn_chunk_fwd(...,
+    for_backward=True) on the same inputs; the forward is not recomputed.
     """
     batched = q.dim() == 4
     B = q.shape[0] if batched else 1
@@ -144,6 +149,8 @@ def gdn_chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
     if q.dtype != torch.bfloat16 or d_out.dtype != torch.bfloat16:
         raise ValueError("the backward takes bf16 q/k/v and d_out")
+    if reuse_forward and (workspace is None or plan is None):
+        raise ValueError("reuse_forward needs the plan and workspace of the gdn_chunk_fwd(for_backward=True) call")
     if g.dtype != torch.float32 or beta.dtype != torch.float32:
         raise ValueError("g and beta must be float32")
     for name, t in (("initial_state", initial_state), ("d_final_state", d_final_state)):
@@ -164,7 +171,8 @@ def gdn_chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
     st = L.load().gdn_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
                                 _ptr(cu_seqlens), _ptr(d_out), _ptr(d_final_state), _ptr(dq), _ptr(dk), _ptr(dv),
                                 _ptr(dg), _ptr(dbeta), _ptr(dh0), ctypes.byref(dims), ctypes.byref(plan.raw),
-                                _ptr(workspace), workspace.numel(), _stream_handle(stream))
+                                _ptr(workspace), workspace.numel(), int(bool(reuse_forward)),
+                                _stream_handle(stream))
     L.check(st, "gdn_chunk_bwd")
     return dq, dk, dv, dg, dbeta, dh0
 

@@ -399,15 +399,16 @@ gdn_status gdn_cp_plan(const gdn_dims* dims, const int32_t* cu, const gdn_cp_opt
   return GDN_OK;
 }
 
-// The forward.  For the backward's recompute (hchunk != null) a context-
-// parallel plan combines every head exactly, and the WY and output-scan kernels
-// also write A^T (wyA) and every chunk's start state (hchunk); *p_out receives
-// the problem the kernels ran with.
+// The forward.  For the backward (hchunk != null) a context-parallel plan
+// combines every head exactly, and the WY and output-scan kernels also write
+// A^T (wyA) and every chunk's start state (hchunk); *p_out receives the
+// problem the kernels run with.  launch = false: only that problem (the
+// backward of a forward that already ran with the same arguments).
 static gdn_status forward_impl(const void* q, const void* k, const void* v, const float* g, const float* beta,
                                const float* initial_state, const int32_t* cu_dev, void* out, float* final_state,
                                const gdn_dims* dims, const gdn_cp_plan_t* plan, void* workspace,
                                size_t workspace_bytes, void* stream, uint8_t* wyA, uint8_t* hchunk,
-                               Problem* p_out) {
+                               Problem* p_out, bool launch = true) {
   gdn_status st = check_dims(dims);
   if (st != GDN_OK) return st;
   if (!plan) return GDN_ERR_INVALID_ARG;
@@ -483,6 +484,10 @@ static gdn_status forward_impl(const void* q, const void* k, const void* v, cons
     p.wy = ws + plan->off_wy;
   }
   p.stall_ns = g_debug_stall_ns.load(std::memory_order_relaxed);
+  if (!launch) {
+    if (p_out) *p_out = p;
+    return GDN_OK;
+  }
 
   cudaError_t e = cudaMemsetAsync(ws, 0, 256, cs);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -583,6 +588,19 @@ static BwdLayout bwd_layout(const gdn_cp_plan_t* plan) {
   return L;
 }
 
+gdn_status gdn_chunk_fwd_train(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                               const float* initial_state, const int32_t* cu_dev, void* out, float* final_state,
+                               const gdn_dims* dims, const gdn_cp_plan_t* plan, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (!plan || !dims) return GDN_ERR_INVALID_ARG;
+  if (dims->dtype != GDN_BF16 || plan->dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+  const BwdLayout L = bwd_layout(plan);
+  if (!workspace || workspace_bytes < L.end) return GDN_ERR_WORKSPACE;
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  return forward_impl(q, k, v, g, beta, initial_state, cu_dev, out, final_state, dims, plan, workspace,
+                      workspace_bytes, stream, ws + L.wyA, ws + L.hchunk, nullptr);
+}
+
 gdn_status gdn_bwd_workspace_bytes(const gdn_cp_plan_t* plan, size_t* bytes) {
   if (!plan || !bytes) return GDN_ERR_INVALID_ARG;
   if (plan->dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
@@ -594,7 +612,7 @@ gdn_status gdn_chunk_bwd(const void* q, const void* k, const void* v, const floa
                          const float* initial_state, const int32_t* cu_dev, const void* d_out,
                          const float* d_final_state, void* dq, void* dk, void* dv, float* dg, float* dbeta,
                          float* d_initial_state, const gdn_dims* dims, const gdn_cp_plan_t* plan, void* workspace,
-                         size_t workspace_bytes, void* stream) {
+                         size_t workspace_bytes, int reuse_forward, void* stream) {
   gdn_status st = check_dims(dims);
   if (st != GDN_OK) return st;
   if (!plan) return GDN_ERR_INVALID_ARG;
@@ -627,7 +645,7 @@ gdn_status gdn_chunk_bwd(const void* q, const void* k, const void* v, const floa
   }
   Problem p;
   st = forward_impl(q, k, v, g, beta, initial_state, cu_dev, ws + L.out, nullptr, dims, plan, workspace,
-                    workspace_bytes, stream, ws + L.wyA, ws + L.hchunk, &p);
+                    workspace_bytes, stream, ws + L.wyA, ws + L.hchunk, &p, reuse_forward == 0);
   if (st != GDN_OK) return st;
   int dev = 0;
   if ((st = device_setup(&dev)) != GDN_OK) return st;

@@ -308,10 +308,11 @@ gdn_status gdn_bwd_workspace_bytes(const gdn_cp_plan_t* plan, size_t* bytes);
  * the exact gradients of gdn_chunk_fwd's function].  For the scalar
  *   sum(o * d_out) + sum(final_state * d_final_state),
  * writes its gradient with respect to q, k, v, g, beta and initial_state.
- * Asynchronous on `stream`.  The forward is recomputed inside the call (no
- * forward state is kept between calls); a context-parallel plan combines every
- * head exactly there (no warmup restarts), so the gradients are those of the
- * exact forward.  bf16 only.
+ * Asynchronous on `stream`.  The forward is recomputed inside the call unless
+ * reuse_forward = 1, in which case `workspace` must hold the state a
+ * gdn_chunk_fwd_train with the same inputs and plan left there; a
+ * context-parallel plan combines every head exactly (no warmup restarts), so
+ * the gradients are those of the exact forward.  bf16 only.
  *   q, k, v, g, beta, initial_state, cu_seqlens_dev, dims, plan: as gdn_chunk_fwd.
  *   d_out         : device, [B*T, h_v, d_v] bf16.
  *   d_final_state : device, [n_seqs, h_v, d_k, d_v] fp32, or NULL (zero).
@@ -331,7 +332,24 @@ gdn_status gdn_chunk_bwd(const void* q, const void* k, const void* v, const floa
                          const float* initial_state, const int32_t* cu_seqlens_dev, const void* d_out,
                          const float* d_final_state, void* dq, void* dk, void* dv, float* dg, float* dbeta,
                          float* d_initial_state, const gdn_dims* dims, const gdn_cp_plan_t* plan,
-                         void* workspace, size_t workspace_bytes, void* stream);
+                         void* workspace, size_t workspace_bytes, int reuse_forward, void* stream);
+
+/*
+ * gdn_chunk_fwd_train -- gdn_chunk_fwd that also keeps, in `workspace`, what
+ * gdn_chunk_bwd needs (no counterpart on the FlashQLA pages: the training
+ * pattern of forward then backward).  Same arguments and outputs as
+ * gdn_chunk_fwd; the workspace must hold gdn_bwd_workspace_bytes(plan).  A
+ * context-parallel plan combines every head exactly here (no warmup
+ * restarts), so o and final_state are the exact forward's; besides them the
+ * call writes A^T and every chunk's start state into the workspace.  A later
+ * gdn_chunk_bwd with the same inputs, plan and workspace and reuse_forward = 1
+ * then skips its own recompute; nothing checks that the inputs are the same.
+ * bf16 only.  Errors: as gdn_chunk_fwd, UNSUPPORTED for fp32.
+ */
+gdn_status gdn_chunk_fwd_train(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                               const float* initial_state, const int32_t* cu_seqlens_dev, void* out,
+                               float* final_state, const gdn_dims* dims, const gdn_cp_plan_t* plan,
+                               void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * gdn_debug_stall_ns -- test hook of the failure path (no counterpart on the

@@ -155,3 +155,30 @@ def test_bwd_full_size(name, heads):
     else:  # the sampled heads' own gradients (dq and dk sum over every head of a group)
         names = ("dv", "dg", "dbeta", "dh0")
         check({n: got[n][:, heads] for n in names}, {n: ref[n][:, heads] for n in names}, names=names)
+
+
+@pytest.mark.parametrize("mode", ["off", "auto"])
+def test_bwd_after_training_forward(mode):
+    """gdn_chunk_fwd(for_backward=True) then gdn_chunk_bwd(reuse_forward=True): the same
+    gradients, bit for bit, as a backward that recomputes the forward itself, and the
+    training forward's o and final state are the exact forward's (parity with the oracle)."""
+    from gated_deltanet_linear_fwd_gb300 import gdn_chunk_fwd
+    import oracle
+    w = make_inputs(cu_seqlens=[0, 300, 700], h_qk=2, h_v=4, seed=41, with_h0=True)
+    d_out, dhT = make_output_grads(w, seed=42)
+    d = w.to(DEV)
+    plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, cu_seqlens=w.cu_seqlens, mode=mode)
+    ws = torch.empty(gdn_bwd_workspace_bytes(plan), dtype=torch.uint8, device=DEV)
+    o, hT = gdn_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, plan=plan, workspace=ws, for_backward=True)
+    reused = gdn_chunk_bwd(d.q, d.k, d.v, d.g, d.beta, d_out.to(DEV), d.h0, dhT.to(DEV), d.cu_seqlens, plan=plan,
+                           workspace=ws, reuse_forward=True)
+    assert gdn_get_device_status(ws)[0] == 0
+    fresh, _ = run_bwd(w, d_out, dhT, mode=mode)
+    for n, x in zip(NAMES, reused):
+        assert torch.equal(x, fresh[n]), n
+    f = util.to64
+    ro, rh = oracle.recurrence(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0), w.seq_offsets())
+    excess, _ = util.parity_bf16(o, ro)
+    assert excess <= 2e-2
+    err = np.abs(hT.double().cpu().numpy() - rh).max() / np.sqrt(np.mean(rh * rh))
+    assert err < 2e-2
