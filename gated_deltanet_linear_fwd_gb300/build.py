@@ -10,7 +10,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgdn.so")
-SOURCES = ["gdn_api.cu", "gdn_wy.cu", "gdn_scan.cu", "gdn_combine.cu", "gdn_f32.cu", "gdn_decode.cu", "gdn_bwd.cu", "gdn_bwd_tc.cu"]
+SOURCES = ["gdn_api.cu", "gdn_wy.cu", "gdn_scan.cu", "gdn_combine.cu", "gdn_f32.cu", "gdn_decode.cu", "gdn_bwd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off",
          "-I", os.path.join(ROOT, "include"), "-I", CSRC]

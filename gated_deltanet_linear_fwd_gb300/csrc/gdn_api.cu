@@ -663,7 +663,7 @@ gdn_status gdn_chunk_bwd(const void* q, const void* k, const void* v, const floa
   b.dstate = ws + L.dstate;
   LaunchLog log(true);
   cudaError_t e;
-  if ((e = log.before(cs)) != cudaSuccess || (e = launch_bwd_pre(p, b, cs)) != cudaSuccess ||
+  if ((e = log.before(cs)) != cudaSuccess || (e = launch_bwd_pre_tc(p, b, cs)) != cudaSuccess ||
       (e = log.after("bwd_pre", cs)) != cudaSuccess)
     return cuda_fail(e);
   if (p.plan_mode != kModeOff) {

@@ -15,122 +15,207 @@
 //   dKK  = dL * beta * Gam;  the gates through dG and a reverse cumulative sum.
 //
 // Three kernels after a forward pass that also leaves each chunk's start state
-// and A^T (fp16):
-//   bwd_pre_kernel    per (chunk, value head): T' and E            (chunk-parallel)
-//   bwd_chain_tc_kernel (gdn_bwd_tc.cu) per segment and value head: D over the
-//                     chunks in reverse, D kept in fp32; writes every chunk's D
-//                     (fp16) and dh0; context parallel like the forward
-//   bwd_local_tc_kernel (gdn_bwd_tc.cu) per (chunk, q/k head), over the value
-//                     heads of the group: every other gradient on tcgen05
-// bwd_pre_kernel runs its products on the tensor cores through mma.sync
-// m16n8k16 (fp16 operands in the forward's 128-byte-swizzled tile image, fp32
-// accumulators); tiles arrive by bulk copies on an mbarrier with a bounded wait.
-#include <cuda_fp16.h>
+// and A^T (fp16), all on the 5th-generation tensor cores (tcgen05, accumulators
+// in TMEM; fp16 operands in the forward's 128-byte-swizzled tile image; tiles
+// by bulk copies on mbarriers; every wait bounded):
+//   bwd_pre_tc_kernel    per (chunk, value head): T' and E (chunk-parallel)
+//   bwd_chain_tc_kernel  per segment and value head: D over the chunks in
+//                        reverse, in fp32 registers; every chunk's D (fp16) and
+//                        dh0; context parallel like the forward (a transition
+//                        and a local pass per segment, the combine run
+//                        backwards, then the final pass)
+//   bwd_local_tc_kernel  per (chunk, q/k head), over the value heads of the
+//                        group: every other gradient
+//
+// The chunk-local gradients, one CTA per (chunk, q/k head), the value heads of
+// the group one after the other:
+//   V'^T = U^T - S W^T                      (S = H^T, the chunk-start state)
+//   dV'^T = scale dO^T P + D^T Ktil^T
+//   dq^T += scale H dO^T diag(gamma) + K^T (dP * Gam)^T
+//   dk^T += Q^T (dP * Gam) + D V'^T diag(dec) - H Y_U^T diag(beta gamma)
+//           + K^T (dKK^T + dKK)
+//   Y_U^T = dV'^T A,  dv = diag(beta) Y_U
+//   [dP; dL_raw] = scale [dO; dV'] V'^T (lower triangles),  dL = -A^T dL_raw
+// Products have M = 128: a head dimension (d_k or d_v) as rows and the 64
+// tokens as columns, or two stacked 64-row operands ([dO; dV'], [Q; K]).  The
+// per-token sums over a head dimension (dgamma, ddec, <Y_U, V>, <Y_W, K>) are
+// column sums across TMEM lanes: a 31-shuffle butterfly per warp, then the
+// four lane quarters through shared memory.  Operand tiles are fp16 in the
+// forward's 128-byte-swizzled image (bulk copies of the records and states,
+// the rest written by the epilogues); one thread issues the MMAs and commits
+// each phase to an mbarrier; every wait is bounded.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "gdn_dev.cuh"
 
 namespace gdn {
 namespace {
 
-constexpr int kBwdThreads = 256;
+constexpr int kTcThreads = 256;
 
-// ---------------------------------------------------------------- fragments
-// An fp16 tile of `rows` rows and 64 * panels columns, stored as panels of
-// rows x 64 (128 bytes a row, 16-byte chunk c of row r at chunk c ^ (r & 7)).
-struct Tile {
-  uint32_t base;
-  uint32_t panel_bytes;  // rows * 128
-  __device__ __forceinline__ uint32_t at(int row, int col) const {
-    return base + (uint32_t)(col >> 6) * panel_bytes + sw128_offset((uint32_t)row, (uint32_t)((col & 63) >> 3)) +
-           (uint32_t)(col & 7) * 2u;
-  }
+// ---- shared memory (bytes from a 1024-byte aligned base) ----
+constexpr uint32_t sQK = 0;          // [Q d0-63 | K d0-63 | Q d64-127 | K d64-127], 64 rows each
+constexpr uint32_t sS = 32768;       // S = H^T: 128 (d_v) x 128 (d_k), panels d_k 0-63 | 64-127
+constexpr uint32_t sD = 65536;       // D: 128 (d_k) x 128 (d_v), panels d_v 0-63 | 64-127
+constexpr uint32_t sWt = 98304;      // -W^T record tile 128 (d_k) x 64; then dV'^T 128 (d_v) x 64
+constexpr uint32_t sUt = 114688;     // U^T record tile 128 (d_v) x 64; then Y_U^T 128 (d_v) x 64
+constexpr uint32_t sP = 131072;      // P record tile 64 x 64; then dL_raw; then dKK
+constexpr uint32_t sPG = 139264;     // dP * Gam 64 x 64 (also rows 0-63 of the padded dL product)
+constexpr uint32_t sAT = 147456;     // A^T 64 x 64
+constexpr uint32_t sDOV = 155648;    // [dO d0-63 | dV' d0-63 | dO d64-127 | dV' d64-127], 64 rows each
+constexpr uint32_t sVpT = 188416;    // V'^T 128 (d_v) x 64; then dv staged (64 rows x 128 bf16, row-major)
+constexpr uint32_t sV = 204800;      // V: 64 rows x 128 bf16, plain row-major (bulk copies of its rows)
+constexpr uint32_t sF = 221184;      // fp32: G, exp(G), dec, beta [64 each]
+constexpr uint32_t sRed = sF + 1024; // fp32 reductions (below)
+constexpr int kRedCol = 0;           //   [4 kinds][4 lane quarters][64]: dgamma gamma, ddec, t1, t2
+constexpr int kRedRowE = 1024;       //   [2 sources][2 halves][64]: row sums of dGam * Gam
+constexpr int kRedColE = 1280;       //   [4 quarters][64]: column sums of dGam * Gam
+constexpr int kRedRowB = 1536;       //   [2 halves][64]: sum_s dL KK Gam
+constexpr int kRedMisc = 1664;       //   [16]: scan carries
+constexpr uint32_t sCtl = sRed + 7168;
+constexpr uint32_t kTcSmem = sCtl + 256 + 1024;
+static_assert(kTcSmem <= 232448, "shared memory over the per-block limit");
+
+// ---- TMEM columns (512: one CTA per SM) ----
+constexpr uint32_t tQK = 0;     // lanes 0-63: Q K^T [r][s]; lanes 64-127: K K^T [r][s]
+constexpr uint32_t tDQ = 64;    // dq^T [k][r], summed over the group's heads
+constexpr uint32_t tDK = 128;   // dk^T [k][s]
+constexpr uint32_t tA = 192;    // -S W^T, then Y_U^T
+constexpr uint32_t tB = 256;    // dO^T P, then H Y_U^T
+constexpr uint32_t tC = 320;    // D^T K^T, then [dP_raw; dL_raw]
+constexpr uint32_t tE = 384;    // H dO^T, then A^T dL_raw (lanes 64-127)
+constexpr uint32_t tF = 448;    // D V'^T
+
+// Loads of a head's tiles, in three groups issued as their slots free up in
+// the head before: A (D, -W^T) once phase 2's products are done, B (S, U^T,
+// A^T, V) once phase 3's are, C (P) once phase 4's are.
+struct TcCtl {
+  uint64_t loadA, loadB, loadC, ph[5];
+  uint32_t tmem;
+  int abort;
 };
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr)
-               : "memory");
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr)
-               : "memory");
-}
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+__device__ __forceinline__ uint8_t* tc_smem_base() {
+  extern __shared__ uint8_t smem_raw[];
+  return smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 }
 
-// acc[NT][4] += A[m0 .. m0+15][k0 .. k0+16 KS) * B[k0 ..][n0 .. n0 + 8 NT), one warp.
-// TA: A is stored transposed (tile rows index k); TB: B is stored with rows
-// indexing k (else rows index n).  Accumulator element e of n-tile t sits at
-// row m0 + lane/4 + 8 (e >> 1), column n0 + 8 t + 2 (lane % 4) + (e & 1).
-template <int NT, int KS, bool TA, bool TB>
-__device__ __forceinline__ void warp_mma(float (&acc)[NT][4], const Tile& ta, const Tile& tb, int m0, int n0,
-                                         int k0) {
-  static_assert(NT % 2 == 0, "n-tiles come in pairs");
-  const int lane = threadIdx.x & 31, i = lane & 7, q = lane >> 3;
+// K-major operand (rows run along M or N, 64 K-elements a row per panel):
+// K step ks (16 elements) of a tile whose 64-wide K panels are panel_bytes apart.
+__device__ __forceinline__ uint64_t dk_(uint32_t base, int ks, uint32_t panel_bytes) {
+  return sdesc_sw128(base + (uint32_t)(ks >> 2) * panel_bytes + (uint32_t)(ks & 3) * 32u, 16, 1024);
+}
+// MN-major operand (rows run along K, 64 M/N-elements a row per block; blocks
+// lbo bytes apart): K step ks = 16 rows.
+__device__ __forceinline__ uint64_t dmn_(uint32_t base, int ks, uint32_t lbo) {
+  return sdesc_sw128(base + (uint32_t)ks * 2048u, lbo, 1024);
+}
+
+__device__ __forceinline__ bool tc_wait(TcCtl* c, int b, uint32_t parity) {
+  return wait_phase(&c->ph[b], parity, &c->abort, 200 + b);
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void ld32(uint32_t taddr, float (&x)[32]) {
+  uint32_t a[16], b[16];
+  tmem_ld16(taddr, a);
+  tmem_ld16(taddr + 16, b);
+  tmem_ld_wait(a, b);
 #pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
-    const int kk = k0 + 16 * ks;
-    uint32_t a[4];
-    if (!TA)
-      ldsm_x4(ta.at(m0 + i + (q & 1) * 8, kk + (q >> 1) * 8), a);
-    else
-      ldsm_x4_t(ta.at(kk + i + (q >> 1) * 8, m0 + (q & 1) * 8), a);
+  for (int i = 0; i < 16; ++i) {
+    x[i] = __uint_as_float(a[i]);
+    x[16 + i] = __uint_as_float(b[i]);
+  }
+}
+__device__ __forceinline__ void st32(uint32_t taddr, const float (&x)[32]) {
+  uint32_t a[32];
 #pragma unroll
-    for (int t = 0; t < NT; t += 2) {
-      const int nn = n0 + 8 * t;
-      uint32_t b[4];
-      if (!TB)
-        ldsm_x4(tb.at(nn + i + (q >> 1) * 8, kk + (q & 1) * 8), b);
-      else
-        ldsm_x4_t(tb.at(kk + i + (q & 1) * 8, nn + (q >> 1) * 8), b);
-      mma16816(acc[t], a, b[0], b[1]);
-      mma16816(acc[t + 1], a, b[2], b[3]);
+  for (int i = 0; i < 32; ++i) a[i] = __float_as_uint(x[i]);
+  tmem_st32(taddr, a);
+}
+
+// Column sums of x[0..31] over the 32 lanes of a warp: lane l returns the sum of
+// column l (recursive halving, 31 shuffles).
+template <int OFF>
+__device__ __forceinline__ void butterfly_step(float (&x)[32], int lane) {
+  const bool up = (lane & OFF) != 0;
+#pragma unroll
+  for (int i = 0; i < OFF; ++i) {
+    const float send = up ? x[i] : x[i + OFF];
+    const float keep = up ? x[i + OFF] : x[i];
+    x[i] = keep + __shfl_xor_sync(0xffffffffu, send, OFF);
+  }
+}
+__device__ __forceinline__ float butterfly_colsum(float (&x)[32]) {
+  const int lane = threadIdx.x & 31;
+  butterfly_step<16>(x, lane);
+  butterfly_step<8>(x, lane);
+  butterfly_step<4>(x, lane);
+  butterfly_step<2>(x, lane);
+  butterfly_step<1>(x, lane);
+  return x[0];
+}
+
+// 32 fp16 values (x, optionally scaled per column) as row `row` of an fp16
+// tile, columns c0 .. c0 + 31 (c0 a multiple of 8, within one 64-wide panel).
+__device__ __forceinline__ void row_f16(uint32_t panel, int row, int c0, const float (&x)[32], float& mx) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      mx = absmax_nan(absmax_nan(mx, x[8 * q + 2 * e]), x[8 * q + 2 * e + 1]);
+      w[e] = pack_f16x2(x[8 * q + 2 * e], x[8 * q + 2 * e + 1]);
     }
+    st_shared_v4(panel + sw128_offset((uint32_t)row, (uint32_t)((c0 >> 3) + q)), w[0], w[1], w[2], w[3]);
   }
 }
 
-template <int NT>
-__device__ __forceinline__ void zero(float (&acc)[NT][4]) {
-#pragma unroll
-  for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+// Element (row, col) of a one-panel fp16 tile.
+__device__ __forceinline__ uint32_t el(uint32_t panel, int row, int col) {
+  return panel + sw128_offset((uint32_t)row, (uint32_t)(col >> 3)) + (uint32_t)(col & 7) * 2u;
+}
+__device__ __forceinline__ float ld_h(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+  return __half2float(__ushort_as_half(v));
+}
+__device__ __forceinline__ void st_h(uint32_t addr, float x) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(__half_as_ushort(__float2half_rn(x))) : "memory");
 }
 
-__device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ float2 h2f(uint32_t h) {
-  return __half22float2(*reinterpret_cast<const __half2*>(&h));
-}
-
-// The fragment of a 16 x 8 NT accumulator as fp16 pairs into a tile (scaled per row).
-template <int NT>
-__device__ __forceinline__ void store_frag(const Tile& t, const float (&acc)[NT][4], int m0, int n0, float& mx) {
-  const int lane = threadIdx.x & 31, r = m0 + (lane >> 2), c = n0 + 2 * (lane & 3);
+// 64 rows x 128 bf16 of a [tokens, heads, 128] tensor into two fp16 panels
+// (panel stride pstride); rows >= cv are zero.
+__device__ __forceinline__ void rows_to_f16(uint32_t base, uint32_t pstride, const __nv_bfloat16* src, int64_t t0,
+                                            int heads, int head, int cv, float& mx, const float* row_scale = nullptr) {
+  // all four loads in flight before the first store (the stores are ordered memory operations)
+  constexpr int kPer = 64 * 16 / kTcThreads;
+  uint4 raw[kPer];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
+  for (int u = 0; u < kPer; ++u) {
+    const int idx = threadIdx.x + u * kTcThreads, r = idx >> 4, c = idx & 15;
+    raw[u] = make_uint4(0, 0, 0, 0);
+    if (r < cv) raw[u] = *reinterpret_cast<const uint4*>(src + ((size_t)(t0 + r) * heads + head) * kDim + c * 8);
+  }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) mx = absmax_nan(mx, acc[nt][e]);
-    sts_u32(t.at(r, c + 8 * nt), pack_f16x2(acc[nt][0], acc[nt][1]));
-    sts_u32(t.at(r + 8, c + 8 * nt), pack_f16x2(acc[nt][2], acc[nt][3]));
+  for (int u = 0; u < kPer; ++u) {
+    const int idx = threadIdx.x + u * kTcThreads, r = idx >> 4, c = idx & 15;
+    const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+    const float sc = row_scale ? row_scale[r] : 1.f;
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+      mx = absmax_nan(absmax_nan(mx, f.x * sc), f.y * sc);
+      o[e] = pack_f16x2(f.x * sc, f.y * sc);
+    }
+    st_shared_v4(base + (uint32_t)(c >> 3) * pstride + sw128_offset((uint32_t)r, (uint32_t)(c & 7)), o[0], o[1],
+                 o[2], o[3]);
   }
 }
 
-// ------------------------------------------------------------------- chunks
-// Sequence, first token and valid rows of global chunk gc (as the forward).
-__device__ __forceinline__ bool chunk_rows(const Problem& p, int gc, int& n, int64_t& t0, int& cv) {
+__device__ __forceinline__ bool tc_chunk_rows(const Problem& p, int gc, int& n, int64_t& t0, int& cv) {
   if (p.cu) {
     const int4 ci = p.chunk_info[gc];
     n = ci.x;
@@ -145,176 +230,899 @@ __device__ __forceinline__ bool chunk_rows(const Problem& p, int gc, int& n, int
   return n >= 0 && n < p.n_seqs && cv > 0 && cv <= kChunk;
 }
 
-// 64 rows x 128 bf16 of a [tokens, heads, 128] tensor into an fp16 tile (two
-// panels), row r scaled by row_scale[r] (null: 1); rows >= cv are zero.
-__device__ __forceinline__ void load_rows_f16(const Tile& t, const __nv_bfloat16* src, int64_t t0, int heads, int head,
-                                              int cv, const float* row_scale, float& mx) {
-  // all loads in flight before the first store (the stores are ordered memory operations)
-  constexpr int kPer = 64 * 16 / kBwdThreads;
-  uint4 raw[kPer];
-#pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int idx = threadIdx.x + u * kBwdThreads, r = idx >> 4, c = idx & 15;
-    raw[u] = make_uint4(0, 0, 0, 0);
-    if (r < cv) raw[u] = *reinterpret_cast<const uint4*>(src + ((size_t)(t0 + r) * heads + head) * kDim + c * 8);
-  }
-#pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int idx = threadIdx.x + u * kBwdThreads, r = idx >> 4, c = idx & 15;
-    const float sc = row_scale ? row_scale[r] : 1.f;
-    const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-    uint32_t o[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
-      mx = absmax_nan(absmax_nan(mx, f.x * sc), f.y * sc);
-      o[e] = pack_f16x2(f.x * sc, f.y * sc);
-    }
-    st_shared_v4(t.at(r, c * 8), o[0], o[1], o[2], o[3]);
-  }
-}
-
-// A bounded wait on a load barrier by every thread; false (in every thread
-// alike) when it ran out, after recording the timeout.
-__device__ __forceinline__ bool loads_landed(uint64_t* bar, uint32_t parity, const Problem& p) {
-  const bool ok = mbar_wait(bar, parity, kWaitLimitNs);
-  if (__syncthreads_or(!ok)) {
-    if (threadIdx.x == 0) report(p.status, kDevTimeout, kDetTmaWait);
-    // let copies still in flight land before the shared memory is released
-    const uint64_t t_start = globaltimer_ns();
-    while (globaltimer_ns() - t_start < 2000000ull) {
-    }
-    return false;
-  }
-  return true;
-}
-
-__device__ __forceinline__ uint8_t* smem_base() {
-  extern __shared__ uint8_t smem_raw[];
-  return smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-}
-
-// ------------------------------------------------------------------ bwd_pre
-// T' = -W^T Ktil (128 x 128) and E = scale (diag(gamma) Q)^T dO + (-W^T) Y with
-// Y = scale P^T dO, for one (chunk, value head); both fp16 in the tile image
-// (rows d_k; panels d_k resp. d_v 0-63 | 64-127).
-constexpr uint32_t kPreWt = 0;                 // -W^T record tile: 128 rows (d_k) x 64 (r)
-constexpr uint32_t kPreP = kPreWt + 16384;     // P record tile: 64 x 64
-constexpr uint32_t kPreKt = kPreP + 8192;      // diag(dec) K: 64 x 128
-constexpr uint32_t kPreQ = kPreKt + 16384;     // scale diag(gamma) Q: 64 x 128
-constexpr uint32_t kPreDo = kPreQ + 16384;     // dO: 64 x 128
-constexpr uint32_t kPreY = kPreDo + 16384;     // Y: 64 x 128
-constexpr uint32_t kPreGam = kPreY + 16384;    // record gates: exp(G) [64], dec [64]
-constexpr uint32_t kPreBar = kPreGam + 512;
-constexpr uint32_t kPreSmem = kPreBar + 64 + 1024;
-
-__global__ void __launch_bounds__(kBwdThreads, 2) bwd_pre_kernel(const Problem p, const BwdArgs b) {
-  uint8_t* sm = smem_base();
+__global__ void __launch_bounds__(kTcThreads, 1) bwd_local_tc_kernel(const Problem p, const BwdArgs b) {
+  uint8_t* sm = tc_smem_base();
   const uint32_t s0 = smem_u32(sm);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kPreBar);
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int gc = (int)(blockIdx.x / (unsigned)p.h_v), j = (int)(blockIdx.x % (unsigned)p.h_v);
+  TcCtl* ctl = reinterpret_cast<TcCtl*>(sm + sCtl);
+  float* sG = reinterpret_cast<float*>(sm + sF);
+  float* sGam = sG + 64;
+  float* sDec = sG + 128;
+  float* sBeta = sG + 192;
+  float* red = reinterpret_cast<float*>(sm + sRed);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q = warp & 3, h = warp >> 2;         // TMEM lane quarter, column half
+  const int d = 32 * q + lane;                   // this thread's TMEM lane
+  const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+  const int gc = (int)(blockIdx.x / (unsigned)p.h_qk), iq = (int)(blockIdx.x % (unsigned)p.h_qk);
   if (tid == 0) {
-    mbar_init(bar, 1);
+    mbar_init(&ctl->loadA, 1);
+    mbar_init(&ctl->loadB, 1);
+    mbar_init(&ctl->loadC, 1);
+    for (int i = 0; i < 5; ++i) mbar_init(&ctl->ph[i], 1);
+    ctl->abort = 0;
     fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&ctl->tmem, 512);
+    tmem_relinquish();
   }
   grid_dependency_wait();
   grid_launch_dependents();
   int n, cv;
   int64_t t0;
-  if (!chunk_rows(p, gc, n, t0, cv)) {
-    if (tid == 0) report(p.status, kDevCheck, kDetSegMismatch);
-    return;
-  }
-  // one read of the status word per CTA: an earlier kernel's failure means incomplete inputs
-  if (__syncthreads_or(tid == 0 && earlier_failure(p.status))) return;  // (also: barrier initialised)
-  const int iq = (int)(((int64_t)j * p.h_qk) / p.h_v);
-  const uint8_t* rec = p.wy + ((size_t)gc * p.h_v + j) * kRecBytes;
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar, 16384u + 8192u + 512u);
-    bulk_load(sm + kPreWt, rec + kRecWn, 16384u, bar);
-    bulk_load(sm + kPreP, rec + kRecP, 8192u, bar);
-    bulk_load(sm + kPreGam, rec + kRecGam, 512u, bar);
-  }
+  const bool rows_ok = tc_chunk_rows(p, gc, n, t0, cv);
+  tc_fence_before();
+  const bool skip = __syncthreads_or(tid == 0 && (!rows_ok || earlier_failure(p.status)));
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem + lane_base;
+  const int j_lo = (int)(((int64_t)iq * p.h_v + p.h_qk - 1) / p.h_qk);
+  const int j_hi = (int)(((int64_t)(iq + 1) * p.h_v + p.h_qk - 1) / p.h_qk);
   float mx = 0.f;
-  const Tile tWt{s0 + kPreWt, 16384}, tP{s0 + kPreP, 8192}, tKt{s0 + kPreKt, 8192}, tQ{s0 + kPreQ, 8192},
-      tDo{s0 + kPreDo, 8192}, tY{s0 + kPreY, 8192};
-  load_rows_f16(tDo, reinterpret_cast<const __nv_bfloat16*>(b.dout), t0, p.h_v, j, cv, nullptr, mx);
-  if (!loads_landed(bar, 0, p)) return;
-  float* gam = reinterpret_cast<float*>(sm + kPreGam);  // exp(G) [64], dec [64]
-  {
-    // rows scaled: K by dec, Q by scale * exp(G)
-    __shared__ float qsc[64];
-    if (tid < 64) qsc[tid] = p.scale * gam[tid];
-    __syncthreads();
-    load_rows_f16(tKt, reinterpret_cast<const __nv_bfloat16*>(p.k), t0, p.h_qk, iq, cv, gam + 64, mx);
-    load_rows_f16(tQ, reinterpret_cast<const __nv_bfloat16*>(p.q), t0, p.h_qk, iq, cv, qsc, mx);
-  }
-  __syncthreads();
-  // Y = scale P^T dO: warp (rows 16 (w & 3), columns 64 (w >> 2))
-  {
-    const int m0 = 16 * (warp & 3), n0 = 64 * (warp >> 2);
-    float acc[8][4];
-    zero(acc);
-    warp_mma<8, 4, true, true>(acc, tP, tDo, m0, n0, 0);
-#pragma unroll
-    for (int t = 0; t < 8; ++t)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[t][e] *= p.scale;
-    store_frag(tY, acc, m0, n0, mx);
-  }
-  __syncthreads();
-  // T' and E: warp w owns rows 16 w .. 16 w + 15 (d_k), all 128 columns
-  const size_t slot = ((size_t)gc * p.h_v + j) * 32768u;
-  const int m0 = 16 * warp, lane = tid & 31;
-  auto store_global = [&](uint8_t* dst, const float(&acc)[16][4]) {
-    const int r = m0 + (lane >> 2), c = 2 * (lane & 3);
-#pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      const int col = 8 * t + c;
-      const uint32_t off0 = (uint32_t)(col >> 6) * 16384u + sw128_offset(r, (col & 63) >> 3) + (col & 7) * 2;
-      const uint32_t off1 = (uint32_t)(col >> 6) * 16384u + sw128_offset(r + 8, (col & 63) >> 3) + (col & 7) * 2;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) mx = absmax_nan(mx, acc[t][e]);
-      *reinterpret_cast<uint32_t*>(dst + off0) = pack_f16x2(acc[t][0], acc[t][1]);
-      *reinterpret_cast<uint32_t*>(dst + off1) = pack_f16x2(acc[t][2], acc[t][3]);
-    }
+  bool ok = !skip;
+  int n_heads = 0;
+  // (one thread) head jj's tile groups
+  auto issue_A = [&](int jj) {
+    const size_t slot = (size_t)gc * p.h_v + jj;
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(&ctl->loadA, 32768u + 16384u);
+    bulk_load(sm + sD, b.dstate + slot * 32768u, 32768u, &ctl->loadA);
+    bulk_load(sm + sWt, p.wy + slot * kRecBytes + kRecWn, 16384u, &ctl->loadA);
   };
-  {
-    float acc[16][4];
-    zero(acc);
-    warp_mma<16, 4, false, true>(acc, tWt, tKt, m0, 0, 0);
-    store_global(b.tmat + slot, acc);
+  auto issue_B = [&](int jj) {
+    const size_t slot = (size_t)gc * p.h_v + jj;
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(&ctl->loadB, 32768u + 16384u + 8192u + (uint32_t)cv * 256u);
+    bulk_load(sm + sS, p.hchunk + slot * 32768u, 32768u, &ctl->loadB);
+    bulk_load(sm + sUt, p.wy + slot * kRecBytes + kRecU, 16384u, &ctl->loadB);
+    bulk_load(sm + sAT, p.wyA + slot * 8192u, 8192u, &ctl->loadB);
+    const uint8_t* vrow = reinterpret_cast<const uint8_t*>(p.v) + ((size_t)t0 * p.h_v + jj) * (kDim * 2);
+    for (int r = 0; r < cv; ++r) bulk_load(sm + sV + r * 256, vrow + (size_t)r * p.h_v * (kDim * 2), 256u, &ctl->loadB);
+  };
+  auto issue_C = [&](int jj) {
+    const size_t slot = (size_t)gc * p.h_v + jj;
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(&ctl->loadC, 8192u);
+    bulk_load(sm + sP, p.wy + slot * kRecBytes + kRecP, 8192u, &ctl->loadC);
+  };
+  if (ok) {
+    // dq^T and dk^T accumulators start at zero
+    {
+      float z[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z[i] = 0.f;
+      st32(tmem + tDQ + 32 * h, z);
+      st32(tmem + tDK + 32 * h, z);
+    }
+    rows_to_f16(s0 + sQK, 16384, reinterpret_cast<const __nv_bfloat16*>(p.q), t0, p.h_qk, iq, cv, mx);
+    rows_to_f16(s0 + sQK + 8192, 16384, reinterpret_cast<const __nv_bfloat16*>(p.k), t0, p.h_qk, iq, cv, mx);
+    fence_proxy_async_smem();
+    tmem_st_wait();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {  // [Q; K] K^T: Q K^T on lanes 0-63, K K^T on lanes 64-127
+      tc_fence_after();
+      const uint32_t id = idesc_f16(128, 64, false, false);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_bf16(ctl->tmem + tQK, dk_(s0 + sQK, ks, 16384), dk_(s0 + sQK + 8192, ks, 16384), id, ks > 0);
+      mma_commit(&ctl->ph[0]);
+      if (j_lo < j_hi) {
+        issue_A(j_lo);
+        issue_B(j_lo);
+        issue_C(j_lo);
+      }
+    }
+    if (j_lo < j_hi)
+      rows_to_f16(s0 + sDOV, 16384, reinterpret_cast<const __nv_bfloat16*>(b.dout), t0, p.h_v, j_lo, cv, mx);
   }
-  {
-    float acc[16][4];
-    zero(acc);
-    warp_mma<16, 4, true, true>(acc, tQ, tDo, m0, 0, 0);
-    warp_mma<16, 4, false, true>(acc, tWt, tY, m0, 0, 0);
-    store_global(b.emat + slot, acc);
+  // this head's g and beta for threads 0-63 (prefetched during the head before)
+  float g_cur = 0.f, b_cur = 0.f;
+  if (tid < 64 && j_lo < j_hi && tid < cv) {
+    g_cur = p.g[(size_t)(t0 + tid) * p.h_v + j_lo];
+    b_cur = p.beta[(size_t)(t0 + tid) * p.h_v + j_lo];
+  }
+  for (int j = j_lo; ok && j < j_hi; ++j, ++n_heads) {
+    const uint32_t par = (uint32_t)(n_heads & 1);
+    // the previous head's last products (they read K and dKK) are done
+    if (n_heads > 0 && !tc_wait(ctl, 4, par ^ 1u)) ok = false;
+    if (__syncthreads_or(!ok)) {
+      ok = false;
+      break;
+    }
+    if (tid == 0 && n_heads > 0) issue_C(j);  // (A, B and dO came during the head before)
+    if (tid < 64) {  // G = inclusive cumulative gate (two warps, as the forward)
+      const int r = tid;
+      float x = g_cur;
+      sBeta[r] = b_cur;
+#pragma unroll
+      for (int dd = 1; dd < 32; dd <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, dd);
+        if (lane >= dd) x += y;
+      }
+      if (lane == 31 && warp == 0) red[kRedMisc] = x;
+      named_bar_sync(1, 64);
+      if (warp == 1) x += red[kRedMisc];
+      sG[r] = x;
+      sGam[r] = __expf(x);
+      named_bar_sync(1, 64);
+      sDec[r] = __expf(sG[63] - x);
+    }
+    const bool landed = mbar_wait(&ctl->loadA, par, kWaitLimitNs) && mbar_wait(&ctl->loadB, par, kWaitLimitNs) &&
+                        mbar_wait(&ctl->loadC, par, kWaitLimitNs);
+    if (!landed) atomicCAS(&ctl->abort, 0, kDetTmaWait);
+    if (n_heads == 0 && !tc_wait(ctl, 0, 0)) ok = false;
+    fence_proxy_async_smem();
+    tc_fence_before();
+    if (__syncthreads_or(!landed || !ok)) {
+      ok = false;
+      break;
+    }
+    // ---- phase 1: -S W^T, dO^T P, D^T K^T, H dO^T ----
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t t = ctl->tmem;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_bf16(t + tA, dk_(s0 + sS, ks, 16384), dmn_(s0 + sWt, ks, 16384), idesc_f16(128, 64, false, true), ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(t + tB, dmn_(s0 + sDOV, ks, 16384), dmn_(s0 + sP, ks, 8192), idesc_f16(128, 64, true, true), ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_bf16(t + tC, dmn_(s0 + sD, ks, 16384), dk_(s0 + sQK + 8192, ks, 16384), idesc_f16(128, 64, true, false),
+                 ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_bf16(t + tE, dmn_(s0 + sS, ks, 16384), dk_(s0 + sDOV, ks, 16384), idesc_f16(128, 64, true, false), ks > 0);
+      mma_commit(&ctl->ph[1]);
+    }
+    // <D, H> = sum D[k][v] S[v][k] (the gradient of gamma_C) while the products run:
+    // thread = one 8 x 8 block, rows k0.. of D against rows v0.. of S
+    {
+      const int k0 = 8 * (tid >> 4), v0 = 8 * (tid & 15);
+      const uint32_t dpanel = s0 + sD + (uint32_t)(v0 >> 6) * 16384u;
+      const uint32_t spanel = s0 + sS + (uint32_t)(k0 >> 6) * 16384u;
+      float dblk[8][8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) {
+        const uint4 w = lds_u32x4(dpanel + sw128_offset((uint32_t)(k0 + a), (uint32_t)((v0 & 63) >> 3)));
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[e]));
+          dblk[a][2 * e] = f.x;
+          dblk[a][2 * e + 1] = f.y;
+        }
+      }
+      float dh = 0.f;
+#pragma unroll
+      for (int bb = 0; bb < 8; ++bb) {  // row v0 + bb of S: S[v][k0 .. k0 + 7]
+        const uint4 w = lds_u32x4(spanel + sw128_offset((uint32_t)(v0 + bb), (uint32_t)((k0 & 63) >> 3)));
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[e]));
+          dh = fmaf(dblk[2 * e][bb], f.x, fmaf(dblk[2 * e + 1][bb], f.y, dh));
+        }
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) dh += __shfl_xor_sync(0xffffffffu, dh, o);
+      if (lane == 0) red[kRedMisc + 4 + warp] = dh;
+    }
+    if (!tc_wait(ctl, 1, par)) ok = false;
+    tc_fence_after();
+    if (ok) {
+      // V'^T = U^T - S W^T (lane = d_v)
+      float x[32];
+      ld32(tmem + tA + 32 * h, x);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint4 u = lds_u32x4(s0 + sUt + sw128_offset((uint32_t)d, (uint32_t)(4 * h + c)));
+        const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 u2 = __half22float2(*reinterpret_cast<const __half2*>(&uw[e]));
+          x[8 * c + 2 * e] += u2.x;
+          x[8 * c + 2 * e + 1] += u2.y;
+        }
+      }
+      row_f16(s0 + sVpT, d, 32 * h, x, mx);
+      // dV'^T = scale dO^T P + diag(dec) applied to D^T K^T's columns; also dV' (rows r)
+      float y[32];
+      ld32(tmem + tB + 32 * h, x);
+      ld32(tmem + tC + 32 * h, y);
+      const uint32_t dvp = s0 + sDOV + 8192u + (uint32_t)(d >> 6) * 16384u;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        x[i] = fmaf(p.scale, x[i], sDec[32 * h + i] * y[i]);
+        st_h(el(dvp, 32 * h + i, d & 63), x[i]);
+      }
+      row_f16(s0 + sWt, d, 32 * h, x, mx);
+      // H dO^T (lane = d_k): dq^T += scale gamma_r (H dO^T); dgamma_r gamma_r = <Q_r, that>
+      ld32(tmem + tE + 32 * h, x);
+      ld32(tmem + tDQ + 32 * h, y);
+      const uint32_t qpanel = s0 + sQK + (uint32_t)(d >> 6) * 16384u;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        x[i] *= p.scale * sGam[32 * h + i];
+        y[i] += x[i];
+        x[i] *= ld_h(el(qpanel, 32 * h + i, d & 63));
+      }
+      st32(tmem + tDQ + 32 * h, y);
+      red[kRedCol + (0 * 4 + q) * 64 + 32 * h + lane] = butterfly_colsum(x);
+    }
+    fence_proxy_async_smem();
+    tmem_st_wait();
+    tc_fence_before();
+    if (__syncthreads_or(!ok)) {
+      ok = false;
+      break;
+    }
+    // ---- phase 2: D V'^T, [dO; dV'] V'^T, dV'^T A ----
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t t = ctl->tmem;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_bf16(t + tF, dk_(s0 + sD, ks, 16384), dmn_(s0 + sVpT, ks, 16384), idesc_f16(128, 64, false, true), ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_bf16(t + tC, dk_(s0 + sDOV, ks, 16384), dmn_(s0 + sVpT, ks, 16384), idesc_f16(128, 64, false, true),
+                 ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(t + tA, dk_(s0 + sWt, ks, 16384), dk_(s0 + sAT, ks, 8192), idesc_f16(128, 64, false, false), ks > 0);
+      mma_commit(&ctl->ph[2]);
+    }
+    if (!tc_wait(ctl, 2, par)) ok = false;
+    if (tid == 0 && ok && j + 1 < j_hi) issue_A(j + 1);  // D and -W^T are read
+    tc_fence_after();
+    if (ok) {
+      float x[32], y[32];
+      // D V'^T (lane = d_k): dk^T += dec_r (.); ddec_r = <K_r, .>
+      ld32(tmem + tF + 32 * h, x);
+      ld32(tmem + tDK + 32 * h, y);
+      const uint32_t kpanel = s0 + sQK + 8192u + (uint32_t)(d >> 6) * 16384u;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        y[i] = fmaf(sDec[32 * h + i], x[i], y[i]);
+        x[i] *= ld_h(el(kpanel, 32 * h + i, d & 63));
+      }
+      st32(tmem + tDK + 32 * h, y);
+      red[kRedCol + (1 * 4 + q) * 64 + 32 * h + lane] = butterfly_colsum(x);
+      // Y_U^T (lane = d_v): dv = beta_r Y_U; t1_r = <Y_U_r, V_r>; Y_U^T into the U^T slot
+      ld32(tmem + tA + 32 * h, x);
+      row_f16(s0 + sUt, d, 32 * h, x, mx);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {  // dv staged in the V'^T slot (read by phase 2), stored in epilogue 3
+        const int r = 32 * h + i;
+        const __nv_bfloat16 dvb = __float2bfloat16_rn(sBeta[r] * x[i]);
+        asm volatile("st.shared.u16 [%0], %1;" ::"r"(s0 + sVpT + (uint32_t)(r * 256 + 2 * d)),
+                     "h"(*reinterpret_cast<const unsigned short*>(&dvb))
+                     : "memory");
+        unsigned short vb;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(vb) : "r"(s0 + sV + (uint32_t)(r * 256 + 2 * d)) : "memory");
+        x[i] = r < cv ? x[i] * __uint_as_float((uint32_t)vb << 16) : 0.f;
+      }
+      red[kRedCol + (2 * 4 + q) * 64 + 32 * h + lane] = butterfly_colsum(x);
+      // [dP_raw; dL_raw] (lane = token r, or 64 + r)
+      ld32(tmem + tC + 32 * h, x);
+      if (q < 2) {
+        const int r = d;
+        ld32(tmem + tQK + 32 * h, y);
+        float rowsum = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int s = 32 * h + i;
+          const float gam = s <= r ? __expf(sG[r] - sG[s]) : 0.f;
+          const float dP = s <= r ? p.scale * x[i] : 0.f;
+          const float e = dP * y[i] * gam;
+          rowsum += e;
+          x[i] = dP * gam;
+          y[i] = e;
+        }
+        row_f16(s0 + sPG, r, 32 * h, x, mx);
+        red[kRedRowE + (0 * 2 + h) * 64 + r] = rowsum;
+        red[kRedColE + q * 64 + 32 * h + lane] = butterfly_colsum(y);
+      } else {
+        row_f16(s0 + sP, d - 64, 32 * h, x, mx);
+      }
+    }
+    fence_proxy_async_smem();
+    tmem_st_wait();
+    tc_fence_before();
+    if (__syncthreads_or(!ok)) {
+      ok = false;
+      break;
+    }
+    // ---- phase 3: H Y_U^T; dq^T += K^T (dP*Gam)^T; dk^T += Q^T (dP*Gam); A^T dL_raw ----
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t t = ctl->tmem;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_bf16(t + tB, dmn_(s0 + sS, ks, 16384), dmn_(s0 + sUt, ks, 16384), idesc_f16(128, 64, true, true), ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(t + tDQ, dmn_(s0 + sQK + 8192, ks, 16384), dk_(s0 + sPG, ks, 8192), idesc_f16(128, 64, true, false), 1);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(t + tDK, dmn_(s0 + sQK, ks, 16384), dmn_(s0 + sPG, ks, 8192), idesc_f16(128, 64, true, true), 1);
+      // rows 64-127 of this A operand are A^T (rows 0-63 read the tile before it and are discarded)
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(t + tE, dk_(s0 + sPG, ks, 16384), dmn_(s0 + sP, ks, 8192), idesc_f16(128, 64, false, true), ks > 0);
+      mma_commit(&ctl->ph[3]);
+    }
+    if (!tc_wait(ctl, 3, par)) ok = false;
+    if (tid == 0 && ok && j + 1 < j_hi) issue_B(j + 1);  // S, U^T / Y_U^T, A^T and V are read
+    tc_fence_after();
+    if (ok) {  // dv of this head from its staging rows: 16-byte stores, whole rows per warp
+      uint8_t* dvo = reinterpret_cast<uint8_t*>(b.dv);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int idx = tid + u * kTcThreads, r = idx >> 4, c = idx & 15;
+        const uint4 w = lds_u32x4(s0 + sVpT + (uint32_t)(r * 256 + c * 16));
+        if (r < cv) *reinterpret_cast<uint4*>(dvo + (((size_t)(t0 + r) * p.h_v + j) * kDim) * 2 + c * 16) = w;
+      }
+    }
+    // the next head's g and beta, in flight during this epilogue
+    float g_next = 0.f, b_next = 0.f;
+    if (tid < 64 && j + 1 < j_hi && tid < cv) {
+      g_next = p.g[(size_t)(t0 + tid) * p.h_v + j + 1];
+      b_next = p.beta[(size_t)(t0 + tid) * p.h_v + j + 1];
+    }
+    if (ok) {
+      float x[32], y[32];
+      // Y_W^T = -H Y_U^T (lane = d_k): dk^T += beta_r gamma_r Y_W^T; t2_r = <Y_W_r, K_r>
+      ld32(tmem + tB + 32 * h, x);
+      ld32(tmem + tDK + 32 * h, y);
+      const uint32_t kpanel = s0 + sQK + 8192u + (uint32_t)(d >> 6) * 16384u;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int r = 32 * h + i;
+        y[i] = fmaf(-sBeta[r] * sGam[r], x[i], y[i]);
+        x[i] = -x[i] * ld_h(el(kpanel, r, d & 63));
+      }
+      st32(tmem + tDK + 32 * h, y);
+      red[kRedCol + (3 * 4 + q) * 64 + 32 * h + lane] = butterfly_colsum(x);
+      // dL = -A^T dL_raw, s < r (lanes 64-127: r = lane - 64)
+      if (q >= 2) {
+        const int r = d - 64;
+        ld32(tmem + tE + 32 * h, x);
+        ld32(tmem + tQK + 32 * h, y);  // K K^T [r][s]
+        const float br = sBeta[r];
+        float rowb = 0.f, rowe = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int s = 32 * h + i;
+          const float gam = s < r ? __expf(sG[r] - sG[s]) : 0.f;
+          const float dL = s < r ? -x[i] : 0.f;
+          const float xb = dL * y[i] * gam;
+          rowb += xb;
+          rowe += br * xb;
+          x[i] = dL * br * gam;
+          y[i] = br * xb;
+        }
+        row_f16(s0 + sP, r, 32 * h, x, mx);
+        red[kRedRowB + h * 64 + r] = rowb;
+        red[kRedRowE + (1 * 2 + h) * 64 + r] = rowe;
+        red[kRedColE + q * 64 + 32 * h + lane] = butterfly_colsum(y);
+      }
+    }
+    if (ok && j + 1 < j_hi)  // the next head's dO (its slots were last read by phase 2)
+      rows_to_f16(s0 + sDOV, 16384, reinterpret_cast<const __nv_bfloat16*>(b.dout), t0, p.h_v, j + 1, cv, mx);
+    fence_proxy_async_smem();
+    tmem_st_wait();
+    tc_fence_before();
+    if (__syncthreads_or(!ok)) {
+      ok = false;
+      break;
+    }
+    // ---- phase 4: dk^T += K^T (dKK^T + dKK) ----
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t t = ctl->tmem;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(t + tDK, dmn_(s0 + sQK + 8192, ks, 16384), dk_(s0 + sP, ks, 8192), idesc_f16(128, 64, true, false), 1);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(t + tDK, dmn_(s0 + sQK + 8192, ks, 16384), dmn_(s0 + sP, ks, 8192), idesc_f16(128, 64, true, true), 1);
+      mma_commit(&ctl->ph[4]);
+    }
+    // ---- the gates: dG, dg = its reverse cumulative sum, dbeta ----
+    if (tid < 64) {
+      const int r = tid;
+      auto col = [&](int kind) {
+        return red[kRedCol + (kind * 4 + 0) * 64 + r] + red[kRedCol + (kind * 4 + 1) * 64 + r] +
+               red[kRedCol + (kind * 4 + 2) * 64 + r] + red[kRedCol + (kind * 4 + 3) * 64 + r];
+      };
+      const float t2 = col(3);
+      const float erow = red[kRedRowE + 0 * 64 + r] + red[kRedRowE + 1 * 64 + r] + red[kRedRowE + 2 * 64 + r] +
+                         red[kRedRowE + 3 * 64 + r];
+      const float ecol = red[kRedColE + r] + red[kRedColE + 64 + r] + red[kRedColE + 128 + r] +
+                         red[kRedColE + 192 + r];
+      const float ddec = col(1) * sDec[r];
+      float dG = col(0) + sBeta[r] * t2 * sGam[r] + erow - ecol - ddec;
+      const float dbeta = col(2) + sGam[r] * t2 + red[kRedRowB + r] + red[kRedRowB + 64 + r];
+      float dd = ddec;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, o);
+      if (lane == 0) red[kRedMisc + 1 + warp] = dd;
+      named_bar_sync(1, 64);
+      if (r == 63) {
+        float dgc = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) dgc += red[kRedMisc + 4 + w];
+        dG += dgc * sGam[63] + red[kRedMisc + 1] + red[kRedMisc + 2];
+      }
+      float x = dG;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_down_sync(0xffffffffu, x, o);
+        if (lane + o < 32) x += y;
+      }
+      if (warp == 1 && lane == 0) red[kRedMisc + 3] = x;
+      named_bar_sync(1, 64);
+      if (warp == 0) x += red[kRedMisc + 3];
+      if (r < cv) {
+        b.dg[(size_t)(t0 + r) * p.h_v + j] = x;
+        b.dbeta[(size_t)(t0 + r) * p.h_v + j] = dbeta;
+      }
+    }
+    g_cur = g_next;
+    b_cur = b_next;
+  }
+  // ---- dq, dk (bf16) from their accumulators ----
+  if (ok && n_heads > 0 && !tc_wait(ctl, 4, (uint32_t)((n_heads - 1) & 1))) ok = false;
+  if (ok && n_heads == 0 && !tc_wait(ctl, 0, 0)) ok = false;  // [Q; K] K^T done before TMEM is freed
+  tc_fence_after();
+  if (__syncthreads_or(!ok) == 0 && !skip) {
+    float x[32], y[32];
+    ld32(tmem + tDQ + 32 * h, x);
+    ld32(tmem + tDK + 32 * h, y);
+    __nv_bfloat16* dqo = reinterpret_cast<__nv_bfloat16*>(b.dq);
+    __nv_bfloat16* dko = reinterpret_cast<__nv_bfloat16*>(b.dk);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int r = 32 * h + i;
+      if (r < cv) {
+        const size_t o = ((size_t)(t0 + r) * p.h_qk + iq) * kDim + d;
+        dqo[o] = __float2bfloat16_rn(x[i]);
+        dko[o] = __float2bfloat16_rn(y[i]);
+      }
+    }
+  }
+  if (skip && tid == 0 && !rows_ok) report(p.status, kDevCheck, kDetSegMismatch);
+  tc_fence_before();
+  __syncthreads();
+  if (ctl->abort || (!ok && !skip)) {
+    if (tid == 0) report(p.status, kDevTimeout, ctl->abort ? ctl->abort : kDetMmaWait);
+    // let copies and MMAs already in flight land before the memory is released
+    const uint64_t t_start = globaltimer_ns();
+    while (globaltimer_ns() - t_start < 2000000ull) {
+    }
+    __syncthreads();
   }
   if (!(mx < 65504.f)) report(p.status, kDevCheck, kDetFp16Range);
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(ctl->tmem, 512);
+  }
+}
+
+
+// ------------------------------------------------------------ per-chunk T' and E
+// For one (chunk, value head): T' = -W^T Ktil (the chunk's map of the state
+// gradient) and E = scale (diag(gamma) Q)^T dO - W^T Y with Y = scale P^T dO,
+// both fp16 in the tile image the chain reads (rows d_k; panels d_k resp. d_v).
+// Products (M = 128 rows of d): Y^T = dO^T P; T' = (-W^T) Ktil;
+// E = Qg^T dO + (-W^T) Y  (Qg = scale diag(gamma) Q).  Two CTAs per SM.
+constexpr uint32_t pWt = 0;        // -W^T record tile 128 (d_k) x 64
+constexpr uint32_t pKt = 16384;    // Ktil = diag(dec) K: 64 x 128, panels d_k 0-63 | 64-127 (8 KB)
+constexpr uint32_t pQg = 32768;    // Qg: 64 x 128
+constexpr uint32_t pDo = 49152;    // dO: 64 x 128
+constexpr uint32_t pYt = 65536;    // Y^T: 128 (d_v) x 64
+constexpr uint32_t pP = 81920;     // P record tile 64 x 64
+constexpr uint32_t pGam = 90112;   // record gates: exp(G) [64], dec [64]
+constexpr uint32_t pSc = pGam + 512;   // scale exp(G) [64]
+constexpr uint32_t pCtl = pSc + 256;
+constexpr uint32_t kPreTcSmem = pCtl + 64 + 1024;
+constexpr uint32_t qT = 0, qE = 128;   // TMEM columns: T' [0, 128); Y^T then E [128, 256)
+
+struct PreCtl {
+  uint64_t load, mma1, mma2;
+  uint32_t tmem;
+  int abort;
+};
+
+__global__ void __launch_bounds__(kTcThreads, 2) bwd_pre_tc_kernel(const Problem p, const BwdArgs b) {
+  uint8_t* sm = tc_smem_base();
+  const uint32_t s0 = smem_u32(sm);
+  PreCtl* ctl = reinterpret_cast<PreCtl*>(sm + pCtl);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q = warp & 3, h = warp >> 2, d = 32 * q + lane;
+  const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+  const int gc = (int)(blockIdx.x / (unsigned)p.h_v), j = (int)(blockIdx.x % (unsigned)p.h_v);
+  if (tid == 0) {
+    mbar_init(&ctl->load, 1);
+    mbar_init(&ctl->mma1, 1);
+    mbar_init(&ctl->mma2, 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&ctl->tmem, 256);
+    tmem_relinquish();
+  }
+  grid_dependency_wait();
+  grid_launch_dependents();
+  int n, cv;
+  int64_t t0;
+  const bool rows_ok = tc_chunk_rows(p, gc, n, t0, cv);
+  tc_fence_before();
+  const bool skip = __syncthreads_or(tid == 0 && (!rows_ok || earlier_failure(p.status)));
+  tc_fence_after();
+  const uint32_t tm = ctl->tmem;
+  float mx = 0.f;
+  bool ok = !skip;
+  if (ok) {
+    const int iq = (int)(((int64_t)j * p.h_qk) / p.h_v);
+    const uint8_t* rec = p.wy + ((size_t)gc * p.h_v + j) * kRecBytes;
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&ctl->load, 16384u + 8192u + 512u);
+      bulk_load(sm + pWt, rec + kRecWn, 16384u, &ctl->load);
+      bulk_load(sm + pP, rec + kRecP, 8192u, &ctl->load);
+      bulk_load(sm + pGam, rec + kRecGam, 512u, &ctl->load);
+    }
+    rows_to_f16(s0 + pDo, 8192, reinterpret_cast<const __nv_bfloat16*>(b.dout), t0, p.h_v, j, cv, mx);
+    if (!mbar_wait(&ctl->load, 0, kWaitLimitNs)) atomicCAS(&ctl->abort, 0, kDetTmaWait);
+    float* gam = reinterpret_cast<float*>(sm + pGam);
+    float* qsc = reinterpret_cast<float*>(sm + pSc);
+    if (tid < 64) qsc[tid] = p.scale * gam[tid];
+    __syncthreads();
+    rows_to_f16(s0 + pKt, 8192, reinterpret_cast<const __nv_bfloat16*>(p.k), t0, p.h_qk, iq, cv, mx, gam + 64);
+    rows_to_f16(s0 + pQg, 8192, reinterpret_cast<const __nv_bfloat16*>(p.q), t0, p.h_qk, iq, cv, mx, qsc);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    if (__syncthreads_or(ctl->abort != 0)) ok = false;
+  }
+  if (ok && tid == 0) {  // phase 1: Y^T = dO^T P -> E's columns; T' = (-W^T) Ktil
+    tc_fence_after();
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      mma_bf16(tm + qE, dmn_(s0 + pDo, ks, 8192), dmn_(s0 + pP, ks, 8192), idesc_f16(128, 64, true, true), ks > 0);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      mma_bf16(tm + qT, dk_(s0 + pWt, ks, 16384), dmn_(s0 + pKt, ks, 8192), idesc_f16(128, 128, false, true), ks > 0);
+    mma_commit(&ctl->mma1);
+  }
+  if (ok) {
+    if (!wait_phase(&ctl->mma1, 0, &ctl->abort, 220)) ok = false;
+    tc_fence_after();
+  }
+  if (__syncthreads_or(!ok)) ok = false;
+  if (ok) {  // Y^T (lane = d_v) scaled, into its K-major tile
+    float x[32];
+    ld32(tm + lane_base + qE + 32 * h, x);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] *= p.scale;
+    row_f16(s0 + pYt, d, 32 * h, x, mx);
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (ok && tid == 0) {  // phase 2: E = Qg^T dO + (-W^T) Y
+    tc_fence_after();
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      mma_bf16(tm + qE, dmn_(s0 + pQg, ks, 8192), dmn_(s0 + pDo, ks, 8192), idesc_f16(128, 128, true, true), ks > 0);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      mma_bf16(tm + qE, dk_(s0 + pWt, ks, 16384), dk_(s0 + pYt, ks, 16384), idesc_f16(128, 128, false, false), 1);
+    mma_commit(&ctl->mma2);
+  }
+  const size_t slot = ((size_t)gc * p.h_v + j) * 32768u;
+  // T' rows (lane = d_k out) while E's products run: columns 64 h .. 64 h + 63 (panel h)
+  auto store_rows = [&](uint32_t col0, uint8_t* dst) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float x[32];
+      ld32(tm + lane_base + col0 + 64 * h + 32 * half, x);
+      uint32_t w[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        mx = absmax_nan(absmax_nan(mx, x[2 * e]), x[2 * e + 1]);
+        w[e] = pack_f16x2(x[2 * e], x[2 * e + 1]);
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(dst + (size_t)h * 16384u + sw128_offset((uint32_t)d, (uint32_t)(4 * half + c))) =
+            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    }
+  };
+  if (ok) store_rows(qT, b.tmat + slot);
+  if (ok) {
+    if (!wait_phase(&ctl->mma2, 0, &ctl->abort, 221)) ok = false;
+    tc_fence_after();
+  }
+  if (__syncthreads_or(!ok)) ok = false;
+  if (ok) store_rows(qE, b.emat + slot);
+  if (skip && tid == 0 && !rows_ok) report(p.status, kDevCheck, kDetSegMismatch);
+  tc_fence_before();
+  __syncthreads();
+  if (!skip && (!ok || ctl->abort)) {
+    if (tid == 0) report(p.status, kDevTimeout, ctl->abort ? ctl->abort : kDetMmaWait);
+    const uint64_t t_start = globaltimer_ns();
+    while (globaltimer_ns() - t_start < 2000000ull) {
+    }
+    __syncthreads();
+  }
+  if (!(mx < 65504.f)) report(p.status, kDevCheck, kDetFp16Range);
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tm, 256);
+  }
+}
+
+// ------------------------------------------------------------ state-gradient chain
+// One chain over one segment's chunks in reverse, D <- gamma_C D + E_c + T'_c D_c:
+// the product on tcgen05 (M = d_k out, N = d_v, K = d_k in; A = T' from the
+// record, B = D's fp16 copy in shared memory), D itself in fp32 registers
+// (thread: TMEM lane = row d_k, 64 of the 128 columns).  Modes: final
+// (PREP = false; grid x = segment) writes every chunk's D
+// before its step (fp16 tile image) and dh0 for a sequence's first segment,
+// starting from dh_T (a sequence's last segment) or the combine's D_end;
+// preprocessing (PREP; grid x = 2 segment + chain) runs the transition (chain
+// 0, from I, no E) or the local offset (chain 1, from 0) and stores it
+// transposed for the combine.  Without context parallelism every sequence is
+// one segment.
+constexpr uint32_t cT = 0;          // 2 x T' (32 KB): rows d_k out, panels d_k in 0-63 | 64-127
+constexpr uint32_t cE = 65536;      // 2 x E (32 KB): rows d_k, panels d_v
+constexpr uint32_t cD = 131072;     // D's fp16 copy: rows d_k (K), panels d_v 0-63 | 64-127
+constexpr uint32_t cCtl = 163840;
+constexpr uint32_t kChainSmem = cCtl + 128 + 1024;
+
+struct ChCtl {
+  uint64_t load[2], mma;
+  uint32_t tmem;
+  int abort;
+  SegInfo si;
+  int ok;
+};
+
+template <bool PREP>
+__global__ void __launch_bounds__(kTcThreads, 1) bwd_chain_tc_kernel(const Problem p, const BwdArgs b) {
+  uint8_t* sm = tc_smem_base();
+  const uint32_t s0 = smem_u32(sm);
+  ChCtl* ctl = reinterpret_cast<ChCtl*>(sm + cCtl);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q = warp & 3, h = warp >> 2, k = 32 * q + lane;
+  const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+  const int j = blockIdx.y;
+  const int chain = PREP ? (int)(blockIdx.x & 1) : 0;
+  const int seg = PREP ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  if (warp == 1) {
+    SegInfo si;
+    const bool okseg = locate_segment(p, seg, si);
+    if (lane == 0) {
+      ctl->si = si;
+      ctl->ok = okseg;
+    }
+  }
+  if (tid == 0) {
+    mbar_init(&ctl->load[0], 1);
+    mbar_init(&ctl->load[1], 1);
+    mbar_init(&ctl->mma, 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&ctl->tmem, 128);
+    tmem_relinquish();
+  }
+  grid_dependency_wait();
+  grid_launch_dependents();
+  tc_fence_before();
+  const bool failed = __syncthreads_or(tid == 0 && earlier_failure(p.status));
+  tc_fence_after();
+  const uint32_t tm = ctl->tmem;
+  const SegInfo si = ctl->si;
+  bool run = !failed && ctl->ok;
+  if (!failed && !ctl->ok && tid == 0) report(p.status, kDevCheck, kDetSegMismatch);
+  const bool last_seg = si.s == si.n_seg - 1;
+  if (PREP && run) {
+    if (si.s == 0) run = false;                                   // segment 0 is taken by the final pass
+    if (chain == 0 && last_seg && b.dhT == nullptr) run = false;  // its transition would act on zero
+  }
+  const int c0 = run ? seq_first_chunk(p, si.n) + si.cb : 0, nc = run ? si.ce - si.cb : 0;
+  const size_t mat = (size_t)kDim * kDim;
+  const size_t head_seg = ((size_t)(si.seg_base + si.s) * p.h_v + j) * mat;
+  const bool with_e = !(PREP && chain == 0);
+  float D[64];  // row k, columns 64 h .. 64 h + 63
+  if (run) {
+    if (PREP) {
+#pragma unroll
+      for (int e = 0; e < 64; ++e) D[e] = (chain == 0 && 64 * h + e == k) ? 1.f : 0.f;
+    } else if (!last_seg) {  // D_end of this segment from the combine, stored transposed (rows d_v)
+      const float* src = p.Sstart + head_seg;
+#pragma unroll
+      for (int e = 0; e < 64; ++e) D[e] = src[(size_t)(64 * h + e) * kDim + k];
+    } else if (b.dhT) {
+      const float4* src = reinterpret_cast<const float4*>(b.dhT + ((size_t)si.n * p.h_v + j) * mat + (size_t)k * kDim + 64 * h);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const float4 v4 = src[e];
+        D[4 * e] = v4.x;
+        D[4 * e + 1] = v4.y;
+        D[4 * e + 2] = v4.z;
+        D[4 * e + 3] = v4.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 64; ++e) D[e] = 0.f;
+    }
+  }
+  float mx = 0.f;
+  // D's fp16 copy as row k of the tile (panel h), and as chunk c's record when asked
+  auto store_d = [&](uint8_t* global_row) {
+    uint32_t w[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      mx = absmax_nan(absmax_nan(mx, D[2 * e]), D[2 * e + 1]);
+      w[e] = pack_f16x2(D[2 * e], D[2 * e + 1]);
+    }
+    const uint32_t panel = s0 + cD + (uint32_t)h * 16384u;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      st_shared_v4(panel + sw128_offset((uint32_t)k, (uint32_t)c), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+      if (global_row)
+        *reinterpret_cast<uint4*>(global_row + sw128_offset((uint32_t)k, (uint32_t)c)) =
+            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    }
+  };
+  auto issue = [&](int it) {  // T' (and E) of step it into buffer it & 1 (one thread)
+    const int c = c0 + nc - 1 - it;
+    const size_t slot = ((size_t)c * p.h_v + j) * 32768u;
+    const uint32_t buf = (uint32_t)(it & 1) * 32768u;
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(&ctl->load[it & 1], with_e ? 65536u : 32768u);
+    bulk_load(sm + cT + buf, b.tmat + slot, 32768u, &ctl->load[it & 1]);
+    if (with_e) bulk_load(sm + cE + buf, b.emat + slot, 32768u, &ctl->load[it & 1]);
+  };
+  if (tid == 0 && nc > 0) issue(0);
+  bool ok = true;
+  if (nc > 0) {
+    // the first step's D_c is D itself
+    store_d(PREP ? nullptr : b.dstate + ((size_t)(c0 + nc - 1) * p.h_v + j) * 32768u + (size_t)h * 16384u);
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  for (int it = 0; it < nc && ok; ++it) {
+    const int c = c0 + nc - 1 - it;
+    const uint32_t buf = (uint32_t)(it & 1) * 32768u;
+    const float gC = reinterpret_cast<const float*>(p.wy + ((size_t)c * p.h_v + j) * kRecBytes + kRecGam)[63];
+    if (!mbar_wait(&ctl->load[it & 1], (uint32_t)((it >> 1) & 1), kWaitLimitNs)) atomicCAS(&ctl->abort, 0, kDetTmaWait);
+    if (tid == 0 && !ctl->abort) {  // T'_c D_c
+      tc_fence_after();
+      const uint32_t id = idesc_f16(128, 128, false, true);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_bf16(tm, dk_(s0 + cT + buf, ks, 16384), dmn_(s0 + cD, ks, 16384), id, ks > 0);
+      mma_commit(&ctl->mma);
+      if (it + 1 < nc) issue(it + 1);  // buffer (it + 1) & 1 was last read in step it - 1
+    }
+    // E_c and gamma_C D while the product runs
+    if (with_e) {
+      const uint32_t epanel = s0 + cE + buf + (uint32_t)h * 16384u;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        const uint4 w = lds_u32x4(epanel + sw128_offset((uint32_t)k, (uint32_t)c8));
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[e]));
+          D[8 * c8 + 2 * e] = fmaf(gC, D[8 * c8 + 2 * e], f.x);
+          D[8 * c8 + 2 * e + 1] = fmaf(gC, D[8 * c8 + 2 * e + 1], f.y);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 64; ++e) D[e] *= gC;
+    }
+    if (!wait_phase(&ctl->mma, (uint32_t)(it & 1), &ctl->abort, 210)) ok = false;
+    tc_fence_after();
+    if (__syncthreads_or(!ok || ctl->abort)) {
+      ok = false;
+      break;
+    }
+    {
+      float a[32];
+      ld32(tm + lane_base + 64 * h, a);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) D[e] += a[e];
+      ld32(tm + lane_base + 64 * h + 32, a);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) D[32 + e] += a[e];
+    }
+    // D_{c-1} for the next step (and as the previous chunk's record)
+    if (it + 1 < nc)
+      store_d(PREP ? nullptr : b.dstate + ((size_t)(c - 1) * p.h_v + j) * 32768u + (size_t)h * 16384u);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+  }
+  if (run && ok && !ctl->abort) {
+    if (PREP) {  // transposed (rows d_v, or the transition's column index) for the combine
+      float* dst = (chain == 0 ? p.R : p.Sloc) + head_seg;
+#pragma unroll
+      for (int e = 0; e < 64; ++e) dst[(size_t)(64 * h + e) * kDim + k] = D[e];
+    } else if (si.s == 0 && b.dh0) {
+      float4* dst = reinterpret_cast<float4*>(b.dh0 + ((size_t)si.n * p.h_v + j) * mat + (size_t)k * kDim + 64 * h);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) dst[e] = make_float4(D[4 * e], D[4 * e + 1], D[4 * e + 2], D[4 * e + 3]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (ctl->abort || !ok) {
+    if (tid == 0) report(p.status, kDevTimeout, ctl->abort ? ctl->abort : kDetMmaWait);
+    const uint64_t t_start = globaltimer_ns();
+    while (globaltimer_ns() - t_start < 2000000ull) {
+    }
+    __syncthreads();
+  }
+  if (!(mx < 65504.f)) report(p.status, kDevCheck, kDetFp16Range);
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tm, 128);
+  }
 }
 
 }  // namespace
 
-namespace {
-cudaError_t bwd_attrs() {
-  static cudaError_t once = [] {
-    cudaError_t e = cudaFuncSetAttribute(bwd_pre_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPreSmem);
+cudaError_t launch_bwd_pre_tc(const Problem& p, const BwdArgs& b, cudaStream_t st) {
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(bwd_pre_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPreTcSmem);
+  if (attr != cudaSuccess) return attr;
+  const unsigned grid = (unsigned)p.n_chunks_total * (unsigned)p.h_v;
+  return launch_kernel(bwd_pre_tc_kernel, dim3(grid), dim3(kTcThreads), kPreTcSmem, st, true, p, b);
+}
+
+cudaError_t launch_bwd_chain_tc(const Problem& p, const BwdArgs& b, bool prep, cudaStream_t st) {
+  static const cudaError_t attr = [] {
+    cudaError_t e = cudaFuncSetAttribute(bwd_chain_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kChainSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(bwd_chain_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kChainSmem);
     return e;
   }();
-  return once;
-}
-}  // namespace
-
-cudaError_t launch_bwd_pre(const Problem& p, const BwdArgs& b, cudaStream_t st) {
-  cudaError_t e = bwd_attrs();
-  if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)p.n_chunks_total * (unsigned)p.h_v;
-  return launch_kernel(bwd_pre_kernel, dim3(grid), dim3(kBwdThreads), kPreSmem, st, true, p, b);
+  if (attr != cudaSuccess) return attr;
+  if (prep)
+    return launch_kernel(bwd_chain_tc_kernel<true>, dim3(2 * p.n_seg_total, p.h_v), dim3(kTcThreads), kChainSmem, st,
+                         true, p, b);
+  return launch_kernel(bwd_chain_tc_kernel<false>, dim3(p.n_seg_total, p.h_v), dim3(kTcThreads), kChainSmem, st, true,
+                       p, b);
 }
 
-
+cudaError_t launch_bwd_local_tc(const Problem& p, const BwdArgs& b, cudaStream_t st) {
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(bwd_local_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+  if (attr != cudaSuccess) return attr;
+  const unsigned grid = (unsigned)p.n_chunks_total * (unsigned)p.h_qk;
+  return launch_kernel(bwd_local_tc_kernel, dim3(grid), dim3(kTcThreads), kTcSmem, st, true, p, b);
+}
 
 }  // namespace gdn

@@ -334,10 +334,10 @@ cudaError_t launch_recurrence_f32(const Problem& p, cudaStream_t st, bool depend
 cudaError_t launch_f32_prep(const Problem& p, cudaStream_t st);
 cudaError_t f32_kernel_setup();
 cudaError_t launch_decode(const DecodeArgs& a, bool f32, cudaStream_t st);
-cudaError_t launch_bwd_pre(const Problem& p, const BwdArgs& b, cudaStream_t st);
 cudaError_t launch_combine_bwd(const Problem& p, int sm_count, cudaStream_t st);
 cudaError_t launch_bwd_local_tc(const Problem& p, const BwdArgs& b, cudaStream_t st);
 cudaError_t launch_bwd_chain_tc(const Problem& p, const BwdArgs& b, bool prep, cudaStream_t st);
+cudaError_t launch_bwd_pre_tc(const Problem& p, const BwdArgs& b, cudaStream_t st);
 cudaError_t scan_kernel_setup();
 cudaError_t wy_kernel_setup();
 cudaError_t combine_kernel_setup();
