@@ -40,7 +40,8 @@
 // tokens as columns, or two stacked 64-row operands ([dO; dV'], [Q; K]).  The
 // per-token sums over a head dimension (dgamma, ddec, <Y_U, V>, <Y_W, K>) are
 // column sums across TMEM lanes: a 31-shuffle butterfly per warp, then the
-// four lane quarters through shared memory.  Operand tiles are fp16 in the
+// four lane quarters through shared memory.  16 warps: four per lane quarter,
+// each thread taking 16 of a 64-column accumulator.  Operand tiles are fp16 in the
 // forward's 128-byte-swizzled image (bulk copies of the records and states,
 // the rest written by the epilogues); one thread issues the MMAs and commits
 // each phase to an mbarrier; every wait is bounded.
@@ -53,6 +54,7 @@ namespace gdn {
 namespace {
 
 constexpr int kTcThreads = 256;
+constexpr int kLocThreads = 512;  // the chunk-local kernel: 16 warps (4 per lane quarter)
 
 // ---- shared memory (bytes from a 1024-byte aligned base) ----
 constexpr uint32_t sQK = 0;          // [Q d0-63 | K d0-63 | Q d64-127 | K d64-127], 64 rows each
@@ -69,11 +71,11 @@ constexpr uint32_t sV = 204800;      // V: 64 rows x 128 bf16, plain row-major (
 constexpr uint32_t sF = 221184;      // fp32: G, exp(G), dec, beta [64 each]
 constexpr uint32_t sRed = sF + 1024; // fp32 reductions (below)
 constexpr int kRedCol = 0;           //   [4 kinds][4 lane quarters][64]: dgamma gamma, ddec, t1, t2
-constexpr int kRedRowE = 1024;       //   [2 sources][2 halves][64]: row sums of dGam * Gam
-constexpr int kRedColE = 1280;       //   [4 quarters][64]: column sums of dGam * Gam
-constexpr int kRedRowB = 1536;       //   [2 halves][64]: sum_s dL KK Gam
-constexpr int kRedMisc = 1664;       //   [16]: scan carries
-constexpr uint32_t sCtl = sRed + 7168;
+constexpr int kRedRowE = 1024;       //   [2 sources][4 column groups][64]: row sums of dGam * Gam
+constexpr int kRedColE = 1536;       //   [4 quarters][64]: column sums of dGam * Gam
+constexpr int kRedRowB = 1792;       //   [4 column groups][64]: sum_s dL KK Gam
+constexpr int kRedMisc = 2048;       //   [16]: scan carries, <D, H> per warp
+constexpr uint32_t sCtl = sRed + 8448;
 constexpr uint32_t kTcSmem = sCtl + 256 + 1024;
 static_assert(kTcSmem <= 232448, "shared memory over the per-block limit");
 
@@ -128,17 +130,10 @@ __device__ __forceinline__ void ld32(uint32_t taddr, float (&x)[32]) {
     x[16 + i] = __uint_as_float(b[i]);
   }
 }
-__device__ __forceinline__ void st32(uint32_t taddr, const float (&x)[32]) {
-  uint32_t a[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) a[i] = __float_as_uint(x[i]);
-  tmem_st32(taddr, a);
-}
-
-// Column sums of x[0..31] over the 32 lanes of a warp: lane l returns the sum of
-// column l (recursive halving, 31 shuffles).
+// One recursive-halving step of a column sum over the lanes of a warp (see
+// butterfly16): lanes with bit OFF set keep the upper half of their values.
 template <int OFF>
-__device__ __forceinline__ void butterfly_step(float (&x)[32], int lane) {
+__device__ __forceinline__ void butterfly_step16(float (&x)[16], int lane) {
   const bool up = (lane & OFF) != 0;
 #pragma unroll
   for (int i = 0; i < OFF; ++i) {
@@ -146,15 +141,6 @@ __device__ __forceinline__ void butterfly_step(float (&x)[32], int lane) {
     const float keep = up ? x[i + OFF] : x[i];
     x[i] = keep + __shfl_xor_sync(0xffffffffu, send, OFF);
   }
-}
-__device__ __forceinline__ float butterfly_colsum(float (&x)[32]) {
-  const int lane = threadIdx.x & 31;
-  butterfly_step<16>(x, lane);
-  butterfly_step<8>(x, lane);
-  butterfly_step<4>(x, lane);
-  butterfly_step<2>(x, lane);
-  butterfly_step<1>(x, lane);
-  return x[0];
 }
 
 // 32 fp16 values (x, optionally scaled per column) as row `row` of an fp16
@@ -187,20 +173,21 @@ __device__ __forceinline__ void st_h(uint32_t addr, float x) {
 
 // 64 rows x 128 bf16 of a [tokens, heads, 128] tensor into two fp16 panels
 // (panel stride pstride); rows >= cv are zero.
+template <int NT = kTcThreads>
 __device__ __forceinline__ void rows_to_f16(uint32_t base, uint32_t pstride, const __nv_bfloat16* src, int64_t t0,
                                             int heads, int head, int cv, float& mx, const float* row_scale = nullptr) {
   // all four loads in flight before the first store (the stores are ordered memory operations)
-  constexpr int kPer = 64 * 16 / kTcThreads;
+  constexpr int kPer = 64 * 16 / NT;
   uint4 raw[kPer];
 #pragma unroll
   for (int u = 0; u < kPer; ++u) {
-    const int idx = threadIdx.x + u * kTcThreads, r = idx >> 4, c = idx & 15;
+    const int idx = threadIdx.x + u * NT, r = idx >> 4, c = idx & 15;
     raw[u] = make_uint4(0, 0, 0, 0);
     if (r < cv) raw[u] = *reinterpret_cast<const uint4*>(src + ((size_t)(t0 + r) * heads + head) * kDim + c * 8);
   }
 #pragma unroll
   for (int u = 0; u < kPer; ++u) {
-    const int idx = threadIdx.x + u * kTcThreads, r = idx >> 4, c = idx & 15;
+    const int idx = threadIdx.x + u * NT, r = idx >> 4, c = idx & 15;
     const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
     const float sc = row_scale ? row_scale[r] : 1.f;
     uint32_t o[4];
@@ -212,6 +199,46 @@ __device__ __forceinline__ void rows_to_f16(uint32_t base, uint32_t pstride, con
     }
     st_shared_v4(base + (uint32_t)(c >> 3) * pstride + sw128_offset((uint32_t)r, (uint32_t)(c & 7)), o[0], o[1],
                  o[2], o[3]);
+  }
+}
+
+// 16-column variants (the chunk-local kernel: 16 warps, a thread takes 16 of a
+// 64-column accumulator)
+__device__ __forceinline__ void ld16f(uint32_t taddr, float (&x)[16]) {
+  uint32_t a[16];
+  tmem_ld16(taddr, a);
+  tmem_ld_wait(a);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(a[i]);
+}
+__device__ __forceinline__ void st16f(uint32_t taddr, const float (&x)[16]) {
+  uint32_t a[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a[i] = __float_as_uint(x[i]);
+  tmem_st16(taddr, a);
+}
+// Column sums of x[0..15] over the 32 lanes of a warp: lanes l and l + 16 return
+// the sum of column l (the halves added first, then recursive halving).
+__device__ __forceinline__ float butterfly16(float (&x)[16]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) x[i] += __shfl_xor_sync(0xffffffffu, x[i], 16);
+  butterfly_step16<8>(x, lane);
+  butterfly_step16<4>(x, lane);
+  butterfly_step16<2>(x, lane);
+  butterfly_step16<1>(x, lane);
+  return x[0];
+}
+__device__ __forceinline__ void row_f16_16(uint32_t panel, int row, int c0, const float (&x)[16], float& mx) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      mx = absmax_nan(absmax_nan(mx, x[8 * q + 2 * e]), x[8 * q + 2 * e + 1]);
+      w[e] = pack_f16x2(x[8 * q + 2 * e], x[8 * q + 2 * e + 1]);
+    }
+    st_shared_v4(panel + sw128_offset((uint32_t)row, (uint32_t)((c0 >> 3) + q)), w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -230,7 +257,7 @@ __device__ __forceinline__ bool tc_chunk_rows(const Problem& p, int gc, int& n, 
   return n >= 0 && n < p.n_seqs && cv > 0 && cv <= kChunk;
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1) bwd_local_tc_kernel(const Problem p, const BwdArgs b) {
+__global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Problem p, const BwdArgs b) {
   uint8_t* sm = tc_smem_base();
   const uint32_t s0 = smem_u32(sm);
   TcCtl* ctl = reinterpret_cast<TcCtl*>(sm + sCtl);
@@ -240,7 +267,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_local_tc_kernel(const Probl
   float* sBeta = sG + 192;
   float* red = reinterpret_cast<float*>(sm + sRed);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int q = warp & 3, h = warp >> 2;         // TMEM lane quarter, column half
+  const int q = warp & 3, h = warp >> 2;         // TMEM lane quarter, group of 16 columns
   const int d = 32 * q + lane;                   // this thread's TMEM lane
   const uint32_t lane_base = (uint32_t)(32 * q) << 16;
   const int gc = (int)(blockIdx.x / (unsigned)p.h_qk), iq = (int)(blockIdx.x % (unsigned)p.h_qk);
@@ -297,14 +324,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_local_tc_kernel(const Probl
   if (ok) {
     // dq^T and dk^T accumulators start at zero
     {
-      float z[32];
+      float z[16];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) z[i] = 0.f;
-      st32(tmem + tDQ + 32 * h, z);
-      st32(tmem + tDK + 32 * h, z);
+      for (int i = 0; i < 16; ++i) z[i] = 0.f;
+      st16f(tmem + tDQ + 16 * h, z);
+      st16f(tmem + tDK + 16 * h, z);
     }
-    rows_to_f16(s0 + sQK, 16384, reinterpret_cast<const __nv_bfloat16*>(p.q), t0, p.h_qk, iq, cv, mx);
-    rows_to_f16(s0 + sQK + 8192, 16384, reinterpret_cast<const __nv_bfloat16*>(p.k), t0, p.h_qk, iq, cv, mx);
+    rows_to_f16<kLocThreads>(s0 + sQK, 16384, reinterpret_cast<const __nv_bfloat16*>(p.q), t0, p.h_qk, iq, cv, mx);
+    rows_to_f16<kLocThreads>(s0 + sQK + 8192, 16384, reinterpret_cast<const __nv_bfloat16*>(p.k), t0, p.h_qk, iq, cv, mx);
     fence_proxy_async_smem();
     tmem_st_wait();
     tc_fence_before();
@@ -323,7 +350,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_local_tc_kernel(const Probl
       }
     }
     if (j_lo < j_hi)
-      rows_to_f16(s0 + sDOV, 16384, reinterpret_cast<const __nv_bfloat16*>(b.dout), t0, p.h_v, j_lo, cv, mx);
+      rows_to_f16<kLocThreads>(s0 + sDOV, 16384, reinterpret_cast<const __nv_bfloat16*>(b.dout), t0, p.h_v, j_lo, cv, mx);
   }
   // this head's g and beta for threads 0-63 (prefetched during the head before)
   float g_cur = 0.f, b_cur = 0.f;
@@ -388,7 +415,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_local_tc_kernel(const Probl
     }
     // <D, H> = sum D[k][v] S[v][k] (the gradient of gamma_C) while the products run:
     // thread = one 8 x 8 block, rows k0.. of D against rows v0.. of S
-    {
+    if (tid < 256) {  // 16 x 16 blocks of 8 x 8: the first eight warps
       const int k0 = 8 * (tid >> 4), v0 = 8 * (tid & 15);
       const uint32_t dpanel = s0 + sD + (uint32_t)(v0 >> 6) * 16384u;
       const uint32_t spanel = s0 + sS + (uint32_t)(k0 >> 6) * 16384u;
@@ -423,11 +450,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_local_tc_kernel(const Probl
     tc_fence_after();
     if (ok) {
       // V'^T = U^T - S W^T (lane = d_v)
-      float x[32];
-      ld32(tmem + tA + 32 * h, x);
+      float x[16];
+      ld16f(tmem + tA + 16 * h, x);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint4 u = lds_u32x4(s0 + sUt + sw128_offset((uint32_t)d, (uint32_t)(4 * h + c)));
+      for (int c = 0; c < 2; ++c) {
+        const uint4 u = lds_u32x4(s0 + sUt + sw128_offset((uint32_t)d, (uint32_t)(2 * h + c)));
         const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -436,30 +463,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_local_tc_kernel(const Probl
           x[8 * c + 2 * e + 1] += u2.y;
         }
       }
-      row_f16(s0 + sVpT, d, 32 * h, x, mx);
+      row_f16_16(s0 + sVpT, d, 16 * h, x, mx);
       // dV'^T = scale dO^T P + diag(dec) applied to D^T K^T's columns; also dV' (rows r)
-      float y[32];
-      ld32(tmem + tB + 32 * h, x);
-      ld32(tmem + tC + 32 * h, y);
+      float y[16];
+      ld16f(tmem + tB + 16 * h, x);
+      ld16f(tmem + tC + 16 * h, y);
       const uint32_t dvp = s0 + sDOV + 8192u + (uint32_t)(d >> 6) * 16384u;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        x[i] = fmaf(p.scale, x[i], sDec[32 * h + i] * y[i]);
-        st_h(el(dvp, 32 * h + i, d & 63), x[i]);
+      for (int i = 0; i < 16; ++i) {
+        x[i] = fmaf(p.scale, x[i], sDec[16 * h + i] * y[i]);
+        st_h(el(dvp, 16 * h + i, d & 63), x[i]);
       }
-      row_f16(s0 + sWt, d, 32 * h, x, mx);
+      row_f16_16(s0 + sWt, d, 16 * h, x, mx);
       // H dO^T (lane = d_k): dq^T += scale gamma_r (H dO^T); dgamma_r gamma_r = <Q_r, that>
-      ld32(tmem + tE + 32 * h, x);
-      ld32(tmem + tDQ + 32 * h, y);
+      ld16f(tmem + tE + 16 * h, x);
+      ld16f(tmem + tDQ + 16 * h, y);
       const uint32_t qpanel = s0 + sQK + (uint32_t)(d >> 6) * 16384u;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        x[i] *= p.scale * sGam[32 * h + i];
+      for (int i = 0; i < 16; ++i) {
+        x[i] *= p.scale * sGam[16 * h + i];
         y[i] += x[i];
-        x[i] *= ld_h(el(qpanel, 32 * h + i, d & 63));
+        x[i] *= ld_h(el(qpanel, 16 * h + i, d & 63));
       }
-      st32(tmem + tDQ + 32 * h, y);
-      red[kRedCol + (0 * 4 + q) * 64 + 32 * h + lane] = butterfly_colsum(x);
+      st16f(tmem + tDQ + 16 * h, y);
+      {
+        const float cs_ = butterfly16(x);
+        if (lane < 16) red[kRedCol + (0 * 4 + q) * 64 + 16 * h + lane] = cs_;
+      }
     }
     fence_proxy_async_smem();
     tmem_st_wait();
@@ -488,24 +518,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_local_tc_kernel(const Probl
     if (tid == 0 && ok && j + 1 < j_hi) issue_A(j + 1);  // D and -W^T are read
     tc_fence_after();
     if (ok) {
-      float x[32], y[32];
+      float x[16], y[16];
       // D V'^T (lane = d_k): dk^T += dec_r (.); ddec_r = <K_r, .>
-      ld32(tmem + tF + 32 * h, x);
-      ld32(tmem + tDK + 32 * h, y);
+      ld16f(tmem + tF + 16 * h, x);
+      ld16f(tmem + tDK + 16 * h, y);
       const uint32_t kpanel = s0 + sQK + 8192u + (uint32_t)(d >> 6) * 16384u;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        y[i] = fmaf(sDec[32 * h + i], x[i], y[i]);
-        x[i] *= ld_h(el(kpanel, 32 * h + i, d & 63));
+      for (int i = 0; i < 16; ++i) {
+        y[i] = fmaf(sDec[16 * h + i], x[i], y[i]);
+        x[i] *= ld_h(el(kpanel, 16 * h + i, d & 63));
       }
-      st32(tmem + tDK + 32 * h, y);
-      red[kRedCol + (1 * 4 + q) * 64 + 32 * h + lane] = butterfly_colsum(x);
+      st16f(tmem + tDK + 16 * h, y);
+      {
+        const float cs_ = butterfly16(x);
+        if (lane < 16) red[kRedCol + (1 * 4 + q) * 64 + 16 * h + lane] = cs_;
+      }
       // Y_U^T (lane = d_v): dv = beta_r Y_U; t1_r = <Y_U_r, V_r>; Y_U^T into the U^T slot
-      ld32(tmem + tA + 32 * h, x);
-      row_f16(s0 + sUt, d, 32 * h, x, mx);
+      ld16f(tmem + tA + 16 * h, x);
+      row_f16_16(s0 + sUt, d, 16 * h, x, mx);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {  // dv staged in the V'^T slot (read by phase 2), stored in epilogue 3
-        const int r = 32 * h + i;
+      for (int i = 0; i < 16; ++i) {  // dv staged in the V'^T slot (read by phase 2), stored in epilogue 3
+        const int r = 16 * h + i;
         const __nv_bfloat16 dvb = __float2bfloat16_rn(sBeta[r] * x[i]);
         asm volatile("st.shared.u16 [%0], %1;" ::"r"(s0 + sVpT + (uint32_t)(r * 256 + 2 * d)),
                      "h"(*reinterpret_cast<const unsigned short*>(&dvb))
@@ -514,16 +547,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_local_tc_kernel(const Probl
         asm volatile("ld.shared.u16 %0, [%1];" : "=h"(vb) : "r"(s0 + sV + (uint32_t)(r * 256 + 2 * d)) : "memory");
         x[i] = r < cv ? x[i] * __uint_as_float((uint32_t)vb << 16) : 0.f;
       }
-      red[kRedCol + (2 * 4 + q) * 64 + 32 * h + lane] = butterfly_colsum(x);
+      {
+        const float cs_ = butterfly16(x);
+        if (lane < 16) red[kRedCol + (2 * 4 + q) * 64 + 16 * h + lane] = cs_;
+      }
       // [dP_raw; dL_raw] (lane = token r, or 64 + r)
-      ld32(tmem + tC + 32 * h, x);
+      ld16f(tmem + tC + 16 * h, x);
       if (q < 2) {
         const int r = d;
-        ld32(tmem + tQK + 32 * h, y);
+        ld16f(tmem + tQK + 16 * h, y);
         float rowsum = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int s = 32 * h + i;
+        for (int i = 0; i < 16; ++i) {
+          const int s = 16 * h + i;
           const float gam = s <= r ? __expf(sG[r] - sG[s]) : 0.f;
           const float dP = s <= r ? p.scale * x[i] : 0.f;
           const float e = dP * y[i] * gam;
@@ -531,11 +567,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_local_tc_kernel(const Probl
           x[i] = dP * gam;
           y[i] = e;
         }
-        row_f16(s0 + sPG, r, 32 * h, x, mx);
-        red[kRedRowE + (0 * 2 + h) * 64 + r] = rowsum;
-        red[kRedColE + q * 64 + 32 * h + lane] = butterfly_colsum(y);
+        row_f16_16(s0 + sPG, r, 16 * h, x, mx);
+        red[kRedRowE + (0 * 4 + h) * 64 + r] = rowsum;
+        {
+        const float cs_ = butterfly16(y);
+        if (lane < 16) red[kRedColE + q * 64 + 16 * h + lane] = cs_;
+      }
       } else {
-        row_f16(s0 + sP, d - 64, 32 * h, x, mx);
+        row_f16_16(s0 + sP, d - 64, 16 * h, x, mx);
       }
     }
     fence_proxy_async_smem();
@@ -570,8 +609,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_local_tc_kernel(const Probl
     if (ok) {  // dv of this head from its staging rows: 16-byte stores, whole rows per warp
       uint8_t* dvo = reinterpret_cast<uint8_t*>(b.dv);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int idx = tid + u * kTcThreads, r = idx >> 4, c = idx & 15;
+      for (int u = 0; u < 2; ++u) {
+        const int idx = tid + u * kLocThreads, r = idx >> 4, c = idx & 15;
         const uint4 w = lds_u32x4(s0 + sVpT + (uint32_t)(r * 256 + c * 16));
         if (r < cv) *reinterpret_cast<uint4*>(dvo + (((size_t)(t0 + r) * p.h_v + j) * kDim) * 2 + c * 16) = w;
       }
@@ -583,29 +622,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_local_tc_kernel(const Probl
       b_next = p.beta[(size_t)(t0 + tid) * p.h_v + j + 1];
     }
     if (ok) {
-      float x[32], y[32];
+      float x[16], y[16];
       // Y_W^T = -H Y_U^T (lane = d_k): dk^T += beta_r gamma_r Y_W^T; t2_r = <Y_W_r, K_r>
-      ld32(tmem + tB + 32 * h, x);
-      ld32(tmem + tDK + 32 * h, y);
+      ld16f(tmem + tB + 16 * h, x);
+      ld16f(tmem + tDK + 16 * h, y);
       const uint32_t kpanel = s0 + sQK + 8192u + (uint32_t)(d >> 6) * 16384u;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int r = 32 * h + i;
+      for (int i = 0; i < 16; ++i) {
+        const int r = 16 * h + i;
         y[i] = fmaf(-sBeta[r] * sGam[r], x[i], y[i]);
         x[i] = -x[i] * ld_h(el(kpanel, r, d & 63));
       }
-      st32(tmem + tDK + 32 * h, y);
-      red[kRedCol + (3 * 4 + q) * 64 + 32 * h + lane] = butterfly_colsum(x);
+      st16f(tmem + tDK + 16 * h, y);
+      {
+        const float cs_ = butterfly16(x);
+        if (lane < 16) red[kRedCol + (3 * 4 + q) * 64 + 16 * h + lane] = cs_;
+      }
       // dL = -A^T dL_raw, s < r (lanes 64-127: r = lane - 64)
       if (q >= 2) {
         const int r = d - 64;
-        ld32(tmem + tE + 32 * h, x);
-        ld32(tmem + tQK + 32 * h, y);  // K K^T [r][s]
+        ld16f(tmem + tE + 16 * h, x);
+        ld16f(tmem + tQK + 16 * h, y);  // K K^T [r][s]
         const float br = sBeta[r];
         float rowb = 0.f, rowe = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int s = 32 * h + i;
+        for (int i = 0; i < 16; ++i) {
+          const int s = 16 * h + i;
           const float gam = s < r ? __expf(sG[r] - sG[s]) : 0.f;
           const float dL = s < r ? -x[i] : 0.f;
           const float xb = dL * y[i] * gam;
@@ -614,14 +656,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_local_tc_kernel(const Probl
           x[i] = dL * br * gam;
           y[i] = br * xb;
         }
-        row_f16(s0 + sP, r, 32 * h, x, mx);
+        row_f16_16(s0 + sP, r, 16 * h, x, mx);
         red[kRedRowB + h * 64 + r] = rowb;
-        red[kRedRowE + (1 * 2 + h) * 64 + r] = rowe;
-        red[kRedColE + q * 64 + 32 * h + lane] = butterfly_colsum(y);
+        red[kRedRowE + (1 * 4 + h) * 64 + r] = rowe;
+        {
+        const float cs_ = butterfly16(y);
+        if (lane < 16) red[kRedColE + q * 64 + 16 * h + lane] = cs_;
+      }
       }
     }
     if (ok && j + 1 < j_hi)  // the next head's dO (its slots were last read by phase 2)
-      rows_to_f16(s0 + sDOV, 16384, reinterpret_cast<const __nv_bfloat16*>(b.dout), t0, p.h_v, j + 1, cv, mx);
+      rows_to_f16<kLocThreads>(s0 + sDOV, 16384, reinterpret_cast<const __nv_bfloat16*>(b.dout), t0, p.h_v, j + 1, cv, mx);
     fence_proxy_async_smem();
     tmem_st_wait();
     tc_fence_before();
@@ -649,13 +694,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_local_tc_kernel(const Probl
                red[kRedCol + (kind * 4 + 2) * 64 + r] + red[kRedCol + (kind * 4 + 3) * 64 + r];
       };
       const float t2 = col(3);
-      const float erow = red[kRedRowE + 0 * 64 + r] + red[kRedRowE + 1 * 64 + r] + red[kRedRowE + 2 * 64 + r] +
-                         red[kRedRowE + 3 * 64 + r];
+      float erow = 0.f;
+#pragma unroll
+      for (int g8 = 0; g8 < 8; ++g8) erow += red[kRedRowE + g8 * 64 + r];
       const float ecol = red[kRedColE + r] + red[kRedColE + 64 + r] + red[kRedColE + 128 + r] +
                          red[kRedColE + 192 + r];
       const float ddec = col(1) * sDec[r];
       float dG = col(0) + sBeta[r] * t2 * sGam[r] + erow - ecol - ddec;
-      const float dbeta = col(2) + sGam[r] * t2 + red[kRedRowB + r] + red[kRedRowB + 64 + r];
+      const float dbeta = col(2) + sGam[r] * t2 + red[kRedRowB + r] + red[kRedRowB + 64 + r] +
+                          red[kRedRowB + 128 + r] + red[kRedRowB + 192 + r];
       float dd = ddec;
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, o);
@@ -689,14 +736,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_local_tc_kernel(const Probl
   if (ok && n_heads == 0 && !tc_wait(ctl, 0, 0)) ok = false;  // [Q; K] K^T done before TMEM is freed
   tc_fence_after();
   if (__syncthreads_or(!ok) == 0 && !skip) {
-    float x[32], y[32];
-    ld32(tmem + tDQ + 32 * h, x);
-    ld32(tmem + tDK + 32 * h, y);
+    float x[16], y[16];
+    ld16f(tmem + tDQ + 16 * h, x);
+    ld16f(tmem + tDK + 16 * h, y);
     __nv_bfloat16* dqo = reinterpret_cast<__nv_bfloat16*>(b.dq);
     __nv_bfloat16* dko = reinterpret_cast<__nv_bfloat16*>(b.dk);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int r = 32 * h + i;
+    for (int i = 0; i < 16; ++i) {
+      const int r = 16 * h + i;
       if (r < cv) {
         const size_t o = ((size_t)(t0 + r) * p.h_qk + iq) * kDim + d;
         dqo[o] = __float2bfloat16_rn(x[i]);
@@ -1122,7 +1169,7 @@ cudaError_t launch_bwd_local_tc(const Problem& p, const BwdArgs& b, cudaStream_t
       cudaFuncSetAttribute(bwd_local_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
   if (attr != cudaSuccess) return attr;
   const unsigned grid = (unsigned)p.n_chunks_total * (unsigned)p.h_qk;
-  return launch_kernel(bwd_local_tc_kernel, dim3(grid), dim3(kTcThreads), kTcSmem, st, true, p, b);
+  return launch_kernel(bwd_local_tc_kernel, dim3(grid), dim3(kLocThreads), kTcSmem, st, true, p, b);
 }
 
 }  // namespace gdn
