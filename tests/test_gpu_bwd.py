@@ -182,3 +182,13 @@ def test_bwd_after_training_forward(mode):
     assert excess <= 2e-2
     err = np.abs(hT.double().cpu().numpy() - rh).max() / np.sqrt(np.mean(rh * rh))
     assert err < 2e-2
+
+
+def test_bwd_empty_sequence_and_uneven_gqa():
+    """A varlen batch with an empty sequence (its dh0 is its dh_T), and h_v not a
+    multiple of h_qk (q/k head 0 feeds value heads 0 and 1, heads 1 and 2 one each)."""
+    w = make_inputs(cu_seqlens=[0, 130, 130, 330], h_qk=3, h_v=4, seed=43, with_h0=True)
+    d_out, dhT = make_output_grads(w, seed=44)
+    got, _ = run_bwd(w, d_out, dhT, mode="auto")
+    check(got, ref_grads(w, d_out, dhT))
+    assert torch.equal(got["dh0"][1].cpu(), dhT[1])

@@ -82,3 +82,47 @@ def test_timeout_path_reports_and_the_next_call_is_clean(mode):
     f = util.to64
     ro, rh = oracle.recurrence(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0))
     assert util.parity_bf16(o, ro)[0] <= util.TOL_BF16 and util.parity_f32(h, rh) <= util.TOL_STATE
+
+
+def test_bwd_values_past_fp16_range_are_reported():
+    """An upstream gradient far beyond the fp16 range of the backward's operands."""
+    from gated_deltanet_linear_fwd_gb300 import gdn_bwd_workspace_bytes, gdn_chunk_bwd
+    w = make_inputs(300, h_qk=1, h_v=2, seed=5, with_h0=True)
+    d = w.to("cuda:0")
+    plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, mode="off")
+    ws = torch.empty(gdn_bwd_workspace_bytes(plan), dtype=torch.uint8, device="cuda:0")
+    d_out = (torch.randn(w.v.shape, generator=torch.Generator().manual_seed(6)) * 1e6).to(torch.bfloat16)
+    gdn_chunk_bwd(d.q, d.k, d.v, d.g, d.beta, d_out.to("cuda:0"), d.h0, None, plan=plan, workspace=ws)
+    assert gdn_get_device_status(ws) == (DEVICE_CHECK, FP16_RANGE)
+
+
+@pytest.mark.parametrize("mode", ["off", "exact"])
+def test_bwd_timeout_path_reports_and_the_next_call_is_clean(mode):
+    """The backward's recompute meets the same hook: the status reads (5, 6), the
+    backward's kernels do no work (the gradients stay NaN), and the next ordinary
+    backward on the same workspace gives the same gradients as a fresh one."""
+    from gated_deltanet_linear_fwd_gb300 import gdn_bwd_workspace_bytes, gdn_chunk_bwd
+    from gated_deltanet_linear_fwd_gb300.inputs import make_output_grads
+    w = make_inputs(700, h_qk=2, h_v=4, seed=7, with_h0=True)
+    d = w.to("cuda:0")
+    d_out, dhT = (x.to("cuda:0") for x in make_output_grads(w, seed=8))
+    plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v, mode=mode, lambda_=0.5)
+    ws = torch.empty(gdn_bwd_workspace_bytes(plan), dtype=torch.uint8, device="cuda:0")
+    nan = float("nan")
+    grads = (torch.full_like(d.q, nan), torch.full_like(d.k, nan), torch.full_like(d.v, nan),
+             torch.full_like(d.g, nan), torch.full_like(d.beta, nan),
+             torch.full((1, w.h_v, 128, 128), nan, device="cuda:0"))
+    try:
+        gdn_debug_stall_ns(20000)
+        gdn_chunk_bwd(d.q, d.k, d.v, d.g, d.beta, d_out, d.h0, dhT, plan=plan, grads=grads, workspace=ws)
+        status = gdn_get_device_status(ws)
+    finally:
+        gdn_debug_stall_ns(0)
+    assert status == (5, 6), describe_device_status(*status)
+    assert all(torch.isnan(x).all() for x in grads)
+    again = gdn_chunk_bwd(d.q, d.k, d.v, d.g, d.beta, d_out, d.h0, dhT, plan=plan, workspace=ws)
+    assert gdn_get_device_status(ws) == (0, 0)
+    ws2 = torch.empty_like(ws)
+    fresh = gdn_chunk_bwd(d.q, d.k, d.v, d.g, d.beta, d_out, d.h0, dhT, plan=plan, workspace=ws2)
+    for x, y in zip(again, fresh):
+        assert torch.equal(x, y)
