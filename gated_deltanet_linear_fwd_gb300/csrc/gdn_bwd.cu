@@ -62,8 +62,8 @@ constexpr uint32_t sS = 32768;       // S = H^T: 128 (d_v) x 128 (d_k), panels d
 constexpr uint32_t sD = 65536;       // D: 128 (d_k) x 128 (d_v), panels d_v 0-63 | 64-127
 constexpr uint32_t sWt = 98304;      // -W^T record tile 128 (d_k) x 64; then dV'^T 128 (d_v) x 64
 constexpr uint32_t sUt = 114688;     // U^T record tile 128 (d_v) x 64; then Y_U^T 128 (d_v) x 64
-constexpr uint32_t sP = 131072;      // P record tile 64 x 64; then dL_raw; then dKK
-constexpr uint32_t sPG = 139264;     // dP * Gam 64 x 64 (also rows 0-63 of the padded dL product)
+constexpr uint32_t sP = 131072;      // P record tile 64 x 64; then dL_raw
+constexpr uint32_t sPG = 139264;     // dP * Gam 64 x 64 (also rows 0-63 of the padded dL product); then dKK
 constexpr uint32_t sAT = 147456;     // A^T 64 x 64
 constexpr uint32_t sDOV = 155648;    // [dO d0-63 | dV' d0-63 | dO d64-127 | dV' d64-127], 64 rows each
 constexpr uint32_t sVpT = 188416;    // V'^T 128 (d_v) x 64; then dv staged (64 rows x 128 bf16, row-major)
@@ -89,9 +89,9 @@ constexpr uint32_t tC = 320;    // D^T K^T, then [dP_raw; dL_raw]
 constexpr uint32_t tE = 384;    // H dO^T, then A^T dL_raw (lanes 64-127)
 constexpr uint32_t tF = 448;    // D V'^T
 
-// Loads of a head's tiles, in three groups issued as their slots free up in
-// the head before: A (D, -W^T) once phase 2's products are done, B (S, U^T,
-// A^T, V) once phase 3's are, C (P) once phase 4's are.
+// Loads of a head's tiles, in groups issued as their slots free up in the
+// head before: A (D, -W^T) once phase 2's products are done, B (S, U^T, A^T,
+// V) and C (P) once phase 3's are.
 struct TcCtl {
   uint64_t loadA, loadB, loadC, ph[5];
   uint32_t tmem;
@@ -361,12 +361,11 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
   for (int j = j_lo; ok && j < j_hi; ++j, ++n_heads) {
     const uint32_t par = (uint32_t)(n_heads & 1);
     // the previous head's last products (they read K and dKK) are done
-    if (n_heads > 0 && !tc_wait(ctl, 4, par ^ 1u)) ok = false;
     if (__syncthreads_or(!ok)) {
       ok = false;
       break;
     }
-    if (tid == 0 && n_heads > 0) issue_C(j);  // (A, B and dO came during the head before)
+    // (this head's tiles came during the head before)
     if (tid < 64) {  // G = inclusive cumulative gate (two warps, as the forward)
       const int r = tid;
       float x = g_cur;
@@ -515,6 +514,8 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
       mma_commit(&ctl->ph[2]);
     }
     if (!tc_wait(ctl, 2, par)) ok = false;
+    // the previous head's last products (they read dKK and update dk^T) are done
+    if (n_heads > 0 && !tc_wait(ctl, 4, par ^ 1u)) ok = false;
     if (tid == 0 && ok && j + 1 < j_hi) issue_A(j + 1);  // D and -W^T are read
     tc_fence_after();
     if (ok) {
@@ -604,7 +605,10 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
       mma_commit(&ctl->ph[3]);
     }
     if (!tc_wait(ctl, 3, par)) ok = false;
-    if (tid == 0 && ok && j + 1 < j_hi) issue_B(j + 1);  // S, U^T / Y_U^T, A^T and V are read
+    if (tid == 0 && ok && j + 1 < j_hi) {  // S, U^T / Y_U^T, A^T, V and P / dL_raw are read
+      issue_B(j + 1);
+      issue_C(j + 1);
+    }
     tc_fence_after();
     if (ok) {  // dv of this head from its staging rows: 16-byte stores, whole rows per warp
       uint8_t* dvo = reinterpret_cast<uint8_t*>(b.dv);
@@ -656,7 +660,7 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
           x[i] = dL * br * gam;
           y[i] = br * xb;
         }
-        row_f16_16(s0 + sP, r, 16 * h, x, mx);
+        row_f16_16(s0 + sPG, r, 16 * h, x, mx);
         red[kRedRowB + h * 64 + r] = rowb;
         red[kRedRowE + (1 * 4 + h) * 64 + r] = rowe;
         {
@@ -680,10 +684,10 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
       const uint32_t t = ctl->tmem;
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(t + tDK, dmn_(s0 + sQK + 8192, ks, 16384), dk_(s0 + sP, ks, 8192), idesc_f16(128, 64, true, false), 1);
+        mma_bf16(t + tDK, dmn_(s0 + sQK + 8192, ks, 16384), dk_(s0 + sPG, ks, 8192), idesc_f16(128, 64, true, false), 1);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(t + tDK, dmn_(s0 + sQK + 8192, ks, 16384), dmn_(s0 + sP, ks, 8192), idesc_f16(128, 64, true, true), 1);
+        mma_bf16(t + tDK, dmn_(s0 + sQK + 8192, ks, 16384), dmn_(s0 + sPG, ks, 8192), idesc_f16(128, 64, true, true), 1);
       mma_commit(&ctl->ph[4]);
     }
     // ---- the gates: dG, dg = its reverse cumulative sum, dbeta ----
