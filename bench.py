@@ -17,7 +17,7 @@ The line also carries, for every workload: its time and roofline fraction;
 the AutoCP modes of the varlen workload (time and distance from exact); the
 decode step over a batch of 256 states; the fp32 path's time on the headline
 workload; the host planning time; the backward (`backward`: gdn_chunk_bwd with
-its forward recompute on the headline and three other workloads, per-kernel
+its forward recompute on the headline and four other workloads, per-kernel
 times, its roofline fraction, a training step of gdn_chunk_fwd(for_backward)
 then gdn_chunk_bwd(reuse_forward), and its gradients against the float64
 oracle's); and, from the CPU-baseline leg (which runs the float64 oracle on
@@ -261,7 +261,7 @@ def time_gpu(name, steps, warmup, device, cp="auto", lambda_=0.0, trace=True, to
 
 
 VARLEN = "varlen4_T348160_h2x8"
-BWD_SWEEP = ["T32768_h8x24_h0", "T32768_h16x16", "batch8_T4096_h8x32"]
+BWD_SWEEP = ["T32768_h8x24_h0", "T32768_h16x16", "varlen4_T348160_h2x8", "batch8_T4096_h8x32"]
 
 
 def time_bwd(name, steps, warmup, device, cp="auto"):

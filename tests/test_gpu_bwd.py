@@ -142,7 +142,8 @@ def test_bwd_strong_decay():
     check(got, ref_grads(w, d_out, dhT))
 
 
-@pytest.mark.parametrize("name,heads", [("T32768_h2x8", None), ("T32768_h16x16", [0, 7, 15])])
+@pytest.mark.parametrize("name,heads", [("T32768_h2x8", None), ("T32768_h16x16", [0, 7, 15]),
+                                        ("varlen4_T348160_h2x8", [1, 6])])
 def test_bwd_full_size(name, heads):
     """The benchmark's 1 x 32768 workloads at full size, in the bench's launch
     configuration (auto plan); every head, or a sample of heads, element by element."""
