@@ -305,15 +305,19 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
     bulk_load(sm + sD, b.dstate + slot * 32768u, 32768u, &ctl->loadA);
     bulk_load(sm + sWt, p.wy + slot * kRecBytes + kRecWn, 16384u, &ctl->loadA);
   };
-  auto issue_B = [&](int jj) {
+  auto issue_B = [&](int jj) {  // (the 32 lanes of one warp: V's rows spread over them)
     const size_t slot = (size_t)gc * p.h_v + jj;
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(&ctl->loadB, 32768u + 16384u + 8192u + (uint32_t)cv * 256u);
-    bulk_load(sm + sS, p.hchunk + slot * 32768u, 32768u, &ctl->loadB);
-    bulk_load(sm + sUt, p.wy + slot * kRecBytes + kRecU, 16384u, &ctl->loadB);
-    bulk_load(sm + sAT, p.wyA + slot * 8192u, 8192u, &ctl->loadB);
+    if (lane == 0) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&ctl->loadB, 32768u + 16384u + 8192u + (uint32_t)cv * 256u);
+      bulk_load(sm + sS, p.hchunk + slot * 32768u, 32768u, &ctl->loadB);
+      bulk_load(sm + sUt, p.wy + slot * kRecBytes + kRecU, 16384u, &ctl->loadB);
+      bulk_load(sm + sAT, p.wyA + slot * 8192u, 8192u, &ctl->loadB);
+    }
+    __syncwarp();
     const uint8_t* vrow = reinterpret_cast<const uint8_t*>(p.v) + ((size_t)t0 * p.h_v + jj) * (kDim * 2);
-    for (int r = 0; r < cv; ++r) bulk_load(sm + sV + r * 256, vrow + (size_t)r * p.h_v * (kDim * 2), 256u, &ctl->loadB);
+    for (int r = lane; r < cv; r += 32)
+      bulk_load(sm + sV + r * 256, vrow + (size_t)r * p.h_v * (kDim * 2), 256u, &ctl->loadB);
   };
   auto issue_C = [&](int jj) {
     const size_t slot = (size_t)gc * p.h_v + jj;
@@ -345,10 +349,10 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
       mma_commit(&ctl->ph[0]);
       if (j_lo < j_hi) {
         issue_A(j_lo);
-        issue_B(j_lo);
         issue_C(j_lo);
       }
     }
+    if (warp == 0 && j_lo < j_hi) issue_B(j_lo);
     if (j_lo < j_hi)
       rows_to_f16<kLocThreads>(s0 + sDOV, 16384, reinterpret_cast<const __nv_bfloat16*>(b.dout), t0, p.h_v, j_lo, cv, mx);
   }
@@ -518,6 +522,19 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
     if (n_heads > 0 && !tc_wait(ctl, 4, par ^ 1u)) ok = false;
     if (tid == 0 && ok && j + 1 < j_hi) issue_A(j + 1);  // D and -W^T are read
     tc_fence_after();
+    // the next head's dO rows, in flight during this epilogue (its slots were last
+    // read by phase 2; they are written at the epilogue's end)
+    const bool next_do = ok && j + 1 < j_hi;
+    uint4 dro[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    if (next_do) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int idx = tid + u * kLocThreads, r = idx >> 4, c = idx & 15;
+        if (r < cv)
+          dro[u] = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(b.dout) +
+                                                   ((size_t)(t0 + r) * p.h_v + j + 1) * kDim + c * 8);
+      }
+    }
     if (ok) {
       float x[16], y[16];
       // D V'^T (lane = d_k): dk^T += dec_r (.); ddec_r = <K_r, .>
@@ -578,6 +595,22 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
         row_f16_16(s0 + sP, d - 64, 16 * h, x, mx);
       }
     }
+    if (next_do) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int idx = tid + u * kLocThreads, r = idx >> 4, c = idx & 15;
+        const uint32_t w[4] = {dro[u].x, dro[u].y, dro[u].z, dro[u].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+          mx = absmax_nan(absmax_nan(mx, f.x), f.y);
+          o[e] = pack_f16x2(f.x, f.y);
+        }
+        st_shared_v4(s0 + sDOV + (uint32_t)(c >> 3) * 16384u + sw128_offset((uint32_t)r, (uint32_t)(c & 7)), o[0], o[1],
+                     o[2], o[3]);
+      }
+    }
     fence_proxy_async_smem();
     tmem_st_wait();
     tc_fence_before();
@@ -605,9 +638,11 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
       mma_commit(&ctl->ph[3]);
     }
     if (!tc_wait(ctl, 3, par)) ok = false;
-    if (tid == 0 && ok && j + 1 < j_hi) {  // S, U^T / Y_U^T, A^T, V and P / dL_raw are read
-      issue_B(j + 1);
-      issue_C(j + 1);
+    if (warp == 0) {  // S, U^T / Y_U^T, A^T, V and P / dL_raw are read
+      if (__all_sync(0xffffffffu, ok) && j + 1 < j_hi) {
+        issue_B(j + 1);
+        if (lane == 0) issue_C(j + 1);
+      }
     }
     tc_fence_after();
     if (ok) {  // dv of this head from its staging rows: 16-byte stores, whole rows per warp
@@ -669,8 +704,6 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
       }
       }
     }
-    if (ok && j + 1 < j_hi)  // the next head's dO (its slots were last read by phase 2)
-      rows_to_f16<kLocThreads>(s0 + sDOV, 16384, reinterpret_cast<const __nv_bfloat16*>(b.dout), t0, p.h_v, j + 1, cv, mx);
     fence_proxy_async_smem();
     tmem_st_wait();
     tc_fence_before();
