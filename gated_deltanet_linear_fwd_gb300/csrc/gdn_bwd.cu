@@ -202,6 +202,42 @@ __device__ __forceinline__ void rows_to_f16(uint32_t base, uint32_t pstride, con
   }
 }
 
+// rows_to_f16 in two halves: the loads (into registers, before the row
+// scales are known), then the conversion and the stores.
+template <int NT>
+struct RowLoads {
+  uint4 raw[64 * 16 / NT];
+};
+template <int NT>
+__device__ __forceinline__ void rows_load(RowLoads<NT>& L, const __nv_bfloat16* src, int64_t t0, int heads, int head,
+                                          int cv) {
+#pragma unroll
+  for (int u = 0; u < 64 * 16 / NT; ++u) {
+    const int idx = threadIdx.x + u * NT, r = idx >> 4, c = idx & 15;
+    L.raw[u] = make_uint4(0, 0, 0, 0);
+    if (r < cv) L.raw[u] = *reinterpret_cast<const uint4*>(src + ((size_t)(t0 + r) * heads + head) * kDim + c * 8);
+  }
+}
+template <int NT>
+__device__ __forceinline__ void rows_store(const RowLoads<NT>& L, uint32_t base, uint32_t pstride, float& mx,
+                                           const float* row_scale = nullptr) {
+#pragma unroll
+  for (int u = 0; u < 64 * 16 / NT; ++u) {
+    const int idx = threadIdx.x + u * NT, r = idx >> 4, c = idx & 15;
+    const uint32_t w[4] = {L.raw[u].x, L.raw[u].y, L.raw[u].z, L.raw[u].w};
+    const float sc = row_scale ? row_scale[r] : 1.f;
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+      mx = absmax_nan(absmax_nan(mx, f.x * sc), f.y * sc);
+      o[e] = pack_f16x2(f.x * sc, f.y * sc);
+    }
+    st_shared_v4(base + (uint32_t)(c >> 3) * pstride + sw128_offset((uint32_t)r, (uint32_t)(c & 7)), o[0], o[1],
+                 o[2], o[3]);
+  }
+}
+
 // 16-column variants (the chunk-local kernel: 16 warps, a thread takes 16 of a
 // 64-column accumulator)
 __device__ __forceinline__ void ld16f(uint32_t taddr, float (&x)[16]) {
@@ -870,14 +906,19 @@ __global__ void __launch_bounds__(kTcThreads, 2) bwd_pre_tc_kernel(const Problem
       bulk_load(sm + pP, rec + kRecP, 8192u, &ctl->load);
       bulk_load(sm + pGam, rec + kRecGam, 512u, &ctl->load);
     }
-    rows_to_f16(s0 + pDo, 8192, reinterpret_cast<const __nv_bfloat16*>(b.dout), t0, p.h_v, j, cv, mx);
+    // all row loads in flight before the gates (which scale K and Q) have landed
+    RowLoads<kTcThreads> lo_do, lo_k, lo_q;
+    rows_load(lo_do, reinterpret_cast<const __nv_bfloat16*>(b.dout), t0, p.h_v, j, cv);
+    rows_load(lo_k, reinterpret_cast<const __nv_bfloat16*>(p.k), t0, p.h_qk, iq, cv);
+    rows_load(lo_q, reinterpret_cast<const __nv_bfloat16*>(p.q), t0, p.h_qk, iq, cv);
+    rows_store(lo_do, s0 + pDo, 8192, mx);
     if (!mbar_wait(&ctl->load, 0, kWaitLimitNs)) atomicCAS(&ctl->abort, 0, kDetTmaWait);
     float* gam = reinterpret_cast<float*>(sm + pGam);
     float* qsc = reinterpret_cast<float*>(sm + pSc);
     if (tid < 64) qsc[tid] = p.scale * gam[tid];
     __syncthreads();
-    rows_to_f16(s0 + pKt, 8192, reinterpret_cast<const __nv_bfloat16*>(p.k), t0, p.h_qk, iq, cv, mx, gam + 64);
-    rows_to_f16(s0 + pQg, 8192, reinterpret_cast<const __nv_bfloat16*>(p.q), t0, p.h_qk, iq, cv, mx, qsc);
+    rows_store(lo_k, s0 + pKt, 8192, mx, gam + 64);
+    rows_store(lo_q, s0 + pQg, 8192, mx, qsc);
     fence_proxy_async_smem();
     tc_fence_before();
     if (__syncthreads_or(ctl->abort != 0)) ok = false;
