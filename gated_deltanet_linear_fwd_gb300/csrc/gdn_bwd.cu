@@ -19,11 +19,13 @@
 // in TMEM; fp16 operands in the forward's 128-byte-swizzled tile image; tiles
 // by bulk copies on mbarriers; every wait bounded):
 //   bwd_pre_tc_kernel    per (chunk, value head): T' and E (chunk-parallel)
-//   bwd_chain_tc_kernel  per segment and value head: D over the chunks in
-//                        reverse, in fp32 registers; every chunk's D (fp16) and
-//                        dh0; context parallel like the forward (a transition
-//                        and a local pass per segment, the combine run
-//                        backwards, then the final pass)
+//   bwd_chain2_tc_kernel, the combine run backwards, bwd_chain_tc_kernel:
+//                        the state gradient D over each segment's chunks in
+//                        reverse, in fp32 registers, context parallel like the
+//                        forward (per segment the transition and the local
+//                        offset together, the segments' end-state gradients by
+//                        the combine, then the final pass writing every chunk's
+//                        D (fp16) and dh0)
 //   bwd_local_tc_kernel  per (chunk, q/k head), over the value heads of the
 //                        group: every other gradient
 //
@@ -1002,17 +1004,15 @@ __global__ void __launch_bounds__(kTcThreads, 2) bwd_pre_tc_kernel(const Problem
 }
 
 // ------------------------------------------------------------ state-gradient chain
-// One chain over one segment's chunks in reverse, D <- gamma_C D + E_c + T'_c D_c:
-// the product on tcgen05 (M = d_k out, N = d_v, K = d_k in; A = T' from the
-// record, B = D's fp16 copy in shared memory), D itself in fp32 registers
-// (thread: TMEM lane = row d_k, 64 of the 128 columns).  Modes: final
-// (PREP = false; grid x = segment) writes every chunk's D
-// before its step (fp16 tile image) and dh0 for a sequence's first segment,
-// starting from dh_T (a sequence's last segment) or the combine's D_end;
-// preprocessing (PREP; grid x = 2 segment + chain) runs the transition (chain
-// 0, from I, no E) or the local offset (chain 1, from 0) and stores it
-// transposed for the combine.  Without context parallelism every sequence is
-// one segment.
+// The final pass over one segment's chunks in reverse, D <- gamma_C D + E_c +
+// T'_c D_c: the product on tcgen05 (M = d_k out, N = d_v, K = d_k in; A = T'
+// from the record, B = D's fp16 copy in shared memory), D itself in fp32
+// registers (thread: TMEM lane = row d_k, 64 of the 128 columns).  D starts
+// from dh_T (a sequence's last segment) or from the combine's D_end; every
+// chunk's D is written before its step (fp16 tile image), and dh0 for a
+// sequence's first segment.  Without context parallelism every sequence is
+// one segment.  (The segments' transitions and local offsets for the combine
+// come from bwd_chain2_tc_kernel.)
 constexpr uint32_t cT = 0;          // 2 x T' (32 KB): rows d_k out, panels d_k in 0-63 | 64-127
 constexpr uint32_t cE = 65536;      // 2 x E (32 KB): rows d_k, panels d_v
 constexpr uint32_t cD = 131072;     // D's fp16 copy: rows d_k (K), panels d_v 0-63 | 64-127
@@ -1027,7 +1027,6 @@ struct ChCtl {
   int ok;
 };
 
-template <bool PREP>
 __global__ void __launch_bounds__(kTcThreads, 1) bwd_chain_tc_kernel(const Problem p, const BwdArgs b) {
   uint8_t* sm = tc_smem_base();
   const uint32_t s0 = smem_u32(sm);
@@ -1036,8 +1035,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_chain_tc_kernel(const Probl
   const int q = warp & 3, h = warp >> 2, k = 32 * q + lane;
   const uint32_t lane_base = (uint32_t)(32 * q) << 16;
   const int j = blockIdx.y;
-  const int chain = PREP ? (int)(blockIdx.x & 1) : 0;
-  const int seg = PREP ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int seg = (int)blockIdx.x;
   if (warp == 1) {
     SegInfo si;
     const bool okseg = locate_segment(p, seg, si);
@@ -1067,20 +1065,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_chain_tc_kernel(const Probl
   bool run = !failed && ctl->ok;
   if (!failed && !ctl->ok && tid == 0) report(p.status, kDevCheck, kDetSegMismatch);
   const bool last_seg = si.s == si.n_seg - 1;
-  if (PREP && run) {
-    if (si.s == 0) run = false;                                   // segment 0 is taken by the final pass
-    if (chain == 0 && last_seg && b.dhT == nullptr) run = false;  // its transition would act on zero
-  }
   const int c0 = run ? seq_first_chunk(p, si.n) + si.cb : 0, nc = run ? si.ce - si.cb : 0;
   const size_t mat = (size_t)kDim * kDim;
   const size_t head_seg = ((size_t)(si.seg_base + si.s) * p.h_v + j) * mat;
-  const bool with_e = !(PREP && chain == 0);
   float D[64];  // row k, columns 64 h .. 64 h + 63
   if (run) {
-    if (PREP) {
-#pragma unroll
-      for (int e = 0; e < 64; ++e) D[e] = (chain == 0 && 64 * h + e == k) ? 1.f : 0.f;
-    } else if (!last_seg) {  // D_end of this segment from the combine, stored transposed (rows d_v)
+    if (!last_seg) {  // D_end of this segment from the combine, stored transposed (rows d_v)
       const float* src = p.Sstart + head_seg;
 #pragma unroll
       for (int e = 0; e < 64; ++e) D[e] = src[(size_t)(64 * h + e) * kDim + k];
@@ -1122,15 +1112,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_chain_tc_kernel(const Probl
     const size_t slot = ((size_t)c * p.h_v + j) * 32768u;
     const uint32_t buf = (uint32_t)(it & 1) * 32768u;
     fence_proxy_async_smem();
-    mbar_arrive_expect_tx(&ctl->load[it & 1], with_e ? 65536u : 32768u);
+    mbar_arrive_expect_tx(&ctl->load[it & 1], 65536u);
     bulk_load(sm + cT + buf, b.tmat + slot, 32768u, &ctl->load[it & 1]);
-    if (with_e) bulk_load(sm + cE + buf, b.emat + slot, 32768u, &ctl->load[it & 1]);
+    bulk_load(sm + cE + buf, b.emat + slot, 32768u, &ctl->load[it & 1]);
   };
   if (tid == 0 && nc > 0) issue(0);
   bool ok = true;
   if (nc > 0) {
     // the first step's D_c is D itself
-    store_d(PREP ? nullptr : b.dstate + ((size_t)(c0 + nc - 1) * p.h_v + j) * 32768u + (size_t)h * 16384u);
+    store_d(b.dstate + ((size_t)(c0 + nc - 1) * p.h_v + j) * 32768u + (size_t)h * 16384u);
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -1150,7 +1140,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_chain_tc_kernel(const Probl
       if (it + 1 < nc) issue(it + 1);  // buffer (it + 1) & 1 was last read in step it - 1
     }
     // E_c and gamma_C D while the product runs
-    if (with_e) {
+    {
       const uint32_t epanel = s0 + cE + buf + (uint32_t)h * 16384u;
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8) {
@@ -1163,9 +1153,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_chain_tc_kernel(const Probl
           D[8 * c8 + 2 * e + 1] = fmaf(gC, D[8 * c8 + 2 * e + 1], f.y);
         }
       }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 64; ++e) D[e] *= gC;
     }
     if (!wait_phase(&ctl->mma, (uint32_t)(it & 1), &ctl->abort, 210)) ok = false;
     tc_fence_after();
@@ -1184,17 +1171,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_chain_tc_kernel(const Probl
     }
     // D_{c-1} for the next step (and as the previous chunk's record)
     if (it + 1 < nc)
-      store_d(PREP ? nullptr : b.dstate + ((size_t)(c - 1) * p.h_v + j) * 32768u + (size_t)h * 16384u);
+      store_d(b.dstate + ((size_t)(c - 1) * p.h_v + j) * 32768u + (size_t)h * 16384u);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
   }
   if (run && ok && !ctl->abort) {
-    if (PREP) {  // transposed (rows d_v, or the transition's column index) for the combine
-      float* dst = (chain == 0 ? p.R : p.Sloc) + head_seg;
-#pragma unroll
-      for (int e = 0; e < 64; ++e) dst[(size_t)(64 * h + e) * kDim + k] = D[e];
-    } else if (si.s == 0 && b.dh0) {
+    if (si.s == 0 && b.dh0) {
       float4* dst = reinterpret_cast<float4*>(b.dh0 + ((size_t)si.n * p.h_v + j) * mat + (size_t)k * kDim + 64 * h);
 #pragma unroll
       for (int e = 0; e < 16; ++e) dst[e] = make_float4(D[4 * e], D[4 * e + 1], D[4 * e + 2], D[4 * e + 3]);
@@ -1216,6 +1199,175 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_chain_tc_kernel(const Probl
   }
 }
 
+
+// The preprocessing's two chains of one segment in one CTA: the transition X0
+// (from I, no E) and the local offset X1 (from 0, with E) share each step's T'
+// as the A operand of one N = 256 product T' [X0 | X1]; both stay in fp32
+// registers.  Stored transposed for the combine (p.R, p.Sloc).
+constexpr uint32_t c2T = 0;          // 2 x T' (32 KB)
+constexpr uint32_t c2E = 65536;      // 2 x E (32 KB)
+constexpr uint32_t c2D = 131072;     // [X0 | X1] fp16: four 64-column panels of 128 rows (16 KB each)
+constexpr uint32_t c2Ctl = 196608;
+constexpr uint32_t kChain2Smem = c2Ctl + 128 + 1024;
+
+__global__ void __launch_bounds__(kTcThreads, 1) bwd_chain2_tc_kernel(const Problem p, const BwdArgs b) {
+  uint8_t* sm = tc_smem_base();
+  const uint32_t s0 = smem_u32(sm);
+  ChCtl* ctl = reinterpret_cast<ChCtl*>(sm + c2Ctl);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q = warp & 3, h = warp >> 2, k = 32 * q + lane;
+  const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+  const int j = blockIdx.y, seg = blockIdx.x;
+  if (warp == 1) {
+    SegInfo si;
+    const bool okseg = locate_segment(p, seg, si);
+    if (lane == 0) {
+      ctl->si = si;
+      ctl->ok = okseg;
+    }
+  }
+  if (tid == 0) {
+    mbar_init(&ctl->load[0], 1);
+    mbar_init(&ctl->load[1], 1);
+    mbar_init(&ctl->mma, 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&ctl->tmem, 256);
+    tmem_relinquish();
+  }
+  grid_dependency_wait();
+  grid_launch_dependents();
+  tc_fence_before();
+  const bool failed = __syncthreads_or(tid == 0 && earlier_failure(p.status));
+  tc_fence_after();
+  const uint32_t tm = ctl->tmem;
+  const SegInfo si = ctl->si;
+  bool run = !failed && ctl->ok;
+  if (!failed && !ctl->ok && tid == 0) report(p.status, kDevCheck, kDetSegMismatch);
+  if (run && si.s == 0) run = false;  // segment 0 is taken by the final pass
+  const int c0 = run ? seq_first_chunk(p, si.n) + si.cb : 0, nc = run ? si.ce - si.cb : 0;
+  const size_t mat = (size_t)kDim * kDim;
+  const size_t head_seg = ((size_t)(si.seg_base + si.s) * p.h_v + j) * mat;
+  float X0[64], X1[64];  // row k, columns 64 h .. 64 h + 63
+#pragma unroll
+  for (int e = 0; e < 64; ++e) {
+    X0[e] = (64 * h + e == k) ? 1.f : 0.f;
+    X1[e] = 0.f;
+  }
+  float mx = 0.f;
+  auto store_x = [&]() {  // both as row k of their tiles (panels h and 2 + h)
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      const float* X = m ? X1 : X0;
+      const uint32_t panel = s0 + c2D + (uint32_t)(2 * m + h) * 16384u;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          mx = absmax_nan(absmax_nan(mx, X[8 * c + 2 * e]), X[8 * c + 2 * e + 1]);
+          w[e] = pack_f16x2(X[8 * c + 2 * e], X[8 * c + 2 * e + 1]);
+        }
+        st_shared_v4(panel + sw128_offset((uint32_t)k, (uint32_t)c), w[0], w[1], w[2], w[3]);
+      }
+    }
+  };
+  auto issue = [&](int it) {  // T' and E of step it into buffer it & 1 (one thread)
+    const int c = c0 + nc - 1 - it;
+    const size_t slot = ((size_t)c * p.h_v + j) * 32768u;
+    const uint32_t buf = (uint32_t)(it & 1) * 32768u;
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(&ctl->load[it & 1], 65536u);
+    bulk_load(sm + c2T + buf, b.tmat + slot, 32768u, &ctl->load[it & 1]);
+    bulk_load(sm + c2E + buf, b.emat + slot, 32768u, &ctl->load[it & 1]);
+  };
+  if (tid == 0 && nc > 0) issue(0);
+  if (nc > 0) {
+    store_x();
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  bool ok = true;
+  for (int it = 0; it < nc && ok; ++it) {
+    const int c = c0 + nc - 1 - it;
+    const uint32_t buf = (uint32_t)(it & 1) * 32768u;
+    const float gC = reinterpret_cast<const float*>(p.wy + ((size_t)c * p.h_v + j) * kRecBytes + kRecGam)[63];
+    if (!mbar_wait(&ctl->load[it & 1], (uint32_t)((it >> 1) & 1), kWaitLimitNs)) atomicCAS(&ctl->abort, 0, kDetTmaWait);
+    if (tid == 0 && !ctl->abort) {  // T'_c [X0 | X1]
+      tc_fence_after();
+      const uint32_t id = idesc_f16(128, 256, false, true);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_bf16(tm, dk_(s0 + c2T + buf, ks, 16384), dmn_(s0 + c2D, ks, 16384), id, ks > 0);
+      mma_commit(&ctl->mma);
+      if (it + 1 < nc) issue(it + 1);  // buffer (it + 1) & 1 was last read in step it - 1
+    }
+    {  // gamma_C X0, gamma_C X1 + E_c while the product runs
+      const uint32_t epanel = s0 + c2E + buf + (uint32_t)h * 16384u;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        const uint4 w = lds_u32x4(epanel + sw128_offset((uint32_t)k, (uint32_t)c8));
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[e]));
+          X1[8 * c8 + 2 * e] = fmaf(gC, X1[8 * c8 + 2 * e], f.x);
+          X1[8 * c8 + 2 * e + 1] = fmaf(gC, X1[8 * c8 + 2 * e + 1], f.y);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 64; ++e) X0[e] *= gC;
+    }
+    if (!wait_phase(&ctl->mma, (uint32_t)(it & 1), &ctl->abort, 211)) ok = false;
+    tc_fence_after();
+    if (__syncthreads_or(!ok || ctl->abort)) {
+      ok = false;
+      break;
+    }
+    {
+      float a[32];
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        float* X = m ? X1 : X0;
+        ld32(tm + lane_base + 128 * m + 64 * h, a);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) X[e] += a[e];
+        ld32(tm + lane_base + 128 * m + 64 * h + 32, a);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) X[32 + e] += a[e];
+      }
+    }
+    if (it + 1 < nc) store_x();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+  }
+  if (run && ok && !ctl->abort) {  // transposed (rows d_v, or the transition's column index) for the combine
+#pragma unroll
+    for (int e = 0; e < 64; ++e) {
+      p.R[head_seg + (size_t)(64 * h + e) * kDim + k] = X0[e];
+      p.Sloc[head_seg + (size_t)(64 * h + e) * kDim + k] = X1[e];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (ctl->abort || !ok) {
+    if (tid == 0) report(p.status, kDevTimeout, ctl->abort ? ctl->abort : kDetMmaWait);
+    const uint64_t t_start = globaltimer_ns();
+    while (globaltimer_ns() - t_start < 2000000ull) {
+    }
+    __syncthreads();
+  }
+  if (!(mx < 65504.f)) report(p.status, kDevCheck, kDetFp16Range);
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tm, 256);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_pre_tc(const Problem& p, const BwdArgs& b, cudaStream_t st) {
@@ -1227,19 +1379,17 @@ cudaError_t launch_bwd_pre_tc(const Problem& p, const BwdArgs& b, cudaStream_t s
 }
 
 cudaError_t launch_bwd_chain_tc(const Problem& p, const BwdArgs& b, bool prep, cudaStream_t st) {
-  static const cudaError_t attr = [] {
-    cudaError_t e = cudaFuncSetAttribute(bwd_chain_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kChainSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(bwd_chain_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kChainSmem);
-    return e;
-  }();
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(bwd_chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kChainSmem);
   if (attr != cudaSuccess) return attr;
-  if (prep)
-    return launch_kernel(bwd_chain_tc_kernel<true>, dim3(2 * p.n_seg_total, p.h_v), dim3(kTcThreads), kChainSmem, st,
-                         true, p, b);
-  return launch_kernel(bwd_chain_tc_kernel<false>, dim3(p.n_seg_total, p.h_v), dim3(kTcThreads), kChainSmem, st, true,
-                       p, b);
+  if (prep) {
+    static const cudaError_t a2 =
+        cudaFuncSetAttribute(bwd_chain2_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kChain2Smem);
+    if (a2 != cudaSuccess) return a2;
+    return launch_kernel(bwd_chain2_tc_kernel, dim3(p.n_seg_total, p.h_v), dim3(kTcThreads), kChain2Smem, st, true, p,
+                         b);
+  }
+  return launch_kernel(bwd_chain_tc_kernel, dim3(p.n_seg_total, p.h_v), dim3(kTcThreads), kChainSmem, st, true, p, b);
 }
 
 cudaError_t launch_bwd_local_tc(const Problem& p, const BwdArgs& b, cudaStream_t st) {
