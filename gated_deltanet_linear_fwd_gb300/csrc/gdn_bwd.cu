@@ -249,6 +249,18 @@ __device__ __forceinline__ void ld16f(uint32_t taddr, float (&x)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(a[i]);
 }
+// Two 16-column loads in flight together, one wait.
+__device__ __forceinline__ void ld16f2(uint32_t ta, float (&x)[16], uint32_t tb, float (&y)[16]) {
+  uint32_t a[16], b[16];
+  tmem_ld16(ta, a);
+  tmem_ld16(tb, b);
+  tmem_ld_wait(a, b);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    x[i] = __uint_as_float(a[i]);
+    y[i] = __uint_as_float(b[i]);
+  }
+}
 __device__ __forceinline__ void st16f(uint32_t taddr, const float (&x)[16]) {
   uint32_t a[16];
 #pragma unroll
@@ -507,8 +519,7 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
       row_f16_16(s0 + sVpT, d, 16 * h, x, mx);
       // dV'^T = scale dO^T P + diag(dec) applied to D^T K^T's columns; also dV' (rows r)
       float y[16];
-      ld16f(tmem + tB + 16 * h, x);
-      ld16f(tmem + tC + 16 * h, y);
+      ld16f2(tmem + tB + 16 * h, x, tmem + tC + 16 * h, y);
       const uint32_t dvp = s0 + sDOV + 8192u + (uint32_t)(d >> 6) * 16384u;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -517,8 +528,7 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
       }
       row_f16_16(s0 + sWt, d, 16 * h, x, mx);
       // H dO^T (lane = d_k): dq^T += scale gamma_r (H dO^T); dgamma_r gamma_r = <Q_r, that>
-      ld16f(tmem + tE + 16 * h, x);
-      ld16f(tmem + tDQ + 16 * h, y);
+      ld16f2(tmem + tE + 16 * h, x, tmem + tDQ + 16 * h, y);
       const uint32_t qpanel = s0 + sQK + (uint32_t)(d >> 6) * 16384u;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -576,8 +586,7 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
     if (ok) {
       float x[16], y[16];
       // D V'^T (lane = d_k): dk^T += dec_r (.); ddec_r = <K_r, .>
-      ld16f(tmem + tF + 16 * h, x);
-      ld16f(tmem + tDK + 16 * h, y);
+      ld16f2(tmem + tF + 16 * h, x, tmem + tDK + 16 * h, y);
       const uint32_t kpanel = s0 + sQK + 8192u + (uint32_t)(d >> 6) * 16384u;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -608,10 +617,12 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
         if (lane < 16) red[kRedCol + (2 * 4 + q) * 64 + 16 * h + lane] = cs_;
       }
       // [dP_raw; dL_raw] (lane = token r, or 64 + r)
-      ld16f(tmem + tC + 16 * h, x);
+      if (q < 2)
+        ld16f2(tmem + tC + 16 * h, x, tmem + tQK + 16 * h, y);
+      else
+        ld16f(tmem + tC + 16 * h, x);
       if (q < 2) {
         const int r = d;
-        ld16f(tmem + tQK + 16 * h, y);
         float rowsum = 0.f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -701,8 +712,7 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
     if (ok) {
       float x[16], y[16];
       // Y_W^T = -H Y_U^T (lane = d_k): dk^T += beta_r gamma_r Y_W^T; t2_r = <Y_W_r, K_r>
-      ld16f(tmem + tB + 16 * h, x);
-      ld16f(tmem + tDK + 16 * h, y);
+      ld16f2(tmem + tB + 16 * h, x, tmem + tDK + 16 * h, y);
       const uint32_t kpanel = s0 + sQK + 8192u + (uint32_t)(d >> 6) * 16384u;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -718,8 +728,7 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
       // dL = -A^T dL_raw, s < r (lanes 64-127: r = lane - 64)
       if (q >= 2) {
         const int r = d - 64;
-        ld16f(tmem + tE + 16 * h, x);
-        ld16f(tmem + tQK + 16 * h, y);  // K K^T [r][s]
+        ld16f2(tmem + tE + 16 * h, x, tmem + tQK + 16 * h, y);  // y: K K^T [r][s]
         const float br = sBeta[r];
         float rowb = 0.f, rowe = 0.f;
 #pragma unroll
