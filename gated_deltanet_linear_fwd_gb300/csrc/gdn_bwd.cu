@@ -76,7 +76,8 @@ constexpr int kRedCol = 0;           //   [4 kinds][4 lane quarters][64]: dgamma
 constexpr int kRedRowE = 1024;       //   [2 sources][4 column groups][64]: row sums of dGam * Gam
 constexpr int kRedColE = 1536;       //   [4 quarters][64]: column sums of dGam * Gam
 constexpr int kRedRowB = 1792;       //   [4 column groups][64]: sum_s dL KK Gam
-constexpr int kRedMisc = 2048;       //   [16]: scan carries, <D, H> per warp
+constexpr int kRedMisc = 2048;       //   [20]: scan carry, gate sums, <D, H> per warp for two heads
+constexpr int kGate0 = 256;          // warps 8 and 9 (threads 256-319) scan the gates and reduce dg, dbeta
 constexpr uint32_t sCtl = sRed + 8448;
 constexpr uint32_t kTcSmem = sCtl + 256 + 1024;
 static_assert(kTcSmem <= 232448, "shared memory over the per-block limit");
@@ -406,12 +407,59 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
     if (j_lo < j_hi)
       rows_to_f16<kLocThreads>(s0 + sDOV, 16384, reinterpret_cast<const __nv_bfloat16*>(b.dout), t0, p.h_v, j_lo, cv, mx);
   }
-  // this head's g and beta for threads 0-63 (prefetched during the head before)
+  // The gate threads: row gr of the chunk.  They hold this head's g and beta (prefetched
+  // during the head before); a head's dg and dbeta are reduced while the next head's
+  // first products run.
+  const bool gate_thr = tid >= kGate0 && tid < kGate0 + 64;
+  const int gr = tid - kGate0, gw = warp - (kGate0 >> 5);
   float g_cur = 0.f, b_cur = 0.f;
-  if (tid < 64 && j_lo < j_hi && tid < cv) {
-    g_cur = p.g[(size_t)(t0 + tid) * p.h_v + j_lo];
-    b_cur = p.beta[(size_t)(t0 + tid) * p.h_v + j_lo];
+  if (gate_thr && j_lo < j_hi && gr < cv) {
+    g_cur = p.g[(size_t)(t0 + gr) * p.h_v + j_lo];
+    b_cur = p.beta[(size_t)(t0 + gr) * p.h_v + j_lo];
   }
+  // dG, dg = its reverse cumulative sum, and dbeta of head jj from the epilogues' sums
+  // and that head's gates in sBeta, sGam, sDec; dh_par selects its <D, H> slots.
+  auto gates = [&](int jj, uint32_t dh_par) {
+    const int r = gr;
+    auto col = [&](int kind) {
+      return red[kRedCol + (kind * 4 + 0) * 64 + r] + red[kRedCol + (kind * 4 + 1) * 64 + r] +
+             red[kRedCol + (kind * 4 + 2) * 64 + r] + red[kRedCol + (kind * 4 + 3) * 64 + r];
+    };
+    const float t2 = col(3);
+    float erow = 0.f;
+#pragma unroll
+    for (int g8 = 0; g8 < 8; ++g8) erow += red[kRedRowE + g8 * 64 + r];
+    const float ecol = red[kRedColE + r] + red[kRedColE + 64 + r] + red[kRedColE + 128 + r] +
+                       red[kRedColE + 192 + r];
+    const float ddec = col(1) * sDec[r];
+    float dG = col(0) + sBeta[r] * t2 * sGam[r] + erow - ecol - ddec;
+    const float dbeta = col(2) + sGam[r] * t2 + red[kRedRowB + r] + red[kRedRowB + 64 + r] +
+                        red[kRedRowB + 128 + r] + red[kRedRowB + 192 + r];
+    float dd = ddec;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, o);
+    if (lane == 0) red[kRedMisc + 1 + gw] = dd;
+    named_bar_sync(1, 64);
+    if (r == 63) {
+      float dgc = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) dgc += red[kRedMisc + 4 + 8 * dh_par + w];
+      dG += dgc * sGam[63] + red[kRedMisc + 1] + red[kRedMisc + 2];
+    }
+    float x = dG;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_down_sync(0xffffffffu, x, o);
+      if (lane + o < 32) x += y;
+    }
+    if (gw == 1 && lane == 0) red[kRedMisc + 3] = x;
+    named_bar_sync(1, 64);
+    if (gw == 0) x += red[kRedMisc + 3];
+    if (r < cv) {
+      b.dg[(size_t)(t0 + r) * p.h_v + jj] = x;
+      b.dbeta[(size_t)(t0 + r) * p.h_v + jj] = dbeta;
+    }
+  };
   for (int j = j_lo; ok && j < j_hi; ++j, ++n_heads) {
     const uint32_t par = (uint32_t)(n_heads & 1);
     // the previous head's last products (they read K and dKK) are done
@@ -420,23 +468,6 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
       break;
     }
     // (this head's tiles came during the head before)
-    if (tid < 64) {  // G = inclusive cumulative gate (two warps, as the forward)
-      const int r = tid;
-      float x = g_cur;
-      sBeta[r] = b_cur;
-#pragma unroll
-      for (int dd = 1; dd < 32; dd <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, x, dd);
-        if (lane >= dd) x += y;
-      }
-      if (lane == 31 && warp == 0) red[kRedMisc] = x;
-      named_bar_sync(1, 64);
-      if (warp == 1) x += red[kRedMisc];
-      sG[r] = x;
-      sGam[r] = __expf(x);
-      named_bar_sync(1, 64);
-      sDec[r] = __expf(sG[63] - x);
-    }
     const bool landed = mbar_wait(&ctl->loadA, par, kWaitLimitNs) && mbar_wait(&ctl->loadB, par, kWaitLimitNs) &&
                         mbar_wait(&ctl->loadC, par, kWaitLimitNs);
     if (!landed) atomicCAS(&ctl->abort, 0, kDetTmaWait);
@@ -465,6 +496,26 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
       for (int ks = 0; ks < 8; ++ks)
         mma_bf16(t + tE, dmn_(s0 + sS, ks, 16384), dk_(s0 + sDOV, ks, 16384), idesc_f16(128, 64, true, false), ks > 0);
       mma_commit(&ctl->ph[1]);
+    }
+    // the previous head's dg and dbeta while these products run
+    if (gate_thr) {
+      if (n_heads > 0) gates(j - 1, par ^ 1u);
+      // then this head's G = inclusive cumulative gate (two warps, as the forward)
+      const int r = gr;
+      float x = g_cur;
+      sBeta[r] = b_cur;
+#pragma unroll
+      for (int dd = 1; dd < 32; dd <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, dd);
+        if (lane >= dd) x += y;
+      }
+      if (lane == 31 && gw == 0) red[kRedMisc] = x;
+      named_bar_sync(1, 64);
+      if (gw == 1) x += red[kRedMisc];
+      sG[r] = x;
+      sGam[r] = __expf(x);
+      named_bar_sync(1, 64);
+      sDec[r] = __expf(sG[63] - x);
     }
     // <D, H> = sum D[k][v] S[v][k] (the gradient of gamma_C) while the products run:
     // thread = one 8 x 8 block, rows k0.. of D against rows v0.. of S
@@ -497,10 +548,12 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
       }
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) dh += __shfl_xor_sync(0xffffffffu, dh, o);
-      if (lane == 0) red[kRedMisc + 4 + warp] = dh;
+      if (lane == 0) red[kRedMisc + 4 + 8 * par + warp] = dh;
     }
     if (!tc_wait(ctl, 1, par)) ok = false;
     tc_fence_after();
+    // the previous head's sums are read and this head's gates written before the epilogue
+    __syncthreads();
     if (ok) {
       // V'^T = U^T - S W^T (lane = d_v)
       float x[16];
@@ -705,9 +758,9 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
     }
     // the next head's g and beta, in flight during this epilogue
     float g_next = 0.f, b_next = 0.f;
-    if (tid < 64 && j + 1 < j_hi && tid < cv) {
-      g_next = p.g[(size_t)(t0 + tid) * p.h_v + j + 1];
-      b_next = p.beta[(size_t)(t0 + tid) * p.h_v + j + 1];
+    if (gate_thr && j + 1 < j_hi && gr < cv) {
+      g_next = p.g[(size_t)(t0 + gr) * p.h_v + j + 1];
+      b_next = p.beta[(size_t)(t0 + gr) * p.h_v + j + 1];
     }
     if (ok) {
       float x[16], y[16];
@@ -770,51 +823,11 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
         mma_bf16(t + tDK, dmn_(s0 + sQK + 8192, ks, 16384), dmn_(s0 + sPG, ks, 8192), idesc_f16(128, 64, true, true), 1);
       mma_commit(&ctl->ph[4]);
     }
-    // ---- the gates: dG, dg = its reverse cumulative sum, dbeta ----
-    if (tid < 64) {
-      const int r = tid;
-      auto col = [&](int kind) {
-        return red[kRedCol + (kind * 4 + 0) * 64 + r] + red[kRedCol + (kind * 4 + 1) * 64 + r] +
-               red[kRedCol + (kind * 4 + 2) * 64 + r] + red[kRedCol + (kind * 4 + 3) * 64 + r];
-      };
-      const float t2 = col(3);
-      float erow = 0.f;
-#pragma unroll
-      for (int g8 = 0; g8 < 8; ++g8) erow += red[kRedRowE + g8 * 64 + r];
-      const float ecol = red[kRedColE + r] + red[kRedColE + 64 + r] + red[kRedColE + 128 + r] +
-                         red[kRedColE + 192 + r];
-      const float ddec = col(1) * sDec[r];
-      float dG = col(0) + sBeta[r] * t2 * sGam[r] + erow - ecol - ddec;
-      const float dbeta = col(2) + sGam[r] * t2 + red[kRedRowB + r] + red[kRedRowB + 64 + r] +
-                          red[kRedRowB + 128 + r] + red[kRedRowB + 192 + r];
-      float dd = ddec;
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, o);
-      if (lane == 0) red[kRedMisc + 1 + warp] = dd;
-      named_bar_sync(1, 64);
-      if (r == 63) {
-        float dgc = 0.f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) dgc += red[kRedMisc + 4 + w];
-        dG += dgc * sGam[63] + red[kRedMisc + 1] + red[kRedMisc + 2];
-      }
-      float x = dG;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_down_sync(0xffffffffu, x, o);
-        if (lane + o < 32) x += y;
-      }
-      if (warp == 1 && lane == 0) red[kRedMisc + 3] = x;
-      named_bar_sync(1, 64);
-      if (warp == 0) x += red[kRedMisc + 3];
-      if (r < cv) {
-        b.dg[(size_t)(t0 + r) * p.h_v + j] = x;
-        b.dbeta[(size_t)(t0 + r) * p.h_v + j] = dbeta;
-      }
-    }
     g_cur = g_next;
     b_cur = b_next;
   }
+  // the last head's dg and dbeta
+  if (ok && n_heads > 0 && gate_thr) gates(j_lo + n_heads - 1, (uint32_t)((n_heads - 1) & 1));
   // ---- dq, dk (bf16) from their accumulators ----
   if (ok && n_heads > 0 && !tc_wait(ctl, 4, (uint32_t)((n_heads - 1) & 1))) ok = false;
   if (ok && n_heads == 0 && !tc_wait(ctl, 0, 0)) ok = false;  // [Q; K] K^T done before TMEM is freed
