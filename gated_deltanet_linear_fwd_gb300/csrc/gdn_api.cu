@@ -83,6 +83,7 @@ gdn_status device_setup(int* dev_out) {
   if ((e = wy_kernel_setup()) != cudaSuccess) return cuda_fail(e);
   if ((e = combine_kernel_setup()) != cudaSuccess) return cuda_fail(e);
   if ((e = f32_kernel_setup()) != cudaSuccess) return cuda_fail(e);
+  if ((e = bwd_kernel_setup()) != cudaSuccess) return cuda_fail(e);
   int sms = 0;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return cuda_fail(e);
   g_sm_count[dev] = sms;

@@ -1392,32 +1392,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_chain2_tc_kernel(const Prob
 
 }  // namespace
 
+cudaError_t bwd_kernel_setup() {
+  cudaError_t e = cudaFuncSetAttribute(bwd_pre_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPreTcSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bwd_chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kChainSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bwd_chain2_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kChain2Smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bwd_local_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+  return e;
+}
+
 cudaError_t launch_bwd_pre_tc(const Problem& p, const BwdArgs& b, cudaStream_t st) {
-  static const cudaError_t attr =
-      cudaFuncSetAttribute(bwd_pre_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPreTcSmem);
-  if (attr != cudaSuccess) return attr;
   const unsigned grid = (unsigned)p.n_chunks_total * (unsigned)p.h_v;
   return launch_kernel(bwd_pre_tc_kernel, dim3(grid), dim3(kTcThreads), kPreTcSmem, st, true, p, b);
 }
 
 cudaError_t launch_bwd_chain_tc(const Problem& p, const BwdArgs& b, bool prep, cudaStream_t st) {
-  static const cudaError_t attr =
-      cudaFuncSetAttribute(bwd_chain_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kChainSmem);
-  if (attr != cudaSuccess) return attr;
-  if (prep) {
-    static const cudaError_t a2 =
-        cudaFuncSetAttribute(bwd_chain2_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kChain2Smem);
-    if (a2 != cudaSuccess) return a2;
+  if (prep)
     return launch_kernel(bwd_chain2_tc_kernel, dim3(p.n_seg_total, p.h_v), dim3(kTcThreads), kChain2Smem, st, true, p,
                          b);
-  }
   return launch_kernel(bwd_chain_tc_kernel, dim3(p.n_seg_total, p.h_v), dim3(kTcThreads), kChainSmem, st, true, p, b);
 }
 
 cudaError_t launch_bwd_local_tc(const Problem& p, const BwdArgs& b, cudaStream_t st) {
-  static const cudaError_t attr =
-      cudaFuncSetAttribute(bwd_local_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
-  if (attr != cudaSuccess) return attr;
   const unsigned grid = (unsigned)p.n_chunks_total * (unsigned)p.h_qk;
   return launch_kernel(bwd_local_tc_kernel, dim3(grid), dim3(kLocThreads), kTcSmem, st, true, p, b);
 }

@@ -333,6 +333,7 @@ cudaError_t launch_scan_out(const Problem& p, const CUtensorMap& mq, const CUten
 cudaError_t launch_recurrence_f32(const Problem& p, cudaStream_t st, bool dependent);
 cudaError_t launch_f32_prep(const Problem& p, cudaStream_t st);
 cudaError_t f32_kernel_setup();
+cudaError_t bwd_kernel_setup();
 cudaError_t launch_decode(const DecodeArgs& a, bool f32, cudaStream_t st);
 cudaError_t launch_combine_bwd(const Problem& p, int sm_count, cudaStream_t st);
 cudaError_t launch_bwd_local_tc(const Problem& p, const BwdArgs& b, cudaStream_t st);
