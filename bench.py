@@ -15,7 +15,9 @@ rank's time is used.
 
 The line also carries, for every workload: its time and roofline fraction;
 the AutoCP modes of the varlen workload (time and distance from exact); the
-decode step over a batch of 256 states; the fp32 path's time on the headline
+decode step over a batch of 256 states; `graphs`: microseconds per call of the
+tiny forward and of the decode step, called eagerly and replayed from a CUDA
+graph that captured 20 calls; the fp32 path's time on the headline
 workload; the host planning time; the backward (`backward`: gdn_chunk_bwd with
 its forward recompute on the headline and four other workloads, per-kernel
 times, its roofline fraction, a training step of gdn_chunk_fwd(for_backward)
@@ -24,7 +26,7 @@ oracle's); and, from the CPU-baseline leg (which runs the float64 oracle on
 the host cores anyway), the raw max|diff|/RMS of o and of the final state
 against the oracle and the excess over bf16's half-ulp store rounding.
 
-`--only NAME` times just one case (a workload name, `decode`, `f32`, `bwd` or
+`--only NAME` times just one case (a workload name, `decode`, `graphs`, `f32`, `bwd` or
 `bwd:NAME`) and prints a short line: the entry point of the ncu captures
 under profiles/.
 
@@ -696,10 +698,68 @@ def run_reference(args, world, rank):
     return 0
 
 
+def time_graphs(device, calls=200, per_graph=20):
+    """Back-to-back calls, eager (each one a Python call through the C ABI) against the
+    same calls captured once as a CUDA graph and replayed: microseconds per call for
+    the tiny forward (T = 512, h 2/4) and for the decode step over 256 states, where
+    launching, not the kernels, can set the pace."""
+    from gated_deltanet_linear_fwd_gb300 import gdn_chunk_fwd, gdn_cp_plan, gdn_decode_step
+    from gated_deltanet_linear_fwd_gb300.inputs import make_inputs, workload
+    stream = torch.cuda.current_stream(device)
+
+    def per_call_us(fn, n):
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(n):
+            fn()
+        s1.record(stream)
+        s1.synchronize()
+        return s0.elapsed_time(s1) * 1e3 / n
+
+    def measure(call):
+        for _ in range(5):
+            call()
+        torch.cuda.synchronize(device)
+        eager = per_call_us(call, calls)
+        side = torch.cuda.Stream(device)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            call()
+        stream.wait_stream(side)
+        torch.cuda.synchronize(device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(per_graph):
+                call()
+        graph.replay()
+        torch.cuda.synchronize(device)
+        replayed = per_call_us(graph.replay, calls // per_graph) / per_graph
+        return {"eager_us_per_call": eager, "graph_us_per_call": replayed}
+
+    res = {}
+    w = workload("tiny_T512_h2x4")
+    d = w.to(device)
+    plan = gdn_cp_plan(T=w.T, h_qk=w.h_qk, h_v=w.h_v)
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
+    out = torch.empty_like(d.v)
+    hT = torch.empty(1, w.h_v, D, D, dtype=torch.float32, device=device)
+    res["forward_tiny_T512_h2x4"] = measure(
+        lambda: gdn_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, None, None, plan=plan, out=out, final_state=hT, workspace=ws))
+    B, hqk, hv = DECODE_BATCH
+    w = make_inputs(cu_seqlens=list(range(B + 1)), h_qk=hqk, h_v=hv, seed=5, with_h0=True)
+    d = w.to(device)
+    state = d.h0.clone()
+    out = torch.empty_like(d.v)
+    res[f"decode_B{B}_h{hqk}x{hv}"] = measure(lambda: gdn_decode_step(d.q, d.k, d.v, d.g, d.beta, state, out=out))
+    return res
+
+
 def run_only(args, device, hbm):
     """One case alone, few steps: the command the ncu captures run."""
     if args.only == "decode":
         r = time_decode(args.steps, args.warmup, device, hbm)
+    elif args.only == "graphs":
+        r = time_graphs(device)
     elif args.only == "f32":
         r = time_f32(HEADLINE, args.steps, args.warmup, device)
     elif args.only.startswith("bwd"):
@@ -801,6 +861,7 @@ def main(argv=None):
         line["sweep"] = sweep
     if not args.no_sweep and rank == 0:
         line["decode"] = time_decode(max(20, args.steps // 10), 5, device, hbm)
+        line["graphs"] = time_graphs(device)
         f32 = time_f32(HEADLINE, max(5, args.steps // 50), 3, device)
         f32["vs_bf16_path"] = f32["ms"] / ms
         line["f32"] = f32
