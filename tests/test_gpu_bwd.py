@@ -142,6 +142,45 @@ def test_bwd_strong_decay():
     check(got, ref_grads(w, d_out, dhT))
 
 
+@pytest.mark.parametrize("kind", ["beta_zero", "no_decay"])
+@pytest.mark.parametrize("mode", ["off", "exact"])
+def test_bwd_degenerate_gates(kind, mode):
+    """beta = 0 (the state only decays: k and v never reach o or h_T, so dk and dv are
+    exactly zero) and g = 0 (alpha = 1, no decay at all), with and without context
+    parallelism (lambda 0.5: several segments)."""
+    w = make_inputs(cu_seqlens=[0, 200, 517], h_qk=1, h_v=2, seed=36, with_h0=True,
+                    g_kind="zero" if kind == "no_decay" else "mix")
+    if kind == "beta_zero":
+        w.beta = torch.zeros_like(w.beta)
+    d_out, dhT = make_output_grads(w, seed=37)
+    d = w.to(DEV)
+    plan = gdn_cp_plan(T=w.T, h_qk=1, h_v=2, cu_seqlens=w.cu_seqlens, mode=mode, lambda_=0.5)
+    if mode == "exact":
+        assert plan.n_seg_total > 2
+    ws = torch.empty(gdn_bwd_workspace_bytes(plan), dtype=torch.uint8, device=DEV)
+    grads = gdn_chunk_bwd(d.q, d.k, d.v, d.g, d.beta, d_out.to(DEV), d.h0, dhT.to(DEV), d.cu_seqlens, plan=plan,
+                          workspace=ws)
+    assert gdn_get_device_status(ws) == (0, 0)
+    got = dict(zip(NAMES, grads))
+    if kind == "beta_zero":
+        assert float(got["dk"].abs().max()) == 0.0 and float(got["dv"].abs().max()) == 0.0
+        check(got, ref_grads(w, d_out, dhT), names=("dq", "dg", "dbeta", "dh0"))
+    else:
+        check(got, ref_grads(w, d_out, dhT))
+
+
+def test_bwd_million_token_sequence():
+    """One sequence of 2^20 tokens (16384 chunks), the largest the forward's tests
+    run, in the bench's launch configuration (auto plan); every gradient of both
+    value heads element by element against the float64 chunk-level oracle."""
+    w = make_inputs(1 << 20, h_qk=1, h_v=2, seed=38, with_h0=True)
+    d_out, dhT = make_output_grads(w, seed=39)
+    got, plan = run_bwd(w, d_out, dhT, mode="auto")
+    assert plan.n_seg_total > 16
+    worst = check(got, ref_grads(w, d_out, dhT))
+    print(f"bwd 2^20 tokens, {plan.n_seg_total} segments: {worst}")
+
+
 @pytest.mark.parametrize("name,heads", [("T32768_h2x8", None), ("T32768_h16x16", [0, 7, 15]),
                                         ("varlen4_T348160_h2x8", [1, 6])])
 def test_bwd_full_size(name, heads):
