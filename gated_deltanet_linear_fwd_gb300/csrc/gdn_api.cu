@@ -400,9 +400,9 @@ gdn_status gdn_cp_plan(const gdn_dims* dims, const int32_t* cu, const gdn_cp_opt
   return GDN_OK;
 }
 
-// The forward.  For the backward (hchunk != null) a context-parallel plan
-// combines every head exactly, and the WY and output-scan kernels also write
-// A^T (wyA) and every chunk's start state (hchunk); *p_out receives the
+// The forward.  For the backward (hchunk != null) the WY and output-scan
+// kernels also write A^T (wyA) and every output chunk's start state (hchunk),
+// in the plan's own mode; *p_out receives the
 // problem the kernels run with.  launch = false: only that problem (the
 // backward of a forward that already ran with the same arguments).
 static gdn_status forward_impl(const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -458,7 +458,6 @@ static gdn_status forward_impl(const void* q, const void* k, const void* v, cons
   // runs without the preprocessing and the combine
   const bool cp = plan->mode != GDN_CP_OFF && plan->n_seg_total > plan->n_seqs;
   if (!cp) p.plan_mode = kModeOff;
-  if (hchunk && cp) p.plan_mode = kModeExact;
   p.wyA = wyA;
   p.hchunk = hchunk;
   p.lambda_q8 = plan->lambda_q8;
@@ -650,6 +649,10 @@ gdn_status gdn_chunk_bwd(const void* q, const void* k, const void* v, const floa
   if (st != GDN_OK) return st;
   int dev = 0;
   if ((st = device_setup(&dev)) != GDN_OK) return st;
+  // The forward above kept the chunk states of the plan's own mode (a warmup
+  // restart only where its acceptance rule allows one); the state gradient's
+  // chain is always combined exactly.
+  if (p.plan_mode != kModeOff) p.plan_mode = kModeExact;
   BwdArgs b;
   b.dout = d_out;
   b.dhT = d_final_state;

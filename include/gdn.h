@@ -310,9 +310,12 @@ gdn_status gdn_bwd_workspace_bytes(const gdn_cp_plan_t* plan, size_t* bytes);
  * writes its gradient with respect to q, k, v, g, beta and initial_state.
  * Asynchronous on `stream`.  The forward is recomputed inside the call unless
  * reuse_forward = 1, in which case `workspace` must hold the state a
- * gdn_chunk_fwd_train with the same inputs and plan left there; a
- * context-parallel plan combines every head exactly (no warmup restarts), so
- * the gradients are those of the exact forward.  bf16 only.
+ * gdn_chunk_fwd_train with the same inputs and plan left there.  The chunk
+ * states the gradients use are the forward's in the plan's mode (with
+ * GDN_CP_AUTO, a warmup restart where the forward's acceptance rule allows
+ * one, so they agree with the exact states within its tolerance; GDN_CP_EXACT
+ * gives the exact forward's gradients); the state gradient's own chain is
+ * always combined exactly.  bf16 only.
  *   q, k, v, g, beta, initial_state, cu_seqlens_dev, dims, plan: as gdn_chunk_fwd.
  *   d_out         : device, [B*T, h_v, d_v] bf16.
  *   d_final_state : device, [n_seqs, h_v, d_k, d_v] fp32, or NULL (zero).
@@ -338,10 +341,10 @@ gdn_status gdn_chunk_bwd(const void* q, const void* k, const void* v, const floa
  * gdn_chunk_fwd_train -- gdn_chunk_fwd that also keeps, in `workspace`, what
  * gdn_chunk_bwd needs (no counterpart on the FlashQLA pages: the training
  * pattern of forward then backward).  Same arguments and outputs as
- * gdn_chunk_fwd; the workspace must hold gdn_bwd_workspace_bytes(plan).  A
- * context-parallel plan combines every head exactly here (no warmup
- * restarts), so o and final_state are the exact forward's; besides them the
- * call writes A^T and every chunk's start state into the workspace.  A later
+ * gdn_chunk_fwd; the workspace must hold gdn_bwd_workspace_bytes(plan).  It
+ * runs in the plan's mode like gdn_chunk_fwd (o and final_state are the same);
+ * besides them the call writes A^T and every chunk's start state into the
+ * workspace.  A later
  * gdn_chunk_bwd with the same inputs, plan and workspace and reuse_forward = 1
  * then skips its own recompute; nothing checks that the inputs are the same.
  * bf16 only.  Errors: as gdn_chunk_fwd, UNSUPPORTED for fp32.

@@ -201,7 +201,7 @@ def test_bwd_full_size(name, heads):
 def test_bwd_after_training_forward(mode):
     """gdn_chunk_fwd(for_backward=True) then gdn_chunk_bwd(reuse_forward=True): the same
     gradients, bit for bit, as a backward that recomputes the forward itself, and the
-    training forward's o and final state are the exact forward's (parity with the oracle)."""
+    training forward's o and final state meet the forward's bar against the oracle."""
     from gated_deltanet_linear_fwd_gb300 import gdn_chunk_fwd
     import oracle
     w = make_inputs(cu_seqlens=[0, 300, 700], h_qk=2, h_v=4, seed=41, with_h0=True)
