@@ -654,16 +654,19 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
       // Y_U^T (lane = d_v): dv = beta_r Y_U; t1_r = <Y_U_r, V_r>; Y_U^T into the U^T slot
       ld16f(tmem + tA + 16 * h, x);
       row_f16_16(s0 + sUt, d, 16 * h, x, mx);
+      {  // dv staged in the V'^T slot (read by phase 2), stored in epilogue 3
+        const unsigned short* vcol = reinterpret_cast<const unsigned short*>(sm + sV) + d;
+        unsigned short* dvcol = reinterpret_cast<unsigned short*>(sm + sVpT) + d;
+        unsigned short vb[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {  // dv staged in the V'^T slot (read by phase 2), stored in epilogue 3
-        const int r = 16 * h + i;
-        const __nv_bfloat16 dvb = __float2bfloat16_rn(sBeta[r] * x[i]);
-        asm volatile("st.shared.u16 [%0], %1;" ::"r"(s0 + sVpT + (uint32_t)(r * 256 + 2 * d)),
-                     "h"(*reinterpret_cast<const unsigned short*>(&dvb))
-                     : "memory");
-        unsigned short vb;
-        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(vb) : "r"(s0 + sV + (uint32_t)(r * 256 + 2 * d)) : "memory");
-        x[i] = r < cv ? x[i] * __uint_as_float((uint32_t)vb << 16) : 0.f;
+        for (int i = 0; i < 16; ++i) vb[i] = vcol[(16 * h + i) * 128];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int r = 16 * h + i;
+          const __nv_bfloat16 dvb = __float2bfloat16_rn(sBeta[r] * x[i]);
+          dvcol[r * 128] = *reinterpret_cast<const unsigned short*>(&dvb);
+          x[i] = r < cv ? x[i] * __uint_as_float((uint32_t)vb[i] << 16) : 0.f;
+        }
       }
       {
         const float cs_ = butterfly16(x);
