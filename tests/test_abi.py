@@ -145,6 +145,49 @@ def test_chunk_fwd_rejects_before_device_work(lib):
     assert f(A, A, A, A, A, None, None, A, None, ctypes.byref(dims3), ctypes.byref(p), A, ws, None) == 2
 
 
+def test_bwd_workspace_layout(lib):
+    """The backward's workspace: the forward's (rounded up to 1 KB), then per (chunk,
+    value head) A^T (8 KB) and four 32 KB tiles, then a bf16 copy of o."""
+    st, p = plan(lib, 32768, h_v=8, mode=3)
+    assert st == 0
+    n = ctypes.c_size_t(0)
+    assert lib.gdn_bwd_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == 0
+    base = -(-p.workspace_bytes // 1024) * 1024
+    o_end = base + 512 * 8 * (8192 + 4 * 32768) + 32768 * 8 * 128 * 2
+    assert n.value == -(-o_end // 256) * 256
+    assert lib.gdn_bwd_workspace_bytes(None, ctypes.byref(n)) == 1
+    st, pf = plan(lib, 32768, h_v=8, mode=3, dtype=1)  # the fp32 path has no backward
+    assert st == 0 and lib.gdn_bwd_workspace_bytes(ctypes.byref(pf), ctypes.byref(n)) == 2
+
+
+def test_chunk_bwd_rejects_before_device_work(lib):
+    from gated_deltanet_linear_fwd_gb300 import _lib as L
+    st, p = plan(lib, 128, h_qk=1, h_v=1, mode=0)
+    assert st == 0
+    n = ctypes.c_size_t(0)
+    assert lib.gdn_bwd_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == 0
+    ws = n.value
+    dims = L.gdn_dims(1, 128, 1, 1, 128, 128, 1, 0.0, 0)
+    A = ctypes.c_void_p(0x100000)  # never dereferenced: every case fails a host check first
+    U = ctypes.c_void_p(0x100008)  # not 16-byte aligned
+    f = lib.gdn_chunk_bwd
+    D, P = ctypes.byref(dims), ctypes.byref(p)
+
+    def call(d_out=A, dq=A, dims_=D, plan_=P, work=A, nbytes=ws, dhT=None):
+        return f(A, A, A, A, A, None, None, d_out, dhT, dq, A, A, A, A, None, dims_, plan_, work, nbytes, 0, None)
+
+    assert call(dims_=None) == 1 and call(plan_=None) == 1       # null dims / plan
+    assert call(nbytes=ws - 1) == 6 and call(work=None) == 6     # workspace missing or too small
+    assert call(d_out=None) == 1 and call(dq=None) == 1          # null upstream gradient / output
+    assert call(d_out=U) == 3 and call(dhT=U) == 3               # misaligned
+    dims32 = L.gdn_dims(1, 128, 1, 1, 128, 128, 1, 0.0, 1)
+    assert call(dims_=ctypes.byref(dims32)) == 2                 # fp32: no backward
+    g = lib.gdn_chunk_fwd_train
+    assert g(A, A, A, A, A, None, None, A, None, D, None, A, ws, None) == 1
+    assert g(A, A, A, A, A, None, None, A, None, D, P, A, ws - 1, None) == 6
+    assert g(A, A, A, A, A, None, None, A, None, ctypes.byref(dims32), P, A, ws, None) == 2
+
+
 def test_decode_step_rejects_before_device_work(lib):
     from gated_deltanet_linear_fwd_gb300 import _lib as L
     A = ctypes.c_void_p(0x100000)  # never dereferenced: every case fails a host check first
