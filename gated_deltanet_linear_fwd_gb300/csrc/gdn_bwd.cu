@@ -14,8 +14,9 @@
 //   Y_U  = A^T dV',  dV = diag(beta) Y_U,  dL = -A^T dV' V'^T (strict lower)
 //   dKK  = dL * beta * Gam;  the gates through dG and a reverse cumulative sum.
 //
-// Three kernels after a forward pass that also leaves each chunk's start state
-// and A^T (fp16), all on the 5th-generation tensor cores (tcgen05, accumulators
+// Three stages (five kernels) after a forward pass, in the plan's mode, that
+// also leaves each chunk's start state and A^T (fp16), all on the 5th-generation
+// tensor cores (tcgen05, accumulators
 // in TMEM; fp16 operands in the forward's 128-byte-swizzled tile image; tiles
 // by bulk copies on mbarriers; every wait bounded):
 //   bwd_pre_tc_kernel    per (chunk, value head): T' and E (chunk-parallel)
