@@ -1091,7 +1091,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_chain_tc_kernel(const Probl
   bool run = !failed && ctl->ok;
   if (!failed && !ctl->ok && tid == 0) report(p.status, kDevCheck, kDetSegMismatch);
   const bool last_seg = si.s == si.n_seg - 1;
-  const int c0 = run ? seq_first_chunk(p, si.n) + si.cb : 0, nc = run ? si.ce - si.cb : 0;
+  int c0 = run ? seq_first_chunk(p, si.n) + si.cb : 0, nc = run ? si.ce - si.cb : 0;
+  if (run && (c0 < 0 || c0 + nc > p.n_chunks_total)) {  // the chunk index disagrees with the plan
+    if (tid == 0) report(p.status, kDevCheck, kDetSegMismatch);
+    run = false;
+    c0 = nc = 0;
+  }
   const size_t mat = (size_t)kDim * kDim;
   const size_t head_seg = ((size_t)(si.seg_base + si.s) * p.h_v + j) * mat;
   float D[64];  // row k, columns 64 h .. 64 h + 63
@@ -1273,7 +1278,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) bwd_chain2_tc_kernel(const Prob
   bool run = !failed && ctl->ok;
   if (!failed && !ctl->ok && tid == 0) report(p.status, kDevCheck, kDetSegMismatch);
   if (run && si.s == 0) run = false;  // segment 0 is taken by the final pass
-  const int c0 = run ? seq_first_chunk(p, si.n) + si.cb : 0, nc = run ? si.ce - si.cb : 0;
+  int c0 = run ? seq_first_chunk(p, si.n) + si.cb : 0, nc = run ? si.ce - si.cb : 0;
+  if (run && (c0 < 0 || c0 + nc > p.n_chunks_total)) {  // the chunk index disagrees with the plan
+    if (tid == 0) report(p.status, kDevCheck, kDetSegMismatch);
+    run = false;
+    c0 = nc = 0;
+  }
   const size_t mat = (size_t)kDim * kDim;
   const size_t head_seg = ((size_t)(si.seg_base + si.s) * p.h_v + j) * mat;
   float X0[64], X1[64];  // row k, columns 64 h .. 64 h + 63

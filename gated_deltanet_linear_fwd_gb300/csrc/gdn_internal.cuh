@@ -48,7 +48,7 @@ struct Problem {
   const int32_t* cu;        // device cu_seqlens or null
   void* out;
   float* hT;                // [n_seqs, h_v, d_k, d_v] or null
-  int T_row;                // tokens per batch row when cu == null
+  int T_row;                // tokens per batch row (with cu: all tokens, one row)
   int n_seqs, h_qk, h_v;
   float scale;
   int elem_f32;             // q/k/v/out are fp32 (else bf16)
@@ -144,12 +144,19 @@ __device__ __forceinline__ int seq_first_chunk(const Problem& p, int n) {
   return p.cu ? p.seq_chunk_base[n] : n * chunks_of(p.T_row);
 }
 
-// Segments of sequence n (cp_off: one).
+// Segments of sequence n (cp_off: one); -1 when its device offsets are not a
+// range inside [0, T], or the first sequence does not start at 0 or the last
+// end at T (the offsets disagree with the plan: nothing of it is touched).
 __device__ __forceinline__ int seq_seg_count(const Problem& p, int n, int64_t& bos, int64_t& eos,
                                              int& n_chunks) {
   if (p.cu) {
     bos = p.cu[n];
     eos = p.cu[n + 1];
+    if (bos < 0 || eos < bos || eos > (int64_t)p.T_row || (n == 0 && bos != 0) ||
+        (n == p.n_seqs - 1 && eos != (int64_t)p.T_row)) {
+      n_chunks = 0;
+      return -1;
+    }
   } else {
     bos = (int64_t)n * p.T_row;
     eos = bos + p.T_row;
@@ -159,7 +166,9 @@ __device__ __forceinline__ int seq_seg_count(const Problem& p, int n, int64_t& b
 }
 
 // Locates global segment `seg` (warp-cooperative; call with a full warp,
-// every lane gets the result).  Returns false if seg is out of range.
+// every lane gets the result).  Returns false if seg is out of range, if a
+// sequence up to it has offsets outside [0, T], or if the sequence's segments
+// reach past the plan's.
 __device__ inline bool locate_segment(const Problem& p, int seg, SegInfo& out) {
   const int lane = threadIdx.x & 31;
   int base = 0;
@@ -168,6 +177,7 @@ __device__ inline bool locate_segment(const Problem& p, int seg, SegInfo& out) {
     int cnt = 0, nch = 0;
     int64_t bos = 0, eos = 0;
     if (n < p.n_seqs) cnt = seq_seg_count(p, n, bos, eos, nch);
+    if (__any_sync(0xffffffffu, cnt < 0)) return false;
     int incl = cnt;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -188,7 +198,7 @@ __device__ inline bool locate_segment(const Problem& p, int seg, SegInfo& out) {
       out.s = seg - out.seg_base;
       out.cb = seg_first(out.s, out.n_chunks, out.n_seg);
       out.ce = seg_first(out.s + 1, out.n_chunks, out.n_seg);
-      return true;
+      return out.seg_base + out.n_seg <= p.n_seg_total;
     }
     base += __shfl_sync(0xffffffffu, incl, 31);
   }
@@ -196,14 +206,18 @@ __device__ inline bool locate_segment(const Problem& p, int seg, SegInfo& out) {
 }
 
 // Segment range of sequence n (warp-cooperative, every lane gets the result).
+// Offsets outside [0, T] up to n, or segments reaching past the plan's, give
+// no segments (n_seg = 0).
 __device__ inline void locate_sequence(const Problem& p, int n, SegInfo& out) {
   const int lane = threadIdx.x & 31;
   int base = 0;
+  bool bad = false;
   for (int n0 = 0; n0 < n; n0 += 32) {
     const int m = n0 + lane;
     int cnt = 0, nch = 0;
     int64_t bos, eos;
     if (m < n) cnt = seq_seg_count(p, m, bos, eos, nch);
+    bad |= __any_sync(0xffffffffu, cnt < 0);
 #pragma unroll
     for (int d = 16; d >= 1; d >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, d);
     base += cnt;
@@ -211,6 +225,10 @@ __device__ inline void locate_sequence(const Problem& p, int n, SegInfo& out) {
   out.n = n;
   out.seg_base = base;
   out.n_seg = seq_seg_count(p, n, out.bos, out.eos, out.n_chunks);
+  if (bad || out.n_seg < 0 || base + out.n_seg > p.n_seg_total) {
+    out.n_seg = 0;
+    out.n_chunks = 0;
+  }
   out.s = 0;
   out.cb = 0;
   out.ce = out.n_chunks;

@@ -652,8 +652,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool none = false;
     if (PREP && p.plan_mode == kModeWarmup) {
       const SegInfo si = si0;
-      if (ok0) {
-        const int chunk0 = seq_first_chunk(p, si.n);
+      const int chunk0 = ok0 ? seq_first_chunk(p, si.n) : -1;
+      if (ok0 && chunk0 >= 0 && chunk0 + si.n_chunks <= p.n_chunks_total) {
         for (int s2 = lane; s2 < si.n_seg; s2 += 32) {
           int w = 0;
           float b = -__int_as_float(0x7f800000);

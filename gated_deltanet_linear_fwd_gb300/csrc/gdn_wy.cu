@@ -572,18 +572,30 @@ constexpr int kMapThreads = 1024;
 
 __global__ void __launch_bounds__(kMapThreads) chunk_map_kernel(const Problem p) {
   __shared__ int warp_sum[32];
-  __shared__ int carry;
+  __shared__ int carry, seg_total;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   grid_launch_dependents();
-  if (tid == 0) carry = 0;
+  if (tid == 0) {
+    carry = 0;
+    seg_total = 0;
+  }
   __syncthreads();
+  // The device offsets must be the plan's: sequence bounds that run from 0 to
+  // T without going back, and the plan's numbers of chunks and segments.
+  int bad = 0;
   for (int n0 = 0; n0 < p.n_seqs; n0 += kMapThreads) {
     const int n = n0 + tid;
     int cnt = 0;
     if (n < p.n_seqs) {
       int64_t bos, eos;
       seq_bounds(p, n, bos, eos);
-      cnt = chunks_of(eos - bos);
+      if (bos < 0 || eos < bos || eos > (int64_t)p.T_row || (n == 0 && bos != 0) ||
+          (n == p.n_seqs - 1 && eos != (int64_t)p.T_row)) {
+        bad = 1;
+      } else {
+        cnt = chunks_of(eos - bos);
+        atomicAdd(&seg_total, seg_count(cnt, p.lambda_q8, p.plan_mode == kModeOff));
+      }
     }
     int x = cnt;
 #pragma unroll
@@ -609,11 +621,18 @@ __global__ void __launch_bounds__(kMapThreads) chunk_map_kernel(const Problem p)
     if (tid == kMapThreads - 1) carry = incl;
     __syncthreads();
   }
-  if (tid == 0) p.seq_chunk_base[p.n_seqs] = carry;
   const int total = carry;
-  if (tid == 0 && total != p.n_chunks_total) report(p.status, kDevCheck, kDetSegMismatch);
+  const bool valid =
+      __syncthreads_or(bad) == 0 && total == p.n_chunks_total && seg_total == p.n_seg_total;
+  if (!valid) {  // nothing later may follow these offsets: every chunk is marked as outside the plan
+    if (tid == 0) report(p.status, kDevCheck, kDetSegMismatch);
+    for (int n = tid; n <= p.n_seqs; n += kMapThreads) p.seq_chunk_base[n] = -1;
+    for (int gc = tid; gc < p.n_chunks_total; gc += kMapThreads) p.chunk_info[gc] = make_int4(-1, 0, 0, 0);
+    return;
+  }
+  if (tid == 0) p.seq_chunk_base[p.n_seqs] = total;
   __syncthreads();
-  for (int gc = tid; gc < total && gc < p.n_chunks_total; gc += kMapThreads) {
+  for (int gc = tid; gc < total; gc += kMapThreads) {
     int lo = 0, hi = p.n_seqs - 1;  // last n with base[n] <= gc
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;

@@ -126,3 +126,28 @@ def test_bwd_timeout_path_reports_and_the_next_call_is_clean(mode):
     fresh = gdn_chunk_bwd(d.q, d.k, d.v, d.g, d.beta, d_out, d.h0, dhT, plan=plan, workspace=ws2)
     for x, y in zip(again, fresh):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("mode", ["off", "exact"])
+@pytest.mark.parametrize("bad", [[0, 300, 900], [0, 800, 700], [0, 300, 650]])
+def test_device_offsets_that_disagree_with_the_plan_are_reported(bad, mode, dtype):
+    """Device cu_seqlens other than the plan's: a sequence past T, one going back, the
+    last ending before T.  The kernels check the offsets before following them: status 7
+    (detail 3), no access outside the buffers, and the next call with the plan's offsets
+    on the same workspace is clean and correct."""
+    w = make_inputs(cu_seqlens=[0, 300, 700], h_qk=2, h_v=4, seed=5, with_h0=True, dtype=dtype)
+    d = w.to("cuda:0")
+    plan = gdn_cp_plan(T=w.T, h_qk=2, h_v=4, cu_seqlens=w.cu_seqlens, mode=mode, lambda_=0.5, dtype=dtype)
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device="cuda:0")
+    cu_bad = torch.tensor(bad, dtype=torch.int32, device="cuda:0")
+    gdn_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, cu_bad, plan=plan, workspace=ws)
+    assert gdn_get_device_status(ws) == (DEVICE_CHECK, 3)
+    o, hT = gdn_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, plan=plan, workspace=ws)
+    assert gdn_get_device_status(ws) == (0, 0)
+    f = util.to64
+    ro, rh = oracle.recurrence(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0), w.seq_offsets())
+    if dtype == torch.float32:
+        assert util.parity_f32(o, ro) <= 1e-4 and util.parity_f32(hT, rh) <= 1e-4
+    else:
+        assert util.parity_bf16(o, ro)[0] <= util.TOL_BF16 and util.parity_f32(hT, rh) <= util.TOL_STATE
