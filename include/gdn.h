@@ -179,7 +179,12 @@ gdn_status gdn_cp_plan(const gdn_dims* dims, const int32_t* cu_seqlens_host,
  *   beta          : device, [B*T, h_v] fp32, write strength.
  *   initial_state : device, [n_seqs, h_v, d_k, d_v] fp32 (H = S^T), or NULL for zeros.
  *   cu_seqlens_dev: device int32 [n_seqs+1], the same offsets given to gdn_cp_plan,
- *                   or NULL for fixed-length rows.
+ *                   or NULL for fixed-length rows.  The kernels check them before
+ *                   following them: offsets outside [0, T], going back, not ending
+ *                   at T, or giving other chunk or segment counts than the plan's
+ *                   are reported as GDN_ERR_DEVICE_CHECK with detail 3 in the status
+ *                   word, and nothing is read or written by them (o is then not
+ *                   written).  Other boundaries with the same counts go undetected.
  *   out           : device, [B*T, h_v, d_v], dims->dtype (bf16 rounded to nearest even).
  *   final_state   : device, [n_seqs, h_v, d_k, d_v] fp32, or NULL (not written).
  *   dims, plan    : host; plan must come from gdn_cp_plan with these dims.
