@@ -183,8 +183,9 @@ gdn_status gdn_cp_plan(const gdn_dims* dims, const int32_t* cu_seqlens_host,
  *                   following them: offsets outside [0, T], going back, not ending
  *                   at T, or giving other chunk or segment counts than the plan's
  *                   are reported as GDN_ERR_DEVICE_CHECK with detail 3 in the status
- *                   word, and nothing is read or written by them (o is then not
- *                   written).  Other boundaries with the same counts go undetected.
+ *                   word, and no access follows them outside the buffers (o and
+ *                   final_state are then incomplete).  Other boundaries with the
+ *                   same counts go undetected.
  *   out           : device, [B*T, h_v, d_v], dims->dtype (bf16 rounded to nearest even).
  *   final_state   : device, [n_seqs, h_v, d_k, d_v] fp32, or NULL (not written).
  *   dims, plan    : host; plan must come from gdn_cp_plan with these dims.
