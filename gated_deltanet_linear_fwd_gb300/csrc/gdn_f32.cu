@@ -6,9 +6,13 @@
 //   o_t = scale S_t q_t.
 // Each row s of S (one d_v index) evolves on its own given k, g and beta:
 //   s <- a s + c k,   a = exp(g_t),  c = beta_t (v_t[row] - a (s . k)),
-// so two neighbouring threads of a warp hold one row (64 fp32 registers each,
-// their dot products joined by one shuffle) and a CTA of 256 threads holds a
-// whole state.
+// so a CTA of 256 threads holds a whole state: eight neighbouring threads of a
+// warp hold four rows, each thread 16 columns of them (64 fp32 registers), so
+// that every k and q value a thread reads from shared memory serves four rows;
+// the eight partial dot products of a row are joined by three shuffles.  The
+// state is kept as S = sigma R with one scale for the whole state: the decay
+// a multiplies sigma, so a token's update R <- R + (c / sigma) k is one FMA
+// per element; sigma is folded back into R whenever it leaves [2^-60, 2^60].
 //
 // Context parallelism (FlashQLA pages, section "AutoCP": segments whose start
 // states are combined exactly through the correction term M) supplies the
@@ -25,15 +29,16 @@
 // (sequence, value head).
 //
 // Tokens are staged through shared memory in blocks of 16 (k, q, v rows by
-// cp.async, the gates by plain loads), double buffered, so each thread reads
-// k and q as broadcasts.
+// cp.async, the gates by plain loads), double buffered; a thread's columns
+// 4 part + 32 m + e (m, e < 4) make each warp-wide k or q read one contiguous
+// 128-byte line.
 #include "gdn_dev.cuh"
 
 namespace gdn {
 namespace {
 
 constexpr int kF32Threads = 256;
-constexpr int kHalf = kDim / 2;  // columns per thread
+constexpr int kRowsT = 4, kColsT = 16;  // rows and columns of S per thread (8 threads per row group)
 constexpr int kTokBlock = 16;
 constexpr int kBufFloats = 3 * kTokBlock * kDim + 2 * kTokBlock;  // k, q, v rows, then exp(g), beta
 constexpr int kF32Smem = 2 * kBufFloats * 4;
@@ -48,14 +53,6 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-// A shared-memory float4 read the compiler may not merge with an earlier read
-// of the same address: the update pass reads k again rather than keep all of
-// it in registers across the dot product.
-__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
-  return v;
-}
 
 // OUT: the output role; else blockIdx.z = 0 runs the transition and 1 the
 // local state.
@@ -66,7 +63,7 @@ __global__ void __launch_bounds__(kF32Threads, 2) recurrence_f32_kernel(const Pr
   __shared__ SegInfo s_seg;
   __shared__ int s_skip;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int row = tid >> 1, half = tid & 1, c0 = half * kHalf;  // this thread: row, columns c0 .. c0 + 63
+  const int part = tid & 7, row0 = kRowsT * (tid >> 3);  // rows row0 .. row0 + 3, columns 4 part + 32 m + e
   const int j = blockIdx.y;
   const bool transition = !OUT && blockIdx.z == 0;  // rows of the identity, no value input
   const bool with_v = !transition;
@@ -98,27 +95,40 @@ __global__ void __launch_bounds__(kF32Threads, 2) recurrence_f32_kernel(const Pr
   const size_t mat = (size_t)kDim * kDim;
   const size_t seg_off = ((size_t)(si.seg_base + si.s) * p.h_v + j) * mat;
 
-  float s[kHalf];
+  float s[kRowsT][kColsT];  // s[r][4 m + e] = R[row0 + r][4 part + 32 m + e], S = sigma R
   if (!OUT) {
 #pragma unroll
-    for (int i = 0; i < kHalf; ++i) s[i] = (transition && c0 + i == row) ? 1.f : 0.f;
-  } else if (si.s > 0) {  // the combined start state, rows = d_v
-    const float4* src = reinterpret_cast<const float4*>(p.Sstart + seg_off + (size_t)row * kDim + c0);
+    for (int r = 0; r < kRowsT; ++r)
 #pragma unroll
-    for (int i = 0; i < kHalf / 4; ++i) {
-      const float4 v4 = src[i];
-      s[4 * i] = v4.x;
-      s[4 * i + 1] = v4.y;
-      s[4 * i + 2] = v4.z;
-      s[4 * i + 3] = v4.w;
-    }
-  } else if (p.h0) {  // H = S^T: S[row][i] = h0[i][row]
+      for (int i = 0; i < kColsT; ++i)
+        s[r][i] = (transition && 4 * part + 32 * (i >> 2) + (i & 3) == row0 + r) ? 1.f : 0.f;
+  } else if (si.s > 0) {  // the combined start state, rows = d_v
+#pragma unroll
+    for (int r = 0; r < kRowsT; ++r)
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float4 v4 = *reinterpret_cast<const float4*>(p.Sstart + seg_off + (size_t)(row0 + r) * kDim + 4 * part +
+                                                           32 * m);
+        s[r][4 * m] = v4.x;
+        s[r][4 * m + 1] = v4.y;
+        s[r][4 * m + 2] = v4.z;
+        s[r][4 * m + 3] = v4.w;
+      }
+  } else if (p.h0) {  // H = S^T: S[row][c] = h0[c][row], four rows in one float4
     const float* h0 = p.h0 + (size_t)(si.n * p.h_v + j) * mat;
 #pragma unroll
-    for (int i = 0; i < kHalf; ++i) s[i] = h0[(size_t)(c0 + i) * kDim + row];
+    for (int i = 0; i < kColsT; ++i) {
+      const float4 v4 = *reinterpret_cast<const float4*>(h0 + (size_t)(4 * part + 32 * (i >> 2) + (i & 3)) * kDim + row0);
+      s[0][i] = v4.x;
+      s[1][i] = v4.y;
+      s[2][i] = v4.z;
+      s[3][i] = v4.w;
+    }
   } else {
 #pragma unroll
-    for (int i = 0; i < kHalf; ++i) s[i] = 0.f;
+    for (int r = 0; r < kRowsT; ++r)
+#pragma unroll
+      for (int i = 0; i < kColsT; ++i) s[r][i] = 0.f;
   }
 
   const float* q = reinterpret_cast<const float*>(p.q);
@@ -163,6 +173,14 @@ __global__ void __launch_bounds__(kF32Threads, 2) recurrence_f32_kernel(const Pr
       smem[(b & 1) * kBufFloats + 3 * kTokBlock * kDim + kTokBlock + tid] = be;
     }
   };
+  // a row's eight partial dot products, summed in every one of its threads
+  auto row_sum = [](float x) {
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    x += __shfl_xor_sync(0xffffffffu, x, 4);
+    return x;
+  };
+  float sigma = 1.f;  // S = sigma R
   if (n_blocks > 0) {
     float a0, b0;
     stage(0);
@@ -182,61 +200,102 @@ __global__ void __launch_bounds__(kF32Threads, 2) recurrence_f32_kernel(const Pr
     const float* buf = smem + (b & 1) * kBufFloats;
     const int nt = (int)min((int64_t)kTokBlock, t_end - t_begin - (int64_t)b * kTokBlock);
     for (int tt = 0; tt < nt; ++tt) {
-      const float4* kr = reinterpret_cast<const float4*>(buf + tt * kDim + c0);
       const float a = buf[3 * kTokBlock * kDim + tt], be = buf[3 * kTokBlock * kDim + kTokBlock + tt];
-      // s . k over four partial sums
-      float sk[4] = {0.f, 0.f, 0.f, 0.f};
+      float kc[kColsT];
 #pragma unroll
-      for (int i = 0; i < kHalf / 4; ++i) {
-        const float4 k4 = kr[i];
-        sk[i & 3] = fmaf(s[4 * i], k4.x, sk[i & 3]);
-        sk[i & 3] = fmaf(s[4 * i + 1], k4.y, sk[i & 3]);
-        sk[i & 3] = fmaf(s[4 * i + 2], k4.z, sk[i & 3]);
-        sk[i & 3] = fmaf(s[4 * i + 3], k4.w, sk[i & 3]);
+      for (int m = 0; m < 4; ++m) {
+        const float4 k4 = *reinterpret_cast<const float4*>(buf + tt * kDim + 4 * part + 32 * m);
+        kc[4 * m] = k4.x;
+        kc[4 * m + 1] = k4.y;
+        kc[4 * m + 2] = k4.z;
+        kc[4 * m + 3] = k4.w;
       }
-      float skv = (sk[0] + sk[1]) + (sk[2] + sk[3]);
-      skv += __shfl_xor_sync(0xffffffffu, skv, 1);  // the row's other half
-      const float vr = with_v ? buf[2 * kTokBlock * kDim + tt * kDim + row] : 0.f;
-      const float c = be * (vr - a * skv);
-      const uint32_t kaddr = smem_u32(kr);
+      float vr[kRowsT] = {0.f, 0.f, 0.f, 0.f};
+      if (with_v) {
+        const float4 v4 = *reinterpret_cast<const float4*>(buf + 2 * kTokBlock * kDim + tt * kDim + row0);
+        vr[0] = v4.x;
+        vr[1] = v4.y;
+        vr[2] = v4.z;
+        vr[3] = v4.w;
+      }
 #pragma unroll
-      for (int i = 0; i < kHalf / 4; ++i) {
-        const float4 k4 = lds_f4(kaddr + 16u * i);
-        s[4 * i] = fmaf(c, k4.x, a * s[4 * i]);
-        s[4 * i + 1] = fmaf(c, k4.y, a * s[4 * i + 1]);
-        s[4 * i + 2] = fmaf(c, k4.z, a * s[4 * i + 2]);
-        s[4 * i + 3] = fmaf(c, k4.w, a * s[4 * i + 3]);
+      float c[kRowsT];
+#pragma unroll
+      for (int r = 0; r < kRowsT; ++r) {  // c = beta (v - a s . k) with s . k = sigma (R . k)
+        float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < kColsT; i += 2) {
+          x0 = fmaf(s[r][i], kc[i], x0);
+          x1 = fmaf(s[r][i + 1], kc[i + 1], x1);
+        }
+        c[r] = be * (vr[r] - a * (sigma * row_sum(x0 + x1)));
+      }
+      // S <- a S + c k: sigma <- a sigma, R <- R + (c / sigma) k
+      sigma *= a;
+      if (!(sigma >= 0x1p-60f && sigma <= 0x1p60f)) {  // (the same in every thread)
+#pragma unroll
+        for (int r = 0; r < kRowsT; ++r)
+#pragma unroll
+          for (int i = 0; i < kColsT; ++i) s[r][i] *= sigma;
+        sigma = 1.f;
+      }
+      const float inv = 1.f / sigma;
+#pragma unroll
+      for (int r = 0; r < kRowsT; ++r) {
+        const float cr = c[r] * inv;
+#pragma unroll
+        for (int i = 0; i < kColsT; ++i) s[r][i] = fmaf(cr, kc[i], s[r][i]);
       }
       if (OUT) {
-        const float4* qr = reinterpret_cast<const float4*>(buf + kTokBlock * kDim + tt * kDim + c0);
-        float so[4] = {0.f, 0.f, 0.f, 0.f};
+        float qc[kColsT];
 #pragma unroll
-        for (int i = 0; i < kHalf / 4; ++i) {
-          const float4 q4 = qr[i];
-          so[i & 3] = fmaf(s[4 * i], q4.x, so[i & 3]);
-          so[i & 3] = fmaf(s[4 * i + 1], q4.y, so[i & 3]);
-          so[i & 3] = fmaf(s[4 * i + 2], q4.z, so[i & 3]);
-          so[i & 3] = fmaf(s[4 * i + 3], q4.w, so[i & 3]);
+        for (int m = 0; m < 4; ++m) {
+          const float4 q4 = *reinterpret_cast<const float4*>(buf + kTokBlock * kDim + tt * kDim + 4 * part + 32 * m);
+          qc[4 * m] = q4.x;
+          qc[4 * m + 1] = q4.y;
+          qc[4 * m + 2] = q4.z;
+          qc[4 * m + 3] = q4.w;
         }
-        float sov = (so[0] + so[1]) + (so[2] + so[3]);
-        sov += __shfl_xor_sync(0xffffffffu, sov, 1);
+        float so[kRowsT];
+#pragma unroll
+        for (int r = 0; r < kRowsT; ++r) {
+          float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+          for (int i = 0; i < kColsT; i += 2) {
+            x0 = fmaf(s[r][i], qc[i], x0);
+            x1 = fmaf(s[r][i + 1], qc[i + 1], x1);
+          }
+          so[r] = sigma * row_sum(x0 + x1);
+        }
         const int64_t t = t_begin + (int64_t)b * kTokBlock + tt;
-        if (half == 0) o[((size_t)t * p.h_v + j) * kDim + row] = p.scale * sov;
+        if (part == 0)
+          *reinterpret_cast<float4*>(o + ((size_t)t * p.h_v + j) * kDim + row0) =
+              make_float4(p.scale * so[0], p.scale * so[1], p.scale * so[2], p.scale * so[3]);
       }
     }
     put_gates(b + 1, a1, b1);  // buffer (b + 1) & 1's gates: read from the next block on
     __syncthreads();           // buffer b & 1 is read before block b + 2 is staged into it
   }
+#pragma unroll
+  for (int r = 0; r < kRowsT; ++r)
+#pragma unroll
+    for (int i = 0; i < kColsT; ++i) s[r][i] *= sigma;
   if (OUT) {
-    if (p.hT && si.s == si.n_seg - 1) {  // H = S^T
+    if (p.hT && si.s == si.n_seg - 1) {  // H = S^T: four rows of S are one float4 of a row of H
       float* hT = p.hT + (size_t)(si.n * p.h_v + j) * mat;
 #pragma unroll
-      for (int i = 0; i < kHalf; ++i) hT[(size_t)(c0 + i) * kDim + row] = s[i];
+      for (int i = 0; i < kColsT; ++i)
+        *reinterpret_cast<float4*>(hT + (size_t)(4 * part + 32 * (i >> 2) + (i & 3)) * kDim + row0) =
+            make_float4(s[0][i], s[1][i], s[2][i], s[3][i]);
     }
   } else {
-    float4* dst = reinterpret_cast<float4*>((transition ? p.R : p.Sloc) + seg_off + (size_t)row * kDim + c0);
+    float* dst = (transition ? p.R : p.Sloc) + seg_off;
 #pragma unroll
-    for (int i = 0; i < kHalf / 4; ++i) dst[i] = make_float4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
+    for (int r = 0; r < kRowsT; ++r)
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        *reinterpret_cast<float4*>(dst + (size_t)(row0 + r) * kDim + 4 * part + 32 * m) =
+            make_float4(s[r][4 * m], s[r][4 * m + 1], s[r][4 * m + 2], s[r][4 * m + 3]);
   }
 }
 

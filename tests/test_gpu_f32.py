@@ -60,3 +60,30 @@ def test_f32_parity_full_size():
     eo, eh = util.parity_f32(o, ro), util.parity_f32(hT, rh)
     print(f"f32 full size ({plan.n_seg_total} segments): o {eo:.2e}  hT {eh:.2e}")
     assert eo <= TOL_F32 and eh <= TOL_F32
+
+
+@pytest.mark.parametrize("kind", ["no_decay", "decay_30", "decay_100", "beta_zero"])
+@pytest.mark.parametrize("mode", ["off", "exact"])
+def test_f32_degenerate_gates(kind, mode):
+    """The kernel keeps S as one scale times a matrix and folds the scale in when it
+    leaves [2^-60, 2^60]: no decay (the scale stays 1), a decay of e^-30 a token (a
+    fold every other token), e^-100 (exp(g) subnormal or zero: each token restarts
+    the state), and beta = 0 (the state only decays)."""
+    w = make_inputs(cu_seqlens=[0, 150, 600], h_qk=1, h_v=2, seed=23, with_h0=True, dtype=torch.float32,
+                    g_kind="zero" if kind == "no_decay" else "mix")
+    if kind.startswith("decay_"):
+        w.g = torch.full_like(w.g, -float(kind.split("_")[1]))
+    if kind == "beta_zero":
+        w.beta = torch.zeros_like(w.beta)
+    d = w.to("cuda:0")
+    plan = gdn_cp_plan(T=w.T, h_qk=1, h_v=2, cu_seqlens=w.cu_seqlens, dtype=torch.float32, mode=mode,
+                       lambda_=0.5)
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device="cuda:0")
+    o, hT = gdn_chunk_fwd(d.q, d.k, d.v, d.g, d.beta, d.h0, d.cu_seqlens, plan=plan, workspace=ws)
+    assert gdn_get_device_status(ws)[0] == 0
+    f = util.to64
+    ro, rh = oracle.recurrence(f(w.q), f(w.k), f(w.v), f(w.g), f(w.beta), f(w.h0), w.seq_offsets())
+    eo, eh = util.parity_f32(o, ro), util.parity_f32(hT, rh)
+    print(f"f32 {kind}/{mode}: o {eo:.2e}  hT {eh:.2e}")
+    assert torch.isfinite(o).all() and torch.isfinite(hT).all()
+    assert eo <= TOL_F32 and eh <= TOL_F32
