@@ -9,7 +9,8 @@
 // so a CTA of 256 threads holds a whole state: eight neighbouring threads of a
 // warp hold four rows, each thread 16 columns of them (64 fp32 registers), so
 // that every k and q value a thread reads from shared memory serves four rows;
-// the eight partial dot products of a row are joined by three shuffles.  The
+// the group's partial dot products of its four rows are summed in four
+// shuffles, each thread ending with one row's total.  The
 // state is kept as S = sigma R with one scale for the whole state: the decay
 // a multiplies sigma, so a token's update R <- R + (c / sigma) k is one FMA
 // per element; sigma is folded back into R whenever it leaves [2^-60, 2^60].
@@ -173,12 +174,18 @@ __global__ void __launch_bounds__(kF32Threads, 2) recurrence_f32_kernel(const Pr
       smem[(b & 1) * kBufFloats + 3 * kTokBlock * kDim + kTokBlock + tid] = be;
     }
   };
-  // a row's eight partial dot products, summed in every one of its threads
-  auto row_sum = [](float x) {
-    x += __shfl_xor_sync(0xffffffffu, x, 1);
-    x += __shfl_xor_sync(0xffffffffu, x, 2);
-    x += __shfl_xor_sync(0xffffffffu, x, 4);
-    return x;
+  // The four rows' partial dot products x[0..3] of the eight threads of a row
+  // group, summed so that thread (part) ends with the total of row rsel =
+  // 2 (part >> 2 & 1) + (part >> 1 & 1): each level sends the half it does
+  // not keep (four shuffles in all instead of twelve).
+  const int b2 = (part >> 2) & 1, b1 = (part >> 1) & 1, rsel = 2 * b2 + b1;
+  const int group_lane = lane & ~7;
+  auto rows_sum = [&](const float (&x)[kRowsT]) {
+    const float y0 = (b2 ? x[2] : x[0]) + __shfl_xor_sync(0xffffffffu, b2 ? x[0] : x[2], 4);
+    const float y1 = (b2 ? x[3] : x[1]) + __shfl_xor_sync(0xffffffffu, b2 ? x[1] : x[3], 4);
+    float z = (b1 ? y1 : y0) + __shfl_xor_sync(0xffffffffu, b1 ? y0 : y1, 2);
+    z += __shfl_xor_sync(0xffffffffu, z, 1);
+    return z;
   };
   float sigma = 1.f;  // S = sigma R
   if (n_blocks > 0) {
@@ -210,26 +217,23 @@ __global__ void __launch_bounds__(kF32Threads, 2) recurrence_f32_kernel(const Pr
         kc[4 * m + 2] = k4.z;
         kc[4 * m + 3] = k4.w;
       }
-      float vr[kRowsT] = {0.f, 0.f, 0.f, 0.f};
-      if (with_v) {
-        const float4 v4 = *reinterpret_cast<const float4*>(buf + 2 * kTokBlock * kDim + tt * kDim + row0);
-        vr[0] = v4.x;
-        vr[1] = v4.y;
-        vr[2] = v4.z;
-        vr[3] = v4.w;
-      }
+      const float vsel = with_v ? buf[2 * kTokBlock * kDim + tt * kDim + row0 + rsel] : 0.f;
+      float x[kRowsT];
 #pragma unroll
-      float c[kRowsT];
-#pragma unroll
-      for (int r = 0; r < kRowsT; ++r) {  // c = beta (v - a s . k) with s . k = sigma (R . k)
+      for (int r = 0; r < kRowsT; ++r) {  // this thread's part of R . k
         float x0 = 0.f, x1 = 0.f;
 #pragma unroll
         for (int i = 0; i < kColsT; i += 2) {
           x0 = fmaf(s[r][i], kc[i], x0);
           x1 = fmaf(s[r][i + 1], kc[i + 1], x1);
         }
-        c[r] = be * (vr[r] - a * (sigma * row_sum(x0 + x1)));
+        x[r] = x0 + x1;
       }
+      // c = beta (v - a s . k) with s . k = sigma (R . k): for row rsel, then every row's
+      const float csel = be * (vsel - a * (sigma * rows_sum(x)));
+      float c[kRowsT];
+#pragma unroll
+      for (int r = 0; r < kRowsT; ++r) c[r] = __shfl_sync(0xffffffffu, csel, group_lane | (4 * (r >> 1) + 2 * (r & 1)));
       // S <- a S + c k: sigma <- a sigma, R <- R + (c / sigma) k
       sigma *= a;
       if (!(sigma >= 0x1p-60f && sigma <= 0x1p60f)) {  // (the same in every thread)
@@ -256,7 +260,7 @@ __global__ void __launch_bounds__(kF32Threads, 2) recurrence_f32_kernel(const Pr
           qc[4 * m + 2] = q4.z;
           qc[4 * m + 3] = q4.w;
         }
-        float so[kRowsT];
+        float xq[kRowsT];
 #pragma unroll
         for (int r = 0; r < kRowsT; ++r) {
           float x0 = 0.f, x1 = 0.f;
@@ -265,12 +269,11 @@ __global__ void __launch_bounds__(kF32Threads, 2) recurrence_f32_kernel(const Pr
             x0 = fmaf(s[r][i], qc[i], x0);
             x1 = fmaf(s[r][i + 1], qc[i + 1], x1);
           }
-          so[r] = sigma * row_sum(x0 + x1);
+          xq[r] = x0 + x1;
         }
+        const float osel = p.scale * (sigma * rows_sum(xq));
         const int64_t t = t_begin + (int64_t)b * kTokBlock + tt;
-        if (part == 0)
-          *reinterpret_cast<float4*>(o + ((size_t)t * p.h_v + j) * kDim + row0) =
-              make_float4(p.scale * so[0], p.scale * so[1], p.scale * so[2], p.scale * so[3]);
+        if ((part & 1) == 0) o[((size_t)t * p.h_v + j) * kDim + row0 + rsel] = osel;
       }
     }
     put_gates(b + 1, a1, b1);  // buffer (b + 1) & 1's gates: read from the next block on
