@@ -129,7 +129,7 @@ __device__ __forceinline__ bool wait_bar(Ctl* ctl, int b, uint32_t parity) {
   return wait_phase(&ctl->bar[b], parity, &ctl->abort, 100 + b);
 }
 
-// A warp's verdict on a wait: true only if every lane's wait succeeded, so
+// A warp's outcome of a wait: true only if every lane's wait succeeded, so
 // the warp stays converged for its warp-collective instructions.
 __device__ __forceinline__ bool warp_ok(bool ok) { return __all_sync(0xffffffffu, ok); }
 
