@@ -98,15 +98,15 @@ gdn_status device_setup(int* dev_out) {
 // block scheduler hands CTAs out in launch order (the segments of sequence
 // 0, 1, ..., then the next value head) to whichever SM frees first, so the
 // planner replays that list schedule.  The combine then walks each
-// sequence's segments in order, about half a chunk-time per segment.  Among
-// lambda = k/8 the planner takes the smallest (schedule finish + half the
-// largest segment count of a sequence); ties go to fewer segments.
+// sequence's segments in order, about a chunk-time per segment.  Among
+// lambda = k/8 the planner takes the smallest (schedule finish + the largest
+// segment count of a sequence); ties go to fewer segments.
 namespace {
 
 constexpr int kCtaOverheadChunks = 3;
 
 // The model's constants per path.  The bf16 scan: a CTA costs its chunks + 3
-// (start-up, pipeline fill, warmup) and a combine step about half a chunk.
+// (start-up, pipeline fill, warmup) and a combine step about a chunk.
 // The fp32 path: a chunk is ~40x a combine step and the start-up is small
 // against a chunk, so both count zero; its chains run two CTAs per SM.
 struct PlanModel {
@@ -169,7 +169,7 @@ int pick_lambda_q8_uncached(const gdn_dims* d, const int32_t* cu, int slots, con
   std::vector<int32_t> free_at;
   for (int q8 = 32; q8 <= 4096; q8 += 32) {
     const SegStats st = seg_stats(d, cu, q8, m);
-    const int64_t comb = m.combine ? st.most_segs : 0;
+    const int64_t comb = m.combine ? 2 * st.most_segs : 0;
     // in half chunk-times; no schedule ends before its longest CTA or the average slot load
     const int64_t total = st.work * d->h_v;
     const int64_t lower = 2 * std::max<int64_t>(st.longest + m.overhead, (total + slots - 1) / slots) + comb;

@@ -110,7 +110,8 @@ typedef struct gdn_cp_opts {
                         steps of 1/256; <= 0 lets the planner choose it: the lambda (a
                         multiple of 1/8) minimising 2 x (finish of the list schedule of
                         the scan's CTAs in launch order on sm_count SMs, each taking its
-                        segment's chunks + 3) + (most segments of one sequence); ties go
+                        segment's chunks + 3) + 2 x (most segments of one sequence: a
+                        combine step costs about a chunk-time); ties go
                         to fewer segments.  For GDN_F32, whose chains run two CTAs per
                         SM and whose chunks dwarf a combine step, the schedule has 2 x
                         sm_count slots, a CTA takes its chunks alone, and the score is

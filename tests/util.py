@@ -101,7 +101,8 @@ def warmup_depths(w, lambda_q8, wmax, tol, rule="fixed"):
 def auto_lambda_q8(T_list, h_v, sm_count, overhead=3, combine=True):
     """The planner's automatic lambda, restated from its documented rule:
     among lambda = k/8 (k = 1..128) take the smallest (2 x finish of the list
-    schedule of the scan's CTAs + the largest segment count of a sequence),
+    schedule of the scan's CTAs + 2 x the largest segment count of a sequence:
+    a combine step costs about a chunk-time),
     ties to fewer segments.  The schedule: launch order (the segments of every
     sequence, head after head), each CTA taking segment chunks + overhead on
     the first of sm_count slots to free up.  The fp32 path: 2 x SMs slots, no
@@ -115,7 +116,7 @@ def auto_lambda_q8(T_list, h_v, sm_count, overhead=3, combine=True):
                 for a, b in sg:
                     i = min(range(sm_count), key=free.__getitem__)
                     free[i] += b - a + overhead
-        comb = max(len(sg) for sg in seglists) if combine else 0
+        comb = 2 * max(len(sg) for sg in seglists) if combine else 0
         key = (2 * max(free) + comb, sum(len(sg) for sg in seglists))
         if best is None or key < best[0]:
             best = (key, q8)
