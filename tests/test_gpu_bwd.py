@@ -182,7 +182,8 @@ def test_bwd_million_token_sequence():
 
 
 @pytest.mark.parametrize("name,heads", [("T32768_h2x8", None), ("T32768_h16x16", [0, 7, 15]),
-                                        ("varlen4_T348160_h2x8", [1, 6])])
+                                        ("T32768_h8x24_h0", [0, 11, 23]), ("varlen4_T348160_h2x8", [1, 6]),
+                                        ("batch8_T4096_h8x32", [0, 13, 31])])
 def test_bwd_full_size(name, heads):
     """The benchmark's 1 x 32768 workloads at full size, in the bench's launch
     configuration (auto plan); every head, or a sample of heads, element by element."""
