@@ -176,38 +176,9 @@ __device__ __forceinline__ void st_h(uint32_t addr, float x) {
 }
 
 // 64 rows x 128 bf16 of a [tokens, heads, 128] tensor into two fp16 panels
-// (panel stride pstride); rows >= cv are zero.
-template <int NT = kTcThreads>
-__device__ __forceinline__ void rows_to_f16(uint32_t base, uint32_t pstride, const __nv_bfloat16* src, int64_t t0,
-                                            int heads, int head, int cv, float& mx, const float* row_scale = nullptr) {
-  // all four loads in flight before the first store (the stores are ordered memory operations)
-  constexpr int kPer = 64 * 16 / NT;
-  uint4 raw[kPer];
-#pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int idx = threadIdx.x + u * NT, r = idx >> 4, c = idx & 15;
-    raw[u] = make_uint4(0, 0, 0, 0);
-    if (r < cv) raw[u] = *reinterpret_cast<const uint4*>(src + ((size_t)(t0 + r) * heads + head) * kDim + c * 8);
-  }
-#pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int idx = threadIdx.x + u * NT, r = idx >> 4, c = idx & 15;
-    const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-    const float sc = row_scale ? row_scale[r] : 1.f;
-    uint32_t o[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
-      mx = absmax_nan(absmax_nan(mx, f.x * sc), f.y * sc);
-      o[e] = pack_f16x2(f.x * sc, f.y * sc);
-    }
-    st_shared_v4(base + (uint32_t)(c >> 3) * pstride + sw128_offset((uint32_t)r, (uint32_t)(c & 7)), o[0], o[1],
-                 o[2], o[3]);
-  }
-}
-
-// rows_to_f16 in two halves: the loads (into registers, before the row
-// scales are known), then the conversion and the stores.
+// (panel stride pstride; rows >= cv are zero), in two halves: the loads into
+// registers (issued together, and before any row scale is known), then the
+// conversion and the stores.
 template <int NT>
 struct RowLoads {
   uint4 raw[64 * 16 / NT];
@@ -378,6 +349,14 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
     bulk_load(sm + sP, p.wy + slot * kRecBytes + kRecP, 8192u, &ctl->loadC);
   };
   if (ok) {
+    // the first head's tiles need nothing of Q and K: their copies start first
+    if (j_lo < j_hi) {
+      if (tid == 0) {
+        issue_A(j_lo);
+        issue_C(j_lo);
+      }
+      if (warp == 0) issue_B(j_lo);
+    }
     // dq^T and dk^T accumulators start at zero
     {
       float z[16];
@@ -386,8 +365,13 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
       st16f(tmem + tDQ + 16 * h, z);
       st16f(tmem + tDK + 16 * h, z);
     }
-    rows_to_f16<kLocThreads>(s0 + sQK, 16384, reinterpret_cast<const __nv_bfloat16*>(p.q), t0, p.h_qk, iq, cv, mx);
-    rows_to_f16<kLocThreads>(s0 + sQK + 8192, 16384, reinterpret_cast<const __nv_bfloat16*>(p.k), t0, p.h_qk, iq, cv, mx);
+    // Q, K and the first head's dO rows: every load in flight before any store
+    RowLoads<kLocThreads> lq, lk, ldo;
+    rows_load(lq, reinterpret_cast<const __nv_bfloat16*>(p.q), t0, p.h_qk, iq, cv);
+    rows_load(lk, reinterpret_cast<const __nv_bfloat16*>(p.k), t0, p.h_qk, iq, cv);
+    if (j_lo < j_hi) rows_load(ldo, reinterpret_cast<const __nv_bfloat16*>(b.dout), t0, p.h_v, j_lo, cv);
+    rows_store(lq, s0 + sQK, 16384, mx);
+    rows_store(lk, s0 + sQK + 8192, 16384, mx);
     fence_proxy_async_smem();
     tmem_st_wait();
     tc_fence_before();
@@ -399,14 +383,8 @@ __global__ void __launch_bounds__(kLocThreads, 1) bwd_local_tc_kernel(const Prob
       for (int ks = 0; ks < 8; ++ks)
         mma_bf16(ctl->tmem + tQK, dk_(s0 + sQK, ks, 16384), dk_(s0 + sQK + 8192, ks, 16384), id, ks > 0);
       mma_commit(&ctl->ph[0]);
-      if (j_lo < j_hi) {
-        issue_A(j_lo);
-        issue_C(j_lo);
-      }
     }
-    if (warp == 0 && j_lo < j_hi) issue_B(j_lo);
-    if (j_lo < j_hi)
-      rows_to_f16<kLocThreads>(s0 + sDOV, 16384, reinterpret_cast<const __nv_bfloat16*>(b.dout), t0, p.h_v, j_lo, cv, mx);
+    if (j_lo < j_hi) rows_store(ldo, s0 + sDOV, 16384, mx);
   }
   // The gate threads: row gr of the chunk.  They hold this head's g and beta (prefetched
   // during the head before); a head's dg and dbeta are reduced while the next head's
